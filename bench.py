@@ -1,0 +1,383 @@
+"""Benchmark: attention fwd+bwd per 16,384-token packed microbatch on GB300.
+
+One step = the whole hot path over one synthetic microbatch: the forward
+kernel, then the backward (rowsum preprocess, dK/dV pass, dQ pass), all
+through the library's C ABI.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Timing: CUDA events on the launching stream around every kernel of every
+step; the L2 (129 MB) is flushed by writing a 512 MiB buffer between steps,
+outside the events.  SM clocks are sampled with nvidia-smi during the timed
+steps.  Multi-GPU: replicas only (every rank runs its own microbatch; there
+is no data-path collective), weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from varlen_sliding_window_gb300 import synth  # noqa: E402
+
+METRIC = "attn fwd+bwd ms per 16K-token microbatch; unmasked TFLOPS & % of bf16 peak"
+# The page's FlashAttention-2 fwd+bwd per layer on its own (unnamed, clock-capped)
+# GPU, for the same workloads: context for vs_baseline, not a target.
+PAGE_FA2_MS = {"ctx512_global": 0.68, "ctx4096_global": 1.43, "ctx4096_w512": 0.95,
+               "sweep_ctx512_global": 0.68, "sweep_ctx1024_global": 0.94, "sweep_ctx2048_global": 1.26,
+               "sweep_ctx4096_global": 1.43, "sweep_ctx512_w512": 0.69, "sweep_ctx1024_w512": 0.85,
+               "sweep_ctx2048_w512": 0.91, "sweep_ctx4096_w512": 0.95}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GEMM units (2*d*Hq*pairs flops each) each kernel does that the counting rule
+# credits: forward QK^T + PV; dK/dV pass S, dP, dV, dK; dQ pass dQ only (its
+# recomputed S and dP are not counted).
+KERNEL_UNITS = {"fwd": 2.0, "bwd_preprocess": 0.0, "bwd_dkdv": 4.0, "bwd_dq": 1.0}
+
+
+def unmasked_pairs(cu: np.ndarray, window: int) -> int:
+    """Closed form of sum_i |V(i)| per segment (global: L(L+1)/2; window w:
+    (w+1)(w+2)/2 + (L-w-1)(w+1) when L > w+1)."""
+    n = 0
+    for L in np.diff(cu.astype(np.int64)):
+        L = int(L)
+        if window < 0 or L <= window + 1:
+            n += L * (L + 1) // 2
+        else:
+            n += (window + 1) * (window + 2) // 2 + (L - window - 1) * (window + 1)
+    return n
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_time(inp, window: int, scale: float, budget_s: float):
+    """Times the float64 oracle (fwd + bwd) on whole segments, in order, until
+    `budget_s` seconds have passed; returns (ms per full microbatch, sample
+    description, cores).  The oracle's cost per segment and head grows with
+    L^2, so the sample is scaled to the microbatch by sum(L^2)."""
+    import oracle
+    cu = inp.cu_seqlens
+    segs = [(int(a), int(b)) for a, b in zip(cu[:-1], cu[1:]) if b > a]
+    # Longest first so that the sample includes the dominant segments.
+    segs.sort(key=lambda s: -(s[1] - s[0]))
+    total_w = sum((b - a) ** 2 for a, b in segs)
+    done_w, elapsed, n = 0, 0.0, 0
+    for a, b in segs:
+        sl = slice(a, b)
+        c = np.array([0, b - a])
+        t0 = time.perf_counter()
+        oracle.forward(inp.q[sl], inp.k[sl], inp.v[sl], c, window, scale)
+        oracle.backward(inp.dout[sl], inp.q[sl], inp.k[sl], inp.v[sl], c, window, scale)
+        elapsed += time.perf_counter() - t0
+        done_w += (b - a) ** 2
+        n += 1
+        if elapsed >= budget_s:
+            break
+    ms = 1e3 * elapsed * total_w / done_w
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"{n} of {len(segs)} segments (longest first, {done_w / total_w:.1%} of sum L^2), all heads, "
+              f"oracle fwd+bwd in numpy float64; scaled to the microbatch by sum L^2")
+    return ms, sample, cores
+
+
+def run_reference(args, wl):
+    """The reference arm: the CPU oracle as it stands, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = wl.inputs()
+    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_time(inp, wl.window_left, wl.softmax_scale, budget)
+    vals = []
+    sample = cores = None
+    for _ in range(args.steps):
+        ms, sample, cores = oracle_time(inp, wl.window_left, wl.softmax_scale, budget)
+        vals.append(ms)
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "ms", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "tokens": wl.total, "context": wl.context,
+                       "window_left": wl.window_left, "hq": wl.hq, "hkv": wl.hkv, "head_dim": wl.d},
+            "cpu_baseline": {"value": value, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="ctx512_global")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--also", default="ctx4096_global,ctx4096_w512",
+                    help="extra 16K workloads measured in the same run (comma list, '' for none)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    wls = synth.workloads()
+    wl = wls[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    import torch.distributed as dist
+
+    from varlen_sliding_window_gb300 import binding
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load_library()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    def prepare(w):
+        inp = w.inputs()
+        cu = inp.cu_seqlens
+        to = lambda bits: torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(dev)  # noqa: E731
+        t = {"q": to(inp.q_bits), "k": to(inp.k_bits), "v": to(inp.v_bits), "dout": to(inp.dout_bits),
+             "cu": torch.from_numpy(cu).to(dev)}
+        t["out"] = torch.empty_like(t["q"])
+        t["lse"] = torch.empty(w.hq, w.total, dtype=torch.float32, device=dev)
+        t["delta"] = torch.empty(w.hq, w.total, dtype=torch.float32, device=dev)
+        t["dq"], t["dk"], t["dv"] = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+        return inp, t
+
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step(w, t, evs=None):
+        """One step through the C ABI; evs = 5 events recorded between kernels."""
+        ms, win, sc = w.context, w.window_left, w.softmax_scale
+        if evs:
+            evs[0].record(stream)
+        binding.attn_varlen_fwd(t["q"], t["k"], t["v"], t["cu"], ms, win, sc, t["out"], t["lse"])
+        if evs:
+            evs[1].record(stream)
+        binding.attn_varlen_bwd_preprocess(t["dout"], t["out"], t["delta"])
+        if evs:
+            evs[2].record(stream)
+        binding.attn_varlen_bwd_dkdv(t["dout"], t["q"], t["k"], t["v"], t["lse"], t["delta"], t["cu"], ms, win, sc,
+                                     t["dk"], t["dv"])
+        if evs:
+            evs[3].record(stream)
+        binding.attn_varlen_bwd_dq(t["dout"], t["q"], t["k"], t["v"], t["lse"], t["delta"], t["cu"], ms, win, sc,
+                                   t["dq"])
+        if evs:
+            evs[4].record(stream)
+
+    def measure(w, steps, warmup, sample_clocks=False):
+        inp, t = prepare(w)
+        for _ in range(warmup):
+            step(w, t)
+            flush.fill_(1.0)
+        torch.cuda.synchronize()
+        evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        sampler = ClockSampler(local) if sample_clocks else None
+        if sampler:
+            sampler.__enter__()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for s in range(steps):
+            flush.fill_(float(s))  # L2 flush between steps, outside the events
+            step(w, t, evsets[s])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        if sampler:
+            sampler.__exit__(None, None, None)
+        status = binding.attn_varlen_get_status()
+        if status:
+            raise RuntimeError(f"device status word {status}")
+        names = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
+        per = {n: [] for n in names}
+        tot = []
+        for ev in evsets:
+            for i, n in enumerate(names):
+                per[n].append(ev[i].elapsed_time(ev[i + 1]))
+            tot.append(ev[0].elapsed_time(ev[4]))
+        pairs = unmasked_pairs(inp.cu_seqlens, w.window_left)
+        return {"inp": inp, "t": t, "total_ms": tot, "per_ms": per, "pairs": pairs, "wall_s": wall,
+                "clocks": sampler.summary() if sampler else None}
+
+    def tflops(w, pairs, ms):
+        return 4.0 * w.d * w.hq * pairs * 3.5 / (ms * 1e-3) / 1e12
+
+    main_res = measure(wl, args.steps, args.warmup, sample_clocks=True)
+    step_ms = statistics.mean(main_res["total_ms"])
+    # Whole job: every rank processes its own microbatch; time = max over ranks.
+    t_job = torch.tensor([sum(main_res["total_ms"])], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_job, op=dist.ReduceOp.MAX)
+    value = t_job.item() / (args.steps * world)  # ms per microbatch over the whole job
+    peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tf = tflops(wl, main_res["pairs"], step_ms)
+
+    # Dominant kernel roofline.
+    kern_ms = {n: statistics.mean(v) for n, v in main_res["per_ms"].items()}
+    dom = max(kern_ms, key=kern_ms.get)
+    gemm_unit = 2.0 * wl.d * wl.hq * main_res["pairs"]
+    achieved = KERNEL_UNITS[dom] * gemm_unit / (kern_ms[dom] * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get(wl.name, {}).get(dom)
+        except Exception:
+            traffic = None
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                "frac": achieved / peak_t, "traffic": traffic,
+                "peak_source": f"bf16 dense burst, {'of measured' if peak_src == 'measured' else 'of fallback'}"}
+
+    # e2e through the public calls with host buffers and copies in the timed region.
+    inp, t = main_res["inp"], main_res["t"]
+    pin = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "dout", "cu")}
+    host_out = {n: torch.empty(t[n].shape, dtype=t[n].dtype).pin_memory() for n in ("out", "lse", "dq", "dk", "dv")}
+    h2d = sum(pin[n].numel() * pin[n].element_size() for n in pin)
+    d2h = sum(host_out[n].numel() * host_out[n].element_size() for n in host_out)
+
+    def e2e_step():
+        for n in pin:
+            t[n].copy_(pin[n], non_blocking=True)
+        binding.attn_varlen_fwd(t["q"], t["k"], t["v"], t["cu"], wl.context, wl.window_left, wl.softmax_scale,
+                                t["out"], t["lse"])
+        binding.attn_varlen_bwd(t["dout"], t["q"], t["k"], t["v"], t["out"], t["lse"], t["cu"], wl.context,
+                                wl.window_left, wl.softmax_scale, t["dq"], t["dk"], t["dv"])
+        for n in host_out:
+            host_out[n].copy_(t[n], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_times = []
+    for _ in range(args.steps):
+        flush.fill_(0.5)
+        e_s.record(stream)
+        e2e_step()
+        e_e.record(stream)
+        e_e.synchronize()
+        e2e_times.append(e_s.elapsed_time(e_e))
+    e2e_ms = statistics.mean(e2e_times)
+
+    also = {}
+    for name in [x for x in args.also.split(",") if x]:
+        w2 = wls[name]
+        r = measure(w2, max(5, args.steps // 2), 3)
+        ms2 = statistics.mean(r["total_ms"])
+        also[name] = {"ms": ms2, "tflops": tflops(w2, r["pairs"], ms2), "frac": tflops(w2, r["pairs"], ms2) / peak_t,
+                      "pairs": r["pairs"], "segments": int(len(r["inp"].cu_seqlens) - 1),
+                      "kernel_ms": {n: statistics.mean(v) for n, v in r["per_ms"].items()}}
+        del r
+
+    line = None
+    if rank == 0:
+        cpu_ms, sample, cores = oracle_time(inp, wl.window_left, wl.softmax_scale, args.cpu_budget)
+        line = {
+            "metric": METRIC, "value": value, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": (value / PAGE_FA2_MS[wl.name]) if wl.name in PAGE_FA2_MS else None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "tokens": wl.total, "context": wl.context, "window_left": wl.window_left,
+                       "hq": wl.hq, "hkv": wl.hkv, "head_dim": wl.d, "segments": int(len(inp.cu_seqlens) - 1),
+                       "doc_seed": wl.doc_seed, "tensor_seed": wl.tensor_seed, "unmasked_pairs": main_res["pairs"],
+                       "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
+            "tflops": tf, "pct_of_bf16_peak": 100.0 * tf / peak_t,
+            "kernel_ms": kern_ms,
+            "roofline": roofline,
+            "cpu_baseline": {"value": cpu_ms, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 4 * args.steps,
+            "clocks": main_res["clocks"],
+            "also": also,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+/*
+ * attn_varlen.h -- C ABI of a GB300 (sm_103a) library for the training-step
+ * forward and backward of document-masked causal grouped-query attention.
+ *
+ * The operation (research.dws.rip/llm/kernels, section 01 "How it was
+ * measured", Fig. 2 "Benchmark setup", section 02): a microbatch of T tokens
+ * is packed from many documents and cut into rows at the context length.  No
+ * token attends across its document boundary or row cut, so attention is
+ * confined to segments [cu_seqlens[s], cu_seqlens[s+1]).  Inside a segment it
+ * is causal; a local layer additionally limits each query to a left window.
+ * Heads are grouped: Hq query heads share Hkv key/value heads (8 and 2 of
+ * width 128 on the page), query head h reading kv head h / (Hq / Hkv).
+ *
+ * Definition, for a query i in segment [a, b) and query head h (g = its kv
+ * head):
+ *     V(i)   = { j : a <= j <= i  and  (window_left < 0 or i - j <= window_left) }
+ *     s_ij   = softmax_scale * <q[i,h,:], k[j,g,:]>
+ *     lse[h,i] = log sum_{j in V(i)} exp(s_ij)            (natural log)
+ *     out[i,h,:] = sum_{j in V(i)} exp(s_ij - lse[h,i]) * v[j,g,:]
+ * The backward returns dq, dk, dv of  L = sum(dout * out).
+ * window_left = w keeps w+1 keys including the query itself (a 512-token
+ * window is window_left = 512); window_left = -1 is global causal.
+ *
+ * Layouts (all row-major, contiguous, bf16 = IEEE bfloat16 bit patterns):
+ *     q, out, dout, dq : [T, Hq, 128]      k, v, dk, dv : [T, Hkv, 128]
+ *     lse              : float32 [Hq, T]
+ *     cu_seqlens       : int32 [num_segments + 1], non-decreasing,
+ *                        cu_seqlens[0] = 0, cu_seqlens[num_segments] = T.
+ * Repeated entries (empty segments) are allowed and change no output bit;
+ * they let callers pad the boundary list to a fixed size for CUDA-graph
+ * replay (section 06 of the same page).
+ *
+ * Ownership and memory: every pointer except `stream` is caller-owned DEVICE
+ * memory on the current CUDA device, 16-byte aligned.  The library keeps no
+ * reference after the enqueued work completes.  Outputs are fully
+ * overwritten.  The forward allocates nothing.  The backward takes a scratch
+ * buffer of attn_varlen_bwd_workspace_bytes() bytes from the stream-ordered
+ * allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ * stream).  No call synchronises the host except attn_varlen_get_status();
+ * all device work is enqueued on `stream`.
+ *
+ * Errors: every call returns ATTN_OK (0) or a negative ATTN_ERR_* code and
+ * never throws.  Argument errors are detected before anything is enqueued.
+ * cu_seqlens is only read on the device; a list that breaks the rules above,
+ * or a segment longer than max_seqlen, gives unspecified outputs but every
+ * loop stays bounded.  Asynchronous device errors (a bounded wait that gave
+ * up) are recorded in a per-device status word read by
+ * attn_varlen_get_status().
+ */
+#ifndef ATTN_VARLEN_H_
+#define ATTN_VARLEN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_OK 0
+#define ATTN_ERR_NULL_POINTER (-1)   /* a required pointer is NULL */
+#define ATTN_ERR_SHAPE (-2)          /* T < 0, heads <= 0, Hq % Hkv != 0, num_segments < 0 ... */
+#define ATTN_ERR_HEAD_DIM (-3)       /* head_dim != 128 */
+#define ATTN_ERR_ALIGNMENT (-4)      /* a tensor pointer is not 16-byte aligned */
+#define ATTN_ERR_WINDOW (-5)         /* window_left < -1 */
+#define ATTN_ERR_SCALE (-6)          /* softmax_scale not finite and > 0 */
+#define ATTN_ERR_MAX_SEQLEN (-7)     /* max_seqlen < 0, or > T when T > 0 */
+#define ATTN_ERR_DEVICE (-8)         /* current device is not an sm_103 GPU */
+#define ATTN_ERR_CUDA (-9)           /* a CUDA runtime/driver call failed */
+#define ATTN_ERR_TOO_LARGE (-10)     /* T or a head count beyond the supported range */
+#define ATTN_ERR_ALLOC (-11)         /* the backward scratch could not be allocated */
+#define ATTN_ERR_DEVICE_STATUS (-12) /* attn_varlen_get_status: a kernel reported an error */
+
+/*
+ * Forward.  Writes out [T, Hq, 128] (bf16) and lse [Hq, T] (float32).
+ * softmax_scale is normally 1/sqrt(128).  max_seqlen is an upper bound on
+ * every segment length (the context length is a valid, graph-friendly choice).
+ */
+int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens, int32_t max_seqlen,
+                    int32_t window_left, float softmax_scale, void* out, float* lse, int64_t total,
+                    int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t num_segments,
+                    void* stream);
+
+/*
+ * Backward.  Given dout, the forward's inputs and its outputs out and lse,
+ * writes dq [T, Hq, 128], dk and dv [T, Hkv, 128] (bf16).  Runs three kernels
+ * on `stream`: a preprocess computing D = rowsum(dout * out), a
+ * key/value-stationary pass producing dk and dv, and a query-stationary pass
+ * producing dq.  No atomics: results are bitwise reproducible.
+ */
+int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                    const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                    float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
+                    int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream);
+
+/* Bytes of scratch the backward takes from the stream-ordered allocator. */
+size_t attn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads_q);
+
+/*
+ * The three kernels of attn_varlen_bwd as separate calls, for callers that
+ * manage the scratch themselves or run the two passes on different streams.
+ * `delta` is caller-owned device float32 [Hq, T] (16-byte aligned):
+ *   attn_varlen_bwd_preprocess writes delta[h, i] = sum_c dout[i,h,c] * out[i,h,c];
+ *   attn_varlen_bwd_dkdv reads it (with q, k, v, dout, lse) and writes dk, dv;
+ *   attn_varlen_bwd_dq reads it and writes dq.
+ * The two passes only read delta, so they may run concurrently once the
+ * preprocess has completed.  Arguments mean what they mean in attn_varlen_bwd.
+ */
+int attn_varlen_bwd_preprocess(const void* dout, const void* out, float* delta, int64_t total, int32_t num_heads_q,
+                               int32_t head_dim, void* stream);
+int attn_varlen_bwd_dkdv(const void* dout, const void* q, const void* k, const void* v, const float* lse,
+                         const float* delta, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                         float softmax_scale, void* dk, void* dv, int64_t total, int32_t num_heads_q,
+                         int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream);
+int attn_varlen_bwd_dq(const void* dout, const void* q, const void* k, const void* v, const float* lse,
+                       const float* delta, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                       float softmax_scale, void* dq, int64_t total, int32_t num_heads_q, int32_t num_heads_kv,
+                       int32_t head_dim, int32_t num_segments, void* stream);
+
+/*
+ * Synchronises `stream`, then returns ATTN_OK if no kernel of this library
+ * recorded an error on the current device since the last call, else
+ * ATTN_ERR_DEVICE_STATUS; *device_code (optional) receives the raw word
+ * (1 = a bounded wait timed out, 2 = a CTA work list overflowed).
+ * The word is cleared.  For tests and debugging; it blocks the host.
+ */
+int attn_varlen_get_status(void* stream, int32_t* device_code);
+
+/* Static description of an error code. */
+const char* attn_varlen_strerror(int code);
+
+/*
+ * Test hook: runs the kernels' own mask and tile-range logic on the device.
+ * by_key = 0: for every query token i, ranges[3*i + 0..2] = (first visible
+ *   key, last visible key, number of visible keys), scanning exactly the kv
+ *   tiles and per-row column bounds the forward and dQ kernels use.
+ * by_key = 1: for every key token j, (first query that sees j, last query
+ *   that sees j, number of such queries), scanning the q tiles and bounds the
+ *   dK/dV kernel uses.
+ * A token that sees (or is seen by) nothing gets (0, -1, 0).
+ * ranges is device int32 [3 * T].
+ */
+int attn_varlen_mask_ranges(const int32_t* cu_seqlens, int32_t num_segments, int64_t total, int32_t max_seqlen,
+                            int32_t window_left, int32_t by_key, int32_t* ranges, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_VARLEN_H_ */

@@ -1,0 +1,84 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function the header declares, and rejects invalid
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_varlen.h")
+
+
+@pytest.fixture(scope="module")
+def clib():
+    from varlen_sliding_window_gb300 import _build, binding
+    _build.build_library()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_varlen_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for required in ("attn_varlen_fwd", "attn_varlen_bwd", "attn_varlen_get_status", "attn_varlen_strerror"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(clib):
+    for name in declared_functions():
+        assert hasattr(clib, name), name
+
+
+def test_strerror(clib):
+    assert clib.attn_varlen_strerror(0) == b"ok"
+    assert b"128" in clib.attn_varlen_strerror(-3)
+    assert clib.attn_varlen_strerror(12345) == b"unknown error code"
+
+
+def _fwd(clib, **kw):
+    args = dict(q=16, k=16, v=16, cu=16, max_seqlen=4, window=-1, scale=0.088, out=16, lse=16, total=4, hq=8,
+                hkv=2, d=128, nseg=1, stream=None)
+    args.update(kw)
+    vp = ctypes.c_void_p
+    return clib.attn_varlen_fwd(vp(args["q"]), vp(args["k"]), vp(args["v"]), vp(args["cu"]), args["max_seqlen"],
+                                args["window"], args["scale"], vp(args["out"]), vp(args["lse"]), args["total"],
+                                args["hq"], args["hkv"], args["d"], args["nseg"], vp(args["stream"]))
+
+
+def test_argument_validation(clib):
+    # All of these are rejected before any CUDA call, so no GPU is needed.
+    assert _fwd(clib, q=None) == -1
+    assert _fwd(clib, cu=None) == -1
+    assert _fwd(clib, hq=6, hkv=4) == -2
+    assert _fwd(clib, total=-1) == -2
+    assert _fwd(clib, d=64) == -3
+    assert _fwd(clib, q=17) == -4
+    assert _fwd(clib, lse=20) == -4
+    assert _fwd(clib, window=-2) == -5
+    assert _fwd(clib, scale=float("nan")) == -6
+    assert _fwd(clib, scale=0.0) == -6
+    assert _fwd(clib, max_seqlen=5) == -7
+    assert _fwd(clib, max_seqlen=-1) == -7
+
+
+def test_workspace_bytes(clib):
+    assert clib.attn_varlen_bwd_workspace_bytes(16384, 8) == 16384 * 8 * 4
+    assert clib.attn_varlen_bwd_workspace_bytes(0, 8) == 0
+    assert clib.attn_varlen_bwd_workspace_bytes(3, 1) == 256
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from varlen_sliding_window_gb300 import binding
+    saved = binding._lib
+    binding._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="not built"):
+            binding.load_library(str(tmp_path / "missing.so"))
+    finally:
+        binding._lib = saved

@@ -1,0 +1,200 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Tolerances (relative L2 over the whole tensor): out <= 5e-3, dq/dk/dv <= 1e-2;
+lse within 1e-3 absolute.  Which keys each query sees is checked bit-exactly.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from varlen_sliding_window_gb300 import synth
+
+from helpers import (TOL_GRAD, TOL_LSE_ABS, TOL_OUT, by_key_ranges_from_oracle, rel_l2, run_gpu, segment_slice,
+                     to_device_bf16)
+
+pytestmark = pytest.mark.gpu
+
+WL = synth.workloads()
+
+
+def _check_full(inp, window, scale, max_seqlen, res):
+    ref_out, ref_lse = oracle.forward(inp.q, inp.k, inp.v, inp.cu_seqlens, window, scale)
+    dq, dk, dv = oracle.backward(inp.dout, inp.q, inp.k, inp.v, inp.cu_seqlens, window, scale)
+    errs = {"out": rel_l2(res["out"], ref_out)}
+    assert errs["out"] <= TOL_OUT, errs
+    for g, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if np.linalg.norm(ref) < 1e-9:
+            # window_left = 0: every query sees only itself, P = 1 and
+            # dS = dP - D = 0, so dq and dk vanish exactly; the GPU's D comes
+            # from the bf16-rounded out, leaving rounding-level residue.
+            errs[g] = float(np.sqrt(np.mean(res[g] ** 2)))
+            assert errs[g] <= 1e-4, errs
+        else:
+            errs[g] = rel_l2(res[g], ref)
+            assert errs[g] <= TOL_GRAD, errs
+    assert np.abs(res["lse"] - ref_lse).max() <= TOL_LSE_ABS
+    return errs
+
+
+@pytest.mark.parametrize("name", ["tiny_global", "tiny_w64"])
+def test_tiny_workloads(name):
+    wl = WL[name]
+    inp = wl.inputs()
+    res = run_gpu(inp, wl.window_left, wl.softmax_scale, 256)
+    _check_full(inp, wl.window_left, wl.softmax_scale, 256, res)
+
+
+@pytest.mark.parametrize("window", [-1, 0, 1, 64, 127, 128, 129, 300, 512])
+def test_ragged_multi_tile(window):
+    """Segments spanning several tiles with ragged tails, a length-1 segment,
+    an exact tile multiple, and both global and many window widths."""
+    cu = np.array([0, 1, 130, 386, 387, 900, 1024, 1536, 1800], dtype=np.int32)
+    inp = synth.make_inputs(cu, 8, 2, 128, tensor_seed=3)
+    res = run_gpu(inp, window, 1 / np.sqrt(128), 600)
+    _check_full(inp, window, 1 / np.sqrt(128), 600, res)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (16, 4), (4, 4), (6, 2), (8, 1)])
+def test_head_ratios(hq, hkv):
+    cu = np.array([0, 200, 333, 700], dtype=np.int32)
+    inp = synth.make_inputs(cu, hq, hkv, 128, tensor_seed=4)
+    for window in (-1, 100):
+        res = run_gpu(inp, window, 0.0884, 400)
+        _check_full(inp, window, 0.0884, 400, res)
+
+
+@pytest.mark.parametrize("name", ["ctx512_global", "ctx4096_w512", "ctx4096_global"])
+def test_full_size_sampled_segments(name):
+    """At the full 16,384-token sizes (the benchmark's launch configuration),
+    the oracle is run on a sample of whole segments (first, last, longest,
+    shortest, and one in the middle); every segment is independent."""
+    wl = WL[name]
+    inp = wl.inputs()
+    res = run_gpu(inp, wl.window_left, wl.softmax_scale, wl.context)
+    cu = inp.cu_seqlens
+    lens = np.diff(cu)
+    picks = sorted({0, len(lens) - 1, int(np.argmax(lens)), int(np.argmin(lens)), len(lens) // 2})
+    for s in picks:
+        a, b = int(cu[s]), int(cu[s + 1])
+        sub = segment_slice(inp, a, b)
+        ref_out, ref_lse = oracle.forward(sub.q, sub.k, sub.v, sub.cu_seqlens, wl.window_left, wl.softmax_scale)
+        g = oracle.backward(sub.dout, sub.q, sub.k, sub.v, sub.cu_seqlens, wl.window_left, wl.softmax_scale)
+        assert rel_l2(res["out"][a:b], ref_out) <= TOL_OUT
+        assert np.abs(res["lse"][:, a:b] - ref_lse).max() <= TOL_LSE_ABS
+        for got, ref in zip((res["dq"][a:b], res["dk"][a:b], res["dv"][a:b]), g):
+            assert rel_l2(got, ref) <= TOL_GRAD
+    # Properties that hold for every segment at any size.
+    assert np.all(np.isfinite(res["out"])) and np.all(np.isfinite(res["dq"]))
+    # Per segment, kv head and column: sum_j dk = 0 and sum_j dv = sum of dout
+    # over the group.  The GPU values carry bf16 rounding (2^-9 relative) and
+    # the kernel's own error (~3e-3 of the column norm), which add up like a
+    # random walk over the rows, so the bound is 3 % of the column's L2 norm.
+    for a, b in oracle.segments(cu):
+        dk = res["dk"][a:b]
+        assert np.all(np.abs(dk.sum(axis=0)) <= 3e-2 * np.linalg.norm(dk, axis=0) + 1e-3)
+        dv = res["dv"][a:b]
+        do_sum = inp.dout[a:b].astype(np.float64).reshape(b - a, wl.hkv, wl.hq // wl.hkv, 128).sum(axis=(0, 2))
+        assert np.all(np.abs(dv.sum(axis=0) - do_sum) <= 3e-2 * np.linalg.norm(dv, axis=0) + 1e-2)
+
+
+@pytest.mark.parametrize("name", ["tiny_global", "tiny_w64", "ctx512_global", "ctx4096_w512", "ctx4096_global"])
+def test_mask_ranges_bit_exact(name):
+    """The kernels' own mask/tile logic, exported by the test hook, against the
+    oracle's visible sets, per query and per key."""
+    import torch
+    from varlen_sliding_window_gb300 import binding
+    wl = WL[name]
+    cu = wl.cu_seqlens()
+    T = int(cu[-1])
+    dcu = torch.from_numpy(cu).cuda()
+    ranges = torch.empty(3 * T, dtype=torch.int32, device="cuda")
+    binding.attn_varlen_mask_ranges(dcu, T, wl.context, wl.window_left, False, ranges)
+    got = ranges.view(T, 3).cpu().numpy().astype(np.int64)
+    np.testing.assert_array_equal(got, oracle.visible_ranges(cu, wl.window_left, T))
+    binding.attn_varlen_mask_ranges(dcu, T, wl.context, wl.window_left, True, ranges)
+    got = ranges.view(T, 3).cpu().numpy().astype(np.int64)
+    np.testing.assert_array_equal(got, by_key_ranges_from_oracle(cu, wl.window_left, T))
+
+
+@pytest.mark.parametrize("name", ["tiny_w64", "ctx512_global", "ctx4096_w512", "ctx4096_global"])
+def test_zero_q_counts_visible_keys(name):
+    """With q = 0 every visible key has the same logit, so exp(lse) is exactly
+    the number of keys the real forward kernel let each query see."""
+    wl = WL[name]
+    inp = wl.inputs()
+    inp.q_bits = np.zeros_like(inp.q_bits)
+    res = run_gpu(inp, wl.window_left, wl.softmax_scale, wl.context, backward=False)
+    counts = oracle.visible_ranges(inp.cu_seqlens, wl.window_left, wl.total)[:, 2]
+    np.testing.assert_array_equal(np.rint(np.exp(res["lse"])).astype(np.int64), np.broadcast_to(counts, res["lse"].shape))
+
+
+def test_empty_segments_are_bit_identical():
+    """Padding cu_seqlens with empty segments (front, middle, end) changes no bit."""
+    wl = WL["ctx4096_w512"]
+    inp = wl.inputs()
+    cu = inp.cu_seqlens
+    padded = np.concatenate([[0, 0], cu[1:5], [cu[4]] * 3, cu[5:], [cu[-1]] * 4]).astype(np.int32)
+    a = run_gpu(inp, wl.window_left, wl.softmax_scale, wl.context)
+    b = run_gpu(inp, wl.window_left, wl.softmax_scale, wl.context, cu_override=padded)
+    for key in ("out", "lse", "dq", "dk", "dv"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_deterministic():
+    wl = WL["ctx4096_global"]
+    inp = wl.inputs()
+    a = run_gpu(inp, wl.window_left, wl.softmax_scale, wl.context)
+    b = run_gpu(inp, wl.window_left, wl.softmax_scale, wl.context)
+    for key in ("out", "lse", "dq", "dk", "dv"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_cuda_graph_replay_matches_eager():
+    """Forward + backward captured once in a CUDA graph with a padded boundary
+    list, replayed over three batches with different boundaries, matches eager
+    runs bit for bit (research.dws.rip/llm/kernels, section 06)."""
+    import torch
+    from varlen_sliding_window_gb300 import binding
+    wl = WL["ctx4096_w512"]
+    nseg_pad = 48
+    batches = []
+    for seed in (0, 1, 2):
+        cu = synth.pad_cu_seqlens(synth.pack_microbatch(16384, 4096, seed), nseg_pad)
+        batches.append((cu, synth.make_inputs(cu, 8, 2, 128, tensor_seed=10 + seed)))
+    dev = torch.device("cuda")
+    q = torch.empty(16384, 8, 128, dtype=torch.bfloat16, device=dev)
+    k = torch.empty(16384, 2, 128, dtype=torch.bfloat16, device=dev)
+    v, do = torch.empty_like(k), torch.empty_like(q)
+    cu_d = torch.zeros(nseg_pad + 1, dtype=torch.int32, device=dev)
+    out, dq = torch.empty_like(q), torch.empty_like(q)
+    dk, dv = torch.empty_like(k), torch.empty_like(k)
+    lse = torch.empty(8, 16384, dtype=torch.float32, device=dev)
+
+    def load(cu, inp):
+        cu_d.copy_(torch.from_numpy(cu))
+        for dst, bits in ((q, inp.q_bits), (k, inp.k_bits), (v, inp.v_bits), (do, inp.dout_bits)):
+            dst.copy_(to_device_bf16(bits))
+
+    def step():
+        binding.attn_varlen_fwd(q, k, v, cu_d, 4096, 512, wl.softmax_scale, out, lse)
+        binding.attn_varlen_bwd(do, q, k, v, out, lse, cu_d, 4096, 512, wl.softmax_scale, dq, dk, dv)
+
+    s = torch.cuda.Stream()
+    load(*batches[0])
+    with torch.cuda.stream(s):
+        step()  # warm-up (allocator pool, function attributes) outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for cu, inp in batches:
+        load(cu, inp)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        replayed = [t.clone() for t in (out, lse, dq, dk, dv)]
+        step()
+        torch.cuda.synchronize()
+        for x, y in zip(replayed, (out, lse, dq, dk, dv)):
+            assert torch.equal(x, y)
+    assert binding.attn_varlen_get_status() == 0

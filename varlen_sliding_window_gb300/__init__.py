@@ -1,0 +1,19 @@
+"""Document-masked (varlen) causal grouped-query attention for GB300 (sm_103a).
+
+The compute lives in the C-ABI library libvsw_attn.so (include/attn_varlen.h);
+``binding`` marshals torch CUDA tensors into it.  ``synth`` generates the
+seeded packed-document workloads.
+"""
+from importlib import import_module
+
+_BINDING_NAMES = {
+    "attn_varlen_fwd", "attn_varlen_bwd", "attn_varlen_bwd_workspace_bytes", "attn_varlen_get_status",
+    "attn_varlen_strerror", "attn_varlen_mask_ranges", "attn_varlen_bwd_preprocess",
+    "attn_varlen_bwd_dkdv", "attn_varlen_bwd_dq", "load_library", "AttnError",
+}
+
+
+def __getattr__(name):
+    if name in _BINDING_NAMES:
+        return getattr(import_module(".binding", __name__), name)
+    raise AttributeError(name)

@@ -1,0 +1,163 @@
+"""Python binding of the C ABI in include/attn_varlen.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libvsw_attn.so.  Tensors are torch CUDA tensors (PyTorch is used
+for device memory and streams).  There is no CPU fallback: if the library is
+missing or the device is not an sm_103 GPU, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from ._build import LIB_PATH
+
+_lib = None
+
+ATTN_OK = 0
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        msg = _strerror(code) if _lib is not None else str(code)
+        super().__init__(f"{what} failed with {code}: {msg}")
+        self.code = code
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Loads the in-tree library (built by __graft_entry__.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    lib.attn_varlen_fwd.argtypes = [vp, vp, vp, vp, i32, i32, f32, vp, vp, i64, i32, i32, i32, i32, vp]
+    lib.attn_varlen_fwd.restype = ctypes.c_int
+    lib.attn_varlen_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp, vp, i64, i32, i32, i32, i32, vp]
+    lib.attn_varlen_bwd.restype = ctypes.c_int
+    lib.attn_varlen_bwd_workspace_bytes.argtypes = [i64, i32]
+    lib.attn_varlen_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_varlen_get_status.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.attn_varlen_get_status.restype = ctypes.c_int
+    lib.attn_varlen_strerror.argtypes = [ctypes.c_int]
+    lib.attn_varlen_strerror.restype = ctypes.c_char_p
+    lib.attn_varlen_bwd_preprocess.argtypes = [vp, vp, vp, i64, i32, i32, vp]
+    lib.attn_varlen_bwd_preprocess.restype = ctypes.c_int
+    lib.attn_varlen_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp, i64, i32, i32, i32, i32, vp]
+    lib.attn_varlen_bwd_dkdv.restype = ctypes.c_int
+    lib.attn_varlen_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, vp, i64, i32, i32, i32, i32, vp]
+    lib.attn_varlen_bwd_dq.restype = ctypes.c_int
+    lib.attn_varlen_mask_ranges.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp]
+    lib.attn_varlen_mask_ranges.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _strerror(code: int) -> str:
+    return _lib.attn_varlen_strerror(code).decode()
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(code: int, what: str) -> None:
+    if code != ATTN_OK:
+        raise AttnError(code, what)
+
+
+def _dims(q, k, cu_seqlens):
+    total, hq, d = q.shape
+    hkv = k.shape[1]
+    return int(total), int(hq), int(hkv), int(d), int(cu_seqlens.numel()) - 1
+
+
+def attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen: int, window_left: int, softmax_scale: float, out, lse,
+                    stream=None) -> None:
+    """Forward.  q [T,Hq,128], k/v [T,Hkv,128] bf16; out [T,Hq,128] bf16, lse [Hq,T] fp32."""
+    lib = load_library()
+    total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
+    rc = lib.attn_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), int(max_seqlen), int(window_left),
+                             float(softmax_scale), _ptr(out), _ptr(lse), total, hq, hkv, d, nseg,
+                             _stream_handle(stream))
+    _check(rc, "attn_varlen_fwd")
+
+
+def attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seqlen: int, window_left: int, softmax_scale: float,
+                    dq, dk, dv, stream=None) -> None:
+    """Backward.  Writes dq [T,Hq,128], dk/dv [T,Hkv,128] (bf16)."""
+    lib = load_library()
+    total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
+    rc = lib.attn_varlen_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
+                             int(max_seqlen), int(window_left), float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv),
+                             total, hq, hkv, d, nseg, _stream_handle(stream))
+    _check(rc, "attn_varlen_bwd")
+
+
+def attn_varlen_bwd_preprocess(dout, out, delta, stream=None) -> None:
+    """delta [Hq, T] fp32 = rowsum(dout * out)."""
+    lib = load_library()
+    total, hq, d = dout.shape
+    _check(lib.attn_varlen_bwd_preprocess(_ptr(dout), _ptr(out), _ptr(delta), int(total), int(hq), int(d),
+                                          _stream_handle(stream)), "attn_varlen_bwd_preprocess")
+
+
+def attn_varlen_bwd_dkdv(dout, q, k, v, lse, delta, cu_seqlens, max_seqlen: int, window_left: int,
+                         softmax_scale: float, dk, dv, stream=None) -> None:
+    lib = load_library()
+    total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
+    _check(lib.attn_varlen_bwd_dkdv(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(cu_seqlens),
+                                    int(max_seqlen), int(window_left), float(softmax_scale), _ptr(dk), _ptr(dv),
+                                    total, hq, hkv, d, nseg, _stream_handle(stream)), "attn_varlen_bwd_dkdv")
+
+
+def attn_varlen_bwd_dq(dout, q, k, v, lse, delta, cu_seqlens, max_seqlen: int, window_left: int,
+                       softmax_scale: float, dq, stream=None) -> None:
+    lib = load_library()
+    total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
+    _check(lib.attn_varlen_bwd_dq(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(cu_seqlens),
+                                  int(max_seqlen), int(window_left), float(softmax_scale), _ptr(dq), total, hq, hkv,
+                                  d, nseg, _stream_handle(stream)), "attn_varlen_bwd_dq")
+
+
+def attn_varlen_bwd_workspace_bytes(total: int, num_heads_q: int) -> int:
+    return int(load_library().attn_varlen_bwd_workspace_bytes(int(total), int(num_heads_q)))
+
+
+def attn_varlen_get_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status word."""
+    lib = load_library()
+    word = ctypes.c_int32(0)
+    rc = lib.attn_varlen_get_status(_stream_handle(stream), ctypes.byref(word))
+    if rc not in (ATTN_OK, -12):
+        _check(rc, "attn_varlen_get_status")
+    return int(word.value)
+
+
+def attn_varlen_strerror(code: int) -> str:
+    load_library()
+    return _strerror(code)
+
+
+def attn_varlen_mask_ranges(cu_seqlens, total: int, max_seqlen: int, window_left: int, by_key: bool, ranges,
+                            stream=None) -> None:
+    """Test hook: per-token (first, last, count) from the kernels' own mask logic."""
+    lib = load_library()
+    rc = lib.attn_varlen_mask_ranges(_ptr(cu_seqlens), int(cu_seqlens.numel()) - 1, int(total), int(max_seqlen),
+                                     int(window_left), 1 if by_key else 0, _ptr(ranges), _stream_handle(stream))
+    _check(rc, "attn_varlen_mask_ranges")
+
+
+def default_scale(head_dim: int = 128) -> float:
+    return 1.0 / math.sqrt(head_dim)

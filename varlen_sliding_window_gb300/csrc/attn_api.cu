@@ -1,0 +1,322 @@
+// C ABI of the library: argument validation, TMA descriptor encoding, scratch
+// handling and stream-ordered launches.  See include/attn_varlen.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_internal.h"
+#include "attn_varlen.h"
+#include "mask.cuh"
+
+namespace vsw {
+
+// Per-device error word written by the kernels (1 = wait timeout, 2 = work
+// list overflow).  Host code reaches it through its device address.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool supported = false;
+  int num_sms = 0;
+  int* status = nullptr;  // device address of g_status_word
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device(DeviceInfo** info) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    if (d.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return ATTN_ERR_CUDA;
+      d.status = static_cast<int*>(p);
+      if (cudaMemset(d.status, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    }
+    d.probed = true;
+  }
+  if (!d.supported) return ATTN_ERR_DEVICE;
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return ATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *info = &d;
+  return ATTN_OK;
+}
+
+// [T, heads, 128] bf16 -> 3-D map (d, head, token), box (64, 1, 128),
+// 128-byte swizzle: one box is a 128-token x 64-column swizzled half tile.
+int make_tile_map(CUtensorMap* m, const void* base, int heads, int64_t total) {
+  cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)total};
+  cuuint64_t strides[2] = {128 * 2, (cuuint64_t)heads * 128 * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate_common(const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left, float softmax_scale,
+                    int64_t total, int32_t hq, int32_t hkv, int32_t head_dim, int32_t nseg) {
+  if (!cu_seqlens) return ATTN_ERR_NULL_POINTER;
+  if (total < 0 || hq <= 0 || hkv <= 0 || nseg < 0 || (hq % hkv) != 0) return ATTN_ERR_SHAPE;
+  if (total > 0 && nseg == 0) return ATTN_ERR_SHAPE;
+  if (head_dim != 128) return ATTN_ERR_HEAD_DIM;
+  // cu_seqlens is staged in shared memory by every kernel: at most 8191 segments.
+  if (total > (int64_t(1) << 30) || hq > 1024 || nseg > kMaxSegments) return ATTN_ERR_TOO_LARGE;
+  if (window_left < -1) return ATTN_ERR_WINDOW;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return ATTN_ERR_SCALE;
+  if (max_seqlen < 0 || (total > 0 && max_seqlen > total)) return ATTN_ERR_MAX_SEQLEN;
+  return ATTN_OK;
+}
+
+AttnParams make_params(const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left, float softmax_scale,
+                       int64_t total, int32_t hq, int32_t hkv, int32_t nseg, int* status) {
+  AttnParams a;
+  a.cu_seqlens = cu_seqlens;
+  a.nseg = nseg;
+  a.total = (int)total;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.group = hq / hkv;
+  // A window at least as long as the microbatch is global causal; clamping
+  // keeps every index computation far from int overflow.
+  a.window = (window_left >= total) ? -1 : window_left;
+  a.max_levels = (max_seqlen + kTile - 1) / kTile;
+  a.scale = softmax_scale;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.status = status;
+  return a;
+}
+
+}  // namespace
+}  // namespace vsw
+
+using namespace vsw;
+
+extern "C" {
+
+int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens, int32_t max_seqlen,
+                    int32_t window_left, float softmax_scale, void* out, float* lse, int64_t total,
+                    int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t num_segments,
+                    void* stream) {
+  int rc = validate_common(cu_seqlens, max_seqlen, window_left, softmax_scale, total, num_heads_q, num_heads_kv,
+                           head_dim, num_segments);
+  if (rc) return rc;
+  if (!q || !k || !v || !out || !lse) return ATTN_ERR_NULL_POINTER;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return ATTN_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev))) return rc;
+  if (total == 0) return ATTN_OK;
+  CUtensorMap tq, tk, tv;
+  if (make_tile_map(&tq, q, num_heads_q, total) || make_tile_map(&tk, k, num_heads_kv, total) ||
+      make_tile_map(&tv, v, num_heads_kv, total))
+    return ATTN_ERR_CUDA;
+  FwdParams p;
+  p.a = make_params(cu_seqlens, max_seqlen, window_left, softmax_scale, total, num_heads_q, num_heads_kv,
+                    num_segments, dev->status);
+  p.out = out;
+  p.lse = lse;
+  if (launch_fwd(tq, tk, tv, p, dev->num_sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+size_t attn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads_q) {
+  if (total <= 0 || num_heads_q <= 0) return 0;
+  // delta = rowsum(dout * out), fp32 [Hq, T], padded to 256 bytes.
+  return ((size_t)total * num_heads_q * sizeof(float) + 255) & ~(size_t)255;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validation, device check, tensor maps and parameters shared by the
+// backward entry points.
+struct BwdSetup {
+  DeviceInfo* dev = nullptr;
+  CUtensorMap tq, tk, tv, tdo;
+  BwdParams p;
+};
+
+int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, const void* v, const void* out,
+                const float* lse, const float* delta, const int32_t* cu_seqlens, int32_t max_seqlen,
+                int32_t window_left, float softmax_scale, void* dq, void* dk, void* dv, int64_t total,
+                int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t num_segments) {
+  int rc = validate_common(cu_seqlens, max_seqlen, window_left, softmax_scale, total, num_heads_q, num_heads_kv,
+                           head_dim, num_segments);
+  if (rc) return rc;
+  const void* ptrs[] = {dout, q, k, v, lse};
+  for (const void* x : ptrs)
+    if (!x) return ATTN_ERR_NULL_POINTER;
+  for (const void* x : ptrs)
+    if (!aligned16(x)) return ATTN_ERR_ALIGNMENT;
+  const void* opt[] = {out, delta, dq, dk, dv};  // the callers pass the ones they need (checked there)
+  for (const void* x : opt)
+    if (x && !aligned16(x)) return ATTN_ERR_ALIGNMENT;
+  if ((rc = current_device(&b.dev))) return rc;
+  if (total == 0) return ATTN_OK;
+  if (make_tile_map(&b.tq, q, num_heads_q, total) || make_tile_map(&b.tk, k, num_heads_kv, total) ||
+      make_tile_map(&b.tv, v, num_heads_kv, total) || make_tile_map(&b.tdo, dout, num_heads_q, total))
+    return ATTN_ERR_CUDA;
+  b.p.a = make_params(cu_seqlens, max_seqlen, window_left, softmax_scale, total, num_heads_q, num_heads_kv,
+                      num_segments, b.dev->status);
+  b.p.dout = dout;
+  b.p.out = out;
+  b.p.lse = lse;
+  b.p.delta = const_cast<float*>(delta);
+  b.p.dq = dq;
+  b.p.dk = dk;
+  b.p.dv = dv;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                    const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                    float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
+                    int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream) {
+  if (!out || !dq || !dk || !dv) return ATTN_ERR_NULL_POINTER;
+  BwdSetup b;
+  int rc = prepare_bwd(b, dout, q, k, v, out, lse, nullptr, cu_seqlens, max_seqlen, window_left, softmax_scale, dq,
+                       dk, dv, total, num_heads_q, num_heads_kv, head_dim, num_segments);
+  if (rc || total == 0) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, attn_varlen_bwd_workspace_bytes(total, num_heads_q), s) != cudaSuccess)
+    return ATTN_ERR_ALLOC;
+  b.p.delta = static_cast<float*>(ws);
+  int lr = launch_bwd_preprocess(b.p, s);
+  if (!lr) lr = launch_bwd_dkdv(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, s);
+  if (!lr) lr = launch_bwd_dq(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, s);
+  const cudaError_t fr = cudaFreeAsync(ws, s);
+  if (lr != cudaSuccess || fr != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+int attn_varlen_bwd_preprocess(const void* dout, const void* out, float* delta, int64_t total, int32_t num_heads_q,
+                               int32_t head_dim, void* stream) {
+  if (!dout || !out || !delta) return ATTN_ERR_NULL_POINTER;
+  if (total < 0 || num_heads_q <= 0) return ATTN_ERR_SHAPE;
+  if (head_dim != 128) return ATTN_ERR_HEAD_DIM;
+  if (total > (int64_t(1) << 30) || num_heads_q > 1024) return ATTN_ERR_TOO_LARGE;
+  if (!aligned16(dout) || !aligned16(out) || !aligned16(delta)) return ATTN_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc || total == 0) return rc;
+  BwdParams p{};
+  p.a.total = (int)total;
+  p.a.hq = num_heads_q;
+  p.dout = dout;
+  p.out = out;
+  p.delta = delta;
+  return launch_bwd_preprocess(p, static_cast<cudaStream_t>(stream)) ? ATTN_ERR_CUDA : ATTN_OK;
+}
+
+int attn_varlen_bwd_dkdv(const void* dout, const void* q, const void* k, const void* v, const float* lse,
+                         const float* delta, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                         float softmax_scale, void* dk, void* dv, int64_t total, int32_t num_heads_q,
+                         int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream) {
+  if (!delta || !dk || !dv) return ATTN_ERR_NULL_POINTER;
+  BwdSetup b;
+  int rc = prepare_bwd(b, dout, q, k, v, nullptr, lse, delta, cu_seqlens, max_seqlen, window_left, softmax_scale,
+                       nullptr, dk, dv, total, num_heads_q, num_heads_kv, head_dim, num_segments);
+  if (rc || total == 0) return rc;
+  return launch_bwd_dkdv(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, static_cast<cudaStream_t>(stream))
+             ? ATTN_ERR_CUDA
+             : ATTN_OK;
+}
+
+int attn_varlen_bwd_dq(const void* dout, const void* q, const void* k, const void* v, const float* lse,
+                       const float* delta, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                       float softmax_scale, void* dq, int64_t total, int32_t num_heads_q, int32_t num_heads_kv,
+                       int32_t head_dim, int32_t num_segments, void* stream) {
+  if (!delta || !dq) return ATTN_ERR_NULL_POINTER;
+  BwdSetup b;
+  int rc = prepare_bwd(b, dout, q, k, v, nullptr, lse, delta, cu_seqlens, max_seqlen, window_left, softmax_scale,
+                       dq, nullptr, nullptr, total, num_heads_q, num_heads_kv, head_dim, num_segments);
+  if (rc || total == 0) return rc;
+  return launch_bwd_dq(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, static_cast<cudaStream_t>(stream))
+             ? ATTN_ERR_CUDA
+             : ATTN_OK;
+}
+
+int attn_varlen_get_status(void* stream, int32_t* device_code) {
+  DeviceInfo* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemset(dev->status, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (device_code) *device_code = word;
+  return word ? ATTN_ERR_DEVICE_STATUS : ATTN_OK;
+}
+
+const char* attn_varlen_strerror(int code) {
+  switch (code) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "invalid shape (T, head counts, Hq % Hkv, or segment count)";
+    case ATTN_ERR_HEAD_DIM: return "head_dim must be 128";
+    case ATTN_ERR_ALIGNMENT: return "a tensor pointer is not 16-byte aligned";
+    case ATTN_ERR_WINDOW: return "window_left must be -1 (global) or >= 0";
+    case ATTN_ERR_SCALE: return "softmax_scale must be finite and positive";
+    case ATTN_ERR_MAX_SEQLEN: return "max_seqlen must be in [0, T]";
+    case ATTN_ERR_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
+    case ATTN_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case ATTN_ERR_TOO_LARGE: return "problem size beyond the supported range";
+    case ATTN_ERR_ALLOC: return "backward scratch allocation failed";
+    case ATTN_ERR_DEVICE_STATUS: return "a kernel recorded a device-side error";
+    default: return "unknown error code";
+  }
+}
+
+int attn_varlen_mask_ranges(const int32_t* cu_seqlens, int32_t num_segments, int64_t total, int32_t max_seqlen,
+                            int32_t window_left, int32_t by_key, int32_t* ranges, void* stream) {
+  int rc = validate_common(cu_seqlens, max_seqlen, window_left, 1.f, total, 1, 1, 128, num_segments);
+  if (rc) return rc;
+  if (!ranges) return ATTN_ERR_NULL_POINTER;
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev))) return rc;
+  if (total == 0) return ATTN_OK;
+  if (window_left >= total) window_left = -1;
+  if (launch_mask_probe(cu_seqlens, num_segments, (int)total, window_left, (max_seqlen + kTile - 1) / kTile,
+                        by_key, ranges, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+}  // extern "C"

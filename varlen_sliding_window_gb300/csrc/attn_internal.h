@@ -1,0 +1,56 @@
+// Host/device parameter blocks and launcher declarations shared by the
+// translation units of the library.  Not part of the public C ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace vsw {
+
+// Parameters common to every attention kernel.
+struct AttnParams {
+  const int* cu_seqlens;  // device, [nseg + 1]
+  int nseg;
+  int total;       // tokens T
+  int hq;          // query heads
+  int hkv;         // key/value heads
+  int group;       // hq / hkv
+  int window;      // window_left, -1 = global
+  int max_levels;  // ceil(max_seqlen / 128)
+  float scale;        // softmax_scale
+  float scale_log2;   // softmax_scale * log2(e)
+  int* status;        // device status word
+};
+
+struct FwdParams {
+  AttnParams a;
+  void* out;   // bf16 [T, hq, 128]
+  float* lse;  // fp32 [hq, T]
+};
+
+struct BwdParams {
+  AttnParams a;
+  const void* dout;  // bf16 [T, hq, 128]
+  const void* out;   // bf16 [T, hq, 128]
+  const float* lse;  // fp32 [hq, T]
+  float* delta;      // fp32 [hq, T], scratch: rowsum(dout * out)
+  void* dq;          // bf16 [T, hq, 128]
+  void* dk;          // bf16 [T, hkv, 128]
+  void* dv;          // bf16 [T, hkv, 128]
+};
+
+// Launchers (return a cudaError_t value).
+int launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
+               int num_sms, cudaStream_t stream);
+int launch_bwd_dkdv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,
+                    const BwdParams& p, int num_sms, cudaStream_t stream);
+int launch_bwd_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,
+                  const BwdParams& p, int num_sms, cudaStream_t stream);
+int launch_bwd_preprocess(const BwdParams& p, cudaStream_t stream);
+int launch_mask_probe(const int* cu_seqlens, int nseg, int total, int window, int max_levels, int by_key,
+                      int* ranges, cudaStream_t stream);
+
+// Units of work (tile x head unit) an upper bound: used to size grids.
+inline long long upper_bound_tiles(long long total, int nseg) { return total / 128 + nseg + 1; }
+
+}  // namespace vsw
