@@ -57,6 +57,18 @@ def unmasked_pairs(cu: np.ndarray, window: int) -> int:
     return n
 
 
+def csrc_hash() -> str:
+    """sha1 (12 hex digits) of the CUDA sources: *.cu, then *.cuh, then *.h, each sorted."""
+    import glob
+    import hashlib
+    d = os.path.join(ROOT, "varlen_sliding_window_gb300", "csrc")
+    h = hashlib.sha1()
+    for pat in ("*.cu", "*.cuh", "*.h"):
+        for f in sorted(glob.glob(os.path.join(d, pat))):
+            h.update(open(f, "rb").read())
+    return h.hexdigest()[:12]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -304,7 +316,10 @@ def main():
     tpath = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if os.path.exists(tpath):
         try:
-            traffic = json.load(open(tpath)).get(wl.name, {}).get(dom)
+            rec = json.load(open(tpath))
+            # Counters only count while the kernels are the ones they were taken on.
+            if rec.get("csrc_hash") == csrc_hash():
+                traffic = rec.get(wl.name, {}).get(dom)
         except Exception:
             traffic = None
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
