@@ -4,6 +4,7 @@
 
 #include "attn_internal.h"
 #include "mask.cuh"
+#include "ptx.cuh"
 
 namespace vsw {
 
@@ -11,36 +12,58 @@ namespace {
 
 // D[h, i] = sum_c dout[i,h,c] * out[i,h,c]  (fp32 accumulation of bf16 values).
 // 16 threads per (token, head) row, each reading 16 contiguous bytes of both
-// tensors; rows are visited in memory order so loads are fully coalesced.
+// tensors; a block covers 64 consecutive rows per step (4 rows per thread,
+// all 8 loads issued before any arithmetic) so loads are coalesced and many
+// are in flight.  HBM-bound: 2 x 256 bytes read + 4 bytes written per row.
+// out is read with an evict-first hint (nothing reads it again); dout stays
+// cached for the dK/dV and dQ passes that follow.
+constexpr int kPreRowsPerBlock = 64;
+
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __restrict__ dout,
                                                              const uint4* __restrict__ out,
                                                              float* __restrict__ delta, int total, int hq) {
+  grid_dependency_wait();
   const long long rows = (long long)total * hq;
   const int sub = threadIdx.x & 15;
-  // The loop bound is warp-uniform (a warp covers two consecutive rows) so that
-  // the shuffles below always see both half-warps.
-  for (long long r0 = (long long)blockIdx.x * 16 + ((threadIdx.x >> 5) << 1); r0 < rows;
-       r0 += (long long)gridDim.x * 16) {
-    const long long r = r0 + ((threadIdx.x >> 4) & 1);
-    const bool valid = r < rows;
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    const uint4 a = valid ? dout[r * 16 + sub] : zero;
-    const uint4 b = valid ? out[r * 16 + sub] : zero;
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-    float acc = 0.f;
+  const int r_in = threadIdx.x >> 4;  // 0..15
+  for (long long base = (long long)blockIdx.x * kPreRowsPerBlock; base < rows;
+       base += (long long)gridDim.x * kPreRowsPerBlock) {
+    uint4 a[4], b[4];
+    bool valid[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 x = __bfloat1622float2(a2[e]);
-      const float2 y = __bfloat1622float2(b2[e]);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
+    for (int k = 0; k < 4; ++k) {
+      const long long r = base + 16 * k + r_in;
+      valid[k] = r < rows;
+      a[k] = valid[k] ? __ldg(dout + r * 16 + sub) : make_uint4(0, 0, 0, 0);
+      b[k] = valid[k] ? __ldcs(out + r * 16 + sub) : make_uint4(0, 0, 0, 0);
+    }
+    float acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[k]);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[k]);
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(a2[e]);
+        const float2 y = __bfloat1622float2(b2[e]);
+        s = fmaf(x.x, y.x, s);
+        s = fmaf(x.y, y.y, s);
+      }
+      acc[k] = s;
     }
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (sub == 0 && valid) {
-      const int i = (int)(r / hq), h = (int)(r % hq);
-      delta[(size_t)h * total + i] = acc;
+    for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+    if (sub == 0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (!valid[k]) continue;
+        const long long r = base + 16 * k + r_in;
+        const int i = (int)(r / hq), h = (int)(r % hq);
+        delta[(size_t)h * total + i] = acc[k];
+      }
     }
   }
 }
@@ -112,12 +135,11 @@ __global__ void mask_probe_kernel(const int* __restrict__ cu, int nseg, int tota
 
 int launch_bwd_preprocess(const BwdParams& p, cudaStream_t stream) {
   const long long rows = (long long)p.a.total * p.a.hq;
-  long long blocks = (rows + 15) / 16;
+  long long blocks = (rows + kPreRowsPerBlock - 1) / kPreRowsPerBlock;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  bwd_preprocess_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(p.dout),
-                                                              static_cast<const uint4*>(p.out), p.delta,
-                                                              p.a.total, p.a.hq);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(bwd_preprocess_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                         static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.out), p.delta, p.a.total,
+                         p.a.hq);
 }
 
 int launch_mask_probe(const int* cu_seqlens, int nseg, int total, int window, int max_levels, int by_key,

@@ -12,15 +12,20 @@
 //   1. preprocess (attn_aux.cu): D = rowsum(dout * out)
 //   2. dK/dV pass: one CTA item = (segment, kv tile, kv head).  K and V stay
 //      in shared memory; the CTA loops over the q tiles that can see the kv
-//      tile and over the query heads of the group.  S^T = K Q^T and
-//      dP^T = V dO^T land in TMEM; one thread per key row turns them into
-//      P^T and dS^T (bf16, written back into the same TMEM columns), and
-//      dV += P^T dO, dK += dS^T Q run with the A operand read from TMEM.
+//      tile and over the query heads of the group.
 //   3. dQ pass: one CTA item = (segment, q tile, query head).  Q and dO stay
-//      in shared memory; K/V tiles stream through a ring.  S = Q K^T and
-//      dP = dO V^T in TMEM, dS (bf16) back into TMEM, dQ += dS K.
-// Both passes visit only tiles the mask can see and use the same
-// longest-first schedule as the forward.
+//      in shared memory; K/V tiles stream through a ring.
+//
+// Both passes split the streamed 128-token tile into two 64-token halves.
+// Half x is owned by elementwise warpgroup x and has its own TMEM buffer
+// (64 columns of S plus 64 of dP), so the tensor cores compute one half's
+// S/dP while the other half's elementwise work runs:
+//     MMA:  S/dP(h0)  S/dP(h1)  [P(h0)] dV,dK(h0)  S/dP(next h0)  [P(h1)] dV,dK(h1) ...
+// P^T/dS^T (dK/dV pass) and dS (dQ pass) go back as bf16 into their own
+// buffer's columns and feed the next MMA as its A operand straight from TMEM.
+// tcgen05 MMAs issued by one thread execute in order, so an S/dP MMA that
+// overwrites a buffer always runs after the MMAs that read that buffer's bf16
+// operands.
 #include <cuda_bf16.h>
 
 #include "attn_internal.h"
@@ -34,6 +39,7 @@ namespace vsw {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kHalfRows = 64 * 128;  // byte offset of row 64 inside a swizzled half tile
 
 // Writes 32 fp32 accumulator columns of one row, scaled, as bf16 to global.
 __device__ __forceinline__ void store_row32_bf16(void* dst_row, int c, const uint32_t (&r)[32], float mul) {
@@ -49,19 +55,34 @@ __device__ __forceinline__ void store_row32_bf16(void* dst_row, int c, const uin
   }
 }
 
+// One TMEM load of 64 consecutive columns (two x32 loads, one wait).
+__device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]) {
+  uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+  uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+  tmem_ld32(taddr, lo);
+  tmem_ld32(taddr + 32, hi);
+  tmem_wait_ld(lo);
+  tmem_wait_ld(hi);
+}
+
+// Role split of the 384-thread backward CTAs: warpgroup 0 holds the producer,
+// MMA, TMEM and scheduler warps (few registers), warpgroups 1 and 2 do the
+// elementwise work (launch 168 x 384 = 104 x 128 + 200 x 256 registers).
+constexpr int kBwdThreads = 384;
+
 // ============================================================== dK / dV pass
 struct DkvCfg {
   static constexpr int kStages = 2;  // Q/dO tile pairs in flight
-  static constexpr int kThreads = 256;
   static constexpr uint32_t kKOff = 0;
   static constexpr uint32_t kVOff = kTileBytes;
   static constexpr uint32_t kQOff = 2 * kTileBytes;  // stage s: Q at kQOff + 2s tiles, dO right after
   static constexpr uint32_t kSmemBytes = (2 + 2 * kStages) * kTileBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+  // buffer x: S^T at 128x, dP^T at 128x + 64 (64 columns each); dV, dK after.
+  static constexpr uint32_t kColDV = 256, kColDK = 384;
 };
 
-__global__ void __launch_bounds__(DkvCfg::kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const BwdParams p) {
@@ -72,10 +93,10 @@ __global__ void __launch_bounds__(DkvCfg::kThreads, 1)
   __shared__ int item_counter, n_items;
   __shared__ __align__(8) uint64_t bar_kv_full, bar_kv_empty;
   __shared__ __align__(8) uint64_t bar_qdo_full[S], bar_qdo_empty[S];
-  __shared__ __align__(8) uint64_t bar_s_full, bar_p_full, bar_mma_done, bar_acc_full;
-  __shared__ __align__(8) uint64_t bar_stage[2];
-  __shared__ __align__(16) float s_lse[2][128];
-  __shared__ __align__(16) float s_delta[2][128];
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2];
+  __shared__ __align__(8) uint64_t bar_acc_full, bar_acc_empty;
+  __shared__ __align__(16) float s_lse[S][128];    // lse * log2(e) of the stage's 128 queries
+  __shared__ __align__(16) float s_delta[S][128];  // D of the stage's 128 queries
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -94,12 +115,12 @@ __global__ void __launch_bounds__(DkvCfg::kThreads, 1)
       mbar_init(smem_u32(&bar_qdo_full[s]), 1);
       mbar_init(smem_u32(&bar_qdo_empty[s]), 1);
     }
-    mbar_init(smem_u32(&bar_s_full), 1);
-    mbar_init(smem_u32(&bar_p_full), 128);
-    mbar_init(smem_u32(&bar_mma_done), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&bar_s_full[x]), 1);
+      mbar_init(smem_u32(&bar_p_full[x]), 128);
+    }
     mbar_init(smem_u32(&bar_acc_full), 1);
-    mbar_init(smem_u32(&bar_stage[0]), 128);
-    mbar_init(smem_u32(&bar_stage[1]), 128);
+    mbar_init(smem_u32(&bar_acc_empty), 256);
     fence_mbar_init();
     tma_prefetch_map(&tmQ);
     tma_prefetch_map(&tmK);
@@ -111,6 +132,7 @@ __global__ void __launch_bounds__(DkvCfg::kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 3) {
+    grid_dependency_wait();
     int* cu = reinterpret_cast<int*>(gbase + C::kQOff);
     for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
     __syncwarp();
@@ -121,6 +143,7 @@ __global__ void __launch_bounds__(DkvCfg::kThreads, 1)
       if (n < 0) atomicExch(a.status, 2);
     }
   }
+  grid_dependency_wait();  // inputs written by earlier kernels are read after this
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -129,28 +152,47 @@ __global__ void __launch_bounds__(DkvCfg::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int cnt = 0;
-      bool ok = true;
-      for (int it = 0; it < nit && ok; ++it) {
-        const WorkItem w = items[it];
-        const int nb = num_tiles(w.seg_hi - w.seg_lo);
-        const int k0 = w.seg_lo + w.blk * kTile;
-        const int bl = last_q_tile(w.blk, nb, a.window);
-        const int g = w.unit;
-        if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_kv_empty), (it - 1) & 1, &abort_flag, a.status))) break;
-        mbar_arrive_expect_tx(smem_u32(&bar_kv_full), 2 * kTileBytes);
-        tma_load_3d(sK, &tmK, smem_u32(&bar_kv_full), 0, g, k0);
-        tma_load_3d(sK + kHalfTile, &tmK, smem_u32(&bar_kv_full), 64, g, k0);
-        tma_load_3d(sV, &tmV, smem_u32(&bar_kv_full), 0, g, k0);
-        tma_load_3d(sV + kHalfTile, &tmV, smem_u32(&bar_kv_full), 64, g, k0);
-        for (int b = w.blk; b <= bl && ok; ++b) {
-          const int q0 = w.seg_lo + b * kTile;
-          for (int hh = 0; hh < a.group; ++hh) {
-            const int h = g * a.group + hh;
-            const int slot = cnt % S, use = cnt / S;
-            if (use > 0 && !(ok = mbar_wait(smem_u32(&bar_qdo_empty[slot]), (use - 1) & 1, &abort_flag, a.status)))
-              break;
+    // TMA for K, V (per item) and Q, dO (per q tile and head); the warp's 32
+    // lanes stage lse*log2(e) and D of the stage's queries in shared memory.
+    regs_decrease<104>();
+    int cnt = 0;
+    bool ok = true;
+    for (int it = 0; it < nit && ok; ++it) {
+      const WorkItem w = items[it];
+      const int nb = num_tiles(w.seg_hi - w.seg_lo);
+      const int k0 = w.seg_lo + w.blk * kTile;
+      const int bl = last_q_tile(w.blk, nb, a.window);
+      const int g = w.unit;
+      if (lane == 0) {
+        if (it > 0) ok = mbar_wait(smem_u32(&bar_kv_empty), (it - 1) & 1, &abort_flag, a.status);
+        if (ok) {
+          mbar_arrive_expect_tx(smem_u32(&bar_kv_full), 2 * kTileBytes);
+          tma_load_3d(sK, &tmK, smem_u32(&bar_kv_full), 0, g, k0);
+          tma_load_3d(sK + kHalfTile, &tmK, smem_u32(&bar_kv_full), 64, g, k0);
+          tma_load_3d(sV, &tmV, smem_u32(&bar_kv_full), 0, g, k0);
+          tma_load_3d(sV + kHalfTile, &tmV, smem_u32(&bar_kv_full), 64, g, k0);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      for (int b = w.blk; b <= bl && ok; ++b) {
+        const int q0 = w.seg_lo + b * kTile;
+        for (int hh = 0; hh < a.group && ok; ++hh) {
+          const int h = g * a.group + hh;
+          const int slot = cnt % S, use = cnt / S;
+          if (use > 0) {
+            if (lane == 0) ok = mbar_wait(smem_u32(&bar_qdo_empty[slot]), (use - 1) & 1, &abort_flag, a.status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = lane + 32 * e, iq = q0 + c;
+            const bool in = token_in_range(iq, a.total);
+            s_lse[slot][c] = in ? p.lse[(size_t)h * a.total + iq] * kLog2e : 0.f;
+            s_delta[slot][c] = in ? p.delta[(size_t)h * a.total + iq] : 0.f;
+          }
+          __syncwarp();
+          if (lane == 0) {
             const uint32_t bar = smem_u32(&bar_qdo_full[slot]);
             const uint32_t sq = sQ0 + slot * 2 * kTileBytes, sdo = sq + kTileBytes;
             mbar_arrive_expect_tx(bar, 2 * kTileBytes);
@@ -158,68 +200,90 @@ __global__ void __launch_bounds__(DkvCfg::kThreads, 1)
             tma_load_3d(sq + kHalfTile, &tmQ, bar, 64, h, q0);
             tma_load_3d(sdo, &tmDO, bar, 0, h, q0);
             tma_load_3d(sdo + kHalfTile, &tmDO, bar, 64, h, q0);
-            ++cnt;
           }
+          ++cnt;
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    regs_decrease<104>();
     if (lane == 0) {
-      constexpr uint32_t idesc_ss = make_idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idesc_ts = make_idesc_bf16(128, 128, 0, 1);
-      int cnt = 0;
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, 64, 0, 0);    // S^T, dP^T: 128 keys x 64 queries
+      constexpr uint32_t idesc_g = make_idesc_bf16(128, 128, 0, 1);   // dV, dK: 128 keys x 128 dims
+      int cnt = 0;   // (q tile, head) pairs, for the Q/dO ring
+      int u = 0;     // half tiles, for the S/dP buffers
       bool ok = true;
+      // S^T_x = K Q_half^T and dP^T_x = V dO_half^T into buffer x = half.
+      auto issue_sdp = [&](int slot, int half) {
+        const uint32_t sq = sQ0 + slot * 2 * kTileBytes + half * kHalfRows, sdo = sq + kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 128 * half, kmajor_desc(sK, kk), kmajor_desc(sq, kk), idesc_s, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 128 * half + 64, kmajor_desc(sV, kk), kmajor_desc(sdo, kk), idesc_s, kk > 0);
+        tc_commit(smem_u32(&bar_s_full[half]));
+      };
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
         const int nb = num_tiles(w.seg_hi - w.seg_lo);
         const int bl = last_q_tile(w.blk, nb, a.window);
+        const int npairs = (bl - w.blk + 1) * a.group;
         if (!(ok = mbar_wait(smem_u32(&bar_kv_full), it & 1, &abort_flag, a.status))) break;
         tc_fence_after();
-        bool first = true;
-        for (int b = w.blk; b <= bl && ok; ++b) {
-          for (int hh = 0; hh < a.group; ++hh) {
-            const int slot = cnt % S;
-            if (!(ok = mbar_wait(smem_u32(&bar_qdo_full[slot]), (cnt / S) & 1, &abort_flag, a.status))) break;
-            // The previous iteration's dV/dK MMAs read P^T/dS^T from the S/dP
-            // columns; they must finish before S^T/dP^T are overwritten.
-            if (cnt > 0 && !(ok = mbar_wait(smem_u32(&bar_mma_done), (cnt - 1) & 1, &abort_flag, a.status))) break;
+        // First pair's Q/dO, then both halves' S/dP.
+        if (!(ok = mbar_wait(smem_u32(&bar_qdo_full[cnt % S]), (cnt / S) & 1, &abort_flag, a.status))) break;
+        tc_fence_after();
+        issue_sdp(cnt % S, 0);
+        issue_sdp(cnt % S, 1);
+        // The accumulators of the previous item must have been read out.
+        if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_acc_empty), (it - 1) & 1, &abort_flag, a.status))) break;
+        for (int pr = 0; pr < npairs && ok; ++pr) {
+          const int slot = cnt % S;
+          const bool more = pr + 1 < npairs;
+          if (more) {
+            const int ns = (cnt + 1) % S;
+            if (!(ok = mbar_wait(smem_u32(&bar_qdo_full[ns]), ((cnt + 1) / S) & 1, &abort_flag, a.status))) break;
+          }
+          for (int half = 0; half < 2 && ok; ++half) {
+            if (!(ok = mbar_wait(smem_u32(&bar_p_full[half]), (u >> 1) & 1, &abort_flag, a.status))) break;
             tc_fence_after();
             const uint32_t sq = sQ0 + slot * 2 * kTileBytes, sdo = sq + kTileBytes;
+            const bool acc = pr > 0 || half > 0;
+            // dV += P^T dO_half (K = 64 queries), dK += dS^T Q_half.
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + C::kColS, kmajor_desc(sK, kk), kmajor_desc(sq, kk), idesc_ss, kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tmem + C::kColDV, tmem + 128 * half + kk * 8, mnmajor_desc(sdo, 4 * half + kk), idesc_g,
+                     (acc || kk > 0) ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + C::kColDP, kmajor_desc(sV, kk), kmajor_desc(sdo, kk), idesc_ss, kk > 0);
-            tc_commit(smem_u32(&bar_s_full));
-            if (!(ok = mbar_wait(smem_u32(&bar_p_full), cnt & 1, &abort_flag, a.status))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8, mnmajor_desc(sdo, kk), idesc_ts,
-                     (!first || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8, mnmajor_desc(sq, kk), idesc_ts,
-                     (!first || kk > 0) ? 1u : 0u);
-            tc_commit(smem_u32(&bar_qdo_empty[slot]));
-            tc_commit(smem_u32(&bar_mma_done));
-            first = false;
-            ++cnt;
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tmem + C::kColDK, tmem + 128 * half + 64 + kk * 8, mnmajor_desc(sq, 4 * half + kk), idesc_g,
+                     (acc || kk > 0) ? 1u : 0u);
+            if (half == 1) tc_commit(smem_u32(&bar_qdo_empty[slot]));
+            ++u;
+            // Refill this half's buffer with the next pair's S/dP.
+            if (more) issue_sdp((cnt + 1) % S, half);
           }
+          ++cnt;
         }
         if (!ok) break;
         tc_commit(smem_u32(&bar_acc_full));
         tc_commit(smem_u32(&bar_kv_empty));
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    regs_decrease<104>();
+  } else {
     // ------------------------------------------------------------ elementwise
+    // Warpgroup x = half x of every streamed q tile; thread = key row.
+    regs_increase<200>();
+    const int x = (warp >> 2) - 1;
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // key row of the kv tile
+    const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
-    uint32_t s_cnt = 0;
+    const uint32_t tS = lane_base + 128 * x, tDP = tS + 64;
+    int cnt = 0;
     bool ok = true;
     for (int it = 0; it < nit && ok; ++it) {
       const WorkItem w = items[it];
@@ -229,94 +293,75 @@ __global__ void __launch_bounds__(DkvCfg::kThreads, 1)
       const int g = w.unit;
       const int j = k0 + row;  // this thread's key token
       for (int b = w.blk; b <= bl && ok; ++b) {
-        const int q0 = w.seg_lo + b * kTile;
+        const int q0 = w.seg_lo + b * kTile + 64 * x;  // first query of this half
+        const bool full = tile_fully_visible_kv(k0, w.seg_lo + b * kTile, w.seg_hi, a.window);
         for (int hh = 0; hh < a.group; ++hh) {
-          const int h = g * a.group + hh;
-          // Stage lse (log2 domain) and D of the tile's 128 queries.
-          const int buf = s_cnt & 1;
-          {
-            const int iq = q0 + row;
-            const bool in = token_in_range(iq, a.total);
-            s_lse[buf][row] = in ? p.lse[(size_t)h * a.total + iq] * kLog2e : 0.f;
-            s_delta[buf][row] = in ? p.delta[(size_t)h * a.total + iq] : 0.f;
-          }
-          // All 128 values staged before anyone reads them (bounded wait).
-          mbar_arrive(smem_u32(&bar_stage[buf]));
-          if (!(ok = mbar_wait(smem_u32(&bar_stage[buf]), (s_cnt >> 1) & 1, &abort_flag, a.status))) break;
-          if (!(ok = mbar_wait(smem_u32(&bar_s_full), s_cnt & 1, &abort_flag, a.status))) break;
-          ++s_cnt;
+          const int slot = cnt % S;
+          if (!(ok = mbar_wait(smem_u32(&bar_qdo_full[slot]), (cnt / S) & 1, &abort_flag, a.status))) break;
+          if (!(ok = mbar_wait(smem_u32(&bar_s_full[x]), cnt & 1, &abort_flag, a.status))) break;
           tc_fence_after();
-          int c_lo = 0, c_hi = kTile - 1;
-          if (!tile_fully_visible_kv(k0, q0, w.seg_hi, a.window)) col_visible_rows(j, q0, w.seg_hi, a.window, c_lo, c_hi);
-          float pr[128];
+          int c_lo = 0, c_hi = 63;
+          if (!full) col_visible_rows(j, q0, w.seg_hi, a.window, c_lo, c_hi);
+          const float* lse2 = &s_lse[slot][64 * x];
+          const float* dlt = &s_delta[slot][64 * x];
+          uint32_t sr[64];
+          tmem_ld64_wait(tS, sr);
+          float* pr = reinterpret_cast<float*>(sr);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + C::kColS + c * 32, r);
-            tmem_wait_ld(r);
+          for (int c = 0; c < 64; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              const float4 l4 = *reinterpret_cast<const float4*>(&s_lse[buf][c * 32 + e]);
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int col = c * 32 + e + u;
-                const float x = ex2_approx(fmaf(__uint_as_float(r[e + u]), a.scale_log2, -lv[u]));
-                pr[col] = (col >= c_lo && col <= c_hi) ? x : 0.f;
-              }
+            for (int e = 0; e < 4; ++e) {
+              const float v = ex2_approx(fmaf(pr[c + e], a.scale_log2, -lv[e]));
+              pr[c + e] = (c + e >= c_lo && c + e <= c_hi) ? v : 0.f;
             }
           }
-          // P^T (bf16) over the S^T columns: 64 packed columns.
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          {
             uint32_t pk[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pr[c * 64 + 2 * e], pr[c * 64 + 2 * e + 1]);
-            tmem_st32(lane_base + C::kColS + c * 32, pk);
+            for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
+            tmem_st32(tS, pk);
           }
-          // dS^T = P^T (dP^T - D), written packed over the dP^T columns chunk by chunk.
+          uint32_t dr[64];
+          tmem_ld64_wait(tDP, dr);
+          {
+            uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + C::kColDP + c * 32, r);
-            tmem_wait_ld(r);
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const int col = c * 32 + e;
-              const float d0 = pr[col] * (__uint_as_float(r[e]) - s_delta[buf][col]);
-              const float d1 = pr[col + 1] * (__uint_as_float(r[e + 1]) - s_delta[buf][col + 1]);
-              pk[e >> 1] = pack_bf16x2(d0, d1);
+            for (int c = 0; c < 64; c += 4) {
+              const float4 d4 = *reinterpret_cast<const float4*>(dlt + c);
+              const float d0 = pr[c + 0] * (__uint_as_float(dr[c + 0]) - d4.x);
+              const float d1 = pr[c + 1] * (__uint_as_float(dr[c + 1]) - d4.y);
+              const float d2 = pr[c + 2] * (__uint_as_float(dr[c + 2]) - d4.z);
+              const float d3 = pr[c + 3] * (__uint_as_float(dr[c + 3]) - d4.w);
+              pk[c / 2] = pack_bf16x2(d0, d1);
+              pk[c / 2 + 1] = pack_bf16x2(d2, d3);
             }
-            tmem_st16(lane_base + C::kColDP + c * 16, pk);
+            tmem_st32(tDP, pk);
           }
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(smem_u32(&bar_p_full));
+          mbar_arrive(smem_u32(&bar_p_full[x]));
+          ++cnt;
         }
       }
       if (!ok) break;
-      // ---- epilogue: dV, dK (x scale) of this kv tile
+      // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (x scale).
       if (!(ok = mbar_wait(smem_u32(&bar_acc_full), it & 1, &abort_flag, a.status))) break;
       tc_fence_after();
       const bool valid = j < w.seg_hi && token_in_range(j, a.total);
-      void* dv_row = static_cast<__nv_bfloat16*>(p.dv) + ((size_t)j * a.hkv + g) * kHeadDim;
-      void* dk_row = static_cast<__nv_bfloat16*>(p.dk) + ((size_t)j * a.hkv + g) * kHeadDim;
+      void* dst_row = static_cast<__nv_bfloat16*>(x == 0 ? p.dv : p.dk) + ((size_t)j * a.hkv + g) * kHeadDim;
+      const uint32_t tacc = lane_base + (x == 0 ? C::kColDV : C::kColDK);
+      const float mul = x == 0 ? 1.f : a.scale;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        tmem_ld32(lane_base + C::kColDV + c * 32, r);
+        tmem_ld32(tacc + c * 32, r);
         tmem_wait_ld(r);
-        if (valid) store_row32_bf16(dv_row, c * 32, r, 1.f);
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(lane_base + C::kColDK + c * 32, r);
-        tmem_wait_ld(r);
-        if (valid) store_row32_bf16(dk_row, c * 32, r, a.scale);
+        if (valid) store_row32_bf16(dst_row, c * 32, r, mul);
       }
       tc_fence_before();
+      mbar_arrive(smem_u32(&bar_acc_empty));
     }
   }
 
@@ -331,16 +376,16 @@ __global__ void __launch_bounds__(DkvCfg::kThreads, 1)
 // ============================================================== dQ pass
 struct DqCfg {
   static constexpr int kStages = 4;  // K/V tile slots
-  static constexpr int kThreads = 256;
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kDOOff = kTileBytes;
   static constexpr uint32_t kKVOff = 2 * kTileBytes;
   static constexpr uint32_t kSmemBytes = (2 + kStages) * kTileBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  // buffer x: S at 128x, dP at 128x + 64 (64 columns each); dQ after.
+  static constexpr uint32_t kColDQ = 256;
 };
 
-__global__ void __launch_bounds__(DqCfg::kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwdParams p) {
@@ -351,7 +396,8 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
   __shared__ int item_counter, n_items;
   __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty;
   __shared__ __align__(8) uint64_t bar_kv_full[S], bar_kv_empty[S];
-  __shared__ __align__(8) uint64_t bar_s_full, bar_p_full, bar_mma_done, bar_acc_full;
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2];
+  __shared__ __align__(8) uint64_t bar_acc_full, bar_acc_empty;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -370,10 +416,12 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
       mbar_init(smem_u32(&bar_kv_full[s]), 1);
       mbar_init(smem_u32(&bar_kv_empty[s]), 1);
     }
-    mbar_init(smem_u32(&bar_s_full), 1);
-    mbar_init(smem_u32(&bar_p_full), 128);
-    mbar_init(smem_u32(&bar_mma_done), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&bar_s_full[x]), 1);
+      mbar_init(smem_u32(&bar_p_full[x]), 128);
+    }
     mbar_init(smem_u32(&bar_acc_full), 1);
+    mbar_init(smem_u32(&bar_acc_empty), 256);
     fence_mbar_init();
     tma_prefetch_map(&tmQ);
     tma_prefetch_map(&tmK);
@@ -385,6 +433,7 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 3) {
+    grid_dependency_wait();
     int* cu = reinterpret_cast<int*>(gbase + C::kKVOff);
     for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
     __syncwarp();
@@ -395,6 +444,7 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
       if (n < 0) atomicExch(a.status, 2);
     }
   }
+  grid_dependency_wait();  // inputs written by earlier kernels are read after this
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -403,6 +453,7 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    regs_decrease<104>();
     if (lane == 0) {
       int kv_cnt = 0;
       bool ok = true;
@@ -435,56 +486,81 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    regs_decrease<104>();
     if (lane == 0) {
-      constexpr uint32_t idesc_ss = make_idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idesc_ts = make_idesc_bf16(128, 128, 0, 1);
-      int kv_cnt = 0, cnt = 0;
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, 64, 0, 0);    // S, dP: 128 queries x 64 keys
+      constexpr uint32_t idesc_g = make_idesc_bf16(128, 128, 0, 1);   // dQ: 128 queries x 128 dims
+      int kv_cnt = 0;  // K/V ring position (K and V take one slot each)
+      int u = 0;       // half tiles
       bool ok = true;
+      // S_x = Q K_half^T, dP_x = dO V_half^T for the K/V pair at ring position kc.
+      auto issue_sdp = [&](int kc, int half) {
+        const uint32_t kt = sKV + (kc % S) * kTileBytes + half * kHalfRows;
+        const uint32_t vt = sKV + ((kc + 1) % S) * kTileBytes + half * kHalfRows;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 128 * half, kmajor_desc(sQ, kk), kmajor_desc(kt, kk), idesc_s, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 128 * half + 64, kmajor_desc(sDO, kk), kmajor_desc(vt, kk), idesc_s, kk > 0);
+        tc_commit(smem_u32(&bar_s_full[half]));
+      };
+      auto wait_kv_pair = [&](int kc) -> bool {
+        for (int e = 0; e < 2; ++e)
+          if (!mbar_wait(smem_u32(&bar_kv_full[(kc + e) % S]), ((kc + e) / S) & 1, &abort_flag, a.status))
+            return false;
+        tc_fence_after();
+        return true;
+      };
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
         const int n0 = first_kv_tile(w.blk, a.window);
+        const int nt = w.blk - n0 + 1;
         if (!(ok = mbar_wait(smem_u32(&bar_q_full), it & 1, &abort_flag, a.status))) break;
         tc_fence_after();
-        for (int n = n0; n <= w.blk && ok; ++n) {
-          const int slotK = kv_cnt % S;
-          if (!(ok = mbar_wait(smem_u32(&bar_kv_full[slotK]), (kv_cnt / S) & 1, &abort_flag, a.status))) break;
-          ++kv_cnt;
-          const int slotV = kv_cnt % S;
-          if (!(ok = mbar_wait(smem_u32(&bar_kv_full[slotV]), (kv_cnt / S) & 1, &abort_flag, a.status))) break;
-          ++kv_cnt;
-          // dS of the previous step (read by its dQ MMA) lives in the S columns.
-          if (cnt > 0 && !(ok = mbar_wait(smem_u32(&bar_mma_done), (cnt - 1) & 1, &abort_flag, a.status))) break;
-          tc_fence_after();
-          const uint32_t kt = sKV + slotK * kTileBytes, vt = sKV + slotV * kTileBytes;
+        if (!(ok = wait_kv_pair(kv_cnt))) break;
+        issue_sdp(kv_cnt, 0);
+        issue_sdp(kv_cnt, 1);
+        if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_acc_empty), (it - 1) & 1, &abort_flag, a.status))) break;
+        for (int n = 0; n < nt && ok; ++n) {
+          const int kc = kv_cnt;
+          const bool more = n + 1 < nt;
+          if (more && !(ok = wait_kv_pair(kc + 2))) break;
+          for (int half = 0; half < 2 && ok; ++half) {
+            if (!(ok = mbar_wait(smem_u32(&bar_p_full[half]), (u >> 1) & 1, &abort_flag, a.status))) break;
+            tc_fence_after();
+            const uint32_t kt = sKV + (kc % S) * kTileBytes;
+            // dQ += dS_half K_half (K = 64 keys).
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::kColS, kmajor_desc(sQ, kk), kmajor_desc(kt, kk), idesc_ss, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::kColDP, kmajor_desc(sDO, kk), kmajor_desc(vt, kk), idesc_ss, kk > 0);
-          tc_commit(smem_u32(&bar_s_full));
-          tc_commit(smem_u32(&bar_kv_empty[slotV]));
-          if (!(ok = mbar_wait(smem_u32(&bar_p_full), cnt & 1, &abort_flag, a.status))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C::kColDQ, tmem + C::kColS + kk * 8, mnmajor_desc(kt, kk), idesc_ts,
-                   (n > n0 || kk > 0) ? 1u : 0u);
-          tc_commit(smem_u32(&bar_kv_empty[slotK]));
-          tc_commit(smem_u32(&bar_mma_done));
-          ++cnt;
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tmem + C::kColDQ, tmem + 128 * half + kk * 8, mnmajor_desc(kt, 4 * half + kk), idesc_g,
+                     (n > 0 || half > 0 || kk > 0) ? 1u : 0u);
+            if (half == 1) {
+              tc_commit(smem_u32(&bar_kv_empty[kc % S]));
+              tc_commit(smem_u32(&bar_kv_empty[(kc + 1) % S]));
+            }
+            ++u;
+            if (more) issue_sdp(kc + 2, half);
+          }
+          kv_cnt += 2;
         }
         if (!ok) break;
         tc_commit(smem_u32(&bar_acc_full));
         tc_commit(smem_u32(&bar_q_empty));
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    regs_decrease<104>();
+  } else {
     // ------------------------------------------------------------ elementwise
+    // Warpgroup x = half x (64 keys) of every streamed kv tile; thread = query row.
+    regs_increase<200>();
+    const int x = (warp >> 2) - 1;
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // query row of the q tile
+    const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
-    uint32_t s_cnt = 0;
+    const uint32_t tS = lane_base + 128 * x, tDP = tS + 64;
+    int cnt = 0;
     bool ok = true;
     for (int it = 0; it < nit && ok; ++it) {
       const WorkItem w = items[it];
@@ -496,56 +572,45 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
       const float lse2 = valid ? p.lse[(size_t)h * a.total + i] * kLog2e : 0.f;
       const float dlt = valid ? p.delta[(size_t)h * a.total + i] : 0.f;
       for (int n = n0; n <= w.blk; ++n) {
-        const int k0 = w.seg_lo + n * kTile;
-        if (!(ok = mbar_wait(smem_u32(&bar_s_full), s_cnt & 1, &abort_flag, a.status))) break;
-        ++s_cnt;
+        const int kt0 = w.seg_lo + n * kTile;
+        if (!(ok = mbar_wait(smem_u32(&bar_s_full[x]), cnt & 1, &abort_flag, a.status))) break;
         tc_fence_after();
-        int c_lo = 0, c_hi = kTile - 1;
-        if (!tile_fully_visible(q0, k0, a.window)) row_visible_cols(i, k0, a.window, c_lo, c_hi);
-        float pr[128];
+        int c_lo = 0, c_hi = 63;
+        if (!tile_fully_visible(q0, kt0, a.window)) row_visible_cols(i, kt0 + 64 * x, a.window, c_lo, c_hi);
+        uint32_t sr[64];
+        tmem_ld64_wait(tS, sr);
+        float* pr = reinterpret_cast<float*>(sr);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + C::kColS + c * 32, r);
-          tmem_wait_ld(r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = c * 32 + e;
-            const float x = ex2_approx(fmaf(__uint_as_float(r[e]), a.scale_log2, -lse2));
-            pr[col] = (col >= c_lo && col <= c_hi) ? x : 0.f;
-          }
+        for (int c = 0; c < 64; ++c) {
+          const float v = ex2_approx(fmaf(pr[c], a.scale_log2, -lse2));
+          pr[c] = (c >= c_lo && c <= c_hi) ? v : 0.f;
         }
-        // dS = P (dP - D) -> bf16, packed over the S columns.
+        uint32_t dr[64];
+        tmem_ld64_wait(tDP, dr);
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + C::kColDP + c * 32, r);
-          tmem_wait_ld(r);
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int col = c * 32 + e;
-            pk[e >> 1] = pack_bf16x2(pr[col] * (__uint_as_float(r[e]) - dlt),
-                                     pr[col + 1] * (__uint_as_float(r[e + 1]) - dlt));
-          }
-          tmem_st16(lane_base + C::kColS + c * 16, pk);
-        }
+        for (int c = 0; c < 64; c += 2)
+          pk[c / 2] = pack_bf16x2(pr[c] * (__uint_as_float(dr[c]) - dlt), pr[c + 1] * (__uint_as_float(dr[c + 1]) - dlt));
+        tmem_st32(tS, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&bar_p_full));
+        mbar_arrive(smem_u32(&bar_p_full[x]));
+        ++cnt;
       }
       if (!ok) break;
+      // ---- epilogue: warpgroup x writes dQ columns [64x, 64x + 64) (x scale).
       if (!(ok = mbar_wait(smem_u32(&bar_acc_full), it & 1, &abort_flag, a.status))) break;
       tc_fence_after();
       void* dq_row = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)i * a.hq + h) * kHeadDim;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
-        tmem_ld32(lane_base + C::kColDQ + c * 32, r);
+        tmem_ld32(lane_base + C::kColDQ + 64 * x + c * 32, r);
         tmem_wait_ld(r);
-        if (valid) store_row32_bf16(dq_row, c * 32, r, a.scale);
+        if (valid) store_row32_bf16(dq_row, 64 * x + c * 32, r, a.scale);
       }
       tc_fence_before();
+      mbar_arrive(smem_u32(&bar_acc_empty));
     }
   }
 
@@ -573,8 +638,8 @@ int launch_bwd_dkdv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtens
                                        (int)DkvCfg::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
   const long long g = persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hkv, num_sms);
-  attn_bwd_dkdv_kernel<<<(unsigned)g, DkvCfg::kThreads, DkvCfg::kSmemBytes, stream>>>(tmQ, tmK, tmV, tmDO, p);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(attn_bwd_dkdv_kernel, dim3((unsigned)g), dim3(kBwdThreads), DkvCfg::kSmemBytes, stream, tmQ,
+                         tmK, tmV, tmDO, p);
 }
 
 int launch_bwd_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,
@@ -583,8 +648,8 @@ int launch_bwd_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensor
       cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DqCfg::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
   const long long g = persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hq, num_sms);
-  attn_bwd_dq_kernel<<<(unsigned)g, DqCfg::kThreads, DqCfg::kSmemBytes, stream>>>(tmQ, tmK, tmV, tmDO, p);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(attn_bwd_dq_kernel, dim3((unsigned)g), dim3(kBwdThreads), DqCfg::kSmemBytes, stream, tmQ,
+                         tmK, tmV, tmDO, p);
 }
 
 }  // namespace vsw

@@ -7,20 +7,28 @@
 // log-sum-exp of the scaled logits (fp32, [Hq, T]) for the backward pass.
 //
 // How (one persistent CTA per SM, warp-specialised):
-//   warp 0        TMA producer: Q tiles of NQT heads, then K_j, V_j tiles
-//                 through a ring of shared-memory slots
-//   warp 1        MMA issuer: S_t = Q_t K_j^T and O_t += P_t V_j with tcgen05,
-//                 accumulators in Tensor Memory
+//   warp 0        TMA producer: Q tiles of NQT heads (double-buffered across
+//                 work items), then K_j, V_j tiles through a ring of slots
+//   warp 1        MMA issuer: S_t = Q_t K_j^T (both operands in shared memory)
+//                 and O_t += P_t V_j (P_t read from TMEM), fp32 accumulators
+//                 in Tensor Memory
 //   warp 2        owns the TMEM allocation
 //   warp 3        builds the CTA's longest-first work list (sched.cuh)
 //   warpgroup 1+t online softmax of q tile t: one thread per query row reads
 //                 its S row from TMEM, masks only tiles that straddle the mask
-//                 edge, rescales O in TMEM when the running max moves, writes
-//                 P (bf16) to shared memory for the PV MMA, and finally
-//                 normalises O and stores out and lse.
+//                 edge, writes P (bf16) back over the first half of its S
+//                 columns, rescales O in TMEM when the running max moves, and
+//                 finally normalises O and stores out and lse.
 // The NQT q tiles of a CTA are heads of the same group, so each K/V tile
 // loaded from HBM/L2 feeds NQT heads.  Tiles that the mask hides completely
 // are never loaded (the kv tile range comes from mask.cuh).
+//
+// P_t aliases S_t in TMEM.  This is safe because the MMA warp issues PV_t(j)
+// (which reads P_t) before S_t(j+1) (which overwrites it) and tcgen05 MMAs of
+// one thread execute in order; and the softmax only writes P_t(j) after it
+// has read all of S_t(j).  When the softmax sees S_t(j+1) complete, PV_t(j)
+// is complete too (the commit covers every earlier MMA), so O_t may then be
+// rescaled without another barrier.
 #include <cuda_bf16.h>
 
 #include "attn_internal.h"
@@ -35,12 +43,12 @@ namespace {
 
 template <int NQT>
 struct FwdCfg {
-  static constexpr int kStages = NQT == 2 ? 3 : 4;
+  static constexpr int kQStages = 2;                   // Q tiles of consecutive work items
+  static constexpr int kStages = NQT == 2 ? 3 : 5;     // K/V tile slots
   static constexpr int kThreads = 128 * (1 + NQT);
-  static constexpr uint32_t kQOff = 0;
-  static constexpr uint32_t kKVOff = NQT * kTileBytes;
-  static constexpr uint32_t kPOff = kKVOff + kStages * kTileBytes;
-  static constexpr uint32_t kSmemBytes = kPOff + NQT * kTileBytes + 1024;
+  static constexpr uint32_t kQOff = 0;                  // Q stage s, tile t: (s * NQT + t) tiles
+  static constexpr uint32_t kKVOff = kQStages * NQT * kTileBytes;
+  static constexpr uint32_t kSmemBytes = kKVOff + kStages * kTileBytes + 1024;
   static constexpr uint32_t kTmemCols = NQT == 2 ? 512 : 256;
   static constexpr uint32_t kOCol = NQT * 128;  // O accumulators follow the S tiles
 };
@@ -55,7 +63,7 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
   __shared__ WorkItem items[kMaxItemsPerCta];
   __shared__ int item_counter;
   __shared__ int n_items;
-  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty;
+  __shared__ __align__(8) uint64_t bar_q_full[2], bar_q_empty[2];
   __shared__ __align__(8) uint64_t bar_kv_full[S], bar_kv_empty[S];
   __shared__ __align__(8) uint64_t bar_s_full[NQT], bar_p_full[NQT], bar_o_done[NQT];
   __shared__ uint32_t tmem_slot;
@@ -64,14 +72,16 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (sbase - raw);
-  const uint32_t sQ = sbase + C::kQOff, sKV = sbase + C::kKVOff, sP = sbase + C::kPOff;
+  const uint32_t sQ = sbase + C::kQOff, sKV = sbase + C::kKVOff;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const AttnParams& a = p.a;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(smem_u32(&bar_q_full), 1);
-    mbar_init(smem_u32(&bar_q_empty), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bar_q_full[s]), 1);
+      mbar_init(smem_u32(&bar_q_empty[s]), 1);
+    }
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&bar_kv_full[s]), 1);
       mbar_init(smem_u32(&bar_kv_empty[s]), 1);
@@ -91,8 +101,9 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 3) {
-    // cu_seqlens is staged in the (not yet used) P region.
-    int* cu = reinterpret_cast<int*>(gbase + C::kPOff);
+    grid_dependency_wait();
+    // cu_seqlens is staged in the (not yet used) K/V region.
+    int* cu = reinterpret_cast<int*>(gbase + C::kKVOff);
     for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
     __syncwarp();
     const int n = build_schedule(cu, a.nseg, a.max_levels, a.hq / NQT, false, items, kMaxItemsPerCta,
@@ -102,14 +113,18 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
       if (n < 0) atomicExch(a.status, 2);
     }
   }
+  grid_dependency_wait();  // inputs written by earlier kernels are read after this
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const int nit = n_items;
-
+  // With two softmax warpgroups, they take the registers the single-thread
+  // roles do not need (launch: 168 x 384 threads; after: 104 x 128 +
+  // 200 x 256, the same total, with no spills at these limits).
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    if (NQT == 2) regs_decrease<104>();
     if (lane == 0) {
       int kv_cnt = 0;
       bool ok = true;
@@ -118,12 +133,16 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
         const int q_lo = w.seg_lo + w.blk * kTile;
         const int n0 = first_kv_tile(w.blk, a.window);
         const int nt = w.blk - n0 + 1;
-        if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_q_empty), (it - 1) & 1, &abort_flag, a.status))) break;
-        mbar_arrive_expect_tx(smem_u32(&bar_q_full), NQT * kTileBytes);
+        const int qs = it & 1;
+        if (it >= 2 && !(ok = mbar_wait(smem_u32(&bar_q_empty[qs]), ((it >> 1) - 1) & 1, &abort_flag, a.status)))
+          break;
+        const uint32_t qbar = smem_u32(&bar_q_full[qs]);
+        mbar_arrive_expect_tx(qbar, NQT * kTileBytes);
         for (int t = 0; t < NQT; ++t) {
           const int h = w.unit * NQT + t;
-          tma_load_3d(sQ + t * kTileBytes, &tmQ, smem_u32(&bar_q_full), 0, h, q_lo);
-          tma_load_3d(sQ + t * kTileBytes + kHalfTile, &tmQ, smem_u32(&bar_q_full), 64, h, q_lo);
+          const uint32_t dst = sQ + (qs * NQT + t) * kTileBytes;
+          tma_load_3d(dst, &tmQ, qbar, 0, h, q_lo);
+          tma_load_3d(dst + kHalfTile, &tmQ, qbar, 64, h, q_lo);
         }
         const int g = (w.unit * NQT) / a.group;
         for (int j = 0; j < nt && ok; ++j) {
@@ -144,6 +163,7 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    if (NQT == 2) regs_decrease<104>();
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, 128, 0, 1);
@@ -158,18 +178,19 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
         tc_fence_after();
         return r;
       };
-      auto issue_qk = [&](int t, int slotK) {
-        const uint32_t d = tmem + t * 128;
-        const uint32_t qt = sQ + t * kTileBytes, kt = sKV + slotK * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(d, kmajor_desc(qt, kk), kmajor_desc(kt, kk), idesc_qk, kk > 0);
-        tc_commit(smem_u32(&bar_s_full[t]));
-      };
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
         const int n0 = first_kv_tile(w.blk, a.window);
         const int nt = w.blk - n0 + 1;
-        if (!(ok = mbar_wait(smem_u32(&bar_q_full), it & 1, &abort_flag, a.status))) break;
+        const int qs = it & 1;
+        auto issue_qk = [&](int t, int slotK) {
+          const uint32_t d = tmem + t * 128;
+          const uint32_t qt = sQ + (qs * NQT + t) * kTileBytes, kt = sKV + slotK * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss(d, kmajor_desc(qt, kk), kmajor_desc(kt, kk), idesc_qk, kk > 0);
+          tc_commit(smem_u32(&bar_s_full[t]));
+        };
+        if (!(ok = mbar_wait(smem_u32(&bar_q_full[qs]), (it >> 1) & 1, &abort_flag, a.status))) break;
         tc_fence_after();
         int slotK;
         if (!(ok = wait_kv(slotK))) break;
@@ -183,11 +204,12 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
             ++p_cnt[t];
             tc_fence_after();
             const uint32_t d = tmem + C::kOCol + t * 128;
-            const uint32_t pt = sP + t * kTileBytes, vt = sKV + slotV * kTileBytes;
+            const uint32_t vt = sKV + slotV * kTileBytes;
+            // O_t += P_t V: P_t (bf16, 64 packed columns over S_t) is the A operand.
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_ss(d, kmajor_desc(pt, kk), mnmajor_desc(vt, kk), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(smem_u32(&bar_o_done[t]));
+              mma_ts(d, tmem + t * 128 + kk * 8, mnmajor_desc(vt, kk), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            if (j + 1 == nt) tc_commit(smem_u32(&bar_o_done[t]));
             if (j + 1 < nt) {
               if (t == 0 && !(ok = wait_kv(slotK2))) break;
               issue_qk(t, slotK2);
@@ -197,19 +219,22 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
           tc_commit(smem_u32(&bar_kv_empty[slotV]));
           if (j + 1 < nt) tc_commit(smem_u32(&bar_kv_empty[slotK2]));
         }
-        if (ok) tc_commit(smem_u32(&bar_q_empty));
+        if (ok) tc_commit(smem_u32(&bar_q_empty[qs]));
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    if (NQT == 2) regs_decrease<104>();
+  } else {
     // ------------------------------------------------------------ softmax
+    if (NQT == 2) regs_increase<200>();
     const int t = (warp >> 2) - 1;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
     const uint32_t tS = lane_base + t * 128;
     const uint32_t tO = lane_base + C::kOCol + t * 128;
-    const uint32_t pT = sP + t * kTileBytes;
-    uint32_t s_cnt = 0, o_cnt = 0;
+    const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2);
+    uint32_t s_cnt = 0;
     bool ok = true;
     for (int it = 0; it < nit && ok; ++it) {
       const WorkItem w = items[it];
@@ -224,15 +249,9 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
         if (!(ok = mbar_wait(smem_u32(&bar_s_full[t]), s_cnt & 1, &abort_flag, a.status))) break;
         ++s_cnt;
         tc_fence_after();
-        float s[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tS + c * 32, r);
-          tmem_wait_ld(r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
-        }
+        uint32_t sr[128];
+        tmem_ld128_wait(tS, sr);
+        float* s = reinterpret_cast<float*>(sr);
         if (!tile_fully_visible(q_lo, k0, a.window)) {
           int lo_rel, hi_rel;
           row_visible_cols(i, k0, a.window, lo_rel, hi_rel);
@@ -240,52 +259,79 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c < lo_rel || c > hi_rel) s[c] = -INFINITY;
         }
-        float mx = s[0];
+        // Row max: a tree of three-input maxima.
+        float mx[16];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        const float m_new = fmaxf(m, mx * a.scale_log2);
+        for (int e = 0; e < 16; ++e) mx[e] = fmax3(s[8 * e], s[8 * e + 1], s[8 * e + 2]);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) mx[e] = fmax3(mx[e], s[8 * e + 3], s[8 * e + 4]);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) mx[e] = fmax3(mx[e], s[8 * e + 5], s[8 * e + 6]);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) mx[e] = fmaxf(mx[e], s[8 * e + 7]);
+#pragma unroll
+        for (int e = 0; e < 5; ++e) mx[e] = fmax3(mx[e], mx[e + 5], mx[e + 10]);
+        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[15]), -INFINITY) * a.scale_log2;
+        // Lazy rescaling: the reference max moves only when the tile max
+        // exceeds it by more than 8 (log2 units), so P stays <= 2^8 and O is
+        // rescaled in TMEM only on those (rare) tiles.  out = O / l and lse
+        // use the same reference, so the result is exact.
+        const bool bump = mt > m + 8.f;
+        const float m_new = bump ? mt : m;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ex2_approx(m - m_use);
-        float rs = 0.f;
+        const float alpha = bump ? ex2_approx(m - m_use) : 1.f;
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
+        uint64_t rs2[4] = {0, 0, 0, 0};
+        // p = exp2(s * scale*log2e - m), packed to bf16 pairs 32 at a time and
+        // stored over the first 64 columns of S_t.
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          s[c] = ex2_approx(fmaf(s[c], a.scale_log2, -m_use));
-          rs += s[c];
-        }
-        if (j > 0) {
-          // PV of the previous tile must be done before O is rescaled and P overwritten.
-          if (!(ok = mbar_wait(smem_u32(&bar_o_done[t]), o_cnt & 1, &abort_flag, a.status))) break;
-          ++o_cnt;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t r[32];
-              tmem_ld32(tO + c * 32, r);
-              tmem_wait_ld(r);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              tmem_st32(tO + c * 32, r);
-            }
-            tmem_wait_st();
+          for (int e = 0; e < 32; ++e) {
+            const int c = 64 * h2 + 2 * e;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), scale2, negm2), x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            rs2[e & 3] = f2_add(rs2[e & 3], f2_pack(p0, p1));
+            pk[e] = pack_bf16x2(p0, p1);
           }
+          tmem_st32(tS + 32 * h2, pk);
         }
+        float r0, r1, r2, r3, r4, r5, r6, r7;
+        f2_unpack(rs2[0], r0, r1);
+        f2_unpack(rs2[1], r2, r3);
+        f2_unpack(rs2[2], r4, r5);
+        f2_unpack(rs2[3], r6, r7);
+        const float rs = ((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7));
         l = l * alpha + rs;
         m = m_new;
-        // P (bf16) into the 128-byte-swizzled K-major layout the MMA reads.
+        // PV of the previous tile is complete here: the S commit just waited on
+        // was issued after it.  Rescale O only where the reference moved.
+        if (j > 0 && __any_sync(0xffffffffu, bump)) {
+          const uint64_t alpha2 = f2_pack(alpha, alpha);
 #pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8)
-          st_shared_v4(swizzled_chunk(pT, row, c8), pack_bf16x2(s[c8 * 8 + 0], s[c8 * 8 + 1]),
-                       pack_bf16x2(s[c8 * 8 + 2], s[c8 * 8 + 3]), pack_bf16x2(s[c8 * 8 + 4], s[c8 * 8 + 5]),
-                       pack_bf16x2(s[c8 * 8 + 6], s[c8 * 8 + 7]));
-        fence_proxy_async_smem();
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tO + c * 32, r);
+            tmem_wait_ld(r);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float y0, y1;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), alpha2), y0, y1);
+              r[e] = __float_as_uint(y0);
+              r[e + 1] = __float_as_uint(y1);
+            }
+            tmem_st32(tO + c * 32, r);
+          }
+        }
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_p_full[t]));
       }
       if (!ok) break;
       // ---- epilogue: O / l -> out (bf16), lse
-      if (!(ok = mbar_wait(smem_u32(&bar_o_done[t]), o_cnt & 1, &abort_flag, a.status))) break;
-      ++o_cnt;
+      if (!(ok = mbar_wait(smem_u32(&bar_o_done[t]), it & 1, &abort_flag, a.status))) break;
       tc_fence_after();
       const bool valid = i < w.seg_hi && token_in_range(i, a.total);
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
@@ -325,20 +371,16 @@ template <int NQT>
 int launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
                  int num_sms, cudaStream_t stream) {
   using C = FwdCfg<NQT>;
-  static bool attr_set = false;  // per process; the attribute is per function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<NQT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmemBytes);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<NQT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C::kSmemBytes);
+  if (e != cudaSuccess) return (int)e;
   const long long units = upper_bound_tiles(p.a.total, p.a.nseg) * (p.a.hq / NQT);
   long long grid = num_sms;
   const long long need = (units + kMaxItemsPerCta - 1) / kMaxItemsPerCta;
   if (need > grid) grid = need;
   if (units < grid) grid = units > 0 ? units : 1;
-  attn_fwd_kernel<NQT><<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, p);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(attn_fwd_kernel<NQT>, dim3((unsigned)grid), dim3(C::kThreads), C::kSmemBytes, stream, tmQ,
+                         tmK, tmV, p);
 }
 
 }  // namespace

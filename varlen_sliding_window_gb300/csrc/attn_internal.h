@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 namespace vsw {
 
@@ -49,6 +50,26 @@ int launch_bwd_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensor
 int launch_bwd_preprocess(const BwdParams& p, cudaStream_t stream);
 int launch_mask_probe(const int* cu_seqlens, int nseg, int total, int window, int max_levels, int by_key,
                       int* ranges, cudaStream_t stream);
+
+// Launches `kernel` on `stream` with programmatic stream serialization, so
+// that its CTAs may start (and run their prologue) while the previous kernel
+// in the stream drains.  Every kernel of this library calls
+// grid_dependency_wait() before reading global memory written earlier.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Units of work (tile x head unit) an upper bound: used to size grids.
 inline long long upper_bound_tiles(long long total, int nseg) { return total / 128 + nseg + 1; }
