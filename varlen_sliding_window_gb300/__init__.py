@@ -9,7 +9,7 @@ from importlib import import_module
 _BINDING_NAMES = {
     "attn_varlen_fwd", "attn_varlen_bwd", "attn_varlen_bwd_workspace_bytes", "attn_varlen_get_status",
     "attn_varlen_strerror", "attn_varlen_mask_ranges", "attn_varlen_bwd_preprocess",
-    "attn_varlen_bwd_dkdv", "attn_varlen_bwd_dq", "load_library", "AttnError",
+    "attn_varlen_bwd_dkdv", "attn_varlen_bwd_dq", "attn_varlen_bwd_noalloc", "load_library", "AttnError",
 }
 
 

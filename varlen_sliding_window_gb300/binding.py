@@ -51,6 +51,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.attn_varlen_bwd_dkdv.restype = ctypes.c_int
     lib.attn_varlen_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, vp, i64, i32, i32, i32, i32, vp]
     lib.attn_varlen_bwd_dq.restype = ctypes.c_int
+    lib.attn_varlen_bwd_noalloc.argtypes = lib.attn_varlen_bwd.argtypes
+    lib.attn_varlen_bwd_noalloc.restype = ctypes.c_int
     lib.attn_varlen_mask_ranges.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp]
     lib.attn_varlen_mask_ranges.restype = ctypes.c_int
     _lib = lib
@@ -103,6 +105,17 @@ def attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seqlen: int, window
                              int(max_seqlen), int(window_left), float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv),
                              total, hq, hkv, d, nseg, _stream_handle(stream))
     _check(rc, "attn_varlen_bwd")
+
+
+def attn_varlen_bwd_noalloc(dout, q, k, v, out, lse, cu_seqlens, max_seqlen: int, window_left: int,
+                            softmax_scale: float, dq, dk, dv, stream=None) -> None:
+    """Backward with its scratch in the library's fixed device array (no allocation)."""
+    lib = load_library()
+    total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
+    rc = lib.attn_varlen_bwd_noalloc(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
+                                     int(max_seqlen), int(window_left), float(softmax_scale), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), total, hq, hkv, d, nseg, _stream_handle(stream))
+    _check(rc, "attn_varlen_bwd_noalloc")
 
 
 def attn_varlen_bwd_preprocess(dout, out, delta, stream=None) -> None:

@@ -300,6 +300,8 @@ const char* attn_varlen_strerror(int code) {
     case ATTN_ERR_TOO_LARGE: return "problem size beyond the supported range";
     case ATTN_ERR_ALLOC: return "backward scratch allocation failed";
     case ATTN_ERR_DEVICE_STATUS: return "a kernel recorded a device-side error";
+    case ATTN_ERR_NOALLOC_TOO_LARGE:
+      return "T * Hq exceeds the fixed scratch of attn_varlen_bwd_noalloc (2,097,152 floats)";
     default: return "unknown error code";
   }
 }
