@@ -233,7 +233,7 @@ def main():
              "cu": torch.from_numpy(cu).to(dev)}
         t["out"] = torch.empty_like(t["q"])
         t["lse"] = torch.empty(w.hq, w.total, dtype=torch.float32, device=dev)
-        t["delta"] = torch.empty(w.hq, w.total, dtype=torch.float32, device=dev)
+        t["ws"] = torch.empty(binding.attn_varlen_bwd_workspace_bytes(w.total, w.hq), dtype=torch.uint8, device=dev)
         t["dq"], t["dk"], t["dv"] = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
         return inp, t
 
@@ -247,14 +247,14 @@ def main():
         binding.attn_varlen_fwd(t["q"], t["k"], t["v"], t["cu"], ms, win, sc, t["out"], t["lse"])
         if evs:
             evs[1].record(stream)
-        binding.attn_varlen_bwd_preprocess(t["dout"], t["out"], t["delta"])
+        binding.attn_varlen_bwd_preprocess(t["dout"], t["out"], t["ws"])
         if evs:
             evs[2].record(stream)
-        binding.attn_varlen_bwd_dkdv(t["dout"], t["q"], t["k"], t["v"], t["lse"], t["delta"], t["cu"], ms, win, sc,
+        binding.attn_varlen_bwd_dkdv(t["dout"], t["q"], t["k"], t["v"], t["lse"], t["ws"], t["cu"], ms, win, sc,
                                      t["dk"], t["dv"])
         if evs:
             evs[3].record(stream)
-        binding.attn_varlen_bwd_dq(t["dout"], t["q"], t["k"], t["v"], t["lse"], t["delta"], t["cu"], ms, win, sc,
+        binding.attn_varlen_bwd_dq(t["dout"], t["q"], t["k"], t["v"], t["lse"], t["ws"], t["cu"], ms, win, sc,
                                    t["dq"])
         if evs:
             evs[4].record(stream)

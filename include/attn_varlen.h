@@ -33,9 +33,10 @@
  * Ownership and memory: every pointer except `stream` is caller-owned DEVICE
  * memory on the current CUDA device, 16-byte aligned.  The library keeps no
  * reference after the enqueued work completes.  Outputs are fully
- * overwritten.  The forward allocates nothing.  The backward takes a scratch
- * buffer of attn_varlen_bwd_workspace_bytes() bytes from the stream-ordered
- * allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * overwritten.  The forward allocates nothing.  attn_varlen_bwd takes a
+ * scratch buffer of attn_varlen_bwd_workspace_bytes() bytes from the
+ * stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`); the
+ * sub-step calls below take a caller-provided workspace instead.
  *
  * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
  * stream).  No call synchronises the host except attn_varlen_get_status();
@@ -73,6 +74,7 @@ extern "C" {
 #define ATTN_ERR_ALLOC (-11)         /* the backward scratch could not be allocated */
 #define ATTN_ERR_DEVICE_STATUS (-12) /* attn_varlen_get_status: a kernel reported an error */
 #define ATTN_ERR_NOALLOC_TOO_LARGE (-13) /* attn_varlen_bwd_noalloc: T * Hq above its fixed scratch (2,097,152) */
+#define ATTN_ERR_WORKSPACE (-14)     /* workspace below its minimum size or not 256-byte aligned */
 
 /*
  * Forward.  Writes out [T, Hq, 128] (bf16) and lse [Hq, T] (float32).
@@ -124,29 +126,68 @@ int attn_varlen_bwd_noalloc(const void* dout, const void* q, const void* k, cons
                             float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
                             int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream);
 
-/* Bytes of scratch the backward takes from the stream-ordered allocator. */
+/* Bytes of scratch the backward takes from the stream-ordered allocator:
+ * D (T * Hq floats, 256-byte padded) plus 40 MiB of chain buffers. */
 size_t attn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads_q);
 
 /*
  * The three kernels of attn_varlen_bwd as separate calls, for callers that
- * manage the scratch themselves or run the two passes on different streams.
- * `delta` is caller-owned device float32 [Hq, T] (16-byte aligned):
- *   attn_varlen_bwd_preprocess writes delta[h, i] = sum_c dout[i,h,c] * out[i,h,c];
- *   attn_varlen_bwd_dkdv reads it (with q, k, v, dout, lse) and writes dk, dv;
- *   attn_varlen_bwd_dq reads it and writes dq.
- * The two passes only read delta, so they may run concurrently once the
- * preprocess has completed.  Arguments mean what they mean in attn_varlen_bwd.
+ * manage the scratch themselves.  `workspace` is caller-owned device memory,
+ * 256-byte aligned, of `workspace_bytes` bytes; the same workspace goes to all
+ * three calls, in this order on one stream:
+ *   attn_varlen_bwd_preprocess writes D = rowsum(dout * out) (float32 [Hq, T],
+ *     at the start of the workspace) and resets the dK/dV pass's counters;
+ *   attn_varlen_bwd_dkdv reads D (with q, k, v, dout, lse) and writes dk, dv;
+ *   attn_varlen_bwd_dq reads D and writes dq.
+ * Minimum size: T * Hq * 4 bytes rounded up to 256.  With
+ * attn_varlen_bwd_workspace_bytes() bytes the dK/dV pass may split long
+ * key/value tiles into chunks that different CTAs reduce in a fixed order
+ * (better load balance, same bits); a smaller workspace splits less.
+ * Arguments otherwise mean what they mean in attn_varlen_bwd.
  */
-int attn_varlen_bwd_preprocess(const void* dout, const void* out, float* delta, int64_t total, int32_t num_heads_q,
-                               int32_t head_dim, void* stream);
+int attn_varlen_bwd_preprocess(const void* dout, const void* out, void* workspace, size_t workspace_bytes,
+                               int64_t total, int32_t num_heads_q, int32_t head_dim, void* stream);
 int attn_varlen_bwd_dkdv(const void* dout, const void* q, const void* k, const void* v, const float* lse,
-                         const float* delta, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
-                         float softmax_scale, void* dk, void* dv, int64_t total, int32_t num_heads_q,
-                         int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream);
+                         const void* workspace, size_t workspace_bytes, const int32_t* cu_seqlens, int32_t max_seqlen,
+                         int32_t window_left, float softmax_scale, void* dk, void* dv, int64_t total,
+                         int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t num_segments,
+                         void* stream);
 int attn_varlen_bwd_dq(const void* dout, const void* q, const void* k, const void* v, const float* lse,
-                       const float* delta, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
-                       float softmax_scale, void* dq, int64_t total, int32_t num_heads_q, int32_t num_heads_kv,
-                       int32_t head_dim, int32_t num_segments, void* stream);
+                       const void* workspace, size_t workspace_bytes, const int32_t* cu_seqlens, int32_t max_seqlen,
+                       int32_t window_left, float softmax_scale, void* dq, int64_t total, int32_t num_heads_q,
+                       int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream);
+
+/*
+ * The backward for callers that cannot allocate device memory.  (The page
+ * has no counterpart; this is a property of the library, not of the method.)
+ * Some callers may not call cudaMalloc or the stream-ordered allocator: code
+ * running under an allocator it does not own (a framework's caching
+ * allocator, a fixed pre-reserved memory budget), real-time or embedded
+ * callers for which a driver allocation may block or synchronise the device,
+ * or paths that must not allocate at all.  This call computes exactly what
+ * attn_varlen_bwd computes, with the same arguments, but keeps its scratch
+ * (D = rowsum(dout * out), float32 [Hq, T]) in a fixed device array compiled
+ * into the library instead of allocating it; it calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *   Limit: T * Hq <= 2,097,152 (8 MiB of scratch); larger problems return
+ *   ATTN_ERR_NOALLOC_TOO_LARGE before anything is enqueued.  Every GPU that
+ *   loads the library holds the array until the process exits.
+ *   Sharing: all calls on a device use the same array.  The previous call's
+ *   contents are irrelevant (every element read is written first in the same
+ *   call), but calls whose GPU work overlaps in time (different streams or
+ *   host threads) race on the array; the caller must order them.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (with that device current) and caches it; make that first call
+ *   before any stream capture.
+ */
+int attn_varlen_bwd_noalloc(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                            const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                            float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
+                            int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream);
+
+/* Bytes of scratch the backward takes from the stream-ordered allocator:
+ * D (T * Hq floats, 256-byte padded) plus 40 MiB of chain buffers. */
+size_t attn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads_q);
 
 /*
  * Synchronises `stream`, then returns ATTN_OK if no kernel of this library

@@ -68,9 +68,12 @@ def test_argument_validation(clib):
 
 
 def test_workspace_bytes(clib):
-    assert clib.attn_varlen_bwd_workspace_bytes(16384, 8) == 16384 * 8 * 4
+    clib.attn_varlen_bwd_workspace_bytes.restype = ctypes.c_size_t
+    clib.attn_varlen_bwd_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
+    chains = 2816 + 320 * 2 * 128 * 128 * 4
+    assert clib.attn_varlen_bwd_workspace_bytes(16384, 8) == 16384 * 8 * 4 + chains
     assert clib.attn_varlen_bwd_workspace_bytes(0, 8) == 0
-    assert clib.attn_varlen_bwd_workspace_bytes(3, 1) == 256
+    assert clib.attn_varlen_bwd_workspace_bytes(3, 1) == 256 + chains
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -45,11 +45,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.attn_varlen_get_status.restype = ctypes.c_int
     lib.attn_varlen_strerror.argtypes = [ctypes.c_int]
     lib.attn_varlen_strerror.restype = ctypes.c_char_p
-    lib.attn_varlen_bwd_preprocess.argtypes = [vp, vp, vp, i64, i32, i32, vp]
+    sz = ctypes.c_size_t
+    lib.attn_varlen_bwd_preprocess.argtypes = [vp, vp, vp, sz, i64, i32, i32, vp]
     lib.attn_varlen_bwd_preprocess.restype = ctypes.c_int
-    lib.attn_varlen_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp, i64, i32, i32, i32, i32, vp]
+    lib.attn_varlen_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, sz, vp, i32, i32, f32, vp, vp, i64, i32, i32, i32, i32,
+                                         vp]
     lib.attn_varlen_bwd_dkdv.restype = ctypes.c_int
-    lib.attn_varlen_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, vp, i64, i32, i32, i32, i32, vp]
+    lib.attn_varlen_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, sz, vp, i32, i32, f32, vp, i64, i32, i32, i32, i32, vp]
     lib.attn_varlen_bwd_dq.restype = ctypes.c_int
     lib.attn_varlen_bwd_noalloc.argtypes = lib.attn_varlen_bwd.argtypes
     lib.attn_varlen_bwd_noalloc.restype = ctypes.c_int
@@ -118,28 +120,35 @@ def attn_varlen_bwd_noalloc(dout, q, k, v, out, lse, cu_seqlens, max_seqlen: int
     _check(rc, "attn_varlen_bwd_noalloc")
 
 
-def attn_varlen_bwd_preprocess(dout, out, delta, stream=None) -> None:
-    """delta [Hq, T] fp32 = rowsum(dout * out)."""
+def _ws(workspace):
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+def attn_varlen_bwd_preprocess(dout, out, workspace, stream=None) -> None:
+    """D = rowsum(dout * out) into the workspace (a 256-byte-aligned uint8 CUDA tensor)."""
     lib = load_library()
     total, hq, d = dout.shape
-    _check(lib.attn_varlen_bwd_preprocess(_ptr(dout), _ptr(out), _ptr(delta), int(total), int(hq), int(d),
+    wp, wb = _ws(workspace)
+    _check(lib.attn_varlen_bwd_preprocess(_ptr(dout), _ptr(out), wp, wb, int(total), int(hq), int(d),
                                           _stream_handle(stream)), "attn_varlen_bwd_preprocess")
 
 
-def attn_varlen_bwd_dkdv(dout, q, k, v, lse, delta, cu_seqlens, max_seqlen: int, window_left: int,
+def attn_varlen_bwd_dkdv(dout, q, k, v, lse, workspace, cu_seqlens, max_seqlen: int, window_left: int,
                          softmax_scale: float, dk, dv, stream=None) -> None:
     lib = load_library()
     total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
-    _check(lib.attn_varlen_bwd_dkdv(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(cu_seqlens),
+    wp, wb = _ws(workspace)
+    _check(lib.attn_varlen_bwd_dkdv(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(lse), wp, wb, _ptr(cu_seqlens),
                                     int(max_seqlen), int(window_left), float(softmax_scale), _ptr(dk), _ptr(dv),
                                     total, hq, hkv, d, nseg, _stream_handle(stream)), "attn_varlen_bwd_dkdv")
 
 
-def attn_varlen_bwd_dq(dout, q, k, v, lse, delta, cu_seqlens, max_seqlen: int, window_left: int,
+def attn_varlen_bwd_dq(dout, q, k, v, lse, workspace, cu_seqlens, max_seqlen: int, window_left: int,
                        softmax_scale: float, dq, stream=None) -> None:
     lib = load_library()
     total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
-    _check(lib.attn_varlen_bwd_dq(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(cu_seqlens),
+    wp, wb = _ws(workspace)
+    _check(lib.attn_varlen_bwd_dq(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(lse), wp, wb, _ptr(cu_seqlens),
                                   int(max_seqlen), int(window_left), float(softmax_scale), _ptr(dq), total, hq, hkv,
                                   d, nseg, _stream_handle(stream)), "attn_varlen_bwd_dq")
 

@@ -91,6 +91,8 @@ int validate_common(const int32_t* cu_seqlens, int32_t max_seqlen, int32_t windo
   if (head_dim != 128) return ATTN_ERR_HEAD_DIM;
   // cu_seqlens is staged in shared memory by every kernel: at most 8191 segments.
   if (total > (int64_t(1) << 30) || hq > 1024 || nseg > kMaxSegments) return ATTN_ERR_TOO_LARGE;
+  // Work units (tiles x heads) are numbered with 32-bit integers on the device.
+  if (upper_bound_tiles(total, nseg) * hq > (int64_t(1) << 30)) return ATTN_ERR_TOO_LARGE;
   if (window_left < -1) return ATTN_ERR_WINDOW;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return ATTN_ERR_SCALE;
   if (max_seqlen < 0 || (total > 0 && max_seqlen > total)) return ATTN_ERR_MAX_SEQLEN;
@@ -152,8 +154,9 @@ int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* 
 
 size_t attn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads_q) {
   if (total <= 0 || num_heads_q <= 0) return 0;
-  // delta = rowsum(dout * out), fp32 [Hq, T], padded to 256 bytes.
-  return ((size_t)total * num_heads_q * sizeof(float) + 255) & ~(size_t)255;
+  // delta = rowsum(dout * out), fp32 [Hq, T] (256-byte padded), then the
+  // chain counters and buffers that let the dK/dV pass split long kv items.
+  return full_workspace_bytes(total, num_heads_q);
 }
 
 }  // extern "C"
@@ -169,7 +172,7 @@ struct BwdSetup {
 };
 
 int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, const void* v, const void* out,
-                const float* lse, const float* delta, const int32_t* cu_seqlens, int32_t max_seqlen,
+                const float* lse, const void* workspace, const int32_t* cu_seqlens, int32_t max_seqlen,
                 int32_t window_left, float softmax_scale, void* dq, void* dk, void* dv, int64_t total,
                 int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t num_segments) {
   int rc = validate_common(cu_seqlens, max_seqlen, window_left, softmax_scale, total, num_heads_q, num_heads_kv,
@@ -180,7 +183,7 @@ int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, con
     if (!x) return ATTN_ERR_NULL_POINTER;
   for (const void* x : ptrs)
     if (!aligned16(x)) return ATTN_ERR_ALIGNMENT;
-  const void* opt[] = {out, delta, dq, dk, dv};  // the callers pass the ones they need (checked there)
+  const void* opt[] = {out, workspace, dq, dk, dv};  // the callers pass the ones they need (checked there)
   for (const void* x : opt)
     if (x && !aligned16(x)) return ATTN_ERR_ALIGNMENT;
   if ((rc = current_device(&b.dev))) return rc;
@@ -193,7 +196,10 @@ int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, con
   b.p.dout = dout;
   b.p.out = out;
   b.p.lse = lse;
-  b.p.delta = const_cast<float*>(delta);
+  b.p.delta = nullptr;
+  b.p.chains = nullptr;
+  b.p.chain_progress = nullptr;
+  b.p.chains_max = 0;
   b.p.dq = dq;
   b.p.dk = dk;
   b.p.dv = dv;
@@ -215,9 +221,9 @@ int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* 
   if (rc || total == 0) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, attn_varlen_bwd_workspace_bytes(total, num_heads_q), s) != cudaSuccess)
-    return ATTN_ERR_ALLOC;
-  b.p.delta = static_cast<float*>(ws);
+  const size_t ws_bytes = attn_varlen_bwd_workspace_bytes(total, num_heads_q);
+  if (cudaMallocAsync(&ws, ws_bytes, s) != cudaSuccess) return ATTN_ERR_ALLOC;
+  carve_workspace(ws, ws_bytes, total, num_heads_q, b.p);
   int lr = launch_bwd_preprocess(b.p, s);
   if (!lr) lr = launch_bwd_dkdv(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, s);
   if (!lr) lr = launch_bwd_dq(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, s);
@@ -226,13 +232,14 @@ int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* 
   return ATTN_OK;
 }
 
-int attn_varlen_bwd_preprocess(const void* dout, const void* out, float* delta, int64_t total, int32_t num_heads_q,
-                               int32_t head_dim, void* stream) {
-  if (!dout || !out || !delta) return ATTN_ERR_NULL_POINTER;
+int attn_varlen_bwd_preprocess(const void* dout, const void* out, void* workspace, size_t workspace_bytes,
+                               int64_t total, int32_t num_heads_q, int32_t head_dim, void* stream) {
+  if (!dout || !out || !workspace) return ATTN_ERR_NULL_POINTER;
   if (total < 0 || num_heads_q <= 0) return ATTN_ERR_SHAPE;
   if (head_dim != 128) return ATTN_ERR_HEAD_DIM;
   if (total > (int64_t(1) << 30) || num_heads_q > 1024) return ATTN_ERR_TOO_LARGE;
-  if (!aligned16(dout) || !aligned16(out) || !aligned16(delta)) return ATTN_ERR_ALIGNMENT;
+  if (!aligned16(dout) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_ALIGNMENT;
   DeviceInfo* dev = nullptr;
   int rc = current_device(&dev);
   if (rc || total == 0) return rc;
@@ -241,33 +248,40 @@ int attn_varlen_bwd_preprocess(const void* dout, const void* out, float* delta, 
   p.a.hq = num_heads_q;
   p.dout = dout;
   p.out = out;
-  p.delta = delta;
+  if (!carve_workspace(workspace, workspace_bytes, total, num_heads_q, p)) return ATTN_ERR_WORKSPACE;
   return launch_bwd_preprocess(p, static_cast<cudaStream_t>(stream)) ? ATTN_ERR_CUDA : ATTN_OK;
 }
 
 int attn_varlen_bwd_dkdv(const void* dout, const void* q, const void* k, const void* v, const float* lse,
-                         const float* delta, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
-                         float softmax_scale, void* dk, void* dv, int64_t total, int32_t num_heads_q,
-                         int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream) {
-  if (!delta || !dk || !dv) return ATTN_ERR_NULL_POINTER;
+                         const void* workspace, size_t workspace_bytes, const int32_t* cu_seqlens, int32_t max_seqlen,
+                         int32_t window_left, float softmax_scale, void* dk, void* dv, int64_t total,
+                         int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t num_segments,
+                         void* stream) {
+  if (!workspace || !dk || !dv) return ATTN_ERR_NULL_POINTER;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGNMENT;
   BwdSetup b;
-  int rc = prepare_bwd(b, dout, q, k, v, nullptr, lse, delta, cu_seqlens, max_seqlen, window_left, softmax_scale,
+  int rc = prepare_bwd(b, dout, q, k, v, nullptr, lse, workspace, cu_seqlens, max_seqlen, window_left, softmax_scale,
                        nullptr, dk, dv, total, num_heads_q, num_heads_kv, head_dim, num_segments);
   if (rc || total == 0) return rc;
+  if (!carve_workspace(const_cast<void*>(workspace), workspace_bytes, total, num_heads_q, b.p))
+    return ATTN_ERR_WORKSPACE;
   return launch_bwd_dkdv(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, static_cast<cudaStream_t>(stream))
              ? ATTN_ERR_CUDA
              : ATTN_OK;
 }
 
 int attn_varlen_bwd_dq(const void* dout, const void* q, const void* k, const void* v, const float* lse,
-                       const float* delta, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
-                       float softmax_scale, void* dq, int64_t total, int32_t num_heads_q, int32_t num_heads_kv,
-                       int32_t head_dim, int32_t num_segments, void* stream) {
-  if (!delta || !dq) return ATTN_ERR_NULL_POINTER;
+                       const void* workspace, size_t workspace_bytes, const int32_t* cu_seqlens, int32_t max_seqlen,
+                       int32_t window_left, float softmax_scale, void* dq, int64_t total, int32_t num_heads_q,
+                       int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream) {
+  if (!workspace || !dq) return ATTN_ERR_NULL_POINTER;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGNMENT;
   BwdSetup b;
-  int rc = prepare_bwd(b, dout, q, k, v, nullptr, lse, delta, cu_seqlens, max_seqlen, window_left, softmax_scale,
+  int rc = prepare_bwd(b, dout, q, k, v, nullptr, lse, workspace, cu_seqlens, max_seqlen, window_left, softmax_scale,
                        dq, nullptr, nullptr, total, num_heads_q, num_heads_kv, head_dim, num_segments);
   if (rc || total == 0) return rc;
+  if (!carve_workspace(const_cast<void*>(workspace), workspace_bytes, total, num_heads_q, b.p))
+    return ATTN_ERR_WORKSPACE;
   return launch_bwd_dq(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, static_cast<cudaStream_t>(stream))
              ? ATTN_ERR_CUDA
              : ATTN_OK;
@@ -300,6 +314,7 @@ const char* attn_varlen_strerror(int code) {
     case ATTN_ERR_TOO_LARGE: return "problem size beyond the supported range";
     case ATTN_ERR_ALLOC: return "backward scratch allocation failed";
     case ATTN_ERR_DEVICE_STATUS: return "a kernel recorded a device-side error";
+    case ATTN_ERR_WORKSPACE: return "workspace smaller than delta (T * Hq floats) or not 256-byte aligned";
     case ATTN_ERR_NOALLOC_TOO_LARGE:
       return "T * Hq exceeds the fixed scratch of attn_varlen_bwd_noalloc (2,097,152 floats)";
     default: return "unknown error code";

@@ -21,8 +21,12 @@ constexpr int kPreRowsPerBlock = 64;
 
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __restrict__ dout,
                                                              const uint4* __restrict__ out,
-                                                             float* __restrict__ delta, int total, int hq) {
+                                                             float* __restrict__ delta, int total, int hq,
+                                                             int* __restrict__ chain_progress, int nprogress) {
   grid_dependency_wait();
+  // The dK/dV pass that follows counts published chain links from zero.
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e < nprogress; e += blockDim.x) chain_progress[e] = 0;
   const long long rows = (long long)total * hq;
   const int sub = threadIdx.x & 15;
   const int r_in = threadIdx.x >> 4;  // 0..15
@@ -139,7 +143,7 @@ int launch_bwd_preprocess(const BwdParams& p, cudaStream_t stream) {
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
   return (int)launch_pdl(bwd_preprocess_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
                          static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.out), p.delta, p.a.total,
-                         p.a.hq);
+                         p.a.hq, p.chain_progress, p.chain_progress ? 2 * p.chains_max : 0);
 }
 
 int launch_mask_probe(const int* cu_seqlens, int nseg, int total, int window, int max_levels, int by_key,

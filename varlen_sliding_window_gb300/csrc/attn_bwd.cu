@@ -16,16 +16,20 @@
 //   3. dQ pass: one CTA item = (segment, q tile, query head).  Q and dO stay
 //      in shared memory; K/V tiles stream through a ring.
 //
-// Both passes split the streamed 128-token tile into two 64-token halves.
-// Half x is owned by elementwise warpgroup x and has its own TMEM buffer
-// (64 columns of S plus 64 of dP), so the tensor cores compute one half's
-// S/dP while the other half's elementwise work runs:
-//     MMA:  S/dP(h0)  S/dP(h1)  [P(h0)] dV,dK(h0)  S/dP(next h0)  [P(h1)] dV,dK(h1) ...
-// P^T/dS^T (dK/dV pass) and dS (dQ pass) go back as bf16 into their own
-// buffer's columns and feed the next MMA as its A operand straight from TMEM.
-// tcgen05 MMAs issued by one thread execute in order, so an S/dP MMA that
-// overwrites a buffer always runs after the MMAs that read that buffer's bf16
-// operands.
+// TMEM holds the fp32 accumulators of the MMAs (128 lanes x 512 columns):
+//   dK/dV pass: S^T, dP^T (N = 128 queries), dV, dK.  The two elementwise
+//     warpgroups split each tile's 128 query columns; the dV/dK MMAs of a
+//     64-query half start as soon as that half's bf16 P^T/dS^T are back in
+//     TMEM.
+//   dQ pass: two S buffers, dP, dQ.  S of the next kv tile is computed while
+//     the elementwise warpgroups work on the current one, and dP is released
+//     as soon as it has been read into registers.
+// bf16 operands (P^T, dS^T, dS) go back over the first half of the fp32
+// columns they were computed from and feed the next MMA as its A operand
+// straight from TMEM.  tcgen05 MMAs issued by one thread execute in order, so
+// an MMA that overwrites such columns always runs after the MMAs that read
+// them.  Measured on GB300: a 128x64x16 MMA takes as long as a 128x128x16 one,
+// so every S/dP MMA here uses N = 128.
 #include <cuda_bf16.h>
 
 #include "attn_internal.h"
@@ -69,6 +73,30 @@ __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]
 // MMA, TMEM and scheduler warps (few registers), warpgroups 1 and 2 do the
 // elementwise work (launch 168 x 384 = 104 x 128 + 200 x 256 registers).
 constexpr int kBwdThreads = 384;
+constexpr int kBwdMaxItems = 96;  // work units one CTA may own
+
+// Spins (bounded) until *flag >= target, reading with acquire semantics at GPU
+// scope.  The flag is published by another CTA of the same grid that holds an
+// earlier unit of the global order, so it is resident and makes progress.
+__device__ __forceinline__ bool wait_flag_at_least(const int* flag, int target, volatile int* abort_flag,
+                                                   int* status) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v >= target) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > VSW_WAIT_TIMEOUT_NS) {
+      *abort_flag = 1;
+      if (status) atomicExch(status, kDevTimeout);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+__device__ __forceinline__ void store_release(int* flag, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
 
 // ============================================================== dK / dV pass
 struct DkvCfg {
@@ -78,8 +106,8 @@ struct DkvCfg {
   static constexpr uint32_t kQOff = 2 * kTileBytes;  // stage s: Q at kQOff + 2s tiles, dO right after
   static constexpr uint32_t kSmemBytes = (2 + 2 * kStages) * kTileBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // buffer x: S^T at 128x, dP^T at 128x + 64 (64 columns each); dV, dK after.
-  static constexpr uint32_t kColDV = 256, kColDK = 384;
+  // S^T, dP^T (128 columns each, fp32; bf16 P^T/dS^T over their halves), dV, dK.
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 };
 
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -89,12 +117,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using C = DkvCfg;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ WorkItem items[kMaxItemsPerCta];
-  __shared__ int item_counter, n_items;
+  __shared__ WorkItem items[kBwdMaxItems];
+  __shared__ int n_items;
   __shared__ __align__(8) uint64_t bar_kv_full, bar_kv_empty;
   __shared__ __align__(8) uint64_t bar_qdo_full[S], bar_qdo_empty[S];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2];
   __shared__ __align__(8) uint64_t bar_acc_full, bar_acc_empty;
+  __shared__ __align__(8) uint64_t bar_chain[2];
   __shared__ __align__(16) float s_lse[S][128];    // lse * log2(e) of the stage's 128 queries
   __shared__ __align__(16) float s_delta[S][128];  // D of the stage's 128 queries
   __shared__ uint32_t tmem_slot;
@@ -121,6 +150,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(smem_u32(&bar_acc_full), 1);
     mbar_init(smem_u32(&bar_acc_empty), 256);
+    mbar_init(smem_u32(&bar_chain[0]), 128);
+    mbar_init(smem_u32(&bar_chain[1]), 128);
     fence_mbar_init();
     tma_prefetch_map(&tmQ);
     tma_prefetch_map(&tmK);
@@ -136,8 +167,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int* cu = reinterpret_cast<int*>(gbase + C::kQOff);
     for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
     __syncwarp();
-    const int n = build_schedule(cu, a.nseg, a.max_levels, a.hkv, true, items, kMaxItemsPerCta, &item_counter,
-                                 blockIdx.x, gridDim.x);
+    const int n = build_schedule<true>(cu, a.nseg, a.window, a.max_levels, a.hkv, p.chains_max, items, kBwdMaxItems,
+                                       cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
     if (lane == 0) {
       n_items = n < 0 ? 0 : n;
       if (n < 0) atomicExch(a.status, 2);
@@ -159,9 +190,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     for (int it = 0; it < nit && ok; ++it) {
       const WorkItem w = items[it];
-      const int nb = num_tiles(w.seg_hi - w.seg_lo);
       const int k0 = w.seg_lo + w.blk * kTile;
-      const int bl = last_q_tile(w.blk, nb, a.window);
       const int g = w.unit;
       if (lane == 0) {
         if (it > 0) ok = mbar_wait(smem_u32(&bar_kv_empty), (it - 1) & 1, &abort_flag, a.status);
@@ -174,7 +203,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      for (int b = w.blk; b <= bl && ok; ++b) {
+      for (int b = w.t0; b <= w.t1 && ok; ++b) {
         const int q0 = w.seg_lo + b * kTile;
         for (int hh = 0; hh < a.group && ok; ++hh) {
           const int h = g * a.group + hh;
@@ -209,62 +238,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     regs_decrease<104>();
     if (lane == 0) {
-      constexpr uint32_t idesc_s = make_idesc_bf16(128, 64, 0, 0);    // S^T, dP^T: 128 keys x 64 queries
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, 0, 0);   // S^T, dP^T: 128 keys x 128 queries
       constexpr uint32_t idesc_g = make_idesc_bf16(128, 128, 0, 1);   // dV, dK: 128 keys x 128 dims
-      int cnt = 0;   // (q tile, head) pairs, for the Q/dO ring
-      int u = 0;     // half tiles, for the S/dP buffers
+      int cnt = 0;  // (q tile, head) pairs, for the Q/dO ring and the S/dP buffer
       bool ok = true;
-      // S^T_x = K Q_half^T and dP^T_x = V dO_half^T into buffer x = half.
-      auto issue_sdp = [&](int slot, int half) {
-        const uint32_t sq = sQ0 + slot * 2 * kTileBytes + half * kHalfRows, sdo = sq + kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 128 * half, kmajor_desc(sK, kk), kmajor_desc(sq, kk), idesc_s, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 128 * half + 64, kmajor_desc(sV, kk), kmajor_desc(sdo, kk), idesc_s, kk > 0);
-        tc_commit(smem_u32(&bar_s_full[half]));
-      };
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
-        const int nb = num_tiles(w.seg_hi - w.seg_lo);
-        const int bl = last_q_tile(w.blk, nb, a.window);
-        const int npairs = (bl - w.blk + 1) * a.group;
+        const int npairs = (w.t1 - w.t0 + 1) * a.group;
         if (!(ok = mbar_wait(smem_u32(&bar_kv_full), it & 1, &abort_flag, a.status))) break;
         tc_fence_after();
-        // First pair's Q/dO, then both halves' S/dP.
-        if (!(ok = mbar_wait(smem_u32(&bar_qdo_full[cnt % S]), (cnt / S) & 1, &abort_flag, a.status))) break;
-        tc_fence_after();
-        issue_sdp(cnt % S, 0);
-        issue_sdp(cnt % S, 1);
-        // The accumulators of the previous item must have been read out.
-        if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_acc_empty), (it - 1) & 1, &abort_flag, a.status))) break;
         for (int pr = 0; pr < npairs && ok; ++pr) {
           const int slot = cnt % S;
-          const bool more = pr + 1 < npairs;
-          if (more) {
-            const int ns = (cnt + 1) % S;
-            if (!(ok = mbar_wait(smem_u32(&bar_qdo_full[ns]), ((cnt + 1) / S) & 1, &abort_flag, a.status))) break;
-          }
+          if (!(ok = mbar_wait(smem_u32(&bar_qdo_full[slot]), (cnt / S) & 1, &abort_flag, a.status))) break;
+          tc_fence_after();
+          const uint32_t sq = sQ0 + slot * 2 * kTileBytes, sdo = sq + kTileBytes;
+          // S^T = K Q^T and dP^T = V dO^T (N = 128 queries).  They overwrite
+          // the previous pair's bf16 P^T/dS^T, which the dV/dK MMAs issued
+          // just before have read (in-order execution).
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::kColS, kmajor_desc(sK, kk), kmajor_desc(sq, kk), idesc_s, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::kColDP, kmajor_desc(sV, kk), kmajor_desc(sdo, kk), idesc_s, kk > 0);
+          tc_commit(smem_u32(&bar_s_full[0]));
+          // The accumulators of the previous item must have been read out.
+          if (pr == 0 && it > 0 &&
+              !(ok = mbar_wait(smem_u32(&bar_acc_empty), (it - 1) & 1, &abort_flag, a.status)))
+            break;
           for (int half = 0; half < 2 && ok; ++half) {
-            if (!(ok = mbar_wait(smem_u32(&bar_p_full[half]), (u >> 1) & 1, &abort_flag, a.status))) break;
+            if (!(ok = mbar_wait(smem_u32(&bar_p_full[half]), cnt & 1, &abort_flag, a.status))) break;
             tc_fence_after();
-            const uint32_t sq = sQ0 + slot * 2 * kTileBytes, sdo = sq + kTileBytes;
             const bool acc = pr > 0 || half > 0;
-            // dV += P^T dO_half (K = 64 queries), dK += dS^T Q_half.
+            // dV += P^T_half dO_half, dK += dS^T_half Q_half (K = 64 queries).
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + C::kColDV, tmem + 128 * half + kk * 8, mnmajor_desc(sdo, 4 * half + kk), idesc_g,
-                     (acc || kk > 0) ? 1u : 0u);
+              mma_ts(tmem + C::kColDV, tmem + C::kColS + 64 * half + kk * 8, mnmajor_desc(sdo, 4 * half + kk),
+                     idesc_g, (acc || kk > 0) ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + C::kColDK, tmem + 128 * half + 64 + kk * 8, mnmajor_desc(sq, 4 * half + kk), idesc_g,
-                     (acc || kk > 0) ? 1u : 0u);
-            if (half == 1) tc_commit(smem_u32(&bar_qdo_empty[slot]));
-            ++u;
-            // Refill this half's buffer with the next pair's S/dP.
-            if (more) issue_sdp((cnt + 1) % S, half);
+              mma_ts(tmem + C::kColDK, tmem + C::kColDP + 64 * half + kk * 8, mnmajor_desc(sq, 4 * half + kk),
+                     idesc_g, (acc || kk > 0) ? 1u : 0u);
           }
+          if (!ok) break;
+          tc_commit(smem_u32(&bar_qdo_empty[slot]));
           ++cnt;
         }
         if (!ok) break;
@@ -276,29 +293,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     regs_decrease<104>();
   } else {
     // ------------------------------------------------------------ elementwise
-    // Warpgroup x = half x of every streamed q tile; thread = key row.
+    // Warpgroup x = query columns [64x, 64x + 64) of every S^T/dP^T tile;
+    // thread = key row.  Its bf16 P^T and dS^T go over the first 32 of its
+    // own 64 columns.
     regs_increase<200>();
     const int x = (warp >> 2) - 1;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
-    const uint32_t tS = lane_base + 128 * x, tDP = tS + 64;
+    const uint32_t tS = lane_base + C::kColS + 64 * x, tDP = lane_base + C::kColDP + 64 * x;
     int cnt = 0;
+    uint32_t chain_uses = 0;
     bool ok = true;
     for (int it = 0; it < nit && ok; ++it) {
       const WorkItem w = items[it];
-      const int nb = num_tiles(w.seg_hi - w.seg_lo);
       const int k0 = w.seg_lo + w.blk * kTile;
-      const int bl = last_q_tile(w.blk, nb, a.window);
       const int g = w.unit;
       const int j = k0 + row;  // this thread's key token
-      for (int b = w.blk; b <= bl && ok; ++b) {
+      for (int b = w.t0; b <= w.t1 && ok; ++b) {
         const int q0 = w.seg_lo + b * kTile + 64 * x;  // first query of this half
         const bool full = tile_fully_visible_kv(k0, w.seg_lo + b * kTile, w.seg_hi, a.window);
         for (int hh = 0; hh < a.group; ++hh) {
           const int slot = cnt % S;
           if (!(ok = mbar_wait(smem_u32(&bar_qdo_full[slot]), (cnt / S) & 1, &abort_flag, a.status))) break;
-          if (!(ok = mbar_wait(smem_u32(&bar_s_full[x]), cnt & 1, &abort_flag, a.status))) break;
+          if (!(ok = mbar_wait(smem_u32(&bar_s_full[0]), cnt & 1, &abort_flag, a.status))) break;
           tc_fence_after();
           int c_lo = 0, c_hi = 63;
           if (!full) col_visible_rows(j, q0, w.seg_hi, a.window, c_lo, c_hi);
@@ -353,12 +371,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       void* dst_row = static_cast<__nv_bfloat16*>(x == 0 ? p.dv : p.dk) + ((size_t)j * a.hkv + g) * kHeadDim;
       const uint32_t tacc = lane_base + (x == 0 ? C::kColDV : C::kColDK);
       const float mul = x == 0 ? 1.f : a.scale;
+      if (w.chain < 0) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tacc + c * 32, r);
-        tmem_wait_ld(r);
-        if (valid) store_row32_bf16(dst_row, c * 32, r, mul);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tacc + c * 32, r);
+          tmem_wait_ld(r);
+          if (valid) store_row32_bf16(dst_row, c * 32, r, mul);
+        }
+      } else {
+        // A chunk of a split kv item: add the partial sums of the earlier
+        // chunks in chunk order (fp32, through the chain buffer), then
+        // either pass the running sum on or, as the last chunk, store it.
+        const int li = link_index(w), lk = link_count(w);
+        float* buf = p.chains + ((size_t)w.chain * 2 + x) * (128 * 128) + (size_t)row * 128;
+        int* prog = p.chain_progress + w.chain * 2 + x;
+        if (li > 0 && !(ok = wait_flag_at_least(prog, li, &abort_flag, a.status))) break;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tacc + c * 32, r);
+          tmem_wait_ld(r);
+          if (li > 0) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 prev = __ldcg(reinterpret_cast<const float4*>(buf + c * 32 + e));
+              r[e + 0] = __float_as_uint(__uint_as_float(r[e + 0]) + prev.x);
+              r[e + 1] = __float_as_uint(__uint_as_float(r[e + 1]) + prev.y);
+              r[e + 2] = __float_as_uint(__uint_as_float(r[e + 2]) + prev.z);
+              r[e + 3] = __float_as_uint(__uint_as_float(r[e + 3]) + prev.w);
+            }
+          }
+          if (li == lk - 1) {
+            if (valid) store_row32_bf16(dst_row, c * 32, r, mul);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              __stcg(reinterpret_cast<float4*>(buf + c * 32 + e),
+                     make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                                 __uint_as_float(r[e + 3])));
+          }
+        }
+        if (li < lk - 1) {
+          // Publish once every row of this warpgroup has written its part.
+          __threadfence();
+          mbar_arrive(smem_u32(&bar_chain[x]));
+          if (!(ok = mbar_wait(smem_u32(&bar_chain[x]), chain_uses & 1, &abort_flag, a.status))) break;
+          ++chain_uses;
+          if (row == 0) store_release(prog, li + 1);
+        }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_acc_empty));
@@ -381,8 +442,8 @@ struct DqCfg {
   static constexpr uint32_t kKVOff = 2 * kTileBytes;
   static constexpr uint32_t kSmemBytes = (2 + kStages) * kTileBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // buffer x: S at 128x, dP at 128x + 64 (64 columns each); dQ after.
-  static constexpr uint32_t kColDQ = 256;
+  // S buffers b = 0, 1 at 128b (fp32; bf16 dS over them), dP, dQ.
+  static constexpr uint32_t kColDP = 256, kColDQ = 384;
 };
 
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -392,11 +453,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using C = DqCfg;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ WorkItem items[kMaxItemsPerCta];
-  __shared__ int item_counter, n_items;
+  __shared__ WorkItem items[kBwdMaxItems];
+  __shared__ int n_items;
   __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty;
   __shared__ __align__(8) uint64_t bar_kv_full[S], bar_kv_empty[S];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2];
+  __shared__ __align__(8) uint64_t bar_dp_full, bar_dp_free;
   __shared__ __align__(8) uint64_t bar_acc_full, bar_acc_empty;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -420,6 +482,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&bar_s_full[x]), 1);
       mbar_init(smem_u32(&bar_p_full[x]), 128);
     }
+    mbar_init(smem_u32(&bar_dp_full), 1);
+    mbar_init(smem_u32(&bar_dp_free), 256);
     mbar_init(smem_u32(&bar_acc_full), 1);
     mbar_init(smem_u32(&bar_acc_empty), 256);
     fence_mbar_init();
@@ -437,8 +501,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int* cu = reinterpret_cast<int*>(gbase + C::kKVOff);
     for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
     __syncwarp();
-    const int n = build_schedule(cu, a.nseg, a.max_levels, a.hq, false, items, kMaxItemsPerCta, &item_counter,
-                                 blockIdx.x, gridDim.x);
+    const int n = build_schedule<false>(cu, a.nseg, a.window, a.max_levels, a.hq, 0, items, kBwdMaxItems,
+                                        cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
     if (lane == 0) {
       n_items = n < 0 ? 0 : n;
       if (n < 0) atomicExch(a.status, 2);
@@ -460,7 +524,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
         const int q0 = w.seg_lo + w.blk * kTile;
-        const int n0 = first_kv_tile(w.blk, a.window);
+        const int n0 = w.t0;
         const int h = w.unit, g = h / a.group;
         if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_q_empty), (it - 1) & 1, &abort_flag, a.status))) break;
         mbar_arrive_expect_tx(smem_u32(&bar_q_full), 2 * kTileBytes);
@@ -468,7 +532,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(sQ + kHalfTile, &tmQ, smem_u32(&bar_q_full), 64, h, q0);
         tma_load_3d(sDO, &tmDO, smem_u32(&bar_q_full), 0, h, q0);
         tma_load_3d(sDO + kHalfTile, &tmDO, smem_u32(&bar_q_full), 64, h, q0);
-        for (int n = n0; n <= w.blk && ok; ++n) {
+        for (int n = n0; n <= w.t1 && ok; ++n) {
           const int k0 = w.seg_lo + n * kTile;
           for (int kv = 0; kv < 2; ++kv) {
             const int slot = kv_cnt % S, use = kv_cnt / S;
@@ -486,63 +550,72 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per kv tile c (counted over all items): S(c) into buffer c & 1, dP(c)
+    // into the single dP buffer once dP(c-1) has been read, then dQ(c) half
+    // by half as the elementwise warpgroups finish.  S(c+1) is issued before
+    // dQ(c), so the next tile's QK^T overlaps this tile's elementwise work.
     regs_decrease<104>();
     if (lane == 0) {
-      constexpr uint32_t idesc_s = make_idesc_bf16(128, 64, 0, 0);    // S, dP: 128 queries x 64 keys
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, 0, 0);   // S, dP: 128 queries x 128 keys
       constexpr uint32_t idesc_g = make_idesc_bf16(128, 128, 0, 1);   // dQ: 128 queries x 128 dims
-      int kv_cnt = 0;  // K/V ring position (K and V take one slot each)
-      int u = 0;       // half tiles
+      int c = 0;  // kv tiles issued (S/dP), over all items
       bool ok = true;
-      // S_x = Q K_half^T, dP_x = dO V_half^T for the K/V pair at ring position kc.
-      auto issue_sdp = [&](int kc, int half) {
-        const uint32_t kt = sKV + (kc % S) * kTileBytes + half * kHalfRows;
-        const uint32_t vt = sKV + ((kc + 1) % S) * kTileBytes + half * kHalfRows;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 128 * half, kmajor_desc(sQ, kk), kmajor_desc(kt, kk), idesc_s, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 128 * half + 64, kmajor_desc(sDO, kk), kmajor_desc(vt, kk), idesc_s, kk > 0);
-        tc_commit(smem_u32(&bar_s_full[half]));
-      };
-      auto wait_kv_pair = [&](int kc) -> bool {
-        for (int e = 0; e < 2; ++e)
-          if (!mbar_wait(smem_u32(&bar_kv_full[(kc + e) % S]), ((kc + e) / S) & 1, &abort_flag, a.status))
-            return false;
+      auto wait_kv_pair = [&](int cc) -> bool {
+        for (int e = 0; e < 2; ++e) {
+          const int pos = 2 * cc + e;
+          if (!mbar_wait(smem_u32(&bar_kv_full[pos % S]), (pos / S) & 1, &abort_flag, a.status)) return false;
+        }
         tc_fence_after();
+        return true;
+      };
+      auto issue_s = [&](int cc) {
+        const uint32_t kt = sKV + ((2 * cc) % S) * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 128 * (cc & 1), kmajor_desc(sQ, kk), kmajor_desc(kt, kk), idesc_s, kk > 0);
+        tc_commit(smem_u32(&bar_s_full[cc & 1]));
+      };
+      auto issue_dp = [&](int cc) -> bool {
+        // dP(cc) overwrites dP(cc-1): wait until both warpgroups have read it.
+        if (cc > 0 && !mbar_wait(smem_u32(&bar_dp_free), (cc - 1) & 1, &abort_flag, a.status)) return false;
+        tc_fence_after();
+        const uint32_t vt = sKV + ((2 * cc + 1) % S) * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::kColDP, kmajor_desc(sDO, kk), kmajor_desc(vt, kk), idesc_s, kk > 0);
+        tc_commit(smem_u32(&bar_dp_full));
         return true;
       };
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
-        const int n0 = first_kv_tile(w.blk, a.window);
-        const int nt = w.blk - n0 + 1;
+        const int nt = w.t1 - w.t0 + 1;
         if (!(ok = mbar_wait(smem_u32(&bar_q_full), it & 1, &abort_flag, a.status))) break;
         tc_fence_after();
-        if (!(ok = wait_kv_pair(kv_cnt))) break;
-        issue_sdp(kv_cnt, 0);
-        issue_sdp(kv_cnt, 1);
-        if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_acc_empty), (it - 1) & 1, &abort_flag, a.status))) break;
-        for (int n = 0; n < nt && ok; ++n) {
-          const int kc = kv_cnt;
-          const bool more = n + 1 < nt;
-          if (more && !(ok = wait_kv_pair(kc + 2))) break;
+        if (!(ok = wait_kv_pair(c))) break;
+        issue_s(c);
+        if (!(ok = issue_dp(c))) break;
+        for (int n = 0; n < nt && ok; ++n, ++c) {
+          if (n + 1 < nt) {
+            if (!(ok = wait_kv_pair(c + 1))) break;
+            issue_s(c + 1);
+          }
+          if (n == 0 && it > 0 && !(ok = mbar_wait(smem_u32(&bar_acc_empty), (it - 1) & 1, &abort_flag, a.status)))
+            break;
+          const uint32_t kt = sKV + ((2 * c) % S) * kTileBytes;
           for (int half = 0; half < 2 && ok; ++half) {
-            if (!(ok = mbar_wait(smem_u32(&bar_p_full[half]), (u >> 1) & 1, &abort_flag, a.status))) break;
+            if (!(ok = mbar_wait(smem_u32(&bar_p_full[half]), c & 1, &abort_flag, a.status))) break;
             tc_fence_after();
-            const uint32_t kt = sKV + (kc % S) * kTileBytes;
-            // dQ += dS_half K_half (K = 64 keys).
+            // dQ += dS_half K_half: bf16 dS of keys [64 half, +64) over the
+            // first 32 columns of that half of S buffer c & 1.
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + C::kColDQ, tmem + 128 * half + kk * 8, mnmajor_desc(kt, 4 * half + kk), idesc_g,
-                     (n > 0 || half > 0 || kk > 0) ? 1u : 0u);
-            if (half == 1) {
-              tc_commit(smem_u32(&bar_kv_empty[kc % S]));
-              tc_commit(smem_u32(&bar_kv_empty[(kc + 1) % S]));
-            }
-            ++u;
-            if (more) issue_sdp(kc + 2, half);
+              mma_ts(tmem + C::kColDQ, tmem + 128 * (c & 1) + 64 * half + kk * 8, mnmajor_desc(kt, 4 * half + kk),
+                     idesc_g, (n > 0 || half > 0 || kk > 0) ? 1u : 0u);
           }
-          kv_cnt += 2;
+          if (!ok) break;
+          tc_commit(smem_u32(&bar_kv_empty[(2 * c) % S]));
+          tc_commit(smem_u32(&bar_kv_empty[(2 * c + 1) % S]));
+          if (n + 1 < nt && !(ok = issue_dp(c + 1))) break;
         }
         if (!ok) break;
         tc_commit(smem_u32(&bar_acc_full));
@@ -553,49 +626,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     regs_decrease<104>();
   } else {
     // ------------------------------------------------------------ elementwise
-    // Warpgroup x = half x (64 keys) of every streamed kv tile; thread = query row.
+    // Warpgroup x = keys [64x, 64x + 64) of every kv tile; thread = query row.
     regs_increase<200>();
     const int x = (warp >> 2) - 1;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
-    const uint32_t tS = lane_base + 128 * x, tDP = tS + 64;
-    int cnt = 0;
+    int c = 0;
     bool ok = true;
     for (int it = 0; it < nit && ok; ++it) {
       const WorkItem w = items[it];
       const int q0 = w.seg_lo + w.blk * kTile;
-      const int n0 = first_kv_tile(w.blk, a.window);
       const int h = w.unit;
       const int i = q0 + row;  // this thread's query token
       const bool valid = i < w.seg_hi && token_in_range(i, a.total);
       const float lse2 = valid ? p.lse[(size_t)h * a.total + i] * kLog2e : 0.f;
       const float dlt = valid ? p.delta[(size_t)h * a.total + i] : 0.f;
-      for (int n = n0; n <= w.blk; ++n) {
+      const uint64_t nl2 = f2_pack(-lse2, -lse2), nd2 = f2_pack(-dlt, -dlt);
+      const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+      for (int n = w.t0; n <= w.t1; ++n, ++c) {
         const int kt0 = w.seg_lo + n * kTile;
-        if (!(ok = mbar_wait(smem_u32(&bar_s_full[x]), cnt & 1, &abort_flag, a.status))) break;
+        const uint32_t tS = lane_base + 128 * (c & 1) + 64 * x;
+        const uint32_t tDP = lane_base + C::kColDP + 64 * x;
+        if (!(ok = mbar_wait(smem_u32(&bar_s_full[c & 1]), (c >> 1) & 1, &abort_flag, a.status))) break;
+        if (!(ok = mbar_wait(smem_u32(&bar_dp_full), c & 1, &abort_flag, a.status))) break;
         tc_fence_after();
-        int c_lo = 0, c_hi = 63;
-        if (!tile_fully_visible(q0, kt0, a.window)) row_visible_cols(i, kt0 + 64 * x, a.window, c_lo, c_hi);
-        uint32_t sr[64];
+        uint32_t sr[64], dr[64];
         tmem_ld64_wait(tS, sr);
-        float* pr = reinterpret_cast<float*>(sr);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float v = ex2_approx(fmaf(pr[c], a.scale_log2, -lse2));
-          pr[c] = (c >= c_lo && c <= c_hi) ? v : 0.f;
-        }
-        uint32_t dr[64];
         tmem_ld64_wait(tDP, dr);
+        // dP is in registers: let the next tile's dP MMA overwrite it.
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_dp_free));
+        int c_lo = 0, c_hi = 63;
+        const bool full = tile_fully_visible(q0, kt0, a.window);
+        if (!full) row_visible_cols(i, kt0 + 64 * x, a.window, c_lo, c_hi);
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2)
-          pk[c / 2] = pack_bf16x2(pr[c] * (__uint_as_float(dr[c]) - dlt), pr[c + 1] * (__uint_as_float(dr[c + 1]) - dlt));
+        for (int e = 0; e < 32; ++e) {
+          const int cc = 2 * e;
+          float p0, p1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), sc2, nl2), p0, p1);
+          p0 = ex2_approx(p0);
+          p1 = ex2_approx(p1);
+          if (!full) {
+            p0 = (cc >= c_lo && cc <= c_hi) ? p0 : 0.f;
+            p1 = (cc + 1 >= c_lo && cc + 1 <= c_hi) ? p1 : 0.f;
+          }
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(p0, p1),
+                           f2_add(f2_pack(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1])), nd2)),
+                    d0, d1);
+          pk[e] = pack_bf16x2(d0, d1);
+        }
         tmem_st32(tS, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_p_full[x]));
-        ++cnt;
       }
       if (!ok) break;
       // ---- epilogue: warpgroup x writes dQ columns [64x, 64x + 64) (x scale).
@@ -603,11 +689,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       void* dq_row = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)i * a.hq + h) * kHeadDim;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t r[32];
-        tmem_ld32(lane_base + C::kColDQ + 64 * x + c * 32, r);
+        tmem_ld32(lane_base + C::kColDQ + 64 * x + cc * 32, r);
         tmem_wait_ld(r);
-        if (valid) store_row32_bf16(dq_row, 64 * x + c * 32, r, a.scale);
+        if (valid) store_row32_bf16(dq_row, 64 * x + cc * 32, r, a.scale);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_acc_empty));
@@ -624,7 +710,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 long long persistent_grid(long long units, int num_sms) {
   long long grid = num_sms;
-  const long long need = (units + kMaxItemsPerCta - 1) / kMaxItemsPerCta;
+  const long long need = (units + kBwdMaxItems - 1) / kBwdMaxItems;
   if (need > grid) grid = need;
   if (units < grid) grid = units > 0 ? units : 1;
   return grid;
@@ -638,8 +724,12 @@ int launch_bwd_dkdv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtens
                                        (int)DkvCfg::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
   const long long g = persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hkv, num_sms);
+  // A chunk waits for the chunk before it in its chain, which belongs to
+  // another CTA; that is only safe while every CTA of the grid is resident.
+  BwdParams q = p;
+  if (g > num_sms) q.chains_max = 0;
   return (int)launch_pdl(attn_bwd_dkdv_kernel, dim3((unsigned)g), dim3(kBwdThreads), DkvCfg::kSmemBytes, stream, tmQ,
-                         tmK, tmV, tmDO, p);
+                         tmK, tmV, tmDO, q);
 }
 
 int launch_bwd_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,

@@ -41,6 +41,8 @@ namespace vsw {
 
 namespace {
 
+constexpr int kFwdMaxItems = 40;  // work units one CTA may own
+
 template <int NQT>
 struct FwdCfg {
   static constexpr int kQStages = 2;                   // Q tiles of consecutive work items
@@ -60,8 +62,7 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
   using C = FwdCfg<NQT>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ WorkItem items[kMaxItemsPerCta];
-  __shared__ int item_counter;
+  __shared__ WorkItem items[kFwdMaxItems];
   __shared__ int n_items;
   __shared__ __align__(8) uint64_t bar_q_full[2], bar_q_empty[2];
   __shared__ __align__(8) uint64_t bar_kv_full[S], bar_kv_empty[S];
@@ -106,8 +107,8 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
     int* cu = reinterpret_cast<int*>(gbase + C::kKVOff);
     for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
     __syncwarp();
-    const int n = build_schedule(cu, a.nseg, a.max_levels, a.hq / NQT, false, items, kMaxItemsPerCta,
-                                 &item_counter, blockIdx.x, gridDim.x);
+    const int n = build_schedule<false>(cu, a.nseg, a.window, a.max_levels, a.hq / NQT, 0, items, kFwdMaxItems,
+                                        cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
     if (lane == 0) {
       n_items = n < 0 ? 0 : n;
       if (n < 0) atomicExch(a.status, 2);
@@ -131,8 +132,8 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
         const int q_lo = w.seg_lo + w.blk * kTile;
-        const int n0 = first_kv_tile(w.blk, a.window);
-        const int nt = w.blk - n0 + 1;
+        const int n0 = w.t0;
+        const int nt = w.t1 - w.t0 + 1;
         const int qs = it & 1;
         if (it >= 2 && !(ok = mbar_wait(smem_u32(&bar_q_empty[qs]), ((it >> 1) - 1) & 1, &abort_flag, a.status)))
           break;
@@ -180,8 +181,8 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
       };
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
-        const int n0 = first_kv_tile(w.blk, a.window);
-        const int nt = w.blk - n0 + 1;
+        const int n0 = w.t0;
+        const int nt = w.t1 - w.t0 + 1;
         const int qs = it & 1;
         auto issue_qk = [&](int t, int slotK) {
           const uint32_t d = tmem + t * 128;
@@ -239,8 +240,8 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
     for (int it = 0; it < nit && ok; ++it) {
       const WorkItem w = items[it];
       const int q_lo = w.seg_lo + w.blk * kTile;
-      const int n0 = first_kv_tile(w.blk, a.window);
-      const int nt = w.blk - n0 + 1;
+      const int n0 = w.t0;
+      const int nt = w.t1 - w.t0 + 1;
       const int h = w.unit * NQT + t;
       const int i = q_lo + row;  // this thread's query token
       float m = -INFINITY, l = 0.f;
@@ -376,7 +377,7 @@ int launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorM
   if (e != cudaSuccess) return (int)e;
   const long long units = upper_bound_tiles(p.a.total, p.a.nseg) * (p.a.hq / NQT);
   long long grid = num_sms;
-  const long long need = (units + kMaxItemsPerCta - 1) / kMaxItemsPerCta;
+  const long long need = (units + kFwdMaxItems - 1) / kFwdMaxItems;
   if (need > grid) grid = need;
   if (units < grid) grid = units > 0 ? units : 1;
   return (int)launch_pdl(attn_fwd_kernel<NQT>, dim3((unsigned)grid), dim3(C::kThreads), C::kSmemBytes, stream, tmQ,

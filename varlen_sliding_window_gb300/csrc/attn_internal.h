@@ -38,7 +38,38 @@ struct BwdParams {
   void* dq;          // bf16 [T, hq, 128]
   void* dk;          // bf16 [T, hkv, 128]
   void* dv;          // bf16 [T, hkv, 128]
+  // dK/dV chains (split kv items reduced in order), scratch:
+  float* chains;         // fp32 [chains_max][2][128][128] partial dV, dK
+  int* chain_progress;   // int [chains_max][2], links published so far
+  int chains_max;        // 0 disables splitting
 };
+
+// Backward workspace layout: delta, chain progress counters, chain buffers.
+constexpr int kMaxChains = 320;
+constexpr size_t kChainBytes = 2ull * 128 * 128 * sizeof(float);
+constexpr size_t kProgressBytes = 2816;  // >= kMaxChains * 2 * 4, rounded to 256
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline size_t delta_bytes(long long total, int hq) { return align256((size_t)total * hq * sizeof(float)); }
+inline size_t full_workspace_bytes(long long total, int hq) {
+  return delta_bytes(total, hq) + kProgressBytes + kMaxChains * kChainBytes;
+}
+// Carves a caller-provided workspace; returns false if it cannot hold delta.
+inline bool carve_workspace(void* ws, size_t bytes, long long total, int hq, BwdParams& p) {
+  const size_t db = delta_bytes(total, hq);
+  if (!ws || bytes < db) return false;
+  char* base = static_cast<char*>(ws);
+  p.delta = reinterpret_cast<float*>(base);
+  p.chains_max = 0;
+  p.chain_progress = nullptr;
+  p.chains = nullptr;
+  if (bytes >= db + kProgressBytes + kChainBytes) {
+    size_t n = (bytes - db - kProgressBytes) / kChainBytes;
+    p.chains_max = (int)(n < (size_t)kMaxChains ? n : (size_t)kMaxChains);
+    p.chain_progress = reinterpret_cast<int*>(base + db);
+    p.chains = reinterpret_cast<float*>(base + db + kProgressBytes);
+  }
+  return true;
+}
 
 // Launchers (return a cudaError_t value).
 int launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,

@@ -10,12 +10,13 @@
 // array instead.  It calls no cudaMalloc, cudaFree or allocating library
 // routine.
 //
-// The array holds at most kNoAllocMaxDelta floats (T * Hq <= 2,097,152, 8 MiB);
-// every GPU that loads the library keeps it until the process exits.  All
+// The array is kNoAllocMaxDelta floats (8 MiB; T * Hq <= 2,097,152); every
+// GPU that loads the library keeps it until the process exits.  It holds D
+// first; the rest, if any, serves as the dK/dV pass's chain buffers.  All
 // calls on a device share it and it keeps the previous call's contents: the
-// preprocess overwrites every element the passes read, so nothing needs to
-// start at zero, but calls whose GPU work overlaps (two streams, or two host
-// threads) race on it and must be serialised by the caller.
+// preprocess overwrites every element of D and resets the chain counters, so
+// nothing needs to start at zero, but calls whose GPU work overlaps (two
+// streams, or two host threads) race on it and must be serialised.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -76,11 +77,13 @@ extern "C" int attn_varlen_bwd_noalloc(const void* dout, const void* q, const vo
   int rc = noalloc_scratch(&delta);
   if (rc) return rc;
   // The same three kernels as attn_varlen_bwd, with the fixed scratch.
-  rc = attn_varlen_bwd_preprocess(dout, out, delta, total, num_heads_q, head_dim, stream);
+  // What the array holds beyond D lets the dK/dV pass split long kv tiles.
+  const size_t bytes = sizeof(float) * (size_t)kNoAllocMaxDelta;
+  rc = attn_varlen_bwd_preprocess(dout, out, delta, bytes, total, num_heads_q, head_dim, stream);
   if (rc) return rc;
-  rc = attn_varlen_bwd_dkdv(dout, q, k, v, lse, delta, cu_seqlens, max_seqlen, window_left, softmax_scale, dk, dv,
+  rc = attn_varlen_bwd_dkdv(dout, q, k, v, lse, delta, bytes, cu_seqlens, max_seqlen, window_left, softmax_scale, dk,
+                            dv, total, num_heads_q, num_heads_kv, head_dim, num_segments, stream);
+  if (rc) return rc;
+  return attn_varlen_bwd_dq(dout, q, k, v, lse, delta, bytes, cu_seqlens, max_seqlen, window_left, softmax_scale, dq,
                             total, num_heads_q, num_heads_kv, head_dim, num_segments, stream);
-  if (rc) return rc;
-  return attn_varlen_bwd_dq(dout, q, k, v, lse, delta, cu_seqlens, max_seqlen, window_left, softmax_scale, dq, total,
-                            num_heads_q, num_heads_kv, head_dim, num_segments, stream);
 }
