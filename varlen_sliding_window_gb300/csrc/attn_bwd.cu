@@ -322,41 +322,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!full) col_visible_rows(j, q0, w.seg_hi, a.window, c_lo, c_hi);
           const float* lse2 = &s_lse[slot][64 * x];
           const float* dlt = &s_delta[slot][64 * x];
-          uint32_t sr[64];
+          uint32_t sr[64], dr[64];
           tmem_ld64_wait(tS, sr);
-          float* pr = reinterpret_cast<float*>(sr);
+          tmem_ld64_wait(tDP, dr);
+          const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+          uint32_t pp[32], pd[32];
 #pragma unroll
           for (int c = 0; c < 64; c += 4) {
+            // Pairs of query columns: P = exp2(s*scale*log2e - lse*log2e),
+            // dS = P (dP - D); staged lse/D are broadcast reads.
             const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float4 d4 = *reinterpret_cast<const float4*>(dlt + c);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float v = ex2_approx(fmaf(pr[c + e], a.scale_log2, -lv[e]));
-              pr[c + e] = (c + e >= c_lo && c + e <= c_hi) ? v : 0.f;
+            for (int hp = 0; hp < 2; ++hp) {
+              const int cc = c + 2 * hp;
+              const uint64_t nl = hp ? f2_pack(-l4.z, -l4.w) : f2_pack(-l4.x, -l4.y);
+              const uint64_t nd = hp ? f2_pack(-d4.z, -d4.w) : f2_pack(-d4.x, -d4.y);
+              float p0, p1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), sc2, nl), p0, p1);
+              p0 = ex2_approx(p0);
+              p1 = ex2_approx(p1);
+              if (!full) {
+                p0 = (cc >= c_lo && cc <= c_hi) ? p0 : 0.f;
+                p1 = (cc + 1 >= c_lo && cc + 1 <= c_hi) ? p1 : 0.f;
+              }
+              float d0, d1;
+              f2_unpack(f2_mul(f2_pack(p0, p1),
+                               f2_add(f2_pack(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1])), nd)),
+                        d0, d1);
+              pp[cc / 2] = pack_bf16x2(p0, p1);
+              pd[cc / 2] = pack_bf16x2(d0, d1);
             }
           }
-          {
-            uint32_t pk[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
-            tmem_st32(tS, pk);
-          }
-          uint32_t dr[64];
-          tmem_ld64_wait(tDP, dr);
-          {
-            uint32_t pk[32];
-#pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-              const float4 d4 = *reinterpret_cast<const float4*>(dlt + c);
-              const float d0 = pr[c + 0] * (__uint_as_float(dr[c + 0]) - d4.x);
-              const float d1 = pr[c + 1] * (__uint_as_float(dr[c + 1]) - d4.y);
-              const float d2 = pr[c + 2] * (__uint_as_float(dr[c + 2]) - d4.z);
-              const float d3 = pr[c + 3] * (__uint_as_float(dr[c + 3]) - d4.w);
-              pk[c / 2] = pack_bf16x2(d0, d1);
-              pk[c / 2 + 1] = pack_bf16x2(d2, d3);
-            }
-            tmem_st32(tDP, pk);
-          }
+          tmem_st32(tS, pp);
+          tmem_st32(tDP, pd);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(smem_u32(&bar_p_full[x]));
@@ -552,8 +551,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // Per kv tile c (counted over all items): S(c) into buffer c & 1, dP(c)
     // into the single dP buffer once dP(c-1) has been read, then dQ(c) half
-    // by half as the elementwise warpgroups finish.  S(c+1) is issued before
-    // dQ(c), so the next tile's QK^T overlaps this tile's elementwise work.
+    // by half as the elementwise warpgroups finish.  S(c+1) and dP(c+1) are
+    // issued before dQ(c), so they overlap this tile's elementwise work.
     regs_decrease<104>();
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, 0, 0);   // S, dP: 128 queries x 128 keys
@@ -596,8 +595,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = issue_dp(c))) break;
         for (int n = 0; n < nt && ok; ++n, ++c) {
           if (n + 1 < nt) {
+            // Next tile's S, and its dP as soon as this tile's dP has been
+            // read, so both are ready when the elementwise work moves on.
             if (!(ok = wait_kv_pair(c + 1))) break;
             issue_s(c + 1);
+            if (!(ok = issue_dp(c + 1))) break;
           }
           if (n == 0 && it > 0 && !(ok = mbar_wait(smem_u32(&bar_acc_empty), (it - 1) & 1, &abort_flag, a.status)))
             break;
@@ -615,7 +617,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!ok) break;
           tc_commit(smem_u32(&bar_kv_empty[(2 * c) % S]));
           tc_commit(smem_u32(&bar_kv_empty[(2 * c + 1) % S]));
-          if (n + 1 < nt && !(ok = issue_dp(c + 1))) break;
         }
         if (!ok) break;
         tc_commit(smem_u32(&bar_acc_full));
