@@ -435,47 +435,79 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // ============================================================== dQ pass
 struct DqCfg {
-  static constexpr int kStages = 4;  // K/V tile slots
+  static constexpr int kKStages = 3;  // K tiles: held from S(c) until dQ(c)
+  static constexpr int kVStages = 2;  // V tiles: held only until dP(c)
+  static constexpr int kMaxItems = 64;
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kDOOff = kTileBytes;
-  static constexpr uint32_t kKVOff = 2 * kTileBytes;
-  static constexpr uint32_t kSmemBytes = (2 + kStages) * kTileBytes + 1024;
+  static constexpr uint32_t kKOff = 2 * kTileBytes;
+  static constexpr uint32_t kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr uint32_t kStateOff = kVOff + kVStages * kTileBytes;  // 224 KB of tiles, then the state below
   static constexpr uint32_t kTmemCols = 512;
   // S buffers b = 0, 1 at 128b (fp32; bf16 dS over them), dP, dQ.
   static constexpr uint32_t kColDP = 256, kColDQ = 384;
 };
+
+// Everything else the dQ kernel keeps in shared memory, carved from the
+// dynamic allocation after the tiles (the tiles need all but ~3 KB of it, so
+// nothing is declared statically and no alignment slack is spent).
+struct DqState {
+  WorkItem items[DqCfg::kMaxItems];
+  uint64_t q_full, q_empty;
+  uint64_t k_full[DqCfg::kKStages], k_empty[DqCfg::kKStages];
+  uint64_t v_full[DqCfg::kVStages], v_empty[DqCfg::kVStages];
+  uint64_t s_full[2], p_full[2];
+  uint64_t dp_full, dp_free, acc_full, acc_empty;
+  int n_items;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+constexpr uint32_t kDqSmemBytes = DqCfg::kStateOff + sizeof(DqState);
 
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwdParams p) {
   using C = DqCfg;
-  constexpr int S = C::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ WorkItem items[kBwdMaxItems];
-  __shared__ int n_items;
-  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty;
-  __shared__ __align__(8) uint64_t bar_kv_full[S], bar_kv_empty[S];
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2];
-  __shared__ __align__(8) uint64_t bar_dp_full, bar_dp_free;
-  __shared__ __align__(8) uint64_t bar_acc_full, bar_acc_empty;
-  __shared__ uint32_t tmem_slot;
-  __shared__ int abort_flag;
-
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sbase = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (sbase - raw);
-  const uint32_t sQ = sbase + C::kQOff, sDO = sbase + C::kDOOff, sKV = sbase + C::kKVOff;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const AttnParams& a = p.a;
+  const uint32_t sbase = smem_u32(smem_raw);
+  // The swizzled tiles need a 1024-byte-aligned base; there is no static
+  // shared memory in this kernel, so the dynamic allocation starts aligned.
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicExch(a.status, 3);
+    return;
+  }
+  uint8_t* gbase = smem_raw;
+  DqState& st = *reinterpret_cast<DqState*>(smem_raw + C::kStateOff);
+  WorkItem* items = st.items;
+  const uint32_t sQ = sbase + C::kQOff, sDO = sbase + C::kDOOff, sK = sbase + C::kKOff, sV = sbase + C::kVOff;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_ptr = &st.abort_flag;
+#define abort_flag (*abort_ptr)
+#define bar_q_full st.q_full
+#define bar_q_empty st.q_empty
+#define bar_s_full st.s_full
+#define bar_p_full st.p_full
+#define bar_dp_full st.dp_full
+#define bar_dp_free st.dp_free
+#define bar_acc_full st.acc_full
+#define bar_acc_empty st.acc_empty
+#define tmem_slot st.tmem_slot
+#define n_items st.n_items
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_q_full), 1);
     mbar_init(smem_u32(&bar_q_empty), 1);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&bar_kv_full[s]), 1);
-      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(smem_u32(&st.k_full[s]), 1);
+      mbar_init(smem_u32(&st.k_empty[s]), 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(smem_u32(&st.v_full[s]), 1);
+      mbar_init(smem_u32(&st.v_empty[s]), 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&bar_s_full[x]), 1);
@@ -497,10 +529,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   if (warp == 3) {
     grid_dependency_wait();
-    int* cu = reinterpret_cast<int*>(gbase + C::kKVOff);
+    int* cu = reinterpret_cast<int*>(gbase + C::kKOff);
     for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
     __syncwarp();
-    const int n = build_schedule<false>(cu, a.nseg, a.window, a.max_levels, a.hq, 0, items, kBwdMaxItems,
+    const int n = build_schedule<false>(cu, a.nseg, a.window, a.max_levels, a.hq, 0, items, C::kMaxItems,
                                         cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
     if (lane == 0) {
       n_items = n < 0 ? 0 : n;
@@ -518,7 +550,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ producer
     regs_decrease<104>();
     if (lane == 0) {
-      int kv_cnt = 0;
+      int kc = 0, vc = 0;  // K and V tiles loaded so far
       bool ok = true;
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
@@ -533,16 +565,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(sDO + kHalfTile, &tmDO, smem_u32(&bar_q_full), 64, h, q0);
         for (int n = n0; n <= w.t1 && ok; ++n) {
           const int k0 = w.seg_lo + n * kTile;
-          for (int kv = 0; kv < 2; ++kv) {
-            const int slot = kv_cnt % S, use = kv_cnt / S;
-            if (use > 0 && !(ok = mbar_wait(smem_u32(&bar_kv_empty[slot]), (use - 1) & 1, &abort_flag, a.status)))
+          {
+            const int slot = kc % C::kKStages, use = kc / C::kKStages;
+            if (use > 0 && !(ok = mbar_wait(smem_u32(&st.k_empty[slot]), (use - 1) & 1, &abort_flag, a.status)))
               break;
-            const uint32_t bar = smem_u32(&bar_kv_full[slot]);
+            const uint32_t bar = smem_u32(&st.k_full[slot]);
             mbar_arrive_expect_tx(bar, kTileBytes);
-            const CUtensorMap* m = kv ? &tmV : &tmK;
-            tma_load_3d(sKV + slot * kTileBytes, m, bar, 0, g, k0);
-            tma_load_3d(sKV + slot * kTileBytes + kHalfTile, m, bar, 64, g, k0);
-            ++kv_cnt;
+            tma_load_3d(sK + slot * kTileBytes, &tmK, bar, 0, g, k0);
+            tma_load_3d(sK + slot * kTileBytes + kHalfTile, &tmK, bar, 64, g, k0);
+            ++kc;
+          }
+          {
+            const int slot = vc % C::kVStages, use = vc / C::kVStages;
+            if (use > 0 && !(ok = mbar_wait(smem_u32(&st.v_empty[slot]), (use - 1) & 1, &abort_flag, a.status)))
+              break;
+            const uint32_t bar = smem_u32(&st.v_full[slot]);
+            mbar_arrive_expect_tx(bar, kTileBytes);
+            tma_load_3d(sV + slot * kTileBytes, &tmV, bar, 0, g, k0);
+            tma_load_3d(sV + slot * kTileBytes + kHalfTile, &tmV, bar, 64, g, k0);
+            ++vc;
           }
         }
       }
@@ -559,16 +600,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idesc_g = make_idesc_bf16(128, 128, 0, 1);   // dQ: 128 queries x 128 dims
       int c = 0;  // kv tiles issued (S/dP), over all items
       bool ok = true;
-      auto wait_kv_pair = [&](int cc) -> bool {
-        for (int e = 0; e < 2; ++e) {
-          const int pos = 2 * cc + e;
-          if (!mbar_wait(smem_u32(&bar_kv_full[pos % S]), (pos / S) & 1, &abort_flag, a.status)) return false;
-        }
+      // K(cc) lives in K slot cc % 3, V(cc) in V slot cc % 2.
+      auto wait_k = [&](int cc) -> bool {
+        if (!mbar_wait(smem_u32(&st.k_full[cc % C::kKStages]), (cc / C::kKStages) & 1, &abort_flag, a.status))
+          return false;
         tc_fence_after();
         return true;
       };
       auto issue_s = [&](int cc) {
-        const uint32_t kt = sKV + ((2 * cc) % S) * kTileBytes;
+        const uint32_t kt = sK + (cc % C::kKStages) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + 128 * (cc & 1), kmajor_desc(sQ, kk), kmajor_desc(kt, kk), idesc_s, kk > 0);
@@ -577,12 +617,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto issue_dp = [&](int cc) -> bool {
         // dP(cc) overwrites dP(cc-1): wait until both warpgroups have read it.
         if (cc > 0 && !mbar_wait(smem_u32(&bar_dp_free), (cc - 1) & 1, &abort_flag, a.status)) return false;
+        if (!mbar_wait(smem_u32(&st.v_full[cc % C::kVStages]), (cc / C::kVStages) & 1, &abort_flag, a.status))
+          return false;
         tc_fence_after();
-        const uint32_t vt = sKV + ((2 * cc + 1) % S) * kTileBytes;
+        const uint32_t vt = sV + (cc % C::kVStages) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + C::kColDP, kmajor_desc(sDO, kk), kmajor_desc(vt, kk), idesc_s, kk > 0);
         tc_commit(smem_u32(&bar_dp_full));
+        tc_commit(smem_u32(&st.v_empty[cc % C::kVStages]));  // V(cc) is free once dP(cc) is done
         return true;
       };
       for (int it = 0; it < nit && ok; ++it) {
@@ -590,20 +633,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int nt = w.t1 - w.t0 + 1;
         if (!(ok = mbar_wait(smem_u32(&bar_q_full), it & 1, &abort_flag, a.status))) break;
         tc_fence_after();
-        if (!(ok = wait_kv_pair(c))) break;
+        if (!(ok = wait_k(c))) break;
         issue_s(c);
         if (!(ok = issue_dp(c))) break;
         for (int n = 0; n < nt && ok; ++n, ++c) {
           if (n + 1 < nt) {
             // Next tile's S, and its dP as soon as this tile's dP has been
             // read, so both are ready when the elementwise work moves on.
-            if (!(ok = wait_kv_pair(c + 1))) break;
+            if (!(ok = wait_k(c + 1))) break;
             issue_s(c + 1);
             if (!(ok = issue_dp(c + 1))) break;
           }
           if (n == 0 && it > 0 && !(ok = mbar_wait(smem_u32(&bar_acc_empty), (it - 1) & 1, &abort_flag, a.status)))
             break;
-          const uint32_t kt = sKV + ((2 * c) % S) * kTileBytes;
+          const uint32_t kt = sK + (c % C::kKStages) * kTileBytes;
           for (int half = 0; half < 2 && ok; ++half) {
             if (!(ok = mbar_wait(smem_u32(&bar_p_full[half]), c & 1, &abort_flag, a.status))) break;
             tc_fence_after();
@@ -615,8 +658,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      idesc_g, (n > 0 || half > 0 || kk > 0) ? 1u : 0u);
           }
           if (!ok) break;
-          tc_commit(smem_u32(&bar_kv_empty[(2 * c) % S]));
-          tc_commit(smem_u32(&bar_kv_empty[(2 * c + 1) % S]));
+          tc_commit(smem_u32(&st.k_empty[c % C::kKStages]));
         }
         if (!ok) break;
         tc_commit(smem_u32(&bar_acc_full));
@@ -709,9 +751,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-long long persistent_grid(long long units, int num_sms) {
+#undef abort_flag
+#undef bar_q_full
+#undef bar_q_empty
+#undef bar_s_full
+#undef bar_p_full
+#undef bar_dp_full
+#undef bar_dp_free
+#undef bar_acc_full
+#undef bar_acc_empty
+#undef tmem_slot
+#undef n_items
+
+long long persistent_grid(long long units, int num_sms, int max_items) {
   long long grid = num_sms;
-  const long long need = (units + kBwdMaxItems - 1) / kBwdMaxItems;
+  const long long need = (units + max_items - 1) / max_items;
   if (need > grid) grid = need;
   if (units < grid) grid = units > 0 ? units : 1;
   return grid;
@@ -724,7 +778,7 @@ int launch_bwd_dkdv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtens
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)DkvCfg::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
-  const long long g = persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hkv, num_sms);
+  const long long g = persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hkv, num_sms, kBwdMaxItems);
   // A chunk waits for the chunk before it in its chain, which belongs to
   // another CTA; that is only safe while every CTA of the grid is resident.
   BwdParams q = p;
@@ -736,10 +790,10 @@ int launch_bwd_dkdv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtens
 int launch_bwd_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,
                   const BwdParams& p, int num_sms, cudaStream_t stream) {
   cudaError_t e =
-      cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DqCfg::kSmemBytes);
+      cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmemBytes);
   if (e != cudaSuccess) return (int)e;
-  const long long g = persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hq, num_sms);
-  return (int)launch_pdl(attn_bwd_dq_kernel, dim3((unsigned)g), dim3(kBwdThreads), DqCfg::kSmemBytes, stream, tmQ,
+  const long long g = persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hq, num_sms, DqCfg::kMaxItems);
+  return (int)launch_pdl(attn_bwd_dq_kernel, dim3((unsigned)g), dim3(kBwdThreads), kDqSmemBytes, stream, tmQ,
                          tmK, tmV, tmDO, p);
 }
 
