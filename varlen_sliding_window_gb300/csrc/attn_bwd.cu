@@ -456,7 +456,7 @@ struct DqState {
   uint64_t q_full, q_empty;
   uint64_t k_full[DqCfg::kKStages], k_empty[DqCfg::kKStages];
   uint64_t v_full[DqCfg::kVStages], v_empty[DqCfg::kVStages];
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full[2], p_full[2][2];  // p_full[buffer][half]
   uint64_t dp_full, dp_free, acc_full, acc_empty;
   int n_items;
   uint32_t tmem_slot;
@@ -509,9 +509,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&st.v_full[s]), 1);
       mbar_init(smem_u32(&st.v_empty[s]), 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(smem_u32(&bar_s_full[x]), 1);
-      mbar_init(smem_u32(&bar_p_full[x]), 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bar_s_full[b]), 1);
+      mbar_init(smem_u32(&bar_p_full[b][0]), 128);
+      mbar_init(smem_u32(&bar_p_full[b][1]), 128);
     }
     mbar_init(smem_u32(&bar_dp_full), 1);
     mbar_init(smem_u32(&bar_dp_free), 256);
@@ -648,7 +649,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             break;
           const uint32_t kt = sK + (c % C::kKStages) * kTileBytes;
           for (int half = 0; half < 2 && ok; ++half) {
-            if (!(ok = mbar_wait(smem_u32(&bar_p_full[half]), c & 1, &abort_flag, a.status))) break;
+            if (!(ok = mbar_wait(smem_u32(&bar_p_full[c & 1][half]), (c >> 1) & 1, &abort_flag, a.status))) break;
             tc_fence_after();
             // dQ += dS_half K_half: bf16 dS of keys [64 half, +64) over the
             // first 32 columns of that half of S buffer c & 1.
@@ -724,7 +725,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_st32(tS, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&bar_p_full[x]));
+        // One barrier per S buffer: a warp that has finished this tile may run
+        // on to the next one (its S and dP are issued before this tile's dQ)
+        // and arrive again before the slowest warp of its warpgroup arrives
+        // here; with a single barrier that early arrival would complete this
+        // tile's phase too soon.
+        mbar_arrive(smem_u32(&bar_p_full[c & 1][x]));
       }
       if (!ok) break;
       // ---- epilogue: warpgroup x writes dQ columns [64x, 64x + 64) (x scale).
