@@ -259,13 +259,23 @@ def main():
         if evs:
             evs[4].record(stream)
 
+    def step_api(w, t):
+        """One step as a user makes it: the forward call, then the backward call."""
+        ms, win, sc = w.context, w.window_left, w.softmax_scale
+        binding.attn_varlen_fwd(t["q"], t["k"], t["v"], t["cu"], ms, win, sc, t["out"], t["lse"])
+        binding.attn_varlen_bwd(t["dout"], t["q"], t["k"], t["v"], t["out"], t["lse"], t["cu"], ms, win, sc,
+                                t["dq"], t["dk"], t["dv"])
+
     def measure(w, steps, warmup, sample_clocks=False):
+        """Times whole steps (fwd + bwd calls, events around the step only: the
+        dQ kernel may overlap the dK/dV kernel's tail), then the four kernels
+        one by one (events between them, which also stops that overlap)."""
         inp, t = prepare(w)
         for _ in range(warmup):
-            step(w, t)
+            step_api(w, t)
             flush.fill_(1.0)
         torch.cuda.synchronize()
-        evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        step_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
         sampler = ClockSampler(local) if sample_clocks else None
         if sampler:
             sampler.__enter__()
@@ -275,21 +285,31 @@ def main():
         wall0 = time.perf_counter()
         for s in range(steps):
             flush.fill_(float(s))  # L2 flush between steps, outside the events
-            step(w, t, evsets[s])
+            step_evs[s][0].record(stream)
+            step_api(w, t)
+            step_evs[s][1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
         if sampler:
             sampler.__exit__(None, None, None)
+        for _ in range(warmup):
+            step(w, t)
+            flush.fill_(1.0)
+        torch.cuda.synchronize()
+        evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        for s in range(steps):
+            flush.fill_(float(s))
+            step(w, t, evsets[s])
+        torch.cuda.synchronize()
         status = binding.attn_varlen_get_status()
         if status:
             raise RuntimeError(f"device status word {status}")
         names = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
         per = {n: [] for n in names}
-        tot = []
+        tot = [ev[0].elapsed_time(ev[1]) for ev in step_evs]
         for ev in evsets:
             for i, n in enumerate(names):
                 per[n].append(ev[i].elapsed_time(ev[i + 1]))
-            tot.append(ev[0].elapsed_time(ev[4]))
         pairs = unmasked_pairs(inp.cu_seqlens, w.window_left)
         return {"inp": inp, "t": t, "total_ms": tot, "per_ms": per, "pairs": pairs, "wall_s": wall,
                 "clocks": sampler.summary() if sampler else None}

@@ -34,6 +34,7 @@
 
 #include "attn_internal.h"
 #include "mask.cuh"
+#include "plan.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 #include "tiles.cuh"
@@ -43,7 +44,6 @@ namespace vsw {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kHalfRows = 64 * 128;  // byte offset of row 64 inside a swizzled half tile
 
 // Writes 32 fp32 accumulator columns of one row, scaled, as bf16 to global.
 __device__ __forceinline__ void store_row32_bf16(void* dst_row, int c, const uint32_t (&r)[32], float mul) {
@@ -162,24 +162,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 3) {
-    grid_dependency_wait();
-    int* cu = reinterpret_cast<int*>(gbase + C::kQOff);
-    for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
-    __syncwarp();
-    const int n = build_schedule<true>(cu, a.nseg, a.window, a.max_levels, a.hkv, p.chains_max, items, kBwdMaxItems,
-                                       cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
-    if (lane == 0) {
-      n_items = n < 0 ? 0 : n;
-      if (n < 0) atomicExch(a.status, 2);
-    }
-  }
   grid_dependency_wait();  // inputs written by earlier kernels are read after this
+  const int planned = plan_schedule<true>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hkv, p.chains_max, items,
+                                          kBwdMaxItems, reinterpret_cast<int*>(gbase),
+                                          (int)((C::kSmemBytes - 1024) / 4), blockIdx.x, gridDim.x);
+  if (planned == kPlanDoesNotFit) {
+    if (warp == 3) {
+      int* cu = reinterpret_cast<int*>(gbase + C::kQOff);
+      for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
+      __syncwarp();
+      const int n = build_schedule<true>(cu, a.nseg, a.window, a.max_levels, a.hkv, p.chains_max, items,
+                                         kBwdMaxItems, cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
+      if (lane == 0) {
+        n_items = n < 0 ? 0 : n;
+        if (n < 0) atomicExch(a.status, 2);
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    n_items = planned < 0 ? 0 : planned;
+    if (planned < 0) atomicExch(a.status, 2);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const int nit = n_items;
+  // The dQ kernel that follows in the same backward reads nothing this kernel
+  // writes: let it take the SMs this grid frees (it waits for this grid to
+  // finish only before it exits).
+  grid_dependents_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -528,19 +539,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 3) {
-    grid_dependency_wait();
-    int* cu = reinterpret_cast<int*>(gbase + C::kKOff);
-    for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
-    __syncwarp();
-    const int n = build_schedule<false>(cu, a.nseg, a.window, a.max_levels, a.hq, 0, items, C::kMaxItems,
-                                        cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
-    if (lane == 0) {
-      n_items = n < 0 ? 0 : n;
-      if (n < 0) atomicExch(a.status, 2);
+  // Inputs written by earlier kernels are read after this wait.  Right after
+  // the dK/dV kernel of the same backward there is nothing to wait for: that
+  // kernel only starts this one once all of its CTAs have passed their own
+  // wait (so delta and every input are complete), and it writes nothing this
+  // kernel reads.
+  if (!p.dq_after_dkdv) grid_dependency_wait();
+  const int planned = plan_schedule<false>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hq, 0, items,
+                                           C::kMaxItems, reinterpret_cast<int*>(gbase), (int)(C::kStateOff / 4),
+                                           blockIdx.x, gridDim.x);
+  if (planned == kPlanDoesNotFit) {
+    if (warp == 3) {
+      int* cu = reinterpret_cast<int*>(gbase + C::kKOff);
+      for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
+      __syncwarp();
+      const int n = build_schedule<false>(cu, a.nseg, a.window, a.max_levels, a.hq, 0, items, C::kMaxItems,
+                                          cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
+      if (lane == 0) {
+        n_items = n < 0 ? 0 : n;
+        if (n < 0) atomicExch(a.status, 2);
+      }
     }
+  } else if (threadIdx.x == 0) {
+    n_items = planned < 0 ? 0 : planned;
+    if (planned < 0) atomicExch(a.status, 2);
   }
-  grid_dependency_wait();  // inputs written by earlier kernels are read after this
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -755,6 +778,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  // Finish no earlier than the kernel before (stream order for what follows).
+  grid_dependency_wait();
 }
 
 #undef abort_flag

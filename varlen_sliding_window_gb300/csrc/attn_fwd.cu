@@ -33,6 +33,7 @@
 
 #include "attn_internal.h"
 #include "mask.cuh"
+#include "plan.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 #include "tiles.cuh"
@@ -45,11 +46,16 @@ constexpr int kFwdMaxItems = 40;  // work units one CTA may own
 
 template <int NQT>
 struct FwdCfg {
-  static constexpr int kQStages = 2;                   // Q tiles of consecutive work items
-  static constexpr int kStages = NQT == 2 ? 3 : 5;     // K/V tile slots
+  // Q tiles (one per head) go through a ring of their own: with NQT = 2 the
+  // third slot takes the next item's first head while the current item runs,
+  // and its second head follows as soon as the current first head's last S
+  // MMA is done.  That leaves four K/V slots, so K(j+1) and V(j+1) can be in
+  // flight while K(j)/V(j) are in use.
+  static constexpr int kQSlots = NQT == 2 ? 3 : 2;
+  static constexpr int kStages = NQT == 2 ? 4 : 5;     // K/V tile slots
   static constexpr int kThreads = 128 * (1 + NQT);
-  static constexpr uint32_t kQOff = 0;                  // Q stage s, tile t: (s * NQT + t) tiles
-  static constexpr uint32_t kKVOff = kQStages * NQT * kTileBytes;
+  static constexpr uint32_t kQOff = 0;                  // Q slot s at s tiles
+  static constexpr uint32_t kKVOff = kQSlots * kTileBytes;
   static constexpr uint32_t kSmemBytes = kKVOff + kStages * kTileBytes + 1024;
   static constexpr uint32_t kTmemCols = NQT == 2 ? 512 : 256;
   static constexpr uint32_t kOCol = NQT * 128;  // O accumulators follow the S tiles
@@ -64,7 +70,7 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ WorkItem items[kFwdMaxItems];
   __shared__ int n_items;
-  __shared__ __align__(8) uint64_t bar_q_full[2], bar_q_empty[2];
+  __shared__ __align__(8) uint64_t bar_q_full[C::kQSlots], bar_q_empty[C::kQSlots];
   __shared__ __align__(8) uint64_t bar_kv_full[S], bar_kv_empty[S];
   __shared__ __align__(8) uint64_t bar_s_full[NQT], bar_p_full[NQT], bar_o_done[NQT];
   __shared__ uint32_t tmem_slot;
@@ -79,7 +85,7 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::kQSlots; ++s) {
       mbar_init(smem_u32(&bar_q_full[s]), 1);
       mbar_init(smem_u32(&bar_q_empty[s]), 1);
     }
@@ -101,20 +107,28 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
     tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 3) {
-    grid_dependency_wait();
-    // cu_seqlens is staged in the (not yet used) K/V region.
-    int* cu = reinterpret_cast<int*>(gbase + C::kKVOff);
-    for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
-    __syncwarp();
-    const int n = build_schedule<false>(cu, a.nseg, a.window, a.max_levels, a.hq / NQT, 0, items, kFwdMaxItems,
-                                        cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
-    if (lane == 0) {
-      n_items = n < 0 ? 0 : n;
-      if (n < 0) atomicExch(a.status, 2);
-    }
-  }
   grid_dependency_wait();  // inputs written by earlier kernels are read after this
+  // Work list: every thread plans (plan.cuh) in the not yet used tile region;
+  // inputs too large for that fall back to the single-warp builder.
+  const int planned = plan_schedule<false>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hq / NQT, 0, items,
+                                           kFwdMaxItems, reinterpret_cast<int*>(gbase),
+                                           (int)((C::kSmemBytes - 1024) / 4), blockIdx.x, gridDim.x);
+  if (planned == kPlanDoesNotFit) {
+    if (warp == 3) {
+      int* cu = reinterpret_cast<int*>(gbase + C::kKVOff);
+      for (int s = lane; s <= a.nseg; s += 32) cu[s] = a.cu_seqlens[s];
+      __syncwarp();
+      const int n = build_schedule<false>(cu, a.nseg, a.window, a.max_levels, a.hq / NQT, 0, items, kFwdMaxItems,
+                                          cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
+      if (lane == 0) {
+        n_items = n < 0 ? 0 : n;
+        if (n < 0) atomicExch(a.status, 2);
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    n_items = planned < 0 ? 0 : planned;
+    if (planned < 0) atomicExch(a.status, 2);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -127,24 +141,25 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
     // ------------------------------------------------------------ producer
     if (NQT == 2) regs_decrease<104>();
     if (lane == 0) {
-      int kv_cnt = 0;
+      int kv_cnt = 0, q_cnt = 0;
       bool ok = true;
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
         const int q_lo = w.seg_lo + w.blk * kTile;
         const int n0 = w.t0;
         const int nt = w.t1 - w.t0 + 1;
-        const int qs = it & 1;
-        if (it >= 2 && !(ok = mbar_wait(smem_u32(&bar_q_empty[qs]), ((it >> 1) - 1) & 1, &abort_flag, a.status)))
-          break;
-        const uint32_t qbar = smem_u32(&bar_q_full[qs]);
-        mbar_arrive_expect_tx(qbar, NQT * kTileBytes);
-        for (int t = 0; t < NQT; ++t) {
+        for (int t = 0; t < NQT && ok; ++t, ++q_cnt) {
+          const int slot = q_cnt % C::kQSlots, use = q_cnt / C::kQSlots;
+          if (use > 0 && !(ok = mbar_wait(smem_u32(&bar_q_empty[slot]), (use - 1) & 1, &abort_flag, a.status)))
+            break;
+          const uint32_t qbar = smem_u32(&bar_q_full[slot]);
+          mbar_arrive_expect_tx(qbar, kTileBytes);
           const int h = w.unit * NQT + t;
-          const uint32_t dst = sQ + (qs * NQT + t) * kTileBytes;
+          const uint32_t dst = sQ + slot * kTileBytes;
           tma_load_3d(dst, &tmQ, qbar, 0, h, q_lo);
           tma_load_3d(dst + kHalfTile, &tmQ, qbar, 64, h, q_lo);
         }
+        if (!ok) break;
         const int g = (w.unit * NQT) / a.group;
         for (int j = 0; j < nt && ok; ++j) {
           const int k0 = w.seg_lo + (n0 + j) * kTile;
@@ -168,7 +183,7 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, 128, 0, 1);
-      int kv_cnt = 0;
+      int kv_cnt = 0, q_cnt = 0;
       uint32_t p_cnt[NQT];
       for (int t = 0; t < NQT; ++t) p_cnt[t] = 0;
       bool ok = true;
@@ -183,19 +198,25 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
         const WorkItem w = items[it];
         const int n0 = w.t0;
         const int nt = w.t1 - w.t0 + 1;
-        const int qs = it & 1;
-        auto issue_qk = [&](int t, int slotK) {
+        int qslot[NQT];
+        for (int t = 0; t < NQT && ok; ++t, ++q_cnt) {
+          qslot[t] = q_cnt % C::kQSlots;
+          ok = mbar_wait(smem_u32(&bar_q_full[qslot[t]]), (q_cnt / C::kQSlots) & 1, &abort_flag, a.status);
+        }
+        if (!ok) break;
+        tc_fence_after();
+        // S_t = Q_t K^T; the Q slot of head t is released after its last S.
+        auto issue_qk = [&](int t, int slotK, bool last) {
           const uint32_t d = tmem + t * 128;
-          const uint32_t qt = sQ + (qs * NQT + t) * kTileBytes, kt = sKV + slotK * kTileBytes;
+          const uint32_t qt = sQ + qslot[t] * kTileBytes, kt = sKV + slotK * kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) mma_ss(d, kmajor_desc(qt, kk), kmajor_desc(kt, kk), idesc_qk, kk > 0);
           tc_commit(smem_u32(&bar_s_full[t]));
+          if (last) tc_commit(smem_u32(&bar_q_empty[qslot[t]]));
         };
-        if (!(ok = mbar_wait(smem_u32(&bar_q_full[qs]), (it >> 1) & 1, &abort_flag, a.status))) break;
-        tc_fence_after();
         int slotK;
         if (!(ok = wait_kv(slotK))) break;
-        for (int t = 0; t < NQT; ++t) issue_qk(t, slotK);
+        for (int t = 0; t < NQT; ++t) issue_qk(t, slotK, nt == 1);
         tc_commit(smem_u32(&bar_kv_empty[slotK]));
         for (int j = 0; j < nt && ok; ++j) {
           int slotV, slotK2 = -1;
@@ -211,16 +232,16 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
             for (int kk = 0; kk < 8; ++kk)
               mma_ts(d, tmem + t * 128 + kk * 8, mnmajor_desc(vt, kk), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
             if (j + 1 == nt) tc_commit(smem_u32(&bar_o_done[t]));
+            // V(j) is free once the last head's PV has read it.
+            if (t == NQT - 1) tc_commit(smem_u32(&bar_kv_empty[slotV]));
             if (j + 1 < nt) {
               if (t == 0 && !(ok = wait_kv(slotK2))) break;
-              issue_qk(t, slotK2);
+              issue_qk(t, slotK2, j + 2 == nt);
             }
           }
           if (!ok) break;
-          tc_commit(smem_u32(&bar_kv_empty[slotV]));
           if (j + 1 < nt) tc_commit(smem_u32(&bar_kv_empty[slotK2]));
         }
-        if (ok) tc_commit(smem_u32(&bar_q_empty[qs]));
       }
     }
   } else if (warp < 4) {

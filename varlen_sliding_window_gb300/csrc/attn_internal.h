@@ -42,6 +42,10 @@ struct BwdParams {
   float* chains;         // fp32 [chains_max][2][128][128] partial dV, dK
   int* chain_progress;   // int [chains_max][2], links published so far
   int chains_max;        // 0 disables splitting
+  // Set when the dQ kernel is launched right after the dK/dV kernel of the
+  // same backward: it then needs nothing that kernel writes, starts on the
+  // SMs the dK/dV kernel frees and waits for it only before exiting.
+  int dq_after_dkdv;
 };
 
 // Backward workspace layout: delta, chain progress counters, chain buffers.
@@ -85,7 +89,9 @@ int launch_mask_probe(const int* cu_seqlens, int nseg, int total, int window, in
 // Launches `kernel` on `stream` with programmatic stream serialization, so
 // that its CTAs may start (and run their prologue) while the previous kernel
 // in the stream drains.  Every kernel of this library calls
-// grid_dependency_wait() before reading global memory written earlier.
+// grid_dependency_wait() before reading global memory written earlier, except
+// the dQ kernel launched right after the dK/dV kernel of the same backward,
+// which reads nothing that kernel writes and waits only before exiting.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        Args&&... args) {

@@ -45,6 +45,7 @@ struct WorkItem {
 __device__ __forceinline__ int link_index(const WorkItem& w) { return w.link & 0xffff; }
 __device__ __forceinline__ int link_count(const WorkItem& w) { return w.link >> 16; }
 constexpr int kCostBuckets = 512;  // costs >= 511 tiles share the last bucket
+static_assert(kCostBuckets % 32 == 0, "the bucket prefix gives each lane kCostBuckets / 32 buckets");
 
 // Scratch the builder needs in shared memory, in ints: the histogram / bucket
 // bases, a few counters, and room to reorder up to `max_out` items.
@@ -174,15 +175,27 @@ __device__ __noinline__ int build_schedule(const int* cu, int nseg, int window, 
     }
   }
   __syncwarp();
-  // ---- exclusive prefix over buckets in descending cost order (lane 0)
-  if (lane == 0) {
-    int acc = 0;
-    for (int b = kCostBuckets - 1; b >= 0; --b) {
+  // ---- exclusive prefix over buckets in descending cost order: lane l takes
+  // the 16 buckets 511 - 16l down to 496 - 16l, then a warp scan joins them.
+  {
+    constexpr int kPer = kCostBuckets / 32;
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) sum += hist[kCostBuckets - 1 - (lane * kPer + i)];
+    int incl = sum;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int acc = incl - sum;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int b = kCostBuckets - 1 - (lane * kPer + i);
       const int n = hist[b];
       hist[b] = acc;
       acc += n;
     }
-    counters[0] = 0;
+    if (lane == 0) counters[0] = 0;
   }
   __syncwarp();
   // ---- pass 2: positions (deterministic ranks), deal units, keep own
