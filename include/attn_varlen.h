@@ -34,9 +34,11 @@
  * memory on the current CUDA device, 16-byte aligned.  The library keeps no
  * reference after the enqueued work completes.  Outputs are fully
  * overwritten.  The forward allocates nothing.  attn_varlen_bwd takes a
- * scratch buffer of attn_varlen_bwd_workspace_bytes() bytes from the
- * stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`); the
- * sub-step calls below take a caller-provided workspace instead.
+ * scratch buffer of attn_varlen_bwd_workspace_bytes() bytes, stream-ordered
+ * on `stream`, from a per-device memory pool the library creates on its first
+ * call on that device (make that first call outside any stream capture); the
+ * pool keeps the memory it has reserved for later calls.  The sub-step calls
+ * below take a caller-provided workspace instead.
  *
  * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
  * stream).  No call synchronises the host except attn_varlen_get_status();

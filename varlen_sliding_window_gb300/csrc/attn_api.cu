@@ -27,6 +27,10 @@ struct DeviceInfo {
   bool supported = false;
   int num_sms = 0;
   int* status = nullptr;  // device address of g_status_word
+  // Stream-ordered pool for the backward's workspace.  It keeps what it has
+  // reserved (release threshold: never), so a synchronisation between steps
+  // does not hand the memory back and make the next call map it again.
+  cudaMemPool_t pool = nullptr;
 };
 
 std::mutex g_mu;
@@ -51,6 +55,15 @@ int current_device(DeviceInfo** info) {
       if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return ATTN_ERR_CUDA;
       d.status = static_cast<int*>(p);
       if (cudaMemset(d.status, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.handleTypes = cudaMemHandleTypeNone;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) return ATTN_ERR_CUDA;
+      cuuint64_t keep = ~cuuint64_t(0);
+      if (cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
+        return ATTN_ERR_CUDA;
     }
     d.probed = true;
   }
@@ -223,7 +236,7 @@ int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   const size_t ws_bytes = attn_varlen_bwd_workspace_bytes(total, num_heads_q);
-  if (cudaMallocAsync(&ws, ws_bytes, s) != cudaSuccess) return ATTN_ERR_ALLOC;
+  if (cudaMallocFromPoolAsync(&ws, ws_bytes, b.dev->pool, s) != cudaSuccess) return ATTN_ERR_ALLOC;
   carve_workspace(ws, ws_bytes, total, num_heads_q, b.p);
   int lr = launch_bwd_preprocess(b.p, s);
   if (!lr) lr = launch_bwd_dkdv(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, s);
