@@ -160,38 +160,6 @@ int attn_varlen_bwd_dq(const void* dout, const void* q, const void* k, const voi
                        int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream);
 
 /*
- * The backward for callers that cannot allocate device memory.  (The page
- * has no counterpart; this is a property of the library, not of the method.)
- * Some callers may not call cudaMalloc or the stream-ordered allocator: code
- * running under an allocator it does not own (a framework's caching
- * allocator, a fixed pre-reserved memory budget), real-time or embedded
- * callers for which a driver allocation may block or synchronise the device,
- * or paths that must not allocate at all.  This call computes exactly what
- * attn_varlen_bwd computes, with the same arguments, but keeps its scratch
- * (D = rowsum(dout * out), float32 [Hq, T]) in a fixed device array compiled
- * into the library instead of allocating it; it calls no cudaMalloc,
- * cudaFree or other allocating routine.
- *   Limit: T * Hq <= 2,097,152 (8 MiB of scratch); larger problems return
- *   ATTN_ERR_NOALLOC_TOO_LARGE before anything is enqueued.  Every GPU that
- *   loads the library holds the array until the process exits.
- *   Sharing: all calls on a device use the same array.  The previous call's
- *   contents are irrelevant (every element read is written first in the same
- *   call), but calls whose GPU work overlaps in time (different streams or
- *   host threads) race on the array; the caller must order them.
- *   Set-up: the first call on each device looks up the array's device
- *   address (with that device current) and caches it; make that first call
- *   before any stream capture.
- */
-int attn_varlen_bwd_noalloc(const void* dout, const void* q, const void* k, const void* v, const void* out,
-                            const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
-                            float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
-                            int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream);
-
-/* Bytes of scratch the backward takes from the stream-ordered allocator:
- * D (T * Hq floats, 256-byte padded) plus 40 MiB of chain buffers. */
-size_t attn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads_q);
-
-/*
  * Synchronises `stream`, then returns ATTN_OK if no kernel of this library
  * recorded an error on the current device since the last call, else
  * ATTN_ERR_DEVICE_STATUS; *device_code (optional) receives the raw word

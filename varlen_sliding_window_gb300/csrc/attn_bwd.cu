@@ -59,6 +59,22 @@ __device__ __forceinline__ void store_row32_bf16(void* dst_row, int c, const uin
   }
 }
 
+// Two TMEM loads of 64 consecutive columns each (four x32 loads, one wait).
+__device__ __forceinline__ void tmem_ld64x2_wait(uint32_t ta, uint32_t (&ra)[64], uint32_t tb, uint32_t (&rb)[64]) {
+  uint32_t(&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ra[0]);
+  uint32_t(&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ra[32]);
+  uint32_t(&b0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&rb[0]);
+  uint32_t(&b1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&rb[32]);
+  tmem_ld32(ta, a0);
+  tmem_ld32(ta + 32, a1);
+  tmem_ld32(tb, b0);
+  tmem_ld32(tb + 32, b1);
+  tmem_wait_ld(a0);
+  tmem_wait_ld(a1);
+  tmem_wait_ld(b0);
+  tmem_wait_ld(b1);
+}
+
 // One TMEM load of 64 consecutive columns (two x32 loads, one wait).
 __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]) {
   uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
@@ -104,7 +120,16 @@ struct DkvCfg {
   static constexpr uint32_t kKOff = 0;
   static constexpr uint32_t kVOff = kTileBytes;
   static constexpr uint32_t kQOff = 2 * kTileBytes;  // stage s: Q at kQOff + 2s tiles, dO right after
-  static constexpr uint32_t kSmemBytes = (2 + 2 * kStages) * kTileBytes + 1024;
+  // Extra k-step of S^T and dP^T (tiles.cuh): a block of ones (the A side, for
+  // K and V) and per stage the query-side blocks holding -lse/scale (with Q)
+  // and -D (with dO), each split into a bf16 high and low part, so the MMAs
+  // deliver s - lse/scale and dP - D directly.
+  static constexpr uint32_t kAugOff = (2 + 2 * kStages) * kTileBytes;
+  static constexpr uint32_t kOnesOff = kAugOff;
+  static constexpr uint32_t kQxOff = kAugOff + kAugBytes;                 // + s * kAugBytes
+  static constexpr uint32_t kDOxOff = kAugOff + (1 + kStages) * kAugBytes;  // + s * kAugBytes
+  static constexpr uint32_t kAugEnd = kAugOff + (1 + 2 * kStages) * kAugBytes;
+  static constexpr uint32_t kSmemBytes = kAugEnd + 1024;
   static constexpr uint32_t kTmemCols = 512;
   // S^T, dP^T (128 columns each, fp32; bf16 P^T/dS^T over their halves), dV, dK.
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
@@ -124,8 +149,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2];
   __shared__ __align__(8) uint64_t bar_acc_full, bar_acc_empty;
   __shared__ __align__(8) uint64_t bar_chain[2];
-  __shared__ __align__(16) float s_lse[S][128];    // lse * log2(e) of the stage's 128 queries
-  __shared__ __align__(16) float s_delta[S][128];  // D of the stage's 128 queries
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -164,8 +187,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   grid_dependency_wait();  // inputs written by earlier kernels are read after this
   const int planned = plan_schedule<true>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hkv, p.chains_max, items,
-                                          kBwdMaxItems, reinterpret_cast<int*>(gbase),
-                                          (int)((C::kSmemBytes - 1024) / 4), blockIdx.x, gridDim.x);
+                                          kBwdMaxItems, reinterpret_cast<int*>(gbase), (int)(C::kAugOff / 4),
+                                          blockIdx.x, gridDim.x);
   if (planned == kPlanDoesNotFit) {
     if (warp == 3) {
       int* cu = reinterpret_cast<int*>(gbase + C::kQOff);
@@ -182,6 +205,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     n_items = planned < 0 ? 0 : planned;
     if (planned < 0) atomicExch(a.status, 2);
   }
+  // Extra k-step blocks (after the planner, whose scratch ends at kAugOff):
+  // the ones block gets 1.0 in columns 0 and 1 of every row, the per-stage
+  // blocks start at zero and only their columns 0 and 1 change later.
+  if (threadIdx.x < 128) {
+    const uint32_t ones = sbase + C::kOnesOff;
+    const int r = threadIdx.x;
+    const uint32_t c0 = aug_chunk0(ones, r);
+    st_shared_v4(c0, 0x3F803F80u, 0u, 0u, 0u);
+    st_shared_v4(c0 ^ 16u, 0u, 0u, 0u, 0u);
+  }
+  for (uint32_t off = C::kQxOff + 16u * threadIdx.x; off < C::kAugEnd; off += 16u * blockDim.x)
+    st_shared_v4(sbase + off, 0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -195,8 +231,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // TMA for K, V (per item) and Q, dO (per q tile and head); the warp's 32
-    // lanes stage lse*log2(e) and D of the stage's queries in shared memory.
+    // lanes write the stage's query-side extra k-step blocks (-lse/scale and
+    // -D of its 128 queries, as bf16 high + low parts).
     regs_decrease<104>();
+    const float inv_scale = 1.f / a.scale;
     int cnt = 0;
     bool ok = true;
     for (int it = 0; it < nit && ok; ++it) {
@@ -224,13 +262,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
           }
+          // All eight loads first, so their latencies overlap.
+          float lv[4], dlv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int c = lane + 32 * e, iq = q0 + c;
+            const int iq = q0 + lane + 32 * e;
             const bool in = token_in_range(iq, a.total);
-            s_lse[slot][c] = in ? p.lse[(size_t)h * a.total + iq] * kLog2e : 0.f;
-            s_delta[slot][c] = in ? p.delta[(size_t)h * a.total + iq] : 0.f;
+            lv[e] = in ? __ldg(p.lse + (size_t)h * a.total + iq) : 0.f;
+            dlv[e] = in ? __ldg(p.delta + (size_t)h * a.total + iq) : 0.f;
           }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = lane + 32 * e;
+            const float L = -lv[e] * inv_scale, Dn = -dlv[e];
+            const float L_hi = __bfloat162float(__float2bfloat16_rn(L));
+            const float D_hi = __bfloat162float(__float2bfloat16_rn(Dn));
+            st_shared_u32(aug_chunk0(sbase + C::kQxOff + slot * kAugBytes, c), pack_bf16x2(L_hi, L - L_hi));
+            st_shared_u32(aug_chunk0(sbase + C::kDOxOff + slot * kAugBytes, c), pack_bf16x2(D_hi, Dn - D_hi));
+          }
+          fence_proxy_async_smem();  // the MMA reads these blocks through the async proxy
           __syncwarp();
           if (lane == 0) {
             const uint32_t bar = smem_u32(&bar_qdo_full[slot]);
@@ -251,6 +301,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, 0, 0);   // S^T, dP^T: 128 keys x 128 queries
       constexpr uint32_t idesc_g = make_idesc_bf16(128, 128, 0, 1);   // dV, dK: 128 keys x 128 dims
+      const uint32_t sOnes = sbase + C::kOnesOff;
       int cnt = 0;  // (q tile, head) pairs, for the Q/dO ring and the S/dP buffer
       bool ok = true;
       for (int it = 0; it < nit && ok; ++it) {
@@ -263,15 +314,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!(ok = mbar_wait(smem_u32(&bar_qdo_full[slot]), (cnt / S) & 1, &abort_flag, a.status))) break;
           tc_fence_after();
           const uint32_t sq = sQ0 + slot * 2 * kTileBytes, sdo = sq + kTileBytes;
-          // S^T = K Q^T and dP^T = V dO^T (N = 128 queries).  They overwrite
+          // S^T - lse/scale = [K 1] [Q -lse/scale]^T and dP^T - D = [V 1] [dO -D]^T
+          // (N = 128 queries; the last k-step is the extra block).  They overwrite
           // the previous pair's bf16 P^T/dS^T, which the dV/dK MMAs issued
           // just before have read (in-order execution).
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + C::kColS, kmajor_desc(sK, kk), kmajor_desc(sq, kk), idesc_s, kk > 0);
+          mma_ss(tmem + C::kColS, aug_desc(sOnes), aug_desc(sbase + C::kQxOff + slot * kAugBytes), idesc_s, 1u);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + C::kColDP, kmajor_desc(sV, kk), kmajor_desc(sdo, kk), idesc_s, kk > 0);
+          mma_ss(tmem + C::kColDP, aug_desc(sOnes), aug_desc(sbase + C::kDOxOff + slot * kAugBytes), idesc_s, 1u);
           tc_commit(smem_u32(&bar_s_full[0]));
           // The accumulators of the previous item must have been read out.
           if (pr == 0 && it > 0 &&
@@ -331,39 +385,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
           int c_lo = 0, c_hi = 63;
           if (!full) col_visible_rows(j, q0, w.seg_hi, a.window, c_lo, c_hi);
-          const float* lse2 = &s_lse[slot][64 * x];
-          const float* dlt = &s_delta[slot][64 * x];
           uint32_t sr[64], dr[64];
-          tmem_ld64_wait(tS, sr);
-          tmem_ld64_wait(tDP, dr);
+          tmem_ld64x2_wait(tS, sr, tDP, dr);
           const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
           uint32_t pp[32], pd[32];
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
-            // Pairs of query columns: P = exp2(s*scale*log2e - lse*log2e),
-            // dS = P (dP - D); staged lse/D are broadcast reads.
-            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-            const float4 d4 = *reinterpret_cast<const float4*>(dlt + c);
-#pragma unroll
-            for (int hp = 0; hp < 2; ++hp) {
-              const int cc = c + 2 * hp;
-              const uint64_t nl = hp ? f2_pack(-l4.z, -l4.w) : f2_pack(-l4.x, -l4.y);
-              const uint64_t nd = hp ? f2_pack(-d4.z, -d4.w) : f2_pack(-d4.x, -d4.y);
-              float p0, p1;
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), sc2, nl), p0, p1);
-              p0 = ex2_approx(p0);
-              p1 = ex2_approx(p1);
-              if (!full) {
-                p0 = (cc >= c_lo && cc <= c_hi) ? p0 : 0.f;
-                p1 = (cc + 1 >= c_lo && cc + 1 <= c_hi) ? p1 : 0.f;
-              }
-              float d0, d1;
-              f2_unpack(f2_mul(f2_pack(p0, p1),
-                               f2_add(f2_pack(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1])), nd)),
-                        d0, d1);
-              pp[cc / 2] = pack_bf16x2(p0, p1);
-              pd[cc / 2] = pack_bf16x2(d0, d1);
+          for (int cc = 0; cc < 64; cc += 2) {
+            // Pairs of query columns: the MMAs already subtracted lse/scale
+            // and D, so P = exp2((s - lse/scale) * scale*log2e) and
+            // dS = P (dP - D).
+            float p0, p1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), sc2), p0, p1);
+            p0 = ex2_approx(p0);
+            p1 = ex2_approx(p1);
+            if (!full) {
+              p0 = (cc >= c_lo && cc <= c_hi) ? p0 : 0.f;
+              p1 = (cc + 1 >= c_lo && cc + 1 <= c_hi) ? p1 : 0.f;
             }
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(p0, p1), f2_pack(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1]))), d0, d1);
+            pp[cc / 2] = pack_bf16x2(p0, p1);
+            pd[cc / 2] = pack_bf16x2(d0, d1);
           }
           tmem_st32(tS, pp);
           tmem_st32(tDP, pd);

@@ -178,6 +178,17 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
   return d;
 }
 
+// Shared-memory matrix descriptor, 32-byte swizzle (rows of 16 bf16).
+__device__ __forceinline__ uint64_t make_sdesc_sw32(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t(1) << 46;  // descriptor version for tcgen05
+  d |= uint64_t(6) << 61;  // SWIZZLE_32B
+  return d;
+}
+
 // TMEM loads: the warp reads its 32-lane quarter, 32 consecutive 32-bit columns.
 // Results are only valid after tmem_wait_ld().
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {

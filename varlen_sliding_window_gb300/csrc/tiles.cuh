@@ -28,6 +28,17 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
   return make_sdesc_sw128(tile + kk * 16 * 128, kHalfTile, 1024);
 }
 
+// One extra k-step of 16 columns appended to a K-major operand: 128 rows x
+// 16 bf16 (32 bytes per row) with the 32-byte swizzle, 8-row groups 256 bytes
+// apart.  Used to fold a per-row term into an MMA (row x 1 + term x 1).
+constexpr uint32_t kAugBytes = 128 * 32;
+__device__ __forceinline__ uint64_t aug_desc(uint32_t block) { return make_sdesc_sw32(block, 16, 256); }
+// Byte address of the first 16-byte chunk (columns 0..7) of `row`: under the
+// 32-byte swizzle the two chunks of a row swap places when bit 2 of the row is set.
+__device__ __forceinline__ uint32_t aug_chunk0(uint32_t block, int row) {
+  return block + row * 32 + (((uint32_t(row) >> 2) & 1u) << 4);
+}
+
 // Byte address of the 16-byte chunk holding columns 8*c8 .. 8*c8+7 of `row`.
 __device__ __forceinline__ uint32_t swizzled_chunk(uint32_t tile, int row, int c8) {
   return tile + (c8 >> 3) * kHalfTile + row * 128 + ((uint32_t(c8 & 7) ^ uint32_t(row & 7)) << 4);
@@ -35,6 +46,10 @@ __device__ __forceinline__ uint32_t swizzled_chunk(uint32_t tile, int row, int c
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
