@@ -18,9 +18,10 @@
 //
 // TMEM holds the fp32 accumulators of the MMAs (128 lanes x 512 columns):
 //   dK/dV pass: S^T, dP^T (N = 128 queries), dV, dK.  The two elementwise
-//     warpgroups split each tile's 128 query columns; the dV/dK MMAs of a
-//     64-query half start as soon as that half's bf16 P^T/dS^T are back in
-//     TMEM.
+//     warpgroups split each tile's 128 query columns.  S^T and dP^T complete
+//     separately: P^T (the exp2 work) is computed while dP^T still runs, the
+//     dV MMA of a 64-query half starts as soon as that half of P^T is back
+//     in TMEM, and dK follows dS^T.
 //   dQ pass: two S buffers, dP, dQ.  S of the next kv tile is computed while
 //     the elementwise warpgroups work on the current one, and dP is released
 //     as soon as it has been read into registers.
@@ -57,22 +58,6 @@ __device__ __forceinline__ void store_row32_bf16(void* dst_row, int c, const uin
     pk.w = pack_bf16x2(__uint_as_float(r[v * 8 + 6]) * mul, __uint_as_float(r[v * 8 + 7]) * mul);
     dst[v] = pk;
   }
-}
-
-// Two TMEM loads of 64 consecutive columns each (four x32 loads, one wait).
-__device__ __forceinline__ void tmem_ld64x2_wait(uint32_t ta, uint32_t (&ra)[64], uint32_t tb, uint32_t (&rb)[64]) {
-  uint32_t(&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ra[0]);
-  uint32_t(&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ra[32]);
-  uint32_t(&b0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&rb[0]);
-  uint32_t(&b1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&rb[32]);
-  tmem_ld32(ta, a0);
-  tmem_ld32(ta + 32, a1);
-  tmem_ld32(tb, b0);
-  tmem_ld32(tb + 32, b1);
-  tmem_wait_ld(a0);
-  tmem_wait_ld(a1);
-  tmem_wait_ld(b0);
-  tmem_wait_ld(b1);
 }
 
 // One TMEM load of 64 consecutive columns (two x32 loads, one wait).
@@ -146,7 +131,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ int n_items;
   __shared__ __align__(8) uint64_t bar_kv_full, bar_kv_empty;
   __shared__ __align__(8) uint64_t bar_qdo_full[S], bar_qdo_empty[S];
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2];
+  // s_full[0]: S^T done, s_full[1]: dP^T done; p_full[x] / ds_full[x]: warpgroup
+  // x has written its half of P^T / dS^T.
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_ds_full[2];
   __shared__ __align__(8) uint64_t bar_acc_full, bar_acc_empty;
   __shared__ __align__(8) uint64_t bar_chain[2];
   __shared__ uint32_t tmem_slot;
@@ -170,6 +157,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&bar_s_full[x]), 1);
       mbar_init(smem_u32(&bar_p_full[x]), 128);
+      mbar_init(smem_u32(&bar_ds_full[x]), 128);
     }
     mbar_init(smem_u32(&bar_acc_full), 1);
     mbar_init(smem_u32(&bar_acc_empty), 256);
@@ -257,12 +245,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int hh = 0; hh < a.group && ok; ++hh) {
           const int h = g * a.group + hh;
           const int slot = cnt % S, use = cnt / S;
-          if (use > 0) {
-            if (lane == 0) ok = mbar_wait(smem_u32(&bar_qdo_empty[slot]), (use - 1) & 1, &abort_flag, a.status);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-          }
-          // All eight loads first, so their latencies overlap.
+          // This stage's lse and D loads go out before the wait for its slot.
           float lv[4], dlv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -270,6 +253,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const bool in = token_in_range(iq, a.total);
             lv[e] = in ? __ldg(p.lse + (size_t)h * a.total + iq) : 0.f;
             dlv[e] = in ? __ldg(p.delta + (size_t)h * a.total + iq) : 0.f;
+          }
+          if (use > 0) {
+            if (lane == 0) ok = mbar_wait(smem_u32(&bar_qdo_empty[slot]), (use - 1) & 1, &abort_flag, a.status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
           }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -309,37 +297,73 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int npairs = (w.t1 - w.t0 + 1) * a.group;
         if (!(ok = mbar_wait(smem_u32(&bar_kv_full), it & 1, &abort_flag, a.status))) break;
         tc_fence_after();
-        for (int pr = 0; pr < npairs && ok; ++pr) {
-          const int slot = cnt % S;
-          if (!(ok = mbar_wait(smem_u32(&bar_qdo_full[slot]), (cnt / S) & 1, &abort_flag, a.status))) break;
+        // Pairs are software-pipelined inside an item when the next Q/dO stage
+        // is already there:
+        //   S^T(0) dP^T(0) | dV(0) S^T(1) dK(0) dP^T(1) | dV(1) S^T(2) dK(1) ...
+        // so the elementwise exp2 of pair n+1 runs during dK(n) and dP^T(n+1),
+        // and its dS of pair n during dV(n) and S^T(n+1); otherwise S^T(n+1)
+        // follows dK(n).  S^T(n+1) overwrites
+        // P^T(n), which dV(n) (issued just before) has read; dP^T(n+1)
+        // overwrites dS^T(n) after dK(n) (in-order execution).  Items are not
+        // pipelined into each other: the next item's K/V tiles load only
+        // once this item's MMAs are done.
+        auto issue_s = [&](int c) -> bool {  // S^T of pair c: needs its Q (and staged -lse/scale)
+          const int sl = c % S;
+          if (!mbar_wait(smem_u32(&bar_qdo_full[sl]), (c / S) & 1, &abort_flag, a.status)) return false;
           tc_fence_after();
-          const uint32_t sq = sQ0 + slot * 2 * kTileBytes, sdo = sq + kTileBytes;
-          // S^T - lse/scale = [K 1] [Q -lse/scale]^T and dP^T - D = [V 1] [dO -D]^T
-          // (N = 128 queries; the last k-step is the extra block).  They overwrite
-          // the previous pair's bf16 P^T/dS^T, which the dV/dK MMAs issued
-          // just before have read (in-order execution).
+          const uint32_t sq = sQ0 + sl * 2 * kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + C::kColS, kmajor_desc(sK, kk), kmajor_desc(sq, kk), idesc_s, kk > 0);
-          mma_ss(tmem + C::kColS, aug_desc(sOnes), aug_desc(sbase + C::kQxOff + slot * kAugBytes), idesc_s, 1u);
+          mma_ss(tmem + C::kColS, aug_desc(sOnes), aug_desc(sbase + C::kQxOff + sl * kAugBytes), idesc_s, 1u);
+          tc_commit(smem_u32(&bar_s_full[0]));
+          return true;
+        };
+        auto issue_dp = [&](int c) {  // dP^T of pair c (its Q/dO stage is already waited for)
+          const int sl = c % S;
+          const uint32_t sdo = sQ0 + sl * 2 * kTileBytes + kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + C::kColDP, kmajor_desc(sV, kk), kmajor_desc(sdo, kk), idesc_s, kk > 0);
-          mma_ss(tmem + C::kColDP, aug_desc(sOnes), aug_desc(sbase + C::kDOxOff + slot * kAugBytes), idesc_s, 1u);
-          tc_commit(smem_u32(&bar_s_full[0]));
+          mma_ss(tmem + C::kColDP, aug_desc(sOnes), aug_desc(sbase + C::kDOxOff + sl * kAugBytes), idesc_s, 1u);
+          tc_commit(smem_u32(&bar_s_full[1]));
+        };
+        // S^T - lse/scale = [K 1] [Q -lse/scale]^T and dP^T - D = [V 1] [dO -D]^T
+        // (N = 128 queries; the last k-step is the extra block), committed
+        // separately so the exp2 work starts while dP^T runs.
+        if (!(ok = issue_s(cnt))) break;
+        issue_dp(cnt);
+        for (int pr = 0; pr < npairs && ok; ++pr) {
+          const int slot = cnt % S;
+          const uint32_t sq = sQ0 + slot * 2 * kTileBytes, sdo = sq + kTileBytes;
           // The accumulators of the previous item must have been read out.
           if (pr == 0 && it > 0 &&
               !(ok = mbar_wait(smem_u32(&bar_acc_empty), (it - 1) & 1, &abort_flag, a.status)))
             break;
+          // dV += P^T_half dO_half as each half of P^T arrives (K = 64 queries).
           for (int half = 0; half < 2 && ok; ++half) {
             if (!(ok = mbar_wait(smem_u32(&bar_p_full[half]), cnt & 1, &abort_flag, a.status))) break;
             tc_fence_after();
             const bool acc = pr > 0 || half > 0;
-            // dV += P^T_half dO_half, dK += dS^T_half Q_half (K = 64 queries).
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ts(tmem + C::kColDV, tmem + C::kColS + 64 * half + kk * 8, mnmajor_desc(sdo, 4 * half + kk),
                      idesc_g, (acc || kk > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+          const bool more = pr + 1 < npairs;
+          // S^T(n+1) goes before dK(n) only if its Q stage has landed; the MMA
+          // warp never blocks on it here (it would hold back dK(n)).
+          bool s_next = false;
+          if (more && mbar_try_wait(smem_u32(&bar_qdo_full[(cnt + 1) % S]), ((cnt + 1) / S) & 1)) {
+            ok = issue_s(cnt + 1);
+            s_next = true;
+          }
+          // dK += dS^T_half Q_half.
+          for (int half = 0; half < 2 && ok; ++half) {
+            if (!(ok = mbar_wait(smem_u32(&bar_ds_full[half]), cnt & 1, &abort_flag, a.status))) break;
+            tc_fence_after();
+            const bool acc = pr > 0 || half > 0;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ts(tmem + C::kColDK, tmem + C::kColDP + 64 * half + kk * 8, mnmajor_desc(sq, 4 * half + kk),
@@ -347,6 +371,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           if (!ok) break;
           tc_commit(smem_u32(&bar_qdo_empty[slot]));
+          if (more && !s_next && !(ok = issue_s(cnt + 1))) break;
+          if (more) issue_dp(cnt + 1);
           ++cnt;
         }
         if (!ok) break;
@@ -379,39 +405,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int q0 = w.seg_lo + b * kTile + 64 * x;  // first query of this half
         const bool full = tile_fully_visible_kv(k0, w.seg_lo + b * kTile, w.seg_hi, a.window);
         for (int hh = 0; hh < a.group; ++hh) {
-          const int slot = cnt % S;
-          if (!(ok = mbar_wait(smem_u32(&bar_qdo_full[slot]), (cnt / S) & 1, &abort_flag, a.status))) break;
           if (!(ok = mbar_wait(smem_u32(&bar_s_full[0]), cnt & 1, &abort_flag, a.status))) break;
           tc_fence_after();
           int c_lo = 0, c_hi = 63;
           if (!full) col_visible_rows(j, q0, w.seg_hi, a.window, c_lo, c_hi);
-          uint32_t sr[64], dr[64];
-          tmem_ld64x2_wait(tS, sr, tDP, dr);
-          const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
-          uint32_t pp[32], pd[32];
+          // P^T while the dP^T MMA runs: the MMA already subtracted lse/scale,
+          // so P = exp2((s - lse/scale) * scale*log2e).
+          float pv[64];
+          {
+            uint32_t sr[64];
+            tmem_ld64_wait(tS, sr);
+            const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+            uint32_t pp[32];
 #pragma unroll
-          for (int cc = 0; cc < 64; cc += 2) {
-            // Pairs of query columns: the MMAs already subtracted lse/scale
-            // and D, so P = exp2((s - lse/scale) * scale*log2e) and
-            // dS = P (dP - D).
-            float p0, p1;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), sc2), p0, p1);
-            p0 = ex2_approx(p0);
-            p1 = ex2_approx(p1);
-            if (!full) {
-              p0 = (cc >= c_lo && cc <= c_hi) ? p0 : 0.f;
-              p1 = (cc + 1 >= c_lo && cc + 1 <= c_hi) ? p1 : 0.f;
+            for (int cc = 0; cc < 64; cc += 2) {
+              float p0, p1;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), sc2), p0, p1);
+              p0 = ex2_approx(p0);
+              p1 = ex2_approx(p1);
+              if (!full) {
+                p0 = (cc >= c_lo && cc <= c_hi) ? p0 : 0.f;
+                p1 = (cc + 1 >= c_lo && cc + 1 <= c_hi) ? p1 : 0.f;
+              }
+              pv[cc] = p0;
+              pv[cc + 1] = p1;
+              pp[cc / 2] = pack_bf16x2(p0, p1);
             }
-            float d0, d1;
-            f2_unpack(f2_mul(f2_pack(p0, p1), f2_pack(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1]))), d0, d1);
-            pp[cc / 2] = pack_bf16x2(p0, p1);
-            pd[cc / 2] = pack_bf16x2(d0, d1);
+            tmem_st32(tS, pp);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_p_full[x]));
           }
-          tmem_st32(tS, pp);
-          tmem_st32(tDP, pd);
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(smem_u32(&bar_p_full[x]));
+          // dS^T = P (dP - D) once dP^T is there (the MMA subtracted D).
+          if (!(ok = mbar_wait(smem_u32(&bar_s_full[1]), cnt & 1, &abort_flag, a.status))) break;
+          tc_fence_after();
+          {
+            uint32_t dr[64];
+            tmem_ld64_wait(tDP, dr);
+            uint32_t pd[32];
+#pragma unroll
+            for (int cc = 0; cc < 64; cc += 2) {
+              float d0, d1;
+              f2_unpack(f2_mul(f2_pack(pv[cc], pv[cc + 1]), f2_pack(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1]))),
+                        d0, d1);
+              pd[cc / 2] = pack_bf16x2(d0, d1);
+            }
+            tmem_st32(tDP, pd);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_ds_full[x]));
+          }
           ++cnt;
         }
       }
