@@ -140,14 +140,15 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (NQT == 2) regs_decrease<104>();
-    if (lane == 0) {
-      int kv_cnt = 0, q_cnt = 0;
+    // Lane 1 streams the Q tiles and lane 0 the K/V tiles, each through its
+    // own ring: the next unit's Q tiles load as soon as their slots free up,
+    // not after the last K/V load of the current unit.
+    if (lane == 1) {
+      int q_cnt = 0;
       bool ok = true;
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
         const int q_lo = w.seg_lo + w.blk * kTile;
-        const int n0 = w.t0;
-        const int nt = w.t1 - w.t0 + 1;
         for (int t = 0; t < NQT && ok; ++t, ++q_cnt) {
           const int slot = q_cnt % C::kQSlots, use = q_cnt / C::kQSlots;
           if (use > 0 && !(ok = mbar_wait(smem_u32(&bar_q_empty[slot]), (use - 1) & 1, &abort_flag, a.status)))
@@ -159,7 +160,14 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
           tma_load_3d(dst, &tmQ, qbar, 0, h, q_lo);
           tma_load_3d(dst + kHalfTile, &tmQ, qbar, 64, h, q_lo);
         }
-        if (!ok) break;
+      }
+    } else if (lane == 0) {
+      int kv_cnt = 0;
+      bool ok = true;
+      for (int it = 0; it < nit && ok; ++it) {
+        const WorkItem w = items[it];
+        const int n0 = w.t0;
+        const int nt = w.t1 - w.t0 + 1;
         const int g = (w.unit * NQT) / a.group;
         for (int j = 0; j < nt && ok; ++j) {
           const int k0 = w.seg_lo + (n0 + j) * kTile;
@@ -194,30 +202,43 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
         tc_fence_after();
         return r;
       };
+      // S_t = Q_t K^T into S_t; the Q slot of head t is released after its last S.
+      auto issue_qk = [&](int t, int qs, int slotK, bool last) {
+        const uint32_t d = tmem + t * 128;
+        const uint32_t qt = sQ + qs * kTileBytes, kt = sKV + slotK * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(d, kmajor_desc(qt, kk), kmajor_desc(kt, kk), idesc_qk, kk > 0);
+        tc_commit(smem_u32(&bar_s_full[t]));
+        if (last) tc_commit(smem_u32(&bar_q_empty[qs]));
+      };
+      auto wait_q = [&](int& qs) -> bool {  // the next head's Q tile, in load order
+        qs = q_cnt % C::kQSlots;
+        const bool r = mbar_wait(smem_u32(&bar_q_full[qs]), (q_cnt / C::kQSlots) & 1, &abort_flag, a.status);
+        ++q_cnt;
+        tc_fence_after();
+        return r;
+      };
+      // Units follow each other without a gap: S_t of the next unit's first kv
+      // tile is issued right after PV_t of this unit's last one (it overwrites
+      // P_t, which that PV read: in-order execution), so the softmax finds it
+      // ready when it has finished this unit's epilogue.
+      int qslot[NQT];
+      if (nit > 0) {
+        int slotK;
+        for (int t = 0; t < NQT && ok; ++t) ok = wait_q(qslot[t]);
+        if (ok) ok = wait_kv(slotK);
+        if (ok) {
+          const int nt0 = items[0].t1 - items[0].t0 + 1;
+          for (int t = 0; t < NQT; ++t) issue_qk(t, qslot[t], slotK, nt0 == 1);
+          tc_commit(smem_u32(&bar_kv_empty[slotK]));
+        }
+      }
       for (int it = 0; it < nit && ok; ++it) {
         const WorkItem w = items[it];
-        const int n0 = w.t0;
         const int nt = w.t1 - w.t0 + 1;
-        int qslot[NQT];
-        for (int t = 0; t < NQT && ok; ++t, ++q_cnt) {
-          qslot[t] = q_cnt % C::kQSlots;
-          ok = mbar_wait(smem_u32(&bar_q_full[qslot[t]]), (q_cnt / C::kQSlots) & 1, &abort_flag, a.status);
-        }
-        if (!ok) break;
-        tc_fence_after();
-        // S_t = Q_t K^T; the Q slot of head t is released after its last S.
-        auto issue_qk = [&](int t, int slotK, bool last) {
-          const uint32_t d = tmem + t * 128;
-          const uint32_t qt = sQ + qslot[t] * kTileBytes, kt = sKV + slotK * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss(d, kmajor_desc(qt, kk), kmajor_desc(kt, kk), idesc_qk, kk > 0);
-          tc_commit(smem_u32(&bar_s_full[t]));
-          if (last) tc_commit(smem_u32(&bar_q_empty[qslot[t]]));
-        };
-        int slotK;
-        if (!(ok = wait_kv(slotK))) break;
-        for (int t = 0; t < NQT; ++t) issue_qk(t, slotK, nt == 1);
-        tc_commit(smem_u32(&bar_kv_empty[slotK]));
+        const bool has_next = it + 1 < nit;
+        const int nt_next = has_next ? items[it + 1].t1 - items[it + 1].t0 + 1 : 0;
+        int qnext[NQT];
         for (int j = 0; j < nt && ok; ++j) {
           int slotV, slotK2 = -1;
           if (!(ok = wait_kv(slotV))) break;
@@ -236,12 +257,18 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
             if (t == NQT - 1) tc_commit(smem_u32(&bar_kv_empty[slotV]));
             if (j + 1 < nt) {
               if (t == 0 && !(ok = wait_kv(slotK2))) break;
-              issue_qk(t, slotK2, j + 2 == nt);
+              issue_qk(t, qslot[t], slotK2, j + 2 == nt);
+            } else if (has_next) {
+              if (t == 0 && !(ok = wait_kv(slotK2))) break;
+              if (!(ok = wait_q(qnext[t]))) break;
+              issue_qk(t, qnext[t], slotK2, nt_next == 1);
             }
           }
           if (!ok) break;
-          if (j + 1 < nt) tc_commit(smem_u32(&bar_kv_empty[slotK2]));
+          if (slotK2 >= 0) tc_commit(smem_u32(&bar_kv_empty[slotK2]));
         }
+        if (has_next)
+          for (int t = 0; t < NQT; ++t) qslot[t] = qnext[t];
       }
     }
   } else if (warp < 4) {
