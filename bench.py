@@ -57,6 +57,40 @@ def unmasked_pairs(cu: np.ndarray, window: int) -> int:
     return n
 
 
+def algorithmic_bytes(w) -> int:
+    """HBM bytes one step must move at least: the forward reads q, k, v and
+    writes out, lse; the backward reads q, k, v, out, dout, lse, writes dq, dk,
+    dv, and writes then reads D (fp32 [Hq, T])."""
+    T, row_q, row_kv = w.total, w.hq * w.d * 2, w.hkv * w.d * 2
+    stat = 4 * w.hq * T
+    fwd = T * (row_q + 2 * row_kv + row_q) + stat
+    bwd = T * (row_q + 2 * row_kv + 2 * row_q) + stat + T * (row_q + 2 * row_kv) + 2 * stat
+    return fwd + bwd
+
+
+# ex2 results per clock per SM, measured on a GB300 with a microbenchmark of
+# back-to-back independent ex2.approx.f32 instructions.
+MUFU_EX2_PER_CLK_SM = 31.0
+NUM_SMS = 152
+
+
+def roofs(w, pairs: int, ms: float, peak_t: float, peak_hbm: float, sm_mhz) -> dict:
+    """Both roofs for one step: counted tensor FLOPs against the bf16 peak,
+    algorithmic bytes against the HBM copy peak, and the exp count (pairs * Hq
+    in the forward, twice that in the backward) against the ex2 rate."""
+    sec = ms * 1e-3
+    flops = 4.0 * w.d * w.hq * pairs * 3.5
+    nbytes = algorithmic_bytes(w)
+    nexp = 3 * pairs * w.hq
+    mhz = sm_mhz or 2032.0
+    exp_peak = MUFU_EX2_PER_CLK_SM * NUM_SMS * mhz * 1e6
+    return {"tensor": {"achieved_tflops": flops / sec / 1e12, "frac": flops / sec / 1e12 / peak_t},
+            "hbm": {"bytes": nbytes, "achieved_gbs": nbytes / sec / 1e9, "frac": nbytes / sec / 1e9 / peak_hbm},
+            "exp": {"count": nexp, "per_s": nexp / sec, "frac": nexp / sec / exp_peak,
+                    "peak_per_s": exp_peak, "peak_basis": f"{MUFU_EX2_PER_CLK_SM:g} ex2/clk/SM x {NUM_SMS} SMs x {mhz:g} MHz"},
+            "intensity_flop_per_byte": flops / nbytes}
+
+
 def csrc_hash() -> str:
     """sha1 (12 hex digits) of the CUDA sources: *.cu, then *.cuh, then *.h, each sorted."""
     import glob
@@ -259,10 +293,13 @@ def main():
         if evs:
             evs[4].record(stream)
 
-    def step_api(w, t):
-        """One step as a user makes it: the forward call, then the backward call."""
+    def step_api(w, t, mid_ev=None):
+        """One step as a user makes it: the forward call, then the backward call
+        (mid_ev, if given, is recorded between the two)."""
         ms, win, sc = w.context, w.window_left, w.softmax_scale
         binding.attn_varlen_fwd(t["q"], t["k"], t["v"], t["cu"], ms, win, sc, t["out"], t["lse"])
+        if mid_ev is not None:
+            mid_ev.record(stream)
         binding.attn_varlen_bwd(t["dout"], t["q"], t["k"], t["v"], t["out"], t["lse"], t["cu"], ms, win, sc,
                                 t["dq"], t["dk"], t["dv"])
 
@@ -275,7 +312,7 @@ def main():
             step_api(w, t)
             flush.fill_(1.0)
         torch.cuda.synchronize()
-        step_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        step_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
         sampler = ClockSampler(local) if sample_clocks else None
         if sampler:
             sampler.__enter__()
@@ -286,8 +323,8 @@ def main():
         for s in range(steps):
             flush.fill_(float(s))  # L2 flush between steps, outside the events
             step_evs[s][0].record(stream)
-            step_api(w, t)
-            step_evs[s][1].record(stream)
+            step_api(w, t, step_evs[s][1])
+            step_evs[s][2].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
         if sampler:
@@ -306,13 +343,103 @@ def main():
             raise RuntimeError(f"device status word {status}")
         names = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
         per = {n: [] for n in names}
-        tot = [ev[0].elapsed_time(ev[1]) for ev in step_evs]
+        tot = [ev[0].elapsed_time(ev[2]) for ev in step_evs]
+        fwd = [ev[0].elapsed_time(ev[1]) for ev in step_evs]
+        bwd = [ev[1].elapsed_time(ev[2]) for ev in step_evs]
         for ev in evsets:
             for i, n in enumerate(names):
                 per[n].append(ev[i].elapsed_time(ev[i + 1]))
         pairs = unmasked_pairs(inp.cu_seqlens, w.window_left)
-        return {"inp": inp, "t": t, "total_ms": tot, "per_ms": per, "pairs": pairs, "wall_s": wall,
+        return {"inp": inp, "t": t, "total_ms": tot, "fwd_ms": fwd, "bwd_ms": bwd, "per_ms": per, "pairs": pairs,
+                "wall_s": wall,
                 "clocks": sampler.summary() if sampler else None}
+
+    def graph_replay(w, steps, warmup):
+        """The step as a training loop records it (research.dws.rip/llm/kernels,
+        section 06 and Fig. 8): forward + backward captured once in a CUDA graph
+        over a boundary list padded with empty segments to a fixed count (42,
+        or the next multiple of 8 when a batch has more segments), then replayed
+        on three microbatches with different boundaries.  Every batch's replay
+        is compared bit for bit with eager calls on its unpadded boundaries."""
+        seeds = [w.doc_seed + i for i in range(3)]
+        cus = [synth.pack_microbatch(w.total, w.context, sd, w.cap) for sd in seeds]
+        most = max(len(c) - 1 for c in cus)
+        nseg = 42 if most <= 42 else -(-most // 8) * 8
+        batches = []
+        for i, cu in enumerate(cus):
+            inp = synth.make_inputs(cu, w.hq, w.hkv, w.d, tensor_seed=w.tensor_seed + 100 + i)
+            to = lambda bits: torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(dev)  # noqa: E731
+            batches.append({"q": to(inp.q_bits), "k": to(inp.k_bits), "v": to(inp.v_bits), "dout": to(inp.dout_bits),
+                            "cu": torch.from_numpy(cu).to(dev),
+                            "cu_pad": torch.from_numpy(synth.pad_cu_seqlens(cu, nseg)).to(dev),
+                            "pairs": unmasked_pairs(cu, w.window_left)})
+        st = {n: torch.empty_like(batches[0][n]) for n in ("q", "k", "v", "dout", "cu_pad")}
+        st["out"], st["dq"] = torch.empty_like(st["q"]), torch.empty_like(st["q"])
+        st["dk"], st["dv"] = torch.empty_like(st["k"]), torch.empty_like(st["k"])
+        st["lse"] = torch.empty(w.hq, w.total, dtype=torch.float32, device=dev)
+        ms_, win, sc = w.context, w.window_left, w.softmax_scale
+
+        def load(b):
+            for n in ("q", "k", "v", "dout", "cu_pad"):
+                st[n].copy_(b[n])
+
+        def rec():
+            binding.attn_varlen_fwd(st["q"], st["k"], st["v"], st["cu_pad"], ms_, win, sc, st["out"], st["lse"])
+            binding.attn_varlen_bwd(st["dout"], st["q"], st["k"], st["v"], st["out"], st["lse"], st["cu_pad"], ms_,
+                                    win, sc, st["dq"], st["dk"], st["dv"])
+
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        load(batches[0])
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            rec()  # outside capture: the library's per-device set-up happens here
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            rec()
+        bit_exact = True
+        for b in batches:
+            load(b)
+            g.replay()
+            torch.cuda.synchronize()
+            got = [st[n].clone() for n in ("out", "lse", "dq", "dk", "dv")]
+            ref = {"out": torch.empty_like(b["q"]), "dq": torch.empty_like(b["q"]), "dk": torch.empty_like(b["k"]),
+                   "dv": torch.empty_like(b["k"]), "lse": torch.empty_like(st["lse"])}
+            binding.attn_varlen_fwd(b["q"], b["k"], b["v"], b["cu"], ms_, win, sc, ref["out"], ref["lse"])
+            binding.attn_varlen_bwd(b["dout"], b["q"], b["k"], b["v"], ref["out"], ref["lse"], b["cu"], ms_, win, sc,
+                                    ref["dq"], ref["dk"], ref["dv"])
+            torch.cuda.synchronize()
+            for x, n in zip(got, ("out", "lse", "dq", "dk", "dv")):
+                bit_exact = bit_exact and bool(torch.equal(x, ref[n]))
+            del got, ref
+
+        def timed(fn):
+            for i in range(warmup):
+                load(batches[i % 3])
+                fn()
+            torch.cuda.synchronize()
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+            for i in range(steps):
+                load(batches[i % 3])
+                flush.fill_(float(i))
+                evs[i][0].record(stream)
+                fn()
+                evs[i][1].record(stream)
+            torch.cuda.synchronize()
+            return [e[0].elapsed_time(e[1]) for e in evs]
+
+        replay_ms = timed(g.replay)
+        eager_ms = timed(rec)
+        status = binding.attn_varlen_get_status()
+        del g
+        pairs = [b["pairs"] for b in batches]
+        mean_pairs = sum(pairs[i % 3] for i in range(steps)) / steps
+        res = {"ms": statistics.mean(replay_ms), "eager_ms": statistics.mean(eager_ms),
+               "tflops": tflops(w, mean_pairs, statistics.mean(replay_ms)), "pad_segments": nseg,
+               "segments": [len(c) - 1 for c in cus], "doc_seeds": seeds, "bit_exact_vs_eager_unpadded": bit_exact,
+               "status": status}
+        return res
 
     def tflops(w, pairs, ms):
         return 4.0 * w.d * w.hq * pairs * 3.5 / (ms * 1e-3) / 1e12
@@ -377,15 +504,21 @@ def main():
         e2e_times.append(e_s.elapsed_time(e_e))
     e2e_ms = statistics.mean(e2e_times)
 
+    sm_mhz = (main_res["clocks"] or {}).get("sm_mhz")
+    peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    graph_main = graph_replay(wl, args.steps, args.warmup)
     also = {}
     for name in [x for x in args.also.split(",") if x]:
         w2 = wls[name]
         r = measure(w2, max(5, args.steps // 2), 3)
         ms2 = statistics.mean(r["total_ms"])
         also[name] = {"ms": ms2, "tflops": tflops(w2, r["pairs"], ms2), "frac": tflops(w2, r["pairs"], ms2) / peak_t,
+                      "fwd_ms": statistics.mean(r["fwd_ms"]), "bwd_ms": statistics.mean(r["bwd_ms"]),
                       "pairs": r["pairs"], "segments": int(len(r["inp"].cu_seqlens) - 1),
-                      "kernel_ms": {n: statistics.mean(v) for n, v in r["per_ms"].items()}}
+                      "kernel_ms": {n: statistics.mean(v) for n, v in r["per_ms"].items()},
+                      "roofs": roofs(w2, r["pairs"], ms2, peak_t, peak_hbm, sm_mhz)}
         del r
+        also[name]["graph"] = graph_replay(w2, max(6, args.steps // 2), 3)
 
     line = None
     if rank == 0:
@@ -400,7 +533,10 @@ def main():
                        "doc_seed": wl.doc_seed, "tensor_seed": wl.tensor_seed, "unmasked_pairs": main_res["pairs"],
                        "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
             "tflops": tf, "pct_of_bf16_peak": 100.0 * tf / peak_t,
+            "fwd_ms": statistics.mean(main_res["fwd_ms"]), "bwd_ms": statistics.mean(main_res["bwd_ms"]),
             "kernel_ms": kern_ms,
+            "roofs": roofs(wl, main_res["pairs"], step_ms, peak_t, peak_hbm, sm_mhz),
+            "graph": graph_main,
             "roofline": roofline,
             "cpu_baseline": {"value": cpu_ms, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

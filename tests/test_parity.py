@@ -63,17 +63,37 @@ def test_head_ratios(hq, hkv):
         _check_full(inp, window, 0.0884, 400, res)
 
 
-@pytest.mark.parametrize("name", ["ctx512_global", "ctx4096_w512", "ctx4096_global"])
+@pytest.mark.parametrize("window", [-1, 2])
+def test_many_tiny_segments(window):
+    """8,000 segments of 1 to 4 tokens (about 20,000 tokens): more work tiles
+    than the all-thread planner holds, so every kernel takes its single-warp
+    fallback scheduler, and more work units than one persistent CTA per SM
+    can own, so the grids grow past the SM count.  Compared in full."""
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1, 5, size=8000)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    inp = synth.make_inputs(cu, 8, 2, 128, tensor_seed=21)
+    res = run_gpu(inp, window, 1 / np.sqrt(128), 4)
+    _check_full(inp, window, 1 / np.sqrt(128), 4, res)
+
+
+@pytest.mark.parametrize("name", ["ctx512_global", "ctx4096_w512", "ctx4096_global", "long65536_global"])
 def test_full_size_sampled_segments(name):
-    """At the full 16,384-token sizes (the benchmark's launch configuration),
-    the oracle is run on a sample of whole segments (first, last, longest,
-    shortest, and one in the middle); every segment is independent."""
+    """At the full sizes (the benchmark's launch configuration for the
+    16,384-token microbatches; 65,536 tokens with 16/4 heads for the long
+    case), the oracle is run on a sample of whole segments (first, last,
+    longest, shortest, and one in the middle; in the long case the longest
+    segment of at most 2,048 tokens stands in for the longest, to keep the
+    float64 oracle within seconds); every segment is independent."""
     wl = WL[name]
     inp = wl.inputs()
     res = run_gpu(inp, wl.window_left, wl.softmax_scale, wl.context)
     cu = inp.cu_seqlens
     lens = np.diff(cu)
-    picks = sorted({0, len(lens) - 1, int(np.argmax(lens)), int(np.argmin(lens)), len(lens) // 2})
+    cap = 2048 if wl.total > 16384 else wl.total
+    longest = int(np.argmax(np.where(lens <= cap, lens, -1)))
+    picks = sorted({0, len(lens) - 1, longest, int(np.argmin(lens)), len(lens) // 2})
+    picks = [s for s in picks if lens[s] <= cap] or [int(np.argmin(lens))]
     for s in picks:
         a, b = int(cu[s]), int(cu[s + 1])
         sub = segment_slice(inp, a, b)
@@ -97,14 +117,32 @@ def test_full_size_sampled_segments(name):
         assert np.all(np.abs(dv.sum(axis=0) - do_sum) <= 3e-2 * np.linalg.norm(dv, axis=0) + 1e-2)
 
 
-@pytest.mark.parametrize("name", ["tiny_global", "tiny_w64", "ctx512_global", "ctx4096_w512", "ctx4096_global"])
+def _padded(cu: np.ndarray) -> np.ndarray:
+    """cu_seqlens with empty segments at the front, in the middle and at the end."""
+    m = len(cu) // 2
+    return np.concatenate([[0, 0, 0], cu[1:m], [cu[m - 1]] * 2, cu[m:], [cu[-1]] * 5]).astype(np.int32)
+
+
+def _cu_of(name: str) -> tuple:
+    """(workload, cu_seqlens) for a workload name, '+pad' = padded with empty segments."""
+    base = name.removesuffix("+pad")
+    wl = WL[base]
+    cu = wl.cu_seqlens()
+    return wl, (_padded(cu) if name.endswith("+pad") else cu)
+
+
+MASK_CASES = ["tiny_global", "tiny_w64", "tiny_w64+pad", "ctx512_global", "ctx4096_w512", "ctx4096_w512+pad",
+              "ctx4096_global", "ctx4096_global+pad", "long65536_global"]
+
+
+@pytest.mark.parametrize("name", MASK_CASES)
 def test_mask_ranges_bit_exact(name):
     """The kernels' own mask/tile logic, exported by the test hook, against the
-    oracle's visible sets, per query and per key."""
+    oracle's visible sets, per query and per key (plain and padded boundary
+    lists)."""
     import torch
     from varlen_sliding_window_gb300 import binding
-    wl = WL[name]
-    cu = wl.cu_seqlens()
+    wl, cu = _cu_of(name)
     T = int(cu[-1])
     dcu = torch.from_numpy(cu).cuda()
     ranges = torch.empty(3 * T, dtype=torch.int32, device="cuda")
@@ -116,15 +154,16 @@ def test_mask_ranges_bit_exact(name):
     np.testing.assert_array_equal(got, by_key_ranges_from_oracle(cu, wl.window_left, T))
 
 
-@pytest.mark.parametrize("name", ["tiny_w64", "ctx512_global", "ctx4096_w512", "ctx4096_global"])
+@pytest.mark.parametrize("name", MASK_CASES)
 def test_zero_q_counts_visible_keys(name):
     """With q = 0 every visible key has the same logit, so exp(lse) is exactly
-    the number of keys the real forward kernel let each query see."""
-    wl = WL[name]
-    inp = wl.inputs()
+    the number of keys the real forward kernel let each query see (plain and
+    padded boundary lists)."""
+    wl, cu = _cu_of(name)
+    inp = synth.make_inputs(cu, wl.hq, wl.hkv, wl.d, wl.tensor_seed)
     inp.q_bits = np.zeros_like(inp.q_bits)
     res = run_gpu(inp, wl.window_left, wl.softmax_scale, wl.context, backward=False)
-    counts = oracle.visible_ranges(inp.cu_seqlens, wl.window_left, wl.total)[:, 2]
+    counts = oracle.visible_ranges(cu, wl.window_left, wl.total)[:, 2]
     np.testing.assert_array_equal(np.rint(np.exp(res["lse"])).astype(np.int64), np.broadcast_to(counts, res["lse"].shape))
 
 
@@ -182,18 +221,23 @@ def test_repeated_backward_is_bitwise_stable(window):
     assert binding.attn_varlen_get_status() == 0
 
 
-def test_cuda_graph_replay_matches_eager():
-    """Forward + backward captured once in a CUDA graph with a padded boundary
-    list, replayed over three batches with different boundaries, matches eager
-    runs bit for bit (research.dws.rip/llm/kernels, section 06)."""
+@pytest.mark.parametrize("window", [-1, 512])
+def test_cuda_graph_replay_matches_eager(window):
+    """Forward + backward captured once in a CUDA graph with the boundary list
+    padded to 42 segments (research.dws.rip/llm/kernels, section 06 and
+    Fig. 8), replayed over three batches with different boundaries: each replay
+    matches eager runs bit for bit, both on the same padded list and on the
+    unpadded one."""
     import torch
     from varlen_sliding_window_gb300 import binding
     wl = WL["ctx4096_w512"]
-    nseg_pad = 48
+    nseg_pad = 42
     batches = []
     for seed in (0, 1, 2):
-        cu = synth.pad_cu_seqlens(synth.pack_microbatch(16384, 4096, seed), nseg_pad)
-        batches.append((cu, synth.make_inputs(cu, 8, 2, 128, tensor_seed=10 + seed)))
+        cu = synth.pack_microbatch(16384, 4096, seed)
+        assert len(cu) - 1 <= nseg_pad
+        batches.append((cu, synth.pad_cu_seqlens(cu, nseg_pad), synth.make_inputs(cu, 8, 2, 128, tensor_seed=10 + seed)))
+    assert len({len(c) for c, _, _ in batches}) > 1  # the batches differ in their segment counts
     dev = torch.device("cuda")
     q = torch.empty(16384, 8, 128, dtype=torch.bfloat16, device=dev)
     k = torch.empty(16384, 2, 128, dtype=torch.bfloat16, device=dev)
@@ -202,32 +246,42 @@ def test_cuda_graph_replay_matches_eager():
     out, dq = torch.empty_like(q), torch.empty_like(q)
     dk, dv = torch.empty_like(k), torch.empty_like(k)
     lse = torch.empty(8, 16384, dtype=torch.float32, device=dev)
+    outs = (out, lse, dq, dk, dv)
 
-    def load(cu, inp):
-        cu_d.copy_(torch.from_numpy(cu))
+    def load(cu_pad, inp):
+        cu_d.copy_(torch.from_numpy(cu_pad))
         for dst, bits in ((q, inp.q_bits), (k, inp.k_bits), (v, inp.v_bits), (do, inp.dout_bits)):
             dst.copy_(to_device_bf16(bits))
 
-    def step():
-        binding.attn_varlen_fwd(q, k, v, cu_d, 4096, 512, wl.softmax_scale, out, lse)
-        binding.attn_varlen_bwd(do, q, k, v, out, lse, cu_d, 4096, 512, wl.softmax_scale, dq, dk, dv)
+    def step(cu):
+        binding.attn_varlen_fwd(q, k, v, cu, 4096, window, wl.softmax_scale, out, lse)
+        binding.attn_varlen_bwd(do, q, k, v, out, lse, cu, 4096, window, wl.softmax_scale, dq, dk, dv)
 
     s = torch.cuda.Stream()
-    load(*batches[0])
+    load(*batches[0][1:])
+    torch.cuda.synchronize()
     with torch.cuda.stream(s):
-        step()  # warm-up (allocator pool, function attributes) outside capture
+        step(cu_d)  # warm-up (allocator pool, function attributes) outside capture
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        step()
-    for cu, inp in batches:
-        load(cu, inp)
+        step(cu_d)
+    for cu, cu_pad, inp in batches:
+        load(cu_pad, inp)
         torch.cuda.synchronize()
         g.replay()
         torch.cuda.synchronize()
-        replayed = [t.clone() for t in (out, lse, dq, dk, dv)]
-        step()
+        replayed = [t.clone() for t in outs]
+        for t in outs:
+            t.fill_(float("nan"))
+        step(cu_d)
         torch.cuda.synchronize()
-        for x, y in zip(replayed, (out, lse, dq, dk, dv)):
+        for x, y in zip(replayed, outs):
+            assert torch.equal(x, y)
+        for t in outs:
+            t.fill_(float("nan"))
+        step(torch.from_numpy(cu).to(dev))
+        torch.cuda.synchronize()
+        for x, y in zip(replayed, outs):
             assert torch.equal(x, y)
     assert binding.attn_varlen_get_status() == 0
