@@ -35,7 +35,7 @@ constexpr int kPlanDoesNotFit = -2;
 // Shared-memory ints plan_schedule needs for nseg segments, G CTAs and
 // `threads` threads (upper bounds for the item and chunk arrays).
 __host__ __device__ constexpr int plan_scratch_ints(int nseg, int G, int threads) {
-  return 2 * (nseg + 1) + 3 * (kPlanMaxItems + 1) + kPlanMaxChunks + kCostBuckets + 64;
+  return 2 * (nseg + 1) + 2 * (kPlanMaxItems + 1) + kPlanMaxChunks + kCostBuckets + 64;
 }
 
 namespace plan_detail {
@@ -87,6 +87,28 @@ __device__ __forceinline__ int block_sum(int x, int* tmp) {
   return s;
 }
 
+// Sum of x and maximum of y over the block in one pass.  `tmp` holds at
+// least 2 * threads/32 ints.
+__device__ __forceinline__ void block_sum_max(int x, int y, int* tmp, int& sum, int& mx) {
+  for (int o = 16; o > 0; o >>= 1) {
+    x += __shfl_xor_sync(0xffffffffu, x, o);
+    y = max(y, __shfl_xor_sync(0xffffffffu, y, o));
+  }
+  const int nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    tmp[threadIdx.x >> 5] = x;
+    tmp[nw + (threadIdx.x >> 5)] = y;
+  }
+  __syncthreads();
+  sum = 0;
+  mx = 0;
+  for (int w = 0; w < nw; ++w) {
+    sum += tmp[w];
+    mx = max(mx, tmp[nw + w]);
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ int block_max(int x, int* tmp) {
   for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, o));
   if ((threadIdx.x & 31) == 0) tmp[threadIdx.x >> 5] = x;
@@ -125,21 +147,45 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
   int* s_cu = scratch;                          // [nseg + 1]
   int* s_tiles = s_cu + (nseg + 1);             // [nseg + 1] tile prefix
   int* s_cost = s_tiles + (nseg + 1);           // [kPlanMaxItems + 1]
-  int* s_cbase = s_cost + (kPlanMaxItems + 1);  // chunk prefix
-  int* s_sbase = s_cbase + (kPlanMaxItems + 1); // split-item prefix
+  int* s_sbase = s_cost + (kPlanMaxItems + 1);  // split-item prefix
   int* s_order = s_sbase + (kPlanMaxItems + 1); // [kPlanMaxChunks] item | chunk << 16
   int* s_base = s_order + kPlanMaxChunks;       // [kCostBuckets] size histogram, then bucket cursors
   int* s_misc = s_base + kCostBuckets;          // [64]: scan scratch
 
-  // ---- 1. boundaries and the tile prefix over segments
+  // ---- 1. boundaries and the tile prefix over segments (one warp while
+  // that takes at most 32 segments per lane: fewer barriers)
   for (int s = tid; s <= nseg; s += nt) s_cu[s] = cu_seqlens[s];
   __syncthreads();
-  for (int s = tid; s < nseg; s += nt) s_tiles[s] = num_tiles(s_cu[s + 1] - s_cu[s]);
-  __syncthreads();
-  const int n_items = block_exclusive_scan(s_tiles, nseg, s_misc);
+  int n_items;
+  if (nseg <= 32 * 32) {
+    if (warp == 0) {
+      const int per = (nseg + 31) / 32;
+      const int b0 = min(nseg, lane * per), b1 = min(nseg, b0 + per);
+      int sum = 0;
+      for (int s = b0; s < b1; ++s) sum += num_tiles(s_cu[s + 1] - s_cu[s]);
+      int incl = sum;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int acc = incl - sum;
+      for (int s = b0; s < b1; ++s) {
+        const int x = num_tiles(s_cu[s + 1] - s_cu[s]);
+        s_tiles[s] = acc;
+        acc += x;
+      }
+      if (lane == 31) s_tiles[nseg] = incl;
+    }
+    __syncthreads();
+    n_items = s_tiles[nseg];
+  } else {
+    for (int s = tid; s < nseg; s += nt) s_tiles[s] = num_tiles(s_cu[s + 1] - s_cu[s]);
+    __syncthreads();
+    n_items = block_exclusive_scan(s_tiles, nseg, s_misc);
+    if (tid == 0) s_tiles[nseg] = n_items;
+    __syncthreads();
+  }
   if (n_items > kPlanMaxItems) return kPlanDoesNotFit;
-  if (tid == 0) s_tiles[nseg] = n_items;
-  __syncthreads();
   // ---- 2. cost (streamed tiles) of every item
   int my_total = 0, my_max = 0;
   for (int e = tid; e < n_items; e += nt) {
@@ -157,8 +203,8 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
     my_total += c;
     my_max = max(my_max, c);
   }
-  const int total_cost = block_sum(my_total, s_misc);
-  const int max_cost = block_max(my_max, s_misc);
+  int total_cost, max_cost;
+  block_sum_max(my_total, my_max, s_misc, total_cost, max_cost);
   // ---- 3. split limit C (streamed tiles per chunk), as in sched.cuh
   int C = 0x7fffffff;
   if (chains_max > 0) {
@@ -173,16 +219,17 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
     }
     if (C >= max_cost) C = 0x7fffffff;
   }
-  // ---- 4. chunks per item and split items (prefix sums)
+  // ---- 4. chunks per item; split items get consecutive chain slots (a
+  // prefix sum, only when something is split)
+  int my_chunks = 0;
   for (int e = tid; e < n_items; e += nt) {
     const int c = s_cost[e];
     const int k = c == 0 ? 0 : (c <= C ? 1 : (c + C - 1) / C);
-    s_cbase[e] = k;
-    s_sbase[e] = k > 1;
+    my_chunks += k;
+    if (C != 0x7fffffff) s_sbase[e] = k > 1;
   }
-  __syncthreads();
-  const int n_chunks = block_exclusive_scan(s_cbase, n_items, s_misc);
-  block_exclusive_scan(s_sbase, n_items, s_misc);
+  const int n_chunks = block_sum(my_chunks, s_misc);
+  if (C != 0x7fffffff) block_exclusive_scan(s_sbase, n_items, s_misc);
   if (n_chunks > kPlanMaxChunks) return kPlanDoesNotFit;
   // ---- 5. stable counting sort of the chunks by size, largest first.  Equal
   // sizes keep the order (group of 32 items, chunk index, item): of the orders
@@ -196,10 +243,20 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
   };
   for (int b = tid; b < kCostBuckets; b += nt) s_base[b] = 0;
   __syncthreads();
-  for (int e = tid; e < n_items; e += nt) {
-    int k, base, rem;
-    chunk_of(e, k, base, rem);
-    for (int i = 0; i < k; ++i) atomicAdd(&s_base[bucket_of(base + (i < rem ? 1 : 0))], 1);
+  // Histogram: lanes with the same bucket add once (most items share a few
+  // sizes, and one shared-memory atomic per item would serialise on them).
+  for (int e0 = tid - lane; e0 < n_items; e0 += nt) {
+    const int e = e0 + lane;
+    int k = 0, base = 0, rem = 0;
+    if (e < n_items) chunk_of(e, k, base, rem);
+    int kmax = k;
+    for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    for (int i = 0; i < kmax; ++i) {
+      const bool has = i < k;
+      const int bk = has ? bucket_of(base + (i < rem ? 1 : 0)) : -1;
+      const unsigned same = __match_any_sync(0xffffffffu, bk);
+      if (has && lane == __ffs(same) - 1) atomicAdd(&s_base[bk], __popc(same));
+    }
   }
   __syncthreads();
   if (warp == 0) {
