@@ -214,6 +214,7 @@ int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, con
   b.p.chain_progress = nullptr;
   b.p.chains_max = 0;
   b.p.dq_after_dkdv = 0;
+  b.p.dkdv_after_pre = 0;
   b.p.dq = dq;
   b.p.dk = dk;
   b.p.dv = dv;
@@ -239,7 +240,9 @@ int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* 
   if (cudaMallocFromPoolAsync(&ws, ws_bytes, b.dev->pool, s) != cudaSuccess) return ATTN_ERR_ALLOC;
   carve_workspace(ws, ws_bytes, total, num_heads_q, b.p);
   int lr = launch_bwd_preprocess(b.p, s);
+  b.p.dkdv_after_pre = 1;
   if (!lr) lr = launch_bwd_dkdv(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, s);
+  b.p.dkdv_after_pre = 0;
   b.p.dq_after_dkdv = 1;
   if (!lr) lr = launch_bwd_dq(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, s);
   const cudaError_t fr = cudaFreeAsync(ws, s);

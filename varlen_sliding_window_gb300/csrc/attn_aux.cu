@@ -24,6 +24,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __rest
                                                              float* __restrict__ delta, int total, int hq,
                                                              int* __restrict__ chain_progress, int nprogress) {
   grid_dependency_wait();
+  // Everything before this kernel is complete: the next kernel may start
+  // (it waits for this one before reading what it writes).
+  grid_dependents_launch();
   // The dK/dV pass that follows counts published chain links from zero.
   if (blockIdx.x == 0)
     for (int e = threadIdx.x; e < nprogress; e += blockDim.x) chain_progress[e] = 0;

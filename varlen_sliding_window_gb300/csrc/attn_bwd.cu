@@ -173,7 +173,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  grid_dependency_wait();  // inputs written by earlier kernels are read after this
+  // Inputs written by earlier kernels are read after the wait.  Right after
+  // this backward's own preprocess (which lets this grid start once it has
+  // waited for everything before it), the planner only reads cu_seqlens,
+  // which is complete by then, so the wait comes after planning.
+  if (!p.dkdv_after_pre) grid_dependency_wait();
   const int planned = plan_schedule<true>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hkv, p.chains_max, items,
                                           kBwdMaxItems, reinterpret_cast<int*>(gbase), (int)(C::kAugOff / 4),
                                           blockIdx.x, gridDim.x);
@@ -193,6 +197,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     n_items = planned < 0 ? 0 : planned;
     if (planned < 0) atomicExch(a.status, 2);
   }
+  if (p.dkdv_after_pre) grid_dependency_wait();
   // Extra k-step blocks (after the planner, whose scratch ends at kAugOff):
   // the ones block gets 1.0 in columns 0 and 1 of every row, the per-stage
   // blocks start at zero and only their columns 0 and 1 change later.

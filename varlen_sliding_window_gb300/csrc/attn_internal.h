@@ -46,6 +46,9 @@ struct BwdParams {
   // same backward: it then needs nothing that kernel writes, starts on the
   // SMs the dK/dV kernel frees and waits for it only before exiting.
   int dq_after_dkdv;
+  // Set when the dK/dV kernel is launched right after the preprocess of the
+  // same backward: it plans before waiting for that kernel.
+  int dkdv_after_pre;
 };
 
 // Backward workspace layout: delta, chain progress counters, chain buffers.
