@@ -484,7 +484,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // chunks in chunk order (fp32, through the chain buffer), then
         // either pass the running sum on or, as the last chunk, store it.
         const int li = link_index(w), lk = link_count(w);
-        float* buf = p.chains + ((size_t)w.chain * 2 + x) * (128 * 128) + (size_t)row * 128;
+        // Buffer layout [32 groups of 4 columns][128 rows][4]: a warp's 32 rows
+        // read or write 512 contiguous bytes per group (coalesced).
+        float* buf = p.chains + ((size_t)w.chain * 2 + x) * (128 * 128) + (size_t)row * 4;
         int* prog = p.chain_progress + w.chain * 2 + x;
         if (li > 0 && !(ok = wait_flag_at_least(prog, li, &abort_flag, a.status))) break;
 #pragma unroll
@@ -495,7 +497,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (li > 0) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
-              const float4 prev = __ldcg(reinterpret_cast<const float4*>(buf + c * 32 + e));
+              const float4 prev = __ldcg(reinterpret_cast<const float4*>(buf + ((c * 32 + e) >> 2) * 512));
               r[e + 0] = __float_as_uint(__uint_as_float(r[e + 0]) + prev.x);
               r[e + 1] = __float_as_uint(__uint_as_float(r[e + 1]) + prev.y);
               r[e + 2] = __float_as_uint(__uint_as_float(r[e + 2]) + prev.z);
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           } else {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-              __stcg(reinterpret_cast<float4*>(buf + c * 32 + e),
+              __stcg(reinterpret_cast<float4*>(buf + ((c * 32 + e) >> 2) * 512),
                      make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
                                  __uint_as_float(r[e + 3])));
           }
