@@ -46,20 +46,6 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Writes 32 fp32 accumulator columns of one row, scaled, as bf16 to global.
-__device__ __forceinline__ void store_row32_bf16(void* dst_row, int c, const uint32_t (&r)[32], float mul) {
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst_row) + c);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    uint4 pk;
-    pk.x = pack_bf16x2(__uint_as_float(r[v * 8 + 0]) * mul, __uint_as_float(r[v * 8 + 1]) * mul);
-    pk.y = pack_bf16x2(__uint_as_float(r[v * 8 + 2]) * mul, __uint_as_float(r[v * 8 + 3]) * mul);
-    pk.z = pack_bf16x2(__uint_as_float(r[v * 8 + 4]) * mul, __uint_as_float(r[v * 8 + 5]) * mul);
-    pk.w = pack_bf16x2(__uint_as_float(r[v * 8 + 6]) * mul, __uint_as_float(r[v * 8 + 7]) * mul);
-    dst[v] = pk;
-  }
-}
-
 // One TMEM load of 64 consecutive columns (two x32 loads, one wait).
 __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]) {
   uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
@@ -410,7 +396,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int q0 = w.seg_lo + b * kTile + 64 * x;  // first query of this half
         const bool full = tile_fully_visible_kv(k0, w.seg_lo + b * kTile, w.seg_hi, a.window);
         for (int hh = 0; hh < a.group; ++hh) {
-          if (!(ok = mbar_wait(smem_u32(&bar_s_full[0]), cnt & 1, &abort_flag, a.status))) break;
+          if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[0]), cnt & 1, &abort_flag, a.status))) break;
           tc_fence_after();
           int c_lo = 0, c_hi = 63;
           if (!full) col_visible_rows(j, q0, w.seg_hi, a.window, c_lo, c_hi);
@@ -442,7 +428,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_arrive(smem_u32(&bar_p_full[x]));
           }
           // dS^T = P (dP - D) once dP^T is there (the MMA subtracted D).
-          if (!(ok = mbar_wait(smem_u32(&bar_s_full[1]), cnt & 1, &abort_flag, a.status))) break;
+          if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[1]), cnt & 1, &abort_flag, a.status))) break;
           tc_fence_after();
           {
             uint32_t dr[64];
@@ -465,7 +451,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (x scale).
-      if (!(ok = mbar_wait(smem_u32(&bar_acc_full), it & 1, &abort_flag, a.status))) break;
+      if (!(ok = mbar_wait_warp(smem_u32(&bar_acc_full), it & 1, &abort_flag, a.status))) break;
       tc_fence_after();
       const bool valid = j < w.seg_hi && token_in_range(j, a.total);
       void* dst_row = static_cast<__nv_bfloat16*>(x == 0 ? p.dv : p.dk) + ((size_t)j * a.hkv + g) * kHeadDim;
@@ -477,7 +463,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t r[32];
           tmem_ld32(tacc + c * 32, r);
           tmem_wait_ld(r);
-          if (valid) store_row32_bf16(dst_row, c * 32, r, mul);
+          store_rows32_bf16(dst_row, (long long)a.hkv * kHeadDim * 2, c * 32, r, mul, valid);
         }
       } else {
         // A chunk of a split kv item: add the partial sums of the earlier
@@ -488,7 +474,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // read or write 512 contiguous bytes per group (coalesced).
         float* buf = p.chains + ((size_t)w.chain * 2 + x) * (128 * 128) + (size_t)row * 4;
         int* prog = p.chain_progress + w.chain * 2 + x;
-        if (li > 0 && !(ok = wait_flag_at_least(prog, li, &abort_flag, a.status))) break;
+        if (li > 0 && !(ok = __all_sync(0xffffffffu, wait_flag_at_least(prog, li, &abort_flag, a.status)))) break;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
@@ -505,7 +491,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
           }
           if (li == lk - 1) {
-            if (valid) store_row32_bf16(dst_row, c * 32, r, mul);
+            store_rows32_bf16(dst_row, (long long)a.hkv * kHeadDim * 2, c * 32, r, mul, valid);
           } else {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
@@ -518,7 +504,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // Publish once every row of this warpgroup has written its part.
           __threadfence();
           mbar_arrive(smem_u32(&bar_chain[x]));
-          if (!(ok = mbar_wait(smem_u32(&bar_chain[x]), chain_uses & 1, &abort_flag, a.status))) break;
+          if (!(ok = mbar_wait_warp(smem_u32(&bar_chain[x]), chain_uses & 1, &abort_flag, a.status))) break;
           ++chain_uses;
           if (row == 0) store_release(prog, li + 1);
         }
@@ -807,8 +793,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int kt0 = w.seg_lo + n * kTile;
         const uint32_t tS = lane_base + 128 * (c & 1) + 64 * x;
         const uint32_t tDP = lane_base + C::kColDP + 64 * x;
-        if (!(ok = mbar_wait(smem_u32(&bar_s_full[c & 1]), (c >> 1) & 1, &abort_flag, a.status))) break;
-        if (!(ok = mbar_wait(smem_u32(&bar_dp_full), c & 1, &abort_flag, a.status))) break;
+        if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[c & 1]), (c >> 1) & 1, &abort_flag, a.status))) break;
+        if (!(ok = mbar_wait_warp(smem_u32(&bar_dp_full), c & 1, &abort_flag, a.status))) break;
         tc_fence_after();
         uint32_t sr[64], dr[64];
         tmem_ld64_wait(tS, sr);
@@ -849,7 +835,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: warpgroup x writes dQ columns [64x, 64x + 64) (x scale).
-      if (!(ok = mbar_wait(smem_u32(&bar_acc_full), it & 1, &abort_flag, a.status))) break;
+      if (!(ok = mbar_wait_warp(smem_u32(&bar_acc_full), it & 1, &abort_flag, a.status))) break;
       tc_fence_after();
       void* dq_row = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)i * a.hq + h) * kHeadDim;
 #pragma unroll
@@ -857,7 +843,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t r[32];
         tmem_ld32(lane_base + C::kColDQ + 64 * x + cc * 32, r);
         tmem_wait_ld(r);
-        if (valid) store_row32_bf16(dq_row, 64 * x + cc * 32, r, a.scale);
+        store_rows32_bf16(dq_row, (long long)a.hq * kHeadDim * 2, 64 * x + cc * 32, r, a.scale, valid);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_acc_empty));

@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j) {
         const int k0 = w.seg_lo + (n0 + j) * kTile;
-        if (!(ok = mbar_wait(smem_u32(&bar_s_full[t]), s_cnt & 1, &abort_flag, a.status))) break;
+        if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[t]), s_cnt & 1, &abort_flag, a.status))) break;
         ++s_cnt;
         tc_fence_after();
         uint32_t sr[128];
@@ -380,28 +380,17 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: O / l -> out (bf16), lse
-      if (!(ok = mbar_wait(smem_u32(&bar_o_done[t]), it & 1, &abort_flag, a.status))) break;
+      if (!(ok = mbar_wait_warp(smem_u32(&bar_o_done[t]), it & 1, &abort_flag, a.status))) break;
       tc_fence_after();
       const bool valid = i < w.seg_hi && token_in_range(i, a.total);
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                            ((size_t)i * a.hq + h) * kHeadDim);
+      void* out_row = static_cast<__nv_bfloat16*>(p.out) + ((size_t)i * a.hq + h) * kHeadDim;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tmem_ld32(tO + c * 32, r);
         tmem_wait_ld(r);
-        if (valid) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 pk;
-            pk.x = pack_bf16x2(__uint_as_float(r[v * 8 + 0]) * inv_l, __uint_as_float(r[v * 8 + 1]) * inv_l);
-            pk.y = pack_bf16x2(__uint_as_float(r[v * 8 + 2]) * inv_l, __uint_as_float(r[v * 8 + 3]) * inv_l);
-            pk.z = pack_bf16x2(__uint_as_float(r[v * 8 + 4]) * inv_l, __uint_as_float(r[v * 8 + 5]) * inv_l);
-            pk.w = pack_bf16x2(__uint_as_float(r[v * 8 + 6]) * inv_l, __uint_as_float(r[v * 8 + 7]) * inv_l);
-            dst[c * 4 + v] = pk;
-          }
-        }
+        store_rows32_bf16(out_row, (long long)a.hq * kHeadDim * 2, c * 32, r, inv_l, valid);
       }
       if (valid) p.lse[(size_t)h * a.total + i] = (m + __log2f(l)) * 0.69314718055994531f;
       tc_fence_before();

@@ -78,6 +78,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// mbar_wait by every lane of a warp, with one answer for the whole warp
+// (false if any lane gave up): a timeout never splits a warp, so the warp's
+// later shuffles and votes (which name all 32 lanes) cannot wait on a lane
+// that has left the loop.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               int* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
+}
+
 // Programmatic dependent launch: wait until the preceding kernel in the
 // stream has completed and its memory is visible (a no-op when the kernel
 // was launched without the programmatic-serialization attribute).

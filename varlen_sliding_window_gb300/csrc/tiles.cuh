@@ -28,6 +28,54 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
   return make_sdesc_sw128(tile + kk * 16 * 128, kHalfTile, 1024);
 }
 
+// Writes fp32 columns [c, c + 32) of the warp's 32 rows (one row per lane,
+// lane l's row at dst_row; consecutive lanes hold consecutive tokens,
+// row_stride_bytes apart), times mul, as bf16.  Each quad of lanes first
+// swaps 16-byte pieces (a 4 x 4 transpose in two shuffle rounds), so that a
+// store instruction writes 64 contiguous bytes of each of 8 rows rather
+// than 16 bytes of each of 32 rows: a quarter of the cache lines per
+// instruction.  All 32 lanes call it; rows with valid == false are skipped.
+__device__ __forceinline__ void store_rows32_bf16(void* dst_row, long long row_stride_bytes, int c,
+                                                  const uint32_t (&r)[32], float mul, bool valid) {
+  const int lane = threadIdx.x & 31, qi = lane & 3;
+  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+  uint32_t x[4][4];  // x[v][k]: word v of 16-byte piece k of this lane's row
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      x[v][k] = pack_bf16x2(__uint_as_float(r[8 * k + 2 * v]) * mul, __uint_as_float(r[8 * k + 2 * v + 1]) * mul);
+  // Round 1 (lane bit 0), round 2 (lane bit 1): a lane keeps the pieces whose
+  // index bit equals its own lane bit and trades the others with its partner.
+  // Afterwards piece k of lane qi is piece qi of quad lane k's row.
+  const bool odd = qi & 1, high = qi & 2;
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? x[v][2 * b] : x[v][2 * b + 1], 1);
+      if (odd)
+        x[v][2 * b] = got;
+      else
+        x[v][2 * b + 1] = got;
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const uint32_t got = __shfl_xor_sync(0xffffffffu, high ? x[v][b] : x[v][b + 2], 2);
+      if (high)
+        x[v][b] = got;
+      else
+        x[v][b + 2] = got;
+    }
+  }
+  char* mine = static_cast<char*>(dst_row) + 2 * (c + 8 * qi);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    if ((vmask >> ((lane & ~3) + k)) & 1u)
+      *reinterpret_cast<uint4*>(mine + (long long)(k - qi) * row_stride_bytes) =
+          make_uint4(x[0][k], x[1][k], x[2][k], x[3][k]);
+}
+
 // One extra k-step of 16 columns appended to a K-major operand: 128 rows x
 // 16 bf16 (32 bytes per row) with the 32-byte swizzle, 8-row groups 256 bytes
 // apart.  Used to fold a per-row term into an MMA (row x 1 + term x 1).
