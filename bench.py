@@ -441,6 +441,66 @@ def main():
                "status": status}
         return res
 
+    def layer_leg(w, steps, warmup):
+        """One attention layer around the kernels (QKV projection, attention on
+        strided views of the fused projection output, output projection,
+        loss = sum(y * g), and the whole backward), as the page's Fig. 8 times
+        it: eager steps against one CUDA graph replayed, on three microbatches
+        with boundaries padded to a fixed count.  The replay is checked bit
+        for bit against an eager step on the last batch."""
+        from varlen_sliding_window_gb300.layer import AttentionLayer
+        cus = [synth.pack_microbatch(w.total, w.context, w.doc_seed + i, w.cap) for i in range(3)]
+        most = max(len(c) - 1 for c in cus)
+        nseg = 42 if most <= 42 else -(-most // 8) * 8
+        d_model = w.hq * w.d
+        lay = AttentionLayer(w.total, d_model, w.hq, w.hkv, w.context, w.window_left, nseg, seed=w.tensor_seed)
+        gen = torch.Generator(device="cpu").manual_seed(w.tensor_seed + 7)
+        lay.x.copy_(torch.randn(w.total, d_model, generator=gen).to(torch.bfloat16))
+        lay.g.copy_(torch.randn(w.total, d_model, generator=gen).to(torch.bfloat16))
+        pads = [torch.from_numpy(synth.pad_cu_seqlens(c, nseg)).to(dev) for c in cus]
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        lay.cu.copy_(pads[0])
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            lay.step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            lay.step()
+
+        def timed(fn):
+            for i in range(warmup):
+                lay.cu.copy_(pads[i % 3])
+                fn()
+            torch.cuda.synchronize()
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+            for i in range(steps):
+                lay.cu.copy_(pads[i % 3])
+                flush.fill_(float(i))
+                evs[i][0].record(stream)
+                fn()
+                evs[i][1].record(stream)
+            torch.cuda.synchronize()
+            return statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+
+        eager_ms = timed(lay.step)
+        graph_ms = timed(graph.replay)
+        lay.cu.copy_(pads[2])
+        graph.replay()
+        torch.cuda.synchronize()
+        names = ("qkv", "out", "lse", "y", "loss", "d_out", "d_qkv", "dw_qkv", "dw_o", "dx")
+        got = {n: getattr(lay, n).clone() for n in names}
+        lay.step()
+        torch.cuda.synchronize()
+        exact = all(torch.equal(got[n], getattr(lay, n)) for n in names)
+        gemm_flops = 2.0 * w.total * d_model * ((w.hq + 2 * w.hkv) * w.d) * 3 + 2.0 * w.total * w.hq * w.d * d_model * 3
+        del graph, lay
+        return {"eager_ms": eager_ms, "graph_ms": graph_ms, "d_model": d_model, "pad_segments": nseg,
+                "projection_gflop": gemm_flops / 1e9, "bit_exact_replay_vs_eager": exact,
+                "what": "x@W_qkv, attention on strided views of qkv, @W_o, loss=sum(y*g), full backward "
+                        "(dW_qkv, dW_o, dx); projections via torch.matmul (cuBLAS)"}
+
     def tflops(w, pairs, ms):
         return 4.0 * w.d * w.hq * pairs * 3.5 / (ms * 1e-3) / 1e12
 
@@ -558,6 +618,7 @@ def main():
     sm_mhz = (main_res["clocks"] or {}).get("sm_mhz")
     peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     graph_main = graph_replay(wl, args.steps, args.warmup)
+    layer_main = layer_leg(wl, args.steps, args.warmup)
     also = {}
     for name in [x for x in args.also.split(",") if x]:
         w2 = wls[name]
@@ -588,6 +649,7 @@ def main():
             "kernel_ms": kern_ms,
             "roofs": roofs(wl, main_res["pairs"], step_ms, peak_t, peak_hbm, sm_mhz),
             "graph": graph_main,
+            "layer": layer_main,
             "roofline": roofline,
             "cpu_baseline": {"value": cpu_ms, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -77,6 +77,7 @@ extern "C" {
 #define ATTN_ERR_DEVICE_STATUS (-12) /* attn_varlen_get_status: a kernel reported an error */
 #define ATTN_ERR_NOALLOC_TOO_LARGE (-13) /* attn_varlen_bwd_noalloc: T * Hq above its fixed scratch (2,097,152) */
 #define ATTN_ERR_WORKSPACE (-14)     /* workspace below its minimum size or not 256-byte aligned */
+#define ATTN_ERR_STRIDE (-15)        /* *_strided: a stride pair that is not a valid [T, H, 128] view */
 
 /*
  * Forward.  Writes out [T, Hq, 128] (bf16) and lse [Hq, T] (float32).
@@ -127,6 +128,37 @@ int attn_varlen_bwd_noalloc(const void* dout, const void* q, const void* k, cons
                             const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
                             float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
                             int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream);
+
+/*
+ * The forward and backward on strided views, so that a layer can hand over
+ * its tensors as they come out of its projections and take the gradients
+ * straight into its own buffers (research.dws.rip/llm/kernels, section 06 and
+ * Fig. 8: one attention layer with its projections and a small loss, replayed
+ * as a CUDA graph).  For example q, k and v can be the three head ranges of
+ * one fused [T, Hq + 2 Hkv, 128] projection output, and dq, dk, dv the same
+ * ranges of its gradient.
+ *
+ * Same arguments and results as attn_varlen_fwd / attn_varlen_bwd, plus
+ * `strides`: host int64 pairs (token stride, head stride) in elements, one
+ * pair per [T, H, 128] tensor, in the order
+ *     forward:  q, k, v, out                          (8 values)
+ *     backward: dout, q, k, v, out, dq, dk, dv        (16 values)
+ * Element (t, h, c) of a tensor lives at base + t * token + h * head + c.
+ * Each stride is a positive multiple of 8 elements (16 bytes), head >= 128,
+ * token >= head * H; otherwise the call returns ATTN_ERR_STRIDE before
+ * enqueueing anything.  Output views must not overlap each other or the
+ * inputs.  lse stays a dense float32 [Hq, T].  The array is read during the
+ * call only.
+ */
+int attn_varlen_fwd_strided(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                            int32_t max_seqlen, int32_t window_left, float softmax_scale, void* out, float* lse,
+                            int64_t total, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
+                            int32_t num_segments, const int64_t* strides, void* stream);
+int attn_varlen_bwd_strided(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                            const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                            float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
+                            int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, const int64_t* strides,
+                            void* stream);
 
 /* Bytes of scratch the backward takes from the stream-ordered allocator:
  * D (T * Hq floats, 256-byte padded) plus 40 MiB of chain buffers. */

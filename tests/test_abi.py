@@ -67,6 +67,35 @@ def test_argument_validation(clib):
     assert _fwd(clib, max_seqlen=-1) == -7
 
 
+def test_strided_calls_check_their_strides(clib):
+    # Rejected before any CUDA call: no GPU needed.
+    vp = ctypes.c_void_p
+    fake = vp(256)
+
+    def fwd(strides):
+        arr = None if strides is None else (ctypes.c_int64 * 8)(*strides)
+        return clib.attn_varlen_fwd_strided(fake, fake, fake, fake, 4, -1, 0.088, fake, fake, 4, 8, 2, 128, 1,
+                                            vp(None) if arr is None else ctypes.cast(arr, vp), vp(None))
+    fused = [20 * 128, 128, 20 * 128, 128, 20 * 128, 128, 8 * 128, 128]  # q, k, v from one [T, 20, 128] buffer
+    bad_cases = [
+        [20 * 128, 100, 20 * 128, 128, 20 * 128, 128, 8 * 128, 128],  # head step below 128
+        [20 * 128 + 4, 128, 20 * 128, 128, 20 * 128, 128, 8 * 128, 128],  # not a multiple of 8 elements
+        [7 * 128, 128, 20 * 128, 128, 20 * 128, 128, 8 * 128, 128],  # token step below 8 heads x 128
+        [0, 128, 20 * 128, 128, 20 * 128, 128, 8 * 128, 128],
+        [20 * 128, 128, 20 * 128, 128, 20 * 128, 128, 8 * 128, -128],
+    ]
+    for bad in bad_cases:
+        assert fwd(bad) == -15, bad
+    assert fwd(None) == -1
+    assert b"stride" in clib.attn_varlen_strerror(-15)
+    # Valid strides get past the stride check (and fail later on the fake
+    # pointers' alignment: 256 is aligned, so use a misaligned q instead).
+    arr = (ctypes.c_int64 * 8)(*fused)
+    rc = clib.attn_varlen_fwd_strided(vp(257), fake, fake, fake, 4, -1, 0.088, fake, fake, 4, 8, 2, 128, 1,
+                                      ctypes.cast(arr, vp), vp(None))
+    assert rc == -4
+
+
 def test_workspace_bytes(clib):
     clib.attn_varlen_bwd_workspace_bytes.restype = ctypes.c_size_t
     clib.attn_varlen_bwd_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]

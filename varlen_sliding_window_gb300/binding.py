@@ -53,6 +53,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.attn_varlen_bwd_dkdv.restype = ctypes.c_int
     lib.attn_varlen_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, sz, vp, i32, i32, f32, vp, i64, i32, i32, i32, i32, vp]
     lib.attn_varlen_bwd_dq.restype = ctypes.c_int
+    lib.attn_varlen_fwd_strided.argtypes = lib.attn_varlen_fwd.argtypes[:-1] + [vp, vp]
+    lib.attn_varlen_fwd_strided.restype = ctypes.c_int
+    lib.attn_varlen_bwd_strided.argtypes = lib.attn_varlen_bwd.argtypes[:-1] + [vp, vp]
+    lib.attn_varlen_bwd_strided.restype = ctypes.c_int
     lib.attn_varlen_bwd_noalloc.argtypes = lib.attn_varlen_bwd.argtypes
     lib.attn_varlen_bwd_noalloc.restype = ctypes.c_int
     lib.attn_varlen_mask_ranges.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp]
@@ -87,9 +91,33 @@ def _dims(q, k, cu_seqlens):
     return int(total), int(hq), int(hkv), int(d), int(cu_seqlens.numel()) - 1
 
 
+def _strides(*tensors):
+    """(token, head) element strides of [T, H, 128] views, as the int64 array the
+    *_strided calls take; the last dimension must be contiguous."""
+    vals = []
+    for t in tensors:
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError("expected a [T, H, 128] tensor with a contiguous last dimension")
+        vals += [int(t.stride(0)), int(t.stride(1))]
+    return (ctypes.c_int64 * len(vals))(*vals)
+
+
+def _dense(*tensors) -> bool:
+    return all(t.is_contiguous() for t in tensors)
+
+
+def _check_lse(lse):
+    if not lse.is_contiguous():
+        raise ValueError("lse must be a dense float32 [Hq, T] tensor")
+
+
 def attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen: int, window_left: int, softmax_scale: float, out, lse,
                     stream=None) -> None:
-    """Forward.  q [T,Hq,128], k/v [T,Hkv,128] bf16; out [T,Hq,128] bf16, lse [Hq,T] fp32."""
+    """Forward.  q [T,Hq,128], k/v [T,Hkv,128] bf16; out [T,Hq,128] bf16, lse [Hq,T] fp32.
+    Strided views (last dimension contiguous) go through attn_varlen_fwd_strided."""
+    if not _dense(q, k, v, out):
+        return attn_varlen_fwd_strided(q, k, v, cu_seqlens, max_seqlen, window_left, softmax_scale, out, lse, stream)
+    _check_lse(lse)
     lib = load_library()
     total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
     rc = lib.attn_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), int(max_seqlen), int(window_left),
@@ -98,15 +126,47 @@ def attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen: int, window_left: int, soft
     _check(rc, "attn_varlen_fwd")
 
 
+def attn_varlen_fwd_strided(q, k, v, cu_seqlens, max_seqlen: int, window_left: int, softmax_scale: float, out, lse,
+                            stream=None) -> None:
+    """Forward on [T, H, 128] views with any 16-byte-multiple token/head strides."""
+    _check_lse(lse)
+    lib = load_library()
+    total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
+    st = _strides(q, k, v, out)
+    rc = lib.attn_varlen_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), int(max_seqlen), int(window_left),
+                                     float(softmax_scale), _ptr(out), _ptr(lse), total, hq, hkv, d, nseg,
+                                     ctypes.cast(st, ctypes.c_void_p), _stream_handle(stream))
+    _check(rc, "attn_varlen_fwd_strided")
+
+
 def attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seqlen: int, window_left: int, softmax_scale: float,
                     dq, dk, dv, stream=None) -> None:
-    """Backward.  Writes dq [T,Hq,128], dk/dv [T,Hkv,128] (bf16)."""
+    """Backward.  Writes dq [T,Hq,128], dk/dv [T,Hkv,128] (bf16).  Strided views
+    (last dimension contiguous) go through attn_varlen_bwd_strided."""
+    if not _dense(dout, q, k, v, out, dq, dk, dv):
+        return attn_varlen_bwd_strided(dout, q, k, v, out, lse, cu_seqlens, max_seqlen, window_left, softmax_scale,
+                                       dq, dk, dv, stream)
+    _check_lse(lse)
     lib = load_library()
     total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
     rc = lib.attn_varlen_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
                              int(max_seqlen), int(window_left), float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv),
                              total, hq, hkv, d, nseg, _stream_handle(stream))
     _check(rc, "attn_varlen_bwd")
+
+
+def attn_varlen_bwd_strided(dout, q, k, v, out, lse, cu_seqlens, max_seqlen: int, window_left: int,
+                            softmax_scale: float, dq, dk, dv, stream=None) -> None:
+    """Backward on [T, H, 128] views with any 16-byte-multiple token/head strides."""
+    _check_lse(lse)
+    lib = load_library()
+    total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
+    st = _strides(dout, q, k, v, out, dq, dk, dv)
+    rc = lib.attn_varlen_bwd_strided(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
+                                     int(max_seqlen), int(window_left), float(softmax_scale), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), total, hq, hkv, d, nseg, ctypes.cast(st, ctypes.c_void_p),
+                                     _stream_handle(stream))
+    _check(rc, "attn_varlen_bwd_strided")
 
 
 def attn_varlen_bwd_noalloc(dout, q, k, v, out, lse, cu_seqlens, max_seqlen: int, window_left: int,

@@ -81,11 +81,12 @@ int current_device(DeviceInfo** info) {
   return ATTN_OK;
 }
 
-// [T, heads, 128] bf16 -> 3-D map (d, head, token), box (64, 1, 128),
-// 128-byte swizzle: one box is a 128-token x 64-column swizzled half tile.
-int make_tile_map(CUtensorMap* m, const void* base, int heads, int64_t total) {
+// [T, heads, 128] bf16 with element strides st -> 3-D map (d, head, token),
+// box (64, 1, 128), 128-byte swizzle: one box is a 128-token x 64-column
+// swizzled half tile.
+int make_tile_map(CUtensorMap* m, const void* base, int heads, int64_t total, const RowStrides& st) {
   cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)total};
-  cuuint64_t strides[2] = {128 * 2, (cuuint64_t)heads * 128 * 2};
+  cuuint64_t strides[2] = {(cuuint64_t)st.head * 2, (cuuint64_t)st.token * 2};
   cuuint32_t box[3] = {64, 1, 128};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -95,6 +96,28 @@ int make_tile_map(CUtensorMap* m, const void* base, int heads, int64_t total) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The dense layout [T, heads, 128].
+RowStrides contiguous(int heads) { return RowStrides{(long long)heads * 128, 128}; }
+
+// Strides of a [T, heads, 128] view: 16-byte multiples (TMA and 16-byte
+// stores), the 128 elements of a (token, head) row never overlap another
+// head's row, and a token's heads fit inside one token step.
+bool strides_ok(const RowStrides& st, int heads) {
+  if (st.token <= 0 || st.head <= 0 || (st.token % 8) != 0 || (st.head % 8) != 0) return false;
+  if (st.head < 128 || st.token < st.head * heads) return false;
+  return st.token < (1LL << 36);
+}
+
+// Reads `n` (token, head) stride pairs from a caller's int64 array.
+int read_strides(const int64_t* raw, int n, const int* heads, RowStrides* out) {
+  if (!raw) return ATTN_ERR_NULL_POINTER;
+  for (int t = 0; t < n; ++t) {
+    out[t] = RowStrides{(long long)raw[2 * t], (long long)raw[2 * t + 1]};
+    if (!strides_ok(out[t], heads[t])) return ATTN_ERR_STRIDE;
+  }
+  return ATTN_OK;
+}
 
 int validate_common(const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left, float softmax_scale,
                     int64_t total, int32_t hq, int32_t hkv, int32_t head_dim, int32_t nseg) {
@@ -136,12 +159,12 @@ AttnParams make_params(const int32_t* cu_seqlens, int32_t max_seqlen, int32_t wi
 
 using namespace vsw;
 
-extern "C" {
+namespace {
 
-int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens, int32_t max_seqlen,
-                    int32_t window_left, float softmax_scale, void* out, float* lse, int64_t total,
-                    int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t num_segments,
-                    void* stream) {
+// st: q, k, v, out.
+int fwd_impl(const void* q, const void* k, const void* v, const int32_t* cu_seqlens, int32_t max_seqlen,
+             int32_t window_left, float softmax_scale, void* out, float* lse, int64_t total, int32_t num_heads_q,
+             int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, const RowStrides* st, void* stream) {
   int rc = validate_common(cu_seqlens, max_seqlen, window_left, softmax_scale, total, num_heads_q, num_heads_kv,
                            head_dim, num_segments);
   if (rc) return rc;
@@ -152,17 +175,46 @@ int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* 
   if ((rc = current_device(&dev))) return rc;
   if (total == 0) return ATTN_OK;
   CUtensorMap tq, tk, tv;
-  if (make_tile_map(&tq, q, num_heads_q, total) || make_tile_map(&tk, k, num_heads_kv, total) ||
-      make_tile_map(&tv, v, num_heads_kv, total))
+  if (make_tile_map(&tq, q, num_heads_q, total, st[0]) || make_tile_map(&tk, k, num_heads_kv, total, st[1]) ||
+      make_tile_map(&tv, v, num_heads_kv, total, st[2]))
     return ATTN_ERR_CUDA;
   FwdParams p;
   p.a = make_params(cu_seqlens, max_seqlen, window_left, softmax_scale, total, num_heads_q, num_heads_kv,
                     num_segments, dev->status);
   p.out = out;
   p.lse = lse;
+  p.out_st = st[3];
   if (launch_fwd(tq, tk, tv, p, dev->num_sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens, int32_t max_seqlen,
+                    int32_t window_left, float softmax_scale, void* out, float* lse, int64_t total,
+                    int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t num_segments,
+                    void* stream) {
+  if (num_heads_q <= 0 || num_heads_kv <= 0) return ATTN_ERR_SHAPE;
+  const RowStrides st[4] = {contiguous(num_heads_q), contiguous(num_heads_kv), contiguous(num_heads_kv),
+                            contiguous(num_heads_q)};
+  return fwd_impl(q, k, v, cu_seqlens, max_seqlen, window_left, softmax_scale, out, lse, total, num_heads_q,
+                  num_heads_kv, head_dim, num_segments, st, stream);
+}
+
+int attn_varlen_fwd_strided(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                            int32_t max_seqlen, int32_t window_left, float softmax_scale, void* out, float* lse,
+                            int64_t total, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
+                            int32_t num_segments, const int64_t* strides, void* stream) {
+  if (num_heads_q <= 0 || num_heads_kv <= 0) return ATTN_ERR_SHAPE;
+  const int heads[4] = {num_heads_q, num_heads_kv, num_heads_kv, num_heads_q};
+  RowStrides st[4];
+  int rc = read_strides(strides, 4, heads, st);
+  if (rc) return rc;
+  return fwd_impl(q, k, v, cu_seqlens, max_seqlen, window_left, softmax_scale, out, lse, total, num_heads_q,
+                  num_heads_kv, head_dim, num_segments, st, stream);
 }
 
 size_t attn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads_q) {
@@ -184,10 +236,12 @@ struct BwdSetup {
   BwdParams p;
 };
 
+// st: dout, q, k, v, out, dq, dk, dv (null: all contiguous).
 int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, const void* v, const void* out,
                 const float* lse, const void* workspace, const int32_t* cu_seqlens, int32_t max_seqlen,
                 int32_t window_left, float softmax_scale, void* dq, void* dk, void* dv, int64_t total,
-                int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t num_segments) {
+                int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t num_segments,
+                const RowStrides* st = nullptr) {
   int rc = validate_common(cu_seqlens, max_seqlen, window_left, softmax_scale, total, num_heads_q, num_heads_kv,
                            head_dim, num_segments);
   if (rc) return rc;
@@ -201,8 +255,16 @@ int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, con
     if (x && !aligned16(x)) return ATTN_ERR_ALIGNMENT;
   if ((rc = current_device(&b.dev))) return rc;
   if (total == 0) return ATTN_OK;
-  if (make_tile_map(&b.tq, q, num_heads_q, total) || make_tile_map(&b.tk, k, num_heads_kv, total) ||
-      make_tile_map(&b.tv, v, num_heads_kv, total) || make_tile_map(&b.tdo, dout, num_heads_q, total))
+  RowStrides cs[8];
+  if (!st) {
+    const int heads[8] = {num_heads_q, num_heads_q, num_heads_kv, num_heads_kv,
+                          num_heads_q, num_heads_q, num_heads_kv, num_heads_kv};
+    for (int t = 0; t < 8; ++t) cs[t] = contiguous(heads[t]);
+    st = cs;
+  }
+  if (make_tile_map(&b.tq, q, num_heads_q, total, st[1]) || make_tile_map(&b.tk, k, num_heads_kv, total, st[2]) ||
+      make_tile_map(&b.tv, v, num_heads_kv, total, st[3]) ||
+      make_tile_map(&b.tdo, dout, num_heads_q, total, st[0]))
     return ATTN_ERR_CUDA;
   b.p.a = make_params(cu_seqlens, max_seqlen, window_left, softmax_scale, total, num_heads_q, num_heads_kv,
                       num_segments, b.dev->status);
@@ -218,21 +280,26 @@ int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, con
   b.p.dq = dq;
   b.p.dk = dk;
   b.p.dv = dv;
+  b.p.dout_st = st[0];
+  b.p.out_st = st[4];
+  b.p.dq_st = st[5];
+  b.p.dk_st = st[6];
+  b.p.dv_st = st[7];
   return ATTN_OK;
 }
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
-                    const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
-                    float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
-                    int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream) {
+int bwd_impl(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+             const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left, float softmax_scale, void* dq,
+             void* dk, void* dv, int64_t total, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
+             int32_t num_segments, const RowStrides* st, void* stream) {
   if (!out || !dq || !dk || !dv) return ATTN_ERR_NULL_POINTER;
   BwdSetup b;
   int rc = prepare_bwd(b, dout, q, k, v, out, lse, nullptr, cu_seqlens, max_seqlen, window_left, softmax_scale, dq,
-                       dk, dv, total, num_heads_q, num_heads_kv, head_dim, num_segments);
+                       dk, dv, total, num_heads_q, num_heads_kv, head_dim, num_segments, st);
   if (rc || total == 0) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
@@ -248,6 +315,33 @@ int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* 
   const cudaError_t fr = cudaFreeAsync(ws, s);
   if (lr != cudaSuccess || fr != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                    const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                    float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
+                    int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, void* stream) {
+  return bwd_impl(dout, q, k, v, out, lse, cu_seqlens, max_seqlen, window_left, softmax_scale, dq, dk, dv, total,
+                  num_heads_q, num_heads_kv, head_dim, num_segments, nullptr, stream);
+}
+
+int attn_varlen_bwd_strided(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                            const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                            float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
+                            int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, const int64_t* strides,
+                            void* stream) {
+  if (num_heads_q <= 0 || num_heads_kv <= 0) return ATTN_ERR_SHAPE;
+  const int heads[8] = {num_heads_q, num_heads_q, num_heads_kv, num_heads_kv,
+                        num_heads_q, num_heads_q, num_heads_kv, num_heads_kv};
+  RowStrides st[8];
+  int rc = read_strides(strides, 8, heads, st);
+  if (rc) return rc;
+  return bwd_impl(dout, q, k, v, out, lse, cu_seqlens, max_seqlen, window_left, softmax_scale, dq, dk, dv, total,
+                  num_heads_q, num_heads_kv, head_dim, num_segments, st, stream);
 }
 
 int attn_varlen_bwd_preprocess(const void* dout, const void* out, void* workspace, size_t workspace_bytes,
@@ -266,6 +360,7 @@ int attn_varlen_bwd_preprocess(const void* dout, const void* out, void* workspac
   p.a.hq = num_heads_q;
   p.dout = dout;
   p.out = out;
+  p.dout_st = p.out_st = contiguous(num_heads_q);
   if (!carve_workspace(workspace, workspace_bytes, total, num_heads_q, p)) return ATTN_ERR_WORKSPACE;
   return launch_bwd_preprocess(p, static_cast<cudaStream_t>(stream)) ? ATTN_ERR_CUDA : ATTN_OK;
 }
@@ -333,6 +428,9 @@ const char* attn_varlen_strerror(int code) {
     case ATTN_ERR_ALLOC: return "backward scratch allocation failed";
     case ATTN_ERR_DEVICE_STATUS: return "a kernel recorded a device-side error";
     case ATTN_ERR_WORKSPACE: return "workspace smaller than delta (T * Hq floats) or not 256-byte aligned";
+    case ATTN_ERR_STRIDE:
+      return "a stride is not a positive multiple of 8 elements, a head step is below 128, or a token step "
+             "is below head step x heads";
     case ATTN_ERR_NOALLOC_TOO_LARGE:
       return "T * Hq exceeds the fixed scratch of attn_varlen_bwd_noalloc (2,097,152 floats)";
     default: return "unknown error code";

@@ -22,6 +22,7 @@ constexpr int kPreRowsPerBlock = 64;
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __restrict__ dout,
                                                              const uint4* __restrict__ out,
                                                              float* __restrict__ delta, int total, int hq,
+                                                             RowStrides dout_st, RowStrides out_st,
                                                              int* __restrict__ chain_progress, int nprogress) {
   grid_dependency_wait();
   // Everything before this kernel is complete: the next kernel may start
@@ -31,6 +32,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __rest
   if (blockIdx.x == 0)
     for (int e = threadIdx.x; e < nprogress; e += blockDim.x) chain_progress[e] = 0;
   const long long rows = (long long)total * hq;
+  const bool dense = dout_st.token == 128LL * hq && dout_st.head == 128 && out_st.token == 128LL * hq &&
+                     out_st.head == 128;
   const int sub = threadIdx.x & 15;
   const int r_in = threadIdx.x >> 4;  // 0..15
   for (long long base = (long long)blockIdx.x * kPreRowsPerBlock; base < rows;
@@ -41,8 +44,16 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __rest
     for (int k = 0; k < 4; ++k) {
       const long long r = base + 16 * k + r_in;
       valid[k] = r < rows;
-      a[k] = valid[k] ? __ldg(dout + r * 16 + sub) : make_uint4(0, 0, 0, 0);
-      b[k] = valid[k] ? __ldcs(out + r * 16 + sub) : make_uint4(0, 0, 0, 0);
+      // Row r = (token i, head h); offsets in 16-byte units.  Dense tensors
+      // (the usual case) need no division.
+      long long od = r * 16, oo = r * 16;
+      if (!dense) {
+        const long long i = r / hq, h = r - i * hq;
+        od = (i * dout_st.token + h * dout_st.head) / 8;
+        oo = (i * out_st.token + h * out_st.head) / 8;
+      }
+      a[k] = valid[k] ? __ldg(dout + od + sub) : make_uint4(0, 0, 0, 0);
+      b[k] = valid[k] ? __ldcs(out + oo + sub) : make_uint4(0, 0, 0, 0);
     }
     float acc[4];
 #pragma unroll
@@ -146,7 +157,7 @@ int launch_bwd_preprocess(const BwdParams& p, cudaStream_t stream) {
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
   return (int)launch_pdl(bwd_preprocess_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
                          static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.out), p.delta, p.a.total,
-                         p.a.hq, p.chain_progress, p.chain_progress ? 2 * p.chains_max : 0);
+                         p.a.hq, p.dout_st, p.out_st, p.chain_progress, p.chain_progress ? 2 * p.chains_max : 0);
 }
 
 int launch_mask_probe(const int* cu_seqlens, int nseg, int total, int window, int max_levels, int by_key,

@@ -454,7 +454,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!(ok = mbar_wait_warp(smem_u32(&bar_acc_full), it & 1, &abort_flag, a.status))) break;
       tc_fence_after();
       const bool valid = j < w.seg_hi && token_in_range(j, a.total);
-      void* dst_row = static_cast<__nv_bfloat16*>(x == 0 ? p.dv : p.dk) + ((size_t)j * a.hkv + g) * kHeadDim;
+      const RowStrides dst_st = x == 0 ? p.dv_st : p.dk_st;
+      void* dst_row = static_cast<__nv_bfloat16*>(x == 0 ? p.dv : p.dk) + j * dst_st.token + g * dst_st.head;
       const uint32_t tacc = lane_base + (x == 0 ? C::kColDV : C::kColDK);
       const float mul = x == 0 ? 1.f : a.scale;
       if (w.chain < 0) {
@@ -463,7 +464,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t r[32];
           tmem_ld32(tacc + c * 32, r);
           tmem_wait_ld(r);
-          store_rows32_bf16(dst_row, (long long)a.hkv * kHeadDim * 2, c * 32, r, mul, valid);
+          store_rows32_bf16(dst_row, dst_st.token * 2, c * 32, r, mul, valid);
         }
       } else {
         // A chunk of a split kv item: add the partial sums of the earlier
@@ -491,7 +492,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
           }
           if (li == lk - 1) {
-            store_rows32_bf16(dst_row, (long long)a.hkv * kHeadDim * 2, c * 32, r, mul, valid);
+            store_rows32_bf16(dst_row, dst_st.token * 2, c * 32, r, mul, valid);
           } else {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
@@ -837,13 +838,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // ---- epilogue: warpgroup x writes dQ columns [64x, 64x + 64) (x scale).
       if (!(ok = mbar_wait_warp(smem_u32(&bar_acc_full), it & 1, &abort_flag, a.status))) break;
       tc_fence_after();
-      void* dq_row = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)i * a.hq + h) * kHeadDim;
+      void* dq_row = static_cast<__nv_bfloat16*>(p.dq) + i * p.dq_st.token + h * p.dq_st.head;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t r[32];
         tmem_ld32(lane_base + C::kColDQ + 64 * x + cc * 32, r);
         tmem_wait_ld(r);
-        store_rows32_bf16(dq_row, (long long)a.hq * kHeadDim * 2, 64 * x + cc * 32, r, a.scale, valid);
+        store_rows32_bf16(dq_row, p.dq_st.token * 2, 64 * x + cc * 32, r, a.scale, valid);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_acc_empty));

@@ -384,13 +384,13 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
       tc_fence_after();
       const bool valid = i < w.seg_hi && token_in_range(i, a.total);
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      void* out_row = static_cast<__nv_bfloat16*>(p.out) + ((size_t)i * a.hq + h) * kHeadDim;
+      void* out_row = static_cast<__nv_bfloat16*>(p.out) + i * p.out_st.token + h * p.out_st.head;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tmem_ld32(tO + c * 32, r);
         tmem_wait_ld(r);
-        store_rows32_bf16(out_row, (long long)a.hq * kHeadDim * 2, c * 32, r, inv_l, valid);
+        store_rows32_bf16(out_row, p.out_st.token * 2, c * 32, r, inv_l, valid);
       }
       if (valid) p.lse[(size_t)h * a.total + i] = (m + __log2f(l)) * 0.69314718055994531f;
       tc_fence_before();

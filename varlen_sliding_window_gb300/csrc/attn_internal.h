@@ -23,10 +23,18 @@ struct AttnParams {
   int* status;        // device status word
 };
 
+// Element strides of a [T, H, 128] bf16 tensor whose last dimension is
+// contiguous: token t, head h starts at t * token + h * head.
+struct RowStrides {
+  long long token;
+  long long head;
+};
+
 struct FwdParams {
   AttnParams a;
   void* out;   // bf16 [T, hq, 128]
   float* lse;  // fp32 [hq, T]
+  RowStrides out_st;
 };
 
 struct BwdParams {
@@ -49,6 +57,7 @@ struct BwdParams {
   // Set when the dK/dV kernel is launched right after the preprocess of the
   // same backward: it plans before waiting for that kernel.
   int dkdv_after_pre;
+  RowStrides dout_st, out_st, dq_st, dk_st, dv_st;
 };
 
 // Backward workspace layout: delta, chain progress counters, chain buffers.
