@@ -2,14 +2,17 @@
 
 The compute lives in the C-ABI library libvsw_attn.so (include/attn_varlen.h);
 ``binding`` marshals torch CUDA tensors into it.  ``synth`` generates the
-seeded packed-document workloads.
+seeded packed-document workloads.  ``layer`` wraps one attention layer
+(projections, the library's attention on strided views, a small loss, and the
+backward) for CUDA-graph replay.
 """
 from importlib import import_module
 
 _BINDING_NAMES = {
     "attn_varlen_fwd", "attn_varlen_bwd", "attn_varlen_bwd_workspace_bytes", "attn_varlen_get_status",
     "attn_varlen_strerror", "attn_varlen_mask_ranges", "attn_varlen_bwd_preprocess",
-    "attn_varlen_bwd_dkdv", "attn_varlen_bwd_dq", "attn_varlen_bwd_noalloc", "load_library", "AttnError",
+    "attn_varlen_bwd_dkdv", "attn_varlen_bwd_dq", "attn_varlen_bwd_noalloc", "attn_varlen_fwd_strided",
+    "attn_varlen_bwd_strided", "load_library", "AttnError",
 }
 
 
