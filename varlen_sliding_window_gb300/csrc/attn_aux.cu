@@ -19,6 +19,7 @@ namespace {
 // cached for the dK/dV and dQ passes that follow.
 constexpr int kPreRowsPerBlock = 64;
 
+template <bool DENSE>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __restrict__ dout,
                                                              const uint4* __restrict__ out,
                                                              float* __restrict__ delta, int total, int hq,
@@ -32,8 +33,6 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __rest
   if (blockIdx.x == 0)
     for (int e = threadIdx.x; e < nprogress; e += blockDim.x) chain_progress[e] = 0;
   const long long rows = (long long)total * hq;
-  const bool dense = dout_st.token == 128LL * hq && dout_st.head == 128 && out_st.token == 128LL * hq &&
-                     out_st.head == 128;
   const int sub = threadIdx.x & 15;
   const int r_in = threadIdx.x >> 4;  // 0..15
   for (long long base = (long long)blockIdx.x * kPreRowsPerBlock; base < rows;
@@ -47,7 +46,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __rest
       // Row r = (token i, head h); offsets in 16-byte units.  Dense tensors
       // (the usual case) need no division.
       long long od = r * 16, oo = r * 16;
-      if (!dense) {
+      if (!DENSE) {
         const long long i = r / hq, h = r - i * hq;
         od = (i * dout_st.token + h * dout_st.head) / 8;
         oo = (i * out_st.token + h * out_st.head) / 8;
@@ -155,7 +154,10 @@ int launch_bwd_preprocess(const BwdParams& p, cudaStream_t stream) {
   const long long rows = (long long)p.a.total * p.a.hq;
   long long blocks = (rows + kPreRowsPerBlock - 1) / kPreRowsPerBlock;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  return (int)launch_pdl(bwd_preprocess_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+  const bool dense = p.dout_st.token == 128LL * p.a.hq && p.dout_st.head == 128 &&
+                     p.out_st.token == 128LL * p.a.hq && p.out_st.head == 128;
+  return (int)launch_pdl(dense ? bwd_preprocess_kernel<true> : bwd_preprocess_kernel<false>, dim3((unsigned)blocks),
+                         dim3(256), 0, stream,
                          static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.out), p.delta, p.a.total,
                          p.a.hq, p.dout_st, p.out_st, p.chain_progress, p.chain_progress ? 2 * p.chains_max : 0);
 }
