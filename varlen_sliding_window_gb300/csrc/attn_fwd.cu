@@ -7,13 +7,16 @@
 // log-sum-exp of the scaled logits (fp32, [Hq, T]) for the backward pass.
 //
 // How (one persistent CTA per SM, warp-specialised):
-//   warp 0        TMA producer: Q tiles of NQT heads (double-buffered across
-//                 work items), then K_j, V_j tiles through a ring of slots
+//   warp 0        TMA producer: lane 1 streams the Q tiles of NQT heads per
+//                 work unit through a ring of their own (the next unit's
+//                 first head loads while the current unit runs), lane 0 the
+//                 K_j, V_j tiles through a ring of slots
 //   warp 1        MMA issuer: S_t = Q_t K_j^T (both operands in shared memory)
 //                 and O_t += P_t V_j (P_t read from TMEM), fp32 accumulators
 //                 in Tensor Memory
 //   warp 2        owns the TMEM allocation
-//   warp 3        builds the CTA's longest-first work list (sched.cuh)
+//   all threads   plan the CTA's longest-first work list in the prologue
+//                 (plan.cuh); warp 3 alone when it does not fit (sched.cuh)
 //   warpgroup 1+t online softmax of q tile t: one thread per query row reads
 //                 its S row from TMEM, masks only tiles that straddle the mask
 //                 edge, writes P (bf16) back over the first half of its S
