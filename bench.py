@@ -615,6 +615,17 @@ def main():
         for n in outs:
             assert torch.equal(host_res[k][n], slots[k][n].cpu()), n
 
+    # Spread over document seeds 0-4 of the same workload recipe (the
+    # headline is seed 0): step ms and counted TFLOP/s per seed.
+    import dataclasses
+    spread = []
+    for sd in range(5):
+        w_s = dataclasses.replace(wl, doc_seed=sd)
+        r = measure(w_s, max(5, args.steps // 2), 3)
+        ms_s = statistics.mean(r["total_ms"])
+        spread.append({"doc_seed": sd, "segments": int(len(r["inp"].cu_seqlens) - 1), "pairs": r["pairs"],
+                       "ms": ms_s, "tflops": tflops(w_s, r["pairs"], ms_s)})
+        del r
     sm_mhz = (main_res["clocks"] or {}).get("sm_mhz")
     peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     graph_main = graph_replay(wl, args.steps, args.warmup)
@@ -648,6 +659,7 @@ def main():
             "fwd_ms": statistics.mean(main_res["fwd_ms"]), "bwd_ms": statistics.mean(main_res["bwd_ms"]),
             "kernel_ms": kern_ms,
             "roofs": roofs(wl, main_res["pairs"], step_ms, peak_t, peak_hbm, sm_mhz),
+            "seed_spread": spread,
             "graph": graph_main,
             "layer": layer_main,
             "roofline": roofline,
