@@ -114,3 +114,19 @@ def test_binding_fails_loudly_without_library(tmp_path):
             binding.load_library(str(tmp_path / "missing.so"))
     finally:
         binding._lib = saved
+
+
+def test_binding_rejects_views_where_the_call_has_no_strides():
+    import torch
+    from varlen_sliding_window_gb300 import binding
+    q = torch.zeros(4, 12, 128, dtype=torch.bfloat16)[:, :8]  # a view: token stride 12 * 128
+    k = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
+    dense_q = torch.zeros(4, 8, 128, dtype=torch.bfloat16)
+    lse = torch.zeros(8, 4)
+    cu = torch.tensor([0, 4], dtype=torch.int32)
+    with pytest.raises(ValueError, match="strided"):
+        binding.attn_varlen_bwd_noalloc(dense_q, q, k, k, dense_q, lse, cu, 4, -1, 0.088, dense_q, k, k)
+    with pytest.raises(ValueError, match="strided"):
+        binding.attn_varlen_bwd_preprocess(dense_q, q, torch.zeros(256, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="lse"):
+        binding.attn_varlen_fwd_strided(q, k, k, cu, 4, -1, 0.088, dense_q, lse.t())

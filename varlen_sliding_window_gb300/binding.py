@@ -106,6 +106,12 @@ def _dense(*tensors) -> bool:
     return all(t.is_contiguous() for t in tensors)
 
 
+def _require_dense(what: str, *tensors) -> None:
+    """The calls without stride arguments read and write dense [T, H, 128] tensors."""
+    if not _dense(*tensors):
+        raise ValueError(f"{what} takes dense tensors; use the *_strided calls for views")
+
+
 def _check_lse(lse):
     if not lse.is_contiguous():
         raise ValueError("lse must be a dense float32 [Hq, T] tensor")
@@ -172,6 +178,7 @@ def attn_varlen_bwd_strided(dout, q, k, v, out, lse, cu_seqlens, max_seqlen: int
 def attn_varlen_bwd_noalloc(dout, q, k, v, out, lse, cu_seqlens, max_seqlen: int, window_left: int,
                             softmax_scale: float, dq, dk, dv, stream=None) -> None:
     """Backward with its scratch in the library's fixed device array (no allocation)."""
+    _require_dense("attn_varlen_bwd_noalloc", dout, q, k, v, out, lse, dq, dk, dv)
     lib = load_library()
     total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
     rc = lib.attn_varlen_bwd_noalloc(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
@@ -186,6 +193,7 @@ def _ws(workspace):
 
 def attn_varlen_bwd_preprocess(dout, out, workspace, stream=None) -> None:
     """D = rowsum(dout * out) into the workspace (a 256-byte-aligned uint8 CUDA tensor)."""
+    _require_dense("attn_varlen_bwd_preprocess", dout, out)
     lib = load_library()
     total, hq, d = dout.shape
     wp, wb = _ws(workspace)
@@ -195,6 +203,7 @@ def attn_varlen_bwd_preprocess(dout, out, workspace, stream=None) -> None:
 
 def attn_varlen_bwd_dkdv(dout, q, k, v, lse, workspace, cu_seqlens, max_seqlen: int, window_left: int,
                          softmax_scale: float, dk, dv, stream=None) -> None:
+    _require_dense("attn_varlen_bwd_dkdv", dout, q, k, v, lse, dk, dv)
     lib = load_library()
     total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
     wp, wb = _ws(workspace)
@@ -205,6 +214,7 @@ def attn_varlen_bwd_dkdv(dout, q, k, v, lse, workspace, cu_seqlens, max_seqlen: 
 
 def attn_varlen_bwd_dq(dout, q, k, v, lse, workspace, cu_seqlens, max_seqlen: int, window_left: int,
                        softmax_scale: float, dq, stream=None) -> None:
+    _require_dense("attn_varlen_bwd_dq", dout, q, k, v, lse, dq)
     lib = load_library()
     total, hq, hkv, d, nseg = _dims(q, k, cu_seqlens)
     wp, wb = _ws(workspace)
