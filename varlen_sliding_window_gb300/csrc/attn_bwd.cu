@@ -322,8 +322,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // S^T - lse/scale = [K 1] [Q -lse/scale]^T and dP^T - D = [V 1] [dO -D]^T
         // (N = 128 queries; the last k-step is the extra block), committed
         // separately so the exp2 work starts while dP^T runs.
+        // K and V are read only by S^T and dP^T: the slot is released once the
+        // item's last dP^T is issued (the commit covers every earlier MMA), so
+        // the next item's K and V load while this item's last pair finishes.
         if (!(ok = issue_s(cnt))) break;
         issue_dp(cnt);
+        if (npairs == 1) tc_commit(smem_u32(&bar_kv_empty));
         for (int pr = 0; pr < npairs && ok; ++pr) {
           const int slot = cnt % S;
           const uint32_t sq = sQ0 + slot * 2 * kTileBytes, sdo = sq + kTileBytes;
@@ -364,11 +368,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_commit(smem_u32(&bar_qdo_empty[slot]));
           if (more && !s_next && !(ok = issue_s(cnt + 1))) break;
           if (more) issue_dp(cnt + 1);
+          if (pr + 2 == npairs) tc_commit(smem_u32(&bar_kv_empty));
           ++cnt;
         }
         if (!ok) break;
         tc_commit(smem_u32(&bar_acc_full));
-        tc_commit(smem_u32(&bar_kv_empty));
       }
     }
   } else if (warp < 4) {
@@ -736,9 +740,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int nt = w.t1 - w.t0 + 1;
         if (!(ok = mbar_wait(smem_u32(&bar_q_full), it & 1, &abort_flag, a.status))) break;
         tc_fence_after();
+        // Q and dO are read only by S and dP: their buffer is released once the
+        // item's last dP is issued, so the next item's Q and dO load while
+        // this item's last tile finishes.
         if (!(ok = wait_k(c))) break;
         issue_s(c);
         if (!(ok = issue_dp(c))) break;
+        if (nt == 1) tc_commit(smem_u32(&bar_q_empty));
         for (int n = 0; n < nt && ok; ++n, ++c) {
           if (n + 1 < nt) {
             // Next tile's S, and its dP as soon as this tile's dP has been
@@ -746,6 +754,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!(ok = wait_k(c + 1))) break;
             issue_s(c + 1);
             if (!(ok = issue_dp(c + 1))) break;
+            if (n + 2 == nt) tc_commit(smem_u32(&bar_q_empty));
           }
           if (n == 0 && it > 0 && !(ok = mbar_wait(smem_u32(&bar_acc_empty), (it - 1) & 1, &abort_flag, a.status)))
             break;
@@ -765,7 +774,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (!ok) break;
         tc_commit(smem_u32(&bar_acc_full));
-        tc_commit(smem_u32(&bar_q_empty));
       }
     }
   } else if (warp < 4) {
