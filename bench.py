@@ -6,6 +6,11 @@ through the library's C ABI.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
+The headline workload is the context-4,096 global-causal microbatch; the
+window-512 and context-512 microbatches, the context sweep (512 ... 4,096,
+global and window 512) and the 65,536-token 16/4-head long-context case are
+measured in the same run under "also".
+
 Timing: CUDA events on the launching stream around every kernel of every
 step; the L2 (129 MB) is flushed by writing a 512 MiB buffer between steps,
 outside the events.  SM clocks are sampled with nvidia-smi during the timed
@@ -21,6 +26,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -32,7 +38,8 @@ from varlen_sliding_window_gb300 import synth  # noqa: E402
 
 METRIC = "attn fwd+bwd ms per 16K-token microbatch; unmasked TFLOPS & % of bf16 peak"
 # The page's FlashAttention-2 fwd+bwd per layer on its own (unnamed, clock-capped)
-# GPU, for the same workloads: context for vs_baseline, not a target.
+# GPU, for the same workloads: reported as context ("page_context"), not as a
+# baseline and not as a target.
 PAGE_FA2_MS = {"ctx512_global": 0.68, "ctx4096_global": 1.43, "ctx4096_w512": 0.95,
                "sweep_ctx512_global": 0.68, "sweep_ctx1024_global": 0.94, "sweep_ctx2048_global": 1.26,
                "sweep_ctx4096_global": 1.43, "sweep_ctx512_w512": 0.69, "sweep_ctx1024_w512": 0.85,
@@ -125,11 +132,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"vsw_bench_clocks_{os.getpid()}_gpu{gpu_index}.csv")
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
@@ -173,16 +179,19 @@ class ClockSampler:
 
 
 def oracle_time(inp, window: int, scale: float, budget_s: float):
-    """Times the float64 oracle (fwd + bwd) on whole segments, in order, until
-    `budget_s` seconds have passed; returns (ms per full microbatch, sample
-    description, cores).  The oracle's cost per segment and head grows with
-    L^2, so the sample is scaled to the microbatch by sum(L^2)."""
+    """Times the float64 oracle (fwd + bwd) on whole segments, longest first,
+    until `budget_s` seconds have passed; returns (ms per full microbatch,
+    sample description, cores).  The oracle's work per segment and head is
+    proportional to the segment's unmasked (query, key) pairs (L(L+1)/2 for
+    global causal, about L (w+1) for a window w), so the sample is scaled to
+    the microbatch by the pair count."""
     import oracle
     cu = inp.cu_seqlens
     segs = [(int(a), int(b)) for a, b in zip(cu[:-1], cu[1:]) if b > a]
     # Longest first so that the sample includes the dominant segments.
     segs.sort(key=lambda s: -(s[1] - s[0]))
-    total_w = sum((b - a) ** 2 for a, b in segs)
+    seg_pairs = {s: unmasked_pairs(np.array([0, s[1] - s[0]]), window) for s in segs}
+    total_w = sum(seg_pairs.values())
     done_w, elapsed, n = 0, 0.0, 0
     for a, b in segs:
         sl = slice(a, b)
@@ -191,15 +200,23 @@ def oracle_time(inp, window: int, scale: float, budget_s: float):
         oracle.forward(inp.q[sl], inp.k[sl], inp.v[sl], c, window, scale)
         oracle.backward(inp.dout[sl], inp.q[sl], inp.k[sl], inp.v[sl], c, window, scale)
         elapsed += time.perf_counter() - t0
-        done_w += (b - a) ** 2
+        done_w += seg_pairs[(a, b)]
         n += 1
         if elapsed >= budget_s:
             break
     ms = 1e3 * elapsed * total_w / done_w
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    sample = (f"{n} of {len(segs)} segments (longest first, {done_w / total_w:.1%} of sum L^2), all heads, "
-              f"oracle fwd+bwd in numpy float64; scaled to the microbatch by sum L^2")
+    sample = (f"{n} of {len(segs)} segments (longest first, {done_w / total_w:.1%} of the unmasked pairs), all heads, "
+              f"oracle fwd+bwd in numpy float64; scaled to the microbatch by the unmasked pair count")
     return ms, sample, cores
+
+
+def workload_config(wl, cu, pairs: int, world: int) -> dict:
+    """The "config" object of a bench line, the same for both arms."""
+    return {"workload": wl.name, "tokens": wl.total, "context": wl.context, "window_left": wl.window_left,
+            "hq": wl.hq, "hkv": wl.hkv, "head_dim": wl.d, "segments": int(len(cu) - 1),
+            "doc_seed": wl.doc_seed, "tensor_seed": wl.tensor_seed, "unmasked_pairs": int(pairs),
+            "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"}
 
 
 def run_reference(args, wl):
@@ -220,8 +237,8 @@ def run_reference(args, wl):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "ms", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "tokens": wl.total, "context": wl.context,
-                       "window_left": wl.window_left, "hq": wl.hq, "hkv": wl.hkv, "head_dim": wl.d},
+            "config": workload_config(wl, inp.cu_seqlens, unmasked_pairs(inp.cu_seqlens, wl.window_left),
+                                      int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": value, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -232,10 +249,13 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="ctx512_global")
+    ap.add_argument("--workload", default="ctx4096_global")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--also", default="ctx4096_global,ctx4096_w512",
-                    help="extra 16K workloads measured in the same run (comma list, '' for none)")
+    ap.add_argument("--also", default="ctx4096_w512,ctx512_global",
+                    help="extra workloads measured in full in the same run (comma list, '' for none)")
+    ap.add_argument("--sweep", default=",".join(f"sweep_ctx{c}_{t}" for t in ("global", "w512")
+                                                for c in (512, 1024, 2048, 4096)) + ",long65536_global",
+                    help="workloads whose step and kernel times are reported under also.sweep ('' for none)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args()
     wls = synth.workloads()
@@ -514,24 +534,29 @@ def main():
     peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     tf = tflops(wl, main_res["pairs"], step_ms)
 
-    # Dominant kernel roofline.
-    kern_ms = {n: statistics.mean(v) for n, v in main_res["per_ms"].items()}
-    dom = max(kern_ms, key=kern_ms.get)
-    gemm_unit = 2.0 * wl.d * wl.hq * main_res["pairs"]
-    achieved = KERNEL_UNITS[dom] * gemm_unit / (kern_ms[dom] * 1e-3) / 1e12
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "dram_traffic.json")
-    if os.path.exists(tpath):
-        try:
-            rec = json.load(open(tpath))
-            # Counters only count while the kernels are the ones they were taken on.
-            if rec.get("csrc_hash") == csrc_hash():
-                traffic = rec.get(wl.name, {}).get(dom)
-        except Exception:
-            traffic = None
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
-                "frac": achieved / peak_t, "traffic": traffic,
-                "peak_source": f"bf16 dense burst, {'of measured' if peak_src == 'measured' else 'of fallback'}"}
+    def dominant_roofline(w, res):
+        """Roofline of the kernel with the largest CUDA-event time in the
+        per-kernel run: its credited GEMM units x 2 d Hq pairs, over its mean
+        launch time, against the bf16 peak."""
+        kern = {n: statistics.mean(v) for n, v in res["per_ms"].items()}
+        dom = max(kern, key=kern.get)
+        gemm_unit = 2.0 * w.d * w.hq * res["pairs"]
+        achieved = KERNEL_UNITS[dom] * gemm_unit / (kern[dom] * 1e-3) / 1e12
+        traffic = None
+        tpath = os.path.join(ROOT, "profiles", "dram_traffic.json")
+        if os.path.exists(tpath):
+            try:
+                rec = json.load(open(tpath))
+                # Counters only count while the kernels are the ones they were taken on.
+                if rec.get("csrc_hash") == csrc_hash():
+                    traffic = rec.get(w.name, {}).get(dom)
+            except Exception:
+                traffic = None
+        return kern, {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                      "frac": achieved / peak_t, "traffic": traffic,
+                      "peak_source": f"bf16 dense burst, {'of measured' if peak_src == 'measured' else 'of fallback'}"}
+
+    kern_ms, roofline = dominant_roofline(wl, main_res)
 
     # e2e through the public calls with host buffers and copies in the timed region.
     inp, t = main_res["inp"], main_res["t"]
@@ -635,13 +660,34 @@ def main():
         w2 = wls[name]
         r = measure(w2, max(5, args.steps // 2), 3)
         ms2 = statistics.mean(r["total_ms"])
+        k2, rl2 = dominant_roofline(w2, r)
         also[name] = {"ms": ms2, "tflops": tflops(w2, r["pairs"], ms2), "frac": tflops(w2, r["pairs"], ms2) / peak_t,
                       "fwd_ms": statistics.mean(r["fwd_ms"]), "bwd_ms": statistics.mean(r["bwd_ms"]),
                       "pairs": r["pairs"], "segments": int(len(r["inp"].cu_seqlens) - 1),
-                      "kernel_ms": {n: statistics.mean(v) for n, v in r["per_ms"].items()},
+                      "kernel_ms": k2, "roofline": rl2,
                       "roofs": roofs(w2, r["pairs"], ms2, peak_t, peak_hbm, sm_mhz)}
+        if w2.name in PAGE_FA2_MS:
+            also[name]["page_context"] = {"fa2_ms": PAGE_FA2_MS[w2.name], "ratio": ms2 / PAGE_FA2_MS[w2.name]}
         del r
         also[name]["graph"] = graph_replay(w2, max(6, args.steps // 2), 3)
+    # The context sweep (research.dws.rip/llm/kernels, section 02, Figs. 3
+    # and 4) and the long-context case: step and per-kernel times.
+    sweep = {}
+    for name in [x for x in args.sweep.split(",") if x]:
+        w2 = wls[name]
+        r = measure(w2, max(5, args.steps // 2), 3)
+        ms2 = statistics.mean(r["total_ms"])
+        k2, rl2 = dominant_roofline(w2, r)
+        sweep[name] = {"ms": ms2, "tflops": tflops(w2, r["pairs"], ms2), "frac": tflops(w2, r["pairs"], ms2) / peak_t,
+                       "fwd_ms": statistics.mean(r["fwd_ms"]), "bwd_ms": statistics.mean(r["bwd_ms"]),
+                       "pairs": r["pairs"], "segments": int(len(r["inp"].cu_seqlens) - 1), "tokens": w2.total,
+                       "context": w2.context, "window_left": w2.window_left, "hq": w2.hq, "hkv": w2.hkv,
+                       "kernel_ms": k2, "dominant": {"kernel": rl2["kernel"], "frac": rl2["frac"]}}
+        if w2.name in PAGE_FA2_MS:
+            sweep[name]["page_context"] = {"fa2_ms": PAGE_FA2_MS[w2.name], "ratio": ms2 / PAGE_FA2_MS[w2.name]}
+        del r
+    if sweep:
+        also["sweep"] = sweep
 
     line = None
     if rank == 0:
@@ -649,12 +695,13 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "ms", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": False, "scaling": "weak",
-            "vs_baseline": (value / PAGE_FA2_MS[wl.name]) if wl.name in PAGE_FA2_MS else None,
+            "vs_baseline": None,
+            "page_context": ({"fa2_ms": PAGE_FA2_MS[wl.name], "ratio": value / PAGE_FA2_MS[wl.name],
+                              "what": "the page's FlashAttention-2 fwd+bwd per layer on its own unnamed, "
+                                      "clock-capped GPU (research.dws.rip/llm/kernels, Figs. 3 and 4)"}
+                             if wl.name in PAGE_FA2_MS else None),
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "tokens": wl.total, "context": wl.context, "window_left": wl.window_left,
-                       "hq": wl.hq, "hkv": wl.hkv, "head_dim": wl.d, "segments": int(len(inp.cu_seqlens) - 1),
-                       "doc_seed": wl.doc_seed, "tensor_seed": wl.tensor_seed, "unmasked_pairs": main_res["pairs"],
-                       "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
+            "config": workload_config(wl, inp.cu_seqlens, main_res["pairs"], world),
             "tflops": tf, "pct_of_bf16_peak": 100.0 * tf / peak_t,
             "fwd_ms": statistics.mean(main_res["fwd_ms"]), "bwd_ms": statistics.mean(main_res["bwd_ms"]),
             "kernel_ms": kern_ms,

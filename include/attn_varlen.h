@@ -37,8 +37,10 @@
  * scratch buffer of attn_varlen_bwd_workspace_bytes() bytes, stream-ordered
  * on `stream`, from a per-device memory pool the library creates on its first
  * call on that device (make that first call outside any stream capture); the
- * pool keeps the memory it has reserved for later calls.  The sub-step calls
- * below take a caller-provided workspace instead.
+ * pool keeps the memory it has reserved for later calls.  A caller that owns
+ * its scratch registers it once with attn_varlen_set_workspace(); the
+ * backward then uses that buffer and allocates nothing.  The sub-step calls
+ * below take a caller-provided workspace as an argument.
  *
  * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
  * stream).  No call synchronises the host except attn_varlen_get_status();
@@ -46,11 +48,13 @@
  *
  * Errors: every call returns ATTN_OK (0) or a negative ATTN_ERR_* code and
  * never throws.  Argument errors are detected before anything is enqueued.
- * cu_seqlens is only read on the device; a list that breaks the rules above,
- * or a segment longer than max_seqlen, gives unspecified outputs but every
- * loop stays bounded.  Asynchronous device errors (a bounded wait that gave
- * up) are recorded in a per-device status word read by
- * attn_varlen_get_status().
+ * cu_seqlens is only read on the device; a list that breaks the rules above
+ * gives unspecified outputs but every loop stays bounded.  Asynchronous device
+ * errors are recorded in a per-device status word read by
+ * attn_varlen_get_status(): a bounded wait that gave up, a work list that did
+ * not fit, or a segment longer than max_seqlen (the kernels compute rows only
+ * up to max_seqlen, rounded up to a multiple of 128, so the later rows of such
+ * a segment are left unwritten).
  */
 #ifndef ATTN_VARLEN_H_
 #define ATTN_VARLEN_H_
@@ -76,8 +80,14 @@ extern "C" {
 #define ATTN_ERR_ALLOC (-11)         /* the backward scratch could not be allocated */
 #define ATTN_ERR_DEVICE_STATUS (-12) /* attn_varlen_get_status: a kernel reported an error */
 #define ATTN_ERR_NOALLOC_TOO_LARGE (-13) /* attn_varlen_bwd_noalloc: T * Hq above its fixed scratch (2,097,152) */
-#define ATTN_ERR_WORKSPACE (-14)     /* workspace below its minimum size or not 256-byte aligned */
+#define ATTN_ERR_WORKSPACE (-14)     /* workspace below its minimum size (T * Hq floats, 256-byte padded) */
 #define ATTN_ERR_STRIDE (-15)        /* *_strided: a stride pair that is not a valid [T, H, 128] view */
+
+/* Device status words (attn_varlen_get_status). */
+#define ATTN_STATUS_TIMEOUT 1          /* a bounded wait inside a kernel gave up */
+#define ATTN_STATUS_LIST_OVERFLOW 2    /* a CTA's work list did not fit */
+#define ATTN_STATUS_SMEM_ALIGN 3       /* dynamic shared memory not 1024-byte aligned (internal error) */
+#define ATTN_STATUS_SEGMENT_TOO_LONG 4 /* a segment of cu_seqlens is longer than max_seqlen */
 
 /*
  * Forward.  Writes out [T, Hq, 128] (bf16) and lse [Hq, T] (float32).
@@ -108,18 +118,22 @@ int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* 
  * running under an allocator it does not own (a framework's caching
  * allocator, a fixed pre-reserved memory budget), real-time or embedded
  * callers for which a driver allocation may block or synchronise the device,
- * or paths that must not allocate at all.  This call computes exactly what
- * attn_varlen_bwd computes, with the same arguments, but keeps its scratch
- * (D = rowsum(dout * out), float32 [Hq, T]) in a fixed device array compiled
- * into the library instead of allocating it; it calls no cudaMalloc,
- * cudaFree or other allocating routine.
- *   Limit: T * Hq <= 2,097,152 (8 MiB of scratch); larger problems return
+ * or paths that must not allocate at all.  This call runs the same three
+ * kernels as attn_varlen_bwd, with the same arguments and launch order, and
+ * gives the same bits, but keeps its scratch (D = rowsum(dout * out), float32
+ * [Hq, T], and the dK/dV pass's chain buffers) in a fixed device array
+ * compiled into the library instead of allocating it; it calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   Limit: T * Hq <= 2,097,152.  The array is 50,334,464 bytes (8 MiB of D,
+ *   the chain counters, and the 320 chain buffers of 128 KiB that
+ *   attn_varlen_bwd also uses); larger problems return
  *   ATTN_ERR_NOALLOC_TOO_LARGE before anything is enqueued.  Every GPU that
  *   loads the library holds the array until the process exits.
  *   Sharing: all calls on a device use the same array.  The previous call's
- *   contents are irrelevant (every element read is written first in the same
- *   call), but calls whose GPU work overlaps in time (different streams or
- *   host threads) race on the array; the caller must order them.
+ *   contents are irrelevant (D is overwritten and the chain counters are
+ *   reset at the start of every call), but calls whose GPU work overlaps in
+ *   time (different streams or host threads) race on the array; the caller
+ *   must order them.
  *   Set-up: the first call on each device looks up the array's device
  *   address (with that device current) and caches it; make that first call
  *   before any stream capture.
@@ -161,8 +175,31 @@ int attn_varlen_bwd_strided(const void* dout, const void* q, const void* k, cons
                             void* stream);
 
 /* Bytes of scratch the backward takes from the stream-ordered allocator:
- * D (T * Hq floats, 256-byte padded) plus 40 MiB of chain buffers. */
+ * D (T * Hq floats, 256-byte padded), 2,816 bytes of chain counters, and
+ * 40 MiB of chain buffers.  0 when total <= 0 or num_heads_q <= 0. */
 size_t attn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads_q);
+
+/* The same size, taking the arguments a caller passes to the calls
+ * (num_segments and max_seqlen do not change it; negative values give 0). */
+size_t attn_varlen_workspace_bytes(int64_t total, int32_t num_heads_q, int32_t num_segments, int32_t max_seqlen);
+
+/*
+ * Registers a caller-owned device buffer as the backward's scratch on the
+ * current device (the page's training loop replays a graph over fixed
+ * memory: research.dws.rip/llm/kernels, section 06).  From then on
+ * attn_varlen_bwd and attn_varlen_bwd_strided on this device use it, with
+ * the same kernels, launch order and overlap, and allocate nothing.
+ * dev_ptr must be 256-byte aligned; with
+ * attn_varlen_bwd_workspace_bytes() bytes the results are the same bits as
+ * with the library's own scratch, a smaller buffer (at least T * Hq floats,
+ * 256-byte padded, else a call returns ATTN_ERR_WORKSPACE) splits long
+ * key/value tiles less.  dev_ptr = NULL or bytes = 0 goes back to the
+ * library's own scratch.  The buffer must stay valid while calls that use it
+ * run; calls on one device whose GPU work overlaps race on it.  The library
+ * does not free it.  Returns ATTN_ERR_ALIGNMENT for a misaligned pointer,
+ * ATTN_ERR_DEVICE if the current device is not an sm_103 GPU.
+ */
+int attn_varlen_set_workspace(void* dev_ptr, size_t bytes);
 
 /*
  * The three kernels of attn_varlen_bwd as separate calls, for callers that
@@ -194,8 +231,8 @@ int attn_varlen_bwd_dq(const void* dout, const void* q, const void* k, const voi
 /*
  * Synchronises `stream`, then returns ATTN_OK if no kernel of this library
  * recorded an error on the current device since the last call, else
- * ATTN_ERR_DEVICE_STATUS; *device_code (optional) receives the raw word
- * (1 = a bounded wait timed out, 2 = a CTA work list overflowed).
+ * ATTN_ERR_DEVICE_STATUS; *device_code (optional) receives the raw word,
+ * one of the ATTN_STATUS_* values (the last error recorded).
  * The word is cleared.  For tests and debugging; it blocks the host.
  */
 int attn_varlen_get_status(void* stream, int32_t* device_code);

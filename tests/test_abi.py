@@ -130,3 +130,19 @@ def test_binding_rejects_views_where_the_call_has_no_strides():
         binding.attn_varlen_bwd_preprocess(dense_q, q, torch.zeros(256, dtype=torch.uint8))
     with pytest.raises(ValueError, match="lse"):
         binding.attn_varlen_fwd_strided(q, k, k, cu, 4, -1, 0.088, dense_q, lse.t())
+
+
+def test_workspace_size_calls(clib):
+    clib.attn_varlen_workspace_bytes.restype = ctypes.c_size_t
+    clib.attn_varlen_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
+    clib.attn_varlen_bwd_workspace_bytes.restype = ctypes.c_size_t
+    clib.attn_varlen_bwd_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
+    assert clib.attn_varlen_workspace_bytes(16384, 8, 25, 4096) == clib.attn_varlen_bwd_workspace_bytes(16384, 8)
+    assert clib.attn_varlen_workspace_bytes(16384, 8, -1, 4096) == 0
+    assert clib.attn_varlen_workspace_bytes(0, 8, 1, 0) == 0
+
+
+def test_set_workspace_rejects_a_misaligned_buffer(clib):
+    # The alignment check comes before the device probe: no GPU needed.
+    clib.attn_varlen_set_workspace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    assert clib.attn_varlen_set_workspace(ctypes.c_void_p(256 + 16), 1 << 20) == -4

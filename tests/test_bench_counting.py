@@ -1,7 +1,7 @@
 """The benchmark's counting rules, checked on the CPU against the oracle and
 the definitions they restate: unmasked pairs (the FLOP count's base), the
-algorithmic HBM bytes of a step, and the SURVEY's scratch figures for the
-16K workloads."""
+algorithmic HBM bytes of a step, and the pair counts the input generator
+gives for the named 16K workloads."""
 import numpy as np
 import pytest
 

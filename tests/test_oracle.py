@@ -267,9 +267,16 @@ def test_visible_ranges_and_pair_counts():
         assert r[:, 2].sum() == oracle.unmasked_pairs(cu, window)
         for a, b in ((0, 61), (61, 161), (161, 256)):
             L = b - a
+            i = np.arange(a, b)
             if window < 0:
                 assert r[a:b, 2].sum() == L * (L + 1) // 2
-            assert np.all(r[a:b, 0] >= a) and np.all(r[a:b, 1] == np.arange(a, b))
+                first = np.full(L, a)
+            else:
+                # The window reaches back w keys but never past the segment start.
+                first = np.maximum(a, i - window)
+            np.testing.assert_array_equal(r[a:b, 0], first)
+            np.testing.assert_array_equal(r[a:b, 1], i)
+            np.testing.assert_array_equal(r[a:b, 2], i - first + 1)
     # Closed form for the 3-document workload: 61*62/2 + 100*101/2 + 95*96/2.
     assert oracle.unmasked_pairs(cu, -1) == 1891 + 5050 + 4560
 

@@ -41,6 +41,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.attn_varlen_bwd.restype = ctypes.c_int
     lib.attn_varlen_bwd_workspace_bytes.argtypes = [i64, i32]
     lib.attn_varlen_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_varlen_workspace_bytes.argtypes = [i64, i32, i32, i32]
+    lib.attn_varlen_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_varlen_set_workspace.argtypes = [vp, ctypes.c_size_t]
+    lib.attn_varlen_set_workspace.restype = ctypes.c_int
     lib.attn_varlen_get_status.argtypes = [vp, ctypes.POINTER(i32)]
     lib.attn_varlen_get_status.restype = ctypes.c_int
     lib.attn_varlen_strerror.argtypes = [ctypes.c_int]
@@ -225,6 +229,23 @@ def attn_varlen_bwd_dq(dout, q, k, v, lse, workspace, cu_seqlens, max_seqlen: in
 
 def attn_varlen_bwd_workspace_bytes(total: int, num_heads_q: int) -> int:
     return int(load_library().attn_varlen_bwd_workspace_bytes(int(total), int(num_heads_q)))
+
+
+def attn_varlen_workspace_bytes(total: int, num_heads_q: int, num_segments: int, max_seqlen: int) -> int:
+    return int(load_library().attn_varlen_workspace_bytes(int(total), int(num_heads_q), int(num_segments),
+                                                          int(max_seqlen)))
+
+
+def attn_varlen_set_workspace(workspace) -> None:
+    """Registers a caller-owned CUDA tensor (256-byte aligned) as the backward's
+    scratch on the current device; None goes back to the library's own.  The
+    caller keeps the tensor alive while calls that use it run."""
+    lib = load_library()
+    if workspace is None:
+        _check(lib.attn_varlen_set_workspace(None, 0), "attn_varlen_set_workspace")
+        return
+    wp, wb = _ws(workspace)
+    _check(lib.attn_varlen_set_workspace(wp, wb), "attn_varlen_set_workspace")
 
 
 def attn_varlen_get_status(stream=None) -> int:

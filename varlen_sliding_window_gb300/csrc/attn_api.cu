@@ -31,6 +31,10 @@ struct DeviceInfo {
   // reserved (release threshold: never), so a synchronisation between steps
   // does not hand the memory back and make the next call map it again.
   cudaMemPool_t pool = nullptr;
+  // A caller-registered workspace (attn_varlen_set_workspace): when set,
+  // attn_varlen_bwd uses it instead of the pool.
+  void* user_ws = nullptr;
+  size_t user_ws_bytes = 0;
 };
 
 std::mutex g_mu;
@@ -147,6 +151,7 @@ AttnParams make_params(const int32_t* cu_seqlens, int32_t max_seqlen, int32_t wi
   // A window at least as long as the microbatch is global causal; clamping
   // keeps every index computation far from int overflow.
   a.window = (window_left >= total) ? -1 : window_left;
+  a.max_seqlen = max_seqlen;
   a.max_levels = (max_seqlen + kTile - 1) / kTile;
   a.scale = softmax_scale;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -224,6 +229,24 @@ size_t attn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads_q) {
   return full_workspace_bytes(total, num_heads_q);
 }
 
+size_t attn_varlen_workspace_bytes(int64_t total, int32_t num_heads_q, int32_t num_segments, int32_t max_seqlen) {
+  // The scratch depends on T and Hq only; the other two are accepted so
+  // that a caller can size it from the arguments it passes to the calls.
+  if (num_segments < 0 || max_seqlen < 0) return 0;
+  return attn_varlen_bwd_workspace_bytes(total, num_heads_q);
+}
+
+int attn_varlen_set_workspace(void* dev_ptr, size_t bytes) {
+  if (dev_ptr && (reinterpret_cast<uintptr_t>(dev_ptr) & 255u)) return ATTN_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  const int rc = current_device(&dev);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  dev->user_ws = (dev_ptr && bytes) ? dev_ptr : nullptr;
+  dev->user_ws_bytes = dev->user_ws ? bytes : 0;
+  return ATTN_OK;
+}
+
 }  // extern "C"
 
 namespace {
@@ -290,31 +313,80 @@ int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, con
 
 }  // namespace
 
-namespace {
+namespace vsw {
 
-int bwd_impl(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
-             const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left, float softmax_scale, void* dq,
-             void* dk, void* dv, int64_t total, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
-             int32_t num_segments, const RowStrides* st, void* stream) {
+int check_bwd_call(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+                   const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left, float softmax_scale,
+                   const void* dq, const void* dk, const void* dv, int64_t total, int32_t num_heads_q,
+                   int32_t num_heads_kv, int32_t head_dim, int32_t num_segments) {
+  int rc = validate_common(cu_seqlens, max_seqlen, window_left, softmax_scale, total, num_heads_q, num_heads_kv,
+                           head_dim, num_segments);
+  if (rc) return rc;
+  const void* ptrs[] = {dout, q, k, v, out, lse, dq, dk, dv};
+  for (const void* x : ptrs)
+    if (!x) return ATTN_ERR_NULL_POINTER;
+  for (const void* x : ptrs)
+    if (!aligned16(x)) return ATTN_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  return current_device(&dev);
+}
+
+int bwd_on_workspace(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                     const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                     float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
+                     int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, const RowStrides* st, void* ws,
+                     size_t ws_bytes, void* stream) {
   if (!out || !dq || !dk || !dv) return ATTN_ERR_NULL_POINTER;
   BwdSetup b;
   int rc = prepare_bwd(b, dout, q, k, v, out, lse, nullptr, cu_seqlens, max_seqlen, window_left, softmax_scale, dq,
                        dk, dv, total, num_heads_q, num_heads_kv, head_dim, num_segments, st);
   if (rc || total == 0) return rc;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return ATTN_ERR_ALIGNMENT;
+  if (!carve_workspace(ws, ws_bytes, total, num_heads_q, b.p)) return ATTN_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  const size_t ws_bytes = attn_varlen_bwd_workspace_bytes(total, num_heads_q);
-  if (cudaMallocFromPoolAsync(&ws, ws_bytes, b.dev->pool, s) != cudaSuccess) return ATTN_ERR_ALLOC;
-  carve_workspace(ws, ws_bytes, total, num_heads_q, b.p);
+  // Each kernel starts under the tail of the one before: dK/dV plans while
+  // the preprocess finishes, dQ takes the SMs dK/dV frees.
   int lr = launch_bwd_preprocess(b.p, s);
   b.p.dkdv_after_pre = 1;
   if (!lr) lr = launch_bwd_dkdv(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, s);
   b.p.dkdv_after_pre = 0;
   b.p.dq_after_dkdv = 1;
   if (!lr) lr = launch_bwd_dq(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, s);
+  return lr ? ATTN_ERR_CUDA : ATTN_OK;
+}
+
+}  // namespace vsw
+
+namespace {
+
+int bwd_impl(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+             const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left, float softmax_scale, void* dq,
+             void* dk, void* dv, int64_t total, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
+             int32_t num_segments, const RowStrides* st, void* stream) {
+  int rc = check_bwd_call(dout, q, k, v, out, lse, cu_seqlens, max_seqlen, window_left, softmax_scale, dq, dk, dv,
+                          total, num_heads_q, num_heads_kv, head_dim, num_segments);
+  if (rc || total == 0) return rc;
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev))) return rc;
+  void* user_ws = nullptr;
+  size_t user_bytes = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    user_ws = dev->user_ws;
+    user_bytes = dev->user_ws_bytes;
+  }
+  if (user_ws)
+    return bwd_on_workspace(dout, q, k, v, out, lse, cu_seqlens, max_seqlen, window_left, softmax_scale, dq, dk, dv,
+                            total, num_heads_q, num_heads_kv, head_dim, num_segments, st, user_ws, user_bytes, stream);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  const size_t ws_bytes = full_workspace_bytes(total, num_heads_q);
+  if (cudaMallocFromPoolAsync(&ws, ws_bytes, dev->pool, s) != cudaSuccess) return ATTN_ERR_ALLOC;
+  rc = bwd_on_workspace(dout, q, k, v, out, lse, cu_seqlens, max_seqlen, window_left, softmax_scale, dq, dk, dv, total,
+                        num_heads_q, num_heads_kv, head_dim, num_segments, st, ws, ws_bytes, stream);
   const cudaError_t fr = cudaFreeAsync(ws, s);
-  if (lr != cudaSuccess || fr != cudaSuccess) return ATTN_ERR_CUDA;
-  return ATTN_OK;
+  if (rc) return rc;
+  return fr == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace
@@ -427,7 +499,7 @@ const char* attn_varlen_strerror(int code) {
     case ATTN_ERR_TOO_LARGE: return "problem size beyond the supported range";
     case ATTN_ERR_ALLOC: return "backward scratch allocation failed";
     case ATTN_ERR_DEVICE_STATUS: return "a kernel recorded a device-side error";
-    case ATTN_ERR_WORKSPACE: return "workspace smaller than delta (T * Hq floats) or not 256-byte aligned";
+    case ATTN_ERR_WORKSPACE: return "workspace smaller than delta (T * Hq floats, 256-byte padded)";
     case ATTN_ERR_STRIDE:
       return "a stride is not a positive multiple of 8 elements, a head step is below 128, or a token step "
              "is below head step x heads";

@@ -176,12 +176,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                          kBwdMaxItems, cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
       if (lane == 0) {
         n_items = n < 0 ? 0 : n;
-        if (n < 0) atomicExch(a.status, 2);
+        if (n < 0) atomicExch(a.status, kStatusListOverflow);
       }
     }
   } else if (threadIdx.x == 0) {
     n_items = planned < 0 ? 0 : planned;
-    if (planned < 0) atomicExch(a.status, 2);
+    if (planned < 0) atomicExch(a.status, kStatusListOverflow);
   }
   if (p.dkdv_after_pre) grid_dependency_wait();
   // Extra k-step blocks (after the planner, whose scratch ends at kAugOff):
@@ -377,6 +377,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp < 4) {
     regs_decrease<104>();
+    if (warp == 3 && blockIdx.x == 0) report_long_segments(a);
   } else {
     // ------------------------------------------------------------ elementwise
     // Warpgroup x = query columns [64x, 64x + 64) of every S^T/dP^T tile;
@@ -570,7 +571,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // The swizzled tiles need a 1024-byte-aligned base; there is no static
   // shared memory in this kernel, so the dynamic allocation starts aligned.
   if (sbase & 1023u) {
-    if (threadIdx.x == 0) atomicExch(a.status, 3);
+    if (threadIdx.x == 0) atomicExch(a.status, kStatusSmemAlign);
     return;
   }
   uint8_t* gbase = smem_raw;
@@ -640,12 +641,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                           cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
       if (lane == 0) {
         n_items = n < 0 ? 0 : n;
-        if (n < 0) atomicExch(a.status, 2);
+        if (n < 0) atomicExch(a.status, kStatusListOverflow);
       }
     }
   } else if (threadIdx.x == 0) {
     n_items = planned < 0 ? 0 : planned;
-    if (planned < 0) atomicExch(a.status, 2);
+    if (planned < 0) atomicExch(a.status, kStatusListOverflow);
   }
   tc_fence_before();
   __syncthreads();
@@ -778,6 +779,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp < 4) {
     regs_decrease<104>();
+    if (warp == 3 && blockIdx.x == 0) report_long_segments(a);
   } else {
     // ------------------------------------------------------------ elementwise
     // Warpgroup x = keys [64x, 64x + 64) of every kv tile; thread = query row.

@@ -125,12 +125,12 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
                                           cu + kMaxSegments + 1, blockIdx.x, gridDim.x);
       if (lane == 0) {
         n_items = n < 0 ? 0 : n;
-        if (n < 0) atomicExch(a.status, 2);
+        if (n < 0) atomicExch(a.status, kStatusListOverflow);
       }
     }
   } else if (threadIdx.x == 0) {
     n_items = planned < 0 ? 0 : planned;
-    if (planned < 0) atomicExch(a.status, 2);
+    if (planned < 0) atomicExch(a.status, kStatusListOverflow);
   }
   tc_fence_before();
   __syncthreads();
@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(FwdCfg<NQT>::kThreads, 1)
     }
   } else if (warp < 4) {
     if (NQT == 2) regs_decrease<104>();
+    if (warp == 3 && blockIdx.x == 0) report_long_segments(a);
   } else {
     // ------------------------------------------------------------ softmax
     if (NQT == 2) regs_increase<200>();

@@ -17,6 +17,7 @@ struct AttnParams {
   int hkv;         // key/value heads
   int group;       // hq / hkv
   int window;      // window_left, -1 = global
+  int max_seqlen;  // the caller's bound on every segment length
   int max_levels;  // ceil(max_seqlen / 128)
   float scale;        // softmax_scale
   float scale_log2;   // softmax_scale * log2(e)
@@ -122,5 +123,42 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Units of work (tile x head unit) an upper bound: used to size grids.
 inline long long upper_bound_tiles(long long total, int nseg) { return total / 128 + nseg + 1; }
+
+// Device status words (see attn_varlen_get_status).
+enum : int {
+  kStatusTimeout = 1,        // a bounded wait gave up
+  kStatusListOverflow = 2,   // a CTA's work list did not fit
+  kStatusSmemAlign = 3,      // dynamic shared memory not 1024-byte aligned
+  kStatusSegmentTooLong = 4, // a segment longer than max_seqlen (its tiles past max_seqlen were skipped)
+};
+
+// Run by one warp: reports, through the status word, a segment longer than
+// the caller's max_seqlen.  The kernels' work lists only reach max_seqlen
+// (rounded up to a whole tile), so such a segment's later rows are not
+// computed; the call itself cannot see cu_seqlens, which lives on the device.
+__device__ __forceinline__ void report_long_segments(const AttnParams& a) {
+  const int lane = threadIdx.x & 31;
+  bool bad = false;
+  for (int s = lane; s < a.nseg; s += 32) bad |= (a.cu_seqlens[s + 1] - a.cu_seqlens[s]) > a.max_seqlen;
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicExch(a.status, kStatusSegmentTooLong);
+}
+
+// The whole backward (preprocess, dK/dV pass, dQ pass, each kernel starting
+// under the tail of the one before) on a caller-provided workspace of
+// ws_bytes bytes (256-byte aligned, at least delta_bytes(total, hq)).  st:
+// dout, q, k, v, out, dq, dk, dv (null: all dense).  Validates everything
+// itself; returns an ATTN_* code.
+int bwd_on_workspace(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                     const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
+                     float softmax_scale, void* dq, void* dk, void* dv, int64_t total, int32_t num_heads_q,
+                     int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, const RowStrides* st, void* ws,
+                     size_t ws_bytes, void* stream);
+
+// Argument and device checks shared by the backward entry points, in the
+// order every entry point applies them (arguments first, then the device).
+int check_bwd_call(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+                   const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left, float softmax_scale,
+                   const void* dq, const void* dk, const void* dv, int64_t total, int32_t num_heads_q,
+                   int32_t num_heads_kv, int32_t head_dim, int32_t num_segments);
 
 }  // namespace vsw
