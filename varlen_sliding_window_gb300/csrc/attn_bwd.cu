@@ -62,29 +62,6 @@ __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]
 constexpr int kBwdThreads = 384;
 constexpr int kBwdMaxItems = 96;  // work units one CTA may own
 
-// Spins (bounded) until *flag >= target, reading with acquire semantics at GPU
-// scope.  The flag is published by another CTA of the same grid that holds an
-// earlier unit of the global order, so it is resident and makes progress.
-__device__ __forceinline__ bool wait_flag_at_least(const int* flag, int target, volatile int* abort_flag,
-                                                   int* status) {
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    if (v >= target) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > VSW_WAIT_TIMEOUT_NS) {
-      *abort_flag = 1;
-      if (status) atomicExch(status, kDevTimeout);
-      return false;
-    }
-    __nanosleep(64);
-  }
-}
-__device__ __forceinline__ void store_release(int* flag, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
-}
-
 // ============================================================== dK / dV pass
 struct DkvCfg {
   static constexpr int kStages = 2;  // Q/dO tile pairs in flight
@@ -122,6 +99,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_ds_full[2];
   __shared__ __align__(8) uint64_t bar_acc_full, bar_acc_empty;
   __shared__ __align__(8) uint64_t bar_chain[2];
+  __shared__ int chain_last[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -472,47 +450,79 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           store_rows32_bf16(dst_row, dst_st.token * 2, c * 32, r, mul, valid);
         }
       } else {
-        // A chunk of a split kv item: add the partial sums of the earlier
-        // chunks in chunk order (fp32, through the chain buffer), then
-        // either pass the running sum on or, as the last chunk, store it.
+        // A chunk of a split kv item.  Every chunk writes its fp32 partial sums
+        // to a buffer of its own; the warpgroup that arrives last (an atomic
+        // count per chain) adds all of them in chunk order and stores the
+        // result.  The order of the additions is fixed, so the bits do not
+        // depend on which chunk finishes last, and no chunk ever waits for
+        // another CTA.
         const int li = link_index(w), lk = link_count(w);
+        constexpr size_t kBuf = 128 * 128;
         // Buffer layout [32 groups of 4 columns][128 rows][4]: a warp's 32 rows
         // read or write 512 contiguous bytes per group (coalesced).
-        float* buf = p.chains + ((size_t)w.chain * 2 + x) * (128 * 128) + (size_t)row * 4;
-        int* prog = p.chain_progress + w.chain * 2 + x;
-        if (li > 0 && !(ok = __all_sync(0xffffffffu, wait_flag_at_least(prog, li, &abort_flag, a.status)))) break;
+        float* chain0 = p.chains + ((size_t)w.chain * 2 + x) * kBuf + (size_t)row * 4;
+        float* mine = chain0 + (size_t)li * 2 * kBuf;
+        int* arrivals = p.chain_progress + w.chain * 2 + x;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
           tmem_ld32(tacc + c * 32, r);
           tmem_wait_ld(r);
-          if (li > 0) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              const float4 prev = __ldcg(reinterpret_cast<const float4*>(buf + ((c * 32 + e) >> 2) * 512));
-              r[e + 0] = __float_as_uint(__uint_as_float(r[e + 0]) + prev.x);
-              r[e + 1] = __float_as_uint(__uint_as_float(r[e + 1]) + prev.y);
-              r[e + 2] = __float_as_uint(__uint_as_float(r[e + 2]) + prev.z);
-              r[e + 3] = __float_as_uint(__uint_as_float(r[e + 3]) + prev.w);
-            }
-          }
-          if (li == lk - 1) {
-            store_rows32_bf16(dst_row, dst_st.token * 2, c * 32, r, mul, valid);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              __stcg(reinterpret_cast<float4*>(buf + ((c * 32 + e) >> 2) * 512),
-                     make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
-                                 __uint_as_float(r[e + 3])));
-          }
+          for (int e = 0; e < 32; e += 4)
+            __stcg(reinterpret_cast<float4*>(mine + ((c * 32 + e) >> 2) * 512),
+                   make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                               __uint_as_float(r[e + 3])));
         }
-        if (li < lk - 1) {
-          // Publish once every row of this warpgroup has written its part.
+        // Every row of the warpgroup has written its part (each thread fences
+        // its own stores first), then one thread counts the arrival.
+        __threadfence();
+        mbar_arrive(smem_u32(&bar_chain[x]));
+        if (!(ok = mbar_wait_warp(smem_u32(&bar_chain[x]), chain_uses & 1, &abort_flag, a.status))) break;
+        ++chain_uses;
+        if (row == 0) {
+          // The last arrival also resets the count (every chunk of the chain
+          // has counted by then), so the pass can run again on the same
+          // workspace; the preprocess resets it as well.
+          const bool last = atomicAdd(arrivals, 1) == lk - 1;
+          if (last) atomicExch(arrivals, 0);
+          chain_last[x] = last;
+        }
+        mbar_arrive(smem_u32(&bar_chain[x]));
+        if (!(ok = mbar_wait_warp(smem_u32(&bar_chain[x]), chain_uses & 1, &abort_flag, a.status))) break;
+        ++chain_uses;
+        if (chain_last[x]) {
+          // Sum in chunk order, 64 columns at a time: every other chunk's
+          // partial comes from L2 (16 loads in flight per thread), this
+          // chunk's own from TMEM, where it still is.
           __threadfence();
-          mbar_arrive(smem_u32(&bar_chain[x]));
-          if (!(ok = mbar_wait_warp(smem_u32(&bar_chain[x]), chain_uses & 1, &abort_flag, a.status))) break;
-          ++chain_uses;
-          if (row == 0) store_release(prog, li + 1);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t acc[64];
+            for (int q = 0; q < lk; ++q) {
+              uint32_t v[64];
+              if (q == li) {
+                tmem_ld64_wait(tacc + 64 * half, v);
+              } else {
+                const float* src = chain0 + (size_t)q * 2 * kBuf + (size_t)(16 * half) * 512;
+#pragma unroll
+                for (int g = 0; g < 16; ++g) {
+                  const float4 f = __ldcg(reinterpret_cast<const float4*>(src + g * 512));
+                  v[4 * g + 0] = __float_as_uint(f.x);
+                  v[4 * g + 1] = __float_as_uint(f.y);
+                  v[4 * g + 2] = __float_as_uint(f.z);
+                  v[4 * g + 3] = __float_as_uint(f.w);
+                }
+              }
+#pragma unroll
+              for (int e = 0; e < 64; ++e)
+                acc[e] = q == 0 ? v[e] : __float_as_uint(__uint_as_float(acc[e]) + __uint_as_float(v[e]));
+            }
+            store_rows32_bf16(dst_row, dst_st.token * 2, 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&acc[0]), mul,
+                              valid);
+            store_rows32_bf16(dst_row, dst_st.token * 2, 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&acc[32]),
+                              mul, valid);
+          }
         }
       }
       tc_fence_before();
@@ -899,12 +909,8 @@ int launch_bwd_dkdv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtens
                                        (int)DkvCfg::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
   const long long g = persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hkv, num_sms, kBwdMaxItems);
-  // A chunk waits for the chunk before it in its chain, which belongs to
-  // another CTA; that is only safe while every CTA of the grid is resident.
-  BwdParams q = p;
-  if (g > num_sms) q.chains_max = 0;
   return (int)launch_pdl(attn_bwd_dkdv_kernel, dim3((unsigned)g), dim3(kBwdThreads), DkvCfg::kSmemBytes, stream, tmQ,
-                         tmK, tmV, tmDO, q);
+                         tmK, tmV, tmDO, p);
 }
 
 int launch_bwd_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,

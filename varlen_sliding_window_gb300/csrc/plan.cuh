@@ -10,8 +10,9 @@
 // CTA derives the same order), then dealt to the G CTAs in a snake: round r
 // holds units r G .. r G + G - 1, dealt left to right on even rounds and right
 // to left on odd ones.  Each CTA expands only its own units (one per round,
-// in increasing global order); a chunk of a split item always comes after the
-// chunk before it, which keeps the dK/dV chain reduction free of deadlock.
+// in increasing global order).  The chunks of a split item are independent:
+// each writes its partial sums to a buffer of its own and the last one to
+// finish adds them in chunk order (see the dK/dV kernel).
 // The dealing rule is the one of the single-warp builder in sched.cuh, but
 // every step here runs on all threads of the CTA: the prologue goes from
 // thousands of dependent shared-memory steps to a few dozen barriers.
@@ -147,7 +148,7 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
   int* s_cu = scratch;                          // [nseg + 1]
   int* s_tiles = s_cu + (nseg + 1);             // [nseg + 1] tile prefix
   int* s_cost = s_tiles + (nseg + 1);           // [kPlanMaxItems + 1]
-  int* s_sbase = s_cost + (kPlanMaxItems + 1);  // split-item prefix
+  int* s_sbase = s_cost + (kPlanMaxItems + 1);  // prefix of the chunk counts of split items
   int* s_order = s_sbase + (kPlanMaxItems + 1); // [kPlanMaxChunks] item | chunk << 16
   int* s_base = s_order + kPlanMaxChunks;       // [kCostBuckets] size histogram, then bucket cursors
   int* s_misc = s_base + kCostBuckets;          // [64]: scan scratch
@@ -205,28 +206,29 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
   }
   int total_cost, max_cost;
   block_sum_max(my_total, my_max, s_misc, total_cost, max_cost);
-  // ---- 3. split limit C (streamed tiles per chunk), as in sched.cuh
+  // ---- 3. split limit C (streamed tiles per chunk), as in sched.cuh: every
+  // chunk of a split item needs a partial-sum buffer per unit
   int C = 0x7fffffff;
   if (chains_max > 0) {
     const long long avg = ((long long)total_cost * U + G - 1) / G;
     C = max(5, (int)((avg + 1) / 2));
     while (C < max_cost) {
       int mine = 0;
-      for (int e = tid; e < n_items; e += nt) mine += s_cost[e] > C;
-      const int nsplit = block_sum(mine, s_misc);
-      if ((long long)nsplit * U <= chains_max) break;
+      for (int e = tid; e < n_items; e += nt) mine += s_cost[e] > C ? (s_cost[e] + C - 1) / C : 0;
+      const int nbuf = block_sum(mine, s_misc);
+      if ((long long)nbuf * U <= chains_max) break;
       C *= 2;
     }
     if (C >= max_cost) C = 0x7fffffff;
   }
-  // ---- 4. chunks per item; split items get consecutive chain slots (a
-  // prefix sum, only when something is split)
+  // ---- 4. chunks per item; the chunks of split items get consecutive
+  // buffers (a prefix sum of their chunk counts, only when something is split)
   int my_chunks = 0;
   for (int e = tid; e < n_items; e += nt) {
     const int c = s_cost[e];
     const int k = c == 0 ? 0 : (c <= C ? 1 : (c + C - 1) / C);
     my_chunks += k;
-    if (C != 0x7fffffff) s_sbase[e] = k > 1;
+    if (C != 0x7fffffff) s_sbase[e] = k > 1 ? k : 0;
   }
   const int n_chunks = block_sum(my_chunks, s_misc);
   if (C != 0x7fffffff) block_exclusive_scan(s_sbase, n_items, s_misc);
@@ -341,7 +343,8 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
     w.unit = h;
     w.t0 = r0 + ci * base + min(ci, rem);
     w.t1 = w.t0 + base + (ci < rem ? 1 : 0) - 1;
-    w.chain = k > 1 ? s_sbase[e] * U + h : -1;
+    // Chain of (item, unit): buffers base .. base + k - 1, one per chunk.
+    w.chain = k > 1 ? s_sbase[e] * U + h * k : -1;
     w.link = ci | (k << 16);
     w.order = u;
   }

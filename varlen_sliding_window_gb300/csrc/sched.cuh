@@ -9,20 +9,18 @@
 // range is longer than a limit C is cut into chunks of at most C streamed
 // tiles: a kv tile near the start of a long segment is seen by many q tiles
 // and would otherwise be one unit much larger than a CTA's fair share.  The
-// chunks of an item form a chain that is reduced in chunk order (see the
-// dK/dV kernel), so results stay bitwise reproducible.  C is half the
-// average per-CTA cost (at least 5 tiles), doubled until the split items fit
-// in the available chain slots.
+// chunks of an item form a chain: each writes its partial sums to a buffer
+// of its own and the last to finish adds them in chunk order (see the dK/dV
+// kernel), so results stay bitwise reproducible.  C is half the average
+// per-CTA cost (at least 5 tiles), doubled until the chunks of the split
+// items fit in the available buffers.
 //
 // Every chunk (or unsplit item) expands into `units_per_item` units (heads or
 // head groups) of equal cost.  Units are ordered by cost, largest first, with
 // a counting sort whose ranks are computed warp-synchronously (so every CTA
 // derives the same global order), then dealt to CTAs in a snake: unit u in
 // round r = u / G goes to CTA u % G on even rounds and G-1-(u % G) on odd
-// rounds.  Each CTA keeps its own units, in global order.  A chunk's
-// predecessor in its chain always has a smaller global position, which keeps
-// the chained reduction free of deadlock (the smallest unfinished unit can
-// always proceed).
+// rounds.  Each CTA keeps its own units, in global order.
 #pragma once
 #include <cstdint>
 
@@ -37,7 +35,7 @@ struct WorkItem {
   int unit;   // head / head-group index
   int t0;     // first streamed tile (inside the segment)
   int t1;     // last streamed tile
-  int chain;  // -1: not split; else the chain slot of this (item, unit)
+  int chain;  // -1: not split; else the first partial-sum buffer of this (item, unit)
   int link;   // chunk index in the chain (low 16 bits) | number of chunks << 16
   int order;  // global position of the unit (the CTA processes its units in this order)
 };
@@ -143,17 +141,19 @@ __device__ __noinline__ int build_schedule(const int* cu, int nseg, int window, 
     const long long avg = ((long long)total_cost * units_per_item + G - 1) / G;  // tiles per CTA
     C = max(5, (int)((avg + 1) / 2));
     while (C < max_cost) {
-      int nsplit = 0;
+      int nbuf = 0;  // chunks of split items
       for (int e0 = 0; e0 < n_items; e0 += 32) {
         const int e = e0 + lane;
-        bool split = false;
+        int k = 0;
         if (e < n_items) {
           int lo, hi, t, r0, r1;
-          split = item_range(e, lo, hi, t, r0, r1) > C;
+          const int c = item_range(e, lo, hi, t, r0, r1);
+          k = c > C ? (c + C - 1) / C : 0;
         }
-        nsplit += __popc(__ballot_sync(0xffffffffu, split));
+        for (int o = 16; o > 0; o >>= 1) k += __shfl_xor_sync(0xffffffffu, k, o);
+        nbuf += k;
       }
-      if ((long long)nsplit * units_per_item <= chains_max) break;
+      if ((long long)nbuf * units_per_item <= chains_max) break;
       C *= 2;
     }
     if (C >= max_cost) C = 0x7fffffff;
@@ -200,7 +200,7 @@ __device__ __noinline__ int build_schedule(const int* cu, int nseg, int window, 
   __syncwarp();
   // ---- pass 2: positions (deterministic ranks), deal units, keep own
   bool overflow = false;
-  int split_seen = 0;  // split items enumerated so far (same in every lane)
+  int split_seen = 0;  // chunks of the split items enumerated so far (same in every lane)
   for (int e0 = 0; e0 < n_items; e0 += 32) {
     const int e = e0 + lane;
     int lo = 0, hi = 0, t = 0, r0 = 0, r1 = -1, k = 0;
@@ -210,10 +210,16 @@ __device__ __noinline__ int build_schedule(const int* cu, int nseg, int window, 
     }
     const int c = r1 - r0 + 1;
     const int base = k ? c / k : 0, rem = k ? c % k : 0;
-    // Chain slot base of this lane's item (split items in enumeration order).
-    const unsigned split_mask = __ballot_sync(0xffffffffu, k > 1);
-    const int chain_base = (k > 1) ? (split_seen + __popc(split_mask & lt_mask)) * units_per_item : -1;
-    split_seen += __popc(split_mask);
+    // First buffer of this lane's item: split items in enumeration order, k
+    // buffers per split item and unit.
+    const int ks = k > 1 ? k : 0;
+    int kincl = ks;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, kincl, o);
+      if (lane >= o) kincl += y;
+    }
+    const int chain_base = (k > 1) ? (split_seen + kincl - ks) * units_per_item : -1;
+    split_seen += __shfl_sync(0xffffffffu, kincl, 31);
     int kmax = k;
     for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
     int start = r0;
@@ -244,7 +250,7 @@ __device__ __noinline__ int build_schedule(const int* cu, int nseg, int window, 
               w.unit = h;
               w.t0 = start;
               w.t1 = start + size - 1;
-              w.chain = (k > 1) ? chain_base + h : -1;
+              w.chain = (k > 1) ? chain_base + h * k : -1;
               w.link = i | (k << 16);
               w.order = u;
             } else {
