@@ -124,9 +124,9 @@ int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* 
  * [Hq, T], and the dK/dV pass's chain buffers) in a fixed device array
  * compiled into the library instead of allocating it; it calls no
  * cudaMalloc, cudaFree or other allocating routine.
- *   Limit: T * Hq <= 2,097,152.  The array is 50,334,464 bytes (8 MiB of D,
- *   the chain counters, and the 320 chain buffers of 128 KiB that
- *   attn_varlen_bwd also uses); larger problems return
+ *   Limit: T * Hq <= 2,097,152.  The array is 52,693,760 bytes (8 MiB of D,
+ *   the counters and work lists of the two passes, and the 320 chain
+ *   buffers of 128 KiB that attn_varlen_bwd also uses); larger problems return
  *   ATTN_ERR_NOALLOC_TOO_LARGE before anything is enqueued.  Every GPU that
  *   loads the library holds the array until the process exits.
  *   Sharing: all calls on a device use the same array.  The previous call's
@@ -175,8 +175,9 @@ int attn_varlen_bwd_strided(const void* dout, const void* q, const void* k, cons
                             void* stream);
 
 /* Bytes of scratch the backward takes from the stream-ordered allocator:
- * D (T * Hq floats, 256-byte padded), 2,816 bytes of chain counters, and
- * 40 MiB of chain buffers.  0 when total <= 0 or num_heads_q <= 0. */
+ * D (T * Hq floats, 256-byte padded), 2,816 bytes of counters, two lists of
+ * work items the passes claim at run time (2 x 32,768 x 36 bytes), and 40 MiB
+ * of chain buffers.  0 when total <= 0 or num_heads_q <= 0. */
 size_t attn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads_q);
 
 /* The same size, taking the arguments a caller passes to the calls

@@ -99,7 +99,8 @@ def test_strided_calls_check_their_strides(clib):
 def test_workspace_bytes(clib):
     clib.attn_varlen_bwd_workspace_bytes.restype = ctypes.c_size_t
     clib.attn_varlen_bwd_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
-    chains = 2816 + 320 * 2 * 128 * 128 * 4
+    # counters, two run-time work lists of 32,768 36-byte items, 320 chain buffers
+    chains = 2816 + 2 * 32768 * 36 + 320 * 2 * 128 * 128 * 4
     assert clib.attn_varlen_bwd_workspace_bytes(16384, 8) == 16384 * 8 * 4 + chains
     assert clib.attn_varlen_bwd_workspace_bytes(0, 8) == 0
     assert clib.attn_varlen_bwd_workspace_bytes(3, 1) == 256 + chains

@@ -101,3 +101,27 @@ def test_segment_longer_than_max_seqlen_is_reported():
     binding.attn_varlen_fwd(q, k, v, cu, longest, wl.window_left, wl.softmax_scale, out, lse)
     binding.attn_varlen_bwd(do, q, k, v, out, lse, cu, longest, wl.window_left, wl.softmax_scale, dq, dk, dv)
     assert binding.attn_varlen_get_status() == 0
+
+
+@pytest.mark.parametrize("name", ["ctx4096_global", "ctx512_global"])
+def test_sub_step_calls_repeat_on_one_workspace(name):
+    """The three backward kernels as separate calls on one caller workspace,
+    the dK/dV and dQ passes each run twice without a preprocess in between:
+    their run-time counters (split-item arrivals, claimed units) reset
+    themselves, so every repeat gives the one-call backward's bits."""
+    import torch
+    from varlen_sliding_window_gb300 import binding
+    wl = WL[name]
+    q, k, v, do, cu, out, lse = t = _setup(wl)
+    binding.attn_varlen_get_status()
+    ref = _bwd(wl, t)
+    ws = torch.empty(binding.attn_varlen_bwd_workspace_bytes(wl.total, wl.hq), dtype=torch.uint8, device="cuda")
+    binding.attn_varlen_bwd_preprocess(do, out, ws)
+    for _ in range(2):
+        dq, dk, dv = (torch.full_like(x, float("nan")) for x in (q, k, v))
+        binding.attn_varlen_bwd_dkdv(do, q, k, v, lse, ws, cu, wl.context, wl.window_left, wl.softmax_scale, dk, dv)
+        binding.attn_varlen_bwd_dq(do, q, k, v, lse, ws, cu, wl.context, wl.window_left, wl.softmax_scale, dq)
+        torch.cuda.synchronize()
+        for nm, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+            assert torch.equal(a, b), nm
+    assert binding.attn_varlen_get_status() == 0

@@ -298,6 +298,8 @@ int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, con
   b.p.chains = nullptr;
   b.p.chain_progress = nullptr;
   b.p.chains_max = 0;
+  b.p.sched = nullptr;
+  b.p.unit_lists = nullptr;
   b.p.dq_after_dkdv = 0;
   b.p.dkdv_after_pre = 0;
   b.p.dq = dq;

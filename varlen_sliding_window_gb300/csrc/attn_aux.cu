@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __rest
   // Everything before this kernel is complete: the next kernel may start
   // (it waits for this one before reading what it writes).
   grid_dependents_launch();
-  // The dK/dV pass that follows counts published chain links from zero.
+  // The passes that follow count chain arrivals and claimed units from zero.
   if (blockIdx.x == 0)
     for (int e = threadIdx.x; e < nprogress; e += blockDim.x) chain_progress[e] = 0;
   const long long rows = (long long)total * hq;
@@ -159,7 +159,7 @@ int launch_bwd_preprocess(const BwdParams& p, cudaStream_t stream) {
   return (int)launch_pdl(dense ? bwd_preprocess_kernel<true> : bwd_preprocess_kernel<false>, dim3((unsigned)blocks),
                          dim3(256), 0, stream,
                          static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.out), p.delta, p.a.total,
-                         p.a.hq, p.dout_st, p.out_st, p.chain_progress, p.chain_progress ? 2 * p.chains_max : 0);
+                         p.a.hq, p.dout_st, p.out_st, p.chain_progress, p.chain_progress ? kProgressInts : 0);
 }
 
 int launch_mask_probe(const int* cu_seqlens, int nseg, int total, int window, int max_levels, int by_key,

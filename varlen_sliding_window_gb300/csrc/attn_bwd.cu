@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 
 #include "attn_internal.h"
+#include "claim.cuh"
 #include "mask.cuh"
 #include "plan.cuh"
 #include "ptx.cuh"
@@ -41,6 +42,8 @@
 #include "tiles.cuh"
 
 namespace vsw {
+
+static_assert(sizeof(WorkItem) == kWorkItemBytes, "the workspace sizes its unit lists with this");
 
 namespace {
 
@@ -558,17 +561,24 @@ struct DqCfg {
 // nothing is declared statically and no alignment slack is spent).
 struct DqState {
   WorkItem items[DqCfg::kMaxItems];
+  WorkItem ring[2];  // the items in flight, handed from the claiming warp to the other roles
+  uint64_t item_full[2], item_taken[2], item_empty[2];
   uint64_t q_full, q_empty;
   uint64_t k_full[DqCfg::kKStages], k_empty[DqCfg::kKStages];
   uint64_t v_full[DqCfg::kVStages], v_empty[DqCfg::kVStages];
   uint64_t s_full[2], p_full[2][2];  // p_full[buffer][half]
   uint64_t dp_full, dp_free, acc_full, acc_empty;
   int n_items;
+  int claim_mode;  // units are claimed at run time from the workspace list
+  int n_units;     // size of that list
+  int planner;     // this CTA writes the list
+  int* claim_words;  // kept here, not in a register, for the end of the kernel
   uint32_t tmem_slot;
   int abort_flag;
 };
 
 constexpr uint32_t kDqSmemBytes = DqCfg::kStateOff + sizeof(DqState);
+static_assert(kDqSmemBytes <= 227 * 1024, "the dQ kernel's shared memory fits one CTA per SM");
 
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -623,6 +633,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&bar_dp_free), 256);
     mbar_init(smem_u32(&bar_acc_full), 1);
     mbar_init(smem_u32(&bar_acc_empty), 256);
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(smem_u32(&st.item_full[r]), 1);
+      mbar_init(smem_u32(&st.item_taken[r]), 1);
+      mbar_init(smem_u32(&st.item_empty[r]), 10);  // the producer, the MMA thread, the 8 elementwise warps
+    }
     fence_mbar_init();
     tma_prefetch_map(&tmQ);
     tma_prefetch_map(&tmK);
@@ -639,9 +654,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // wait (so delta and every input are complete), and it writes nothing this
   // kernel reads.
   if (!p.dq_after_dkdv) grid_dependency_wait();
-  const int planned = plan_schedule<false>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hq, 0, items,
-                                           C::kMaxItems, reinterpret_cast<int*>(gbase), (int)(C::kStateOff / 4),
-                                           blockIdx.x, gridDim.x);
+  // Work list: with a workspace for it, one CTA writes the whole
+  // longest-first list and every CTA claims units at run time (claim.cuh);
+  // otherwise, or when the list does not fit, every CTA plans its own share.
+  int* const cw = p.sched ? p.sched + kSchedWords : nullptr;
+  WorkItem* const clist = cw ? reinterpret_cast<WorkItem*>(p.unit_lists) + kMaxDynUnits : nullptr;
+  if (threadIdx.x == 0) {
+    st.claim_mode = 0;
+    st.planner = cw ? claim_elect(cw) : 0;
+    st.claim_words = cw;
+  }
+  __syncthreads();
+  // Pass 0: the elected CTA writes the list.  Pass 1: every CTA, if the list
+  // is not used, plans its own share.  (One call site for both.)
+  int planned = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool run = pass == 0 ? st.planner != 0 : !st.claim_mode && !abort_flag;
+    if (run)
+      planned = plan_schedule<false>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hq, 0, items, C::kMaxItems,
+                                     reinterpret_cast<int*>(gbase), (int)(C::kStateOff / 4), blockIdx.x, gridDim.x,
+                                     pass == 0 ? clist : nullptr, kMaxDynUnits);
+    if (pass == 0) {
+      if (st.planner && threadIdx.x == 0) claim_publish(cw, planned);
+      if (cw && threadIdx.x == 0) {
+        const int state = claim_wait(cw, abort_ptr, a.status);
+        st.claim_mode = state == kClaimReady;
+        st.n_units = st.claim_mode ? __ldcg(cw + 3) : 0;
+        n_items = 0;
+      }
+      __syncthreads();
+      planned = 0;
+    }
+  }
   if (planned == kPlanDoesNotFit) {
     if (warp == 3) {
       int* cu = reinterpret_cast<int*>(gbase + C::kKOff);
@@ -654,7 +698,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (n < 0) atomicExch(a.status, kStatusListOverflow);
       }
     }
-  } else if (threadIdx.x == 0) {
+  } else if (threadIdx.x == 0 && !st.claim_mode) {
     n_items = planned < 0 ? 0 : planned;
     if (planned < 0) atomicExch(a.status, kStatusListOverflow);
   }
@@ -663,6 +707,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const int nit = n_items;
+  const bool claim = st.claim_mode;
+  const int n_units = st.n_units;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -670,8 +716,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       int kc = 0, vc = 0;  // K and V tiles loaded so far
       bool ok = true;
-      for (int it = 0; it < nit && ok; ++it) {
-        const WorkItem w = items[it];
+      for (int it = 0; ok; ++it) {
+        const int rs = it & 1;
+        if (!(ok = mbar_wait(smem_u32(&st.item_full[rs]), (it >> 1) & 1, &abort_flag, a.status))) break;
+        const WorkItem w = st.ring[rs];
+        mbar_arrive(smem_u32(&st.item_empty[rs]));
+        if (w.blk < 0) break;
         const int q0 = w.seg_lo + w.blk * kTile;
         const int n0 = w.t0;
         const int h = w.unit, g = h / a.group;
@@ -746,8 +796,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_commit(smem_u32(&st.v_empty[cc % C::kVStages]));  // V(cc) is free once dP(cc) is done
         return true;
       };
-      for (int it = 0; it < nit && ok; ++it) {
-        const WorkItem w = items[it];
+      for (int it = 0; ok; ++it) {
+        const int rs = it & 1;
+        if (!(ok = mbar_wait(smem_u32(&st.item_full[rs]), (it >> 1) & 1, &abort_flag, a.status))) break;
+        const WorkItem w = st.ring[rs];
+        mbar_arrive(smem_u32(&st.item_taken[rs]));
+        mbar_arrive(smem_u32(&st.item_empty[rs]));
+        if (w.blk < 0) break;
         const int nt = w.t1 - w.t0 + 1;
         if (!(ok = mbar_wait(smem_u32(&bar_q_full), it & 1, &abort_flag, a.status))) break;
         tc_fence_after();
@@ -789,7 +844,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp < 4) {
     regs_decrease<104>();
-    if (warp == 3 && blockIdx.x == 0) report_long_segments(a);
+    if (warp == 2 && blockIdx.x == 0) report_long_segments(a);
+    if (warp == 3 && lane == 0) {
+      // ------------------------------------------------------------ items
+      // The next item: claimed from the list, or the next of this CTA's
+      // share.  It goes to the other roles through a two-slot ring; an item
+      // with blk < 0 tells them there is no more work.  The next claim is
+      // made once the MMA thread has started the item before it (one item of
+      // look-ahead: the claim's round trip to L2 overlaps that item's work,
+      // and a CTA never holds more than one unit it has not started).
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        WorkItem w;
+        bool have;
+        if (claim) {
+          const int u = claim_next(cw);
+          have = u < n_units;
+          if (have) w = claim_item(clist, u);
+        } else {
+          have = it < nit;
+          if (have) w = items[it];
+        }
+        if (!have) w.blk = -1;
+        const int rs = it & 1;
+        if (it >= 2 && !(ok = mbar_wait(smem_u32(&st.item_empty[rs]), ((it >> 1) - 1) & 1, &abort_flag, a.status)))
+          break;
+        st.ring[rs] = w;
+        mbar_arrive(smem_u32(&st.item_full[rs]));
+        if (!have) break;
+        if (!(ok = mbar_wait(smem_u32(&st.item_taken[rs]), (it >> 1) & 1, &abort_flag, a.status))) break;
+      }
+    }
   } else {
     // ------------------------------------------------------------ elementwise
     // Warpgroup x = keys [64x, 64x + 64) of every kv tile; thread = query row.
@@ -800,8 +885,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
     int c = 0;
     bool ok = true;
-    for (int it = 0; it < nit && ok; ++it) {
-      const WorkItem w = items[it];
+    for (int it = 0; ok; ++it) {
+      const int rs = it & 1;
+      if (!(ok = mbar_wait_warp(smem_u32(&st.item_full[rs]), (it >> 1) & 1, &abort_flag, a.status))) break;
+      const WorkItem w = st.ring[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&st.item_empty[rs]));
+      if (w.blk < 0) break;
       const int q0 = w.seg_lo + w.blk * kTile;
       const int h = w.unit;
       const int i = q0 + row;  // this thread's query token
@@ -877,6 +967,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (threadIdx.x == 0 && st.claim_words) claim_finish(st.claim_words);
   // Finish no earlier than the kernel before (stream order for what follows).
   grid_dependency_wait();
 }
@@ -919,8 +1010,13 @@ int launch_bwd_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensor
       cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmemBytes);
   if (e != cudaSuccess) return (int)e;
   const long long g = persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hq, num_sms, DqCfg::kMaxItems);
+  // Run-time claiming pays off when units differ in size (a unit has up to
+  // max_seqlen / 128 kv tiles); at contexts of up to 512 tokens (four tiles)
+  // the fixed longest-first shares are as even and cost no claims.
+  BwdParams q = p;
+  if (q.a.max_levels <= 4) q.sched = nullptr;
   return (int)launch_pdl(attn_bwd_dq_kernel, dim3((unsigned)g), dim3(kBwdThreads), kDqSmemBytes, stream, tmQ,
-                         tmK, tmV, tmDO, p);
+                         tmK, tmV, tmDO, q);
 }
 
 }  // namespace vsw

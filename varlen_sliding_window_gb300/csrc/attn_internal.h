@@ -47,10 +47,15 @@ struct BwdParams {
   void* dq;          // bf16 [T, hq, 128]
   void* dk;          // bf16 [T, hkv, 128]
   void* dv;          // bf16 [T, hkv, 128]
-  // dK/dV chains (split kv items reduced in order), scratch:
+  // dK/dV chains (split kv items, one partial-sum buffer per chunk), scratch:
   float* chains;         // fp32 [chains_max][2][128][128] partial dV, dK
-  int* chain_progress;   // int [chains_max][2], links published so far
+  int* chain_progress;   // int [chains_max][2] arrival counts, then the scheduling words
   int chains_max;        // 0 disables splitting
+  // Run-time work claiming (null: every CTA deals itself a fixed share):
+  // kSchedWords ints per pass (dK/dV first, then dQ) and a unit list of
+  // kMaxDynUnits work items per pass.
+  int* sched;
+  void* unit_lists;
   // Set when the dQ kernel is launched right after the dK/dV kernel of the
   // same backward: it then needs nothing that kernel writes, starts on the
   // SMs the dK/dV kernel frees and waits for it only before exiting.
@@ -61,16 +66,27 @@ struct BwdParams {
   RowStrides dout_st, out_st, dq_st, dk_st, dv_st;
 };
 
-// Backward workspace layout: delta, chain progress counters, chain buffers.
+// Backward workspace layout: delta, the counter area (chain arrival counts,
+// then the scheduling words of the two passes), the two unit lists, the chain
+// buffers.
 constexpr int kMaxChains = 320;
 constexpr size_t kChainBytes = 2ull * 128 * 128 * sizeof(float);
-constexpr size_t kProgressBytes = 2816;  // >= kMaxChains * 2 * 4, rounded to 256
+constexpr size_t kProgressBytes = 2816;  // kMaxChains * 2 ints, then the scheduling words; 256-byte multiple
+constexpr int kSchedWordsOffset = 2 * kMaxChains;  // ints into the counter area
+constexpr int kSchedWords = 4;  // per pass: state, next unit, CTAs done, number of units
+constexpr int kProgressInts = (int)(kProgressBytes / 4);
+static_assert(kSchedWordsOffset + 2 * kSchedWords <= kProgressInts, "scheduling words fit the counter area");
+constexpr int kMaxDynUnits = 32768;   // units a pass may claim at run time
+constexpr size_t kWorkItemBytes = 36;  // sizeof(WorkItem), checked where the type is defined
+constexpr size_t kListBytes = 2ull * kMaxDynUnits * kWorkItemBytes;
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline size_t delta_bytes(long long total, int hq) { return align256((size_t)total * hq * sizeof(float)); }
 inline size_t full_workspace_bytes(long long total, int hq) {
-  return delta_bytes(total, hq) + kProgressBytes + kMaxChains * kChainBytes;
+  return delta_bytes(total, hq) + kProgressBytes + kListBytes + kMaxChains * kChainBytes;
 }
 // Carves a caller-provided workspace; returns false if it cannot hold delta.
+// Run-time claiming needs the counter area and the lists; splitting long kv
+// items needs chain buffers on top.
 inline bool carve_workspace(void* ws, size_t bytes, long long total, int hq, BwdParams& p) {
   const size_t db = delta_bytes(total, hq);
   if (!ws || bytes < db) return false;
@@ -79,11 +95,15 @@ inline bool carve_workspace(void* ws, size_t bytes, long long total, int hq, Bwd
   p.chains_max = 0;
   p.chain_progress = nullptr;
   p.chains = nullptr;
-  if (bytes >= db + kProgressBytes + kChainBytes) {
-    size_t n = (bytes - db - kProgressBytes) / kChainBytes;
-    p.chains_max = (int)(n < (size_t)kMaxChains ? n : (size_t)kMaxChains);
+  p.sched = nullptr;
+  p.unit_lists = nullptr;
+  if (bytes >= db + kProgressBytes + kListBytes) {
     p.chain_progress = reinterpret_cast<int*>(base + db);
-    p.chains = reinterpret_cast<float*>(base + db + kProgressBytes);
+    p.sched = p.chain_progress + kSchedWordsOffset;
+    p.unit_lists = base + db + kProgressBytes;
+    const size_t n = (bytes - db - kProgressBytes - kListBytes) / kChainBytes;
+    p.chains_max = (int)(n < (size_t)kMaxChains ? n : (size_t)kMaxChains);
+    p.chains = reinterpret_cast<float*>(base + db + kProgressBytes + kListBytes);
   }
   return true;
 }

@@ -11,11 +11,11 @@
 // cudaMalloc, cudaFree or allocating library routine.
 //
 // The array holds kNoAllocMaxDelta floats of delta (8 MiB: T * Hq <=
-// 2,097,152), the chain counters, and as many chain buffers as the
-// allocating path uses (320 x 128 KiB), about 48 MiB in all; every GPU that
-// loads the library keeps it until the process exits.  With the same number
-// of chain buffers the dK/dV pass splits its work exactly as in
-// attn_varlen_bwd, so the two calls give the same bits.  All calls on a device
+// 2,097,152), the counters and work lists of the two passes, and as many
+// chain buffers as the allocating path uses (320 x 128 KiB), about 50 MiB in
+// all; every GPU that loads the library keeps it until the process exits.
+// With the same number of chain buffers the dK/dV pass splits its work
+// exactly as in attn_varlen_bwd, so the two calls give the same bits.  All calls on a device
 // share the array and it keeps the previous call's contents: the preprocess
 // overwrites every element of delta and resets the chain counters, so nothing
 // needs to start at zero, but calls whose GPU work overlaps (two streams, or
@@ -32,7 +32,7 @@ namespace {
 
 constexpr long long kNoAllocMaxDelta = 1LL << 21;
 constexpr int kNoAllocMaxDevices = 64;
-constexpr size_t kNoAllocBytes = vsw::kProgressBytes + vsw::kMaxChains * vsw::kChainBytes +
+constexpr size_t kNoAllocBytes = vsw::kProgressBytes + vsw::kListBytes + vsw::kMaxChains * vsw::kChainBytes +
                                  sizeof(float) * (size_t)kNoAllocMaxDelta;
 static_assert(kNoAllocBytes % 256 == 0, "the scratch is carved in 256-byte steps");
 

@@ -136,10 +136,14 @@ __device__ __forceinline__ int last_le(const int* p, int n, int x) {
 // 1024), with cu_seqlens readable.  Writes this CTA's units to out[0..n) in
 // global order and returns n (the same value in every thread), -1 if this
 // CTA would get more than max_out units, or kPlanDoesNotFit.
+// With all_out set (global memory), it instead writes every unit, in global
+// order, to all_out[0..n) and returns n, or kPlanDoesNotFit when n exceeds
+// all_max (for kernels whose CTAs claim units from the list at run time).
 template <bool KV_STATIONARY>
 __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, int window, int max_levels,
                                           int units_per_item, int chains_max, WorkItem* out, int max_out,
-                                          int* scratch, int scratch_ints, int cta, int G) {
+                                          int* scratch, int scratch_ints, int cta, int G,
+                                          WorkItem* all_out = nullptr, int all_max = 0) {
   using namespace plan_detail;
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int U = units_per_item;
@@ -234,15 +238,31 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
   if (C != 0x7fffffff) block_exclusive_scan(s_sbase, n_items, s_misc);
   if (n_chunks > kPlanMaxChunks) return kPlanDoesNotFit;
   // ---- 5. stable counting sort of the chunks by size, largest first.  Equal
-  // sizes keep the order (group of 32 items, chunk index, item): of the orders
-  // tried, this one makes the dK/dV chains wait least.  A chunk always follows
-  // the chunk before it.
+  // sizes keep the order (group of 32 items, chunk index, item).
   auto chunk_of = [&](int e, int& k, int& base, int& rem) {
     const int c = s_cost[e];
     k = c == 0 ? 0 : (c <= C ? 1 : (c + C - 1) / C);
     base = k ? c / k : 0;
     rem = k ? c % k : 0;
   };
+  if (C == 0x7fffffff && n_items <= nt) {
+    // Nothing split and at most one item per thread: each item's position is
+    // its rank (larger cost first, then smaller index), counted in one pass
+    // over the costs.  Same order as the counting sort below, in a fraction
+    // of its barriers and shared-memory steps.
+    if (tid < n_items) {
+      const int c = s_cost[tid];
+      if (c > 0) {
+        const int b = bucket_of(c);
+        int rank = 0;
+        for (int j = 0; j < n_items; ++j) {
+          const int bj = bucket_of(s_cost[j]);
+          rank += (bj > b) | ((bj == b) & (j < tid));
+        }
+        s_order[rank] = tid;
+      }
+    }
+  } else {
   for (int b = tid; b < kCostBuckets; b += nt) s_base[b] = 0;
   __syncthreads();
   // Histogram: lanes with the same bucket add once (most items share a few
@@ -309,23 +329,14 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
       for (int i = 0; i < ks; ++i) place(e, i < k, i);
     }
   }
+  }
   __syncthreads();  // s_order complete
   // ---- 6. deal: unit u of round r = u / G goes to CTA u % G on even rounds
   // and G - 1 - (u % G) on odd rounds, so this CTA's unit of round r is
   // r G + (r even ? cta : G - 1 - cta); thread r expands it.
   const int n_units = n_chunks * U;
-  const int rounds = (n_units + G - 1) / G;
-  int n_mine = 0;
-  for (int r = 0; r < rounds; ++r) {
-    const int u = r * G + ((r & 1) ? G - 1 - cta : cta);
-    if (u < n_units) n_mine = r + 1;
-  }
-  if (n_mine > max_out) {
-    __syncthreads();
-    return -1;
-  }
-  for (int r = tid; r < n_mine; r += nt) {
-    const int u = r * G + ((r & 1) ? G - 1 - cta : cta);
+  // Unit u (global position) as a work item.
+  auto expand = [&](int u, WorkItem& w) {
     const int pos = u / U, h = u - pos * U;
     const int rec = s_order[pos];
     const int e = rec & 0xFFFF, ci = rec >> 16;
@@ -336,7 +347,6 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
     const int t = e - s_tiles[sg];
     int r0, r1;
     stream_range<KV_STATIONARY>(t, nb, window, r0, r1);
-    WorkItem& w = out[r];
     w.seg_lo = s_cu[sg];
     w.seg_hi = s_cu[sg + 1];
     w.blk = t;
@@ -347,7 +357,32 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
     w.chain = k > 1 ? s_sbase[e] * U + h * k : -1;
     w.link = ci | (k << 16);
     w.order = u;
+  };
+  if (all_out) {
+    if (n_units > all_max) {
+      __syncthreads();
+      return kPlanDoesNotFit;
+    }
+    for (int u = tid; u < n_units; u += nt) {
+      WorkItem w;
+      expand(u, w);
+      all_out[u] = w;
+    }
+    __threadfence();  // visible GPU-wide before the list is published
+    __syncthreads();
+    return n_units;
   }
+  const int rounds = (n_units + G - 1) / G;
+  int n_mine = 0;
+  for (int r = 0; r < rounds; ++r) {
+    const int u = r * G + ((r & 1) ? G - 1 - cta : cta);
+    if (u < n_units) n_mine = r + 1;
+  }
+  if (n_mine > max_out) {
+    __syncthreads();
+    return -1;
+  }
+  for (int r = tid; r < n_mine; r += nt) expand(r * G + ((r & 1) ? G - 1 - cta : cta), out[r]);
   __syncthreads();
   return n_mine;
 }
