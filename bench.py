@@ -254,7 +254,7 @@ def main():
     ap.add_argument("--also", default="ctx4096_w512,ctx512_global",
                     help="extra workloads measured in full in the same run (comma list, '' for none)")
     ap.add_argument("--sweep", default=",".join(f"sweep_ctx{c}_{t}" for t in ("global", "w512")
-                                                for c in (512, 1024, 2048, 4096)) + ",long65536_global",
+                                                for c in (512, 1024, 2048, 4096)) + ",long65536_global,long65536_w4096",
                     help="workloads whose step and kernel times are reported under also.sweep ('' for none)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args()

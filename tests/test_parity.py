@@ -59,6 +59,18 @@ def test_ragged_multi_tile(window):
     _check_full(inp, window, 1 / np.sqrt(128), 600, res)
 
 
+@pytest.mark.parametrize("window", [4095, 4096, 4097])
+def test_very_large_window(window):
+    """Windows of about 4,096 tokens (the packed sliding-window benchmark of
+    dewml.dev/reference/performance) on segments longer than the window:
+    each 128-query tile sees the kv tiles of its band, [i - w, i], up to 33
+    of them; compared in full with the oracle, per segment too."""
+    cu = np.array([0, 5000, 5001, 9100, 9500], dtype=np.int32)
+    inp = synth.make_inputs(cu, 8, 2, 128, tensor_seed=8)
+    res = run_gpu(inp, window, 1 / np.sqrt(128), 5000)
+    _check_full(inp, window, 1 / np.sqrt(128), 5000, res)
+
+
 @pytest.mark.parametrize("hq,hkv", [(8, 2), (16, 4), (4, 4), (6, 2), (8, 1)])
 def test_head_ratios(hq, hkv):
     cu = np.array([0, 200, 333, 700], dtype=np.int32)
@@ -96,7 +108,8 @@ def _group_slice(inp, a: int, b: int, g: int, hq: int, hkv: int):
     return sub
 
 
-@pytest.mark.parametrize("name", ["ctx512_global", "ctx4096_w512", "ctx4096_global", "long65536_global"])
+@pytest.mark.parametrize("name", ["ctx512_global", "ctx4096_w512", "ctx4096_global", "long65536_global",
+                                  "long65536_w4096"])
 def test_full_size_sampled_segments(name):
     """At the full sizes (the benchmark's launch configuration for the
     16,384-token microbatches; 65,536 tokens with 16/4 heads for the long
@@ -168,7 +181,7 @@ def _cu_of(name: str) -> tuple:
 
 
 MASK_CASES = ["tiny_global", "tiny_w64", "tiny_w64+pad", "ctx512_global", "ctx4096_w512", "ctx4096_w512+pad",
-              "ctx4096_global", "ctx4096_global+pad", "long65536_global"]
+              "ctx4096_global", "ctx4096_global+pad", "long65536_global", "long65536_w4096"]
 
 
 @pytest.mark.parametrize("name", MASK_CASES)

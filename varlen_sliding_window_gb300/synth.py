@@ -144,7 +144,8 @@ class Workload:
 def workloads() -> dict[str, Workload]:
     """The named workloads: the 256-token three-document check, the
     16,384-token microbatches at context 512 and 4,096 (global and window 512),
-    the context sweep, and the 65,536-token long-context stress case."""
+    the context sweep, and the 65,536-token long-context case, global and with
+    a 4,096-token window."""
     w: dict[str, Workload] = {}
     for win, tag in ((-1, "global"), (64, "w64")):
         w[f"tiny_{tag}"] = Workload(f"tiny_{tag}", 256, 256, win, tensor_seed=0, fixed_cu=(0, 61, 161, 256))
@@ -156,4 +157,7 @@ def workloads() -> dict[str, Workload]:
             name = f"sweep_ctx{ctx}_{tag}"
             w[name] = Workload(name, 16384, ctx, win)
     w["long65536_global"] = Workload("long65536_global", 65536, 32768, -1, hq=16, hkv=4, cap=32768)
+    # The same long microbatch with a 4,096-token window (the packed
+    # sliding-window benchmark of dewml.dev/reference/performance).
+    w["long65536_w4096"] = Workload("long65536_w4096", 65536, 32768, 4096, hq=16, hkv=4, cap=32768)
     return w
