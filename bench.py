@@ -49,6 +49,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # credits: forward QK^T + PV; dK/dV pass S, dP, dV, dK; dQ pass dQ only (its
 # recomputed S and dP are not counted).
 KERNEL_UNITS = {"fwd": 2.0, "bwd_preprocess": 0.0, "bwd_dkdv": 4.0, "bwd_dq": 1.0}
+# Kernels of this library per step: forward, preprocess, planner, dK/dV, dQ.
+KERNELS_PER_STEP = 5
 
 
 def unmasked_pairs(cu: np.ndarray, window: int) -> int:
@@ -294,7 +296,9 @@ def main():
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
     def step(w, t, evs=None):
-        """One step through the C ABI; evs = 5 events recorded between kernels."""
+        """One step through the C ABI, kernel by kernel; evs = 5 events recorded
+        between the forward, the preprocess (with the one-CTA planner beside
+        it), the dK/dV pass and the dQ pass."""
         ms, win, sc = w.context, w.window_left, w.softmax_scale
         if evs:
             evs[0].record(stream)
@@ -302,6 +306,7 @@ def main():
         if evs:
             evs[1].record(stream)
         binding.attn_varlen_bwd_preprocess(t["dout"], t["out"], t["ws"])
+        binding.attn_varlen_bwd_plan(t["cu"], ms, win, t["ws"], w.total, w.hq, w.hkv)
         if evs:
             evs[2].record(stream)
         binding.attn_varlen_bwd_dkdv(t["dout"], t["q"], t["k"], t["v"], t["lse"], t["ws"], t["cu"], ms, win, sc,
@@ -716,7 +721,7 @@ def main():
                     "how": "attn_varlen_fwd + attn_varlen_bwd per step, inputs copied up from pinned host memory "
                            "and all five results copied back every step; copies of neighbouring steps overlap "
                            "the compute on two copy streams (serial_ms: one step at a time)"},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
             "clocks": main_res["clocks"],
             "also": also,
         }

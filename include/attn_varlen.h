@@ -101,10 +101,13 @@ int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* 
 
 /*
  * Backward.  Given dout, the forward's inputs and its outputs out and lse,
- * writes dq [T, Hq, 128], dk and dv [T, Hkv, 128] (bf16).  Runs three kernels
- * on `stream`: a preprocess computing D = rowsum(dout * out), a
+ * writes dq [T, Hq, 128], dk and dv [T, Hkv, 128] (bf16).  Runs four kernels
+ * on `stream`: a preprocess computing D = rowsum(dout * out), a one-CTA
+ * planner writing the longest-first work lists (beside the preprocess), a
  * key/value-stationary pass producing dk and dv, and a query-stationary pass
- * producing dq.  No atomics: results are bitwise reproducible.
+ * producing dq.  No floating-point atomics: results are bitwise reproducible
+ * (the passes' CTAs claim work units at run time, but no sum depends on
+ * which CTA computes which unit).
  */
 int attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                     const float* lse, const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left,
@@ -203,22 +206,31 @@ size_t attn_varlen_workspace_bytes(int64_t total, int32_t num_heads_q, int32_t n
 int attn_varlen_set_workspace(void* dev_ptr, size_t bytes);
 
 /*
- * The three kernels of attn_varlen_bwd as separate calls, for callers that
- * manage the scratch themselves.  `workspace` is caller-owned device memory,
- * 256-byte aligned, of `workspace_bytes` bytes; the same workspace goes to all
- * three calls, in this order on one stream:
+ * The kernels of attn_varlen_bwd as separate calls, for callers that manage
+ * the scratch themselves.  `workspace` is caller-owned device memory, 256-byte
+ * aligned, of `workspace_bytes` bytes; the same workspace goes to every call,
+ * in this order on one stream:
  *   attn_varlen_bwd_preprocess writes D = rowsum(dout * out) (float32 [Hq, T],
- *     at the start of the workspace) and resets the dK/dV pass's counters;
+ *     at the start of the workspace) and resets the passes' counters;
+ *   attn_varlen_bwd_plan (optional) writes the longest-first work lists of
+ *     the two passes into the workspace, from which their CTAs then claim
+ *     units at run time; without it every CTA deals itself a fixed share;
  *   attn_varlen_bwd_dkdv reads D (with q, k, v, dout, lse) and writes dk, dv;
  *   attn_varlen_bwd_dq reads D and writes dq.
+ * A pass consumes its list: run attn_varlen_bwd_plan again before running it
+ * again with lists (without, it falls back to fixed shares, same bits).
  * Minimum size: T * Hq * 4 bytes rounded up to 256.  With
- * attn_varlen_bwd_workspace_bytes() bytes the dK/dV pass may split long
- * key/value tiles into chunks that different CTAs reduce in a fixed order
- * (better load balance, same bits); a smaller workspace splits less.
- * Arguments otherwise mean what they mean in attn_varlen_bwd.
+ * attn_varlen_bwd_workspace_bytes() bytes the lists fit and the dK/dV pass
+ * may split long key/value tiles into chunks whose partial sums are added in
+ * a fixed order (better load balance, same bits); a smaller workspace splits
+ * less and claims nothing.  Arguments otherwise mean what they mean in
+ * attn_varlen_bwd.
  */
 int attn_varlen_bwd_preprocess(const void* dout, const void* out, void* workspace, size_t workspace_bytes,
                                int64_t total, int32_t num_heads_q, int32_t head_dim, void* stream);
+int attn_varlen_bwd_plan(const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left, void* workspace,
+                         size_t workspace_bytes, int64_t total, int32_t num_heads_q, int32_t num_heads_kv,
+                         int32_t num_segments, void* stream);
 int attn_varlen_bwd_dkdv(const void* dout, const void* q, const void* k, const void* v, const float* lse,
                          const void* workspace, size_t workspace_bytes, const int32_t* cu_seqlens, int32_t max_seqlen,
                          int32_t window_left, float softmax_scale, void* dk, void* dv, int64_t total,

@@ -105,10 +105,11 @@ def test_segment_longer_than_max_seqlen_is_reported():
 
 @pytest.mark.parametrize("name", ["ctx4096_global", "ctx512_global"])
 def test_sub_step_calls_repeat_on_one_workspace(name):
-    """The three backward kernels as separate calls on one caller workspace,
-    the dK/dV and dQ passes each run twice without a preprocess in between:
-    their run-time counters (split-item arrivals, claimed units) reset
-    themselves, so every repeat gives the one-call backward's bits."""
+    """The backward's kernels as separate calls on one caller workspace, the
+    dK/dV and dQ passes each run four times after one preprocess, with and
+    without a fresh plan: their run-time counters (split-item arrivals,
+    claimed units) reset themselves, and claimed and fixed shares give the
+    one-call backward's bits."""
     import torch
     from varlen_sliding_window_gb300 import binding
     wl = WL[name]
@@ -117,11 +118,16 @@ def test_sub_step_calls_repeat_on_one_workspace(name):
     ref = _bwd(wl, t)
     ws = torch.empty(binding.attn_varlen_bwd_workspace_bytes(wl.total, wl.hq), dtype=torch.uint8, device="cuda")
     binding.attn_varlen_bwd_preprocess(do, out, ws)
-    for _ in range(2):
+    # With the work lists (claimed at run time), then twice without them
+    # (each pass consumes its list and falls back to fixed shares), then with
+    # a fresh plan again.
+    for plan in (True, False, False, True):
+        if plan:
+            binding.attn_varlen_bwd_plan(cu, wl.context, wl.window_left, ws, wl.total, wl.hq, wl.hkv)
         dq, dk, dv = (torch.full_like(x, float("nan")) for x in (q, k, v))
         binding.attn_varlen_bwd_dkdv(do, q, k, v, lse, ws, cu, wl.context, wl.window_left, wl.softmax_scale, dk, dv)
         binding.attn_varlen_bwd_dq(do, q, k, v, lse, ws, cu, wl.context, wl.window_left, wl.softmax_scale, dq)
         torch.cuda.synchronize()
         for nm, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
-            assert torch.equal(a, b), nm
+            assert torch.equal(a, b), (plan, nm)
     assert binding.attn_varlen_get_status() == 0

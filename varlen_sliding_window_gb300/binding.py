@@ -52,6 +52,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     sz = ctypes.c_size_t
     lib.attn_varlen_bwd_preprocess.argtypes = [vp, vp, vp, sz, i64, i32, i32, vp]
     lib.attn_varlen_bwd_preprocess.restype = ctypes.c_int
+    lib.attn_varlen_bwd_plan.argtypes = [vp, i32, i32, vp, sz, i64, i32, i32, i32, vp]
+    lib.attn_varlen_bwd_plan.restype = ctypes.c_int
     lib.attn_varlen_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, sz, vp, i32, i32, f32, vp, vp, i64, i32, i32, i32, i32,
                                          vp]
     lib.attn_varlen_bwd_dkdv.restype = ctypes.c_int
@@ -203,6 +205,16 @@ def attn_varlen_bwd_preprocess(dout, out, workspace, stream=None) -> None:
     wp, wb = _ws(workspace)
     _check(lib.attn_varlen_bwd_preprocess(_ptr(dout), _ptr(out), wp, wb, int(total), int(hq), int(d),
                                           _stream_handle(stream)), "attn_varlen_bwd_preprocess")
+
+
+def attn_varlen_bwd_plan(cu_seqlens, max_seqlen: int, window_left: int, workspace, total: int, num_heads_q: int,
+                         num_heads_kv: int, stream=None) -> None:
+    """Writes the two passes' work lists into the workspace (optional sub-step)."""
+    lib = load_library()
+    wp, wb = _ws(workspace)
+    _check(lib.attn_varlen_bwd_plan(_ptr(cu_seqlens), int(max_seqlen), int(window_left), wp, wb, int(total),
+                                    int(num_heads_q), int(num_heads_kv), int(cu_seqlens.numel()) - 1,
+                                    _stream_handle(stream)), "attn_varlen_bwd_plan")
 
 
 def attn_varlen_bwd_dkdv(dout, q, k, v, lse, workspace, cu_seqlens, max_seqlen: int, window_left: int,

@@ -301,7 +301,6 @@ int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, con
   b.p.sched = nullptr;
   b.p.unit_lists = nullptr;
   b.p.dq_after_dkdv = 0;
-  b.p.dkdv_after_pre = 0;
   b.p.dq = dq;
   b.p.dk = dk;
   b.p.dv = dv;
@@ -346,12 +345,12 @@ int bwd_on_workspace(const void* dout, const void* q, const void* k, const void*
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return ATTN_ERR_ALIGNMENT;
   if (!carve_workspace(ws, ws_bytes, total, num_heads_q, b.p)) return ATTN_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // Each kernel starts under the tail of the one before: dK/dV plans while
-  // the preprocess finishes, dQ takes the SMs dK/dV frees.
+  // Each kernel starts under the tail of the one before: the unit lists of
+  // both passes are planned while the preprocess computes D, dQ takes the
+  // SMs dK/dV frees.
   int lr = launch_bwd_preprocess(b.p, s);
-  b.p.dkdv_after_pre = 1;
+  if (!lr && b.p.sched) lr = launch_bwd_plan(b.p, b.dev->num_sms, 1, s);
   if (!lr) lr = launch_bwd_dkdv(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, s);
-  b.p.dkdv_after_pre = 0;
   b.p.dq_after_dkdv = 1;
   if (!lr) lr = launch_bwd_dq(b.tq, b.tk, b.tv, b.tdo, b.p, b.dev->num_sms, s);
   return lr ? ATTN_ERR_CUDA : ATTN_OK;
@@ -437,6 +436,26 @@ int attn_varlen_bwd_preprocess(const void* dout, const void* out, void* workspac
   p.dout_st = p.out_st = contiguous(num_heads_q);
   if (!carve_workspace(workspace, workspace_bytes, total, num_heads_q, p)) return ATTN_ERR_WORKSPACE;
   return launch_bwd_preprocess(p, static_cast<cudaStream_t>(stream)) ? ATTN_ERR_CUDA : ATTN_OK;
+}
+
+int attn_varlen_bwd_plan(const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left, void* workspace,
+                         size_t workspace_bytes, int64_t total, int32_t num_heads_q, int32_t num_heads_kv,
+                         int32_t num_segments, void* stream) {
+  int rc = validate_common(cu_seqlens, max_seqlen, window_left, 1.f, total, num_heads_q, num_heads_kv, 128,
+                           num_segments);
+  if (rc) return rc;
+  if (!workspace) return ATTN_ERR_NULL_POINTER;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev))) return rc;
+  if (total == 0) return ATTN_OK;
+  BwdParams p{};
+  p.a = make_params(cu_seqlens, max_seqlen, window_left, 1.f, total, num_heads_q, num_heads_kv, num_segments,
+                    dev->status);
+  if (!carve_workspace(workspace, workspace_bytes, total, num_heads_q, p)) return ATTN_ERR_WORKSPACE;
+  // Without room for the lists the passes plan their own shares: nothing to do.
+  if (!p.sched) return ATTN_OK;
+  return launch_bwd_plan(p, dev->num_sms, 0, static_cast<cudaStream_t>(stream)) ? ATTN_ERR_CUDA : ATTN_OK;
 }
 
 int attn_varlen_bwd_dkdv(const void* dout, const void* q, const void* k, const void* v, const float* lse,

@@ -26,12 +26,17 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __rest
                                                              RowStrides dout_st, RowStrides out_st,
                                                              int* __restrict__ chain_progress, int nprogress) {
   grid_dependency_wait();
+  // The passes that follow count chain arrivals and claimed units from zero;
+  // block 0 clears the counters before it lets the next kernel start (the
+  // planning kernel of the backward sets the claim words right away).
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < nprogress; e += blockDim.x) chain_progress[e] = 0;
+    __threadfence();
+    __syncthreads();
+  }
   // Everything before this kernel is complete: the next kernel may start
   // (it waits for this one before reading what it writes).
   grid_dependents_launch();
-  // The passes that follow count chain arrivals and claimed units from zero.
-  if (blockIdx.x == 0)
-    for (int e = threadIdx.x; e < nprogress; e += blockDim.x) chain_progress[e] = 0;
   const long long rows = (long long)total * hq;
   const int sub = threadIdx.x & 15;
   const int r_in = threadIdx.x >> 4;  // 0..15

@@ -95,6 +95,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ WorkItem items[kBwdMaxItems];
   __shared__ int n_items;
+  // Items in flight, handed from the claiming warp to the other roles.
+  __shared__ WorkItem ring[2];
+  __shared__ __align__(8) uint64_t ring_full[2], ring_taken[2], ring_empty[2];
+  __shared__ int claim_mode, n_units_s;
+  __shared__ int* claim_words;
   __shared__ __align__(8) uint64_t bar_kv_full, bar_kv_empty;
   __shared__ __align__(8) uint64_t bar_qdo_full[S], bar_qdo_empty[S];
   // s_full[0]: S^T done, s_full[1]: dP^T done; p_full[x] / ds_full[x]: warpgroup
@@ -130,6 +135,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&bar_acc_empty), 256);
     mbar_init(smem_u32(&bar_chain[0]), 128);
     mbar_init(smem_u32(&bar_chain[1]), 128);
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(smem_u32(&ring_full[r]), 1);
+      mbar_init(smem_u32(&ring_taken[r]), 1);
+      mbar_init(smem_u32(&ring_empty[r]), 10);  // the producer warp, the MMA thread, the 8 elementwise warps
+    }
     fence_mbar_init();
     tma_prefetch_map(&tmQ);
     tma_prefetch_map(&tmK);
@@ -140,14 +150,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  // Inputs written by earlier kernels are read after the wait.  Right after
-  // this backward's own preprocess (which lets this grid start once it has
-  // waited for everything before it), the planner only reads cu_seqlens,
-  // which is complete by then, so the wait comes after planning.
-  if (!p.dkdv_after_pre) grid_dependency_wait();
-  const int planned = plan_schedule<true>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hkv, p.chains_max, items,
-                                          kBwdMaxItems, reinterpret_cast<int*>(gbase), (int)(C::kAugOff / 4),
-                                          blockIdx.x, gridDim.x);
+  // Inputs written by earlier kernels (and the unit list of this backward's
+  // planning kernel) are read after the wait.  With a fresh list every CTA
+  // claims units at run time (claim.cuh); otherwise it plans its own share.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) {
+    int* cw = p.sched;
+    claim_mode = cw ? claim_ready(cw) : 0;
+    n_units_s = claim_mode ? __ldcg(cw + 3) : 0;
+    claim_words = claim_mode ? cw : nullptr;
+    n_items = 0;
+  }
+  __syncthreads();
+  const int planned = claim_mode ? 0
+                                 : plan_schedule<true>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hkv,
+                                                       p.chains_max, items, kBwdMaxItems, reinterpret_cast<int*>(gbase),
+                                                       (int)(C::kAugOff / 4), blockIdx.x, gridDim.x);
   if (planned == kPlanDoesNotFit) {
     if (warp == 3) {
       int* cu = reinterpret_cast<int*>(gbase + C::kQOff);
@@ -160,11 +178,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (n < 0) atomicExch(a.status, kStatusListOverflow);
       }
     }
-  } else if (threadIdx.x == 0) {
+  } else if (threadIdx.x == 0 && !claim_mode) {
     n_items = planned < 0 ? 0 : planned;
     if (planned < 0) atomicExch(a.status, kStatusListOverflow);
   }
-  if (p.dkdv_after_pre) grid_dependency_wait();
   // Extra k-step blocks (after the planner, whose scratch ends at kAugOff):
   // the ones block gets 1.0 in columns 0 and 1 of every row, the per-stage
   // blocks start at zero and only their columns 0 and 1 change later.
@@ -197,8 +214,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float inv_scale = 1.f / a.scale;
     int cnt = 0;
     bool ok = true;
-    for (int it = 0; it < nit && ok; ++it) {
-      const WorkItem w = items[it];
+    for (int it = 0; ok; ++it) {
+      const int rs = it & 1;
+      if (!(ok = mbar_wait_warp(smem_u32(&ring_full[rs]), (it >> 1) & 1, &abort_flag, a.status))) break;
+      const WorkItem w = ring[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ring_empty[rs]));
+      if (w.blk < 0) break;
       const int k0 = w.seg_lo + w.blk * kTile;
       const int g = w.unit;
       if (lane == 0) {
@@ -264,8 +286,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t sOnes = sbase + C::kOnesOff;
       int cnt = 0;  // (q tile, head) pairs, for the Q/dO ring and the S/dP buffer
       bool ok = true;
-      for (int it = 0; it < nit && ok; ++it) {
-        const WorkItem w = items[it];
+      for (int it = 0; ok; ++it) {
+        const int rs = it & 1;
+        if (!(ok = mbar_wait(smem_u32(&ring_full[rs]), (it >> 1) & 1, &abort_flag, a.status))) break;
+        const WorkItem w = ring[rs];
+        mbar_arrive(smem_u32(&ring_taken[rs]));
+        mbar_arrive(smem_u32(&ring_empty[rs]));
+        if (w.blk < 0) break;
         const int npairs = (w.t1 - w.t0 + 1) * a.group;
         if (!(ok = mbar_wait(smem_u32(&bar_kv_full), it & 1, &abort_flag, a.status))) break;
         tc_fence_after();
@@ -358,7 +385,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp < 4) {
     regs_decrease<104>();
-    if (warp == 3 && blockIdx.x == 0) report_long_segments(a);
+    if (warp == 2 && blockIdx.x == 0) report_long_segments(a);
+    if (warp == 3 && lane == 0) {
+      // ------------------------------------------------------------ items
+      // The next item: claimed from the list, or the next of this CTA's
+      // share.  It goes to the other roles through a two-slot ring; an item
+      // with blk < 0 tells them there is no more work.  The next claim is
+      // made once the MMA thread has started the item before it (one item of
+      // look-ahead: the claim's round trip to L2 overlaps that item's work,
+      // and a CTA never holds more than one unit it has not started).
+      int* cw = claim_words;
+      const WorkItem* clist = static_cast<const WorkItem*>(p.unit_lists);
+      const int n_units = n_units_s;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        WorkItem w;
+        bool have;
+        if (cw) {
+          const int u = claim_next(cw);
+          have = u < n_units;
+          if (have) w = claim_item(clist, u);
+        } else {
+          have = it < nit;
+          if (have) w = items[it];
+        }
+        if (!have) w.blk = -1;
+        const int rs = it & 1;
+        if (it >= 2 && !(ok = mbar_wait(smem_u32(&ring_empty[rs]), ((it >> 1) - 1) & 1, &abort_flag, a.status)))
+          break;
+        ring[rs] = w;
+        mbar_arrive(smem_u32(&ring_full[rs]));
+        if (!have) break;
+        if (!(ok = mbar_wait(smem_u32(&ring_taken[rs]), (it >> 1) & 1, &abort_flag, a.status))) break;
+      }
+    }
   } else {
     // ------------------------------------------------------------ elementwise
     // Warpgroup x = query columns [64x, 64x + 64) of every S^T/dP^T tile;
@@ -373,8 +433,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int cnt = 0;
     uint32_t chain_uses = 0;
     bool ok = true;
-    for (int it = 0; it < nit && ok; ++it) {
-      const WorkItem w = items[it];
+    for (int it = 0; ok; ++it) {
+      const int rs = it & 1;
+      if (!(ok = mbar_wait_warp(smem_u32(&ring_full[rs]), (it >> 1) & 1, &abort_flag, a.status))) break;
+      const WorkItem w = ring[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ring_empty[rs]));
+      if (w.blk < 0) break;
       const int k0 = w.seg_lo + w.blk * kTile;
       const int g = w.unit;
       const int j = k0 + row;  // this thread's key token
@@ -539,6 +604,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (threadIdx.x == 0 && claim_words) claim_finish(claim_words);
 }
 
 // ============================================================== dQ pass
@@ -571,7 +637,6 @@ struct DqState {
   int n_items;
   int claim_mode;  // units are claimed at run time from the workspace list
   int n_units;     // size of that list
-  int planner;     // this CTA writes the list
   int* claim_words;  // kept here, not in a register, for the end of the kernel
   uint32_t tmem_slot;
   int abort_flag;
@@ -654,38 +719,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // wait (so delta and every input are complete), and it writes nothing this
   // kernel reads.
   if (!p.dq_after_dkdv) grid_dependency_wait();
-  // Work list: with a workspace for it, one CTA writes the whole
+  // Work list: the planning kernel of this backward has written the
   // longest-first list and every CTA claims units at run time (claim.cuh);
-  // otherwise, or when the list does not fit, every CTA plans its own share.
+  // without a fresh list every CTA plans its own share.
   int* const cw = p.sched ? p.sched + kSchedWords : nullptr;
   WorkItem* const clist = cw ? reinterpret_cast<WorkItem*>(p.unit_lists) + kMaxDynUnits : nullptr;
   if (threadIdx.x == 0) {
-    st.claim_mode = 0;
-    st.planner = cw ? claim_elect(cw) : 0;
-    st.claim_words = cw;
+    st.claim_mode = cw ? claim_ready(cw) : 0;
+    st.n_units = st.claim_mode ? __ldcg(cw + 3) : 0;
+    st.claim_words = st.claim_mode ? cw : nullptr;
+    n_items = 0;
   }
   __syncthreads();
-  // Pass 0: the elected CTA writes the list.  Pass 1: every CTA, if the list
-  // is not used, plans its own share.  (One call site for both.)
-  int planned = 0;
-  for (int pass = 0; pass < 2; ++pass) {
-    const bool run = pass == 0 ? st.planner != 0 : !st.claim_mode && !abort_flag;
-    if (run)
-      planned = plan_schedule<false>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hq, 0, items, C::kMaxItems,
-                                     reinterpret_cast<int*>(gbase), (int)(C::kStateOff / 4), blockIdx.x, gridDim.x,
-                                     pass == 0 ? clist : nullptr, kMaxDynUnits);
-    if (pass == 0) {
-      if (st.planner && threadIdx.x == 0) claim_publish(cw, planned);
-      if (cw && threadIdx.x == 0) {
-        const int state = claim_wait(cw, abort_ptr, a.status);
-        st.claim_mode = state == kClaimReady;
-        st.n_units = st.claim_mode ? __ldcg(cw + 3) : 0;
-        n_items = 0;
-      }
-      __syncthreads();
-      planned = 0;
-    }
-  }
+  const int planned = st.claim_mode ? 0
+                                    : plan_schedule<false>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hq, 0,
+                                                           items, C::kMaxItems, reinterpret_cast<int*>(gbase),
+                                                           (int)(C::kStateOff / 4), blockIdx.x, gridDim.x);
   if (planned == kPlanDoesNotFit) {
     if (warp == 3) {
       int* cu = reinterpret_cast<int*>(gbase + C::kKOff);
@@ -992,14 +1041,55 @@ long long persistent_grid(long long units, int num_sms, int max_items) {
   return grid;
 }
 
+long long dkdv_grid(const BwdParams& p, int num_sms) {
+  return persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hkv, num_sms, kBwdMaxItems);
+}
+
+// ============================================================== planning
+// Two CTAs write the longest-first unit lists to the workspace and set the
+// claim words (claim.cuh): CTA 0 the dK/dV pass's (kv tiles, long ones split
+// into chunks exactly as the pass itself would split them for its grid),
+// CTA 1 the dQ pass's.  Inside a backward they run beside the preprocess:
+// they read only cu_seqlens, which is complete once the preprocess has let
+// them start, and the grid finishes no earlier than the preprocess, so the
+// passes that wait for it also find D complete.
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_plan_kernel(const BwdParams p, int dkdv_ctas, int after_pre, int scratch_ints) {
+  extern __shared__ int plan_smem[];
+  const AttnParams& a = p.a;
+  if (!after_pre) grid_dependency_wait();
+  WorkItem* lists = static_cast<WorkItem*>(p.unit_lists);
+  if (blockIdx.x == 0) {
+    const int n = plan_schedule<true>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hkv, p.chains_max, nullptr, 0,
+                                      plan_smem, scratch_ints, 0, dkdv_ctas, lists, kMaxDynUnits);
+    if (threadIdx.x == 0) claim_init(p.sched, n);
+  } else {
+    const int n = plan_schedule<false>(a.cu_seqlens, a.nseg, a.window, a.max_levels, a.hq, 0, nullptr, 0,
+                                       plan_smem, scratch_ints, 0, 1, lists + kMaxDynUnits, kMaxDynUnits);
+    if (threadIdx.x == 0) claim_init(p.sched + kSchedWords, n);
+  }
+  __syncthreads();
+  grid_dependents_launch();
+  grid_dependency_wait();
+}
+
 }  // namespace
+
+int launch_bwd_plan(const BwdParams& p, int num_sms, int after_pre, cudaStream_t stream) {
+  const int ints = plan_scratch_ints(p.a.nseg, 1, kBwdThreads);
+  const size_t smem = (size_t)ints * sizeof(int);
+  cudaError_t e = cudaFuncSetAttribute(bwd_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return (int)e;
+  return (int)launch_pdl(bwd_plan_kernel, dim3(2), dim3(kBwdThreads), smem, stream, p, (int)dkdv_grid(p, num_sms),
+                         after_pre, ints);
+}
 
 int launch_bwd_dkdv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,
                     const BwdParams& p, int num_sms, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)DkvCfg::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
-  const long long g = persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hkv, num_sms, kBwdMaxItems);
+  const long long g = dkdv_grid(p, num_sms);
   return (int)launch_pdl(attn_bwd_dkdv_kernel, dim3((unsigned)g), dim3(kBwdThreads), DkvCfg::kSmemBytes, stream, tmQ,
                          tmK, tmV, tmDO, p);
 }
@@ -1010,13 +1100,8 @@ int launch_bwd_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensor
       cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmemBytes);
   if (e != cudaSuccess) return (int)e;
   const long long g = persistent_grid(upper_bound_tiles(p.a.total, p.a.nseg) * p.a.hq, num_sms, DqCfg::kMaxItems);
-  // Run-time claiming pays off when units differ in size (a unit has up to
-  // max_seqlen / 128 kv tiles); at contexts of up to 512 tokens (four tiles)
-  // the fixed longest-first shares are as even and cost no claims.
-  BwdParams q = p;
-  if (q.a.max_levels <= 4) q.sched = nullptr;
   return (int)launch_pdl(attn_bwd_dq_kernel, dim3((unsigned)g), dim3(kBwdThreads), kDqSmemBytes, stream, tmQ,
-                         tmK, tmV, tmDO, q);
+                         tmK, tmV, tmDO, p);
 }
 
 }  // namespace vsw

@@ -60,9 +60,6 @@ struct BwdParams {
   // same backward: it then needs nothing that kernel writes, starts on the
   // SMs the dK/dV kernel frees and waits for it only before exiting.
   int dq_after_dkdv;
-  // Set when the dK/dV kernel is launched right after the preprocess of the
-  // same backward: it plans before waiting for that kernel.
-  int dkdv_after_pre;
   RowStrides dout_st, out_st, dq_st, dk_st, dv_st;
 };
 
@@ -116,6 +113,9 @@ int launch_bwd_dkdv(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtens
 int launch_bwd_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,
                   const BwdParams& p, int num_sms, cudaStream_t stream);
 int launch_bwd_preprocess(const BwdParams& p, cudaStream_t stream);
+// after_pre: launched right after the preprocess of the same backward (reads
+// cu_seqlens before waiting for it).
+int launch_bwd_plan(const BwdParams& p, int num_sms, int after_pre, cudaStream_t stream);
 int launch_mask_probe(const int* cu_seqlens, int nseg, int total, int window, int max_levels, int by_key,
                       int* ranges, cudaStream_t stream);
 
