@@ -1,4 +1,6 @@
-"""CPU float64 oracle for varlen GQA attention (test infrastructure only).
+"""CPU float64 oracles (test infrastructure only): varlen GQA attention
+(attention.py) and the Gated DeltaNet recurrence over packed documents
+(gated_delta.py).
 
 Only tests, the smoke check and the benchmark's CPU-baseline leg import this
 package; the library never does.
