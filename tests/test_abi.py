@@ -9,6 +9,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "attn_varlen.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -19,14 +20,18 @@ def clib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(attn_varlen_\w+)\s*\(", text)))
+    """Every function declared in include/*.h (comments stripped)."""
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b((?:attn|gdn)_varlen_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_calls():
     names = declared_functions()
-    for required in ("attn_varlen_fwd", "attn_varlen_bwd", "attn_varlen_get_status", "attn_varlen_strerror"):
+    for required in ("attn_varlen_fwd", "attn_varlen_bwd", "attn_varlen_get_status", "attn_varlen_strerror",
+                     "gdn_varlen_fwd", "gdn_varlen_workspace_bytes"):
         assert required in names
 
 
@@ -147,3 +152,39 @@ def test_set_workspace_rejects_a_misaligned_buffer(clib):
     # The alignment check comes before the device probe: no GPU needed.
     clib.attn_varlen_set_workspace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
     assert clib.attn_varlen_set_workspace(ctypes.c_void_p(256 + 16), 1 << 20) == -4
+
+
+def _gdn(clib, **kw):
+    args = dict(q=16, k=16, v=16, g=16, beta=16, cu=16, scale=0.088, o=16, ws=256, ws_bytes=1 << 30, total=4, nh=8,
+                d=128, nseg=1, stream=None)
+    args.update(kw)
+    vp = ctypes.c_void_p
+    return clib.gdn_varlen_fwd(vp(args["q"]), vp(args["k"]), vp(args["v"]), vp(args["g"]), vp(args["beta"]),
+                               vp(args["cu"]), args["scale"], vp(args["o"]), vp(args["ws"]), args["ws_bytes"],
+                               args["total"], args["nh"], args["d"], args["nseg"], vp(args["stream"]))
+
+
+def test_gdn_argument_validation(clib):
+    # Rejected before any CUDA call, so no GPU is needed.
+    assert _gdn(clib, q=None) == -1
+    assert _gdn(clib, beta=None) == -1
+    assert _gdn(clib, ws=None) == -1
+    assert _gdn(clib, total=-1) == -2
+    assert _gdn(clib, nh=0) == -2
+    assert _gdn(clib, nseg=0) == -2
+    assert _gdn(clib, d=64) == -3
+    assert _gdn(clib, v=24) == -4
+    assert _gdn(clib, g=20) == -4
+    assert _gdn(clib, ws=272) == -4
+    assert _gdn(clib, scale=float("inf")) == -6
+    assert _gdn(clib, ws_bytes=1024) == -14
+
+
+def test_gdn_workspace_bytes(clib):
+    f = clib.gdn_varlen_workspace_bytes
+    assert f(-1, 8, 1) == 0 and f(16, 0, 1) == 0
+    n = f(16384, 8, 25)
+    # W and U (bf16 [T, H, 128] each), the per-chunk q.k blocks, gamma and the tables
+    assert n >= 2 * 16384 * 8 * 128 * 2 + (16384 // 64 + 25) * 8 * 64 * 64 * 2 + 16384 * 8 * 4
+    assert n % 256 == 0
+    assert f(16384, 8, 50) > n

@@ -1,0 +1,95 @@
+"""Gated DeltaNet forward on the GPU against the float64 oracle, through the
+C ABI (include/gdn_varlen.h).
+
+Tolerance: relative L2 error of o <= 1e-2 over the whole tensor and over
+every segment of at least 16 tokens (shorter ones: RMS error <= 1e-2 x the
+larger of their RMS and the tensor's).  The kernels round to bf16, on the
+way to each output, the WY factors W and U, the masked q.k block, the state
+copy used as a matrix operand, the pseudo-values E, and o itself: six
+roundings, each with a relative RMS error of about 2^-8 / sqrt(3) = 2.3e-3;
+independent, they add up to sqrt(6) x 2.3e-3 = 5.5e-3.  The bound is about
+twice that.  (The oracle sees the same bf16 q, k, v and float32 g, beta.)
+"""
+import numpy as np
+import pytest
+
+from tests.helpers import assert_per_segment, rel_l2
+from varlen_sliding_window_gb300 import synth
+
+TOL_O = 1e-2
+WL = synth.gdn_workloads()
+
+
+def _to_dev(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16).cuda()
+
+
+def _run(inp, scale, cu=None):
+    import torch
+    from varlen_sliding_window_gb300 import binding
+    cu = inp.cu_seqlens if cu is None else cu
+    q, k, v = (_to_dev(b) for b in (inp.q_bits, inp.k_bits, inp.v_bits))
+    g = torch.from_numpy(inp.g).cuda()
+    beta = torch.from_numpy(inp.beta).cuda()
+    cu_t = torch.from_numpy(np.asarray(cu, dtype=np.int32)).cuda()
+    T, nh, _ = q.shape
+    o = torch.full_like(q, float("nan"))
+    ws = torch.empty(binding.gdn_varlen_workspace_bytes(T, nh, len(cu) - 1), dtype=torch.uint8, device="cuda")
+    binding.gdn_varlen_fwd(q, k, v, g, beta, cu_t, scale, o, ws)
+    torch.cuda.synchronize()
+    assert binding.attn_varlen_get_status() == 0
+    return o
+
+
+def _oracle(inp, scale):
+    from oracle import gated_delta
+    return gated_delta.forward(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens, scale)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["gdn_tiny", "gdn_ragged", "gdn_ctx512", "gdn_ctx4096"])
+def test_forward_matches_oracle(name):
+    w = WL[name]
+    inp = w.inputs()
+    got = _run(inp, w.scale).double().cpu().numpy()
+    ref = _oracle(inp, w.scale)
+    assert np.isfinite(got).all()
+    err = rel_l2(got, ref)
+    print(f"{name}: rel L2 {err:.3e}")
+    assert err <= TOL_O, err
+    assert_per_segment(got, ref, inp.cu_seqlens, TOL_O, "o")
+
+
+@pytest.mark.gpu
+def test_empty_segments_and_repeats_are_bit_identical():
+    import torch
+    w = WL["gdn_ragged"]
+    inp = w.inputs()
+    a = _run(inp, w.scale)
+    b = _run(inp, w.scale)
+    assert torch.equal(a, b)
+    cu = inp.cu_seqlens
+    padded = np.concatenate([[0], cu[:4], cu[3:7], cu[6:], [cu[-1]] * 5]).astype(np.int32)
+    assert np.all(np.diff(padded) >= 0) and padded[-1] == cu[-1]
+    c = _run(inp, w.scale, cu=padded)
+    assert torch.equal(a, c)
+
+
+@pytest.mark.gpu
+def test_segments_do_not_share_state():
+    # One document's inputs changed: every other document's outputs keep their bits.
+    import torch
+    w = WL["gdn_ragged"]
+    inp = w.inputs()
+    a = _run(inp, w.scale)
+    cu = inp.cu_seqlens
+    lo, hi = int(cu[5]), int(cu[6])  # the 127-token segment
+    inp2 = synth.make_gdn_inputs(cu, w.nh, w.d, w.tensor_seed)
+    inp2.v_bits = inp2.v_bits.copy()
+    inp2.v_bits[lo:hi] ^= np.uint16(0x0040)
+    inp2.g = inp2.g.copy()
+    inp2.g[lo:hi] *= 0.5
+    b = _run(inp2, w.scale)
+    assert not torch.equal(a[lo:hi], b[lo:hi])
+    assert torch.equal(a[:lo], b[:lo]) and torch.equal(a[hi:], b[hi:])

@@ -67,6 +67,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.attn_varlen_bwd_noalloc.restype = ctypes.c_int
     lib.attn_varlen_mask_ranges.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp]
     lib.attn_varlen_mask_ranges.restype = ctypes.c_int
+    lib.gdn_varlen_workspace_bytes.argtypes = [i64, i32, i32]
+    lib.gdn_varlen_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_varlen_fwd.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp, sz, i64, i32, i32, i32, vp]
+    lib.gdn_varlen_fwd.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -286,3 +290,23 @@ def attn_varlen_mask_ranges(cu_seqlens, total: int, max_seqlen: int, window_left
 
 def default_scale(head_dim: int = 128) -> float:
     return 1.0 / math.sqrt(head_dim)
+
+
+def gdn_varlen_workspace_bytes(total: int, num_heads: int, num_segments: int) -> int:
+    """Device workspace bytes gdn_varlen_fwd needs (include/gdn_varlen.h)."""
+    return int(load_library().gdn_varlen_workspace_bytes(int(total), int(num_heads), int(num_segments)))
+
+
+def gdn_varlen_fwd(q, k, v, g, beta, cu_seqlens, scale: float, o, workspace, stream=None) -> None:
+    """Gated DeltaNet forward over packed documents.  q, k, v, o: dense bf16
+    [T, H, 128]; g, beta: dense float32 [T, H]; workspace: uint8 CUDA tensor of
+    at least gdn_varlen_workspace_bytes(T, H, num_segments) bytes."""
+    _require_dense("gdn_varlen_fwd", q, k, v, o)
+    if not (g.is_contiguous() and beta.is_contiguous()):
+        raise ValueError("g and beta must be dense float32 [T, H] tensors")
+    lib = load_library()
+    total, nh, d = (int(x) for x in q.shape)
+    nseg = int(cu_seqlens.numel()) - 1
+    rc = lib.gdn_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), float(scale), _ptr(o),
+                            _ptr(workspace), int(workspace.numel()), total, nh, d, nseg, _stream_handle(stream))
+    _check(rc, "gdn_varlen_fwd")

@@ -316,6 +316,15 @@ int prepare_bwd(BwdSetup& b, const void* dout, const void* q, const void* k, con
 
 namespace vsw {
 
+int device_for_call(int** status, int* num_sms) {
+  DeviceInfo* dev = nullptr;
+  const int rc = current_device(&dev);
+  if (rc) return rc;
+  *status = dev->status;
+  *num_sms = dev->num_sms;
+  return ATTN_OK;
+}
+
 int check_bwd_call(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
                    const int32_t* cu_seqlens, int32_t max_seqlen, int32_t window_left, float softmax_scale,
                    const void* dq, const void* dk, const void* dv, int64_t total, int32_t num_heads_q,

@@ -174,6 +174,10 @@ int bwd_on_workspace(const void* dout, const void* q, const void* k, const void*
                      int32_t num_heads_kv, int32_t head_dim, int32_t num_segments, const RowStrides* st, void* ws,
                      size_t ws_bytes, void* stream);
 
+// The current device's status word and SM count, after the same device
+// checks every entry point makes (an sm_103 GPU); returns an ATTN_* code.
+int device_for_call(int** status, int* num_sms);
+
 // Argument and device checks shared by the backward entry points, in the
 // order every entry point applies them (arguments first, then the device).
 int check_bwd_call(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,

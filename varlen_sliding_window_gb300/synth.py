@@ -161,3 +161,85 @@ def workloads() -> dict[str, Workload]:
     # sliding-window benchmark of dewml.dev/reference/performance).
     w["long65536_w4096"] = Workload("long65536_w4096", 65536, 32768, 4096, hq=16, hkv=4, cap=32768)
     return w
+
+
+# ---------------------------------------------------------------- Gated DeltaNet
+@dataclasses.dataclass
+class GdnInputs:
+    cu_seqlens: np.ndarray  # int32 [nseg+1]
+    q: np.ndarray           # float32 (bf16 values) [T, H, d], rows of unit L2 norm before rounding
+    k: np.ndarray
+    v: np.ndarray
+    do: np.ndarray          # float32 (bf16 values) [T, H, d]
+    g: np.ndarray           # float32 [T, H], log decay
+    beta: np.ndarray        # float32 [T, H]
+    q_bits: np.ndarray
+    k_bits: np.ndarray
+    v_bits: np.ndarray
+    do_bits: np.ndarray
+
+
+def make_gdn_inputs(cu_seqlens: np.ndarray, nh: int, d: int, tensor_seed: int) -> GdnInputs:
+    """Inputs of the Gated DeltaNet local layer on a packed microbatch.  Drawn
+    from default_rng(tensor_seed) in this order: q, k, v, do as N(0,1) float32
+    [T, H, d]; q and k rows divided by their L2 norm (the layer normalises them
+    before the kernel); all four rounded to bf16; then g = -softplus(x),
+    x ~ N(-5, 1.5) (decays exp(g) mostly 0.9 to 0.9995: long memory), and
+    beta = sigmoid(y), y ~ N(0, 1), both float32 [T, H]."""
+    cu = np.asarray(cu_seqlens, dtype=np.int32)
+    total = int(cu[-1])
+    rng = np.random.default_rng(tensor_seed)
+    draws = {}
+    for name in ("q", "k", "v", "do"):
+        x = rng.standard_normal((total, nh, d), dtype=np.float32)
+        if name in ("q", "k"):
+            x = x / np.maximum(np.linalg.norm(x, axis=-1, keepdims=True), np.float32(1e-6))
+        draws[name] = round_to_bf16(x)
+    x = rng.normal(-5.0, 1.5, size=(total, nh)).astype(np.float32)
+    g = (-np.logaddexp(np.float32(0.0), x)).astype(np.float32)
+    y = rng.standard_normal((total, nh), dtype=np.float32)
+    beta = (1.0 / (1.0 + np.exp(-y))).astype(np.float32)
+    return GdnInputs(cu_seqlens=cu, q=draws["q"][1], k=draws["k"][1], v=draws["v"][1], do=draws["do"][1], g=g,
+                     beta=beta, q_bits=draws["q"][0], k_bits=draws["k"][0], v_bits=draws["v"][0],
+                     do_bits=draws["do"][0])
+
+
+@dataclasses.dataclass(frozen=True)
+class GdnWorkload:
+    """The Gated DeltaNet layer on one of the packed microbatches above
+    (research.dws.rip/llm/kernels, section 03: same microbatches, 8 heads of
+    width 128)."""
+    name: str
+    total: int
+    context: int
+    nh: int = 8
+    d: int = 128
+    doc_seed: int = 0
+    tensor_seed: int = 1
+    fixed_cu: tuple[int, ...] | None = None
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def cu_seqlens(self) -> np.ndarray:
+        if self.fixed_cu is not None:
+            return np.asarray(self.fixed_cu, dtype=np.int32)
+        return pack_microbatch(self.total, self.context, self.doc_seed)
+
+    def inputs(self) -> GdnInputs:
+        return make_gdn_inputs(self.cu_seqlens(), self.nh, self.d, self.tensor_seed)
+
+
+def gdn_workloads() -> dict[str, GdnWorkload]:
+    """The 256-token three-document check (seeds as the attention one), a
+    ragged case whose segments end just before, at and after chunk edges, and
+    the 16,384-token microbatches at context 4,096 and 512."""
+    w: dict[str, GdnWorkload] = {}
+    w["gdn_tiny"] = GdnWorkload("gdn_tiny", 256, 256, tensor_seed=0, fixed_cu=(0, 61, 161, 256))
+    lens = (1, 63, 64, 65, 0, 127, 128, 129, 200, 0, 2, 300)
+    cu = tuple(int(x) for x in np.concatenate([[0], np.cumsum(lens)]))
+    w["gdn_ragged"] = GdnWorkload("gdn_ragged", cu[-1], 512, nh=4, tensor_seed=3, fixed_cu=cu)
+    w["gdn_ctx4096"] = GdnWorkload("gdn_ctx4096", 16384, 4096)
+    w["gdn_ctx512"] = GdnWorkload("gdn_ctx512", 16384, 512)
+    return w
