@@ -215,7 +215,7 @@ __device__ __forceinline__ int plan_schedule(const int* cu_seqlens, int nseg, in
   int C = 0x7fffffff;
   if (chains_max > 0) {
     const long long avg = ((long long)total_cost * U + G - 1) / G;
-    C = max(5, (int)((avg + 1) / 2));
+    C = max(5, (int)avg);
     while (C < max_cost) {
       int mine = 0;
       for (int e = tid; e < n_items; e += nt) mine += s_cost[e] > C ? (s_cost[e] + C - 1) / C : 0;

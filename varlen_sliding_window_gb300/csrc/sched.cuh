@@ -11,9 +11,12 @@
 // and would otherwise be one unit much larger than a CTA's fair share.  The
 // chunks of an item form a chain: each writes its partial sums to a buffer
 // of its own and the last to finish adds them in chunk order (see the dK/dV
-// kernel), so results stay bitwise reproducible.  C is half the average
-// per-CTA cost (at least 5 tiles), doubled until the chunks of the split
-// items fit in the available buffers.
+// kernel), so results stay bitwise reproducible.  C is the average per-CTA
+// cost (at least 5 tiles), doubled until the chunks of the split items fit in
+// the available buffers.  (Half the average balanced fixed shares a little
+// better, but every chunk costs a partial-sum write and read; with units
+// claimed at run time, or the dQ pass filling the SMs this pass leaves idle,
+// fewer and longer chunks make the whole backward shorter.)
 //
 // Every chunk (or unsplit item) expands into `units_per_item` units (heads or
 // head groups) of equal cost.  Units are ordered by cost, largest first, with
@@ -139,7 +142,7 @@ __device__ __noinline__ int build_schedule(const int* cu, int nseg, int window, 
   int C = 0x7fffffff;
   if (chains_max > 0 && units_per_item > 0) {
     const long long avg = ((long long)total_cost * units_per_item + G - 1) / G;  // tiles per CTA
-    C = max(5, (int)((avg + 1) / 2));
+    C = max(5, (int)avg);
     while (C < max_cost) {
       int nbuf = 0;  // chunks of split items
       for (int e0 = 0; e0 < n_items; e0 += 32) {
