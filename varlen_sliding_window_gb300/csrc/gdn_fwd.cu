@@ -20,10 +20,10 @@
 //   gdn_prep_kernel    one CTA per (chunk, head), all in parallel: A, Tm,
 //                      W, U and the masked Q K^T o Gamma, written to the
 //                      workspace (bf16), and gamma (fp32)
-//   gdn_state_kernel   one CTA per (segment, head, 32 value columns): carries
-//                      H (fp32, in registers) across the segment's chunks and
-//                      writes O; chunk c+1's tiles load (cp.async) while
-//                      chunk c computes
+//   gdn_state_kernel   one CTA (8 warps) per (segment, head, 32 value
+//                      columns): carries H (fp32, in registers) across the
+//                      segment's chunks and writes O; the tiles of chunks
+//                      c+1 and c+2 load (cp.async) while chunk c computes
 // The products are small (64-row) and run in bf16 on the warp-level tensor
 // core instruction (mma.sync m16n8k16, fp32 accumulation): the state pass is
 // a dependent chain of 64-row steps whose state lives in registers, where the
@@ -45,7 +45,8 @@ namespace {
 constexpr int kC = 64;         // chunk length (tokens)
 constexpr int kD = 128;        // d_k = d_v
 constexpr int kDvb = 32;       // value columns per state CTA
-constexpr int kGdnThreads = 128;
+constexpr int kGdnThreads = 256;   // prep CTA
+constexpr int kStateThreads = 256; // state CTA
 constexpr int kS128 = 136;     // smem row stride (elements) of 128-wide bf16 tiles: 272 B, conflict-free ldmatrix
 constexpr int kS64 = 72;       // 64-wide: 144 B
 constexpr int kS32 = 40;       // 32-wide: 80 B
@@ -126,8 +127,8 @@ __device__ __forceinline__ void cp_async_wait() {
 // Rows [0, len) of a [T, H, 128] bf16 tensor (token t0 on, head h) into a
 // 64 x 128 smem tile with row stride kS128; rows >= len become zero.
 __device__ __forceinline__ void load_rows128(uint32_t dst, const __nv_bfloat16* src, int t0, int len, int h, int nh,
-                                             int tid) {
-  for (int e = tid; e < kC * 16; e += kGdnThreads) {
+                                             int tid, int nt) {
+  for (int e = tid; e < kC * 16; e += nt) {
     const int r = e >> 4, c = (e & 15) * 8;
     const bool ok = r < len;
     const __nv_bfloat16* s = src + ((size_t)(t0 + (ok ? r : 0)) * nh + h) * kD + c;
@@ -263,13 +264,16 @@ struct PrepSmem {
   __nv_bfloat16 V[kC * kS128];
   float A[kC * kSF];    // A, fp32
   float X[kC * kSF];    // (I + A)^-1, fp32
+  float R[3 * 256];     // off-diagonal block products
   __nv_bfloat16 T1[kC * kS64];  // X diag(beta e^gamma)
   __nv_bfloat16 T2[kC * kS64];  // X diag(beta)
   float gam[kC];
   float bet[kC];
 };
 
-__global__ void __launch_bounds__(kGdnThreads) gdn_prep_kernel(GdnParams p) {
+static_assert(sizeof(PrepSmem) <= 113 * 1024, "two prep CTAs per SM");
+
+__global__ void __launch_bounds__(kGdnThreads, 2) gdn_prep_kernel(GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
   grid_dependency_wait();
@@ -281,9 +285,9 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_prep_kernel(GdnParams p) {
   const int len = min(ch.y, p.total - t0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t sK = smem_u32(sm.K), sQ = smem_u32(sm.Q), sV = smem_u32(sm.V);
-  load_rows128(sK, p.k, t0, len, h, p.nh, tid);
-  load_rows128(sQ, p.q, t0, len, h, p.nh, tid);
-  load_rows128(sV, p.v, t0, len, h, p.nh, tid);
+  load_rows128(sK, p.k, t0, len, h, p.nh, tid, kGdnThreads);
+  load_rows128(sQ, p.q, t0, len, h, p.nh, tid, kGdnThreads);
+  load_rows128(sV, p.v, t0, len, h, p.nh, tid, kGdnThreads);
   cp_async_commit();
   if (warp == 0) {
     // gamma = running sum of g over the chunk (2 tokens per lane), beta
@@ -305,11 +309,12 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_prep_kernel(GdnParams p) {
   cp_async_wait<0>();
   __syncthreads();
 
-  // ---- K K^T and Q K^T: warp w takes rows [16 w, 16 w + 16), all 64 columns.
-  const int r0 = 16 * warp;
-  float skk[8][4], sqk[8][4];
+  // ---- K K^T and Q K^T: warp w takes rows [16 (w % 4), +16) x columns [32 (w / 4), +32).
+  const int r0 = 16 * (warp & 3);
+  const int c0 = 32 * (warp >> 2);
+  float skk[4][4], sqk[4][4];
 #pragma unroll
-  for (int n = 0; n < 8; ++n)
+  for (int n = 0; n < 4; ++n)
 #pragma unroll
     for (int e = 0; e < 4; ++e) skk[n][e] = sqk[n][e] = 0.f;
 #pragma unroll
@@ -318,9 +323,9 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_prep_kernel(GdnParams p) {
     ldsm_x4(ak, frag_a(sK, kS128, r0, 16 * kk, lane));
     ldsm_x4(aq, frag_a(sQ, kS128, r0, 16 * kk, lane));
 #pragma unroll
-    for (int np = 0; np < 4; ++np) {
+    for (int np = 0; np < 2; ++np) {
       uint32_t b[4];
-      ldsm_x4(b, frag_bt(sK, kS128, 16 * np, 16 * kk, lane));
+      ldsm_x4(b, frag_bt(sK, kS128, c0 + 16 * np, 16 * kk, lane));
       mma_bf16(skk[2 * np], ak, b[0], b[1]);
       mma_bf16(skk[2 * np + 1], ak, b[2], b[3]);
       mma_bf16(sqk[2 * np], aq, b[0], b[1]);
@@ -330,49 +335,82 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_prep_kernel(GdnParams p) {
   // A_ij = beta_i Gamma_ij (k_i . k_j) for j < i; lower(Q K^T) o Gamma (j <= i) to the workspace.
   __nv_bfloat16* aqk = p.Aqk + ((size_t)c * p.nh + h) * (kC * kC);
 #pragma unroll
-  for (int n = 0; n < 8; ++n) {
+  for (int n = 0; n < 4; ++n) {
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int i = r0 + (lane >> 2) + 8 * hr;
-      const int j = 8 * n + 2 * (lane & 3);
+      const int j = c0 + 8 * n + 2 * (lane & 3);
       const float gi = sm.gam[i], bi = sm.bet[i];
-      const float G0 = j <= i ? expf(gi - sm.gam[j]) : 0.f;
-      const float G1 = j + 1 <= i ? expf(gi - sm.gam[j + 1]) : 0.f;
+      const float G0 = j <= i ? __expf(gi - sm.gam[j]) : 0.f;
+      const float G1 = j + 1 <= i ? __expf(gi - sm.gam[j + 1]) : 0.f;
       sm.A[i * kSF + j] = j < i ? bi * G0 * skk[n][2 * hr] : 0.f;
       sm.A[i * kSF + j + 1] = j + 1 < i ? bi * G1 * skk[n][2 * hr + 1] : 0.f;
       *reinterpret_cast<uint32_t*>(aqk + i * kC + j) = pack2(G0 * sqk[n][2 * hr], G1 * sqk[n][2 * hr + 1]);
     }
   }
   __syncthreads();
-  // ---- X = (I + A)^-1, unit lower triangular, column by column: lanes l and
-  // l + 16 of warp w solve column 16 w + l together, each summing half of the
-  // earlier rows (even / odd), joined by one shuffle per row.
-  {
-    const int col = 16 * warp + (lane & 15);
-    const int par = lane >> 4;
-    for (int i = 0; i < kC; ++i) {
-      float s = 0.f;
-      for (int j = par; j < i; j += 2) s = fmaf(sm.A[i * kSF + j], sm.X[j * kSF + col], s);
-      s += __shfl_xor_sync(0xffffffffu, s, 16);
-      if (par == 0) sm.X[i * kSF + col] = i < col ? 0.f : (i == col ? 1.f : -s);
-      __syncwarp();
+  // ---- X = (I + A)^-1 (unit lower triangular) in 16 x 16 blocks.
+  // Diagonal blocks by forward substitution, one column per thread (threads
+  // 64..127 clear the blocks above the diagonal meanwhile):
+  //     X_bb[r][c] = [r == c] - sum_{c <= j < r} A_bb[r][j] X_bb[j][c].
+  if (tid < 64) {
+    const int b = tid >> 4, c = tid & 15, o = 16 * b;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < r; ++j) acc = fmaf(sm.A[(o + r) * kSF + o + j], x[j], acc);
+      x[r] = r < c ? 0.f : (r == c ? 1.f : -acc);
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) sm.X[(o + r) * kSF + o + c] = x[r];
+  } else {
+    // blocks (bi, bj) with bi < bj: 6 blocks of 256
+    for (int e = tid - 64; e < 6 * 256; e += kGdnThreads - 64) {
+      const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+      const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      sm.X[(16 * bi + r) * kSF + 16 * bj + c] = 0.f;
     }
   }
   __syncthreads();
+  // Blocks below the diagonal, nearest first (d = i - j = 1, 2, 3):
+  //     X_ij = -X_ii R_ij,   R_ij = sum_{j <= k < i} A_ik X_kj
+  // (the rows of block i of (I + A) X = I).  R goes through sm.R.
+  for (int d = 1; d < 4; ++d) {
+    const int nb = 4 - d;  // blocks (j + d, j), j = 0 .. nb - 1
+    for (int e = tid; e < nb * 256; e += kGdnThreads) {
+      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
+      float acc = 0.f;
+      for (int k = 16 * j; k < 16 * i; ++k) acc = fmaf(sm.A[(16 * i + r) * kSF + k], sm.X[k * kSF + 16 * j + c], acc);
+      sm.R[e] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < nb * 256; e += kGdnThreads) {
+      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc = fmaf(sm.X[(16 * i + r) * kSF + 16 * i + k], sm.R[(j << 8) + (k << 4) + c], acc);
+      sm.X[(16 * i + r) * kSF + 16 * j + c] = -acc;
+    }
+    __syncthreads();
+  }
   // ---- T1 = X diag(beta e^gamma), T2 = X diag(beta) (bf16)
   for (int e = tid; e < kC * kC / 2; e += kGdnThreads) {
     const int i = e >> 5, j = (e & 31) * 2;
     const float x0 = sm.X[i * kSF + j], x1 = sm.X[i * kSF + j + 1];
     const float b0 = sm.bet[j], b1 = sm.bet[j + 1];
     *reinterpret_cast<uint32_t*>(&sm.T1[i * kS64 + j]) =
-        pack2(x0 * b0 * expf(sm.gam[j]), x1 * b1 * expf(sm.gam[j + 1]));
+        pack2(x0 * b0 * __expf(sm.gam[j]), x1 * b1 * __expf(sm.gam[j + 1]));
     *reinterpret_cast<uint32_t*>(&sm.T2[i * kS64 + j]) = pack2(x0 * b0, x1 * b1);
   }
   __syncthreads();
-  // ---- W = T1 K, U = T2 V: warp w rows [16 w, +16), all 128 columns.
-  float cw[16][4], cu[16][4];
+  // ---- W = T1 K, U = T2 V: warp w rows [16 (w % 4), +16) x columns [64 (w / 4), +64).
+  const int d0 = 64 * (warp >> 2);
+  float cw[8][4], cu[8][4];
 #pragma unroll
-  for (int n = 0; n < 16; ++n)
+  for (int n = 0; n < 8; ++n)
 #pragma unroll
     for (int e = 0; e < 4; ++e) cw[n][e] = cu[n][e] = 0.f;
   const uint32_t sT1 = smem_u32(sm.T1), sT2 = smem_u32(sm.T2);
@@ -382,10 +420,10 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_prep_kernel(GdnParams p) {
     ldsm_x4(a1, frag_a(sT1, kS64, r0, 16 * kk, lane));
     ldsm_x4(a2, frag_a(sT2, kS64, r0, 16 * kk, lane));
 #pragma unroll
-    for (int np = 0; np < 8; ++np) {
+    for (int np = 0; np < 4; ++np) {
       uint32_t bk[4], bv[4];
-      ldsm_x4_t(bk, frag_b(sK, kS128, 16 * kk, 16 * np, lane));
-      ldsm_x4_t(bv, frag_b(sV, kS128, 16 * kk, 16 * np, lane));
+      ldsm_x4_t(bk, frag_b(sK, kS128, 16 * kk, d0 + 16 * np, lane));
+      ldsm_x4_t(bv, frag_b(sV, kS128, 16 * kk, d0 + 16 * np, lane));
       mma_bf16(cw[2 * np], a1, bk[0], bk[1]);
       mma_bf16(cw[2 * np + 1], a1, bk[2], bk[3]);
       mma_bf16(cu[2 * np], a2, bv[0], bv[1]);
@@ -394,11 +432,11 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_prep_kernel(GdnParams p) {
   }
   __syncthreads();  // K, V, Q no longer read: stage W in K's place, U in V's
 #pragma unroll
-  for (int n = 0; n < 16; ++n) {
+  for (int n = 0; n < 8; ++n) {
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int i = r0 + (lane >> 2) + 8 * hr;
-      const int j = 8 * n + 2 * (lane & 3);
+      const int j = d0 + 8 * n + 2 * (lane & 3);
       *reinterpret_cast<uint32_t*>(&sm.K[i * kS128 + j]) = pack2(cw[n][2 * hr], cw[n][2 * hr + 1]);
       *reinterpret_cast<uint32_t*>(&sm.V[i * kS128 + j]) = pack2(cu[n][2 * hr], cu[n][2 * hr + 1]);
     }
@@ -424,12 +462,15 @@ struct StateStage {
   __nv_bfloat16 Aq[kC * kS64];
   float gam[kC];
 };
+constexpr int kStateStages = 3;  // chunk c + 2 loads while chunk c computes
 struct StateSmem {
-  StateStage st[2];
+  StateStage st[kStateStages];
   __nv_bfloat16 H[kD * kS32];   // the state at the chunk start, bf16 (B operand)
   __nv_bfloat16 E[kC * kS32];   // E (bf16)
   __nv_bfloat16 E2[kC * kS32];  // diag(e^(gamma_last - gamma)) E (bf16)
 };
+
+static_assert(sizeof(StateSmem) <= 227 * 1024, "the state CTA's shared memory fits one SM");
 
 // Rows of a chunk that lie inside [0, T) (all of them for a valid boundary list).
 __device__ __forceinline__ int chunk_len(const int4& ch, int total) {
@@ -437,19 +478,20 @@ __device__ __forceinline__ int chunk_len(const int4& ch, int total) {
 }
 
 __device__ __forceinline__ void load_stage(StateStage& s, const GdnParams& p, int chunk, int h, int vb, int tid) {
+  constexpr int nt = kStateThreads;
   const int4 ch = p.chunks[chunk];
   const int len = chunk_len(ch, p.total), t0 = len > 0 ? ch.x : 0;
-  load_rows128(smem_u32(s.W), p.W, t0, len, h, p.nh, tid);
-  load_rows128(smem_u32(s.K), p.k, t0, len, h, p.nh, tid);
-  load_rows128(smem_u32(s.Q), p.q, t0, len, h, p.nh, tid);
-  for (int e = tid; e < kC * 4; e += kGdnThreads) {  // U columns [32 vb, 32 vb + 32)
+  load_rows128(smem_u32(s.W), p.W, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(s.K), p.k, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(s.Q), p.q, t0, len, h, p.nh, tid, nt);
+  for (int e = tid; e < kC * 4; e += nt) {  // U columns [32 vb, 32 vb + 32)
     const int r = e >> 2, cc = (e & 3) * 8;
     const bool ok = r < len;
     cp_async16(smem_u32(&s.U[r * kS32 + cc]), p.U + ((size_t)(t0 + (ok ? r : 0)) * p.nh + h) * kD + kDvb * vb + cc,
                ok);
   }
   const __nv_bfloat16* aq = p.Aqk + ((size_t)chunk * p.nh + h) * (kC * kC);
-  for (int e = tid; e < kC * 8; e += kGdnThreads) {
+  for (int e = tid; e < kC * 8; e += nt) {
     const int r = e >> 3, cc = (e & 7) * 8;
     cp_async16(smem_u32(&s.Aq[r * kS64 + cc]), aq + r * kC + cc, true);
   }
@@ -459,7 +501,10 @@ __device__ __forceinline__ void load_stage(StateStage& s, const GdnParams& p, in
   }
 }
 
-__global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(GdnParams p) {
+// Eight warps.  Warp w computes, of the chunk's 64 x 32 products (E, Q H,
+// O), rows [16 (w % 4), +16) x columns [16 (w / 4), +16), and holds rows
+// [16 w, +16) of the 128 x 32 state.
+__global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   StateSmem& sm = *reinterpret_cast<StateSmem*>(smem_raw);
   grid_dependency_wait();
@@ -471,36 +516,37 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(GdnParams p) {
   const int first = sg.x, nch = min(sg.y, p.hdr[0] - sg.x);
   if (first < 0 || nch <= 0) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // H rows [32 warp, 32 warp + 32) x 32 columns, as mma accumulators: m-tile
-  // mt (rows 32 warp + 16 mt ..), n-tile n (columns 8 n ..).
-  float hreg[2][4][4];
+  const int r0 = 16 * (warp & 3);   // token rows of the E / O products
+  const int n0 = 16 * (warp >> 2);  // their value columns
+  const int m0 = 16 * warp;         // state rows (d_k)
+  float hreg[4][4];                 // state rows [m0, +16) x 32 columns, as mma accumulators (n-tile n)
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) hreg[n][e] = 0.f;
+  const uint32_t sH = smem_u32(sm.H), sE = smem_u32(sm.E), sE2 = smem_u32(sm.E2);
+  load_stage(sm.st[0], p, first, h, vb, tid);
+  cp_async_commit();
+  if (nch > 1) load_stage(sm.st[1], p, first + 1, h, vb, tid);
+  cp_async_commit();
+  for (int ci = 0; ci < nch; ++ci) {
+    // Stage (ci + 2) % 3 was last read by chunk ci - 1 (done: the barrier at
+    // the end of that chunk).  One group is committed per chunk, so at most
+    // the two newest groups (chunks ci + 1, ci + 2) are still in flight.
+    if (ci + 2 < nch) load_stage(sm.st[(ci + 2) % kStateStages], p, first + ci + 2, h, vb, tid);
+    cp_async_commit();
+    cp_async_wait<2>();
+    // H (bf16) for this chunk's products
 #pragma unroll
     for (int n = 0; n < 4; ++n)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) hreg[mt][n][e] = 0.f;
-  const uint32_t sH = smem_u32(sm.H), sE = smem_u32(sm.E), sE2 = smem_u32(sm.E2);
-  const int r0 = 16 * warp;  // token rows of this warp in the E and O products
-  load_stage(sm.st[0], p, first, h, vb, tid);
-  cp_async_commit();
-  for (int ci = 0; ci < nch; ++ci) {
-    if (ci + 1 < nch) load_stage(sm.st[(ci + 1) & 1], p, first + ci + 1, h, vb, tid);
-    cp_async_commit();
-    cp_async_wait<1>();
-    // H (bf16) for this chunk's products
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int i = 32 * warp + 16 * mt + (lane >> 2) + 8 * hr;
-          const int j = 8 * n + 2 * (lane & 3);
-          *reinterpret_cast<uint32_t*>(&sm.H[i * kS32 + j]) = pack2(hreg[mt][n][2 * hr], hreg[mt][n][2 * hr + 1]);
-        }
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = m0 + (lane >> 2) + 8 * hr;
+        const int j = 8 * n + 2 * (lane & 3);
+        *reinterpret_cast<uint32_t*>(&sm.H[i * kS32 + j]) = pack2(hreg[n][2 * hr], hreg[n][2 * hr + 1]);
+      }
     __syncthreads();
-    StateStage& s = sm.st[ci & 1];
+    StateStage& s = sm.st[ci % kStateStages];
     const int4 ch = p.chunks[first + ci];
     const int t0 = ch.x, len = chunk_len(ch, p.total);
     if (len <= 0) {  // only with a boundary list that breaks its rules
@@ -509,95 +555,80 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(GdnParams p) {
     }
     const uint32_t sW = smem_u32(s.W), sK = smem_u32(s.K), sQ = smem_u32(s.Q), sAq = smem_u32(s.Aq);
     const float g_last = s.gam[len - 1];
-    // ---- E = U - W H and Q H (rows [16 warp, +16), 32 columns)
-    float ce[4][4], cq[4][4];
+    // ---- E = U - W H and Q H
+    float ce[2][4], cq[2][4];
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) ce[n][e] = cq[n][e] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < kD / 16; ++kk) {
-      uint32_t aw[4], aq[4], b0[4], b1[4];
+      uint32_t aw[4], aq[4], b[4];
       ldsm_x4(aw, frag_a(sW, kS128, r0, 16 * kk, lane));
       ldsm_x4(aq, frag_a(sQ, kS128, r0, 16 * kk, lane));
-      ldsm_x4_t(b0, frag_b(sH, kS32, 16 * kk, 0, lane));
-      ldsm_x4_t(b1, frag_b(sH, kS32, 16 * kk, 16, lane));
-      mma_bf16(ce[0], aw, b0[0], b0[1]);
-      mma_bf16(ce[1], aw, b0[2], b0[3]);
-      mma_bf16(ce[2], aw, b1[0], b1[1]);
-      mma_bf16(ce[3], aw, b1[2], b1[3]);
-      mma_bf16(cq[0], aq, b0[0], b0[1]);
-      mma_bf16(cq[1], aq, b0[2], b0[3]);
-      mma_bf16(cq[2], aq, b1[0], b1[1]);
-      mma_bf16(cq[3], aq, b1[2], b1[3]);
+      ldsm_x4_t(b, frag_b(sH, kS32, 16 * kk, n0, lane));
+      mma_bf16(ce[0], aw, b[0], b[1]);
+      mma_bf16(ce[1], aw, b[2], b[3]);
+      mma_bf16(cq[0], aq, b[0], b[1]);
+      mma_bf16(cq[1], aq, b[2], b[3]);
     }
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int i = r0 + (lane >> 2) + 8 * hr;
-        const int j = 8 * n + 2 * (lane & 3);
-        const __nv_bfloat162 u2 = *reinterpret_cast<const __nv_bfloat162*>(&s.U[i * kS32 + j]);
-        const float2 u = __bfloat1622float2(u2);
+        const int j = n0 + 8 * n + 2 * (lane & 3);
+        const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&s.U[i * kS32 + j]));
         const float e0 = u.x - ce[n][2 * hr], e1 = u.y - ce[n][2 * hr + 1];
-        const float w = i < len ? expf(g_last - s.gam[i]) : 0.f;
+        const float w = i < len ? __expf(g_last - s.gam[i]) : 0.f;
         *reinterpret_cast<uint32_t*>(&sm.E[i * kS32 + j]) = pack2(e0, e1);
         *reinterpret_cast<uint32_t*>(&sm.E2[i * kS32 + j]) = pack2(e0 * w, e1 * w);
       }
     __syncthreads();
     // ---- O = scale (e^gamma Q H + Aq E)
-    float co[4][4];
+    float co[2][4];
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) co[n][e] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
-      uint32_t a[4], b0[4], b1[4];
+      uint32_t a[4], b[4];
       ldsm_x4(a, frag_a(sAq, kS64, r0, 16 * kk, lane));
-      ldsm_x4_t(b0, frag_b(sE, kS32, 16 * kk, 0, lane));
-      ldsm_x4_t(b1, frag_b(sE, kS32, 16 * kk, 16, lane));
-      mma_bf16(co[0], a, b0[0], b0[1]);
-      mma_bf16(co[1], a, b0[2], b0[3]);
-      mma_bf16(co[2], a, b1[0], b1[1]);
-      mma_bf16(co[3], a, b1[2], b1[3]);
+      ldsm_x4_t(b, frag_b(sE, kS32, 16 * kk, n0, lane));
+      mma_bf16(co[0], a, b[0], b[1]);
+      mma_bf16(co[1], a, b[2], b[3]);
     }
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int i = r0 + (lane >> 2) + 8 * hr;
       if (i < len) {
-        const float eg = expf(s.gam[i]);
-        __nv_bfloat16* orow = p.o + ((size_t)(t0 + i) * p.nh + h) * kD + kDvb * vb;
+        const float eg = __expf(s.gam[i]);
+        __nv_bfloat16* orow = p.o + ((size_t)(t0 + i) * p.nh + h) * kD + kDvb * vb + n0;
 #pragma unroll
-        for (int n = 0; n < 4; ++n) {
+        for (int n = 0; n < 2; ++n) {
           const int j = 8 * n + 2 * (lane & 3);
           *reinterpret_cast<uint32_t*>(orow + j) = pack2(p.scale * (eg * cq[n][2 * hr] + co[n][2 * hr]),
                                                          p.scale * (eg * cq[n][2 * hr + 1] + co[n][2 * hr + 1]));
         }
       }
     }
-    // ---- H = e^gamma_last H + K^T E2 (rows [32 warp, +32), K^T from K[token][dk])
-    const float dl = expf(g_last);
+    // ---- H = e^gamma_last H + K^T E2 (state rows [m0, +16); K^T read from K[token][d_k])
+    const float dl = __expf(g_last);
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) hreg[mt][n][e] *= dl;
+      for (int e = 0; e < 4; ++e) hreg[n][e] *= dl;
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
-      uint32_t b0[4], b1[4];
+      uint32_t a[4], b0[4], b1[4];
+      ldsm_x4_t(a, frag_bt(sK, kS128, 16 * kk, m0, lane));
       ldsm_x4_t(b0, frag_b(sE2, kS32, 16 * kk, 0, lane));
       ldsm_x4_t(b1, frag_b(sE2, kS32, 16 * kk, 16, lane));
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        uint32_t a[4];
-        ldsm_x4_t(a, frag_bt(sK, kS128, 16 * kk, 32 * warp + 16 * mt, lane));
-        mma_bf16(hreg[mt][0], a, b0[0], b0[1]);
-        mma_bf16(hreg[mt][1], a, b0[2], b0[3]);
-        mma_bf16(hreg[mt][2], a, b1[0], b1[1]);
-        mma_bf16(hreg[mt][3], a, b1[2], b1[3]);
-      }
+      mma_bf16(hreg[0], a, b0[0], b0[1]);
+      mma_bf16(hreg[1], a, b0[2], b0[3]);
+      mma_bf16(hreg[2], a, b1[0], b1[1]);
+      mma_bf16(hreg[3], a, b1[2], b1[3]);
     }
     __syncthreads();  // this stage, H, E and E2 are reused by the next chunk
   }
@@ -683,7 +714,7 @@ int gdn_varlen_fwd(const void* q, const void* k, const void* v, const float* g, 
     e = cudaFuncSetAttribute(gdn_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StateSmem));
   if (e == cudaSuccess)
     e = launch_pdl(gdn_state_kernel, dim3((unsigned)((long long)num_segments * num_heads * (kD / kDvb))),
-                   dim3(kGdnThreads), sizeof(StateSmem), s, p);
+                   dim3(kStateThreads), sizeof(StateSmem), s, p);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
