@@ -28,8 +28,10 @@
  * and head the WY form of the 64 delta-rule steps (a unit lower-triangular
  * 64 x 64 inverse) is built in parallel; then one pass per (segment, head,
  * 32 value columns) carries the state across the segment's chunks and writes
- * o.  Matrix products run on tensor cores in bf16 with float32 accumulation;
- * the state stays float32.
+ * o.  The backward recomputes that, carries the state's gradient back across
+ * the chunks the same way, and then forms every chunk's gradients in
+ * parallel.  Matrix products run on tensor cores in bf16 with float32
+ * accumulation; states and their gradients stay float32 along the chains.
  *
  * Ownership: every pointer is caller-owned device memory on the current
  * device, 16-byte aligned (workspace: 256-byte aligned), and `stream` is a
@@ -67,6 +69,25 @@ size_t gdn_varlen_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_
 int gdn_varlen_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                    const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes,
                    int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream);
+
+/* Bytes of device workspace gdn_varlen_bwd needs: the forward's, plus the
+ * bf16 state at every chunk start and its gradient at every chunk end
+ * ([chunks, H, 128, 128] each, chunks <= T / 64 + num_segments + 1), the
+ * chunks' pseudo-values E and the gradients dE, dW (bf16 [T, H, 128] each),
+ * a float32 [T, H, 128] part of dk and a float32 [H, T] part of dg.
+ * 0 for invalid sizes. */
+size_t gdn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments);
+
+/* Gradients of L = sum(d_o * o) for the forward above: dq, dk, dv (bf16
+ * [T, H, 128]) and dg, dbeta (float32 [T, H]), all fully overwritten.  d_o:
+ * bf16 [T, H, 128].  The forward is recomputed inside (o itself is not
+ * needed).  workspace: at least gdn_varlen_bwd_workspace_bytes(T, H,
+ * num_segments) bytes, 256-byte aligned.  Same error codes as
+ * gdn_varlen_fwd. */
+int gdn_varlen_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, const void* d_o,
+                   const int32_t* cu_seqlens, float scale, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                   void* workspace, size_t workspace_bytes, int64_t total, int32_t num_heads, int32_t head_dim,
+                   int32_t num_segments, void* stream);
 
 #ifdef __cplusplus
 }

@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_the_calls():
     names = declared_functions()
     for required in ("attn_varlen_fwd", "attn_varlen_bwd", "attn_varlen_get_status", "attn_varlen_strerror",
-                     "gdn_varlen_fwd", "gdn_varlen_workspace_bytes"):
+                     "gdn_varlen_fwd", "gdn_varlen_workspace_bytes", "gdn_varlen_bwd",
+                     "gdn_varlen_bwd_workspace_bytes"):
         assert required in names
 
 
@@ -188,3 +189,23 @@ def test_gdn_workspace_bytes(clib):
     assert n >= 2 * 16384 * 8 * 128 * 2 + (16384 // 64 + 25) * 8 * 64 * 64 * 2 + 16384 * 8 * 4
     assert n % 256 == 0
     assert f(16384, 8, 50) > n
+
+
+def test_gdn_backward_argument_validation(clib):
+    vp = ctypes.c_void_p
+
+    def bwd(**kw):
+        a = dict(q=16, k=16, v=16, g=16, beta=16, do=16, cu=16, dq=16, dk=16, dv=16, dg=16, db=16, ws=256,
+                 ws_bytes=1 << 34, total=4, nh=8, d=128, nseg=1)
+        a.update(kw)
+        return clib.gdn_varlen_bwd(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), vp(a["do"]),
+                                   vp(a["cu"]), ctypes.c_float(0.088), vp(a["dq"]), vp(a["dk"]), vp(a["dv"]),
+                                   vp(a["dg"]), vp(a["db"]), vp(a["ws"]), ctypes.c_size_t(a["ws_bytes"]),
+                                   ctypes.c_int64(a["total"]), a["nh"], a["d"], a["nseg"], vp(None))
+    assert bwd(do=None) == -1
+    assert bwd(db=None) == -1
+    assert bwd(d=64) == -3
+    assert bwd(dk=40) == -4
+    assert bwd(ws_bytes=4096) == -14
+    f, fb = clib.gdn_varlen_workspace_bytes, clib.gdn_varlen_bwd_workspace_bytes
+    assert fb(16384, 8, 25) > f(16384, 8, 25) > 0

@@ -9,6 +9,11 @@ copy used as a matrix operand, the pseudo-values E, and o itself: six
 roundings, each with a relative RMS error of about 2^-8 / sqrt(3) = 2.3e-3;
 independent, they add up to sqrt(6) x 2.3e-3 = 5.5e-3.  The bound is about
 twice that.  (The oracle sees the same bf16 q, k, v and float32 g, beta.)
+The gradients (dq, dk, dv, dg, dbeta; relative L2 <= 1.5e-2 each, same
+per-segment rule) pass through about eight such roundings (the recomputed
+factors, the bf16 copies of the state and of its gradient, dE, dW, the
+masked blocks DG and M, X as an operand, and the output):
+sqrt(8) x 2.3e-3 = 6.5e-3, and the bound is again about twice that.
 """
 import numpy as np
 import pytest
@@ -17,6 +22,7 @@ from tests.helpers import assert_per_segment, rel_l2
 from varlen_sliding_window_gb300 import synth
 
 TOL_O = 1e-2
+TOL_GRAD = {"dq": 1.5e-2, "dk": 1.5e-2, "dv": 1.5e-2, "dg": 1.5e-2, "dbeta": 1.5e-2}
 WL = synth.gdn_workloads()
 
 
@@ -93,3 +99,39 @@ def test_segments_do_not_share_state():
     b = _run(inp2, w.scale)
     assert not torch.equal(a[lo:hi], b[lo:hi])
     assert torch.equal(a[:lo], b[:lo]) and torch.equal(a[hi:], b[hi:])
+
+
+def _run_bwd(inp, scale):
+    import torch
+    from varlen_sliding_window_gb300 import binding
+    cu = inp.cu_seqlens
+    q, k, v, do = (_to_dev(b) for b in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
+    g = torch.from_numpy(inp.g).cuda()
+    beta = torch.from_numpy(inp.beta).cuda()
+    cu_t = torch.from_numpy(np.asarray(cu, dtype=np.int32)).cuda()
+    T, nh, _ = q.shape
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    dg, dbeta = (torch.full_like(g, float("nan")) for _ in range(2))
+    ws = torch.empty(binding.gdn_varlen_bwd_workspace_bytes(T, nh, len(cu) - 1), dtype=torch.uint8, device="cuda")
+    binding.gdn_varlen_bwd(q, k, v, g, beta, do, cu_t, scale, dq, dk, dv, dg, dbeta, ws)
+    torch.cuda.synchronize()
+    assert binding.attn_varlen_get_status() == 0
+    return [x.double().cpu().numpy() for x in (dq, dk, dv, dg, dbeta)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["gdn_tiny", "gdn_ragged", "gdn_ctx4096"])
+def test_backward_matches_oracle(name):
+    from oracle import gated_delta
+    w = WL[name]
+    inp = w.inputs()
+    got = _run_bwd(inp, w.scale)
+    ref = gated_delta.backward(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.do, inp.cu_seqlens, w.scale)
+    errs = {}
+    for nm, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), got, ref):
+        assert np.isfinite(a).all(), nm
+        errs[nm] = rel_l2(a, b)
+    print(name, {k: f"{v:.3e}" for k, v in errs.items()})
+    for nm, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), got, ref):
+        assert errs[nm] <= TOL_GRAD[nm], (nm, errs[nm])
+        assert_per_segment(a, b, inp.cu_seqlens, TOL_GRAD[nm], nm)

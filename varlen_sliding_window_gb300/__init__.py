@@ -14,7 +14,7 @@ _BINDING_NAMES = {
     "attn_varlen_strerror", "attn_varlen_mask_ranges", "attn_varlen_bwd_preprocess", "attn_varlen_bwd_plan",
     "attn_varlen_bwd_dkdv", "attn_varlen_bwd_dq", "attn_varlen_bwd_noalloc", "attn_varlen_fwd_strided",
     "attn_varlen_bwd_strided", "attn_varlen_set_workspace", "attn_varlen_workspace_bytes", "load_library",
-    "AttnError", "gdn_varlen_fwd", "gdn_varlen_workspace_bytes",
+    "AttnError", "gdn_varlen_fwd", "gdn_varlen_workspace_bytes", "gdn_varlen_bwd", "gdn_varlen_bwd_workspace_bytes",
 }
 
 

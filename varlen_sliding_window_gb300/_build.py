@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libvsw_attn.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_aux.cu", "attn_noalloc.cu", "gdn_fwd.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_aux.cu", "attn_noalloc.cu", "gdn.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -71,6 +71,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gdn_varlen_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_varlen_fwd.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp, sz, i64, i32, i32, i32, vp]
     lib.gdn_varlen_fwd.restype = ctypes.c_int
+    lib.gdn_varlen_bwd_workspace_bytes.argtypes = [i64, i32, i32]
+    lib.gdn_varlen_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_varlen_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp, vp, sz, i64, i32, i32, i32, vp]
+    lib.gdn_varlen_bwd.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -310,3 +314,26 @@ def gdn_varlen_fwd(q, k, v, g, beta, cu_seqlens, scale: float, o, workspace, str
     rc = lib.gdn_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), float(scale), _ptr(o),
                             _ptr(workspace), int(workspace.numel()), total, nh, d, nseg, _stream_handle(stream))
     _check(rc, "gdn_varlen_fwd")
+
+
+def gdn_varlen_bwd_workspace_bytes(total: int, num_heads: int, num_segments: int) -> int:
+    """Device workspace bytes gdn_varlen_bwd needs (include/gdn_varlen.h)."""
+    return int(load_library().gdn_varlen_bwd_workspace_bytes(int(total), int(num_heads), int(num_segments)))
+
+
+def gdn_varlen_bwd(q, k, v, g, beta, d_o, cu_seqlens, scale: float, dq, dk, dv, dg, dbeta, workspace,
+                   stream=None) -> None:
+    """Gated DeltaNet backward: dq, dk, dv (bf16 [T, H, 128]) and dg, dbeta
+    (float32 [T, H]) of sum(d_o * o); workspace of at least
+    gdn_varlen_bwd_workspace_bytes(T, H, num_segments) bytes."""
+    _require_dense("gdn_varlen_bwd", q, k, v, d_o, dq, dk, dv)
+    for t in (g, beta, dg, dbeta):
+        if not t.is_contiguous():
+            raise ValueError("g, beta, dg and dbeta must be dense float32 [T, H] tensors")
+    lib = load_library()
+    total, nh, d = (int(x) for x in q.shape)
+    nseg = int(cu_seqlens.numel()) - 1
+    rc = lib.gdn_varlen_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(d_o), _ptr(cu_seqlens), float(scale),
+                            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(workspace),
+                            int(workspace.numel()), total, nh, d, nseg, _stream_handle(stream))
+    _check(rc, "gdn_varlen_bwd")

@@ -1,0 +1,1613 @@
+// Gated DeltaNet forward over packed documents (gdn_varlen.h).
+//
+// The recurrence (per head, state H of d_k x d_v = 128 x 128, reset at every
+// segment start):
+//     e_t = beta_t (v_t - alpha_t H_{t-1}^T k_t),  H_t = alpha_t H_{t-1} + k_t e_t^T,
+//     o_t = scale H_t^T q_t,  alpha_t = exp(g_t).
+// Chunked form, chunks of 64 tokens aligned to each segment's start, gamma_i
+// the running sum of g over the chunk and Gamma_ij = exp(gamma_i - gamma_j):
+//     A    = strictly-lower( diag(beta) (K K^T) o Gamma ),   Tm = (I + A)^-1
+//     W    = Tm diag(beta e^gamma) K,   U = Tm diag(beta) V        (64 x 128 each)
+//     E    = U - W H0                                             (the chunk's e_t)
+//     O    = scale ( diag(e^gamma) Q H0 + (lower(Q K^T) o Gamma) E )
+//     H1   = e^gamma_last H0 + (diag(e^(gamma_last - gamma)) K)^T E
+// (unrolling the recurrence over the chunk: e_t depends on the earlier e_j
+// of the chunk through A, which the triangular inverse resolves at once).
+//
+// Three kernels:
+//   gdn_plan_kernel    one CTA: the chunk table (start, length of every
+//                      chunk) and the non-empty segments ordered longest first
+//   gdn_prep_kernel    one CTA per (chunk, head), all in parallel: A, Tm,
+//                      W, U and the masked Q K^T o Gamma, written to the
+//                      workspace (bf16), and gamma (fp32)
+//   gdn_state_kernel   one CTA (8 warps) per (segment, head, 32 value
+//                      columns): carries H (fp32, in registers) across the
+//                      segment's chunks and writes O; the tiles of chunks
+//                      c+1 and c+2 load (cp.async) while chunk c computes
+// The products are small (64-row) and run in bf16 on the warp-level tensor
+// core instruction (mma.sync m16n8k16, fp32 accumulation): the state pass is
+// a dependent chain of 64-row steps whose state lives in registers, where the
+// asynchronous 128-row tcgen05 path has nothing to overlap.
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn_internal.h"
+#include "attn_varlen.h"
+#include "gdn_varlen.h"
+#include "ptx.cuh"
+
+namespace vsw {
+
+namespace {
+
+constexpr int kC = 64;         // chunk length (tokens)
+constexpr int kD = 128;        // d_k = d_v
+constexpr int kDvb = 32;       // value columns per state CTA
+constexpr int kGdnThreads = 256;   // prep CTA
+constexpr int kStateThreads = 256; // state CTA
+constexpr int kS128 = 136;     // smem row stride (elements) of 128-wide bf16 tiles: 272 B, conflict-free ldmatrix
+constexpr int kS64 = 72;       // 64-wide: 144 B
+constexpr int kS32 = 40;       // 32-wide: 80 B
+constexpr int kSF = 65;        // fp32 64 x 64 tiles
+
+struct GdnParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const float* g;
+  const float* beta;
+  const int* cu;
+  __nv_bfloat16* o;
+  int total, nh, nseg, max_chunks;
+  float scale;
+  // workspace
+  int* hdr;             // [0] chunks, [1] non-empty segments
+  int4* chunks;         // [max_chunks] {start token, length, segment, chunk index in segment}
+  int4* segs;           // [nseg] by length, longest first: {first chunk, chunks, start token, length}
+  __nv_bfloat16* W;     // [T, H, 128]
+  __nv_bfloat16* U;     // [T, H, 128]
+  __nv_bfloat16* Aqk;   // [max_chunks, H, 64, 64]: lower(Q K^T) o Gamma
+  float* gam;           // [H, T]: gamma (running log decay within the chunk)
+  // backward only
+  const __nv_bfloat16* dO;  // [T, H, 128]
+  __nv_bfloat16* dq;        // [T, H, 128]
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* dg;                // [T, H]
+  float* dbeta;             // [T, H]
+  __nv_bfloat16* H0;        // [max_chunks, H, 128, 128]: state at each chunk's start (bf16)
+  __nv_bfloat16* dH1;       // [max_chunks, H, 128, 128]: gradient w.r.t. the state at each chunk's end
+  __nv_bfloat16* E;         // [T, H, 128]: E of every chunk
+  __nv_bfloat16* dE;        // [T, H, 128]: its gradient
+  __nv_bfloat16* dW;        // [T, H, 128]: gradient w.r.t. W
+  float* dKa;               // [T, H, 128]: the part of dk that needs the states
+  float* dgam;              // [H, T]: the part of d gamma that needs the states
+};
+
+// ---------------------------------------------------------------- mma.sync
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Fragment addresses (byte address of the row this lane supplies), for a
+// row-major bf16 tile at `base` with row stride `ld` elements:
+// A operand, 16 x 16 block at (r0, c0) of a row-major M x K tile.
+__device__ __forceinline__ uint32_t frag_a(uint32_t base, int ld, int r0, int c0, int lane) {
+  return base + 2u * (uint32_t)((r0 + (lane & 15)) * ld + c0 + ((lane >> 4) << 3));
+}
+// B operand for two n-tiles (n0, n0 + 8), k-block k0, from storage Bt[n][k]
+// (non-transposed load); also the A operand from storage At[k][m] (transposed
+// load, same lane pattern with (k0, m0) as (row, column)).
+__device__ __forceinline__ uint32_t frag_bt(uint32_t base, int ld, int n0, int k0, int lane) {
+  return base + 2u * (uint32_t)((n0 + (lane & 7) + ((lane >> 4) << 3)) * ld + k0 + (((lane >> 3) & 1) << 3));
+}
+// B operand for two n-tiles (n0, n0 + 8), k-block k0, from storage B[k][n]
+// (transposed load).
+__device__ __forceinline__ uint32_t frag_b(uint32_t base, int ld, int k0, int n0, int lane) {
+  return base + 2u * (uint32_t)((k0 + (lane & 15)) * ld + n0 + ((lane >> 4) << 3));
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Rows [0, len) of a [T, H, 128] bf16 tensor (token t0 on, head h) into a
+// 64 x 128 smem tile with row stride kS128; rows >= len become zero.
+__device__ __forceinline__ void load_rows128(uint32_t dst, const __nv_bfloat16* src, int t0, int len, int h, int nh,
+                                             int tid, int nt) {
+  for (int e = tid; e < kC * 16; e += nt) {
+    const int r = e >> 4, c = (e & 15) * 8;
+    const bool ok = r < len;
+    const __nv_bfloat16* s = src + ((size_t)(t0 + (ok ? r : 0)) * nh + h) * kD + c;
+    cp_async16(dst + 2u * (uint32_t)(r * kS128 + c), s, ok);
+  }
+}
+
+// ============================================================== plan
+__global__ void __launch_bounds__(256) gdn_plan_kernel(GdnParams p) {
+  __shared__ int s_first[1024 + 1];
+  __shared__ int s_hist[1024];
+  __shared__ int s_tmp[32];
+  grid_dependency_wait();
+  const int tid = threadIdx.x, nt = blockDim.x;
+  // Chunks per segment and their prefix, 1024 segments per round.
+  int base_chunk = 0;
+  for (int r0 = 0; r0 < p.nseg; r0 += 1024) {
+    const int n = min(1024, p.nseg - r0);
+    for (int i = tid; i < n; i += nt) {
+      const int L = p.cu[r0 + i + 1] - p.cu[r0 + i];
+      s_first[i] = (max(L, 0) + kC - 1) / kC;
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // exclusive prefix of s_first[0..n) by warp 0
+      const int per = (n + 31) / 32, b0 = min(n, tid * per), b1 = min(n, b0 + per);
+      int sum = 0;
+      for (int i = b0; i < b1; ++i) sum += s_first[i];
+      int incl = sum;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += y;
+      }
+      int acc = incl - sum;
+      for (int i = b0; i < b1; ++i) {
+        const int x = s_first[i];
+        s_first[i] = acc;
+        acc += x;
+      }
+      if (tid == 31) s_first[n] = incl;
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += nt) {
+      const int a = p.cu[r0 + i], L = p.cu[r0 + i + 1] - a;
+      const int f = base_chunk + s_first[i];
+      // (bounds checked against the table, which a boundary list that breaks
+      // its rules could otherwise overrun)
+      for (int j = 0; j * kC < L && f + j < p.max_chunks; ++j)
+        p.chunks[f + j] = make_int4(a + j * kC, min(kC, L - j * kC), r0 + i, j);
+    }
+    base_chunk += s_first[n];
+    __syncthreads();
+  }
+  // Non-empty segments, longest first: counting sort on the chunk count
+  // (capped at 1023; order inside a bucket is free, only the order of the
+  // state CTAs depends on it, not any result).
+  for (int b = tid; b < 1024; b += nt) s_hist[b] = 0;
+  __syncthreads();
+  for (int s = tid; s < p.nseg; s += nt) {
+    const int L = p.cu[s + 1] - p.cu[s];
+    if (L > 0) atomicAdd(&s_hist[min(1023, (L + kC - 1) / kC)], 1);
+  }
+  __syncthreads();
+  if (tid < 32) {
+    // descending exclusive prefix: lane l takes buckets 1023 - 32 l down to 992 - 32 l
+    int sum = 0;
+    for (int i = 0; i < 32; ++i) sum += s_hist[1023 - (tid * 32 + i)];
+    int incl = sum;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (tid >= o) incl += y;
+    }
+    int acc = incl - sum;
+    for (int i = 0; i < 32; ++i) {
+      const int b = 1023 - (tid * 32 + i);
+      const int x = s_hist[b];
+      s_hist[b] = acc;
+      acc += x;
+    }
+    if (tid == 31) s_tmp[0] = incl;
+  }
+  __syncthreads();
+  // first chunk of segment s = number of chunks of the segments before it
+  int chunk_base = 0;
+  for (int r0 = 0; r0 < p.nseg; r0 += 1024) {
+    const int n = min(1024, p.nseg - r0);
+    // recompute the per-round prefix (s_first was overwritten by later rounds)
+    for (int i = tid; i < n; i += nt) {
+      const int L = p.cu[r0 + i + 1] - p.cu[r0 + i];
+      s_first[i] = (max(L, 0) + kC - 1) / kC;
+    }
+    __syncthreads();
+    if (tid < 32) {
+      const int per = (n + 31) / 32, b0 = min(n, tid * per), b1 = min(n, b0 + per);
+      int sum = 0;
+      for (int i = b0; i < b1; ++i) sum += s_first[i];
+      int incl = sum;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += y;
+      }
+      int acc = incl - sum;
+      for (int i = b0; i < b1; ++i) {
+        const int x = s_first[i];
+        s_first[i] = acc;
+        acc += x;
+      }
+      if (tid == 31) s_first[n] = incl;
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += nt) {
+      const int a = p.cu[r0 + i], L = p.cu[r0 + i + 1] - a;
+      if (L > 0) {
+        const int nch = (L + kC - 1) / kC;
+        const int pos = atomicAdd(&s_hist[min(1023, nch)], 1);
+        p.segs[pos] = make_int4(chunk_base + s_first[i], nch, a, L);
+      }
+    }
+    chunk_base += s_first[n];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    p.hdr[0] = min(base_chunk, p.max_chunks);
+    p.hdr[1] = s_tmp[0];
+  }
+}
+
+// X = (I + A)^-1 for the strictly lower triangular 64 x 64 A (fp32, row
+// stride kSF), in 16 x 16 blocks, by all kGdnThreads threads of the CTA; R
+// holds 3 x 256 floats of scratch.  Ends with a CTA barrier.
+__device__ __forceinline__ void wy_inverse(const float* A, float* X, float* R, int tid) {
+  // ---- X = (I + A)^-1 (unit lower triangular) in 16 x 16 blocks.
+  // Diagonal blocks by forward substitution, one column per thread (the other
+  // threads clear the blocks above the diagonal meanwhile):
+  //     X_bb[r][c] = [r == c] - sum_{c <= j < r} A_bb[r][j] X_bb[j][c].
+  if (tid < 64) {
+    const int b = tid >> 4, c = tid & 15, o = 16 * b;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < r; ++j) acc = fmaf(A[(o + r) * kSF + o + j], x[j], acc);
+      x[r] = r < c ? 0.f : (r == c ? 1.f : -acc);
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) X[(o + r) * kSF + o + c] = x[r];
+  } else {
+    // blocks (bi, bj) with bi < bj: 6 blocks of 256
+    for (int e = tid - 64; e < 6 * 256; e += kGdnThreads - 64) {
+      const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+      const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      X[(16 * bi + r) * kSF + 16 * bj + c] = 0.f;
+    }
+  }
+  __syncthreads();
+  // Blocks below the diagonal, nearest first (d = i - j = 1, 2, 3):
+  //     X_ij = -X_ii R_ij,   R_ij = sum_{j <= k < i} A_ik X_kj
+  // (the rows of block i of (I + A) X = I), R_ij kept in R.
+  for (int d = 1; d < 4; ++d) {
+    const int nb = 4 - d;  // blocks (j + d, j), j = 0 .. nb - 1
+    for (int e = tid; e < nb * 256; e += kGdnThreads) {
+      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
+      float acc = 0.f;
+      for (int k = 16 * j; k < 16 * i; ++k) acc = fmaf(A[(16 * i + r) * kSF + k], X[k * kSF + 16 * j + c], acc);
+      R[e] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < nb * 256; e += kGdnThreads) {
+      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc = fmaf(X[(16 * i + r) * kSF + 16 * i + k], R[(j << 8) + (k << 4) + c], acc);
+      X[(16 * i + r) * kSF + 16 * j + c] = -acc;
+    }
+    __syncthreads();
+  }
+}
+
+// ============================================================== prep
+// Shared memory of the prep CTA.
+struct PrepSmem {
+  __nv_bfloat16 K[kC * kS128];
+  __nv_bfloat16 Q[kC * kS128];
+  __nv_bfloat16 V[kC * kS128];
+  float A[kC * kSF];    // A, fp32
+  float X[kC * kSF];    // (I + A)^-1, fp32
+  float R[3 * 256];     // off-diagonal block products
+  __nv_bfloat16 T1[kC * kS64];  // X diag(beta e^gamma)
+  __nv_bfloat16 T2[kC * kS64];  // X diag(beta)
+  float gam[kC];
+  float bet[kC];
+};
+
+static_assert(sizeof(PrepSmem) <= 113 * 1024, "two prep CTAs per SM");
+
+__global__ void __launch_bounds__(kGdnThreads, 2) gdn_prep_kernel(GdnParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
+  grid_dependency_wait();
+  const int c = blockIdx.x, h = blockIdx.y;
+  if (c >= p.hdr[0]) return;
+  const int4 ch = p.chunks[c];
+  const int t0 = ch.x;
+  if (t0 < 0 || t0 >= p.total) return;  // only with a boundary list that breaks its rules
+  const int len = min(ch.y, p.total - t0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t sK = smem_u32(sm.K), sQ = smem_u32(sm.Q), sV = smem_u32(sm.V);
+  load_rows128(sK, p.k, t0, len, h, p.nh, tid, kGdnThreads);
+  load_rows128(sQ, p.q, t0, len, h, p.nh, tid, kGdnThreads);
+  load_rows128(sV, p.v, t0, len, h, p.nh, tid, kGdnThreads);
+  cp_async_commit();
+  if (warp == 0) {
+    // gamma = running sum of g over the chunk (2 tokens per lane), beta
+    const int i0 = 2 * lane;
+    const float g0 = i0 < len ? p.g[(size_t)(t0 + i0) * p.nh + h] : 0.f;
+    const float g1 = i0 + 1 < len ? p.g[(size_t)(t0 + i0 + 1) * p.nh + h] : 0.f;
+    const float s = g0 + g1;
+    float incl = s;
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const float ex = incl - s;
+    sm.gam[i0] = ex + g0;
+    sm.gam[i0 + 1] = ex + g0 + g1;
+    sm.bet[i0] = i0 < len ? p.beta[(size_t)(t0 + i0) * p.nh + h] : 0.f;
+    sm.bet[i0 + 1] = i0 + 1 < len ? p.beta[(size_t)(t0 + i0 + 1) * p.nh + h] : 0.f;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // ---- K K^T and Q K^T: warp w takes rows [16 (w % 4), +16) x columns [32 (w / 4), +32).
+  const int r0 = 16 * (warp & 3);
+  const int c0 = 32 * (warp >> 2);
+  float skk[4][4], sqk[4][4];
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) skk[n][e] = sqk[n][e] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    uint32_t ak[4], aq[4];
+    ldsm_x4(ak, frag_a(sK, kS128, r0, 16 * kk, lane));
+    ldsm_x4(aq, frag_a(sQ, kS128, r0, 16 * kk, lane));
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      uint32_t b[4];
+      ldsm_x4(b, frag_bt(sK, kS128, c0 + 16 * np, 16 * kk, lane));
+      mma_bf16(skk[2 * np], ak, b[0], b[1]);
+      mma_bf16(skk[2 * np + 1], ak, b[2], b[3]);
+      mma_bf16(sqk[2 * np], aq, b[0], b[1]);
+      mma_bf16(sqk[2 * np + 1], aq, b[2], b[3]);
+    }
+  }
+  // A_ij = beta_i Gamma_ij (k_i . k_j) for j < i; lower(Q K^T) o Gamma (j <= i) to the workspace.
+  __nv_bfloat16* aqk = p.Aqk + ((size_t)c * p.nh + h) * (kC * kC);
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const int j = c0 + 8 * n + 2 * (lane & 3);
+      const float gi = sm.gam[i], bi = sm.bet[i];
+      const float G0 = j <= i ? __expf(gi - sm.gam[j]) : 0.f;
+      const float G1 = j + 1 <= i ? __expf(gi - sm.gam[j + 1]) : 0.f;
+      sm.A[i * kSF + j] = j < i ? bi * G0 * skk[n][2 * hr] : 0.f;
+      sm.A[i * kSF + j + 1] = j + 1 < i ? bi * G1 * skk[n][2 * hr + 1] : 0.f;
+      *reinterpret_cast<uint32_t*>(aqk + i * kC + j) = pack2(G0 * sqk[n][2 * hr], G1 * sqk[n][2 * hr + 1]);
+    }
+  }
+  __syncthreads();
+  wy_inverse(sm.A, sm.X, sm.R, tid);
+  // ---- T1 = X diag(beta e^gamma), T2 = X diag(beta) (bf16)
+  for (int e = tid; e < kC * kC / 2; e += kGdnThreads) {
+    const int i = e >> 5, j = (e & 31) * 2;
+    const float x0 = sm.X[i * kSF + j], x1 = sm.X[i * kSF + j + 1];
+    const float b0 = sm.bet[j], b1 = sm.bet[j + 1];
+    *reinterpret_cast<uint32_t*>(&sm.T1[i * kS64 + j]) =
+        pack2(x0 * b0 * __expf(sm.gam[j]), x1 * b1 * __expf(sm.gam[j + 1]));
+    *reinterpret_cast<uint32_t*>(&sm.T2[i * kS64 + j]) = pack2(x0 * b0, x1 * b1);
+  }
+  __syncthreads();
+  // ---- W = T1 K, U = T2 V: warp w rows [16 (w % 4), +16) x columns [64 (w / 4), +64).
+  const int d0 = 64 * (warp >> 2);
+  float cw[8][4], cu[8][4];
+#pragma unroll
+  for (int n = 0; n < 8; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cw[n][e] = cu[n][e] = 0.f;
+  const uint32_t sT1 = smem_u32(sm.T1), sT2 = smem_u32(sm.T2);
+#pragma unroll
+  for (int kk = 0; kk < kC / 16; ++kk) {
+    uint32_t a1[4], a2[4];
+    ldsm_x4(a1, frag_a(sT1, kS64, r0, 16 * kk, lane));
+    ldsm_x4(a2, frag_a(sT2, kS64, r0, 16 * kk, lane));
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      uint32_t bk[4], bv[4];
+      ldsm_x4_t(bk, frag_b(sK, kS128, 16 * kk, d0 + 16 * np, lane));
+      ldsm_x4_t(bv, frag_b(sV, kS128, 16 * kk, d0 + 16 * np, lane));
+      mma_bf16(cw[2 * np], a1, bk[0], bk[1]);
+      mma_bf16(cw[2 * np + 1], a1, bk[2], bk[3]);
+      mma_bf16(cu[2 * np], a2, bv[0], bv[1]);
+      mma_bf16(cu[2 * np + 1], a2, bv[2], bv[3]);
+    }
+  }
+  __syncthreads();  // K, V, Q no longer read: stage W in K's place, U in V's
+#pragma unroll
+  for (int n = 0; n < 8; ++n) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const int j = d0 + 8 * n + 2 * (lane & 3);
+      *reinterpret_cast<uint32_t*>(&sm.K[i * kS128 + j]) = pack2(cw[n][2 * hr], cw[n][2 * hr + 1]);
+      *reinterpret_cast<uint32_t*>(&sm.V[i * kS128 + j]) = pack2(cu[n][2 * hr], cu[n][2 * hr + 1]);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < kC * 16; e += kGdnThreads) {
+    const int r = e >> 4, cc = (e & 15) * 8;
+    if (r < len) {
+      const size_t off = ((size_t)(t0 + r) * p.nh + h) * kD + cc;
+      *reinterpret_cast<uint4*>(p.W + off) = *reinterpret_cast<const uint4*>(&sm.K[r * kS128 + cc]);
+      *reinterpret_cast<uint4*>(p.U + off) = *reinterpret_cast<const uint4*>(&sm.V[r * kS128 + cc]);
+    }
+  }
+  if (tid < kC && tid < len) p.gam[(size_t)h * p.total + t0 + tid] = sm.gam[tid];
+}
+
+// ============================================================== state + output
+struct StateStage {
+  __nv_bfloat16 W[kC * kS128];
+  __nv_bfloat16 K[kC * kS128];
+  __nv_bfloat16 Q[kC * kS128];
+  __nv_bfloat16 U[kC * kS32];
+  __nv_bfloat16 Aq[kC * kS64];
+  float gam[kC];
+};
+constexpr int kStateStages = 3;  // chunk c + 2 loads while chunk c computes
+struct StateSmem {
+  StateStage st[kStateStages];
+  __nv_bfloat16 H[kD * kS32];   // the state at the chunk start, bf16 (B operand)
+  __nv_bfloat16 E[kC * kS32];   // E (bf16)
+  __nv_bfloat16 E2[kC * kS32];  // diag(e^(gamma_last - gamma)) E (bf16)
+};
+
+static_assert(sizeof(StateSmem) <= 227 * 1024, "the state CTA's shared memory fits one SM");
+
+// Rows of a chunk that lie inside [0, T) (all of them for a valid boundary list).
+__device__ __forceinline__ int chunk_len(const int4& ch, int total) {
+  return (ch.x < 0 || ch.x >= total) ? 0 : min(ch.y, total - ch.x);
+}
+
+__device__ __forceinline__ void load_stage(StateStage& s, const GdnParams& p, int chunk, int h, int vb, int tid) {
+  constexpr int nt = kStateThreads;
+  const int4 ch = p.chunks[chunk];
+  const int len = chunk_len(ch, p.total), t0 = len > 0 ? ch.x : 0;
+  load_rows128(smem_u32(s.W), p.W, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(s.K), p.k, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(s.Q), p.q, t0, len, h, p.nh, tid, nt);
+  for (int e = tid; e < kC * 4; e += nt) {  // U columns [32 vb, 32 vb + 32)
+    const int r = e >> 2, cc = (e & 3) * 8;
+    const bool ok = r < len;
+    cp_async16(smem_u32(&s.U[r * kS32 + cc]), p.U + ((size_t)(t0 + (ok ? r : 0)) * p.nh + h) * kD + kDvb * vb + cc,
+               ok);
+  }
+  const __nv_bfloat16* aq = p.Aqk + ((size_t)chunk * p.nh + h) * (kC * kC);
+  for (int e = tid; e < kC * 8; e += nt) {
+    const int r = e >> 3, cc = (e & 7) * 8;
+    cp_async16(smem_u32(&s.Aq[r * kS64 + cc]), aq + r * kC + cc, true);
+  }
+  if (tid < kC) {
+    const bool ok = tid < len;
+    cp_async4(smem_u32(&s.gam[tid]), p.gam + (size_t)h * p.total + t0 + (ok ? tid : 0), ok);
+  }
+}
+
+// Eight warps.  Warp w computes, of the chunk's 64 x 32 products (E, Q H,
+// O), rows [16 (w % 4), +16) x columns [16 (w / 4), +16), and holds rows
+// [16 w, +16) of the 128 x 32 state.
+// kStore (the backward's recomputation): no O; the bf16 state at every chunk
+// start and every chunk's E go to the workspace instead.
+template <bool kStore>
+__global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  StateSmem& sm = *reinterpret_cast<StateSmem*>(smem_raw);
+  grid_dependency_wait();
+  const int per_seg = p.nh * (kD / kDvb);
+  const int r = blockIdx.x / per_seg, rem = blockIdx.x - r * per_seg;
+  const int h = rem / (kD / kDvb), vb = rem - h * (kD / kDvb);
+  if (r >= p.hdr[1]) return;
+  const int4 sg = p.segs[r];
+  const int first = sg.x, nch = min(sg.y, p.hdr[0] - sg.x);
+  if (first < 0 || nch <= 0) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r0 = 16 * (warp & 3);   // token rows of the E / O products
+  const int n0 = 16 * (warp >> 2);  // their value columns
+  const int m0 = 16 * warp;         // state rows (d_k)
+  float hreg[4][4];                 // state rows [m0, +16) x 32 columns, as mma accumulators (n-tile n)
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) hreg[n][e] = 0.f;
+  const uint32_t sH = smem_u32(sm.H), sE = smem_u32(sm.E), sE2 = smem_u32(sm.E2);
+  load_stage(sm.st[0], p, first, h, vb, tid);
+  cp_async_commit();
+  if (nch > 1) load_stage(sm.st[1], p, first + 1, h, vb, tid);
+  cp_async_commit();
+  for (int ci = 0; ci < nch; ++ci) {
+    // Stage (ci + 2) % 3 was last read by chunk ci - 1 (done: the barrier at
+    // the end of that chunk).  One group is committed per chunk, so at most
+    // the two newest groups (chunks ci + 1, ci + 2) are still in flight.
+    if (ci + 2 < nch) load_stage(sm.st[(ci + 2) % kStateStages], p, first + ci + 2, h, vb, tid);
+    cp_async_commit();
+    cp_async_wait<2>();
+    // H (bf16) for this chunk's products
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = m0 + (lane >> 2) + 8 * hr;
+        const int j = 8 * n + 2 * (lane & 3);
+        *reinterpret_cast<uint32_t*>(&sm.H[i * kS32 + j]) = pack2(hreg[n][2 * hr], hreg[n][2 * hr + 1]);
+      }
+    __syncthreads();
+    StateStage& s = sm.st[ci % kStateStages];
+    const int4 ch = p.chunks[first + ci];
+    const int t0 = ch.x, len = chunk_len(ch, p.total);
+    if (kStore) {
+      // H (bf16) of this chunk start: 128 rows x 64 bytes of this CTA's columns
+      __nv_bfloat16* dst = p.H0 + ((size_t)(first + ci) * p.nh + h) * (kD * kD) + kDvb * vb;
+      for (int e = tid; e < kD * 4; e += kStateThreads) {
+        const int rr = e >> 2, cc = (e & 3) * 8;
+        *reinterpret_cast<uint4*>(dst + rr * kD + cc) = *reinterpret_cast<const uint4*>(&sm.H[rr * kS32 + cc]);
+      }
+    }
+    if (len <= 0) {  // only with a boundary list that breaks its rules
+      __syncthreads();
+      continue;
+    }
+    const uint32_t sW = smem_u32(s.W), sK = smem_u32(s.K), sQ = smem_u32(s.Q), sAq = smem_u32(s.Aq);
+    const float g_last = s.gam[len - 1];
+    // ---- E = U - W H and Q H
+    float ce[2][4], cq[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ce[n][e] = cq[n][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      uint32_t aw[4], aq[4], b[4];
+      ldsm_x4(aw, frag_a(sW, kS128, r0, 16 * kk, lane));
+      ldsm_x4(aq, frag_a(sQ, kS128, r0, 16 * kk, lane));
+      ldsm_x4_t(b, frag_b(sH, kS32, 16 * kk, n0, lane));
+      mma_bf16(ce[0], aw, b[0], b[1]);
+      mma_bf16(ce[1], aw, b[2], b[3]);
+      if (!kStore) {
+        mma_bf16(cq[0], aq, b[0], b[1]);
+        mma_bf16(cq[1], aq, b[2], b[3]);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = r0 + (lane >> 2) + 8 * hr;
+        const int j = n0 + 8 * n + 2 * (lane & 3);
+        const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&s.U[i * kS32 + j]));
+        const float e0 = u.x - ce[n][2 * hr], e1 = u.y - ce[n][2 * hr + 1];
+        const float w = i < len ? __expf(g_last - s.gam[i]) : 0.f;
+        *reinterpret_cast<uint32_t*>(&sm.E[i * kS32 + j]) = pack2(e0, e1);
+        *reinterpret_cast<uint32_t*>(&sm.E2[i * kS32 + j]) = pack2(e0 * w, e1 * w);
+      }
+    __syncthreads();
+    if (kStore) {
+      for (int e = tid; e < kC * 4; e += kStateThreads) {
+        const int rr = e >> 2, cc = (e & 3) * 8;
+        if (rr < len)
+          *reinterpret_cast<uint4*>(p.E + ((size_t)(t0 + rr) * p.nh + h) * kD + kDvb * vb + cc) =
+              *reinterpret_cast<const uint4*>(&sm.E[rr * kS32 + cc]);
+      }
+    } else {
+    // ---- O = scale (e^gamma Q H + Aq E)
+    float co[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) co[n][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kC / 16; ++kk) {
+      uint32_t a[4], b[4];
+      ldsm_x4(a, frag_a(sAq, kS64, r0, 16 * kk, lane));
+      ldsm_x4_t(b, frag_b(sE, kS32, 16 * kk, n0, lane));
+      mma_bf16(co[0], a, b[0], b[1]);
+      mma_bf16(co[1], a, b[2], b[3]);
+    }
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      if (i < len) {
+        const float eg = __expf(s.gam[i]);
+        __nv_bfloat16* orow = p.o + ((size_t)(t0 + i) * p.nh + h) * kD + kDvb * vb + n0;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          const int j = 8 * n + 2 * (lane & 3);
+          *reinterpret_cast<uint32_t*>(orow + j) = pack2(p.scale * (eg * cq[n][2 * hr] + co[n][2 * hr]),
+                                                         p.scale * (eg * cq[n][2 * hr + 1] + co[n][2 * hr + 1]));
+        }
+      }
+    }
+    }
+    // ---- H = e^gamma_last H + K^T E2 (state rows [m0, +16); K^T read from K[token][d_k])
+    const float dl = __expf(g_last);
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) hreg[n][e] *= dl;
+#pragma unroll
+    for (int kk = 0; kk < kC / 16; ++kk) {
+      uint32_t a[4], b0[4], b1[4];
+      ldsm_x4_t(a, frag_bt(sK, kS128, 16 * kk, m0, lane));
+      ldsm_x4_t(b0, frag_b(sE2, kS32, 16 * kk, 0, lane));
+      ldsm_x4_t(b1, frag_b(sE2, kS32, 16 * kk, 16, lane));
+      mma_bf16(hreg[0], a, b0[0], b0[1]);
+      mma_bf16(hreg[1], a, b0[2], b0[3]);
+      mma_bf16(hreg[2], a, b1[0], b1[1]);
+      mma_bf16(hreg[3], a, b1[2], b1[3]);
+    }
+    __syncthreads();  // this stage, H, E and E2 are reused by the next chunk
+  }
+  cp_async_wait<0>();
+}
+
+
+// ============================================================== backward: state gradient
+// Reverse over a segment's chunks, per (segment, head, 32 value columns),
+// carrying dH = dL/dH1 (the state at the chunk end; zero after the last
+// chunk) in registers:
+//     dE  = scale Aq^T dO + diag(e^(gamma_last - gamma)) K dH
+//     dH0 = e^gamma_last dH + scale Q^T diag(e^gamma) dO - W^T dE
+// dE and the bf16 dH of every chunk go to the workspace for the local pass.
+struct BwdStage {
+  __nv_bfloat16 K[kC * kS128];
+  __nv_bfloat16 Q[kC * kS128];
+  __nv_bfloat16 W[kC * kS128];
+  __nv_bfloat16 Aq[kC * kS64];
+  __nv_bfloat16 dO[kC * kS32];
+  float gam[kC];
+};
+struct BwdStateSmem {
+  BwdStage st[kStateStages];
+  __nv_bfloat16 H[kD * kS32];    // dH (bf16)
+  __nv_bfloat16 E[kC * kS32];    // dE (bf16)
+  __nv_bfloat16 G[kC * kS32];    // scale e^gamma dO (bf16)
+};
+static_assert(sizeof(BwdStateSmem) <= 227 * 1024, "the backward state CTA's shared memory fits one SM");
+
+__device__ __forceinline__ void load_bwd_stage(BwdStage& s, const GdnParams& p, int chunk, int h, int vb, int tid) {
+  constexpr int nt = kStateThreads;
+  const int4 ch = p.chunks[chunk];
+  const int len = chunk_len(ch, p.total), t0 = len > 0 ? ch.x : 0;
+  load_rows128(smem_u32(s.K), p.k, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(s.Q), p.q, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(s.W), p.W, t0, len, h, p.nh, tid, nt);
+  for (int e = tid; e < kC * 4; e += nt) {  // dO columns [32 vb, 32 vb + 32)
+    const int r = e >> 2, cc = (e & 3) * 8;
+    const bool ok = r < len;
+    cp_async16(smem_u32(&s.dO[r * kS32 + cc]), p.dO + ((size_t)(t0 + (ok ? r : 0)) * p.nh + h) * kD + kDvb * vb + cc,
+               ok);
+  }
+  const __nv_bfloat16* aq = p.Aqk + ((size_t)chunk * p.nh + h) * (kC * kC);
+  for (int e = tid; e < kC * 8; e += nt) {
+    const int r = e >> 3, cc = (e & 7) * 8;
+    cp_async16(smem_u32(&s.Aq[r * kS64 + cc]), aq + r * kC + cc, true);
+  }
+  if (tid < kC) {
+    const bool ok = tid < len;
+    cp_async4(smem_u32(&s.gam[tid]), p.gam + (size_t)h * p.total + t0 + (ok ? tid : 0), ok);
+  }
+}
+
+__global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  BwdStateSmem& sm = *reinterpret_cast<BwdStateSmem*>(smem_raw);
+  grid_dependency_wait();
+  const int per_seg = p.nh * (kD / kDvb);
+  const int r = blockIdx.x / per_seg, rem = blockIdx.x - r * per_seg;
+  const int h = rem / (kD / kDvb), vb = rem - h * (kD / kDvb);
+  if (r >= p.hdr[1]) return;
+  const int4 sg = p.segs[r];
+  const int first = sg.x, nch = min(sg.y, p.hdr[0] - sg.x);
+  if (first < 0 || nch <= 0) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r0 = 16 * (warp & 3);   // token rows of dE
+  const int n0 = 16 * (warp >> 2);  // its value columns
+  const int m0 = 16 * warp;         // dH rows (d_k)
+  float dh[4][4];
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dh[n][e] = 0.f;
+  const uint32_t sH = smem_u32(sm.H), sE = smem_u32(sm.E), sG = smem_u32(sm.G);
+  // chunk ci (0 = the segment's last) is chunk first + nch - 1 - ci, in stage ci % 3
+  load_bwd_stage(sm.st[0], p, first + nch - 1, h, vb, tid);
+  cp_async_commit();
+  if (nch > 1) load_bwd_stage(sm.st[1], p, first + nch - 2, h, vb, tid);
+  cp_async_commit();
+  for (int ci = 0; ci < nch; ++ci) {
+    if (ci + 2 < nch) load_bwd_stage(sm.st[(ci + 2) % kStateStages], p, first + nch - 3 - ci, h, vb, tid);
+    cp_async_commit();
+    cp_async_wait<2>();
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = m0 + (lane >> 2) + 8 * hr;
+        const int j = 8 * n + 2 * (lane & 3);
+        *reinterpret_cast<uint32_t*>(&sm.H[i * kS32 + j]) = pack2(dh[n][2 * hr], dh[n][2 * hr + 1]);
+      }
+    __syncthreads();
+    const int chunk = first + nch - 1 - ci;
+    BwdStage& s = sm.st[ci % kStateStages];
+    const int4 ch = p.chunks[chunk];
+    const int t0 = ch.x, len = chunk_len(ch, p.total);
+    {
+      __nv_bfloat16* dst = p.dH1 + ((size_t)chunk * p.nh + h) * (kD * kD) + kDvb * vb;
+      for (int e = tid; e < kD * 4; e += kStateThreads) {
+        const int rr = e >> 2, cc = (e & 3) * 8;
+        *reinterpret_cast<uint4*>(dst + rr * kD + cc) = *reinterpret_cast<const uint4*>(&sm.H[rr * kS32 + cc]);
+      }
+    }
+    if (len <= 0) {  // only with a boundary list that breaks its rules
+      __syncthreads();
+      continue;
+    }
+    const uint32_t sK = smem_u32(s.K), sQ = smem_u32(s.Q), sW = smem_u32(s.W), sAq = smem_u32(s.Aq),
+                   sdO = smem_u32(s.dO);
+    const float g_last = s.gam[len - 1];
+    // ---- dE = scale Aq^T dO + diag(e^(gamma_last - gamma)) K dH
+    float ca[2][4], ck[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ca[n][e] = ck[n][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kC / 16; ++kk) {
+      uint32_t a[4], b[4];
+      ldsm_x4_t(a, frag_bt(sAq, kS64, 16 * kk, r0, lane));  // Aq^T: Aq stored [i][j]
+      ldsm_x4_t(b, frag_b(sdO, kS32, 16 * kk, n0, lane));
+      mma_bf16(ca[0], a, b[0], b[1]);
+      mma_bf16(ca[1], a, b[2], b[3]);
+    }
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      uint32_t a[4], b[4];
+      ldsm_x4(a, frag_a(sK, kS128, r0, 16 * kk, lane));
+      ldsm_x4_t(b, frag_b(sH, kS32, 16 * kk, n0, lane));
+      mma_bf16(ck[0], a, b[0], b[1]);
+      mma_bf16(ck[1], a, b[2], b[3]);
+    }
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const float w = i < len ? __expf(g_last - s.gam[i]) : 0.f;
+      const float m = i < len ? p.scale : 0.f;
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        const int j = n0 + 8 * n + 2 * (lane & 3);
+        *reinterpret_cast<uint32_t*>(&sm.E[i * kS32 + j]) =
+            pack2(m * ca[n][2 * hr] + w * ck[n][2 * hr], m * ca[n][2 * hr + 1] + w * ck[n][2 * hr + 1]);
+      }
+    }
+    // scale e^gamma dO, the B operand of Q^T (.) below
+    for (int e = tid; e < kC * 16; e += kStateThreads) {
+      const int i = e >> 4, j = (e & 15) * 2;
+      const float m = i < len ? p.scale * __expf(s.gam[i]) : 0.f;
+      const float2 d = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&s.dO[i * kS32 + j]));
+      *reinterpret_cast<uint32_t*>(&sm.G[i * kS32 + j]) = pack2(m * d.x, m * d.y);
+    }
+    __syncthreads();
+    for (int e = tid; e < kC * 4; e += kStateThreads) {
+      const int rr = e >> 2, cc = (e & 3) * 8;
+      if (rr < len)
+        *reinterpret_cast<uint4*>(p.dE + ((size_t)(t0 + rr) * p.nh + h) * kD + kDvb * vb + cc) =
+            *reinterpret_cast<const uint4*>(&sm.E[rr * kS32 + cc]);
+    }
+    // ---- dH = e^gamma_last dH + Q^T G - W^T dE (rows [m0, +16))
+    const float dl = __expf(g_last);
+    float cw[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dh[n][e] *= dl;
+        cw[n][e] = 0.f;
+      }
+#pragma unroll
+    for (int kk = 0; kk < kC / 16; ++kk) {
+      uint32_t aq[4], aw[4], g0[4], g1[4], e0[4], e1[4];
+      ldsm_x4_t(aq, frag_bt(sQ, kS128, 16 * kk, m0, lane));
+      ldsm_x4_t(aw, frag_bt(sW, kS128, 16 * kk, m0, lane));
+      ldsm_x4_t(g0, frag_b(sG, kS32, 16 * kk, 0, lane));
+      ldsm_x4_t(g1, frag_b(sG, kS32, 16 * kk, 16, lane));
+      ldsm_x4_t(e0, frag_b(sE, kS32, 16 * kk, 0, lane));
+      ldsm_x4_t(e1, frag_b(sE, kS32, 16 * kk, 16, lane));
+      mma_bf16(dh[0], aq, g0[0], g0[1]);
+      mma_bf16(dh[1], aq, g0[2], g0[3]);
+      mma_bf16(dh[2], aq, g1[0], g1[1]);
+      mma_bf16(dh[3], aq, g1[2], g1[3]);
+      mma_bf16(cw[0], aw, e0[0], e0[1]);
+      mma_bf16(cw[1], aw, e0[2], e0[3]);
+      mma_bf16(cw[2], aw, e1[0], e1[1]);
+      mma_bf16(cw[3], aw, e1[2], e1[3]);
+    }
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dh[n][e] -= cw[n][e];
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+}
+
+// ============================================================== backward: local, with the states
+// Per (chunk, head), everything that needs the bf16 state at the chunk start
+// (H0) or the gradient at its end (dH1), with dAqk = lower(scale dO E^T) and
+// DG = dAqk o Gamma:
+//     dq   = scale diag(e^gamma) dO H0^T + DG K                    (final)
+//     dW   = -dE H0^T                                              (to the workspace)
+//     dKa  = diag(e^(gamma_last - gamma)) E dH1^T + DG^T Q         (to the workspace)
+//     dgam = rowsum - colsum of DG o (Q K^T) + scale e^gamma_i <dO_i, (Q H0)_i>
+//            - w_i <(K dH1)_i, E_i>, and at the last token + sum_i w_i <(K dH1)_i, E_i>
+//            + e^gamma_last <dH1, H0>      (w_i = e^(gamma_last - gamma_i); to the workspace)
+struct LocalHSmem {
+  __nv_bfloat16 dO[kC * kS128];
+  __nv_bfloat16 dE[kC * kS128];
+  __nv_bfloat16 E[kC * kS128];
+  __nv_bfloat16 Q[kC * kS128];
+  __nv_bfloat16 K[kC * kS128];
+  __nv_bfloat16 H0[kD * kS128];
+  __nv_bfloat16 dH1[kD * kS128];
+  __nv_bfloat16 DG[kC * kS64];
+  float gam[kC];
+  float dgs[kC];
+  float last;  // the gamma_last terms
+};
+static_assert(sizeof(LocalHSmem) <= 227 * 1024, "fits one SM");
+
+// Sum over the 4 lanes of a quad (the lanes holding one row of an mma tile).
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  return x;
+}
+
+__global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  LocalHSmem& sm = *reinterpret_cast<LocalHSmem*>(smem_raw);
+  constexpr int nt = kStateThreads;
+  grid_dependency_wait();
+  const int c = blockIdx.x, h = blockIdx.y;
+  if (c >= p.hdr[0]) return;
+  const int4 ch = p.chunks[c];
+  const int len = chunk_len(ch, p.total);
+  if (len <= 0) return;  // only with a boundary list that breaks its rules
+  const int t0 = ch.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t sdO = smem_u32(sm.dO), sdE = smem_u32(sm.dE), sE = smem_u32(sm.E), sQ = smem_u32(sm.Q),
+                 sK = smem_u32(sm.K), sH0 = smem_u32(sm.H0), sdH1 = smem_u32(sm.dH1), sDG = smem_u32(sm.DG);
+  load_rows128(sdO, p.dO, t0, len, h, p.nh, tid, nt);
+  load_rows128(sdE, p.dE, t0, len, h, p.nh, tid, nt);
+  load_rows128(sE, p.E, t0, len, h, p.nh, tid, nt);
+  load_rows128(sQ, p.q, t0, len, h, p.nh, tid, nt);
+  load_rows128(sK, p.k, t0, len, h, p.nh, tid, nt);
+  {
+    const __nv_bfloat16* h0 = p.H0 + ((size_t)c * p.nh + h) * (kD * kD);
+    const __nv_bfloat16* d1 = p.dH1 + ((size_t)c * p.nh + h) * (kD * kD);
+    for (int e = tid; e < kD * 16; e += nt) {
+      const int r = e >> 4, cc = (e & 15) * 8;
+      cp_async16(sH0 + 2u * (uint32_t)(r * kS128 + cc), h0 + r * kD + cc, true);
+      cp_async16(sdH1 + 2u * (uint32_t)(r * kS128 + cc), d1 + r * kD + cc, true);
+    }
+  }
+  cp_async_commit();
+  if (tid < kC) {
+    sm.gam[tid] = tid < len ? p.gam[(size_t)h * p.total + t0 + tid] : 0.f;
+    sm.dgs[tid] = 0.f;
+  }
+  if (tid == 0) sm.last = 0.f;
+  cp_async_wait<0>();
+  __syncthreads();
+  const float g_last = sm.gam[len - 1];
+  const int r0 = 16 * (warp & 3);
+  // ---- dO E^T and Q K^T (rows [r0, +16), columns [c0, +32)): DG, and the
+  // DG o (Q K^T) row and column sums of dgam.
+  {
+    const int c0 = 32 * (warp >> 2);
+    float s1[4][4], s2[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s1[n][e] = s2[n][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      uint32_t ad[4], aq[4];
+      ldsm_x4(ad, frag_a(sdO, kS128, r0, 16 * kk, lane));
+      ldsm_x4(aq, frag_a(sQ, kS128, r0, 16 * kk, lane));
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        uint32_t be[4], bk[4];
+        ldsm_x4(be, frag_bt(sE, kS128, c0 + 16 * np, 16 * kk, lane));
+        ldsm_x4(bk, frag_bt(sK, kS128, c0 + 16 * np, 16 * kk, lane));
+        mma_bf16(s1[2 * np], ad, be[0], be[1]);
+        mma_bf16(s1[2 * np + 1], ad, be[2], be[3]);
+        mma_bf16(s2[2 * np], aq, bk[0], bk[1]);
+        mma_bf16(s2[2 * np + 1], aq, bk[2], bk[3]);
+      }
+    }
+    float rsum[2] = {0.f, 0.f};
+    float csum[4][2];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      csum[n][0] = csum[n][1] = 0.f;
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = r0 + (lane >> 2) + 8 * hr;
+        const int j = c0 + 8 * n + 2 * (lane & 3);
+        const float gi = sm.gam[i];
+        const float d0 = j <= i ? p.scale * s1[n][2 * hr] * __expf(gi - sm.gam[j]) : 0.f;
+        const float d1 = j + 1 <= i ? p.scale * s1[n][2 * hr + 1] * __expf(gi - sm.gam[j + 1]) : 0.f;
+        *reinterpret_cast<uint32_t*>(&sm.DG[i * kS64 + j]) = pack2(d0, d1);
+        const float r_0 = d0 * s2[n][2 * hr], r_1 = d1 * s2[n][2 * hr + 1];
+        rsum[hr] += r_0 + r_1;
+        csum[n][0] += r_0;
+        csum[n][1] += r_1;
+      }
+    }
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const float x = quad_sum(rsum[hr]);
+      if ((lane & 3) == 0) atomicAdd(&sm.dgs[r0 + (lane >> 2) + 8 * hr], x);
+    }
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float x = csum[n][e];
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        x += __shfl_xor_sync(0xffffffffu, x, 8);
+        x += __shfl_xor_sync(0xffffffffu, x, 16);
+        if (lane < 4) atomicAdd(&sm.dgs[c0 + 8 * n + 2 * lane + e], -x);
+      }
+  }
+  __syncthreads();
+  // ---- 64 x 128 products: rows [r0, +16), columns [d0, +64)
+  const int d0 = 64 * (warp >> 2);
+  float acc[8][4], acc2[8][4];
+  auto zero = [&](float (&x)[8][4]) {
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[n][e] = 0.f;
+  };
+  // acc += A (rows r0, K = 128 over `ld`-strided a) * Bt^T, Bt stored [n][k] (the H0^T / dH1^T forms)
+  auto mm_abt = [&](float (&x)[8][4], uint32_t sa, uint32_t sbt) {
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(a, frag_a(sa, kS128, r0, 16 * kk, lane));
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t b[4];
+        ldsm_x4(b, frag_bt(sbt, kS128, d0 + 16 * np, 16 * kk, lane));
+        mma_bf16(x[2 * np], a, b[0], b[1]);
+        mma_bf16(x[2 * np + 1], a, b[2], b[3]);
+      }
+    }
+  };
+  // acc += A (rows r0, K = 128) * B, B stored [k][n] (128 rows)
+  auto mm_ab = [&](float (&x)[8][4], uint32_t sa, uint32_t sb) {
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(a, frag_a(sa, kS128, r0, 16 * kk, lane));
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t b[4];
+        ldsm_x4_t(b, frag_b(sb, kS128, 16 * kk, d0 + 16 * np, lane));
+        mma_bf16(x[2 * np], a, b[0], b[1]);
+        mma_bf16(x[2 * np + 1], a, b[2], b[3]);
+      }
+    }
+  };
+  // dq = scale e^gamma dO H0^T + DG K
+  zero(acc);
+  zero(acc2);
+  mm_abt(acc, sdO, sH0);
+#pragma unroll
+  for (int kk = 0; kk < kC / 16; ++kk) {
+    uint32_t a[4];
+    ldsm_x4(a, frag_a(sDG, kS64, r0, 16 * kk, lane));
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      uint32_t b[4];
+      ldsm_x4_t(b, frag_b(sK, kS128, 16 * kk, d0 + 16 * np, lane));
+      mma_bf16(acc2[2 * np], a, b[0], b[1]);
+      mma_bf16(acc2[2 * np + 1], a, b[2], b[3]);
+    }
+  }
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int i = r0 + (lane >> 2) + 8 * hr;
+    if (i < len) {
+      const float m = p.scale * __expf(sm.gam[i]);
+      __nv_bfloat16* row = p.dq + ((size_t)(t0 + i) * p.nh + h) * kD + d0;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        const int j = 8 * n + 2 * (lane & 3);
+        *reinterpret_cast<uint32_t*>(row + j) =
+            pack2(m * acc[n][2 * hr] + acc2[n][2 * hr], m * acc[n][2 * hr + 1] + acc2[n][2 * hr + 1]);
+      }
+    }
+  }
+  // dW = -dE H0^T
+  zero(acc);
+  mm_abt(acc, sdE, sH0);
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int i = r0 + (lane >> 2) + 8 * hr;
+    if (i < len) {
+      __nv_bfloat16* row = p.dW + ((size_t)(t0 + i) * p.nh + h) * kD + d0;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        const int j = 8 * n + 2 * (lane & 3);
+        *reinterpret_cast<uint32_t*>(row + j) = pack2(-acc[n][2 * hr], -acc[n][2 * hr + 1]);
+      }
+    }
+  }
+  // dKa = w E dH1^T + DG^T Q
+  zero(acc);
+  zero(acc2);
+  mm_abt(acc, sE, sdH1);
+#pragma unroll
+  for (int kk = 0; kk < kC / 16; ++kk) {
+    uint32_t a[4];
+    ldsm_x4_t(a, frag_bt(sDG, kS64, 16 * kk, r0, lane));  // DG^T: DG stored [i][j]
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      uint32_t b[4];
+      ldsm_x4_t(b, frag_b(sQ, kS128, 16 * kk, d0 + 16 * np, lane));
+      mma_bf16(acc2[2 * np], a, b[0], b[1]);
+      mma_bf16(acc2[2 * np + 1], a, b[2], b[3]);
+    }
+  }
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int i = r0 + (lane >> 2) + 8 * hr;
+    if (i < len) {
+      const float w = __expf(g_last - sm.gam[i]);
+      float* row = p.dKa + ((size_t)(t0 + i) * p.nh + h) * kD + d0;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        const int j = 8 * n + 2 * (lane & 3);
+        *reinterpret_cast<float2*>(row + j) =
+            make_float2(w * acc[n][2 * hr] + acc2[n][2 * hr], w * acc[n][2 * hr + 1] + acc2[n][2 * hr + 1]);
+      }
+    }
+  }
+  // dgam: scale e^gamma_i <dO_i, (Q H0)_i> and the w_i <(K dH1)_i, E_i> terms
+  zero(acc);
+  zero(acc2);
+  mm_ab(acc, sQ, sH0);
+  mm_ab(acc2, sK, sdH1);
+  {
+    float rq[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = r0 + (lane >> 2) + 8 * hr;
+        const int j = d0 + 8 * n + 2 * (lane & 3);
+        const float2 dd = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.dO[i * kS128 + j]));
+        const float2 ee = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.E[i * kS128 + j]));
+        rq[hr] += acc[n][2 * hr] * dd.x + acc[n][2 * hr + 1] * dd.y;
+        rk[hr] += acc2[n][2 * hr] * ee.x + acc2[n][2 * hr + 1] * ee.y;
+      }
+    float lastp = 0.f;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const float q_ = quad_sum(rq[hr]), k_ = quad_sum(rk[hr]);
+      if ((lane & 3) == 0 && i < len) {
+        const float w = __expf(g_last - sm.gam[i]);
+        atomicAdd(&sm.dgs[i], p.scale * __expf(sm.gam[i]) * q_ - w * k_);
+        lastp += w * k_;
+      }
+    }
+    // e^gamma_last <dH1, H0>: this thread's share of the 128 x 128 products
+    float t = 0.f;
+    for (int e = tid; e < kD * kD / 2; e += nt) {
+      const int rr = e >> 6, cc = (e & 63) * 2;
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.H0[rr * kS128 + cc]));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.dH1[rr * kS128 + cc]));
+      t += a.x * b.x + a.y * b.y;
+    }
+    float x = lastp + __expf(g_last) * t;
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) atomicAdd(&sm.last, x);
+  }
+  __syncthreads();
+  if (tid < len) p.dgam[(size_t)h * p.total + t0 + tid] = sm.dgs[tid] + (tid == len - 1 ? sm.last : 0.f);
+}
+
+// ============================================================== backward: local, the WY factors
+// Per (chunk, head), from K, V, dE, dW (A and X = (I + A)^-1 recomputed):
+//     dX  = (dE V^T) diag(beta) + (dW K^T) diag(beta e^gamma)
+//     dA  = strictly-lower(-X^T dX X^T),  M = diag(beta) (dA o Gamma)
+//     dVb = X^T dE,  dKb = X^T dW
+//     dv  = diag(beta) dVb
+//     dk  = dKa + diag(beta e^gamma) dKb + M K + M^T K
+//     dbeta_i = sum_j dA_ij Gamma_ij <k_i, k_j> + <dVb_i, v_i> + e^gamma_i <dKb_i, k_i>
+//     dgam_i += rowsum_i - colsum_i of M o (K K^T) + beta_i e^gamma_i <dKb_i, k_i>
+//     dg  = reverse running sum of dgam over the chunk
+struct LocalWySmem {
+  __nv_bfloat16 K[kC * kS128];
+  __nv_bfloat16 V[kC * kS128];
+  __nv_bfloat16 dE[kC * kS128];
+  __nv_bfloat16 dW[kC * kS128];
+  float A[kC * kSF];   // A, then dA
+  float X[kC * kSF];
+  float R[3 * 256];
+  float KK[kC * kSF];
+  float dX[kC * kSF];
+  float Y[kC * kSF];
+  __nv_bfloat16 Xb[kC * kS64];
+  __nv_bfloat16 M[kC * kS64];
+  float gam[kC];
+  float bet[kC];
+  float dgs[kC];
+  float dbs[kC];
+};
+static_assert(sizeof(LocalWySmem) <= 227 * 1024, "fits one SM");
+
+__global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  LocalWySmem& sm = *reinterpret_cast<LocalWySmem*>(smem_raw);
+  constexpr int nt = kStateThreads;
+  grid_dependency_wait();
+  const int c = blockIdx.x, h = blockIdx.y;
+  if (c >= p.hdr[0]) return;
+  const int4 ch = p.chunks[c];
+  const int len = chunk_len(ch, p.total);
+  if (len <= 0) return;  // only with a boundary list that breaks its rules
+  const int t0 = ch.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t sK = smem_u32(sm.K), sV = smem_u32(sm.V), sdE = smem_u32(sm.dE), sdW = smem_u32(sm.dW),
+                 sXb = smem_u32(sm.Xb), sM = smem_u32(sm.M);
+  load_rows128(sK, p.k, t0, len, h, p.nh, tid, nt);
+  load_rows128(sV, p.v, t0, len, h, p.nh, tid, nt);
+  load_rows128(sdE, p.dE, t0, len, h, p.nh, tid, nt);
+  load_rows128(sdW, p.dW, t0, len, h, p.nh, tid, nt);
+  cp_async_commit();
+  if (tid < kC) {
+    const bool ok = tid < len;
+    sm.gam[tid] = ok ? p.gam[(size_t)h * p.total + t0 + tid] : 0.f;
+    sm.bet[tid] = ok ? p.beta[(size_t)(t0 + tid) * p.nh + h] : 0.f;
+    sm.dgs[tid] = ok ? p.dgam[(size_t)h * p.total + t0 + tid] : 0.f;
+    sm.dbs[tid] = 0.f;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  const int r0 = 16 * (warp & 3);
+  // ---- K K^T (rows [r0, +16), columns [c0, +32)): A and KK
+  {
+    const int c0 = 32 * (warp >> 2);
+    float s[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(a, frag_a(sK, kS128, r0, 16 * kk, lane));
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        uint32_t b[4];
+        ldsm_x4(b, frag_bt(sK, kS128, c0 + 16 * np, 16 * kk, lane));
+        mma_bf16(s[2 * np], a, b[0], b[1]);
+        mma_bf16(s[2 * np + 1], a, b[2], b[3]);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = r0 + (lane >> 2) + 8 * hr;
+          const int j = c0 + 8 * n + 2 * (lane & 3) + e;
+          const float kk_ = s[n][2 * hr + e];
+          sm.KK[i * kSF + j] = kk_;
+          sm.A[i * kSF + j] = j < i ? sm.bet[i] * __expf(sm.gam[i] - sm.gam[j]) * kk_ : 0.f;
+        }
+  }
+  __syncthreads();
+  wy_inverse(sm.A, sm.X, sm.R, tid);
+  // ---- Xb = bf16 X; dX = (dE V^T) diag(beta) + (dW K^T) diag(beta e^gamma)
+  for (int e = tid; e < kC * kC / 2; e += nt) {
+    const int i = e >> 5, j = (e & 31) * 2;
+    *reinterpret_cast<uint32_t*>(&sm.Xb[i * kS64 + j]) = pack2(sm.X[i * kSF + j], sm.X[i * kSF + j + 1]);
+  }
+  {
+    const int c0 = 32 * (warp >> 2);
+    float pv[4][4], pk[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pv[n][e] = pk[n][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      uint32_t ae[4], aw[4];
+      ldsm_x4(ae, frag_a(sdE, kS128, r0, 16 * kk, lane));
+      ldsm_x4(aw, frag_a(sdW, kS128, r0, 16 * kk, lane));
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        uint32_t bv[4], bk[4];
+        ldsm_x4(bv, frag_bt(sV, kS128, c0 + 16 * np, 16 * kk, lane));
+        ldsm_x4(bk, frag_bt(sK, kS128, c0 + 16 * np, 16 * kk, lane));
+        mma_bf16(pv[2 * np], ae, bv[0], bv[1]);
+        mma_bf16(pv[2 * np + 1], ae, bv[2], bv[3]);
+        mma_bf16(pk[2 * np], aw, bk[0], bk[1]);
+        mma_bf16(pk[2 * np + 1], aw, bk[2], bk[3]);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = r0 + (lane >> 2) + 8 * hr;
+          const int j = c0 + 8 * n + 2 * (lane & 3) + e;
+          const float bj = sm.bet[j];
+          sm.dX[i * kSF + j] = pv[n][2 * hr + e] * bj + pk[n][2 * hr + e] * bj * __expf(sm.gam[j]);
+        }
+  }
+  __syncthreads();
+  // ---- Y = dX X^T (X lower triangular: m <= j), then dA = -X^T Y, strictly lower (m >= i)
+  for (int e = tid; e < kC * kC; e += nt) {
+    const int i = e >> 6, j = e & 63;
+    float acc = 0.f;
+    for (int m = 0; m <= j; ++m) acc = fmaf(sm.dX[i * kSF + m], sm.X[j * kSF + m], acc);
+    sm.Y[i * kSF + j] = acc;
+  }
+  __syncthreads();
+  for (int e = tid; e < kC * kC; e += nt) {
+    const int i = e >> 6, j = e & 63;
+    float acc = 0.f;
+    if (j < i)
+      for (int m = i; m < kC; ++m) acc = fmaf(sm.X[m * kSF + i], sm.Y[m * kSF + j], acc);
+    sm.A[i * kSF + j] = -acc;
+  }
+  __syncthreads();
+  // ---- M = diag(beta) (dA o Gamma) (bf16), and the dA sums of dbeta and dgam
+  for (int e = tid; e < kC * kC / 2; e += nt) {
+    const int i = e >> 5, j = (e & 31) * 2;
+    const float g0 = j < i ? __expf(sm.gam[i] - sm.gam[j]) : 0.f;
+    const float g1 = j + 1 < i ? __expf(sm.gam[i] - sm.gam[j + 1]) : 0.f;
+    const float m0 = sm.bet[i] * sm.A[i * kSF + j] * g0, m1 = sm.bet[i] * sm.A[i * kSF + j + 1] * g1;
+    *reinterpret_cast<uint32_t*>(&sm.M[i * kS64 + j]) = pack2(m0, m1);
+    // reuse Y for dA o Gamma (dbeta) and dX for M o KK (dgam)
+    sm.Y[i * kSF + j] = sm.A[i * kSF + j] * g0 * sm.KK[i * kSF + j];
+    sm.Y[i * kSF + j + 1] = sm.A[i * kSF + j + 1] * g1 * sm.KK[i * kSF + j + 1];
+    sm.dX[i * kSF + j] = m0 * sm.KK[i * kSF + j];
+    sm.dX[i * kSF + j + 1] = m1 * sm.KK[i * kSF + j + 1];
+  }
+  __syncthreads();
+  if (tid < kC) {
+    float rb = 0.f, rg = 0.f;
+    for (int j = 0; j < kC; ++j) {
+      rb += sm.Y[tid * kSF + j];
+      rg += sm.dX[tid * kSF + j];
+    }
+    sm.dbs[tid] += rb;
+    sm.dgs[tid] += rg;
+  }
+  __syncthreads();
+  if (tid < kC) {
+    float cg = 0.f;
+    for (int i = 0; i < kC; ++i) cg += sm.dX[i * kSF + tid];
+    sm.dgs[tid] -= cg;
+  }
+  __syncthreads();
+  // ---- 64 x 128 products, rows [r0, +16) x columns [d0, +64)
+  const int d0 = 64 * (warp >> 2);
+  float cv[8][4], ck[8][4];
+#pragma unroll
+  for (int n = 0; n < 8; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cv[n][e] = ck[n][e] = 0.f;
+  // dVb = X^T dE, dKb = X^T dW
+#pragma unroll
+  for (int kk = 0; kk < kC / 16; ++kk) {
+    uint32_t a[4];
+    ldsm_x4_t(a, frag_bt(sXb, kS64, 16 * kk, r0, lane));  // X^T: X stored [i][j]
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      uint32_t be[4], bw[4];
+      ldsm_x4_t(be, frag_b(sdE, kS128, 16 * kk, d0 + 16 * np, lane));
+      ldsm_x4_t(bw, frag_b(sdW, kS128, 16 * kk, d0 + 16 * np, lane));
+      mma_bf16(cv[2 * np], a, be[0], be[1]);
+      mma_bf16(cv[2 * np + 1], a, be[2], be[3]);
+      mma_bf16(ck[2 * np], a, bw[0], bw[1]);
+      mma_bf16(ck[2 * np + 1], a, bw[2], bw[3]);
+    }
+  }
+  // dv, and the <dVb, v>, <dKb, k> row sums; dk starts as diag(beta e^gamma) dKb
+  {
+    float rv[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const float bi = sm.bet[i], be = bi * __expf(sm.gam[i]);
+      __nv_bfloat16* row = p.dv + ((size_t)(t0 + i) * p.nh + h) * kD + d0;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        const int j = 8 * n + 2 * (lane & 3);
+        const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.V[i * kS128 + d0 + j]));
+        const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[i * kS128 + d0 + j]));
+        rv[hr] += cv[n][2 * hr] * vv.x + cv[n][2 * hr + 1] * vv.y;
+        rk[hr] += ck[n][2 * hr] * kv.x + ck[n][2 * hr + 1] * kv.y;
+        if (i < len) *reinterpret_cast<uint32_t*>(row + j) = pack2(bi * cv[n][2 * hr], bi * cv[n][2 * hr + 1]);
+        ck[n][2 * hr] *= be;
+        ck[n][2 * hr + 1] *= be;
+      }
+    }
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const float v_ = quad_sum(rv[hr]), k_ = quad_sum(rk[hr]);
+      if ((lane & 3) == 0) {
+        const float eg = __expf(sm.gam[i]);
+        atomicAdd(&sm.dbs[i], v_ + eg * k_);
+        atomicAdd(&sm.dgs[i], sm.bet[i] * eg * k_);
+      }
+    }
+  }
+  // dk += M K + M^T K (+ dKa)
+#pragma unroll
+  for (int kk = 0; kk < kC / 16; ++kk) {
+    uint32_t am[4], at[4];
+    ldsm_x4(am, frag_a(sM, kS64, r0, 16 * kk, lane));
+    ldsm_x4_t(at, frag_bt(sM, kS64, 16 * kk, r0, lane));  // M^T
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      uint32_t b[4];
+      ldsm_x4_t(b, frag_b(sK, kS128, 16 * kk, d0 + 16 * np, lane));
+      mma_bf16(ck[2 * np], am, b[0], b[1]);
+      mma_bf16(ck[2 * np + 1], am, b[2], b[3]);
+      mma_bf16(ck[2 * np], at, b[0], b[1]);
+      mma_bf16(ck[2 * np + 1], at, b[2], b[3]);
+    }
+  }
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int i = r0 + (lane >> 2) + 8 * hr;
+    if (i < len) {
+      const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + d0;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        const int j = 8 * n + 2 * (lane & 3);
+        const float2 a = *reinterpret_cast<const float2*>(p.dKa + off + j);
+        *reinterpret_cast<uint32_t*>(p.dk + off + j) = pack2(ck[n][2 * hr] + a.x, ck[n][2 * hr + 1] + a.y);
+      }
+    }
+  }
+  __syncthreads();
+  // dbeta, and dg = reverse running sum of dgam (one warp, two tokens per lane)
+  if (tid < len) p.dbeta[(size_t)(t0 + tid) * p.nh + h] = sm.dbs[tid];
+  if (warp == 0) {
+    const int i0 = 62 - 2 * lane;  // lane 0 takes the last two tokens
+    const float a1 = sm.dgs[i0 + 1], a0 = sm.dgs[i0];
+    const float s2 = a0 + a1;
+    float incl = s2;
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const float ex = incl - s2;  // sum over tokens after i0 + 1
+    if (i0 + 1 < len) p.dg[(size_t)(t0 + i0 + 1) * p.nh + h] = ex + a1;
+    if (i0 < len) p.dg[(size_t)(t0 + i0) * p.nh + h] = ex + a1 + a0;
+  }
+}
+}  // namespace
+
+// Workspace layout: offsets off[0..6] of the forward's regions (header,
+// chunk table, segment table, W, U, Aqk, gamma); with bwd, off[7..13] of the
+// backward's (H0, dH1, E, dE, dW, dKa, dgam).  Returns the total size.
+size_t gdn_workspace_layout(int64_t total, int nh, int nseg, size_t off[14], bool bwd) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t max_chunks = (size_t)(total / kC) + (size_t)nseg + 1;
+  const size_t tok = (size_t)total * nh * kD;  // elements of a [T, H, 128] tensor
+  const size_t states = max_chunks * nh * kD * kD;
+  size_t o = 0;
+  off[0] = o; o += 256;                                      // header
+  off[1] = o; o += up(max_chunks * sizeof(int4));            // chunk table
+  off[2] = o; o += up((size_t)nseg * sizeof(int4) + 16);     // segment table
+  off[3] = o; o += up(tok * 2);                              // W
+  off[4] = o; o += up(tok * 2);                              // U
+  off[5] = o; o += up(max_chunks * nh * kC * kC * 2);        // Aqk
+  off[6] = o; o += up((size_t)total * nh * sizeof(float));   // gamma
+  if (bwd) {
+    off[7] = o; o += up(states * 2);                         // H0
+    off[8] = o; o += up(states * 2);                         // dH1
+    off[9] = o; o += up(tok * 2);                            // E
+    off[10] = o; o += up(tok * 2);                           // dE
+    off[11] = o; o += up(tok * 2);                           // dW
+    off[12] = o; o += up(tok * 4);                           // dKa
+    off[13] = o; o += up((size_t)total * nh * sizeof(float)); // dgam
+  }
+  return o;
+}
+
+// Argument checks shared by the forward and the backward, then the parameter
+// block over the workspace.  Returns an ATTN_* code.
+int gdn_setup(GdnParams& p, const void* q, const void* k, const void* v, const float* g, const float* beta,
+              const int32_t* cu_seqlens, float scale, void* workspace, size_t workspace_bytes, int64_t total,
+              int32_t num_heads, int32_t head_dim, int32_t num_segments, bool bwd) {
+  if (!q || !k || !v || !g || !beta || !cu_seqlens || !workspace) return ATTN_ERR_NULL_POINTER;
+  if (total < 0 || num_heads <= 0 || num_segments < 0 || (num_segments == 0 && total > 0)) return ATTN_ERR_SHAPE;
+  if (head_dim != kD) return ATTN_ERR_HEAD_DIM;
+  if (total > (1LL << 30) || num_heads > 1024 || (long long)num_segments > (1LL << 24) ||
+      total * num_heads > (1LL << 31) || (long long)num_segments * num_heads * (kD / kDvb) >= (1LL << 31))
+    return ATTN_ERR_TOO_LARGE;
+  if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  const void* ptrs[] = {q, k, v, g, beta, cu_seqlens};
+  for (const void* x : ptrs)
+    if (reinterpret_cast<uintptr_t>(x) & 15u) return ATTN_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGNMENT;
+  size_t off[14];
+  if (workspace_bytes < gdn_workspace_layout(total, num_heads, num_segments, off, bwd)) return ATTN_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p = GdnParams{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.g = g;
+  p.beta = beta;
+  p.cu = cu_seqlens;
+  p.total = (int)total;
+  p.nh = num_heads;
+  p.nseg = num_segments;
+  p.max_chunks = (int)(total / kC) + num_segments + 1;
+  p.scale = scale;
+  p.hdr = reinterpret_cast<int*>(ws + off[0]);
+  p.chunks = reinterpret_cast<int4*>(ws + off[1]);
+  p.segs = reinterpret_cast<int4*>(ws + off[2]);
+  p.W = reinterpret_cast<__nv_bfloat16*>(ws + off[3]);
+  p.U = reinterpret_cast<__nv_bfloat16*>(ws + off[4]);
+  p.Aqk = reinterpret_cast<__nv_bfloat16*>(ws + off[5]);
+  p.gam = reinterpret_cast<float*>(ws + off[6]);
+  if (bwd) {
+    p.H0 = reinterpret_cast<__nv_bfloat16*>(ws + off[7]);
+    p.dH1 = reinterpret_cast<__nv_bfloat16*>(ws + off[8]);
+    p.E = reinterpret_cast<__nv_bfloat16*>(ws + off[9]);
+    p.dE = reinterpret_cast<__nv_bfloat16*>(ws + off[10]);
+    p.dW = reinterpret_cast<__nv_bfloat16*>(ws + off[11]);
+    p.dKa = reinterpret_cast<float*>(ws + off[12]);
+    p.dgam = reinterpret_cast<float*>(ws + off[13]);
+  }
+  return ATTN_OK;
+}
+
+// The planner and the per-chunk WY factors, shared by both directions.
+cudaError_t launch_gdn_prep(const GdnParams& p, cudaStream_t s) {
+  cudaError_t e = launch_pdl(gdn_plan_kernel, dim3(1), dim3(256), 0, s, p);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(PrepSmem));
+  if (e == cudaSuccess)
+    e = launch_pdl(gdn_prep_kernel, dim3((unsigned)p.max_chunks, (unsigned)p.nh), dim3(kGdnThreads),
+                   sizeof(PrepSmem), s, p);
+  return e;
+}
+
+template <typename Smem, typename... KArgs>
+cudaError_t launch_big(void (*kernel)(KArgs...), dim3 grid, cudaStream_t s, const GdnParams& p) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+  if (e == cudaSuccess) e = launch_pdl(kernel, grid, dim3(kStateThreads), sizeof(Smem), s, p);
+  return e;
+}
+
+}  // namespace vsw
+
+extern "C" {
+
+size_t gdn_varlen_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments) {
+  if (total < 0 || num_heads <= 0 || num_segments < 0 || total > (1LL << 30) || num_heads > 1024) return 0;
+  size_t off[14];
+  return vsw::gdn_workspace_layout(total, num_heads, num_segments, off, false);
+}
+
+size_t gdn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments) {
+  if (total < 0 || num_heads <= 0 || num_segments < 0 || total > (1LL << 30) || num_heads > 1024) return 0;
+  size_t off[14];
+  return vsw::gdn_workspace_layout(total, num_heads, num_segments, off, true);
+}
+
+int gdn_varlen_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                   const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes,
+                   int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream) {
+  using namespace vsw;
+  GdnParams p;
+  int rc = gdn_setup(p, q, k, v, g, beta, cu_seqlens, scale, workspace, workspace_bytes, total, num_heads, head_dim,
+                     num_segments, false);
+  if (rc) return rc;
+  if (!o) return ATTN_ERR_NULL_POINTER;
+  if (reinterpret_cast<uintptr_t>(o) & 15u) return ATTN_ERR_ALIGNMENT;
+  int* status = nullptr;
+  int sms = 0;
+  if ((rc = device_for_call(&status, &sms))) return rc;
+  if (total == 0) return ATTN_OK;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_gdn_prep(p, s);
+  const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
+  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<false>, seg_grid, s, p);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int gdn_varlen_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, const void* d_o,
+                   const int32_t* cu_seqlens, float scale, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                   void* workspace, size_t workspace_bytes, int64_t total, int32_t num_heads, int32_t head_dim,
+                   int32_t num_segments, void* stream) {
+  using namespace vsw;
+  GdnParams p;
+  int rc = gdn_setup(p, q, k, v, g, beta, cu_seqlens, scale, workspace, workspace_bytes, total, num_heads, head_dim,
+                     num_segments, true);
+  if (rc) return rc;
+  const void* outs[] = {d_o, dq, dk, dv, dg, dbeta};
+  for (const void* x : outs)
+    if (!x) return ATTN_ERR_NULL_POINTER;
+  for (const void* x : outs)
+    if (reinterpret_cast<uintptr_t>(x) & 15u) return ATTN_ERR_ALIGNMENT;
+  int* status = nullptr;
+  int sms = 0;
+  if ((rc = device_for_call(&status, &sms))) return rc;
+  if (total == 0) return ATTN_OK;
+  p.dO = static_cast<const __nv_bfloat16*>(d_o);
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dg = dg;
+  p.dbeta = dbeta;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
+  const dim3 chunk_grid((unsigned)p.max_chunks, (unsigned)num_heads);
+  cudaError_t e = launch_gdn_prep(p, s);
+  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<true>, seg_grid, s, p);
+  if (e == cudaSuccess) e = launch_big<BwdStateSmem>(gdn_bwd_state_kernel, seg_grid, s, p);
+  if (e == cudaSuccess) e = launch_big<LocalHSmem>(gdn_bwd_local_h_kernel, chunk_grid, s, p);
+  if (e == cudaSuccess) e = launch_big<LocalWySmem>(gdn_bwd_local_wy_kernel, chunk_grid, s, p);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"
