@@ -46,7 +46,7 @@ constexpr int kC = 64;         // chunk length (tokens)
 constexpr int kD = 128;        // d_k = d_v
 constexpr int kDvb = 32;       // value columns per state CTA
 constexpr int kGdnThreads = 256;   // prep CTA
-constexpr int kStateThreads = 256; // state CTA
+constexpr int kStateThreads = 256; // state CTA (the 4 x 4 output blocks of the local passes assume 256)
 constexpr int kS128 = 136;     // smem row stride (elements) of 128-wide bf16 tiles: 272 B, conflict-free ldmatrix
 constexpr int kS64 = 72;       // 64-wide: 144 B
 constexpr int kS32 = 40;       // 32-wide: 80 B
@@ -1293,20 +1293,53 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
         }
   }
   __syncthreads();
-  // ---- Y = dX X^T (X lower triangular: m <= j), then dA = -X^T Y, strictly lower (m >= i)
-  for (int e = tid; e < kC * kC; e += nt) {
-    const int i = e >> 6, j = e & 63;
-    float acc = 0.f;
-    for (int m = 0; m <= j; ++m) acc = fmaf(sm.dX[i * kSF + m], sm.X[j * kSF + m], acc);
-    sm.Y[i * kSF + j] = acc;
-  }
-  __syncthreads();
-  for (int e = tid; e < kC * kC; e += nt) {
-    const int i = e >> 6, j = e & 63;
-    float acc = 0.f;
-    if (j < i)
-      for (int m = i; m < kC; ++m) acc = fmaf(sm.X[m * kSF + i], sm.Y[m * kSF + j], acc);
-    sm.A[i * kSF + j] = -acc;
+  // ---- Y = dX X^T, then dA = -X^T Y, strictly lower; fp32, each thread a
+  // 4 x 4 block of outputs (16 independent sums; the zeros of the triangular
+  // X make the full sums over m exact).
+  {
+    const int i0 = 4 * (tid >> 4), j0 = 4 * (tid & 15);
+    float y[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
+    for (int m = 0; m < kC; ++m) {
+      float xa[4], xb[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        xa[a] = sm.dX[(i0 + a) * kSF + m];
+        xb[a] = sm.X[(j0 + a) * kSF + m];
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(xa[a], xb[b], y[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) sm.Y[(i0 + a) * kSF + j0 + b] = y[a][b];
+    __syncthreads();
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
+    for (int m = 0; m < kC; ++m) {
+      float xa[4], xb[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        xa[a] = sm.X[m * kSF + i0 + a];
+        xb[a] = sm.Y[m * kSF + j0 + a];
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(xa[a], xb[b], y[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) sm.A[(i0 + a) * kSF + j0 + b] = j0 + b < i0 + a ? -y[a][b] : 0.f;
   }
   __syncthreads();
   // ---- M = diag(beta) (dA o Gamma) (bf16), and the dA sums of dbeta and dgam
