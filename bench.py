@@ -44,6 +44,10 @@ PAGE_FA2_MS = {"ctx512_global": 0.68, "ctx4096_global": 1.43, "ctx4096_w512": 0.
                "sweep_ctx512_global": 0.68, "sweep_ctx1024_global": 0.94, "sweep_ctx2048_global": 1.26,
                "sweep_ctx4096_global": 1.43, "sweep_ctx512_w512": 0.69, "sweep_ctx1024_w512": 0.85,
                "sweep_ctx2048_w512": 0.91, "sweep_ctx4096_w512": 0.95}
+# The page's Gated DeltaNet layer (flash-linear-attention kernels), fwd+bwd per
+# step at context 4,096 on the same unnamed GPU (research.dws.rip/llm/kernels,
+# section 03, Fig. 5): context for the Gated DeltaNet leg.
+PAGE_GDN_MS = 1.73
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # GEMM units (2*d*Hq*pairs flops each) each kernel does that the counting rule
 # credits: forward QK^T + PV; dK/dV pass S, dP, dV, dK; dQ pass dQ only (its
@@ -51,6 +55,23 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_UNITS = {"fwd": 2.0, "bwd_preprocess": 0.0, "bwd_dkdv": 4.0, "bwd_dq": 1.0}
 # Kernels of this library per step: forward, preprocess, planner, dK/dV, dQ.
 KERNELS_PER_STEP = 5
+
+
+def gdn_flops(cu: np.ndarray, nh: int, d: int) -> tuple[float, float]:
+    """Matrix-product FLOPs the Gated DeltaNet kernels perform, per call
+    (forward, backward), summed over chunks of n <= 64 tokens and heads:
+    forward 2d(5n^2 + 3nd) (K K^T, Q K^T, the two WY factors, W H, Q H, the
+    masked Q K^T block times E, K^T E); backward, which recomputes the forward
+    without O, 2d(4n^2 + 2nd) + 2d(n^2 + 3nd) + 2d(4n^2 + 5nd) + 14dn^2 + 4n^3
+    (recomputation, state-gradient pass, the two local passes)."""
+    fwd = bwd = 0.0
+    for L in np.diff(cu.astype(np.int64)):
+        for c0 in range(0, int(L), 64):
+            n = float(min(64, int(L) - c0))
+            fwd += 2 * d * (5 * n * n + 3 * n * d)
+            bwd += 2 * d * (4 * n * n + 2 * n * d) + 2 * d * (n * n + 3 * n * d) + 2 * d * (4 * n * n + 5 * n * d) \
+                + 14 * d * n * n + 4 * n ** 3
+    return fwd * nh, bwd * nh
 
 
 def unmasked_pairs(cu: np.ndarray, window: int) -> int:
@@ -259,6 +280,8 @@ def main():
                                                 for c in (512, 1024, 2048, 4096)) + ",long65536_global,long65536_w4096",
                     help="workloads whose step and kernel times are reported under also.sweep ('' for none)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--gdn", default="gdn_ctx4096,gdn_ctx512",
+                    help="Gated DeltaNet workloads measured under also.gdn ('' for none)")
     args = ap.parse_args()
     wls = synth.workloads()
     wl = wls[args.workload]
@@ -693,6 +716,74 @@ def main():
         del r
     if sweep:
         also["sweep"] = sweep
+
+    def gdn_leg(gw, steps, warmup):
+        """The Gated DeltaNet local layer (include/gdn_varlen.h) on one packed
+        microbatch: the forward and the backward call each timed with CUDA
+        events on the stream, L2 flushed between steps; FLOPs as the kernels
+        perform them (gdn_flops), HBM bytes as the inputs and outputs of each
+        call."""
+        gi = gw.inputs()
+        to = lambda bits: torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(dev)  # noqa: E731
+        q, k, v, do = (to(b) for b in (gi.q_bits, gi.k_bits, gi.v_bits, gi.do_bits))
+        g_ = torch.from_numpy(gi.g).to(dev)
+        be = torch.from_numpy(gi.beta).to(dev)
+        cu = torch.from_numpy(gi.cu_seqlens).to(dev)
+        nseg = len(gi.cu_seqlens) - 1
+        o = torch.empty_like(q)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dg, db = torch.empty_like(g_), torch.empty_like(be)
+        ws = torch.empty(binding.gdn_varlen_bwd_workspace_bytes(gw.total, gw.nh, nseg), dtype=torch.uint8,
+                         device=dev)
+        fwd = lambda: binding.gdn_varlen_fwd(q, k, v, g_, be, cu, gw.scale, o, ws)  # noqa: E731
+        bwd = lambda: binding.gdn_varlen_bwd(q, k, v, g_, be, do, cu, gw.scale, dq, dk, dv, dg, db, ws)  # noqa: E731
+        for _ in range(warmup):
+            fwd()
+            bwd()
+            flush.fill_(1.0)
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            fwd()
+            evs[i][1].record(stream)
+            flush.fill_(float(i) + 0.5)
+            evs[i][2].record(stream)
+            bwd()
+            evs[i][3].record(stream)
+        torch.cuda.synchronize()
+        status = binding.attn_varlen_get_status()
+        f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+        b_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+        ff, fb = gdn_flops(gi.cu_seqlens, gw.nh, gw.d)
+        tok = gw.total * gw.nh * gw.d * 2
+        gates = gw.total * gw.nh * 4
+        bytes_f = 4 * tok + 2 * gates            # q, k, v in, o out; g, beta
+        bytes_b = 7 * tok + 4 * gates            # q, k, v, d_o in; dq, dk, dv out; g, beta in; dg, dbeta out
+        tf_f, tf_b = ff / (f_ms * 1e-3) / 1e12, fb / (b_ms * 1e-3) / 1e12
+        dom = "bwd" if b_ms >= f_ms else "fwd"
+        ach = tf_b if dom == "bwd" else tf_f
+        del ws
+        return {"fwd_ms": f_ms, "bwd_ms": b_ms, "step_ms": f_ms + b_ms, "segments": nseg, "tokens": gw.total,
+                "heads": gw.nh, "gflop_fwd": ff / 1e9, "gflop_bwd": fb / 1e9, "tflops_fwd": tf_f, "tflops_bwd": tf_b,
+                "hbm_gbs_fwd": bytes_f / (f_ms * 1e-3) / 1e9, "hbm_gbs_bwd": bytes_b / (b_ms * 1e-3) / 1e9,
+                "roofline": {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_t, "unit": "TFLOP/s",
+                             "frac": ach / peak_t, "traffic": None,
+                             "peak_source": f"bf16 dense burst, {'of measured' if peak_src == 'measured' else 'of fallback'}",
+                             "note": "warp-level mma.sync bf16 products; the peak is the tcgen05/cuBLAS one"},
+                "page_context": ({"gdn_ms": PAGE_GDN_MS, "ratio": (f_ms + b_ms) / PAGE_GDN_MS,
+                                  "what": "the page's Gated DeltaNet layer fwd+bwd per step at context 4,096 on its "
+                                          "own unnamed GPU (research.dws.rip/llm/kernels, Fig. 5)"}
+                                 if gw.context == 4096 else None),
+                "status": status}
+
+    gdn = {}
+    gwls = synth.gdn_workloads()
+    for name in [x for x in args.gdn.split(",") if x]:
+        gdn[name] = gdn_leg(gwls[name], max(5, args.steps // 2), 3)
+    if gdn:
+        also["gdn"] = gdn
 
     line = None
     if rank == 0:

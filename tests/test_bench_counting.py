@@ -43,3 +43,28 @@ def test_flop_rule():
     r = bench.roofs(wl, pairs, 1.0, 1900.0, 6800.0, 2070.0)
     assert np.isclose(r["tensor"]["achieved_tflops"], flops / 1e-3 / 1e12)
     assert r["exp"]["count"] == 3 * pairs * 8
+
+
+def test_gdn_flop_count_lists_every_product():
+    # One segment of 64 + 1 tokens, one head of width 128: the forward's
+    # products written out shape by shape (M x K x N, 2 MKN flops each).
+    d = 128
+
+    def prods(n):
+        fwd = [(n, d, n), (n, d, n), (n, n, d), (n, n, d),       # K K^T, Q K^T, W, U
+               (n, d, d), (n, d, d), (n, n, d), (d, n, d)]       # W H, Q H, Aq E, K^T E
+        rec = [(n, d, n), (n, d, n), (n, n, d), (n, n, d), (n, d, d), (d, n, d)]
+        state = [(n, n, d), (n, d, d), (d, n, d), (d, n, d)]     # Aq^T dO, K dH, Q^T G, W^T dE
+        loc_h = [(n, d, n), (n, d, n), (n, d, d), (n, n, d), (n, d, d), (n, d, d), (n, n, d), (n, d, d),
+                 (n, d, d)]
+        loc_wy = [(n, d, n)] * 3 + [(n, n, d)] * 4 + [(n, n, n)] * 2
+        f = sum(2 * a * b * c for a, b, c in fwd)
+        b = sum(2 * a * b * c for a, b, c in rec + state + loc_h + loc_wy)
+        return f, b
+
+    f64, b64 = prods(64)
+    f1, b1 = prods(1)
+    ff, fb = bench.gdn_flops(np.array([0, 65], dtype=np.int32), 1, d)
+    assert ff == f64 + f1 and fb == b64 + b1
+    ff2, fb2 = bench.gdn_flops(np.array([0, 65, 65], dtype=np.int32), 3, d)
+    assert ff2 == 3 * ff and fb2 == 3 * fb
