@@ -51,6 +51,7 @@ constexpr int kS128 = 136;     // smem row stride (elements) of 128-wide bf16 ti
 constexpr int kS64 = 72;       // 64-wide: 144 B
 constexpr int kS32 = 40;       // 32-wide: 80 B
 constexpr int kSF = 65;        // fp32 64 x 64 tiles
+constexpr int kS4 = 68;        // fp32 64 x 64 tiles read as float4 rows
 
 struct GdnParams {
   const __nv_bfloat16* q;
@@ -271,8 +272,9 @@ __global__ void __launch_bounds__(256) gdn_plan_kernel(GdnParams p) {
 }
 
 // X = (I + A)^-1 for the strictly lower triangular 64 x 64 A (fp32, row
-// stride kSF), in 16 x 16 blocks, by all kGdnThreads threads of the CTA; R
+// stride kSF; X with row stride LDX), in 16 x 16 blocks, by all kGdnThreads threads of the CTA; R
 // holds 3 x 256 floats of scratch.  Ends with a CTA barrier.
+template <int LDX = kSF>
 __device__ __forceinline__ void wy_inverse(const float* A, float* X, float* R, int tid) {
   // ---- X = (I + A)^-1 (unit lower triangular) in 16 x 16 blocks.
   // Diagonal blocks by forward substitution, one column per thread (the other
@@ -289,14 +291,14 @@ __device__ __forceinline__ void wy_inverse(const float* A, float* X, float* R, i
       x[r] = r < c ? 0.f : (r == c ? 1.f : -acc);
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) X[(o + r) * kSF + o + c] = x[r];
+    for (int r = 0; r < 16; ++r) X[(o + r) * LDX + o + c] = x[r];
   } else {
     // blocks (bi, bj) with bi < bj: 6 blocks of 256
     for (int e = tid - 64; e < 6 * 256; e += kGdnThreads - 64) {
       const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
       const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
       const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      X[(16 * bi + r) * kSF + 16 * bj + c] = 0.f;
+      X[(16 * bi + r) * LDX + 16 * bj + c] = 0.f;
     }
   }
   __syncthreads();
@@ -308,7 +310,7 @@ __device__ __forceinline__ void wy_inverse(const float* A, float* X, float* R, i
     for (int e = tid; e < nb * 256; e += kGdnThreads) {
       const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
       float acc = 0.f;
-      for (int k = 16 * j; k < 16 * i; ++k) acc = fmaf(A[(16 * i + r) * kSF + k], X[k * kSF + 16 * j + c], acc);
+      for (int k = 16 * j; k < 16 * i; ++k) acc = fmaf(A[(16 * i + r) * kSF + k], X[k * LDX + 16 * j + c], acc);
       R[e] = acc;
     }
     __syncthreads();
@@ -316,8 +318,8 @@ __device__ __forceinline__ void wy_inverse(const float* A, float* X, float* R, i
       const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
       float acc = 0.f;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) acc = fmaf(X[(16 * i + r) * kSF + 16 * i + k], R[(j << 8) + (k << 4) + c], acc);
-      X[(16 * i + r) * kSF + 16 * j + c] = -acc;
+      for (int k = 0; k < 16; ++k) acc = fmaf(X[(16 * i + r) * LDX + 16 * i + k], R[(j << 8) + (k << 4) + c], acc);
+      X[(16 * i + r) * LDX + 16 * j + c] = -acc;
     }
     __syncthreads();
   }
@@ -345,8 +347,11 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_prep_kernel(GdnParams p) {
   PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
   grid_dependency_wait();
   const int c = blockIdx.x, h = blockIdx.y;
-  if (c >= p.hdr[0]) return;
+  // (both loads in flight at once: the table entry is in bounds for every
+  // c < max_chunks, and ignored past the number of chunks)
+  const int n_chunks = __ldcg(p.hdr);
   const int4 ch = p.chunks[c];
+  if (c >= n_chunks) return;
   const int t0 = ch.x;
   if (t0 < 0 || t0 >= p.total) return;  // only with a boundary list that breaks its rules
   const int len = min(ch.y, p.total - t0);
@@ -906,8 +911,11 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
   constexpr int nt = kStateThreads;
   grid_dependency_wait();
   const int c = blockIdx.x, h = blockIdx.y;
-  if (c >= p.hdr[0]) return;
+  // (both loads in flight at once: the table entry is in bounds for every
+  // c < max_chunks, and ignored past the number of chunks)
+  const int n_chunks = __ldcg(p.hdr);
   const int4 ch = p.chunks[c];
+  if (c >= n_chunks) return;
   const int len = chunk_len(ch, p.total);
   if (len <= 0) return;  // only with a boundary list that breaks its rules
   const int t0 = ch.x;
@@ -1173,12 +1181,13 @@ struct LocalWySmem {
   __nv_bfloat16 V[kC * kS128];
   __nv_bfloat16 dE[kC * kS128];
   __nv_bfloat16 dW[kC * kS128];
-  float A[kC * kSF];   // A, then dA
-  float X[kC * kSF];
+  float A[kC * kSF];    // A, then dA, then dA o Gamma o KK
+  float KK[kC * kSF];   // K K^T, then M o KK
+  float X[kC * kS4];    // (I + A)^-1
+  float XT[kC * kS4];   // its transpose
+  float dXT[kC * kS4];  // dX, transposed
+  float Y[kC * kS4];    // dX X^T
   float R[3 * 256];
-  float KK[kC * kSF];
-  float dX[kC * kSF];
-  float Y[kC * kSF];
   __nv_bfloat16 Xb[kC * kS64];
   __nv_bfloat16 M[kC * kS64];
   float gam[kC];
@@ -1194,8 +1203,11 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
   constexpr int nt = kStateThreads;
   grid_dependency_wait();
   const int c = blockIdx.x, h = blockIdx.y;
-  if (c >= p.hdr[0]) return;
+  // (both loads in flight at once: the table entry is in bounds for every
+  // c < max_chunks, and ignored past the number of chunks)
+  const int n_chunks = __ldcg(p.hdr);
   const int4 ch = p.chunks[c];
+  if (c >= n_chunks) return;
   const int len = chunk_len(ch, p.total);
   if (len <= 0) return;  // only with a boundary list that breaks its rules
   const int t0 = ch.x;
@@ -1251,11 +1263,14 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
         }
   }
   __syncthreads();
-  wy_inverse(sm.A, sm.X, sm.R, tid);
-  // ---- Xb = bf16 X; dX = (dE V^T) diag(beta) + (dW K^T) diag(beta e^gamma)
+  wy_inverse<kS4>(sm.A, sm.X, sm.R, tid);
+  // ---- Xb = bf16 X, XT; dX = (dE V^T) diag(beta) + (dW K^T) diag(beta e^gamma)
   for (int e = tid; e < kC * kC / 2; e += nt) {
     const int i = e >> 5, j = (e & 31) * 2;
-    *reinterpret_cast<uint32_t*>(&sm.Xb[i * kS64 + j]) = pack2(sm.X[i * kSF + j], sm.X[i * kSF + j + 1]);
+    const float x0 = sm.X[i * kS4 + j], x1 = sm.X[i * kS4 + j + 1];
+    *reinterpret_cast<uint32_t*>(&sm.Xb[i * kS64 + j]) = pack2(x0, x1);
+    sm.XT[j * kS4 + i] = x0;
+    sm.XT[(j + 1) * kS4 + i] = x1;
   }
   {
     const int c0 = 32 * (warp >> 2);
@@ -1289,13 +1304,13 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
           const int i = r0 + (lane >> 2) + 8 * hr;
           const int j = c0 + 8 * n + 2 * (lane & 3) + e;
           const float bj = sm.bet[j];
-          sm.dX[i * kSF + j] = pv[n][2 * hr + e] * bj + pk[n][2 * hr + e] * bj * __expf(sm.gam[j]);
+          sm.dXT[j * kS4 + i] = pv[n][2 * hr + e] * bj + pk[n][2 * hr + e] * bj * __expf(sm.gam[j]);
         }
   }
   __syncthreads();
   // ---- Y = dX X^T, then dA = -X^T Y, strictly lower; fp32, each thread a
-  // 4 x 4 block of outputs (16 independent sums; the zeros of the triangular
-  // X make the full sums over m exact).
+  // 4 x 4 block of outputs (16 independent sums, two float4 loads per step;
+  // the zeros of the triangular X make the full sums over m exact).
   {
     const int i0 = 4 * (tid >> 4), j0 = 4 * (tid & 15);
     float y[4][4];
@@ -1303,38 +1318,33 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
+#pragma unroll 4
     for (int m = 0; m < kC; ++m) {
-      float xa[4], xb[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        xa[a] = sm.dX[(i0 + a) * kSF + m];
-        xb[a] = sm.X[(j0 + a) * kSF + m];
-      }
+      const float4 xa = *reinterpret_cast<const float4*>(&sm.dXT[m * kS4 + i0]);  // dX[i0 + a][m]
+      const float4 xb = *reinterpret_cast<const float4*>(&sm.XT[m * kS4 + j0]);   // X[j0 + b][m]
+      const float av[4] = {xa.x, xa.y, xa.z, xa.w}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(xa[a], xb[b], y[a][b]);
+        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) sm.Y[(i0 + a) * kSF + j0 + b] = y[a][b];
+      *reinterpret_cast<float4*>(&sm.Y[(i0 + a) * kS4 + j0]) = make_float4(y[a][0], y[a][1], y[a][2], y[a][3]);
     __syncthreads();
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
+#pragma unroll 4
     for (int m = 0; m < kC; ++m) {
-      float xa[4], xb[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        xa[a] = sm.X[m * kSF + i0 + a];
-        xb[a] = sm.Y[m * kSF + j0 + a];
-      }
+      const float4 xa = *reinterpret_cast<const float4*>(&sm.X[m * kS4 + i0]);  // X[m][i0 + a]
+      const float4 xb = *reinterpret_cast<const float4*>(&sm.Y[m * kS4 + j0]);  // Y[m][j0 + b]
+      const float av[4] = {xa.x, xa.y, xa.z, xa.w}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(xa[a], xb[b], y[a][b]);
+        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -1342,25 +1352,28 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
       for (int b = 0; b < 4; ++b) sm.A[(i0 + a) * kSF + j0 + b] = j0 + b < i0 + a ? -y[a][b] : 0.f;
   }
   __syncthreads();
-  // ---- M = diag(beta) (dA o Gamma) (bf16), and the dA sums of dbeta and dgam
+  // ---- M = diag(beta) (dA o Gamma) (bf16); in place, A becomes dA o Gamma o KK
+  // (its row sums go to dbeta) and KK becomes M o KK (row minus column sums
+  // to dgam)
   for (int e = tid; e < kC * kC / 2; e += nt) {
     const int i = e >> 5, j = (e & 31) * 2;
     const float g0 = j < i ? __expf(sm.gam[i] - sm.gam[j]) : 0.f;
     const float g1 = j + 1 < i ? __expf(sm.gam[i] - sm.gam[j + 1]) : 0.f;
-    const float m0 = sm.bet[i] * sm.A[i * kSF + j] * g0, m1 = sm.bet[i] * sm.A[i * kSF + j + 1] * g1;
+    const float a0 = sm.A[i * kSF + j] * g0, a1 = sm.A[i * kSF + j + 1] * g1;
+    const float k0 = sm.KK[i * kSF + j], k1 = sm.KK[i * kSF + j + 1];
+    const float m0 = sm.bet[i] * a0, m1 = sm.bet[i] * a1;
     *reinterpret_cast<uint32_t*>(&sm.M[i * kS64 + j]) = pack2(m0, m1);
-    // reuse Y for dA o Gamma (dbeta) and dX for M o KK (dgam)
-    sm.Y[i * kSF + j] = sm.A[i * kSF + j] * g0 * sm.KK[i * kSF + j];
-    sm.Y[i * kSF + j + 1] = sm.A[i * kSF + j + 1] * g1 * sm.KK[i * kSF + j + 1];
-    sm.dX[i * kSF + j] = m0 * sm.KK[i * kSF + j];
-    sm.dX[i * kSF + j + 1] = m1 * sm.KK[i * kSF + j + 1];
+    sm.A[i * kSF + j] = a0 * k0;
+    sm.A[i * kSF + j + 1] = a1 * k1;
+    sm.KK[i * kSF + j] = m0 * k0;
+    sm.KK[i * kSF + j + 1] = m1 * k1;
   }
   __syncthreads();
   if (tid < kC) {
     float rb = 0.f, rg = 0.f;
     for (int j = 0; j < kC; ++j) {
-      rb += sm.Y[tid * kSF + j];
-      rg += sm.dX[tid * kSF + j];
+      rb += sm.A[tid * kSF + j];
+      rg += sm.KK[tid * kSF + j];
     }
     sm.dbs[tid] += rb;
     sm.dgs[tid] += rg;
@@ -1368,7 +1381,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
   __syncthreads();
   if (tid < kC) {
     float cg = 0.f;
-    for (int i = 0; i < kC; ++i) cg += sm.dX[i * kSF + tid];
+    for (int i = 0; i < kC; ++i) cg += sm.KK[i * kSF + tid];
     sm.dgs[tid] -= cg;
   }
   __syncthreads();
