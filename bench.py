@@ -9,7 +9,9 @@ through the library's C ABI.  Prints one JSON line (rank 0).
 The headline workload is the context-4,096 global-causal microbatch; the
 window-512 and context-512 microbatches, the context sweep (512 ... 4,096,
 global and window 512) and the 65,536-token 16/4-head long-context case are
-measured in the same run under "also".
+measured in the same run under "also"; the Gated DeltaNet local layer
+(include/gdn_varlen.h) on the context-4,096 and context-512 microbatches under
+"also.gdn".
 
 Timing: CUDA events on the launching stream around every kernel of every
 step; the L2 (129 MB) is flushed by writing a 512 MiB buffer between steps,
@@ -122,12 +124,13 @@ def roofs(w, pairs: int, ms: float, peak_t: float, peak_hbm: float, sm_mhz) -> d
 
 
 def csrc_hash() -> str:
-    """sha1 (12 hex digits) of the CUDA sources: *.cu, then *.cuh, then *.h, each sorted."""
+    """sha1 (12 hex digits) of the attention kernels' sources: attn_*.cu, then
+    *.cuh, then *.h, each sorted (the Gated DeltaNet file does not change them)."""
     import glob
     import hashlib
     d = os.path.join(ROOT, "varlen_sliding_window_gb300", "csrc")
     h = hashlib.sha1()
-    for pat in ("*.cu", "*.cuh", "*.h"):
+    for pat in ("attn_*.cu", "*.cuh", "*.h"):
         for f in sorted(glob.glob(os.path.join(d, pat))):
             h.update(open(f, "rb").read())
     return h.hexdigest()[:12]
