@@ -46,7 +46,8 @@ constexpr int kC = 64;         // chunk length (tokens)
 constexpr int kD = 128;        // d_k = d_v
 constexpr int kDvb = 32;       // value columns per state CTA
 constexpr int kGdnThreads = 256;   // prep CTA
-constexpr int kStateThreads = 256; // state CTA (the 4 x 4 output blocks of the local passes assume 256)
+constexpr int kStateThreads = 256; // state CTA
+constexpr int kLocalThreads = 512; // local backward CTAs (their output blocks assume 16 warps)
 constexpr int kS128 = 136;     // smem row stride (elements) of 128-wide bf16 tiles: 272 B, conflict-free ldmatrix
 constexpr int kS64 = 72;       // 64-wide: 144 B
 constexpr int kS32 = 40;       // 32-wide: 80 B
@@ -272,9 +273,9 @@ __global__ void __launch_bounds__(256) gdn_plan_kernel(GdnParams p) {
 }
 
 // X = (I + A)^-1 for the strictly lower triangular 64 x 64 A (fp32, row
-// stride kSF; X with row stride LDX), in 16 x 16 blocks, by all kGdnThreads threads of the CTA; R
+// stride kSF; X with row stride LDX), in 16 x 16 blocks, by all NT threads of the CTA; R
 // holds 3 x 256 floats of scratch.  Ends with a CTA barrier.
-template <int LDX = kSF>
+template <int LDX = kSF, int NT = kGdnThreads>
 __device__ __forceinline__ void wy_inverse(const float* A, float* X, float* R, int tid) {
   // ---- X = (I + A)^-1 (unit lower triangular) in 16 x 16 blocks.
   // Diagonal blocks by forward substitution, one column per thread (the other
@@ -294,7 +295,7 @@ __device__ __forceinline__ void wy_inverse(const float* A, float* X, float* R, i
     for (int r = 0; r < 16; ++r) X[(o + r) * LDX + o + c] = x[r];
   } else {
     // blocks (bi, bj) with bi < bj: 6 blocks of 256
-    for (int e = tid - 64; e < 6 * 256; e += kGdnThreads - 64) {
+    for (int e = tid - 64; e < 6 * 256; e += NT - 64) {
       const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
       const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
       const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
@@ -307,14 +308,14 @@ __device__ __forceinline__ void wy_inverse(const float* A, float* X, float* R, i
   // (the rows of block i of (I + A) X = I), R_ij kept in R.
   for (int d = 1; d < 4; ++d) {
     const int nb = 4 - d;  // blocks (j + d, j), j = 0 .. nb - 1
-    for (int e = tid; e < nb * 256; e += kGdnThreads) {
+    for (int e = tid; e < nb * 256; e += NT) {
       const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
       float acc = 0.f;
       for (int k = 16 * j; k < 16 * i; ++k) acc = fmaf(A[(16 * i + r) * kSF + k], X[k * LDX + 16 * j + c], acc);
       R[e] = acc;
     }
     __syncthreads();
-    for (int e = tid; e < nb * 256; e += kGdnThreads) {
+    for (int e = tid; e < nb * 256; e += NT) {
       const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
       float acc = 0.f;
 #pragma unroll
@@ -905,10 +906,10 @@ __device__ __forceinline__ float quad_sum(float x) {
   return x;
 }
 
-__global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParams p) {
+__global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   LocalHSmem& sm = *reinterpret_cast<LocalHSmem*>(smem_raw);
-  constexpr int nt = kStateThreads;
+  constexpr int nt = kLocalThreads;
   grid_dependency_wait();
   const int c = blockIdx.x, h = blockIdx.y;
   // (both loads in flight at once: the table entry is in bounds for every
@@ -946,13 +947,13 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
   __syncthreads();
   const float g_last = sm.gam[len - 1];
   const int r0 = 16 * (warp & 3);
-  // ---- dO E^T and Q K^T (rows [r0, +16), columns [c0, +32)): DG, and the
+  // ---- dO E^T and Q K^T (rows [r0, +16), columns [c0, +16)): DG, and the
   // DG o (Q K^T) row and column sums of dgam.
   {
-    const int c0 = 32 * (warp >> 2);
-    float s1[4][4], s2[4][4];
+    const int c0 = 16 * (warp >> 2);
+    float s1[2][4], s2[2][4];
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) s1[n][e] = s2[n][e] = 0.f;
 #pragma unroll
@@ -961,7 +962,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
       ldsm_x4(ad, frag_a(sdO, kS128, r0, 16 * kk, lane));
       ldsm_x4(aq, frag_a(sQ, kS128, r0, 16 * kk, lane));
 #pragma unroll
-      for (int np = 0; np < 2; ++np) {
+      for (int np = 0; np < 1; ++np) {
         uint32_t be[4], bk[4];
         ldsm_x4(be, frag_bt(sE, kS128, c0 + 16 * np, 16 * kk, lane));
         ldsm_x4(bk, frag_bt(sK, kS128, c0 + 16 * np, 16 * kk, lane));
@@ -972,9 +973,9 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
       }
     }
     float rsum[2] = {0.f, 0.f};
-    float csum[4][2];
+    float csum[2][2];
 #pragma unroll
-    for (int n = 0; n < 4; ++n) {
+    for (int n = 0; n < 2; ++n) {
       csum[n][0] = csum[n][1] = 0.f;
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
@@ -996,7 +997,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
       if ((lane & 3) == 0) atomicAdd(&sm.dgs[r0 + (lane >> 2) + 8 * hr], x);
     }
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         float x = csum[n][e];
@@ -1007,23 +1008,23 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
       }
   }
   __syncthreads();
-  // ---- 64 x 128 products: rows [r0, +16), columns [d0, +64)
-  const int d0 = 64 * (warp >> 2);
-  float acc[8][4], acc2[8][4];
-  auto zero = [&](float (&x)[8][4]) {
+  // ---- 64 x 128 products: rows [r0, +16), columns [d0, +32)
+  const int d0 = 32 * (warp >> 2);
+  float acc[4][4], acc2[4][4];
+  auto zero = [&](float (&x)[4][4]) {
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) x[n][e] = 0.f;
   };
   // acc += A (rows r0, K = 128 over `ld`-strided a) * Bt^T, Bt stored [n][k] (the H0^T / dH1^T forms)
-  auto mm_abt = [&](float (&x)[8][4], uint32_t sa, uint32_t sbt) {
+  auto mm_abt = [&](float (&x)[4][4], uint32_t sa, uint32_t sbt) {
 #pragma unroll
     for (int kk = 0; kk < kD / 16; ++kk) {
       uint32_t a[4];
       ldsm_x4(a, frag_a(sa, kS128, r0, 16 * kk, lane));
 #pragma unroll
-      for (int np = 0; np < 4; ++np) {
+      for (int np = 0; np < 2; ++np) {
         uint32_t b[4];
         ldsm_x4(b, frag_bt(sbt, kS128, d0 + 16 * np, 16 * kk, lane));
         mma_bf16(x[2 * np], a, b[0], b[1]);
@@ -1032,13 +1033,13 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
     }
   };
   // acc += A (rows r0, K = 128) * B, B stored [k][n] (128 rows)
-  auto mm_ab = [&](float (&x)[8][4], uint32_t sa, uint32_t sb) {
+  auto mm_ab = [&](float (&x)[4][4], uint32_t sa, uint32_t sb) {
 #pragma unroll
     for (int kk = 0; kk < kD / 16; ++kk) {
       uint32_t a[4];
       ldsm_x4(a, frag_a(sa, kS128, r0, 16 * kk, lane));
 #pragma unroll
-      for (int np = 0; np < 4; ++np) {
+      for (int np = 0; np < 2; ++np) {
         uint32_t b[4];
         ldsm_x4_t(b, frag_b(sb, kS128, 16 * kk, d0 + 16 * np, lane));
         mma_bf16(x[2 * np], a, b[0], b[1]);
@@ -1055,7 +1056,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
     uint32_t a[4];
     ldsm_x4(a, frag_a(sDG, kS64, r0, 16 * kk, lane));
 #pragma unroll
-    for (int np = 0; np < 4; ++np) {
+    for (int np = 0; np < 2; ++np) {
       uint32_t b[4];
       ldsm_x4_t(b, frag_b(sK, kS128, 16 * kk, d0 + 16 * np, lane));
       mma_bf16(acc2[2 * np], a, b[0], b[1]);
@@ -1069,7 +1070,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
       const float m = p.scale * __expf(sm.gam[i]);
       __nv_bfloat16* row = p.dq + ((size_t)(t0 + i) * p.nh + h) * kD + d0;
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
+      for (int n = 0; n < 4; ++n) {
         const int j = 8 * n + 2 * (lane & 3);
         *reinterpret_cast<uint32_t*>(row + j) =
             pack2(m * acc[n][2 * hr] + acc2[n][2 * hr], m * acc[n][2 * hr + 1] + acc2[n][2 * hr + 1]);
@@ -1085,7 +1086,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
     if (i < len) {
       __nv_bfloat16* row = p.dW + ((size_t)(t0 + i) * p.nh + h) * kD + d0;
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
+      for (int n = 0; n < 4; ++n) {
         const int j = 8 * n + 2 * (lane & 3);
         *reinterpret_cast<uint32_t*>(row + j) = pack2(-acc[n][2 * hr], -acc[n][2 * hr + 1]);
       }
@@ -1100,7 +1101,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
     uint32_t a[4];
     ldsm_x4_t(a, frag_bt(sDG, kS64, 16 * kk, r0, lane));  // DG^T: DG stored [i][j]
 #pragma unroll
-    for (int np = 0; np < 4; ++np) {
+    for (int np = 0; np < 2; ++np) {
       uint32_t b[4];
       ldsm_x4_t(b, frag_b(sQ, kS128, 16 * kk, d0 + 16 * np, lane));
       mma_bf16(acc2[2 * np], a, b[0], b[1]);
@@ -1114,7 +1115,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
       const float w = __expf(g_last - sm.gam[i]);
       float* row = p.dKa + ((size_t)(t0 + i) * p.nh + h) * kD + d0;
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
+      for (int n = 0; n < 4; ++n) {
         const int j = 8 * n + 2 * (lane & 3);
         *reinterpret_cast<float2*>(row + j) =
             make_float2(w * acc[n][2 * hr] + acc2[n][2 * hr], w * acc[n][2 * hr + 1] + acc2[n][2 * hr + 1]);
@@ -1129,7 +1130,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_h_kernel(GdnParam
   {
     float rq[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int i = r0 + (lane >> 2) + 8 * hr;
@@ -1197,10 +1198,10 @@ struct LocalWySmem {
 };
 static_assert(sizeof(LocalWySmem) <= 227 * 1024, "fits one SM");
 
-__global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnParams p) {
+__global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_wy_kernel(GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   LocalWySmem& sm = *reinterpret_cast<LocalWySmem*>(smem_raw);
-  constexpr int nt = kStateThreads;
+  constexpr int nt = kLocalThreads;
   grid_dependency_wait();
   const int c = blockIdx.x, h = blockIdx.y;
   // (both loads in flight at once: the table entry is in bounds for every
@@ -1231,10 +1232,10 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
   const int r0 = 16 * (warp & 3);
   // ---- K K^T (rows [r0, +16), columns [c0, +32)): A and KK
   {
-    const int c0 = 32 * (warp >> 2);
-    float s[4][4];
+    const int c0 = 16 * (warp >> 2);
+    float s[2][4];
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
 #pragma unroll
@@ -1242,7 +1243,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
       uint32_t a[4];
       ldsm_x4(a, frag_a(sK, kS128, r0, 16 * kk, lane));
 #pragma unroll
-      for (int np = 0; np < 2; ++np) {
+      for (int np = 0; np < 1; ++np) {
         uint32_t b[4];
         ldsm_x4(b, frag_bt(sK, kS128, c0 + 16 * np, 16 * kk, lane));
         mma_bf16(s[2 * np], a, b[0], b[1]);
@@ -1250,7 +1251,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
       }
     }
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
@@ -1263,7 +1264,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
         }
   }
   __syncthreads();
-  wy_inverse<kS4>(sm.A, sm.X, sm.R, tid);
+  wy_inverse<kS4, kLocalThreads>(sm.A, sm.X, sm.R, tid);
   // ---- Xb = bf16 X, XT; dX = (dE V^T) diag(beta) + (dW K^T) diag(beta e^gamma)
   for (int e = tid; e < kC * kC / 2; e += nt) {
     const int i = e >> 5, j = (e & 31) * 2;
@@ -1273,10 +1274,10 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
     sm.XT[(j + 1) * kS4 + i] = x1;
   }
   {
-    const int c0 = 32 * (warp >> 2);
-    float pv[4][4], pk[4][4];
+    const int c0 = 16 * (warp >> 2);
+    float pv[2][4], pk[2][4];
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) pv[n][e] = pk[n][e] = 0.f;
 #pragma unroll
@@ -1285,7 +1286,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
       ldsm_x4(ae, frag_a(sdE, kS128, r0, 16 * kk, lane));
       ldsm_x4(aw, frag_a(sdW, kS128, r0, 16 * kk, lane));
 #pragma unroll
-      for (int np = 0; np < 2; ++np) {
+      for (int np = 0; np < 1; ++np) {
         uint32_t bv[4], bk[4];
         ldsm_x4(bv, frag_bt(sV, kS128, c0 + 16 * np, 16 * kk, lane));
         ldsm_x4(bk, frag_bt(sK, kS128, c0 + 16 * np, 16 * kk, lane));
@@ -1296,7 +1297,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
       }
     }
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
@@ -1309,45 +1310,45 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
   }
   __syncthreads();
   // ---- Y = dX X^T, then dA = -X^T Y, strictly lower; fp32, each thread a
-  // 4 x 4 block of outputs (16 independent sums, two float4 loads per step;
-  // the zeros of the triangular X make the full sums over m exact).
+  // 2 x 4 block of outputs (8 independent sums, a float2 and a float4 load
+  // per step; the zeros of the triangular X make the full sums over m exact).
   {
-    const int i0 = 4 * (tid >> 4), j0 = 4 * (tid & 15);
-    float y[4][4];
+    const int i0 = 2 * (tid >> 4), j0 = 4 * (tid & 15);
+    float y[2][4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < 2; ++a)
 #pragma unroll
       for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
 #pragma unroll 4
     for (int m = 0; m < kC; ++m) {
-      const float4 xa = *reinterpret_cast<const float4*>(&sm.dXT[m * kS4 + i0]);  // dX[i0 + a][m]
+      const float2 xa = *reinterpret_cast<const float2*>(&sm.dXT[m * kS4 + i0]);  // dX[i0 + a][m]
       const float4 xb = *reinterpret_cast<const float4*>(&sm.XT[m * kS4 + j0]);   // X[j0 + b][m]
-      const float av[4] = {xa.x, xa.y, xa.z, xa.w}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
+      const float av[2] = {xa.x, xa.y}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 2; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < 2; ++a)
       *reinterpret_cast<float4*>(&sm.Y[(i0 + a) * kS4 + j0]) = make_float4(y[a][0], y[a][1], y[a][2], y[a][3]);
     __syncthreads();
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < 2; ++a)
 #pragma unroll
       for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
 #pragma unroll 4
     for (int m = 0; m < kC; ++m) {
-      const float4 xa = *reinterpret_cast<const float4*>(&sm.X[m * kS4 + i0]);  // X[m][i0 + a]
+      const float2 xa = *reinterpret_cast<const float2*>(&sm.X[m * kS4 + i0]);  // X[m][i0 + a]
       const float4 xb = *reinterpret_cast<const float4*>(&sm.Y[m * kS4 + j0]);  // Y[m][j0 + b]
-      const float av[4] = {xa.x, xa.y, xa.z, xa.w}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
+      const float av[2] = {xa.x, xa.y}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 2; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < 2; ++a)
 #pragma unroll
       for (int b = 0; b < 4; ++b) sm.A[(i0 + a) * kSF + j0 + b] = j0 + b < i0 + a ? -y[a][b] : 0.f;
   }
@@ -1385,11 +1386,11 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
     sm.dgs[tid] -= cg;
   }
   __syncthreads();
-  // ---- 64 x 128 products, rows [r0, +16) x columns [d0, +64)
-  const int d0 = 64 * (warp >> 2);
-  float cv[8][4], ck[8][4];
+  // ---- 64 x 128 products, rows [r0, +16) x columns [d0, +32)
+  const int d0 = 32 * (warp >> 2);
+  float cv[4][4], ck[4][4];
 #pragma unroll
-  for (int n = 0; n < 8; ++n)
+  for (int n = 0; n < 4; ++n)
 #pragma unroll
     for (int e = 0; e < 4; ++e) cv[n][e] = ck[n][e] = 0.f;
   // dVb = X^T dE, dKb = X^T dW
@@ -1398,7 +1399,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
     uint32_t a[4];
     ldsm_x4_t(a, frag_bt(sXb, kS64, 16 * kk, r0, lane));  // X^T: X stored [i][j]
 #pragma unroll
-    for (int np = 0; np < 4; ++np) {
+    for (int np = 0; np < 2; ++np) {
       uint32_t be[4], bw[4];
       ldsm_x4_t(be, frag_b(sdE, kS128, 16 * kk, d0 + 16 * np, lane));
       ldsm_x4_t(bw, frag_b(sdW, kS128, 16 * kk, d0 + 16 * np, lane));
@@ -1417,7 +1418,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
       const float bi = sm.bet[i], be = bi * __expf(sm.gam[i]);
       __nv_bfloat16* row = p.dv + ((size_t)(t0 + i) * p.nh + h) * kD + d0;
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
+      for (int n = 0; n < 4; ++n) {
         const int j = 8 * n + 2 * (lane & 3);
         const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.V[i * kS128 + d0 + j]));
         const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[i * kS128 + d0 + j]));
@@ -1446,7 +1447,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
     ldsm_x4(am, frag_a(sM, kS64, r0, 16 * kk, lane));
     ldsm_x4_t(at, frag_bt(sM, kS64, 16 * kk, r0, lane));  // M^T
 #pragma unroll
-    for (int np = 0; np < 4; ++np) {
+    for (int np = 0; np < 2; ++np) {
       uint32_t b[4];
       ldsm_x4_t(b, frag_b(sK, kS128, 16 * kk, d0 + 16 * np, lane));
       mma_bf16(ck[2 * np], am, b[0], b[1]);
@@ -1461,7 +1462,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_local_wy_kernel(GdnPara
     if (i < len) {
       const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + d0;
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
+      for (int n = 0; n < 4; ++n) {
         const int j = 8 * n + 2 * (lane & 3);
         const float2 a = *reinterpret_cast<const float2*>(p.dKa + off + j);
         *reinterpret_cast<uint32_t*>(p.dk + off + j) = pack2(ck[n][2 * hr] + a.x, ck[n][2 * hr + 1] + a.y);
@@ -1577,9 +1578,10 @@ cudaError_t launch_gdn_prep(const GdnParams& p, cudaStream_t s) {
 }
 
 template <typename Smem, typename... KArgs>
-cudaError_t launch_big(void (*kernel)(KArgs...), dim3 grid, cudaStream_t s, const GdnParams& p) {
+cudaError_t launch_big(void (*kernel)(KArgs...), dim3 grid, cudaStream_t s, const GdnParams& p,
+                       int threads = kStateThreads) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
-  if (e == cudaSuccess) e = launch_pdl(kernel, grid, dim3(kStateThreads), sizeof(Smem), s, p);
+  if (e == cudaSuccess) e = launch_pdl(kernel, grid, dim3(threads), sizeof(Smem), s, p);
   return e;
 }
 
@@ -1651,8 +1653,8 @@ int gdn_varlen_bwd(const void* q, const void* k, const void* v, const float* g, 
   cudaError_t e = launch_gdn_prep(p, s);
   if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<true>, seg_grid, s, p);
   if (e == cudaSuccess) e = launch_big<BwdStateSmem>(gdn_bwd_state_kernel, seg_grid, s, p);
-  if (e == cudaSuccess) e = launch_big<LocalHSmem>(gdn_bwd_local_h_kernel, chunk_grid, s, p);
-  if (e == cudaSuccess) e = launch_big<LocalWySmem>(gdn_bwd_local_wy_kernel, chunk_grid, s, p);
+  if (e == cudaSuccess) e = launch_big<LocalHSmem>(gdn_bwd_local_h_kernel, chunk_grid, s, p, kLocalThreads);
+  if (e == cudaSuccess) e = launch_big<LocalWySmem>(gdn_bwd_local_wy_kernel, chunk_grid, s, p, kLocalThreads);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
