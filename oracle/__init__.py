@@ -1,6 +1,6 @@
 """CPU float64 oracles (test infrastructure only): varlen GQA attention
-(attention.py) and the Gated DeltaNet recurrence over packed documents
-(gated_delta.py).
+(attention.py), and the Gated DeltaNet and Kimi Delta recurrences over packed
+documents (gated_delta.py, kimi_delta.py).
 
 Only tests, the smoke check and the benchmark's CPU-baseline leg import this
 package; the library never does.
