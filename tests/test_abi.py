@@ -24,7 +24,7 @@ def declared_functions():
     names = set()
     for h in HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names |= set(re.findall(r"\b((?:attn|gdn)_varlen_\w+)\s*\(", text))
+        names |= set(re.findall(r"\b((?:attn|gdn|kda)_varlen_\w+)\s*\(", text))
     return sorted(names)
 
 
@@ -32,7 +32,7 @@ def test_header_declares_the_calls():
     names = declared_functions()
     for required in ("attn_varlen_fwd", "attn_varlen_bwd", "attn_varlen_get_status", "attn_varlen_strerror",
                      "gdn_varlen_fwd", "gdn_varlen_workspace_bytes", "gdn_varlen_bwd",
-                     "gdn_varlen_bwd_workspace_bytes"):
+                     "gdn_varlen_bwd_workspace_bytes", "kda_varlen_fwd", "kda_varlen_workspace_bytes"):
         assert required in names
 
 

@@ -1,0 +1,94 @@
+"""Kimi Delta attention on the GPU against the float64 oracle, through the C
+ABI (include/kda_varlen.h).
+
+Tolerance: relative L2 error <= 1.5e-2 over the whole tensor and over every
+segment of at least 16 tokens (shorter ones: RMS error <= the bound x the
+larger of their RMS and the tensor's).  On the way to o the kernels round to
+bf16 the per-block scaled copies of K and Q that carry the per-channel decay
+inside the products, the WY factors W and U, the masked q.k block, K o e^gamma,
+Q o e^gamma, K o e^(gamma_last - gamma), the state copy used as an operand,
+the pseudo-values E and o itself: about nine roundings of relative RMS
+2^-8 / sqrt(3) = 2.3e-3, sqrt(9) x 2.3e-3 = 6.9e-3 together; the bound is
+about twice that.
+"""
+import numpy as np
+import pytest
+
+from tests.helpers import assert_per_segment, rel_l2
+from varlen_sliding_window_gb300 import synth
+
+TOL_O = 1.5e-2
+WL = synth.kda_workloads()
+
+
+def _to_dev(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16).cuda()
+
+
+def _run(inp, scale, cu=None):
+    import torch
+    from varlen_sliding_window_gb300 import binding
+    cu = inp.cu_seqlens if cu is None else cu
+    q, k, v = (_to_dev(b) for b in (inp.q_bits, inp.k_bits, inp.v_bits))
+    g = torch.from_numpy(inp.g).cuda()
+    beta = torch.from_numpy(inp.beta).cuda()
+    cu_t = torch.from_numpy(np.asarray(cu, dtype=np.int32)).cuda()
+    T, nh, _ = q.shape
+    o = torch.full_like(q, float("nan"))
+    ws = torch.empty(binding.kda_varlen_workspace_bytes(T, nh, len(cu) - 1), dtype=torch.uint8, device="cuda")
+    binding.kda_varlen_fwd(q, k, v, g, beta, cu_t, scale, o, ws)
+    torch.cuda.synchronize()
+    assert binding.attn_varlen_get_status() == 0
+    return o
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["kda_tiny", "kda_ragged", "kda_ctx512", "kda_ctx4096"])
+def test_forward_matches_oracle(name):
+    from oracle import kimi_delta
+    w = WL[name]
+    inp = w.inputs()
+    got = _run(inp, w.scale).double().cpu().numpy()
+    ref = kimi_delta.forward(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens, w.scale)
+    assert np.isfinite(got).all()
+    err = rel_l2(got, ref)
+    print(f"{name}: rel L2 {err:.3e}")
+    assert err <= TOL_O, err
+    assert_per_segment(got, ref, inp.cu_seqlens, TOL_O, "o")
+
+
+@pytest.mark.gpu
+def test_equal_channels_match_the_gated_deltanet_kernels():
+    # With the same gate on every channel the layer is Gated DeltaNet: the two
+    # libraries' paths (different roundings) agree to the tolerance.
+    import torch
+    from varlen_sliding_window_gb300 import binding
+    w = synth.gdn_workloads()["gdn_ragged"]
+    inp = w.inputs()
+    gk = np.ascontiguousarray(np.repeat(inp.g[:, :, None], w.d, axis=2))
+    q, k, v = (_to_dev(b) for b in (inp.q_bits, inp.k_bits, inp.v_bits))
+    cu = torch.from_numpy(inp.cu_seqlens).cuda()
+    T, nh = w.total, w.nh
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(max(binding.kda_varlen_workspace_bytes(T, nh, len(inp.cu_seqlens) - 1),
+                         binding.gdn_varlen_workspace_bytes(T, nh, len(inp.cu_seqlens) - 1)), dtype=torch.uint8,
+                     device="cuda")
+    binding.kda_varlen_fwd(q, k, v, torch.from_numpy(gk).cuda(), torch.from_numpy(inp.beta).cuda(), cu, w.scale, o1,
+                           ws)
+    binding.gdn_varlen_fwd(q, k, v, torch.from_numpy(inp.g).cuda(), torch.from_numpy(inp.beta).cuda(), cu, w.scale,
+                           o2, ws)
+    torch.cuda.synchronize()
+    assert rel_l2(o1.double().cpu().numpy(), o2.double().cpu().numpy()) <= TOL_O
+
+
+@pytest.mark.gpu
+def test_empty_segments_and_repeats_are_bit_identical():
+    import torch
+    w = WL["kda_ragged"]
+    inp = w.inputs()
+    a = _run(inp, w.scale)
+    assert torch.equal(a, _run(inp, w.scale))
+    cu = inp.cu_seqlens
+    padded = np.concatenate([[0], cu[:4], cu[3:7], cu[6:], [cu[-1]] * 5]).astype(np.int32)
+    assert torch.equal(a, _run(inp, w.scale, cu=padded))

@@ -1,7 +1,8 @@
 """Document-masked (varlen) causal grouped-query attention for GB300 (sm_103a).
 
 The compute lives in the C-ABI library libvsw_attn.so (include/attn_varlen.h,
-and include/gdn_varlen.h for the Gated DeltaNet local layer);
+include/gdn_varlen.h and include/kda_varlen.h for the Gated DeltaNet and Kimi
+Delta local layers);
 ``binding`` marshals torch CUDA tensors into it.  ``synth`` generates the
 seeded packed-document workloads.  ``layer`` wraps one attention layer
 (projections, the library's attention on strided views, a small loss, and the
@@ -15,6 +16,7 @@ _BINDING_NAMES = {
     "attn_varlen_bwd_dkdv", "attn_varlen_bwd_dq", "attn_varlen_bwd_noalloc", "attn_varlen_fwd_strided",
     "attn_varlen_bwd_strided", "attn_varlen_set_workspace", "attn_varlen_workspace_bytes", "load_library",
     "AttnError", "gdn_varlen_fwd", "gdn_varlen_workspace_bytes", "gdn_varlen_bwd", "gdn_varlen_bwd_workspace_bytes",
+    "kda_varlen_fwd", "kda_varlen_workspace_bytes",
 }
 
 

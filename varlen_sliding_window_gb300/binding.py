@@ -75,6 +75,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gdn_varlen_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_varlen_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp, vp, sz, i64, i32, i32, i32, vp]
     lib.gdn_varlen_bwd.restype = ctypes.c_int
+    lib.kda_varlen_workspace_bytes.argtypes = [i64, i32, i32]
+    lib.kda_varlen_workspace_bytes.restype = ctypes.c_size_t
+    lib.kda_varlen_fwd.argtypes = lib.gdn_varlen_fwd.argtypes
+    lib.kda_varlen_fwd.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -337,3 +341,24 @@ def gdn_varlen_bwd(q, k, v, g, beta, d_o, cu_seqlens, scale: float, dq, dk, dv, 
                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(workspace),
                             int(workspace.numel()), total, nh, d, nseg, _stream_handle(stream))
     _check(rc, "gdn_varlen_bwd")
+
+
+def kda_varlen_workspace_bytes(total: int, num_heads: int, num_segments: int) -> int:
+    """Device workspace bytes kda_varlen_fwd needs (include/kda_varlen.h)."""
+    return int(load_library().kda_varlen_workspace_bytes(int(total), int(num_heads), int(num_segments)))
+
+
+def kda_varlen_fwd(q, k, v, g, beta, cu_seqlens, scale: float, o, workspace, stream=None) -> None:
+    """Kimi Delta forward over packed documents.  q, k, v, o: dense bf16
+    [T, H, 128]; g: dense float32 [T, H, 128] (log decay per key channel);
+    beta: dense float32 [T, H]; workspace: uint8 CUDA tensor of at least
+    kda_varlen_workspace_bytes(T, H, num_segments) bytes."""
+    _require_dense("kda_varlen_fwd", q, k, v, o)
+    if not (g.is_contiguous() and beta.is_contiguous()):
+        raise ValueError("g and beta must be dense float32 tensors")
+    lib = load_library()
+    total, nh, d = (int(x) for x in q.shape)
+    nseg = int(cu_seqlens.numel()) - 1
+    rc = lib.kda_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), float(scale), _ptr(o),
+                            _ptr(workspace), int(workspace.numel()), total, nh, d, nseg, _stream_handle(stream))
+    _check(rc, "kda_varlen_fwd")

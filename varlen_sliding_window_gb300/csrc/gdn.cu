@@ -52,6 +52,7 @@ constexpr int kS128 = 136;     // smem row stride (elements) of 128-wide bf16 ti
 constexpr int kS64 = 72;       // 64-wide: 144 B
 constexpr int kS32 = 40;       // 32-wide: 80 B
 constexpr int kSF = 65;        // fp32 64 x 64 tiles
+constexpr int kG = 132;        // fp32 64 x 128 tiles (gates, per channel): 16-byte rows
 constexpr int kS4 = 68;        // fp32 64 x 64 tiles read as float4 rows
 
 struct GdnParams {
@@ -72,6 +73,12 @@ struct GdnParams {
   __nv_bfloat16* U;     // [T, H, 128]
   __nv_bfloat16* Aqk;   // [max_chunks, H, 64, 64]: lower(Q K^T) o Gamma
   float* gam;           // [H, T]: gamma (running log decay within the chunk)
+  // Kimi Delta (a decay per key channel; g is then [T, H, 128]): the state
+  // pass reads Q o e^gamma and K o e^(gamma_last - gamma) instead of q and k,
+  // and the chunk's total decay e^gamma_last per channel
+  __nv_bfloat16* QB;    // [T, H, 128]
+  __nv_bfloat16* KC;    // [T, H, 128]
+  float* Bc;            // [max_chunks, H, 128]
   // backward only
   const __nv_bfloat16* dO;  // [T, H, 128]
   __nv_bfloat16* dq;        // [T, H, 128]
@@ -150,6 +157,11 @@ __device__ __forceinline__ void load_rows128(uint32_t dst, const __nv_bfloat16* 
     const __nv_bfloat16* s = src + ((size_t)(t0 + (ok ? r : 0)) * nh + h) * kD + c;
     cp_async16(dst + 2u * (uint32_t)(r * kS128 + c), s, ok);
   }
+}
+
+// Rows of a chunk that lie inside [0, T) (all of them for a valid boundary list).
+__device__ __forceinline__ int chunk_len(const int4& ch, int total) {
+  return (ch.x < 0 || ch.x >= total) ? 0 : min(ch.y, total - ch.x);
 }
 
 // ============================================================== plan
@@ -480,6 +492,214 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_prep_kernel(GdnParams p) {
   if (tid < kC && tid < len) p.gam[(size_t)h * p.total + t0 + tid] = sm.gam[tid];
 }
 
+// ============================================================== prep, a decay per channel (Kimi Delta)
+// As gdn_prep_kernel, with gamma a running sum per key channel (B = e^gamma):
+//     A_ij   = beta_i sum_c k_ic k_jc e^(gamma_ic - gamma_jc)   (j < i)
+//     Aqk_ij =        sum_c q_ic k_jc e^(gamma_ic - gamma_jc)   (j <= i)
+//     W = X diag(beta) (K o B),  U = X diag(beta) V,  X = (I + A)^-1
+// and, for the state pass, QB = Q o B, KC = K o e^(gamma_last - gamma) and
+// e^gamma_last.  The exponent gamma_i - gamma_j is split at a reference token
+// r = the first row of i's 16-row block:
+//     e^(gamma_i - gamma_j) = e^(gamma_i - gamma_r) e^(gamma_r - gamma_j),
+// so the first factor is at most 1 and the second is at most 1 for j < r and
+// at most the decay of 15 tokens (j in i's block); each block of 16 rows of A
+// is then one matrix product of scaled operands.  (The decay over 15 tokens
+// must stay within float range, e^88: per-token log decays above -5.8.)
+struct KdaPrepSmem {
+  __nv_bfloat16 K[kC * kS128];
+  __nv_bfloat16 Q[kC * kS128];
+  __nv_bfloat16 V[kC * kS128];
+  float G[kC * kG];                 // g, then gamma (running sum over the chunk), per channel
+  __nv_bfloat16 KB[kC * kS128];     // K o e^(gamma - gamma_r) (row block reference); later K o e^gamma
+  __nv_bfloat16 QB[kC * kS128];     // Q o e^(gamma - gamma_r)
+  __nv_bfloat16 KI[160 * kS128];    // per row block I: K_j o e^(gamma_rI - gamma_j), j < 16 (I + 1)
+  float A[kC * kSF];
+  float X[kC * kSF];
+  float R[3 * 256];
+  __nv_bfloat16 T2[kC * kS64];      // X diag(beta)
+  float bet[kC];
+};
+static_assert(sizeof(KdaPrepSmem) <= 227 * 1024, "fits one SM");
+
+// Row offset of block I's scaled K copy inside KI (blocks of 16, 32, 48, 64 rows).
+__device__ __forceinline__ int ki_row0(int I) { return 8 * I * (I + 1); }
+
+__global__ void __launch_bounds__(kGdnThreads) kda_prep_kernel(GdnParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  KdaPrepSmem& sm = *reinterpret_cast<KdaPrepSmem*>(smem_raw);
+  constexpr int nt = kGdnThreads;
+  grid_dependency_wait();
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int n_chunks = __ldcg(p.hdr);
+  const int4 ch = p.chunks[c];
+  if (c >= n_chunks) return;
+  const int len = chunk_len(ch, p.total);
+  if (len <= 0) return;  // only with a boundary list that breaks its rules
+  const int t0 = ch.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t sK = smem_u32(sm.K), sQ = smem_u32(sm.Q), sV = smem_u32(sm.V), sKB = smem_u32(sm.KB),
+                 sQB = smem_u32(sm.QB), sKI = smem_u32(sm.KI);
+  load_rows128(sK, p.k, t0, len, h, p.nh, tid, nt);
+  load_rows128(sQ, p.q, t0, len, h, p.nh, tid, nt);
+  load_rows128(sV, p.v, t0, len, h, p.nh, tid, nt);
+  for (int e = tid; e < kC * 32; e += nt) {  // g rows, 32 pieces of 16 bytes each
+    const int r = e >> 5, cc = (e & 31) * 4;
+    const bool ok = r < len;
+    cp_async16(smem_u32(&sm.G[r * kG + cc]), p.g + ((size_t)(t0 + (ok ? r : 0)) * p.nh + h) * kD + cc, ok);
+  }
+  cp_async_commit();
+  if (tid < kC) sm.bet[tid] = tid < len ? p.beta[(size_t)(t0 + tid) * p.nh + h] : 0.f;
+  cp_async_wait<0>();
+  __syncthreads();
+  // gamma per channel (rows past the chunk add zeros)
+  if (tid < kD) {
+    float acc = 0.f;
+    for (int i = 0; i < kC; ++i) {
+      acc += sm.G[i * kG + tid];
+      sm.G[i * kG + tid] = acc;
+    }
+  }
+  __syncthreads();
+  // scaled operands: KB, QB (reference = the row's block start) and the KI copies
+  for (int e = tid; e < kC * kD / 2; e += nt) {
+    const int i = e >> 6, cc = (e & 63) * 2;
+    const int r = i & ~15;
+    const float f0 = __expf(sm.G[i * kG + cc] - sm.G[r * kG + cc]);
+    const float f1 = __expf(sm.G[i * kG + cc + 1] - sm.G[r * kG + cc + 1]);
+    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[i * kS128 + cc]));
+    const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.Q[i * kS128 + cc]));
+    *reinterpret_cast<uint32_t*>(&sm.KB[i * kS128 + cc]) = pack2(kv.x * f0, kv.y * f1);
+    *reinterpret_cast<uint32_t*>(&sm.QB[i * kS128 + cc]) = pack2(qv.x * f0, qv.y * f1);
+  }
+  for (int e = tid; e < 160 * kD / 2; e += nt) {
+    const int row = e >> 6, cc = (e & 63) * 2;
+    const int I = row < 16 ? 0 : (row < 48 ? 1 : (row < 96 ? 2 : 3));
+    const int j = row - ki_row0(I), r = 16 * I;
+    const float f0 = __expf(sm.G[r * kG + cc] - sm.G[j * kG + cc]);
+    const float f1 = __expf(sm.G[r * kG + cc + 1] - sm.G[j * kG + cc + 1]);
+    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[j * kS128 + cc]));
+    *reinterpret_cast<uint32_t*>(&sm.KI[row * kS128 + cc]) = pack2(kv.x * f0, kv.y * f1);
+  }
+  __syncthreads();
+  // ---- the 10 blocks (I, J <= I) of 16 x 16: A and Aqk; warp w takes blocks w and w + 8
+  __nv_bfloat16* aqk = p.Aqk + ((size_t)c * p.nh + h) * (kC * kC);
+  for (int bl = warp; bl < 10; bl += 8) {
+    const int I = bl < 1 ? 0 : (bl < 3 ? 1 : (bl < 6 ? 2 : 3));
+    const int J = bl - I * (I + 1) / 2;
+    float sa[2][4], sq[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sa[n][e] = sq[n][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      uint32_t ak[4], aq[4], b[4];
+      ldsm_x4(ak, frag_a(sKB, kS128, 16 * I, 16 * kk, lane));
+      ldsm_x4(aq, frag_a(sQB, kS128, 16 * I, 16 * kk, lane));
+      ldsm_x4(b, frag_bt(sKI, kS128, ki_row0(I) + 16 * J, 16 * kk, lane));
+      mma_bf16(sa[0], ak, b[0], b[1]);
+      mma_bf16(sa[1], ak, b[2], b[3]);
+      mma_bf16(sq[0], aq, b[0], b[1]);
+      mma_bf16(sq[1], aq, b[2], b[3]);
+    }
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = 16 * I + (lane >> 2) + 8 * hr;
+        const int j = 16 * J + 8 * n + 2 * (lane & 3);
+        const float bi = sm.bet[i];
+        sm.A[i * kSF + j] = j < i ? bi * sa[n][2 * hr] : 0.f;
+        sm.A[i * kSF + j + 1] = j + 1 < i ? bi * sa[n][2 * hr + 1] : 0.f;
+        *reinterpret_cast<uint32_t*>(aqk + i * kC + j) =
+            pack2(j <= i ? sq[n][2 * hr] : 0.f, j + 1 <= i ? sq[n][2 * hr + 1] : 0.f);
+      }
+  }
+  // blocks above the diagonal: zero
+  for (int e = tid; e < 6 * 256; e += nt) {
+    const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+    const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+    const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+    const int i = 16 * bi + r, j = 16 * bj + cc;
+    sm.A[i * kSF + j] = 0.f;
+    aqk[i * kC + j] = __float2bfloat16_rn(0.f);
+  }
+  __syncthreads();
+  wy_inverse(sm.A, sm.X, sm.R, tid);
+  // ---- T2 = X diag(beta); KB <- K o e^gamma; QB, KC, e^gamma_last to the workspace
+  for (int e = tid; e < kC * kC / 2; e += nt) {
+    const int i = e >> 5, j = (e & 31) * 2;
+    *reinterpret_cast<uint32_t*>(&sm.T2[i * kS64 + j]) =
+        pack2(sm.X[i * kSF + j] * sm.bet[j], sm.X[i * kSF + j + 1] * sm.bet[j + 1]);
+  }
+  const int last = len - 1;
+  for (int e = tid; e < kC * kD / 8; e += nt) {
+    const int i = e >> 4, cc = (e & 15) * 8;
+    uint32_t kb[4], qb[4], kc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c2 = cc + 2 * u;
+      const float g0 = sm.G[i * kG + c2], g1 = sm.G[i * kG + c2 + 1];
+      const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[i * kS128 + c2]));
+      const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.Q[i * kS128 + c2]));
+      const float e0 = __expf(g0), e1 = __expf(g1);
+      kb[u] = pack2(kv.x * e0, kv.y * e1);
+      qb[u] = pack2(qv.x * e0, qv.y * e1);
+      kc[u] = pack2(kv.x * __expf(sm.G[last * kG + c2] - g0), kv.y * __expf(sm.G[last * kG + c2 + 1] - g1));
+    }
+    *reinterpret_cast<uint4*>(&sm.KB[i * kS128 + cc]) = make_uint4(kb[0], kb[1], kb[2], kb[3]);
+    if (i < len) {
+      const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + cc;
+      *reinterpret_cast<uint4*>(p.QB + off) = make_uint4(qb[0], qb[1], qb[2], qb[3]);
+      *reinterpret_cast<uint4*>(p.KC + off) = make_uint4(kc[0], kc[1], kc[2], kc[3]);
+    }
+  }
+  if (tid < kD) p.Bc[((size_t)c * p.nh + h) * kD + tid] = __expf(sm.G[last * kG + tid]);
+  __syncthreads();
+  // ---- W = T2 (K o e^gamma), U = T2 V: warp w rows [16 (w % 4), +16) x columns [64 (w / 4), +64)
+  const int r0 = 16 * (warp & 3), d0 = 64 * (warp >> 2);
+  float cw[8][4], cu[8][4];
+#pragma unroll
+  for (int n = 0; n < 8; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cw[n][e] = cu[n][e] = 0.f;
+  const uint32_t sT2 = smem_u32(sm.T2);
+#pragma unroll
+  for (int kk = 0; kk < kC / 16; ++kk) {
+    uint32_t a[4];
+    ldsm_x4(a, frag_a(sT2, kS64, r0, 16 * kk, lane));
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      uint32_t bk[4], bv[4];
+      ldsm_x4_t(bk, frag_b(sKB, kS128, 16 * kk, d0 + 16 * np, lane));
+      ldsm_x4_t(bv, frag_b(sV, kS128, 16 * kk, d0 + 16 * np, lane));
+      mma_bf16(cw[2 * np], a, bk[0], bk[1]);
+      mma_bf16(cw[2 * np + 1], a, bk[2], bk[3]);
+      mma_bf16(cu[2 * np], a, bv[0], bv[1]);
+      mma_bf16(cu[2 * np + 1], a, bv[2], bv[3]);
+    }
+  }
+  __syncthreads();  // K, V no longer read: stage W in K's place, U in V's
+#pragma unroll
+  for (int n = 0; n < 8; ++n)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const int j = d0 + 8 * n + 2 * (lane & 3);
+      *reinterpret_cast<uint32_t*>(&sm.K[i * kS128 + j]) = pack2(cw[n][2 * hr], cw[n][2 * hr + 1]);
+      *reinterpret_cast<uint32_t*>(&sm.V[i * kS128 + j]) = pack2(cu[n][2 * hr], cu[n][2 * hr + 1]);
+    }
+  __syncthreads();
+  for (int e = tid; e < kC * 16; e += nt) {
+    const int r = e >> 4, cc = (e & 15) * 8;
+    if (r < len) {
+      const size_t off = ((size_t)(t0 + r) * p.nh + h) * kD + cc;
+      *reinterpret_cast<uint4*>(p.W + off) = *reinterpret_cast<const uint4*>(&sm.K[r * kS128 + cc]);
+      *reinterpret_cast<uint4*>(p.U + off) = *reinterpret_cast<const uint4*>(&sm.V[r * kS128 + cc]);
+    }
+  }
+}
+
 // ============================================================== state + output
 struct StateStage {
   __nv_bfloat16 W[kC * kS128];
@@ -487,7 +707,7 @@ struct StateStage {
   __nv_bfloat16 Q[kC * kS128];
   __nv_bfloat16 U[kC * kS32];
   __nv_bfloat16 Aq[kC * kS64];
-  float gam[kC];
+  float gam[kD];  // gamma of the chunk's tokens; with a decay per channel, e^gamma_last per channel
 };
 constexpr int kStateStages = 3;  // chunk c + 2 loads while chunk c computes
 struct StateSmem {
@@ -499,18 +719,15 @@ struct StateSmem {
 
 static_assert(sizeof(StateSmem) <= 227 * 1024, "the state CTA's shared memory fits one SM");
 
-// Rows of a chunk that lie inside [0, T) (all of them for a valid boundary list).
-__device__ __forceinline__ int chunk_len(const int4& ch, int total) {
-  return (ch.x < 0 || ch.x >= total) ? 0 : min(ch.y, total - ch.x);
-}
 
+template <bool kChan>
 __device__ __forceinline__ void load_stage(StateStage& s, const GdnParams& p, int chunk, int h, int vb, int tid) {
   constexpr int nt = kStateThreads;
   const int4 ch = p.chunks[chunk];
   const int len = chunk_len(ch, p.total), t0 = len > 0 ? ch.x : 0;
   load_rows128(smem_u32(s.W), p.W, t0, len, h, p.nh, tid, nt);
-  load_rows128(smem_u32(s.K), p.k, t0, len, h, p.nh, tid, nt);
-  load_rows128(smem_u32(s.Q), p.q, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(s.K), kChan ? p.KC : p.k, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(s.Q), kChan ? p.QB : p.q, t0, len, h, p.nh, tid, nt);
   for (int e = tid; e < kC * 4; e += nt) {  // U columns [32 vb, 32 vb + 32)
     const int r = e >> 2, cc = (e & 3) * 8;
     const bool ok = r < len;
@@ -522,7 +739,9 @@ __device__ __forceinline__ void load_stage(StateStage& s, const GdnParams& p, in
     const int r = e >> 3, cc = (e & 7) * 8;
     cp_async16(smem_u32(&s.Aq[r * kS64 + cc]), aq + r * kC + cc, true);
   }
-  if (tid < kC) {
+  if (kChan) {
+    if (tid < kD / 4) cp_async16(smem_u32(&s.gam[4 * tid]), p.Bc + ((size_t)chunk * p.nh + h) * kD + 4 * tid, true);
+  } else if (tid < kC) {
     const bool ok = tid < len;
     cp_async4(smem_u32(&s.gam[tid]), p.gam + (size_t)h * p.total + t0 + (ok ? tid : 0), ok);
   }
@@ -533,7 +752,9 @@ __device__ __forceinline__ void load_stage(StateStage& s, const GdnParams& p, in
 // [16 w, +16) of the 128 x 32 state.
 // kStore (the backward's recomputation): no O; the bf16 state at every chunk
 // start and every chunk's E go to the workspace instead.
-template <bool kStore>
+// kChan (Kimi Delta): K and Q arrive pre-scaled (KC, QB), so E and O take no
+// per-token factor, and the state decays by e^gamma_last per channel (row).
+template <bool kStore, bool kChan>
 __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   StateSmem& sm = *reinterpret_cast<StateSmem*>(smem_raw);
@@ -555,15 +776,15 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) hreg[n][e] = 0.f;
   const uint32_t sH = smem_u32(sm.H), sE = smem_u32(sm.E), sE2 = smem_u32(sm.E2);
-  load_stage(sm.st[0], p, first, h, vb, tid);
+  load_stage<kChan>(sm.st[0], p, first, h, vb, tid);
   cp_async_commit();
-  if (nch > 1) load_stage(sm.st[1], p, first + 1, h, vb, tid);
+  if (nch > 1) load_stage<kChan>(sm.st[1], p, first + 1, h, vb, tid);
   cp_async_commit();
   for (int ci = 0; ci < nch; ++ci) {
     // Stage (ci + 2) % 3 was last read by chunk ci - 1 (done: the barrier at
     // the end of that chunk).  One group is committed per chunk, so at most
     // the two newest groups (chunks ci + 1, ci + 2) are still in flight.
-    if (ci + 2 < nch) load_stage(sm.st[(ci + 2) % kStateStages], p, first + ci + 2, h, vb, tid);
+    if (ci + 2 < nch) load_stage<kChan>(sm.st[(ci + 2) % kStateStages], p, first + ci + 2, h, vb, tid);
     cp_async_commit();
     cp_async_wait<2>();
     // H (bf16) for this chunk's products
@@ -592,7 +813,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
       continue;
     }
     const uint32_t sW = smem_u32(s.W), sK = smem_u32(s.K), sQ = smem_u32(s.Q), sAq = smem_u32(s.Aq);
-    const float g_last = s.gam[len - 1];
+    const float g_last = kChan ? 0.f : s.gam[len - 1];
     // ---- E = U - W H and Q H
     float ce[2][4], cq[2][4];
 #pragma unroll
@@ -620,7 +841,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
         const int j = n0 + 8 * n + 2 * (lane & 3);
         const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&s.U[i * kS32 + j]));
         const float e0 = u.x - ce[n][2 * hr], e1 = u.y - ce[n][2 * hr + 1];
-        const float w = i < len ? __expf(g_last - s.gam[i]) : 0.f;
+        const float w = i < len ? (kChan ? 1.f : __expf(g_last - s.gam[i])) : 0.f;
         *reinterpret_cast<uint32_t*>(&sm.E[i * kS32 + j]) = pack2(e0, e1);
         *reinterpret_cast<uint32_t*>(&sm.E2[i * kS32 + j]) = pack2(e0 * w, e1 * w);
       }
@@ -651,7 +872,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
     for (int hr = 0; hr < 2; ++hr) {
       const int i = r0 + (lane >> 2) + 8 * hr;
       if (i < len) {
-        const float eg = __expf(s.gam[i]);
+        const float eg = kChan ? 1.f : __expf(s.gam[i]);
         __nv_bfloat16* orow = p.o + ((size_t)(t0 + i) * p.nh + h) * kD + kDvb * vb + n0;
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
@@ -663,11 +884,16 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
     }
     }
     // ---- H = e^gamma_last H + K^T E2 (state rows [m0, +16); K^T read from K[token][d_k])
-    const float dl = __expf(g_last);
+    // rows m0 + lane / 4 (elements 0, 1) and + 8 (elements 2, 3)
+    const float dl0 = kChan ? s.gam[m0 + (lane >> 2)] : __expf(g_last);
+    const float dl1 = kChan ? s.gam[m0 + (lane >> 2) + 8] : dl0;
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) hreg[n][e] *= dl;
+    for (int n = 0; n < 4; ++n) {
+      hreg[n][0] *= dl0;
+      hreg[n][1] *= dl0;
+      hreg[n][2] *= dl1;
+      hreg[n][3] *= dl1;
+    }
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
       uint32_t a[4], b0[4], b1[4];
@@ -1490,8 +1716,9 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_wy_kernel(GdnPara
 
 // Workspace layout: offsets off[0..6] of the forward's regions (header,
 // chunk table, segment table, W, U, Aqk, gamma); with bwd, off[7..13] of the
-// backward's (H0, dH1, E, dE, dW, dKa, dgam).  Returns the total size.
-size_t gdn_workspace_layout(int64_t total, int nh, int nseg, size_t off[14], bool bwd) {
+// backward's (H0, dH1, E, dE, dW, dKa, dgam); with kda (a decay per channel),
+// off[14..16] (QB, KC, e^gamma_last).  Returns the total size.
+size_t gdn_workspace_layout(int64_t total, int nh, int nseg, size_t off[17], bool bwd, bool kda = false) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t max_chunks = (size_t)(total / kC) + (size_t)nseg + 1;
   const size_t tok = (size_t)total * nh * kD;  // elements of a [T, H, 128] tensor
@@ -1513,6 +1740,11 @@ size_t gdn_workspace_layout(int64_t total, int nh, int nseg, size_t off[14], boo
     off[12] = o; o += up(tok * 4);                           // dKa
     off[13] = o; o += up((size_t)total * nh * sizeof(float)); // dgam
   }
+  if (kda) {
+    off[14] = o; o += up(tok * 2);                           // QB
+    off[15] = o; o += up(tok * 2);                           // KC
+    off[16] = o; o += up(max_chunks * nh * kD * sizeof(float)); // e^gamma_last per chunk and channel
+  }
   return o;
 }
 
@@ -1520,7 +1752,7 @@ size_t gdn_workspace_layout(int64_t total, int nh, int nseg, size_t off[14], boo
 // block over the workspace.  Returns an ATTN_* code.
 int gdn_setup(GdnParams& p, const void* q, const void* k, const void* v, const float* g, const float* beta,
               const int32_t* cu_seqlens, float scale, void* workspace, size_t workspace_bytes, int64_t total,
-              int32_t num_heads, int32_t head_dim, int32_t num_segments, bool bwd) {
+              int32_t num_heads, int32_t head_dim, int32_t num_segments, bool bwd, bool kda = false) {
   if (!q || !k || !v || !g || !beta || !cu_seqlens || !workspace) return ATTN_ERR_NULL_POINTER;
   if (total < 0 || num_heads <= 0 || num_segments < 0 || (num_segments == 0 && total > 0)) return ATTN_ERR_SHAPE;
   if (head_dim != kD) return ATTN_ERR_HEAD_DIM;
@@ -1532,8 +1764,8 @@ int gdn_setup(GdnParams& p, const void* q, const void* k, const void* v, const f
   for (const void* x : ptrs)
     if (reinterpret_cast<uintptr_t>(x) & 15u) return ATTN_ERR_ALIGNMENT;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGNMENT;
-  size_t off[14];
-  if (workspace_bytes < gdn_workspace_layout(total, num_heads, num_segments, off, bwd)) return ATTN_ERR_WORKSPACE;
+  size_t off[17];
+  if (workspace_bytes < gdn_workspace_layout(total, num_heads, num_segments, off, bwd, kda)) return ATTN_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p = GdnParams{};
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -1563,6 +1795,11 @@ int gdn_setup(GdnParams& p, const void* q, const void* k, const void* v, const f
     p.dKa = reinterpret_cast<float*>(ws + off[12]);
     p.dgam = reinterpret_cast<float*>(ws + off[13]);
   }
+  if (kda) {
+    p.QB = reinterpret_cast<__nv_bfloat16*>(ws + off[14]);
+    p.KC = reinterpret_cast<__nv_bfloat16*>(ws + off[15]);
+    p.Bc = reinterpret_cast<float*>(ws + off[16]);
+  }
   return ATTN_OK;
 }
 
@@ -1574,6 +1811,17 @@ cudaError_t launch_gdn_prep(const GdnParams& p, cudaStream_t s) {
   if (e == cudaSuccess)
     e = launch_pdl(gdn_prep_kernel, dim3((unsigned)p.max_chunks, (unsigned)p.nh), dim3(kGdnThreads),
                    sizeof(PrepSmem), s, p);
+  return e;
+}
+
+// The planner and the per-chunk factors with a decay per channel.
+cudaError_t launch_kda_prep(const GdnParams& p, cudaStream_t s) {
+  cudaError_t e = launch_pdl(gdn_plan_kernel, dim3(1), dim3(256), 0, s, p);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(KdaPrepSmem));
+  if (e == cudaSuccess)
+    e = launch_pdl(kda_prep_kernel, dim3((unsigned)p.max_chunks, (unsigned)p.nh), dim3(kGdnThreads),
+                   sizeof(KdaPrepSmem), s, p);
   return e;
 }
 
@@ -1591,13 +1839,13 @@ extern "C" {
 
 size_t gdn_varlen_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments) {
   if (total < 0 || num_heads <= 0 || num_segments < 0 || total > (1LL << 30) || num_heads > 1024) return 0;
-  size_t off[14];
+  size_t off[17];
   return vsw::gdn_workspace_layout(total, num_heads, num_segments, off, false);
 }
 
 size_t gdn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments) {
   if (total < 0 || num_heads <= 0 || num_segments < 0 || total > (1LL << 30) || num_heads > 1024) return 0;
-  size_t off[14];
+  size_t off[17];
   return vsw::gdn_workspace_layout(total, num_heads, num_segments, off, true);
 }
 
@@ -1619,7 +1867,7 @@ int gdn_varlen_fwd(const void* q, const void* k, const void* v, const float* g, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_gdn_prep(p, s);
   const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
-  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<false>, seg_grid, s, p);
+  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<false, false>, seg_grid, s, p);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -1651,10 +1899,38 @@ int gdn_varlen_bwd(const void* q, const void* k, const void* v, const float* g, 
   const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
   const dim3 chunk_grid((unsigned)p.max_chunks, (unsigned)num_heads);
   cudaError_t e = launch_gdn_prep(p, s);
-  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<true>, seg_grid, s, p);
+  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<true, false>, seg_grid, s, p);
   if (e == cudaSuccess) e = launch_big<BwdStateSmem>(gdn_bwd_state_kernel, seg_grid, s, p);
   if (e == cudaSuccess) e = launch_big<LocalHSmem>(gdn_bwd_local_h_kernel, chunk_grid, s, p, kLocalThreads);
   if (e == cudaSuccess) e = launch_big<LocalWySmem>(gdn_bwd_local_wy_kernel, chunk_grid, s, p, kLocalThreads);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t kda_varlen_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments) {
+  if (total < 0 || num_heads <= 0 || num_segments < 0 || total > (1LL << 30) || num_heads > 1024) return 0;
+  size_t off[17];
+  return vsw::gdn_workspace_layout(total, num_heads, num_segments, off, false, true);
+}
+
+int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                   const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes,
+                   int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream) {
+  using namespace vsw;
+  GdnParams p;
+  int rc = gdn_setup(p, q, k, v, g, beta, cu_seqlens, scale, workspace, workspace_bytes, total, num_heads, head_dim,
+                     num_segments, false, true);
+  if (rc) return rc;
+  if (!o) return ATTN_ERR_NULL_POINTER;
+  if (reinterpret_cast<uintptr_t>(o) & 15u) return ATTN_ERR_ALIGNMENT;
+  int* status = nullptr;
+  int sms = 0;
+  if ((rc = device_for_call(&status, &sms))) return rc;
+  if (total == 0) return ATTN_OK;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_kda_prep(p, s);
+  const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
+  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<false, true>, seg_grid, s, p);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

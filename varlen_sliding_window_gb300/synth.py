@@ -179,13 +179,15 @@ class GdnInputs:
     do_bits: np.ndarray
 
 
-def make_gdn_inputs(cu_seqlens: np.ndarray, nh: int, d: int, tensor_seed: int) -> GdnInputs:
-    """Inputs of the Gated DeltaNet local layer on a packed microbatch.  Drawn
-    from default_rng(tensor_seed) in this order: q, k, v, do as N(0,1) float32
-    [T, H, d]; q and k rows divided by their L2 norm (the layer normalises them
-    before the kernel); all four rounded to bf16; then g = -softplus(x),
-    x ~ N(-5, 1.5) (decays exp(g) mostly 0.9 to 0.9995: long memory), and
-    beta = sigmoid(y), y ~ N(0, 1), both float32 [T, H]."""
+def make_gdn_inputs(cu_seqlens: np.ndarray, nh: int, d: int, tensor_seed: int,
+                    per_channel: bool = False) -> GdnInputs:
+    """Inputs of the Gated DeltaNet (or, with per_channel, Kimi Delta) local
+    layer on a packed microbatch.  Drawn from default_rng(tensor_seed) in this
+    order: q, k, v, do as N(0,1) float32 [T, H, d]; q and k rows divided by
+    their L2 norm (the layer normalises them before the kernel); all four
+    rounded to bf16; then g = -softplus(x), x ~ N(-5, 1.5) (decays exp(g)
+    mostly 0.9 to 0.9995: long memory), float32 [T, H], or [T, H, d] with a
+    gate per key channel; and beta = sigmoid(y), y ~ N(0, 1), float32 [T, H]."""
     cu = np.asarray(cu_seqlens, dtype=np.int32)
     total = int(cu[-1])
     rng = np.random.default_rng(tensor_seed)
@@ -195,7 +197,7 @@ def make_gdn_inputs(cu_seqlens: np.ndarray, nh: int, d: int, tensor_seed: int) -
         if name in ("q", "k"):
             x = x / np.maximum(np.linalg.norm(x, axis=-1, keepdims=True), np.float32(1e-6))
         draws[name] = round_to_bf16(x)
-    x = rng.normal(-5.0, 1.5, size=(total, nh)).astype(np.float32)
+    x = rng.normal(-5.0, 1.5, size=(total, nh, d) if per_channel else (total, nh)).astype(np.float32)
     g = (-np.logaddexp(np.float32(0.0), x)).astype(np.float32)
     y = rng.standard_normal((total, nh), dtype=np.float32)
     beta = (1.0 / (1.0 + np.exp(-y))).astype(np.float32)
@@ -217,6 +219,7 @@ class GdnWorkload:
     doc_seed: int = 0
     tensor_seed: int = 1
     fixed_cu: tuple[int, ...] | None = None
+    per_channel: bool = False  # Kimi Delta: a decay per key channel
 
     @property
     def scale(self) -> float:
@@ -228,7 +231,7 @@ class GdnWorkload:
         return pack_microbatch(self.total, self.context, self.doc_seed)
 
     def inputs(self) -> GdnInputs:
-        return make_gdn_inputs(self.cu_seqlens(), self.nh, self.d, self.tensor_seed)
+        return make_gdn_inputs(self.cu_seqlens(), self.nh, self.d, self.tensor_seed, self.per_channel)
 
 
 def gdn_workloads() -> dict[str, GdnWorkload]:
@@ -243,3 +246,11 @@ def gdn_workloads() -> dict[str, GdnWorkload]:
     w["gdn_ctx4096"] = GdnWorkload("gdn_ctx4096", 16384, 4096)
     w["gdn_ctx512"] = GdnWorkload("gdn_ctx512", 16384, 512)
     return w
+
+
+def kda_workloads() -> dict[str, GdnWorkload]:
+    """The Kimi Delta layer on the same cases as gdn_workloads(), with a gate
+    per key channel."""
+    import dataclasses
+    return {n.replace("gdn_", "kda_"): dataclasses.replace(w, name=w.name.replace("gdn_", "kda_"), per_channel=True)
+            for n, w in gdn_workloads().items()}
