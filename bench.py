@@ -50,6 +50,7 @@ PAGE_FA2_MS = {"ctx512_global": 0.68, "ctx4096_global": 1.43, "ctx4096_w512": 0.
 # step at context 4,096 on the same unnamed GPU (research.dws.rip/llm/kernels,
 # section 03, Fig. 5): context for the Gated DeltaNet leg.
 PAGE_GDN_MS = 1.73
+PAGE_KDA_MS = 3.32  # the same for the Kimi Delta layer
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # GEMM units (2*d*Hq*pairs flops each) each kernel does that the counting rule
 # credits: forward QK^T + PV; dK/dV pass S, dP, dV, dK; dQ pass dQ only (its
@@ -59,20 +60,30 @@ KERNEL_UNITS = {"fwd": 2.0, "bwd_preprocess": 0.0, "bwd_dkdv": 4.0, "bwd_dq": 1.
 KERNELS_PER_STEP = 5
 
 
-def gdn_flops(cu: np.ndarray, nh: int, d: int) -> tuple[float, float]:
-    """Matrix-product FLOPs the Gated DeltaNet kernels perform, per call
-    (forward, backward), summed over chunks of n <= 64 tokens and heads:
-    forward 2d(5n^2 + 3nd) (K K^T, Q K^T, the two WY factors, W H, Q H, the
-    masked Q K^T block times E, K^T E); backward, which recomputes the forward
-    without O, 2d(4n^2 + 2nd) + 2d(n^2 + 3nd) + 2d(4n^2 + 5nd) + 14dn^2 + 4n^3
-    (recomputation, state-gradient pass, the two local passes)."""
+def gdn_flops(cu: np.ndarray, nh: int, d: int, per_channel: bool = False) -> tuple[float, float]:
+    """Matrix-product FLOPs the Gated DeltaNet (or, per_channel, Kimi Delta)
+    kernels perform, per call (forward, backward), summed over chunks of
+    n <= 64 tokens and heads.  Gated DeltaNet: forward 2d(5n^2 + 3nd) (K K^T,
+    Q K^T, the two WY factors, W H, Q H, the masked Q K^T block times E,
+    K^T E); backward, which recomputes the forward without O,
+    2d(4n^2 + 2nd) + 2d(n^2 + 3nd) + 2d(4n^2 + 5nd) + 14dn^2 + 4n^3
+    (recomputation, state-gradient pass, the two local passes).  Kimi Delta:
+    K K^T and Q K^T only in the 10 of 16 blocks of 16 rows on or below the
+    diagonal; its local passes take 2d(n^2 + 3nd) and 8dn^2 + 4n^3, and the
+    four decay-weighted sums of its last pass 4 d n^2."""
     fwd = bwd = 0.0
     for L in np.diff(cu.astype(np.int64)):
         for c0 in range(0, int(L), 64):
             n = float(min(64, int(L) - c0))
-            fwd += 2 * d * (5 * n * n + 3 * n * d)
-            bwd += 2 * d * (4 * n * n + 2 * n * d) + 2 * d * (n * n + 3 * n * d) + 2 * d * (4 * n * n + 5 * n * d) \
-                + 14 * d * n * n + 4 * n ** 3
+            qk = 2 * 2 * d * n * n * (10.0 / 16.0 if per_channel else 1.0)  # K K^T and Q K^T
+            wu = 2 * 2 * d * n * n                                           # W, U
+            fwd += qk + wu + 2 * d * (n * n + 3 * n * d)
+            rec = qk + wu + 2 * 2 * n * d * d
+            state = 2 * d * (n * n + 3 * n * d)
+            if per_channel:
+                bwd += rec + state + 2 * d * (n * n + 3 * n * d) + 8 * d * n * n + 4 * n ** 3 + 4 * d * n * n
+            else:
+                bwd += rec + state + 2 * d * (4 * n * n + 5 * n * d) + 14 * d * n * n + 4 * n ** 3
     return fwd * nh, bwd * nh
 
 
@@ -283,8 +294,8 @@ def main():
                                                 for c in (512, 1024, 2048, 4096)) + ",long65536_global,long65536_w4096",
                     help="workloads whose step and kernel times are reported under also.sweep ('' for none)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
-    ap.add_argument("--gdn", default="gdn_ctx4096,gdn_ctx512",
-                    help="Gated DeltaNet workloads measured under also.gdn ('' for none)")
+    ap.add_argument("--gdn", default="gdn_ctx4096,gdn_ctx512,kda_ctx4096,kda_ctx512",
+                    help="Gated DeltaNet / Kimi Delta workloads measured under also.gdn ('' for none)")
     args = ap.parse_args()
     wls = synth.workloads()
     wl = wls[args.workload]
@@ -736,10 +747,13 @@ def main():
         o = torch.empty_like(q)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         dg, db = torch.empty_like(g_), torch.empty_like(be)
-        ws = torch.empty(binding.gdn_varlen_bwd_workspace_bytes(gw.total, gw.nh, nseg), dtype=torch.uint8,
-                         device=dev)
-        fwd = lambda: binding.gdn_varlen_fwd(q, k, v, g_, be, cu, gw.scale, o, ws)  # noqa: E731
-        bwd = lambda: binding.gdn_varlen_bwd(q, k, v, g_, be, do, cu, gw.scale, dq, dk, dv, dg, db, ws)  # noqa: E731
+        # Kimi Delta (a decay per key channel) or Gated DeltaNet: the same calls' shapes
+        f_fwd, f_bwd, f_ws = ((binding.kda_varlen_fwd, binding.kda_varlen_bwd, binding.kda_varlen_bwd_workspace_bytes)
+                              if gw.per_channel else
+                              (binding.gdn_varlen_fwd, binding.gdn_varlen_bwd, binding.gdn_varlen_bwd_workspace_bytes))
+        ws = torch.empty(f_ws(gw.total, gw.nh, nseg), dtype=torch.uint8, device=dev)
+        fwd = lambda: f_fwd(q, k, v, g_, be, cu, gw.scale, o, ws)  # noqa: E731
+        bwd = lambda: f_bwd(q, k, v, g_, be, do, cu, gw.scale, dq, dk, dv, dg, db, ws)  # noqa: E731
         for _ in range(warmup):
             fwd()
             bwd()
@@ -759,13 +773,14 @@ def main():
         status = binding.attn_varlen_get_status()
         f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
         b_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-        ff, fb = gdn_flops(gi.cu_seqlens, gw.nh, gw.d)
+        ff, fb = gdn_flops(gi.cu_seqlens, gw.nh, gw.d, gw.per_channel)
         tok = gw.total * gw.nh * gw.d * 2
-        gates = gw.total * gw.nh * 4
+        gates = gw.total * gw.nh * 4 * (gw.d if gw.per_channel else 1)
         bytes_f = 4 * tok + 2 * gates            # q, k, v in, o out; g, beta
         bytes_b = 7 * tok + 4 * gates            # q, k, v, d_o in; dq, dk, dv out; g, beta in; dg, dbeta out
         tf_f, tf_b = ff / (f_ms * 1e-3) / 1e12, fb / (b_ms * 1e-3) / 1e12
         dom = "bwd" if b_ms >= f_ms else "fwd"
+        layer, page_ms = ("Kimi Delta", PAGE_KDA_MS) if gw.per_channel else ("Gated DeltaNet", PAGE_GDN_MS)
         ach = tf_b if dom == "bwd" else tf_f
         del ws
         return {"fwd_ms": f_ms, "bwd_ms": b_ms, "step_ms": f_ms + b_ms, "segments": nseg, "tokens": gw.total,
@@ -775,14 +790,14 @@ def main():
                              "frac": ach / peak_t, "traffic": None,
                              "peak_source": f"bf16 dense burst, {'of measured' if peak_src == 'measured' else 'of fallback'}",
                              "note": "warp-level mma.sync bf16 products; the peak is the tcgen05/cuBLAS one"},
-                "page_context": ({"gdn_ms": PAGE_GDN_MS, "ratio": (f_ms + b_ms) / PAGE_GDN_MS,
-                                  "what": "the page's Gated DeltaNet layer fwd+bwd per step at context 4,096 on its "
+                "page_context": ({"page_ms": page_ms, "ratio": (f_ms + b_ms) / page_ms,
+                                  "what": f"the page's {layer} layer fwd+bwd per step at context 4,096 on its "
                                           "own unnamed GPU (research.dws.rip/llm/kernels, Fig. 5)"}
                                  if gw.context == 4096 else None),
                 "status": status}
 
     gdn = {}
-    gwls = synth.gdn_workloads()
+    gwls = {**synth.gdn_workloads(), **synth.kda_workloads()}
     for name in [x for x in args.gdn.split(",") if x]:
         gdn[name] = gdn_leg(gwls[name], max(5, args.steps // 2), 3)
     if gdn:

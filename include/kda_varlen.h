@@ -52,6 +52,22 @@ int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* g, 
                    const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes,
                    int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream);
 
+/* Bytes of device workspace kda_varlen_bwd needs: the forward's and the
+ * Gated DeltaNet backward's, plus per chunk and head X = (I + A)^-1, the
+ * unscaled A, and the gradients of the masked q.k block and of A (float32
+ * 64 x 64 each), and float32 [T, H, 128] parts of dq and of dg.  0 for
+ * invalid sizes. */
+size_t kda_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments);
+
+/* Gradients of L = sum(d_o * o): dq, dk, dv (bf16 [T, H, 128]), dg (float32
+ * [T, H, 128], one per key channel) and dbeta (float32 [T, H]), all fully
+ * overwritten; the forward is recomputed inside.  Error codes as
+ * gdn_varlen_bwd. */
+int kda_varlen_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, const void* d_o,
+                   const int32_t* cu_seqlens, float scale, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                   void* workspace, size_t workspace_bytes, int64_t total, int32_t num_heads, int32_t head_dim,
+                   int32_t num_segments, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

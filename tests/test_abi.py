@@ -32,7 +32,8 @@ def test_header_declares_the_calls():
     names = declared_functions()
     for required in ("attn_varlen_fwd", "attn_varlen_bwd", "attn_varlen_get_status", "attn_varlen_strerror",
                      "gdn_varlen_fwd", "gdn_varlen_workspace_bytes", "gdn_varlen_bwd",
-                     "gdn_varlen_bwd_workspace_bytes", "kda_varlen_fwd", "kda_varlen_workspace_bytes"):
+                     "gdn_varlen_bwd_workspace_bytes", "kda_varlen_fwd", "kda_varlen_workspace_bytes",
+                     "kda_varlen_bwd", "kda_varlen_bwd_workspace_bytes"):
         assert required in names
 
 

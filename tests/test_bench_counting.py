@@ -68,3 +68,23 @@ def test_gdn_flop_count_lists_every_product():
     assert ff == f64 + f1 and fb == b64 + b1
     ff2, fb2 = bench.gdn_flops(np.array([0, 65, 65], dtype=np.int32), 3, d)
     assert ff2 == 3 * ff and fb2 == 3 * fb
+
+
+def test_kda_flop_count_lists_every_product():
+    d = 128
+
+    def prods(n):
+        qk = [(n, d, n)] * 2                                                   # K K^T, Q K^T (10 of 16 blocks)
+        fwd_rest = [(n, n, d), (n, n, d), (n, d, d), (n, d, d), (n, n, d), (d, n, d)]  # W, U, W H, QB H, Aq E, KC^T E
+        rec_rest = [(n, n, d), (n, n, d), (n, d, d), (d, n, d)]               # W, U, W H, KC^T E
+        state = [(n, n, d), (n, d, d), (d, n, d), (d, n, d)]
+        loc_h = [(n, d, n), (n, d, d), (n, d, d), (n, d, d)]                   # dO E^T, dO H0^T, dE H0^T, E dH1^T
+        loc_wy = [(n, d, n)] * 2 + [(n, n, n)] * 2 + [(n, n, d)] * 2
+        f = sum(2 * a * b * c for a, b, c in fwd_rest) + sum(2 * a * b * c for a, b, c in qk) * 10 / 16
+        b = (sum(2 * a * b * c for a, b, c in rec_rest + state + loc_h + loc_wy)
+             + sum(2 * a * b * c for a, b, c in qk) * 10 / 16 + 4 * d * n * n)
+        return f, b
+
+    f64, b64 = prods(64)
+    ff, fb = bench.gdn_flops(np.array([0, 64], dtype=np.int32), 1, d, per_channel=True)
+    assert ff == f64 and fb == b64

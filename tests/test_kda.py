@@ -9,7 +9,10 @@ inside the products, the WY factors W and U, the masked q.k block, K o e^gamma,
 Q o e^gamma, K o e^(gamma_last - gamma), the state copy used as an operand,
 the pseudo-values E and o itself: about nine roundings of relative RMS
 2^-8 / sqrt(3) = 2.3e-3, sqrt(9) x 2.3e-3 = 6.9e-3 together; the bound is
-about twice that.
+about twice that.  The gradients (relative L2 <= 2e-2 each, same per-segment
+rule) add the recomputed factors, the bf16 copies of the state and of its
+gradient, dE and dW, X as an operand and their outputs: about fifteen
+roundings, sqrt(15) x 2.3e-3 = 8.9e-3, and again about twice that.
 """
 import numpy as np
 import pytest
@@ -18,6 +21,7 @@ from tests.helpers import assert_per_segment, rel_l2
 from varlen_sliding_window_gb300 import synth
 
 TOL_O = 1.5e-2
+TOL_GRAD = 2e-2
 WL = synth.kda_workloads()
 
 
@@ -92,3 +96,39 @@ def test_empty_segments_and_repeats_are_bit_identical():
     cu = inp.cu_seqlens
     padded = np.concatenate([[0], cu[:4], cu[3:7], cu[6:], [cu[-1]] * 5]).astype(np.int32)
     assert torch.equal(a, _run(inp, w.scale, cu=padded))
+
+
+def _run_bwd(inp, scale):
+    import torch
+    from varlen_sliding_window_gb300 import binding
+    cu = inp.cu_seqlens
+    q, k, v, do = (_to_dev(b) for b in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
+    g = torch.from_numpy(inp.g).cuda()
+    beta = torch.from_numpy(inp.beta).cuda()
+    cu_t = torch.from_numpy(np.asarray(cu, dtype=np.int32)).cuda()
+    T, nh, _ = q.shape
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    dg, dbeta = torch.full_like(g, float("nan")), torch.full_like(beta, float("nan"))
+    ws = torch.empty(binding.kda_varlen_bwd_workspace_bytes(T, nh, len(cu) - 1), dtype=torch.uint8, device="cuda")
+    binding.kda_varlen_bwd(q, k, v, g, beta, do, cu_t, scale, dq, dk, dv, dg, dbeta, ws)
+    torch.cuda.synchronize()
+    assert binding.attn_varlen_get_status() == 0
+    return [x.double().cpu().numpy() for x in (dq, dk, dv, dg, dbeta)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["kda_tiny", "kda_ragged", "kda_ctx4096"])
+def test_backward_matches_oracle(name):
+    from oracle import kimi_delta
+    w = WL[name]
+    inp = w.inputs()
+    got = _run_bwd(inp, w.scale)
+    ref = kimi_delta.backward(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.do, inp.cu_seqlens, w.scale)
+    errs = {}
+    for nm, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), got, ref):
+        assert np.isfinite(a).all(), nm
+        errs[nm] = rel_l2(a, b)
+    print(name, {k: f"{v:.3e}" for k, v in errs.items()})
+    for nm, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), got, ref):
+        assert errs[nm] <= TOL_GRAD, (nm, errs[nm])
+        assert_per_segment(a, b, inp.cu_seqlens, TOL_GRAD, nm)

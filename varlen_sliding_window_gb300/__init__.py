@@ -16,7 +16,7 @@ _BINDING_NAMES = {
     "attn_varlen_bwd_dkdv", "attn_varlen_bwd_dq", "attn_varlen_bwd_noalloc", "attn_varlen_fwd_strided",
     "attn_varlen_bwd_strided", "attn_varlen_set_workspace", "attn_varlen_workspace_bytes", "load_library",
     "AttnError", "gdn_varlen_fwd", "gdn_varlen_workspace_bytes", "gdn_varlen_bwd", "gdn_varlen_bwd_workspace_bytes",
-    "kda_varlen_fwd", "kda_varlen_workspace_bytes",
+    "kda_varlen_fwd", "kda_varlen_workspace_bytes", "kda_varlen_bwd", "kda_varlen_bwd_workspace_bytes",
 }
 
 

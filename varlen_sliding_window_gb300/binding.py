@@ -79,6 +79,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.kda_varlen_workspace_bytes.restype = ctypes.c_size_t
     lib.kda_varlen_fwd.argtypes = lib.gdn_varlen_fwd.argtypes
     lib.kda_varlen_fwd.restype = ctypes.c_int
+    lib.kda_varlen_bwd_workspace_bytes.argtypes = [i64, i32, i32]
+    lib.kda_varlen_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.kda_varlen_bwd.argtypes = lib.gdn_varlen_bwd.argtypes
+    lib.kda_varlen_bwd.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -362,3 +366,25 @@ def kda_varlen_fwd(q, k, v, g, beta, cu_seqlens, scale: float, o, workspace, str
     rc = lib.kda_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), float(scale), _ptr(o),
                             _ptr(workspace), int(workspace.numel()), total, nh, d, nseg, _stream_handle(stream))
     _check(rc, "kda_varlen_fwd")
+
+
+def kda_varlen_bwd_workspace_bytes(total: int, num_heads: int, num_segments: int) -> int:
+    """Device workspace bytes kda_varlen_bwd needs (include/kda_varlen.h)."""
+    return int(load_library().kda_varlen_bwd_workspace_bytes(int(total), int(num_heads), int(num_segments)))
+
+
+def kda_varlen_bwd(q, k, v, g, beta, d_o, cu_seqlens, scale: float, dq, dk, dv, dg, dbeta, workspace,
+                   stream=None) -> None:
+    """Kimi Delta backward: dq, dk, dv (bf16 [T, H, 128]), dg (float32 [T, H, 128])
+    and dbeta (float32 [T, H]) of sum(d_o * o)."""
+    _require_dense("kda_varlen_bwd", q, k, v, d_o, dq, dk, dv)
+    for t in (g, beta, dg, dbeta):
+        if not t.is_contiguous():
+            raise ValueError("g, beta, dg and dbeta must be dense float32 tensors")
+    lib = load_library()
+    total, nh, d = (int(x) for x in q.shape)
+    nseg = int(cu_seqlens.numel()) - 1
+    rc = lib.kda_varlen_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(d_o), _ptr(cu_seqlens), float(scale),
+                            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(workspace),
+                            int(workspace.numel()), total, nh, d, nseg, _stream_handle(stream))
+    _check(rc, "kda_varlen_bwd")

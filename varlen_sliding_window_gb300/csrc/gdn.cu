@@ -79,6 +79,11 @@ struct GdnParams {
   __nv_bfloat16* QB;    // [T, H, 128]
   __nv_bfloat16* KC;    // [T, H, 128]
   float* Bc;            // [max_chunks, H, 128]
+  float* Xw;            // Kimi Delta backward: X = (I + A)^-1 of every chunk, fp32 [max_chunks, H, 64, 64]
+  float* Araw;          //   and sum_c k_ic k_jc e^(gamma_ic - gamma_jc) (j < i), same layout
+  float* Nw;            //   lower(scale dO E^T), same layout
+  float* Mw;            //   diag(beta) dA, same layout
+  float* dQa;           //   the part of dq that needs the states, fp32 [T, H, 128]
   // backward only
   const __nv_bfloat16* dO;  // [T, H, 128]
   __nv_bfloat16* dq;        // [T, H, 128]
@@ -524,6 +529,8 @@ static_assert(sizeof(KdaPrepSmem) <= 227 * 1024, "fits one SM");
 // Row offset of block I's scaled K copy inside KI (blocks of 16, 32, 48, 64 rows).
 __device__ __forceinline__ int ki_row0(int I) { return 8 * I * (I + 1); }
 
+// kBwd (the backward's recomputation) also stores X and the unscaled A.
+template <bool kBwd>
 __global__ void __launch_bounds__(kGdnThreads) kda_prep_kernel(GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   KdaPrepSmem& sm = *reinterpret_cast<KdaPrepSmem*>(smem_raw);
@@ -611,6 +618,10 @@ __global__ void __launch_bounds__(kGdnThreads) kda_prep_kernel(GdnParams p) {
         const float bi = sm.bet[i];
         sm.A[i * kSF + j] = j < i ? bi * sa[n][2 * hr] : 0.f;
         sm.A[i * kSF + j + 1] = j + 1 < i ? bi * sa[n][2 * hr + 1] : 0.f;
+        if (kBwd) {
+          float* ar = p.Araw + ((size_t)c * p.nh + h) * (kC * kC) + i * kC + j;
+          *reinterpret_cast<float2*>(ar) = make_float2(j < i ? sa[n][2 * hr] : 0.f, j + 1 < i ? sa[n][2 * hr + 1] : 0.f);
+        }
         *reinterpret_cast<uint32_t*>(aqk + i * kC + j) =
             pack2(j <= i ? sq[n][2 * hr] : 0.f, j + 1 <= i ? sq[n][2 * hr + 1] : 0.f);
       }
@@ -623,9 +634,14 @@ __global__ void __launch_bounds__(kGdnThreads) kda_prep_kernel(GdnParams p) {
     const int i = 16 * bi + r, j = 16 * bj + cc;
     sm.A[i * kSF + j] = 0.f;
     aqk[i * kC + j] = __float2bfloat16_rn(0.f);
+    if (kBwd) p.Araw[((size_t)c * p.nh + h) * (kC * kC) + i * kC + j] = 0.f;
   }
   __syncthreads();
   wy_inverse(sm.A, sm.X, sm.R, tid);
+  if (kBwd) {
+    float* xw = p.Xw + ((size_t)c * p.nh + h) * (kC * kC);
+    for (int e = tid; e < kC * kC; e += nt) xw[e] = sm.X[(e >> 6) * kSF + (e & 63)];
+  }
   // ---- T2 = X diag(beta); KB <- K o e^gamma; QB, KC, e^gamma_last to the workspace
   for (int e = tid; e < kC * kC / 2; e += nt) {
     const int i = e >> 5, j = (e & 31) * 2;
@@ -924,7 +940,7 @@ struct BwdStage {
   __nv_bfloat16 W[kC * kS128];
   __nv_bfloat16 Aq[kC * kS64];
   __nv_bfloat16 dO[kC * kS32];
-  float gam[kC];
+  float gam[kD];  // as StateStage::gam
 };
 struct BwdStateSmem {
   BwdStage st[kStateStages];
@@ -934,12 +950,13 @@ struct BwdStateSmem {
 };
 static_assert(sizeof(BwdStateSmem) <= 227 * 1024, "the backward state CTA's shared memory fits one SM");
 
+template <bool kChan>
 __device__ __forceinline__ void load_bwd_stage(BwdStage& s, const GdnParams& p, int chunk, int h, int vb, int tid) {
   constexpr int nt = kStateThreads;
   const int4 ch = p.chunks[chunk];
   const int len = chunk_len(ch, p.total), t0 = len > 0 ? ch.x : 0;
-  load_rows128(smem_u32(s.K), p.k, t0, len, h, p.nh, tid, nt);
-  load_rows128(smem_u32(s.Q), p.q, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(s.K), kChan ? p.KC : p.k, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(s.Q), kChan ? p.QB : p.q, t0, len, h, p.nh, tid, nt);
   load_rows128(smem_u32(s.W), p.W, t0, len, h, p.nh, tid, nt);
   for (int e = tid; e < kC * 4; e += nt) {  // dO columns [32 vb, 32 vb + 32)
     const int r = e >> 2, cc = (e & 3) * 8;
@@ -952,12 +969,17 @@ __device__ __forceinline__ void load_bwd_stage(BwdStage& s, const GdnParams& p, 
     const int r = e >> 3, cc = (e & 7) * 8;
     cp_async16(smem_u32(&s.Aq[r * kS64 + cc]), aq + r * kC + cc, true);
   }
-  if (tid < kC) {
+  if (kChan) {
+    if (tid < kD / 4) cp_async16(smem_u32(&s.gam[4 * tid]), p.Bc + ((size_t)chunk * p.nh + h) * kD + 4 * tid, true);
+  } else if (tid < kC) {
     const bool ok = tid < len;
     cp_async4(smem_u32(&s.gam[tid]), p.gam + (size_t)h * p.total + t0 + (ok ? tid : 0), ok);
   }
 }
 
+// kChan (Kimi Delta): KC and QB replace K and Q (no per-token factors), and
+// the gradient decays by e^gamma_last per channel (row).
+template <bool kChan>
 __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   BwdStateSmem& sm = *reinterpret_cast<BwdStateSmem*>(smem_raw);
@@ -980,12 +1002,12 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
     for (int e = 0; e < 4; ++e) dh[n][e] = 0.f;
   const uint32_t sH = smem_u32(sm.H), sE = smem_u32(sm.E), sG = smem_u32(sm.G);
   // chunk ci (0 = the segment's last) is chunk first + nch - 1 - ci, in stage ci % 3
-  load_bwd_stage(sm.st[0], p, first + nch - 1, h, vb, tid);
+  load_bwd_stage<kChan>(sm.st[0], p, first + nch - 1, h, vb, tid);
   cp_async_commit();
-  if (nch > 1) load_bwd_stage(sm.st[1], p, first + nch - 2, h, vb, tid);
+  if (nch > 1) load_bwd_stage<kChan>(sm.st[1], p, first + nch - 2, h, vb, tid);
   cp_async_commit();
   for (int ci = 0; ci < nch; ++ci) {
-    if (ci + 2 < nch) load_bwd_stage(sm.st[(ci + 2) % kStateStages], p, first + nch - 3 - ci, h, vb, tid);
+    if (ci + 2 < nch) load_bwd_stage<kChan>(sm.st[(ci + 2) % kStateStages], p, first + nch - 3 - ci, h, vb, tid);
     cp_async_commit();
     cp_async_wait<2>();
 #pragma unroll
@@ -1014,7 +1036,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
     }
     const uint32_t sK = smem_u32(s.K), sQ = smem_u32(s.Q), sW = smem_u32(s.W), sAq = smem_u32(s.Aq),
                    sdO = smem_u32(s.dO);
-    const float g_last = s.gam[len - 1];
+    const float g_last = kChan ? 0.f : s.gam[len - 1];
     // ---- dE = scale Aq^T dO + diag(e^(gamma_last - gamma)) K dH
     float ca[2][4], ck[2][4];
 #pragma unroll
@@ -1040,7 +1062,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int i = r0 + (lane >> 2) + 8 * hr;
-      const float w = i < len ? __expf(g_last - s.gam[i]) : 0.f;
+      const float w = i < len ? (kChan ? 1.f : __expf(g_last - s.gam[i])) : 0.f;
       const float m = i < len ? p.scale : 0.f;
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
@@ -1052,7 +1074,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
     // scale e^gamma dO, the B operand of Q^T (.) below
     for (int e = tid; e < kC * 16; e += kStateThreads) {
       const int i = e >> 4, j = (e & 15) * 2;
-      const float m = i < len ? p.scale * __expf(s.gam[i]) : 0.f;
+      const float m = i < len ? p.scale * (kChan ? 1.f : __expf(s.gam[i])) : 0.f;
       const float2 d = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&s.dO[i * kS32 + j]));
       *reinterpret_cast<uint32_t*>(&sm.G[i * kS32 + j]) = pack2(m * d.x, m * d.y);
     }
@@ -1064,15 +1086,18 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
             *reinterpret_cast<const uint4*>(&sm.E[rr * kS32 + cc]);
     }
     // ---- dH = e^gamma_last dH + Q^T G - W^T dE (rows [m0, +16))
-    const float dl = __expf(g_last);
+    const float dl0 = kChan ? s.gam[m0 + (lane >> 2)] : __expf(g_last);
+    const float dl1 = kChan ? s.gam[m0 + (lane >> 2) + 8] : dl0;
     float cw[4][4];
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 4; ++n) {
+      dh[n][0] *= dl0;
+      dh[n][1] *= dl0;
+      dh[n][2] *= dl1;
+      dh[n][3] *= dl1;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        dh[n][e] *= dl;
-        cw[n][e] = 0.f;
-      }
+      for (int e = 0; e < 4; ++e) cw[n][e] = 0.f;
+    }
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
       uint32_t aq[4], aw[4], g0[4], g1[4], e0[4], e1[4];
@@ -1391,6 +1416,218 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParam
   }
   __syncthreads();
   if (tid < len) p.dgam[(size_t)h * p.total + t0 + tid] = sm.dgs[tid] + (tid == len - 1 ? sm.last : 0.f);
+}
+
+// ============================================================== Kimi Delta backward: local, with the states
+// Per (chunk, head), with B = e^gamma per channel, QB = Q o B, KC = K o e^(gamma_last - gamma):
+//     dQB = scale dO H0^T       ->  dQa = dQB o B,            dgam += dQB o QB
+//     dW  = -dE H0^T
+//     dKC = E dH1^T             ->  dKa = dKC o e^(gamma_last - gamma),  dgam -= dKC o KC,
+//                                   dgam_last += sum_i dKC_i o KC_i
+//     dgam_last += e^gamma_last o rowsum(dH1 o H0)
+//     N   = lower(scale dO E^T) (the gradient of the masked q.k block, to the workspace)
+struct KdaLocalHSmem {
+  __nv_bfloat16 dO[kC * kS128];
+  __nv_bfloat16 dE[kC * kS128];
+  __nv_bfloat16 E[kC * kS128];
+  __nv_bfloat16 QB[kC * kS128];
+  __nv_bfloat16 KC[kC * kS128];
+  __nv_bfloat16 H0[kD * kS128];
+  __nv_bfloat16 dH1[kD * kS128];
+  float G[kC * kG];  // gamma per channel
+  float last[kD];    // the gamma_last terms per channel
+};
+static_assert(sizeof(KdaLocalHSmem) <= 227 * 1024, "fits one SM");
+
+__global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_h_kernel(GdnParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  KdaLocalHSmem& sm = *reinterpret_cast<KdaLocalHSmem*>(smem_raw);
+  constexpr int nt = kLocalThreads;
+  grid_dependency_wait();
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int n_chunks = __ldcg(p.hdr);
+  const int4 ch = p.chunks[c];
+  if (c >= n_chunks) return;
+  const int len = chunk_len(ch, p.total);
+  if (len <= 0) return;  // only with a boundary list that breaks its rules
+  const int t0 = ch.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t sdO = smem_u32(sm.dO), sdE = smem_u32(sm.dE), sE = smem_u32(sm.E), sH0 = smem_u32(sm.H0),
+                 sdH1 = smem_u32(sm.dH1);
+  load_rows128(sdO, p.dO, t0, len, h, p.nh, tid, nt);
+  load_rows128(sdE, p.dE, t0, len, h, p.nh, tid, nt);
+  load_rows128(sE, p.E, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(sm.QB), p.QB, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(sm.KC), p.KC, t0, len, h, p.nh, tid, nt);
+  {
+    const __nv_bfloat16* h0 = p.H0 + ((size_t)c * p.nh + h) * (kD * kD);
+    const __nv_bfloat16* d1 = p.dH1 + ((size_t)c * p.nh + h) * (kD * kD);
+    for (int e = tid; e < kD * 16; e += nt) {
+      const int r = e >> 4, cc = (e & 15) * 8;
+      cp_async16(sH0 + 2u * (uint32_t)(r * kS128 + cc), h0 + r * kD + cc, true);
+      cp_async16(sdH1 + 2u * (uint32_t)(r * kS128 + cc), d1 + r * kD + cc, true);
+    }
+  }
+  for (int e = tid; e < kC * 32; e += nt) {
+    const int r = e >> 5, cc = (e & 31) * 4;
+    const bool ok = r < len;
+    cp_async16(smem_u32(&sm.G[r * kG + cc]), p.g + ((size_t)(t0 + (ok ? r : 0)) * p.nh + h) * kD + cc, ok);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  if (tid < kD) {  // gamma per channel, and e^gamma_last rowsum(dH1 o H0) of the channel (row tid of H)
+    float acc = 0.f;
+    for (int i = 0; i < kC; ++i) {
+      acc += sm.G[i * kG + tid];
+      sm.G[i * kG + tid] = acc;
+    }
+    float d = 0.f;
+    for (int v = 0; v < kD; v += 2) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.H0[tid * kS128 + v]));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.dH1[tid * kS128 + v]));
+      d += a.x * b.x + a.y * b.y;
+    }
+    sm.last[tid] = d * __expf(sm.G[(len - 1) * kG + tid]);
+  }
+  __syncthreads();
+  const int r0 = 16 * (warp & 3);
+  // ---- N = lower(scale dO E^T): rows [r0, +16) x columns [c0, +16)
+  {
+    const int c0 = 16 * (warp >> 2);
+    float s1[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s1[n][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      uint32_t a[4], b[4];
+      ldsm_x4(a, frag_a(sdO, kS128, r0, 16 * kk, lane));
+      ldsm_x4(b, frag_bt(sE, kS128, c0, 16 * kk, lane));
+      mma_bf16(s1[0], a, b[0], b[1]);
+      mma_bf16(s1[1], a, b[2], b[3]);
+    }
+    float* nw = p.Nw + ((size_t)c * p.nh + h) * (kC * kC);
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = r0 + (lane >> 2) + 8 * hr;
+        const int j = c0 + 8 * n + 2 * (lane & 3);
+        *reinterpret_cast<float2*>(nw + i * kC + j) =
+            make_float2(j <= i ? p.scale * s1[n][2 * hr] : 0.f, j + 1 <= i ? p.scale * s1[n][2 * hr + 1] : 0.f);
+      }
+  }
+  // ---- 64 x 128 products: rows [r0, +16), columns [d0, +32)
+  const int d0 = 32 * (warp >> 2);
+  float acc[4][4], dg[2][4][2];
+  auto zero = [&](float (&x)[4][4]) {
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[n][e] = 0.f;
+  };
+  // acc += A (rows r0, K = 128) * Bt^T, Bt stored [n][k] (the H0^T / dH1^T forms)
+  auto mm_abt = [&](float (&x)[4][4], uint32_t sa, uint32_t sbt) {
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(a, frag_a(sa, kS128, r0, 16 * kk, lane));
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        uint32_t b[4];
+        ldsm_x4(b, frag_bt(sbt, kS128, d0 + 16 * np, 16 * kk, lane));
+        mma_bf16(x[2 * np], a, b[0], b[1]);
+        mma_bf16(x[2 * np + 1], a, b[2], b[3]);
+      }
+    }
+  };
+  // dQB = scale dO H0^T
+  zero(acc);
+  mm_abt(acc, sdO, sH0);
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int i = r0 + (lane >> 2) + 8 * hr;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const int j = d0 + 8 * n + 2 * (lane & 3);
+      const float a0 = p.scale * acc[n][2 * hr], a1 = p.scale * acc[n][2 * hr + 1];
+      const float2 qb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.QB[i * kS128 + j]));
+      dg[hr][n][0] = a0 * qb.x;
+      dg[hr][n][1] = a1 * qb.y;
+      if (i < len)
+        *reinterpret_cast<float2*>(p.dQa + ((size_t)(t0 + i) * p.nh + h) * kD + j) =
+            make_float2(a0 * __expf(sm.G[i * kG + j]), a1 * __expf(sm.G[i * kG + j + 1]));
+    }
+  }
+  // dW = -dE H0^T
+  zero(acc);
+  mm_abt(acc, sdE, sH0);
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int i = r0 + (lane >> 2) + 8 * hr;
+    if (i < len) {
+      __nv_bfloat16* row = p.dW + ((size_t)(t0 + i) * p.nh + h) * kD + d0;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int j = 8 * n + 2 * (lane & 3);
+        *reinterpret_cast<uint32_t*>(row + j) = pack2(-acc[n][2 * hr], -acc[n][2 * hr + 1]);
+      }
+    }
+  }
+  // dKC = E dH1^T
+  zero(acc);
+  mm_abt(acc, sE, sdH1);
+  float colp[4][2];  // this thread's part of sum_i dKC_i o KC_i, per column
+#pragma unroll
+  for (int n = 0; n < 4; ++n) colp[n][0] = colp[n][1] = 0.f;
+  const float* glast = &sm.G[(len - 1) * kG];
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int i = r0 + (lane >> 2) + 8 * hr;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const int j = d0 + 8 * n + 2 * (lane & 3);
+      const float a0 = acc[n][2 * hr], a1 = acc[n][2 * hr + 1];
+      const float2 kc = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.KC[i * kS128 + j]));
+      dg[hr][n][0] -= a0 * kc.x;
+      dg[hr][n][1] -= a1 * kc.y;
+      if (i < len) {
+        colp[n][0] += a0 * kc.x;
+        colp[n][1] += a1 * kc.y;
+        *reinterpret_cast<float2*>(p.dKa + ((size_t)(t0 + i) * p.nh + h) * kD + j) =
+            make_float2(a0 * __expf(glast[j] - sm.G[i * kG + j]), a1 * __expf(glast[j + 1] - sm.G[i * kG + j + 1]));
+      }
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float x = colp[n][e];
+      x += __shfl_xor_sync(0xffffffffu, x, 4);
+      x += __shfl_xor_sync(0xffffffffu, x, 8);
+      x += __shfl_xor_sync(0xffffffffu, x, 16);
+      if (lane < 4) atomicAdd(&sm.last[d0 + 8 * n + 2 * lane + e], x);
+    }
+  __syncthreads();
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int i = r0 + (lane >> 2) + 8 * hr;
+    if (i < len) {
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int j = d0 + 8 * n + 2 * (lane & 3);
+        float x0 = dg[hr][n][0], x1 = dg[hr][n][1];
+        if (i == len - 1) {
+          x0 += sm.last[j];
+          x1 += sm.last[j + 1];
+        }
+        *reinterpret_cast<float2*>(p.dgam + ((size_t)(t0 + i) * p.nh + h) * kD + j) = make_float2(x0, x1);
+      }
+    }
+  }
 }
 
 // ============================================================== backward: local, the WY factors
@@ -1712,13 +1949,368 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_wy_kernel(GdnPara
     if (i0 < len) p.dg[(size_t)(t0 + i0) * p.nh + h] = ex + a1 + a0;
   }
 }
+// ============================================================== Kimi Delta backward: local, the WY factors
+// Per (chunk, head), from K, V, dE, dW and the recomputation's X and A (unscaled):
+//     dX  = (dE V^T + dW KB^T) diag(beta),   KB = K o e^gamma
+//     dA  = strictly-lower(-X^T dX X^T),      M = diag(beta) dA   (to the workspace)
+//     dVb = X^T dE,  XdW = X^T dW
+//     dv  = diag(beta) dVb                                          (final)
+//     dbeta_i = sum_j dA_ij Araw_ij + <dVb_i, v_i> + <XdW_i, KB_i>  (final)
+//     dKa += diag(beta) XdW o e^gamma,  dgam += diag(beta) XdW o KB
+struct KdaLocalWySmem {
+  __nv_bfloat16 KB[kC * kS128];  // K, then K o e^gamma
+  __nv_bfloat16 V[kC * kS128];
+  __nv_bfloat16 dE[kC * kS128];
+  __nv_bfloat16 dW[kC * kS128];
+  float G[kC * kG];
+  float X[kC * kS4];
+  float XT[kC * kS4];
+  float dXT[kC * kS4];
+  float Y[kC * kS4];
+  float A[kC * kSF];    // dA
+  float Ar[kC * kSF];   // the unscaled A
+  __nv_bfloat16 Xb[kC * kS64];
+  float bet[kC];
+  float dbs[kC];
+};
+static_assert(sizeof(KdaLocalWySmem) <= 227 * 1024, "fits one SM");
+
+__global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_wy_kernel(GdnParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  KdaLocalWySmem& sm = *reinterpret_cast<KdaLocalWySmem*>(smem_raw);
+  constexpr int nt = kLocalThreads;
+  grid_dependency_wait();
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int n_chunks = __ldcg(p.hdr);
+  const int4 ch = p.chunks[c];
+  if (c >= n_chunks) return;
+  const int len = chunk_len(ch, p.total);
+  if (len <= 0) return;  // only with a boundary list that breaks its rules
+  const int t0 = ch.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t sKB = smem_u32(sm.KB), sV = smem_u32(sm.V), sdE = smem_u32(sm.dE), sdW = smem_u32(sm.dW),
+                 sXb = smem_u32(sm.Xb);
+  load_rows128(sKB, p.k, t0, len, h, p.nh, tid, nt);
+  load_rows128(sV, p.v, t0, len, h, p.nh, tid, nt);
+  load_rows128(sdE, p.dE, t0, len, h, p.nh, tid, nt);
+  load_rows128(sdW, p.dW, t0, len, h, p.nh, tid, nt);
+  for (int e = tid; e < kC * 32; e += nt) {
+    const int r = e >> 5, cc = (e & 31) * 4;
+    const bool ok = r < len;
+    cp_async16(smem_u32(&sm.G[r * kG + cc]), p.g + ((size_t)(t0 + (ok ? r : 0)) * p.nh + h) * kD + cc, ok);
+  }
+  {
+    const size_t base = ((size_t)c * p.nh + h) * (kC * kC);
+    for (int e = tid; e < kC * 16; e += nt) {  // X and the unscaled A, 16 pieces of 4 floats per row
+      const int r = e >> 4, cc = (e & 15) * 4;
+      cp_async16(smem_u32(&sm.X[r * kS4 + cc]), p.Xw + base + r * kC + cc, true);
+    }
+  }
+  cp_async_commit();
+  if (tid < kC) {
+    sm.bet[tid] = tid < len ? p.beta[(size_t)(t0 + tid) * p.nh + h] : 0.f;
+    sm.dbs[tid] = 0.f;
+  }
+  {
+    const float* ar = p.Araw + ((size_t)c * p.nh + h) * (kC * kC);
+    for (int e = tid; e < kC * kC; e += nt) sm.Ar[(e >> 6) * kSF + (e & 63)] = ar[e];
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  if (tid < kD) {  // gamma per channel
+    float acc = 0.f;
+    for (int i = 0; i < kC; ++i) {
+      acc += sm.G[i * kG + tid];
+      sm.G[i * kG + tid] = acc;
+    }
+  }
+  __syncthreads();
+  // KB = K o e^gamma in place; Xb, XT
+  for (int e = tid; e < kC * kD / 2; e += nt) {
+    const int i = e >> 6, cc = (e & 63) * 2;
+    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.KB[i * kS128 + cc]));
+    *reinterpret_cast<uint32_t*>(&sm.KB[i * kS128 + cc]) =
+        pack2(kv.x * __expf(sm.G[i * kG + cc]), kv.y * __expf(sm.G[i * kG + cc + 1]));
+  }
+  for (int e = tid; e < kC * kC / 2; e += nt) {
+    const int i = e >> 5, j = (e & 31) * 2;
+    const float x0 = sm.X[i * kS4 + j], x1 = sm.X[i * kS4 + j + 1];
+    *reinterpret_cast<uint32_t*>(&sm.Xb[i * kS64 + j]) = pack2(x0, x1);
+    sm.XT[j * kS4 + i] = x0;
+    sm.XT[(j + 1) * kS4 + i] = x1;
+  }
+  __syncthreads();
+  const int r0 = 16 * (warp & 3);
+  // ---- dX = (dE V^T + dW KB^T) diag(beta): rows [r0, +16) x columns [c0, +16), stored transposed
+  {
+    const int c0 = 16 * (warp >> 2);
+    float pv[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pv[n][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      uint32_t ae[4], aw[4], bv[4], bk[4];
+      ldsm_x4(ae, frag_a(sdE, kS128, r0, 16 * kk, lane));
+      ldsm_x4(aw, frag_a(sdW, kS128, r0, 16 * kk, lane));
+      ldsm_x4(bv, frag_bt(sV, kS128, c0, 16 * kk, lane));
+      ldsm_x4(bk, frag_bt(sKB, kS128, c0, 16 * kk, lane));
+      mma_bf16(pv[0], ae, bv[0], bv[1]);
+      mma_bf16(pv[1], ae, bv[2], bv[3]);
+      mma_bf16(pv[0], aw, bk[0], bk[1]);
+      mma_bf16(pv[1], aw, bk[2], bk[3]);
+    }
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = r0 + (lane >> 2) + 8 * hr;
+          const int j = c0 + 8 * n + 2 * (lane & 3) + e;
+          sm.dXT[j * kS4 + i] = pv[n][2 * hr + e] * sm.bet[j];
+        }
+  }
+  __syncthreads();
+  // ---- Y = dX X^T, then dA = -X^T Y, strictly lower (fp32, 2 x 4 blocks per thread)
+  {
+    const int i0 = 2 * (tid >> 4), j0 = 4 * (tid & 15);
+    float y[2][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
+#pragma unroll 4
+    for (int m = 0; m < kC; ++m) {
+      const float2 xa = *reinterpret_cast<const float2*>(&sm.dXT[m * kS4 + i0]);
+      const float4 xb = *reinterpret_cast<const float4*>(&sm.XT[m * kS4 + j0]);
+      const float av[2] = {xa.x, xa.y}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+      *reinterpret_cast<float4*>(&sm.Y[(i0 + a) * kS4 + j0]) = make_float4(y[a][0], y[a][1], y[a][2], y[a][3]);
+    __syncthreads();
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
+#pragma unroll 4
+    for (int m = 0; m < kC; ++m) {
+      const float2 xa = *reinterpret_cast<const float2*>(&sm.X[m * kS4 + i0]);
+      const float4 xb = *reinterpret_cast<const float4*>(&sm.Y[m * kS4 + j0]);
+      const float av[2] = {xa.x, xa.y}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) sm.A[(i0 + a) * kSF + j0 + b] = j0 + b < i0 + a ? -y[a][b] : 0.f;
+  }
+  __syncthreads();
+  // ---- M = diag(beta) dA to the workspace; sum_j dA_ij Araw_ij into dbeta
+  {
+    float* mw = p.Mw + ((size_t)c * p.nh + h) * (kC * kC);
+    for (int e = tid; e < kC * kC; e += nt) {
+      const int i = e >> 6, j = e & 63;
+      mw[e] = sm.bet[i] * sm.A[i * kSF + j];
+    }
+    if (tid < kC) {
+      float rb = 0.f;
+      for (int j = 0; j < kC; ++j) rb += sm.A[tid * kSF + j] * sm.Ar[tid * kSF + j];
+      sm.dbs[tid] += rb;
+    }
+  }
+  __syncthreads();  // dbs gets atomic adds below
+  // ---- dVb = X^T dE, XdW = X^T dW: rows [r0, +16) x columns [d0, +32)
+  const int d0 = 32 * (warp >> 2);
+  float cv[4][4], ck[4][4];
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cv[n][e] = ck[n][e] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < kC / 16; ++kk) {
+    uint32_t a[4];
+    ldsm_x4_t(a, frag_bt(sXb, kS64, 16 * kk, r0, lane));  // X^T: X stored [i][j]
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      uint32_t be[4], bw[4];
+      ldsm_x4_t(be, frag_b(sdE, kS128, 16 * kk, d0 + 16 * np, lane));
+      ldsm_x4_t(bw, frag_b(sdW, kS128, 16 * kk, d0 + 16 * np, lane));
+      mma_bf16(cv[2 * np], a, be[0], be[1]);
+      mma_bf16(cv[2 * np + 1], a, be[2], be[3]);
+      mma_bf16(ck[2 * np], a, bw[0], bw[1]);
+      mma_bf16(ck[2 * np + 1], a, bw[2], bw[3]);
+    }
+  }
+  {
+    float rv[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const float bi = sm.bet[i];
+      const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + d0;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int j = 8 * n + 2 * (lane & 3);
+        const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.V[i * kS128 + d0 + j]));
+        const float2 kb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.KB[i * kS128 + d0 + j]));
+        rv[hr] += cv[n][2 * hr] * vv.x + cv[n][2 * hr + 1] * vv.y;
+        rk[hr] += ck[n][2 * hr] * kb.x + ck[n][2 * hr + 1] * kb.y;
+        if (i < len) {
+          *reinterpret_cast<uint32_t*>(p.dv + off + j) = pack2(bi * cv[n][2 * hr], bi * cv[n][2 * hr + 1]);
+          const float e0 = __expf(sm.G[i * kG + d0 + j]), e1 = __expf(sm.G[i * kG + d0 + j + 1]);
+          float2 ka = *reinterpret_cast<const float2*>(p.dKa + off + j);
+          ka.x += bi * ck[n][2 * hr] * e0;
+          ka.y += bi * ck[n][2 * hr + 1] * e1;
+          *reinterpret_cast<float2*>(p.dKa + off + j) = ka;
+          float2 ga = *reinterpret_cast<const float2*>(p.dgam + off + j);
+          ga.x += bi * ck[n][2 * hr] * kb.x;
+          ga.y += bi * ck[n][2 * hr + 1] * kb.y;
+          *reinterpret_cast<float2*>(p.dgam + off + j) = ga;
+        }
+      }
+    }
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const float v_ = quad_sum(rv[hr]), k_ = quad_sum(rk[hr]);
+      if ((lane & 3) == 0) atomicAdd(&sm.dbs[i], v_ + k_);
+    }
+  }
+  __syncthreads();
+  if (tid < len) p.dbeta[(size_t)(t0 + tid) * p.nh + h] = sm.dbs[tid];
+}
+
+// ============================================================== Kimi Delta backward: the per-channel decay terms
+// The gradients that pass through e^(gamma_ic - gamma_jc) inside the masked
+// q.k block (N = its gradient) and A (M = diag(beta) dA):
+//     a_ic = sum_{j<=i} N_ij k_jc E_ijc     m_ic = sum_{j<i} M_ij k_jc E_ijc
+//     b_jc = sum_{i>=j} N_ij q_ic E_ijc     n_jc = sum_{i>j} M_ij k_ic E_ijc
+// with E_ijc = e^(gamma_ic - gamma_jc) <= 1 (fp32, exponent computed per term);
+// then the final dq = dQa + a, dk = dKa + b + m + n and
+// dgam += q o a - k o b + k o m - k o n, dg = reverse running sum of dgam over
+// the chunk.  Thread (c, I) = (channel tid % 128, 16-row block tid / 128)
+// computes rows 16 I .. 16 I + 15 of channel c: the long i-sums of the low
+// blocks balance the long j-sums of the high ones.
+struct KdaExpSmem {
+  float N[kC * kSF];
+  float M[kC * kSF];
+  __nv_bfloat16 K[kC * kS128];
+  __nv_bfloat16 Q[kC * kS128];
+  float G[kC * kG];  // gamma per channel, then dgam
+};
+static_assert(sizeof(KdaExpSmem) <= 113 * 1024, "two CTAs per SM");
+
+__global__ void __launch_bounds__(kLocalThreads, 2) kda_bwd_exp_kernel(GdnParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  KdaExpSmem& sm = *reinterpret_cast<KdaExpSmem*>(smem_raw);
+  constexpr int nt = kLocalThreads;
+  grid_dependency_wait();
+  const int ci = blockIdx.x, h = blockIdx.y;
+  const int n_chunks = __ldcg(p.hdr);
+  const int4 ch = p.chunks[ci];
+  if (ci >= n_chunks) return;
+  const int len = chunk_len(ch, p.total);
+  if (len <= 0) return;  // only with a boundary list that breaks its rules
+  const int t0 = ch.x;
+  const int tid = threadIdx.x;
+  load_rows128(smem_u32(sm.K), p.k, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(sm.Q), p.q, t0, len, h, p.nh, tid, nt);
+  for (int e = tid; e < kC * 32; e += nt) {
+    const int r = e >> 5, cc = (e & 31) * 4;
+    const bool ok = r < len;
+    cp_async16(smem_u32(&sm.G[r * kG + cc]), p.g + ((size_t)(t0 + (ok ? r : 0)) * p.nh + h) * kD + cc, ok);
+  }
+  cp_async_commit();
+  {
+    const size_t base = ((size_t)ci * p.nh + h) * (kC * kC);
+    for (int e = tid; e < kC * kC; e += nt) {
+      const int i = e >> 6, j = e & 63;
+      sm.N[i * kSF + j] = p.Nw[base + e];
+      sm.M[i * kSF + j] = p.Mw[base + e];
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  if (tid < kD) {
+    float acc = 0.f;
+    for (int i = 0; i < kC; ++i) {
+      acc += sm.G[i * kG + tid];
+      sm.G[i * kG + tid] = acc;
+    }
+  }
+  __syncthreads();
+  const int c = tid & (kD - 1), I = tid >> 7;
+  auto kf = [&](int r) { return __bfloat162float(sm.K[r * kS128 + c]); };
+  auto qf = [&](int r) { return __bfloat162float(sm.Q[r * kS128 + c]); };
+  float tk[16], tg[16];
+  // rows i of block I: a_i (-> dq) and m_i
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int i = 16 * I + r;
+    const float gi = sm.G[i * kG + c];
+    float a = 0.f, m = 0.f;
+    for (int j = 0; j <= i; ++j) {
+      const float w = kf(j) * __expf(gi - sm.G[j * kG + c]);
+      a = fmaf(sm.N[i * kSF + j], w, a);
+      m = fmaf(sm.M[i * kSF + j], w, m);
+    }
+    tk[r] = m;
+    tg[r] = qf(i) * a + kf(i) * m;
+    if (i < len) {
+      const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + c;
+      p.dq[off] = __float2bfloat16_rn(p.dQa[off] + a);
+    }
+  }
+  // rows j of block I: b_j and n_j, then dk and dgam
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int j = 16 * I + r;
+    const float gj = sm.G[j * kG + c];
+    float b = 0.f, n = 0.f;
+    for (int i = j; i < kC; ++i) {
+      const float e = __expf(sm.G[i * kG + c] - gj);
+      b = fmaf(sm.N[i * kSF + j], qf(i) * e, b);
+      n = fmaf(sm.M[i * kSF + j], kf(i) * e, n);
+    }
+    float dgj = 0.f;
+    if (j < len) {
+      const size_t off = ((size_t)(t0 + j) * p.nh + h) * kD + c;
+      p.dk[off] = __float2bfloat16_rn(p.dKa[off] + tk[r] + b + n);
+      dgj = p.dgam[off] + tg[r] - kf(j) * (b + n);
+    }
+    tg[r] = dgj;
+  }
+  __syncthreads();  // gamma no longer read: dgam goes in its place
+#pragma unroll
+  for (int r = 0; r < 16; ++r) sm.G[(16 * I + r) * kG + c] = tg[r];
+  __syncthreads();
+  if (tid < kD) {
+    float acc = 0.f;
+    for (int i = kC - 1; i >= 0; --i) {
+      acc += sm.G[i * kG + tid];
+      if (i < len) p.dg[((size_t)(t0 + i) * p.nh + h) * kD + tid] = acc;
+    }
+  }
+}
+
 }  // namespace
 
 // Workspace layout: offsets off[0..6] of the forward's regions (header,
 // chunk table, segment table, W, U, Aqk, gamma); with bwd, off[7..13] of the
 // backward's (H0, dH1, E, dE, dW, dKa, dgam); with kda (a decay per channel),
-// off[14..16] (QB, KC, e^gamma_last).  Returns the total size.
-size_t gdn_workspace_layout(int64_t total, int nh, int nseg, size_t off[17], bool bwd, bool kda = false) {
+// off[14..16] (QB, KC, e^gamma_last), and with both off[17..22] (X, A
+// unscaled, N, M, dQa, dgam per channel).  Returns the total size.
+size_t gdn_workspace_layout(int64_t total, int nh, int nseg, size_t off[23], bool bwd, bool kda = false) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t max_chunks = (size_t)(total / kC) + (size_t)nseg + 1;
   const size_t tok = (size_t)total * nh * kD;  // elements of a [T, H, 128] tensor
@@ -1744,6 +2336,15 @@ size_t gdn_workspace_layout(int64_t total, int nh, int nseg, size_t off[17], boo
     off[14] = o; o += up(tok * 2);                           // QB
     off[15] = o; o += up(tok * 2);                           // KC
     off[16] = o; o += up(max_chunks * nh * kD * sizeof(float)); // e^gamma_last per chunk and channel
+    if (bwd) {
+      const size_t blk = up(max_chunks * nh * kC * kC * sizeof(float));
+      off[17] = o; o += blk;                                 // X
+      off[18] = o; o += blk;                                 // A unscaled
+      off[19] = o; o += blk;                                 // N
+      off[20] = o; o += blk;                                 // M
+      off[21] = o; o += up(tok * 4);                         // dQa
+      off[22] = o; o += up(tok * 4);                         // dgam per channel
+    }
   }
   return o;
 }
@@ -1764,7 +2365,7 @@ int gdn_setup(GdnParams& p, const void* q, const void* k, const void* v, const f
   for (const void* x : ptrs)
     if (reinterpret_cast<uintptr_t>(x) & 15u) return ATTN_ERR_ALIGNMENT;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGNMENT;
-  size_t off[17];
+  size_t off[23];
   if (workspace_bytes < gdn_workspace_layout(total, num_heads, num_segments, off, bwd, kda)) return ATTN_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p = GdnParams{};
@@ -1799,6 +2400,14 @@ int gdn_setup(GdnParams& p, const void* q, const void* k, const void* v, const f
     p.QB = reinterpret_cast<__nv_bfloat16*>(ws + off[14]);
     p.KC = reinterpret_cast<__nv_bfloat16*>(ws + off[15]);
     p.Bc = reinterpret_cast<float*>(ws + off[16]);
+    if (bwd) {
+      p.Xw = reinterpret_cast<float*>(ws + off[17]);
+      p.Araw = reinterpret_cast<float*>(ws + off[18]);
+      p.Nw = reinterpret_cast<float*>(ws + off[19]);
+      p.Mw = reinterpret_cast<float*>(ws + off[20]);
+      p.dQa = reinterpret_cast<float*>(ws + off[21]);
+      p.dgam = reinterpret_cast<float*>(ws + off[22]);
+    }
   }
   return ATTN_OK;
 }
@@ -1817,11 +2426,12 @@ cudaError_t launch_gdn_prep(const GdnParams& p, cudaStream_t s) {
 // The planner and the per-chunk factors with a decay per channel.
 cudaError_t launch_kda_prep(const GdnParams& p, cudaStream_t s) {
   cudaError_t e = launch_pdl(gdn_plan_kernel, dim3(1), dim3(256), 0, s, p);
+  auto kern = p.Xw ? kda_prep_kernel<true> : kda_prep_kernel<false>;
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(KdaPrepSmem));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(KdaPrepSmem));
   if (e == cudaSuccess)
-    e = launch_pdl(kda_prep_kernel, dim3((unsigned)p.max_chunks, (unsigned)p.nh), dim3(kGdnThreads),
-                   sizeof(KdaPrepSmem), s, p);
+    e = launch_pdl(kern, dim3((unsigned)p.max_chunks, (unsigned)p.nh), dim3(kGdnThreads), sizeof(KdaPrepSmem), s,
+                   p);
   return e;
 }
 
@@ -1839,13 +2449,13 @@ extern "C" {
 
 size_t gdn_varlen_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments) {
   if (total < 0 || num_heads <= 0 || num_segments < 0 || total > (1LL << 30) || num_heads > 1024) return 0;
-  size_t off[17];
+  size_t off[23];
   return vsw::gdn_workspace_layout(total, num_heads, num_segments, off, false);
 }
 
 size_t gdn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments) {
   if (total < 0 || num_heads <= 0 || num_segments < 0 || total > (1LL << 30) || num_heads > 1024) return 0;
-  size_t off[17];
+  size_t off[23];
   return vsw::gdn_workspace_layout(total, num_heads, num_segments, off, true);
 }
 
@@ -1900,7 +2510,7 @@ int gdn_varlen_bwd(const void* q, const void* k, const void* v, const float* g, 
   const dim3 chunk_grid((unsigned)p.max_chunks, (unsigned)num_heads);
   cudaError_t e = launch_gdn_prep(p, s);
   if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<true, false>, seg_grid, s, p);
-  if (e == cudaSuccess) e = launch_big<BwdStateSmem>(gdn_bwd_state_kernel, seg_grid, s, p);
+  if (e == cudaSuccess) e = launch_big<BwdStateSmem>(gdn_bwd_state_kernel<false>, seg_grid, s, p);
   if (e == cudaSuccess) e = launch_big<LocalHSmem>(gdn_bwd_local_h_kernel, chunk_grid, s, p, kLocalThreads);
   if (e == cudaSuccess) e = launch_big<LocalWySmem>(gdn_bwd_local_wy_kernel, chunk_grid, s, p, kLocalThreads);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -1908,7 +2518,7 @@ int gdn_varlen_bwd(const void* q, const void* k, const void* v, const float* g, 
 
 size_t kda_varlen_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments) {
   if (total < 0 || num_heads <= 0 || num_segments < 0 || total > (1LL << 30) || num_heads > 1024) return 0;
-  size_t off[17];
+  size_t off[23];
   return vsw::gdn_workspace_layout(total, num_heads, num_segments, off, false, true);
 }
 
@@ -1931,6 +2541,48 @@ int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* g, 
   cudaError_t e = launch_kda_prep(p, s);
   const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
   if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<false, true>, seg_grid, s, p);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t kda_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments) {
+  if (total < 0 || num_heads <= 0 || num_segments < 0 || total > (1LL << 30) || num_heads > 1024) return 0;
+  size_t off[23];
+  return vsw::gdn_workspace_layout(total, num_heads, num_segments, off, true, true);
+}
+
+int kda_varlen_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, const void* d_o,
+                   const int32_t* cu_seqlens, float scale, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                   void* workspace, size_t workspace_bytes, int64_t total, int32_t num_heads, int32_t head_dim,
+                   int32_t num_segments, void* stream) {
+  using namespace vsw;
+  GdnParams p;
+  int rc = gdn_setup(p, q, k, v, g, beta, cu_seqlens, scale, workspace, workspace_bytes, total, num_heads, head_dim,
+                     num_segments, true, true);
+  if (rc) return rc;
+  const void* outs[] = {d_o, dq, dk, dv, dg, dbeta};
+  for (const void* x : outs)
+    if (!x) return ATTN_ERR_NULL_POINTER;
+  for (const void* x : outs)
+    if (reinterpret_cast<uintptr_t>(x) & 15u) return ATTN_ERR_ALIGNMENT;
+  int* status = nullptr;
+  int sms = 0;
+  if ((rc = device_for_call(&status, &sms))) return rc;
+  if (total == 0) return ATTN_OK;
+  p.dO = static_cast<const __nv_bfloat16*>(d_o);
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dg = dg;
+  p.dbeta = dbeta;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
+  const dim3 chunk_grid((unsigned)p.max_chunks, (unsigned)num_heads);
+  cudaError_t e = launch_kda_prep(p, s);
+  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<true, true>, seg_grid, s, p);
+  if (e == cudaSuccess) e = launch_big<BwdStateSmem>(gdn_bwd_state_kernel<true>, seg_grid, s, p);
+  if (e == cudaSuccess) e = launch_big<KdaLocalHSmem>(kda_bwd_local_h_kernel, chunk_grid, s, p, kLocalThreads);
+  if (e == cudaSuccess) e = launch_big<KdaLocalWySmem>(kda_bwd_local_wy_kernel, chunk_grid, s, p, kLocalThreads);
+  if (e == cudaSuccess) e = launch_big<KdaExpSmem>(kda_bwd_exp_kernel, chunk_grid, s, p, kLocalThreads);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
