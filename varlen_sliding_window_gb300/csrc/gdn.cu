@@ -2194,23 +2194,28 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_wy_kernel(GdnPara
 // The gradients that pass through e^(gamma_ic - gamma_jc) inside the masked
 // q.k block (N = its gradient) and A (M = diag(beta) dA):
 //     a_ic = sum_{j<=i} N_ij k_jc E_ijc     m_ic = sum_{j<i} M_ij k_jc E_ijc
-//     b_jc = sum_{i>=j} N_ij q_ic E_ijc     n_jc = sum_{i>j} M_ij k_ic E_ijc
-// with E_ijc = e^(gamma_ic - gamma_jc) <= 1 (fp32, exponent computed per term);
-// then the final dq = dQa + a, dk = dKa + b + m + n and
-// dgam += q o a - k o b + k o m - k o n, dg = reverse running sum of dgam over
-// the chunk.  Thread (c, I) = (channel tid % 128, 16-row block tid / 128)
-// computes rows 16 I .. 16 I + 15 of channel c: the long i-sums of the low
-// blocks balance the long j-sums of the high ones.
+//     b_jc = sum_{i>=j} N_ij q_ic E_ijc     n_jc = sum_{i>j} M_ij k_ic E_ijc,
+// E_ijc = e^(gamma_ic - gamma_jc); then the final dq = dQa + a,
+// dk = dKa + b + m + n, dgam += q o a - k o b + k o m - k o n and
+// dg = reverse running sum of dgam over the chunk.  The exponent is split at
+// the first row r of i's 16-row block I, as in the forward's prep:
+//     a_I = e^(gamma_I - gamma_r) o (N_I. KI_I),   KI_I = K_j o e^(gamma_r - gamma_j)
+//     b_J = sum_{I >= J} e^(gamma_r - gamma_J) o (N_IJ^T (Q_I o e^(gamma_I - gamma_r)))
+// (and m, n with M and K), so every sum is a matrix product.  Warp w owns rows
+// [16 (w % 4), +16) x channels [32 (w / 4), +32) of a, m, b and n.
 struct KdaExpSmem {
-  float N[kC * kSF];
-  float M[kC * kSF];
+  __nv_bfloat16 N[kC * kS64];
+  __nv_bfloat16 M[kC * kS64];
   __nv_bfloat16 K[kC * kS128];
   __nv_bfloat16 Q[kC * kS128];
-  float G[kC * kG];  // gamma per channel, then dgam
+  __nv_bfloat16 KBr[kC * kS128];   // K o e^(gamma - gamma_r)
+  __nv_bfloat16 QBr[kC * kS128];   // Q o e^(gamma - gamma_r)
+  __nv_bfloat16 KI[160 * kS128];   // per row block I: K_j o e^(gamma_rI - gamma_j), j < 16 (I + 1)
+  float G[kC * kG];                // gamma per channel, then dgam
 };
-static_assert(sizeof(KdaExpSmem) <= 113 * 1024, "two CTAs per SM");
+static_assert(sizeof(KdaExpSmem) <= 227 * 1024, "fits one SM");
 
-__global__ void __launch_bounds__(kLocalThreads, 2) kda_bwd_exp_kernel(GdnParams p) {
+__global__ void __launch_bounds__(kLocalThreads) kda_bwd_exp_kernel(GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   KdaExpSmem& sm = *reinterpret_cast<KdaExpSmem*>(smem_raw);
   constexpr int nt = kLocalThreads;
@@ -2222,7 +2227,9 @@ __global__ void __launch_bounds__(kLocalThreads, 2) kda_bwd_exp_kernel(GdnParams
   const int len = chunk_len(ch, p.total);
   if (len <= 0) return;  // only with a boundary list that breaks its rules
   const int t0 = ch.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t sN = smem_u32(sm.N), sM = smem_u32(sm.M), sKBr = smem_u32(sm.KBr), sQBr = smem_u32(sm.QBr),
+                 sKI = smem_u32(sm.KI);
   load_rows128(smem_u32(sm.K), p.k, t0, len, h, p.nh, tid, nt);
   load_rows128(smem_u32(sm.Q), p.q, t0, len, h, p.nh, tid, nt);
   for (int e = tid; e < kC * 32; e += nt) {
@@ -2233,10 +2240,12 @@ __global__ void __launch_bounds__(kLocalThreads, 2) kda_bwd_exp_kernel(GdnParams
   cp_async_commit();
   {
     const size_t base = ((size_t)ci * p.nh + h) * (kC * kC);
-    for (int e = tid; e < kC * kC; e += nt) {
-      const int i = e >> 6, j = e & 63;
-      sm.N[i * kSF + j] = p.Nw[base + e];
-      sm.M[i * kSF + j] = p.Mw[base + e];
+    for (int e = tid; e < kC * kC / 2; e += nt) {
+      const int i = e >> 5, j = (e & 31) * 2;
+      const float2 nv = *reinterpret_cast<const float2*>(p.Nw + base + i * kC + j);
+      const float2 mv = *reinterpret_cast<const float2*>(p.Mw + base + i * kC + j);
+      *reinterpret_cast<uint32_t*>(&sm.N[i * kS64 + j]) = pack2(nv.x, nv.y);
+      *reinterpret_cast<uint32_t*>(&sm.M[i * kS64 + j]) = pack2(mv.x, mv.y);
     }
   }
   cp_async_wait<0>();
@@ -2249,50 +2258,105 @@ __global__ void __launch_bounds__(kLocalThreads, 2) kda_bwd_exp_kernel(GdnParams
     }
   }
   __syncthreads();
-  const int c = tid & (kD - 1), I = tid >> 7;
-  auto kf = [&](int r) { return __bfloat162float(sm.K[r * kS128 + c]); };
-  auto qf = [&](int r) { return __bfloat162float(sm.Q[r * kS128 + c]); };
-  float tk[16], tg[16];
-  // rows i of block I: a_i (-> dq) and m_i
+  for (int e = tid; e < kC * kD / 2; e += nt) {
+    const int i = e >> 6, cc = (e & 63) * 2;
+    const int r = i & ~15;
+    const float f0 = __expf(sm.G[i * kG + cc] - sm.G[r * kG + cc]);
+    const float f1 = __expf(sm.G[i * kG + cc + 1] - sm.G[r * kG + cc + 1]);
+    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[i * kS128 + cc]));
+    const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.Q[i * kS128 + cc]));
+    *reinterpret_cast<uint32_t*>(&sm.KBr[i * kS128 + cc]) = pack2(kv.x * f0, kv.y * f1);
+    *reinterpret_cast<uint32_t*>(&sm.QBr[i * kS128 + cc]) = pack2(qv.x * f0, qv.y * f1);
+  }
+  for (int e = tid; e < 160 * kD / 2; e += nt) {
+    const int row = e >> 6, cc = (e & 63) * 2;
+    const int I = row < 16 ? 0 : (row < 48 ? 1 : (row < 96 ? 2 : 3));
+    const int j = row - ki_row0(I), r = 16 * I;
+    const float f0 = __expf(sm.G[r * kG + cc] - sm.G[j * kG + cc]);
+    const float f1 = __expf(sm.G[r * kG + cc + 1] - sm.G[j * kG + cc + 1]);
+    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[j * kS128 + cc]));
+    *reinterpret_cast<uint32_t*>(&sm.KI[row * kS128 + cc]) = pack2(kv.x * f0, kv.y * f1);
+  }
+  __syncthreads();
+  const int R = warp & 3, r0 = 16 * R, c0 = 32 * (warp >> 2);
+  float pa[4][4], pm[4][4], pb[4][4], pn[4][4];
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int i = 16 * I + r;
-    const float gi = sm.G[i * kG + c];
-    float a = 0.f, m = 0.f;
-    for (int j = 0; j <= i; ++j) {
-      const float w = kf(j) * __expf(gi - sm.G[j * kG + c]);
-      a = fmaf(sm.N[i * kSF + j], w, a);
-      m = fmaf(sm.M[i * kSF + j], w, m);
-    }
-    tk[r] = m;
-    tg[r] = qf(i) * a + kf(i) * m;
-    if (i < len) {
-      const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + c;
-      p.dq[off] = __float2bfloat16_rn(p.dQa[off] + a);
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pa[n][e] = pm[n][e] = pb[n][e] = pn[n][e] = 0.f;
+  // a, m: rows of block R against KI_R (columns j < 16 (R + 1))
+  for (int J = 0; J <= R; ++J) {
+    uint32_t an[4], am[4];
+    ldsm_x4(an, frag_a(sN, kS64, r0, 16 * J, lane));
+    ldsm_x4(am, frag_a(sM, kS64, r0, 16 * J, lane));
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      uint32_t b[4];
+      ldsm_x4_t(b, frag_b(sKI, kS128, ki_row0(R) + 16 * J, c0 + 16 * np, lane));
+      mma_bf16(pa[2 * np], an, b[0], b[1]);
+      mma_bf16(pa[2 * np + 1], an, b[2], b[3]);
+      mma_bf16(pm[2 * np], am, b[0], b[1]);
+      mma_bf16(pm[2 * np + 1], am, b[2], b[3]);
     }
   }
-  // rows j of block I: b_j and n_j, then dk and dgam
+  // b, n: columns j of block R, from every row block I >= R, each with its own reference
+  for (int I = R; I < 4; ++I) {
+    float tb[4][4], tn[4][4];
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int j = 16 * I + r;
-    const float gj = sm.G[j * kG + c];
-    float b = 0.f, n = 0.f;
-    for (int i = j; i < kC; ++i) {
-      const float e = __expf(sm.G[i * kG + c] - gj);
-      b = fmaf(sm.N[i * kSF + j], qf(i) * e, b);
-      n = fmaf(sm.M[i * kSF + j], kf(i) * e, n);
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) tb[n][e] = tn[n][e] = 0.f;
+    uint32_t an[4], am[4];
+    ldsm_x4_t(an, frag_bt(sN, kS64, 16 * I, r0, lane));  // N_IR^T: N stored [i][j]
+    ldsm_x4_t(am, frag_bt(sM, kS64, 16 * I, r0, lane));
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      uint32_t bq[4], bk[4];
+      ldsm_x4_t(bq, frag_b(sQBr, kS128, 16 * I, c0 + 16 * np, lane));
+      ldsm_x4_t(bk, frag_b(sKBr, kS128, 16 * I, c0 + 16 * np, lane));
+      mma_bf16(tb[2 * np], an, bq[0], bq[1]);
+      mma_bf16(tb[2 * np + 1], an, bq[2], bq[3]);
+      mma_bf16(tn[2 * np], am, bk[0], bk[1]);
+      mma_bf16(tn[2 * np + 1], am, bk[2], bk[3]);
     }
-    float dgj = 0.f;
-    if (j < len) {
-      const size_t off = ((size_t)(t0 + j) * p.nh + h) * kD + c;
-      p.dk[off] = __float2bfloat16_rn(p.dKa[off] + tk[r] + b + n);
-      dgj = p.dgam[off] + tg[r] - kf(j) * (b + n);
-    }
-    tg[r] = dgj;
+    const int rI = 16 * I;
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = r0 + (lane >> 2) + 8 * (e >> 1);
+        const int cc = c0 + 8 * n + 2 * (lane & 3) + (e & 1);
+        const float f = __expf(sm.G[rI * kG + cc] - sm.G[j * kG + cc]);
+        pb[n][e] = fmaf(f, tb[n][e], pb[n][e]);
+        pn[n][e] = fmaf(f, tn[n][e], pn[n][e]);
+      }
   }
+  // epilogue: this thread's (row, channel) elements
+  float dgv[4][4];
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = r0 + (lane >> 2) + 8 * (e >> 1);
+      const int cc = c0 + 8 * n + 2 * (lane & 3) + (e & 1);
+      const float f = __expf(sm.G[i * kG + cc] - sm.G[r0 * kG + cc]);
+      const float a = f * pa[n][e], m = f * pm[n][e], b = pb[n][e], nn = pn[n][e];
+      const float kv = __bfloat162float(sm.K[i * kS128 + cc]), qv = __bfloat162float(sm.Q[i * kS128 + cc]);
+      float dgi = 0.f;
+      if (i < len) {
+        const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + cc;
+        p.dq[off] = __float2bfloat16_rn(p.dQa[off] + a);
+        p.dk[off] = __float2bfloat16_rn(p.dKa[off] + b + m + nn);
+        dgi = p.dgam[off] + qv * a + kv * (m - b - nn);
+      }
+      dgv[n][e] = dgi;
+    }
   __syncthreads();  // gamma no longer read: dgam goes in its place
 #pragma unroll
-  for (int r = 0; r < 16; ++r) sm.G[(16 * I + r) * kG + c] = tg[r];
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      sm.G[(r0 + (lane >> 2) + 8 * (e >> 1)) * kG + c0 + 8 * n + 2 * (lane & 3) + (e & 1)] = dgv[n][e];
   __syncthreads();
   if (tid < kD) {
     float acc = 0.f;
