@@ -531,10 +531,10 @@ __device__ __forceinline__ int ki_row0(int I) { return 8 * I * (I + 1); }
 
 // kBwd (the backward's recomputation) also stores X and the unscaled A.
 template <bool kBwd>
-__global__ void __launch_bounds__(kGdnThreads) kda_prep_kernel(GdnParams p) {
+__global__ void __launch_bounds__(kLocalThreads) kda_prep_kernel(GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   KdaPrepSmem& sm = *reinterpret_cast<KdaPrepSmem*>(smem_raw);
-  constexpr int nt = kGdnThreads;
+  constexpr int nt = kLocalThreads;
   grid_dependency_wait();
   const int c = blockIdx.x, h = blockIdx.y;
   const int n_chunks = __ldcg(p.hdr);
@@ -588,9 +588,9 @@ __global__ void __launch_bounds__(kGdnThreads) kda_prep_kernel(GdnParams p) {
     *reinterpret_cast<uint32_t*>(&sm.KI[row * kS128 + cc]) = pack2(kv.x * f0, kv.y * f1);
   }
   __syncthreads();
-  // ---- the 10 blocks (I, J <= I) of 16 x 16: A and Aqk; warp w takes blocks w and w + 8
+  // ---- the 10 blocks (I, J <= I) of 16 x 16: A and Aqk; warp w < 10 takes block w
   __nv_bfloat16* aqk = p.Aqk + ((size_t)c * p.nh + h) * (kC * kC);
-  for (int bl = warp; bl < 10; bl += 8) {
+  for (int bl = warp; bl < 10; bl += nt / 32) {
     const int I = bl < 1 ? 0 : (bl < 3 ? 1 : (bl < 6 ? 2 : 3));
     const int J = bl - I * (I + 1) / 2;
     float sa[2][4], sq[2][4];
@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(kGdnThreads) kda_prep_kernel(GdnParams p) {
     if (kBwd) p.Araw[((size_t)c * p.nh + h) * (kC * kC) + i * kC + j] = 0.f;
   }
   __syncthreads();
-  wy_inverse(sm.A, sm.X, sm.R, tid);
+  wy_inverse<kSF, kLocalThreads>(sm.A, sm.X, sm.R, tid);
   if (kBwd) {
     float* xw = p.Xw + ((size_t)c * p.nh + h) * (kC * kC);
     for (int e = tid; e < kC * kC; e += nt) xw[e] = sm.X[(e >> 6) * kSF + (e & 63)];
@@ -672,11 +672,11 @@ __global__ void __launch_bounds__(kGdnThreads) kda_prep_kernel(GdnParams p) {
   }
   if (tid < kD) p.Bc[((size_t)c * p.nh + h) * kD + tid] = __expf(sm.G[last * kG + tid]);
   __syncthreads();
-  // ---- W = T2 (K o e^gamma), U = T2 V: warp w rows [16 (w % 4), +16) x columns [64 (w / 4), +64)
-  const int r0 = 16 * (warp & 3), d0 = 64 * (warp >> 2);
-  float cw[8][4], cu[8][4];
+  // ---- W = T2 (K o e^gamma), U = T2 V: warp w rows [16 (w % 4), +16) x columns [32 (w / 4), +32)
+  const int r0 = 16 * (warp & 3), d0 = 32 * (warp >> 2);
+  float cw[4][4], cu[4][4];
 #pragma unroll
-  for (int n = 0; n < 8; ++n)
+  for (int n = 0; n < 4; ++n)
 #pragma unroll
     for (int e = 0; e < 4; ++e) cw[n][e] = cu[n][e] = 0.f;
   const uint32_t sT2 = smem_u32(sm.T2);
@@ -685,7 +685,7 @@ __global__ void __launch_bounds__(kGdnThreads) kda_prep_kernel(GdnParams p) {
     uint32_t a[4];
     ldsm_x4(a, frag_a(sT2, kS64, r0, 16 * kk, lane));
 #pragma unroll
-    for (int np = 0; np < 4; ++np) {
+    for (int np = 0; np < 2; ++np) {
       uint32_t bk[4], bv[4];
       ldsm_x4_t(bk, frag_b(sKB, kS128, 16 * kk, d0 + 16 * np, lane));
       ldsm_x4_t(bv, frag_b(sV, kS128, 16 * kk, d0 + 16 * np, lane));
@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(kGdnThreads) kda_prep_kernel(GdnParams p) {
   }
   __syncthreads();  // K, V no longer read: stage W in K's place, U in V's
 #pragma unroll
-  for (int n = 0; n < 8; ++n)
+  for (int n = 0; n < 4; ++n)
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int i = r0 + (lane >> 2) + 8 * hr;
@@ -2494,7 +2494,7 @@ cudaError_t launch_kda_prep(const GdnParams& p, cudaStream_t s) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(KdaPrepSmem));
   if (e == cudaSuccess)
-    e = launch_pdl(kern, dim3((unsigned)p.max_chunks, (unsigned)p.nh), dim3(kGdnThreads), sizeof(KdaPrepSmem), s,
+    e = launch_pdl(kern, dim3((unsigned)p.max_chunks, (unsigned)p.nh), dim3(kLocalThreads), sizeof(KdaPrepSmem), s,
                    p);
   return e;
 }
