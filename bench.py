@@ -770,9 +770,43 @@ def main():
             bwd()
             evs[i][3].record(stream)
         torch.cuda.synchronize()
-        status = binding.attn_varlen_get_status()
         f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
         b_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+        # The same step captured in a CUDA graph over the boundary list padded
+        # with empty segments to 42 (the page replays these layers too, section
+        # 06): replay time, and its outputs against the eager step's bits.
+        graph_res = None
+        if nseg <= 42:
+            ref = [x.clone() for x in (o, dq, dk, dv, dg, db)]
+            cu_pad = torch.from_numpy(synth.pad_cu_seqlens(gi.cu_seqlens, 42)).to(dev)
+            ws_pad = torch.empty(f_ws(gw.total, gw.nh, 42), dtype=torch.uint8, device=dev)
+
+            def padded():
+                f_fwd(q, k, v, g_, be, cu_pad, gw.scale, o, ws_pad)
+                f_bwd(q, k, v, g_, be, do, cu_pad, gw.scale, dq, dk, dv, dg, db, ws_pad)
+
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                padded()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                padded()
+            graph.replay()
+            torch.cuda.synchronize()
+            exact = all(torch.equal(a, b) for a, b in zip(ref, (o, dq, dk, dv, dg, db)))
+            gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+            for i in range(steps):
+                flush.fill_(float(i))
+                gev[i][0].record(stream)
+                graph.replay()
+                gev[i][1].record(stream)
+            torch.cuda.synchronize()
+            graph_res = {"ms": statistics.mean(e[0].elapsed_time(e[1]) for e in gev), "eager_ms": f_ms + b_ms,
+                         "pad_segments": 42, "bit_exact_vs_eager_unpadded": exact}
+            del graph, ws_pad
+        status = binding.attn_varlen_get_status()
         ff, fb = gdn_flops(gi.cu_seqlens, gw.nh, gw.d, gw.per_channel)
         tok = gw.total * gw.nh * gw.d * 2
         gates = gw.total * gw.nh * 4 * (gw.d if gw.per_channel else 1)
@@ -794,6 +828,7 @@ def main():
                                   "what": f"the page's {layer} layer fwd+bwd per step at context 4,096 on its "
                                           "own unnamed GPU (research.dws.rip/llm/kernels, Fig. 5)"}
                                  if gw.context == 4096 else None),
+                "graph": graph_res,
                 "status": status}
 
     gdn = {}

@@ -135,3 +135,77 @@ def test_backward_matches_oracle(name):
     for nm, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), got, ref):
         assert errs[nm] <= TOL_GRAD[nm], (nm, errs[nm])
         assert_per_segment(a, b, inp.cu_seqlens, TOL_GRAD[nm], nm)
+
+
+def _graph_replay_is_bit_exact(wls, name, per_channel):
+    """Forward + backward captured once in a CUDA graph over a boundary list
+    padded with empty segments to 42 (research.dws.rip/llm/kernels, section
+    06), replayed on three microbatches with different boundaries: every output
+    bit-equal to eager calls on the unpadded boundaries."""
+    import torch
+    from varlen_sliding_window_gb300 import binding
+    w = wls[name]
+    f_fwd, f_bwd, f_ws = ((binding.kda_varlen_fwd, binding.kda_varlen_bwd, binding.kda_varlen_bwd_workspace_bytes)
+                          if per_channel else
+                          (binding.gdn_varlen_fwd, binding.gdn_varlen_bwd, binding.gdn_varlen_bwd_workspace_bytes))
+    cus = [synth.pack_microbatch(w.total, w.context, sd) for sd in (0, 1, 2)]
+    nseg = 42
+    assert max(len(c) - 1 for c in cus) <= nseg
+    batches = [synth.make_gdn_inputs(c, w.nh, w.d, 10 + i, per_channel) for i, c in enumerate(cus)]
+    T, nh = w.total, w.nh
+    st = {"q": torch.empty(T, nh, w.d, dtype=torch.bfloat16, device="cuda")}
+    for n in ("k", "v", "do", "o", "dq", "dk", "dv"):
+        st[n] = torch.empty_like(st["q"])
+    gshape = (T, nh, w.d) if per_channel else (T, nh)
+    for n in ("g", "dg"):
+        st[n] = torch.empty(gshape, dtype=torch.float32, device="cuda")
+    for n in ("beta", "dbeta"):
+        st[n] = torch.empty(T, nh, dtype=torch.float32, device="cuda")
+    st["cu"] = torch.empty(nseg + 1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(f_ws(T, nh, nseg), dtype=torch.uint8, device="cuda")
+
+    def load(b, cu):
+        for n, bits in (("q", b.q_bits), ("k", b.k_bits), ("v", b.v_bits), ("do", b.do_bits)):
+            st[n].copy_(_to_dev(bits))
+        st["g"].copy_(torch.from_numpy(b.g))
+        st["beta"].copy_(torch.from_numpy(b.beta))
+        st["cu"].copy_(torch.from_numpy(synth.pad_cu_seqlens(cu, nseg)))
+
+    def step():
+        f_fwd(st["q"], st["k"], st["v"], st["g"], st["beta"], st["cu"], w.scale, st["o"], ws)
+        f_bwd(st["q"], st["k"], st["v"], st["g"], st["beta"], st["do"], st["cu"], w.scale, st["dq"], st["dk"],
+              st["dv"], st["dg"], st["dbeta"], ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    load(batches[0], cus[0])
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        step()
+    names = ("o", "dq", "dk", "dv", "dg", "dbeta")
+    for b, cu in zip(batches, cus):
+        load(b, cu)
+        graph.replay()
+        torch.cuda.synchronize()
+        got = {n: st[n].clone() for n in names}
+        # eager, unpadded boundaries, own buffers
+        e = {n: torch.empty_like(st[n]) for n in names}
+        cu_t = torch.from_numpy(cu).cuda()
+        ws2 = torch.empty(f_ws(T, nh, len(cu) - 1), dtype=torch.uint8, device="cuda")
+        f_fwd(st["q"], st["k"], st["v"], st["g"], st["beta"], cu_t, w.scale, e["o"], ws2)
+        f_bwd(st["q"], st["k"], st["v"], st["g"], st["beta"], st["do"], cu_t, w.scale, e["dq"], e["dk"], e["dv"],
+              e["dg"], e["dbeta"], ws2)
+        torch.cuda.synchronize()
+        for n in names:
+            assert torch.equal(got[n], e[n]), n
+    from varlen_sliding_window_gb300 import binding as _b
+    assert _b.attn_varlen_get_status() == 0
+
+
+@pytest.mark.gpu
+def test_cuda_graph_replay_with_padded_boundaries_is_bit_exact():
+    _graph_replay_is_bit_exact(synth.gdn_workloads(), "gdn_ctx4096", False)

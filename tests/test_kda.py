@@ -132,3 +132,9 @@ def test_backward_matches_oracle(name):
     for nm, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), got, ref):
         assert errs[nm] <= TOL_GRAD, (nm, errs[nm])
         assert_per_segment(a, b, inp.cu_seqlens, TOL_GRAD, nm)
+
+
+@pytest.mark.gpu
+def test_cuda_graph_replay_with_padded_boundaries_is_bit_exact():
+    from tests.test_gdn import _graph_replay_is_bit_exact
+    _graph_replay_is_bit_exact(synth.kda_workloads(), "kda_ctx4096", True)

@@ -1146,6 +1146,14 @@ struct LocalHSmem {
   __nv_bfloat16 DG[kC * kS64];
   float gam[kC];
   float dgs[kC];
+  // Partial sums of dgam, one slot per contributing warp group, added in a
+  // fixed order at the end (float atomics would make the bits depend on
+  // timing): [0..3] DG o QK row sums, [4..7] minus its column sums, [8..11]
+  // the dO . Q H0 and E . K dH1 terms; lw: w_i <(K dH1)_i, E_i> per slot; tw:
+  // e^gamma_last <dH1, H0> per warp.
+  float part[12][kC];
+  float lw[4][kC];
+  float tw[kLocalThreads / 32];
   float last;  // the gamma_last terms
 };
 static_assert(sizeof(LocalHSmem) <= 227 * 1024, "fits one SM");
@@ -1193,7 +1201,7 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParam
     sm.gam[tid] = tid < len ? p.gam[(size_t)h * p.total + t0 + tid] : 0.f;
     sm.dgs[tid] = 0.f;
   }
-  if (tid == 0) sm.last = 0.f;
+  for (int e = tid; e < 16 * kC; e += nt) (&sm.part[0][0])[e] = 0.f;  // part and lw
   cp_async_wait<0>();
   __syncthreads();
   const float g_last = sm.gam[len - 1];
@@ -1245,7 +1253,7 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParam
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const float x = quad_sum(rsum[hr]);
-      if ((lane & 3) == 0) atomicAdd(&sm.dgs[r0 + (lane >> 2) + 8 * hr], x);
+      if ((lane & 3) == 0) sm.part[warp >> 2][r0 + (lane >> 2) + 8 * hr] = x;
     }
 #pragma unroll
     for (int n = 0; n < 2; ++n)
@@ -1255,7 +1263,7 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParam
         x += __shfl_xor_sync(0xffffffffu, x, 4);
         x += __shfl_xor_sync(0xffffffffu, x, 8);
         x += __shfl_xor_sync(0xffffffffu, x, 16);
-        if (lane < 4) atomicAdd(&sm.dgs[c0 + 8 * n + 2 * lane + e], -x);
+        if (lane < 4) sm.part[4 + (warp & 3)][c0 + 8 * n + 2 * lane + e] = -x;
       }
   }
   __syncthreads();
@@ -1391,15 +1399,14 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParam
         rq[hr] += acc[n][2 * hr] * dd.x + acc[n][2 * hr + 1] * dd.y;
         rk[hr] += acc2[n][2 * hr] * ee.x + acc2[n][2 * hr + 1] * ee.y;
       }
-    float lastp = 0.f;
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int i = r0 + (lane >> 2) + 8 * hr;
       const float q_ = quad_sum(rq[hr]), k_ = quad_sum(rk[hr]);
       if ((lane & 3) == 0 && i < len) {
         const float w = __expf(g_last - sm.gam[i]);
-        atomicAdd(&sm.dgs[i], p.scale * __expf(sm.gam[i]) * q_ - w * k_);
-        lastp += w * k_;
+        sm.part[8 + (warp >> 2)][i] = p.scale * __expf(sm.gam[i]) * q_ - w * k_;
+        sm.lw[warp >> 2][i] = w * k_;
       }
     }
     // e^gamma_last <dH1, H0>: this thread's share of the 128 x 128 products
@@ -1410,9 +1417,22 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParam
       const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.dH1[rr * kS128 + cc]));
       t += a.x * b.x + a.y * b.y;
     }
-    float x = lastp + __expf(g_last) * t;
+    float x = t;
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if (lane == 0) atomicAdd(&sm.last, x);
+    if (lane == 0) sm.tw[warp] = x;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float last = 0.f, t = 0.f;
+    for (int i = 0; i < kC; ++i)
+      for (int sl = 0; sl < 4; ++sl) last += sm.lw[sl][i];
+    for (int w = 0; w < kLocalThreads / 32; ++w) t += sm.tw[w];
+    sm.last = last + __expf(g_last) * t;
+  }
+  if (tid < kC) {
+    float d = 0.f;
+    for (int sl = 0; sl < 12; ++sl) d += sm.part[sl][tid];
+    sm.dgs[tid] = d;
   }
   __syncthreads();
   if (tid < len) p.dgam[(size_t)h * p.total + t0 + tid] = sm.dgs[tid] + (tid == len - 1 ? sm.last : 0.f);
@@ -1436,6 +1456,7 @@ struct KdaLocalHSmem {
   __nv_bfloat16 dH1[kD * kS128];
   float G[kC * kG];  // gamma per channel
   float last[kD];    // the gamma_last terms per channel
+  float lc[4][kD];   // their column partials from the four row groups, added in a fixed order
 };
 static_assert(sizeof(KdaLocalHSmem) <= 227 * 1024, "fits one SM");
 
@@ -1609,8 +1630,10 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_h_kernel(GdnParam
       x += __shfl_xor_sync(0xffffffffu, x, 4);
       x += __shfl_xor_sync(0xffffffffu, x, 8);
       x += __shfl_xor_sync(0xffffffffu, x, 16);
-      if (lane < 4) atomicAdd(&sm.last[d0 + 8 * n + 2 * lane + e], x);
+      if (lane < 4) sm.lc[warp & 3][d0 + 8 * n + 2 * lane + e] = x;
     }
+  __syncthreads();
+  if (tid < kD) sm.last[tid] += ((sm.lc[0][tid] + sm.lc[1][tid]) + sm.lc[2][tid]) + sm.lc[3][tid];
   __syncthreads();
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
@@ -1658,6 +1681,8 @@ struct LocalWySmem {
   float bet[kC];
   float dgs[kC];
   float dbs[kC];
+  float pb[4][kC];  // row partials of dbeta and dgam from the four column groups, added in a fixed order
+  float pg[4][kC];
 };
 static_assert(sizeof(LocalWySmem) <= 227 * 1024, "fits one SM");
 
@@ -1898,8 +1923,8 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_wy_kernel(GdnPara
       const float v_ = quad_sum(rv[hr]), k_ = quad_sum(rk[hr]);
       if ((lane & 3) == 0) {
         const float eg = __expf(sm.gam[i]);
-        atomicAdd(&sm.dbs[i], v_ + eg * k_);
-        atomicAdd(&sm.dgs[i], sm.bet[i] * eg * k_);
+        sm.pb[warp >> 2][i] = v_ + eg * k_;
+        sm.pg[warp >> 2][i] = sm.bet[i] * eg * k_;
       }
     }
   }
@@ -1931,6 +1956,11 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_wy_kernel(GdnPara
         *reinterpret_cast<uint32_t*>(p.dk + off + j) = pack2(ck[n][2 * hr] + a.x, ck[n][2 * hr + 1] + a.y);
       }
     }
+  }
+  __syncthreads();
+  if (tid < kC) {
+    sm.dbs[tid] += ((sm.pb[0][tid] + sm.pb[1][tid]) + sm.pb[2][tid]) + sm.pb[3][tid];
+    sm.dgs[tid] += ((sm.pg[0][tid] + sm.pg[1][tid]) + sm.pg[2][tid]) + sm.pg[3][tid];
   }
   __syncthreads();
   // dbeta, and dg = reverse running sum of dgam (one warp, two tokens per lane)
@@ -1972,6 +2002,7 @@ struct KdaLocalWySmem {
   __nv_bfloat16 Xb[kC * kS64];
   float bet[kC];
   float dbs[kC];
+  float pb[4][kC];  // row partials of dbeta from the four column groups, added in a fixed order
 };
 static_assert(sizeof(KdaLocalWySmem) <= 227 * 1024, "fits one SM");
 
@@ -2183,11 +2214,13 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_wy_kernel(GdnPara
     for (int hr = 0; hr < 2; ++hr) {
       const int i = r0 + (lane >> 2) + 8 * hr;
       const float v_ = quad_sum(rv[hr]), k_ = quad_sum(rk[hr]);
-      if ((lane & 3) == 0) atomicAdd(&sm.dbs[i], v_ + k_);
+      if ((lane & 3) == 0) sm.pb[warp >> 2][i] = v_ + k_;
     }
   }
   __syncthreads();
-  if (tid < len) p.dbeta[(size_t)(t0 + tid) * p.nh + h] = sm.dbs[tid];
+  if (tid < len)
+    p.dbeta[(size_t)(t0 + tid) * p.nh + h] =
+        sm.dbs[tid] + (((sm.pb[0][tid] + sm.pb[1][tid]) + sm.pb[2][tid]) + sm.pb[3][tid]);
 }
 
 // ============================================================== Kimi Delta backward: the per-channel decay terms
