@@ -19,17 +19,17 @@
 // TMEM holds the fp32 accumulators of the MMAs (128 lanes x 512 columns):
 //   dK/dV pass: S^T, dP^T (N = 128 queries), dV, dK.  The two elementwise
 //     warpgroups split each tile's 128 query columns.  S^T and dP^T complete
-//     separately: P^T (the exp2 work) is computed while dP^T still runs, the
-//     dV MMA of a 64-query half starts as soon as that half of P^T is back
-//     in TMEM, and dK follows dS^T.
+//     separately: P^T (the exp2 work) is computed while dP^T still runs, and
+//     both bf16 P^T and dS^T go back over the dP^T columns, so S^T of the
+//     next pair runs as soon as S^T has been read into registers.  dV and dK
+//     of a 64-query half start as soon as that half is back in TMEM.
 //   dQ pass: two S buffers, dP, dQ.  S of the next kv tile is computed while
 //     the elementwise warpgroups work on the current one, and dP is released
 //     as soon as it has been read into registers.
-// bf16 operands (P^T, dS^T, dS) go back over the first half of the fp32
-// columns they were computed from and feed the next MMA as its A operand
-// straight from TMEM.  tcgen05 MMAs issued by one thread execute in order, so
-// an MMA that overwrites such columns always runs after the MMAs that read
-// them.  Measured on GB300: a 128x64x16 MMA takes as long as a 128x128x16 one,
+// bf16 operands (P^T, dS^T, dS) go back over fp32 columns the same warps have
+// already read and feed the next MMA as its A operand straight from TMEM.
+// tcgen05 MMAs issued by one thread execute in order, so an MMA that
+// overwrites such columns always runs after the MMAs that read them.  Measured on GB300: a 128x64x16 MMA takes as long as a 128x128x16 one,
 // so every S/dP MMA here uses N = 128.
 #include <cuda_bf16.h>
 
@@ -82,7 +82,7 @@ struct DkvCfg {
   static constexpr uint32_t kAugEnd = kAugOff + (1 + 2 * kStages) * kAugBytes;
   static constexpr uint32_t kSmemBytes = kAugEnd + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // S^T, dP^T (128 columns each, fp32; bf16 P^T/dS^T over their halves), dV, dK.
+  // S^T, dP^T (128 columns each, fp32; bf16 dS^T and P^T over dP^T), dV, dK.
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 };
 
@@ -102,9 +102,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ int* claim_words;
   __shared__ __align__(8) uint64_t bar_kv_full, bar_kv_empty;
   __shared__ __align__(8) uint64_t bar_qdo_full[S], bar_qdo_empty[S];
-  // s_full[0]: S^T done, s_full[1]: dP^T done; p_full[x] / ds_full[x]: warpgroup
-  // x has written its half of P^T / dS^T.
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_ds_full[2];
+  // s_full[0]: S^T done, s_full[1]: dP^T done; s_free: both warpgroups have
+  // read S^T into registers; ds_full[x]: warpgroup x has written its half of
+  // P^T and dS^T.
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_s_free, bar_ds_full[2];
   __shared__ __align__(8) uint64_t bar_acc_full, bar_acc_empty;
   __shared__ __align__(8) uint64_t bar_chain[2];
   __shared__ int chain_last[2];
@@ -128,9 +129,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&bar_s_full[x]), 1);
-      mbar_init(smem_u32(&bar_p_full[x]), 128);
       mbar_init(smem_u32(&bar_ds_full[x]), 128);
     }
+    mbar_init(smem_u32(&bar_s_free), 256);
     mbar_init(smem_u32(&bar_acc_full), 1);
     mbar_init(smem_u32(&bar_acc_empty), 256);
     mbar_init(smem_u32(&bar_chain[0]), 128);
@@ -296,16 +297,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int npairs = (w.t1 - w.t0 + 1) * a.group;
         if (!(ok = mbar_wait(smem_u32(&bar_kv_full), it & 1, &abort_flag, a.status))) break;
         tc_fence_after();
-        // Pairs are software-pipelined inside an item when the next Q/dO stage
-        // is already there:
-        //   S^T(0) dP^T(0) | dV(0) S^T(1) dK(0) dP^T(1) | dV(1) S^T(2) dK(1) ...
-        // so the elementwise exp2 of pair n+1 runs during dK(n) and dP^T(n+1),
-        // and its dS of pair n during dV(n) and S^T(n+1); otherwise S^T(n+1)
-        // follows dK(n).  S^T(n+1) overwrites
-        // P^T(n), which dV(n) (issued just before) has read; dP^T(n+1)
-        // overwrites dS^T(n) after dK(n) (in-order execution).  Items are not
-        // pipelined into each other: the next item's K/V tiles load only
-        // once this item's MMAs are done.
+        // Pairs are software-pipelined inside an item.  The bf16 P^T and dS^T
+        // of pair n go into the dP^T columns (each warpgroup writes them over
+        // its own 64 dP^T columns once it has read them), so the S^T columns
+        // are free as soon as S^T(n) is in registers:
+        //   S^T(0) dP^T(0) | S^T(1) dV(0) dK(0) dP^T(1) | S^T(2) dV(1) dK(1) ...
+        // S^T(n+1) runs while the elementwise warps wait for dP^T(n) and
+        // compute dS^T(n); their exp2 work of pair n+1 runs during dV(n),
+        // dK(n) and dP^T(n+1).  dP^T(n+1) overwrites P^T(n) and dS^T(n) after
+        // dV(n) and dK(n) have read them (in-order execution).  Items are not
+        // pipelined into each other: the next item's K/V tiles load only once
+        // this item's MMAs are done.
         auto issue_s = [&](int c) -> bool {  // S^T of pair c: needs its Q (and staged -lse/scale)
           const int sl = c % S;
           if (!mbar_wait(smem_u32(&bar_qdo_full[sl]), (c / S) & 1, &abort_flag, a.status)) return false;
@@ -339,38 +341,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int pr = 0; pr < npairs && ok; ++pr) {
           const int slot = cnt % S;
           const uint32_t sq = sQ0 + slot * 2 * kTileBytes, sdo = sq + kTileBytes;
+          const bool more = pr + 1 < npairs;
+          // S^T(n+1) once S^T(n) has been read out, and only if its Q stage
+          // has landed: the MMA warp never blocks on that load here (it would
+          // hold back dV(n) and dK(n)).
+          bool s_next = false;
+          if (more) {
+            if (!(ok = mbar_wait(smem_u32(&bar_s_free), cnt & 1, &abort_flag, a.status))) break;
+            if (mbar_try_wait(smem_u32(&bar_qdo_full[(cnt + 1) % S]), ((cnt + 1) / S) & 1)) {
+              tc_fence_after();
+              if (!(ok = issue_s(cnt + 1))) break;
+              s_next = true;
+            }
+          }
           // The accumulators of the previous item must have been read out.
           if (pr == 0 && it > 0 &&
               !(ok = mbar_wait(smem_u32(&bar_acc_empty), (it - 1) & 1, &abort_flag, a.status)))
             break;
-          // dV += P^T_half dO_half as each half of P^T arrives (K = 64 queries).
-          for (int half = 0; half < 2 && ok; ++half) {
-            if (!(ok = mbar_wait(smem_u32(&bar_p_full[half]), cnt & 1, &abort_flag, a.status))) break;
-            tc_fence_after();
-            const bool acc = pr > 0 || half > 0;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + C::kColDV, tmem + C::kColS + 64 * half + kk * 8, mnmajor_desc(sdo, 4 * half + kk),
-                     idesc_g, (acc || kk > 0) ? 1u : 0u);
-          }
-          if (!ok) break;
-          const bool more = pr + 1 < npairs;
-          // S^T(n+1) goes before dK(n) only if its Q stage has landed; the MMA
-          // warp never blocks on it here (it would hold back dK(n)).
-          bool s_next = false;
-          if (more && mbar_try_wait(smem_u32(&bar_qdo_full[(cnt + 1) % S]), ((cnt + 1) / S) & 1)) {
-            ok = issue_s(cnt + 1);
-            s_next = true;
-          }
-          // dK += dS^T_half Q_half.
+          // dV += P^T_half dO_half and dK += dS^T_half Q_half as each half
+          // arrives (K = 64 queries; P^T in the upper, dS^T in the lower 32
+          // of the half's 64 dP^T columns).
           for (int half = 0; half < 2 && ok; ++half) {
             if (!(ok = mbar_wait(smem_u32(&bar_ds_full[half]), cnt & 1, &abort_flag, a.status))) break;
             tc_fence_after();
             const bool acc = pr > 0 || half > 0;
+            const uint32_t tdp = tmem + C::kColDP + 64 * half;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + C::kColDK, tmem + C::kColDP + 64 * half + kk * 8, mnmajor_desc(sq, 4 * half + kk),
-                     idesc_g, (acc || kk > 0) ? 1u : 0u);
+              mma_ts(tmem + C::kColDV, tdp + 32 + kk * 8, mnmajor_desc(sdo, 4 * half + kk), idesc_g,
+                     (acc || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tmem + C::kColDK, tdp + kk * 8, mnmajor_desc(sq, 4 * half + kk), idesc_g,
+                     (acc || kk > 0) ? 1u : 0u);
           }
           if (!ok) break;
           tc_commit(smem_u32(&bar_qdo_empty[slot]));
@@ -422,8 +425,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------------------------ elementwise
     // Warpgroup x = query columns [64x, 64x + 64) of every S^T/dP^T tile;
-    // thread = key row.  Its bf16 P^T and dS^T go over the first 32 of its
-    // own 64 columns.
+    // thread = key row.  Its bf16 dS^T and P^T go over its own 64 dP^T
+    // columns (dS^T the first 32, P^T the other 32).
     regs_increase<200>();
     const int x = (warp >> 2) - 1;
     const int quarter = warp & 3;
@@ -452,13 +455,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           int c_lo = 0, c_hi = 63;
           if (!full) col_visible_rows(j, q0, w.seg_hi, a.window, c_lo, c_hi);
           // P^T while the dP^T MMA runs: the MMA already subtracted lse/scale,
-          // so P = exp2((s - lse/scale) * scale*log2e).
-          float pv[64];
+          // so P = exp2((s - lse/scale) * scale*log2e).  The S^T columns are
+          // released as soon as they are in registers.
+          // P is kept as the bf16 pairs the dV MMA reads; dS^T is computed
+          // from the same rounded values.
+          uint32_t pp[32];
           {
             uint32_t sr[64];
             tmem_ld64_wait(tS, sr);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_s_free));
             const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
-            uint32_t pp[32];
 #pragma unroll
             for (int cc = 0; cc < 64; cc += 2) {
               float p0, p1;
@@ -469,30 +476,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 p0 = (cc >= c_lo && cc <= c_hi) ? p0 : 0.f;
                 p1 = (cc + 1 >= c_lo && cc + 1 <= c_hi) ? p1 : 0.f;
               }
-              pv[cc] = p0;
-              pv[cc + 1] = p1;
               pp[cc / 2] = pack_bf16x2(p0, p1);
             }
-            tmem_st32(tS, pp);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bar_p_full[x]));
           }
-          // dS^T = P (dP - D) once dP^T is there (the MMA subtracted D).
+          // dS^T = P (dP - D) once dP^T is there (the MMA subtracted D); dS^T
+          // (bf16) goes over the first 32 of this half's dP^T columns, P^T
+          // over the other 32.
           if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[1]), cnt & 1, &abort_flag, a.status))) break;
           tc_fence_after();
           {
             uint32_t dr[64];
             tmem_ld64_wait(tDP, dr);
-            uint32_t pd[32];
 #pragma unroll
-            for (int cc = 0; cc < 64; cc += 2) {
-              float d0, d1;
-              f2_unpack(f2_mul(f2_pack(pv[cc], pv[cc + 1]), f2_pack(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1]))),
-                        d0, d1);
-              pd[cc / 2] = pack_bf16x2(d0, d1);
+            for (int hf = 0; hf < 2; ++hf) {
+              uint32_t pd[16], ph[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int cc = 32 * hf + 2 * e;
+                const uint32_t w2 = pp[16 * hf + e];
+                const float q0 = __uint_as_float(w2 << 16), q1 = __uint_as_float(w2 & 0xffff0000u);
+                float d0, d1;
+                f2_unpack(f2_mul(f2_pack(q0, q1), f2_pack(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1]))), d0, d1);
+                pd[e] = pack_bf16x2(d0, d1);
+                ph[e] = w2;
+              }
+              tmem_st16(tDP + 16 * hf, pd);
+              tmem_st16(tDP + 32 + 16 * hf, ph);
             }
-            tmem_st32(tDP, pd);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_ds_full[x]));
