@@ -256,6 +256,19 @@ def workload_config(wl, cu, pairs: int, world: int) -> dict:
             "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"}
 
 
+def job_ms_per_microbatch(timed_ms: float, steps: int, world: int, device) -> float:
+    """Whole-job value: every rank times `steps` steps of its own microbatch
+    (replicas, weak scaling); the job takes as long as its slowest rank, and
+    it processed steps * world microbatches.  With world > 1 the caller's
+    process group does the MAX (NCCL on GPUs; gloo works the same on CPU)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([timed_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item() / (steps * world)
+
+
 def run_reference(args, wl):
     """The reference arm: the CPU oracle as it stands, timed on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -568,11 +581,7 @@ def main():
 
     main_res = measure(wl, args.steps, args.warmup, sample_clocks=True)
     step_ms = statistics.mean(main_res["total_ms"])
-    # Whole job: every rank processes its own microbatch; time = max over ranks.
-    t_job = torch.tensor([sum(main_res["total_ms"])], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_job, op=dist.ReduceOp.MAX)
-    value = t_job.item() / (args.steps * world)  # ms per microbatch over the whole job
+    value = job_ms_per_microbatch(sum(main_res["total_ms"]), args.steps, world, dev)
     peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     tf = tflops(wl, main_res["pairs"], step_ms)
 
