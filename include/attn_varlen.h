@@ -88,6 +88,7 @@ extern "C" {
 #define ATTN_STATUS_LIST_OVERFLOW 2    /* a CTA's work list did not fit */
 #define ATTN_STATUS_SMEM_ALIGN 3       /* dynamic shared memory not 1024-byte aligned (internal error) */
 #define ATTN_STATUS_SEGMENT_TOO_LONG 4 /* a segment of cu_seqlens is longer than max_seqlen */
+#define ATTN_STATUS_GATE_RANGE 5       /* kda_varlen_*: a log decay g at or below -5.8, or NaN */
 
 /*
  * Forward.  Writes out [T, Hq, 128] (bf16) and lse [Hq, T] (float32).

@@ -23,7 +23,10 @@
  * g is the log decay per token, head and key channel.  The kernels split each
  * chunk's decay at the start of every 16-token block, so the decay over 15
  * tokens of one channel must stay inside float range: every g > -5.8 (a
- * per-token decay above 0.003).
+ * per-token decay above 0.003).  The kernels check this: a chunk holding a g
+ * at or below -5.8 (or a NaN) sets the device status word to
+ * ATTN_STATUS_GATE_RANGE (attn_varlen_get_status), and its outputs are then
+ * not to be trusted.
  *
  * Method: as gdn_varlen.h, chunks of 64 tokens and the WY form of the
  * chunk's delta-rule steps, with the decay applied per channel inside the

@@ -138,3 +138,39 @@ def test_backward_matches_oracle(name):
 def test_cuda_graph_replay_with_padded_boundaries_is_bit_exact():
     from tests.test_gdn import _graph_replay_is_bit_exact
     _graph_replay_is_bit_exact(synth.kda_workloads(), "kda_ctx4096", True)
+
+
+@pytest.mark.gpu
+def test_gate_at_or_below_the_bound_sets_the_status_word():
+    """A log decay at or below -5.8 (the documented bound) is reported as
+    ATTN_STATUS_GATE_RANGE (5) by the forward and by the backward; the same
+    inputs with every gate clamped to -5.7 report nothing.  Out-of-range
+    gates make no kernel fault or wait: the outputs are just not to be
+    trusted."""
+    import torch
+    from varlen_sliding_window_gb300 import binding
+    w = WL["kda_tiny"]
+    inp = w.inputs()
+    cu_t = torch.from_numpy(np.asarray(inp.cu_seqlens, dtype=np.int32)).cuda()
+    q, k, v, do = (_to_dev(b) for b in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
+    beta = torch.from_numpy(inp.beta).cuda()
+    T, nh, _ = q.shape
+    binding.attn_varlen_get_status()  # start from a clear word
+    for bad in (True, False):
+        g_np = np.maximum(inp.g, -5.7).astype(np.float32)
+        if bad:
+            g_np[T // 2, nh - 1, 77] = -6.0
+        g = torch.from_numpy(g_np).cuda()
+        o = torch.empty_like(q)
+        ws = torch.empty(binding.kda_varlen_workspace_bytes(T, nh, len(inp.cu_seqlens) - 1), dtype=torch.uint8,
+                         device="cuda")
+        binding.kda_varlen_fwd(q, k, v, g, beta, cu_t, w.scale, o, ws)
+        torch.cuda.synchronize()
+        assert binding.attn_varlen_get_status() == (5 if bad else 0), ("fwd", bad)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        dg, dbeta = torch.empty_like(g), torch.empty_like(beta)
+        wsb = torch.empty(binding.kda_varlen_bwd_workspace_bytes(T, nh, len(inp.cu_seqlens) - 1),
+                          dtype=torch.uint8, device="cuda")
+        binding.kda_varlen_bwd(q, k, v, g, beta, do, cu_t, w.scale, dq, dk, dv, dg, dbeta, wsb)
+        torch.cuda.synchronize()
+        assert binding.attn_varlen_get_status() == (5 if bad else 0), ("bwd", bad)

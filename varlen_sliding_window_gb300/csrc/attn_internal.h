@@ -150,6 +150,7 @@ enum : int {
   kStatusListOverflow = 2,   // a CTA's work list did not fit
   kStatusSmemAlign = 3,      // dynamic shared memory not 1024-byte aligned
   kStatusSegmentTooLong = 4, // a segment longer than max_seqlen (its tiles past max_seqlen were skipped)
+  kStatusGateRange = 5,      // Kimi Delta: a log decay g at or below -5.8 (or NaN)
 };
 
 // Run by one warp: reports, through the status word, a segment longer than

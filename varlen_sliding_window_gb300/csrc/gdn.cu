@@ -44,6 +44,9 @@ namespace {
 
 constexpr int kC = 64;         // chunk length (tokens)
 constexpr int kD = 128;        // d_k = d_v
+// Kimi Delta: smallest per-token log decay the block-referenced products
+// allow (the decay of 15 tokens stays within float range: 15 x 5.8 < 88).
+constexpr float kKdaMinLogDecay = -5.8f;
 constexpr int kDvb = 32;       // value columns per state CTA
 constexpr int kGdnThreads = 256;   // prep CTA
 constexpr int kStateThreads = 256; // state CTA
@@ -65,6 +68,7 @@ struct GdnParams {
   __nv_bfloat16* o;
   int total, nh, nseg, max_chunks;
   float scale;
+  int* status;  // the device status word (Kimi Delta: gates out of range)
   // workspace
   int* hdr;             // [0] chunks, [1] non-empty segments
   int4* chunks;         // [max_chunks] {start token, length, segment, chunk index in segment}
@@ -558,6 +562,15 @@ __global__ void __launch_bounds__(kLocalThreads) kda_prep_kernel(GdnParams p) {
   if (tid < kC) sm.bet[tid] = tid < len ? p.beta[(size_t)(t0 + tid) * p.nh + h] : 0.f;
   cp_async_wait<0>();
   __syncthreads();
+  {
+    // Every log decay must be above kKdaMinLogDecay (the block-referenced
+    // products need the decay of 15 tokens within float range); anything
+    // else, NaN included, is reported in the status word.  Rows past the
+    // chunk were zero-filled.
+    bool bad = false;
+    for (int e = tid; e < kC * kD; e += nt) bad |= !(sm.G[(e >> 7) * kG + (e & 127)] > kKdaMinLogDecay);
+    if (__syncthreads_or(bad) && tid == 0 && p.status) atomicExch(p.status, kStatusGateRange);
+  }
   // gamma per channel (rows past the chunk add zeros)
   if (tid < kD) {
     float acc = 0.f;
@@ -2634,6 +2647,7 @@ int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* g, 
   if ((rc = device_for_call(&status, &sms))) return rc;
   if (total == 0) return ATTN_OK;
   p.o = static_cast<__nv_bfloat16*>(o);
+  p.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_kda_prep(p, s);
   const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
@@ -2671,6 +2685,7 @@ int kda_varlen_bwd(const void* q, const void* k, const void* v, const float* g, 
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.dg = dg;
   p.dbeta = dbeta;
+  p.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
   const dim3 chunk_grid((unsigned)p.max_chunks, (unsigned)num_heads);
