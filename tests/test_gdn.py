@@ -209,3 +209,41 @@ def _graph_replay_is_bit_exact(wls, name, per_channel):
 @pytest.mark.gpu
 def test_cuda_graph_replay_with_padded_boundaries_is_bit_exact():
     _graph_replay_is_bit_exact(synth.gdn_workloads(), "gdn_ctx4096", False)
+
+
+# Ragged boundaries for the head-count cases: a 1-token segment, segments
+# ending one before, at and one after a 64-token chunk edge, an empty one.
+HEAD_CASE_CU = np.array([0, 1, 64, 65, 129, 129, 200, 330], dtype=np.int32)
+
+
+def check_head_counts(nh, per_channel):
+    """Forward and backward against the oracle with nh heads: the kernels
+    index the [T, H, 128] rows, the per-head chunk tables and every
+    workspace array by H, and the other tests use 8."""
+    from oracle import gated_delta, kimi_delta
+    oracle_mod = kimi_delta if per_channel else gated_delta
+    inp = synth.make_gdn_inputs(HEAD_CASE_CU, nh, 128, tensor_seed=11, per_channel=per_channel)
+    scale = 1 / np.sqrt(128)
+    if per_channel:
+        from tests import test_kda as t
+        tol_o, tol_g = t.TOL_O, {nm: t.TOL_GRAD for nm in ("dq", "dk", "dv", "dg", "dbeta")}
+        run, run_bwd = t._run, t._run_bwd
+    else:
+        tol_o, tol_g, run, run_bwd = TOL_O, TOL_GRAD, _run, _run_bwd
+    got = run(inp, scale).double().cpu().numpy()
+    ref = oracle_mod.forward(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens, scale)
+    assert np.isfinite(got).all()
+    assert rel_l2(got, ref) <= tol_o, rel_l2(got, ref)
+    assert_per_segment(got, ref, inp.cu_seqlens, tol_o, "o")
+    grads = run_bwd(inp, scale)
+    refs = oracle_mod.backward(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.do, inp.cu_seqlens, scale)
+    for nm, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), grads, refs):
+        assert np.isfinite(a).all(), nm
+        assert rel_l2(a, b) <= tol_g[nm], (nm, rel_l2(a, b))
+        assert_per_segment(a, b, inp.cu_seqlens, tol_g[nm], nm)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("nh", [1, 3, 5])
+def test_head_counts(nh):
+    check_head_counts(nh, per_channel=False)

@@ -174,3 +174,10 @@ def test_gate_at_or_below_the_bound_sets_the_status_word():
         binding.kda_varlen_bwd(q, k, v, g, beta, do, cu_t, w.scale, dq, dk, dv, dg, dbeta, wsb)
         torch.cuda.synchronize()
         assert binding.attn_varlen_get_status() == (5 if bad else 0), ("bwd", bad)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("nh", [1, 3, 5])
+def test_head_counts(nh):
+    from tests.test_gdn import check_head_counts
+    check_head_counts(nh, per_channel=True)
