@@ -20,18 +20,22 @@
 //   gdn_prep_kernel    one CTA per (chunk, head), all in parallel: A, Tm,
 //                      W, U and the masked Q K^T o Gamma, written to the
 //                      workspace (bf16), and gamma (fp32)
-//   gdn_state_kernel   one CTA (8 warps) per (segment, head, 32 value
-//                      columns): carries H (fp32, in registers) across the
-//                      segment's chunks and writes O; the tiles of chunks
-//                      c+1 and c+2 load (cp.async) while chunk c computes
+//   gdn_state_kernel   one CTA per (segment, head, 32 value columns):
+//                      eight warps carry H (fp32, in registers) across the
+//                      segment's chunks and write O; a producer warp loads
+//                      the tiles of chunks c+1 and c+2 by TMA while chunk c
+//                      computes
 // The products are small (64-row) and run in bf16 on the warp-level tensor
 // core instruction (mma.sync m16n8k16, fp32 accumulation): the state pass is
 // a dependent chain of 64-row steps whose state lives in registers, where the
 // asynchronous 128-row tcgen05 path has nothing to overlap.
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include "attn_internal.h"
 #include "attn_varlen.h"
@@ -139,6 +143,24 @@ __device__ __forceinline__ uint32_t frag_b(uint32_t base, int ld, int k0, int n0
   return base + 2u * (uint32_t)((k0 + (lane & 15)) * ld + n0 + ((lane >> 4) << 3));
 }
 
+// The state passes' stage tiles as TMA writes them: a 64 x 128 bf16 tile is
+// two 64-column halves of 64 rows x 128 B (8 KB each, 1024-byte aligned), and
+// the 128-byte swizzle stores the 16-byte chunk j of row r at chunk j ^ (r % 8).
+// Byte address of element (r, c), c a multiple of 8.
+__device__ __forceinline__ uint32_t sw128(uint32_t base, int r, int c) {
+  return base + ((uint32_t)(c >> 6) << 13) + ((uint32_t)r << 7) + ((uint32_t)(((c >> 3) & 7) ^ (r & 7)) << 4);
+}
+// frag_a and frag_bt over such a tile: the same lanes supply the same
+// (row, column) as over a row-major tile.  Eight lanes read eight
+// consecutive rows of one column chunk, which the swizzle puts in eight
+// different bank groups.
+__device__ __forceinline__ uint32_t frag_a_sw(uint32_t base, int r0, int c0, int lane) {
+  return sw128(base, r0 + (lane & 15), c0 + ((lane >> 4) << 3));
+}
+__device__ __forceinline__ uint32_t frag_bt_sw(uint32_t base, int n0, int k0, int lane) {
+  return sw128(base, n0 + (lane & 7) + ((lane >> 4) << 3), k0 + (((lane >> 3) & 1) << 3));
+}
+
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -146,9 +168,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -171,6 +190,14 @@ __device__ __forceinline__ void load_rows128(uint32_t dst, const __nv_bfloat16* 
 // Rows of a chunk that lie inside [0, T) (all of them for a valid boundary list).
 __device__ __forceinline__ int chunk_len(const int4& ch, int total) {
   return (ch.x < 0 || ch.x >= total) ? 0 : min(ch.y, total - ch.x);
+}
+
+// Chunk ci of a segment entry {first chunk, chunks, start token, length}:
+// the {start token, length} that the chunk table holds for chunk first + ci
+// (the planner lays a segment's chunks 64 tokens apart from its start), with
+// no load from the table.
+__device__ __forceinline__ int4 seg_chunk(const int4& sg, int ci) {
+  return make_int4(sg.z + ci * kC, min(kC, sg.w - ci * kC), 0, ci);
 }
 
 // ============================================================== plan
@@ -730,63 +757,206 @@ __global__ void __launch_bounds__(kLocalThreads) kda_prep_kernel(GdnParams p) {
 }
 
 // ============================================================== state + output
-struct StateStage {
-  __nv_bfloat16 W[kC * kS128];
-  __nv_bfloat16 K[kC * kS128];
-  __nv_bfloat16 Q[kC * kS128];
-  __nv_bfloat16 U[kC * kS32];
-  __nv_bfloat16 Aq[kC * kS64];
+// The state passes run as a pipeline of three stages.  A producer warp fills
+// stage c % 3 with the pass's chunk c: the chunk's three 64 x 128 token-row
+// tiles (W, K, Q) and its 64 x 64 Aq block, swizzled by 128 bytes (see
+// sw128), and the CTA's 32 value columns of U (forward) or dO (backward),
+// swizzled by 64 bytes (see sw64), all by TMA on the stage's full barrier;
+// the gates by plain loads.  The eight compute warps release the stage on
+// its empty barrier when they are done with it.  So the compute warps spend
+// nothing on loads, and need no barrier at the end of a step.
+// Rows past the end of the tensor arrive as zeros; rows past the chunk's end
+// that belong to the next segment are zeroed once the tiles have landed, so
+// no chunk reads another segment.
+constexpr int kTileBytes = kC * kD * 2;  // 64 x 128 bf16: two 8 KB halves
+constexpr int kColsBytes = kC * kDvb * 2;  // 64 x 32 bf16
+constexpr uint32_t kStageTxBytes = 3 * kTileBytes + kC * kC * 2 + kColsBytes;
+constexpr int kStateBlock = kStateThreads + 32;  // eight compute warps and the producer
+
+// The TMA maps of the state passes.  W, K and Q ([T, H, 128] bf16; Kimi Delta
+// reads K o e^(gamma_last - gamma) and Q o e^gamma) as 4-D tensors (64
+// columns, token, column half, head), box 64 x 64 tokens x 2 halves x 1 head:
+// one copy lands a whole 64 x 128 tile as its two swizzled halves.  Aqk
+// ([chunks x H, 64, 64] bf16), box one block.  U and dO ([T, H, 128] bf16),
+// box 32 columns x 1 head x 64 tokens.
+struct StateMaps {
+  CUtensorMap w, k, q, aq, u, d_o;
+};
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5}], [%6];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+struct alignas(1024) StateStage {
+  __nv_bfloat16 W[kC * kD];      // swizzled; W, K, Q are consecutive
+  __nv_bfloat16 K[kC * kD];      // swizzled
+  __nv_bfloat16 Q[kC * kD];      // swizzled
+  __nv_bfloat16 Aq[kC * kC];     // swizzled
+  __nv_bfloat16 cols[kC * kDvb]; // 64-byte swizzle: value columns of U (forward) or dO (backward)
   float gam[kD];  // gamma of the chunk's tokens; with a decay per channel, e^gamma_last per channel
 };
-constexpr int kStateStages = 3;  // chunk c + 2 loads while chunk c computes
-struct StateSmem {
+static_assert(offsetof(StateStage, K) == kTileBytes && offsetof(StateStage, Q) == 2 * kTileBytes &&
+                  offsetof(StateStage, Aq) == 3 * kTileBytes && offsetof(StateStage, cols) % 1024 == 0,
+              "TMA tiles at 1024-byte offsets");
+constexpr int kStateStages = 3;
+struct StatePipe {
   StateStage st[kStateStages];
+  uint64_t full[kStateStages];   // the producer's copies of stage s have landed
+  uint64_t empty[kStateStages];  // the eight compute warps are done with stage s
+  int abort;                     // a wait of this CTA gave up
+};
+struct StateSmem {
+  StatePipe pp;
   __nv_bfloat16 H[kD * kS32];   // the state at the chunk start, bf16 (B operand)
   __nv_bfloat16 E[kC * kS32];   // E (bf16)
   __nv_bfloat16 E2[kC * kS32];  // diag(e^(gamma_last - gamma)) E (bf16)
 };
+// The launch adds 1024 bytes of slack to align the stages.
+static_assert(sizeof(StateSmem) + 1024 <= 227 * 1024, "the state CTA's shared memory fits one SM");
 
-static_assert(sizeof(StateSmem) <= 227 * 1024, "the state CTA's shared memory fits one SM");
+__device__ __forceinline__ uint8_t* align1024(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
 
+// Byte offset of element (r, c) of the 64 x 32 value columns, 64-byte rows
+// with the 64-byte swizzle (16-byte chunk j of row r at chunk j ^ (r / 2 % 4)).
+// Eight consecutive rows of one chunk fall in eight different bank groups.
+__device__ __forceinline__ uint32_t sw64(int r, int c) {
+  return (uint32_t)(r * 64 + (((((c >> 3) ^ (r >> 1)) & 3)) << 4) + (c & 7) * 2);
+}
+__device__ __forceinline__ float2 cols_pair(const StateStage& s, int r, int c) {
+  return __bfloat1622float2(
+      *reinterpret_cast<const __nv_bfloat162*>(reinterpret_cast<const uint8_t*>(s.cols) + sw64(r, c)));
+}
+// frag_b over the value columns.
+__device__ __forceinline__ uint32_t frag_b_cols(uint32_t base, int k0, int n0, int lane) {
+  return base + sw64(k0 + (lane & 15), n0 + ((lane >> 4) << 3));
+}
 
-template <bool kChan>
-__device__ __forceinline__ void load_stage(StateStage& s, const GdnParams& p, int chunk, int h, int vb, int tid) {
-  constexpr int nt = kStateThreads;
-  const int4 ch = p.chunks[chunk];
-  const int len = chunk_len(ch, p.total), t0 = len > 0 ? ch.x : 0;
-  load_rows128(smem_u32(s.W), p.W, t0, len, h, p.nh, tid, nt);
-  load_rows128(smem_u32(s.K), kChan ? p.KC : p.k, t0, len, h, p.nh, tid, nt);
-  load_rows128(smem_u32(s.Q), kChan ? p.QB : p.q, t0, len, h, p.nh, tid, nt);
-  for (int e = tid; e < kC * 4; e += nt) {  // U columns [32 vb, 32 vb + 32)
-    const int r = e >> 2, cc = (e & 3) * 8;
-    const bool ok = r < len;
-    cp_async16(smem_u32(&s.U[r * kS32 + cc]), p.U + ((size_t)(t0 + (ok ? r : 0)) * p.nh + h) * kD + kDvb * vb + cc,
-               ok);
+// The 256 compute threads' own barrier (the producer warp never joins it).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool compute_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 1, 256, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+// Rows [len, 64) of the stage's token-row tiles and value columns to zero
+// (each keeps row r in one run of bytes, whatever the swizzle).
+__device__ __forceinline__ void zero_tail_rows(StateStage& s, int len, int tid) {
+  uint8_t* base = reinterpret_cast<uint8_t*>(s.W);
+  const int n = (kC - len) * 8;  // 16-byte chunks per half tile
+  for (int e = tid; e < 6 * n; e += kStateThreads) {
+    const int hf = e / n, x = e - hf * n;
+    *reinterpret_cast<uint4*>(base + hf * (kTileBytes / 2) + len * 128 + x * 16) = make_uint4(0u, 0u, 0u, 0u);
   }
-  const __nv_bfloat16* aq = p.Aqk + ((size_t)chunk * p.nh + h) * (kC * kC);
-  for (int e = tid; e < kC * 8; e += nt) {
-    const int r = e >> 3, cc = (e & 7) * 8;
-    cp_async16(smem_u32(&s.Aq[r * kS64 + cc]), aq + r * kC + cc, true);
-  }
-  if (kChan) {
-    if (tid < kD / 4) cp_async16(smem_u32(&s.gam[4 * tid]), p.Bc + ((size_t)chunk * p.nh + h) * kD + 4 * tid, true);
-  } else if (tid < kC) {
-    const bool ok = tid < len;
-    cp_async4(smem_u32(&s.gam[tid]), p.gam + (size_t)h * p.total + t0 + (ok ? tid : 0), ok);
+  uint8_t* cols = reinterpret_cast<uint8_t*>(s.cols);
+  for (int e = tid; e < (kC - len) * 4; e += kStateThreads)
+    *reinterpret_cast<uint4*>(cols + len * 64 + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();  // before the stage's next TMA overwrite
+}
+
+// Lane 0 after a wait gave up: waits (bounded again) for the copies of the
+// pass's chunks [c0, c1) that may still be in flight, so that the CTA leaves
+// no copy writing its shared memory.
+__device__ __forceinline__ void drain_copies(const uint64_t* full, int c0, int c1) {
+  for (int c = c0; c < c1; ++c) {
+    const uint32_t bar = smem_u32(&full[c % kStateStages]);
+    const uint32_t parity = (uint32_t)(c / kStateStages) & 1u;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < VSW_WAIT_TIMEOUT_NS) {
+    }
   }
 }
 
-// Eight warps.  Warp w computes, of the chunk's 64 x 32 products (E, Q H,
-// O), rows [16 (w % 4), +16) x columns [16 (w / 4), +16), and holds rows
+// The producer warp.  The pass visits the segment's chunks in order
+// (forward) or in reverse (backward); its chunk c goes to stage c % 3 once
+// the compute warps have released the stage's previous chunk c - 3.
+template <bool kChan, bool kReverse>
+__device__ __forceinline__ void state_producer(StatePipe& pp, const StateMaps& m, const GdnParams& p, const int4& sg,
+                                               int nch, int h, int vb, int lane) {
+  const CUtensorMap* cols_map = kReverse ? &m.d_o : &m.u;
+  for (int c = 0; c < nch; ++c) {
+    const int st = c % kStateStages;
+    if (c >= kStateStages &&
+        !mbar_wait_warp(smem_u32(&pp.empty[st]), (uint32_t)(c / kStateStages - 1) & 1u, &pp.abort, p.status)) {
+      if (lane == 0) drain_copies(pp.full, c - kStateStages, c);
+      return;
+    }
+    const int ci = kReverse ? nch - 1 - c : c;
+    const int chunk = sg.x + ci;
+    const int4 ch = seg_chunk(sg, ci);
+    const int len = chunk_len(ch, p.total), t0 = len > 0 ? ch.x : 0;
+    StateStage& s = pp.st[st];
+    if (kChan) {
+      *reinterpret_cast<float4*>(&s.gam[4 * lane]) =
+          *reinterpret_cast<const float4*>(p.Bc + ((size_t)chunk * p.nh + h) * kD + 4 * lane);
+    } else {
+      for (int i = lane; i < kC; i += 32) s.gam[i] = i < len ? p.gam[(size_t)h * p.total + t0 + i] : 0.f;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t bar = smem_u32(&pp.full[st]);
+      // generic-proxy accesses of the stage's last use before the async-proxy overwrite
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, kStageTxBytes);  // also publishes the gates
+      tma_load_4d(smem_u32(s.W), &m.w, bar, 0, t0, 0, h);
+      tma_load_4d(smem_u32(s.K), &m.k, bar, 0, t0, 0, h);
+      tma_load_4d(smem_u32(s.Q), &m.q, bar, 0, t0, 0, h);
+      tma_load_3d(smem_u32(s.Aq), &m.aq, bar, 0, 0, chunk * p.nh + h);
+      tma_load_3d(smem_u32(s.cols), cols_map, bar, kDvb * vb, h, t0);
+    }
+  }
+}
+
+// Pipeline set-up of a state CTA: barriers, then (for the producer warp) the
+// whole production.  Returns true for the compute threads.
+template <bool kChan, bool kReverse>
+__device__ __forceinline__ bool state_pipe_start(StatePipe& pp, const StateMaps& m, const GdnParams& p,
+                                                 const int4& sg, int nch, int h, int vb, int tid) {
+  if (tid == 0) {
+    for (int i = 0; i < kStateStages; ++i) {
+      mbar_init(smem_u32(&pp.full[i]), 1);
+      mbar_init(smem_u32(&pp.empty[i]), kStateThreads / 32);
+    }
+    pp.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid >= kStateThreads) {
+    state_producer<kChan, kReverse>(pp, m, p, sg, nch, h, vb, tid & 31);
+    return false;
+  }
+  return true;
+}
+
+// A compute warp is done with stage st.
+__device__ __forceinline__ void release_stage(StatePipe& pp, int st, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&pp.empty[st]));
+}
+
+// Eight compute warps.  Warp w computes, of the chunk's 64 x 32 products (E,
+// Q H, O), rows [16 (w % 4), +16) x columns [16 (w / 4), +16), and holds rows
 // [16 w, +16) of the 128 x 32 state.
 // kStore (the backward's recomputation): no O; the bf16 state at every chunk
 // start and every chunk's E go to the workspace instead.
 // kChan (Kimi Delta): K and Q arrive pre-scaled (KC, QB), so E and O take no
 // per-token factor, and the state decays by e^gamma_last per channel (row).
 template <bool kStore, bool kChan>
-__global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
+__global__ void __launch_bounds__(kStateBlock) gdn_state_kernel(const __grid_constant__ StateMaps maps,
+                                                                GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  StateSmem& sm = *reinterpret_cast<StateSmem*>(smem_raw);
+  StateSmem& sm = *reinterpret_cast<StateSmem*>(align1024(smem_raw));
   grid_dependency_wait();
   const int per_seg = p.nh * (kD / kDvb);
   const int r = blockIdx.x / per_seg, rem = blockIdx.x - r * per_seg;
@@ -796,6 +966,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
   const int first = sg.x, nch = min(sg.y, p.hdr[0] - sg.x);
   if (first < 0 || nch <= 0) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (!state_pipe_start<kChan, false>(sm.pp, maps, p, sg, nch, h, vb, tid)) return;
   const int r0 = 16 * (warp & 3);   // token rows of the E / O products
   const int n0 = 16 * (warp >> 2);  // their value columns
   const int m0 = 16 * warp;         // state rows (d_k)
@@ -805,18 +976,16 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) hreg[n][e] = 0.f;
   const uint32_t sH = smem_u32(sm.H), sE = smem_u32(sm.E), sE2 = smem_u32(sm.E2);
-  load_stage<kChan>(sm.st[0], p, first, h, vb, tid);
-  cp_async_commit();
-  if (nch > 1) load_stage<kChan>(sm.st[1], p, first + 1, h, vb, tid);
-  cp_async_commit();
   for (int ci = 0; ci < nch; ++ci) {
-    // Stage (ci + 2) % 3 was last read by chunk ci - 1 (done: the barrier at
-    // the end of that chunk).  One group is committed per chunk, so at most
-    // the two newest groups (chunks ci + 1, ci + 2) are still in flight.
-    if (ci + 2 < nch) load_stage<kChan>(sm.st[(ci + 2) % kStateStages], p, first + ci + 2, h, vb, tid);
-    cp_async_commit();
-    cp_async_wait<2>();
-    // H (bf16) for this chunk's products
+    const int st = ci % kStateStages;
+    StateStage& s = sm.pp.st[st];
+    const int4 ch = seg_chunk(sg, ci);
+    const int t0 = ch.x, len = chunk_len(ch, p.total);
+    const bool landed =
+        mbar_wait(smem_u32(&sm.pp.full[st]), (uint32_t)(ci / kStateStages) & 1u, &sm.pp.abort, p.status);
+    if (landed && len > 0 && len < kC) zero_tail_rows(s, len, tid);
+    // H (bf16) for this chunk's products.  Its last readers (the previous
+    // chunk's E / Q H products) finished before that chunk's second barrier.
 #pragma unroll
     for (int n = 0; n < 4; ++n)
 #pragma unroll
@@ -825,10 +994,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
         const int j = 8 * n + 2 * (lane & 3);
         *reinterpret_cast<uint32_t*>(&sm.H[i * kS32 + j]) = pack2(hreg[n][2 * hr], hreg[n][2 * hr + 1]);
       }
-    __syncthreads();
-    StateStage& s = sm.st[ci % kStateStages];
-    const int4 ch = p.chunks[first + ci];
-    const int t0 = ch.x, len = chunk_len(ch, p.total);
+    if (compute_sync_or(!landed)) return;  // the producer drains the copies in flight
     if (kStore) {
       // H (bf16) of this chunk start: 128 rows x 64 bytes of this CTA's columns
       __nv_bfloat16* dst = p.H0 + ((size_t)(first + ci) * p.nh + h) * (kD * kD) + kDvb * vb;
@@ -838,7 +1004,8 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
       }
     }
     if (len <= 0) {  // only with a boundary list that breaks its rules
-      __syncthreads();
+      compute_sync();  // the H reads above before the next chunk's H write
+      release_stage(sm.pp, st, lane);
       continue;
     }
     const uint32_t sW = smem_u32(s.W), sK = smem_u32(s.K), sQ = smem_u32(s.Q), sAq = smem_u32(s.Aq);
@@ -852,8 +1019,8 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
 #pragma unroll
     for (int kk = 0; kk < kD / 16; ++kk) {
       uint32_t aw[4], aq[4], b[4];
-      ldsm_x4(aw, frag_a(sW, kS128, r0, 16 * kk, lane));
-      ldsm_x4(aq, frag_a(sQ, kS128, r0, 16 * kk, lane));
+      ldsm_x4(aw, frag_a_sw(sW, r0, 16 * kk, lane));
+      ldsm_x4(aq, frag_a_sw(sQ, r0, 16 * kk, lane));
       ldsm_x4_t(b, frag_b(sH, kS32, 16 * kk, n0, lane));
       mma_bf16(ce[0], aw, b[0], b[1]);
       mma_bf16(ce[1], aw, b[2], b[3]);
@@ -862,19 +1029,21 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
         mma_bf16(cq[1], aq, b[2], b[3]);
       }
     }
+    // E and E2 overwrite the previous chunk's, whose readers (its O and state
+    // update) finished before this chunk's first barrier.
 #pragma unroll
     for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int i = r0 + (lane >> 2) + 8 * hr;
         const int j = n0 + 8 * n + 2 * (lane & 3);
-        const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&s.U[i * kS32 + j]));
+        const float2 u = cols_pair(s, i, j);
         const float e0 = u.x - ce[n][2 * hr], e1 = u.y - ce[n][2 * hr + 1];
         const float w = i < len ? (kChan ? 1.f : __expf(g_last - s.gam[i])) : 0.f;
         *reinterpret_cast<uint32_t*>(&sm.E[i * kS32 + j]) = pack2(e0, e1);
         *reinterpret_cast<uint32_t*>(&sm.E2[i * kS32 + j]) = pack2(e0 * w, e1 * w);
       }
-    __syncthreads();
+    compute_sync();
     if (kStore) {
       for (int e = tid; e < kC * 4; e += kStateThreads) {
         const int rr = e >> 2, cc = (e & 3) * 8;
@@ -883,34 +1052,34 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
               *reinterpret_cast<const uint4*>(&sm.E[rr * kS32 + cc]);
       }
     } else {
-    // ---- O = scale (e^gamma Q H + Aq E)
-    float co[2][4];
+      // ---- O = scale (e^gamma Q H + Aq E)
+      float co[2][4];
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+      for (int n = 0; n < 2; ++n)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) co[n][e] = 0.f;
+        for (int e = 0; e < 4; ++e) co[n][e] = 0.f;
 #pragma unroll
-    for (int kk = 0; kk < kC / 16; ++kk) {
-      uint32_t a[4], b[4];
-      ldsm_x4(a, frag_a(sAq, kS64, r0, 16 * kk, lane));
-      ldsm_x4_t(b, frag_b(sE, kS32, 16 * kk, n0, lane));
-      mma_bf16(co[0], a, b[0], b[1]);
-      mma_bf16(co[1], a, b[2], b[3]);
-    }
+      for (int kk = 0; kk < kC / 16; ++kk) {
+        uint32_t a[4], b[4];
+        ldsm_x4(a, frag_a_sw(sAq, r0, 16 * kk, lane));
+        ldsm_x4_t(b, frag_b(sE, kS32, 16 * kk, n0, lane));
+        mma_bf16(co[0], a, b[0], b[1]);
+        mma_bf16(co[1], a, b[2], b[3]);
+      }
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int i = r0 + (lane >> 2) + 8 * hr;
-      if (i < len) {
-        const float eg = kChan ? 1.f : __expf(s.gam[i]);
-        __nv_bfloat16* orow = p.o + ((size_t)(t0 + i) * p.nh + h) * kD + kDvb * vb + n0;
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = r0 + (lane >> 2) + 8 * hr;
+        if (i < len) {
+          const float eg = kChan ? 1.f : __expf(s.gam[i]);
+          __nv_bfloat16* orow = p.o + ((size_t)(t0 + i) * p.nh + h) * kD + kDvb * vb + n0;
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          const int j = 8 * n + 2 * (lane & 3);
-          *reinterpret_cast<uint32_t*>(orow + j) = pack2(p.scale * (eg * cq[n][2 * hr] + co[n][2 * hr]),
-                                                         p.scale * (eg * cq[n][2 * hr + 1] + co[n][2 * hr + 1]));
+          for (int n = 0; n < 2; ++n) {
+            const int j = 8 * n + 2 * (lane & 3);
+            *reinterpret_cast<uint32_t*>(orow + j) = pack2(p.scale * (eg * cq[n][2 * hr] + co[n][2 * hr]),
+                                                           p.scale * (eg * cq[n][2 * hr + 1] + co[n][2 * hr + 1]));
+          }
         }
       }
-    }
     }
     // ---- H = e^gamma_last H + K^T E2 (state rows [m0, +16); K^T read from K[token][d_k])
     // rows m0 + lane / 4 (elements 0, 1) and + 8 (elements 2, 3)
@@ -926,7 +1095,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
       uint32_t a[4], b0[4], b1[4];
-      ldsm_x4_t(a, frag_bt(sK, kS128, 16 * kk, m0, lane));
+      ldsm_x4_t(a, frag_bt_sw(sK, 16 * kk, m0, lane));
       ldsm_x4_t(b0, frag_b(sE2, kS32, 16 * kk, 0, lane));
       ldsm_x4_t(b1, frag_b(sE2, kS32, 16 * kk, 16, lane));
       mma_bf16(hreg[0], a, b0[0], b0[1]);
@@ -934,9 +1103,8 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
       mma_bf16(hreg[2], a, b1[0], b1[1]);
       mma_bf16(hreg[3], a, b1[2], b1[3]);
     }
-    __syncthreads();  // this stage, H, E and E2 are reused by the next chunk
+    release_stage(sm.pp, st, lane);
   }
-  cp_async_wait<0>();
 }
 
 
@@ -947,55 +1115,22 @@ __global__ void __launch_bounds__(kStateThreads) gdn_state_kernel(GdnParams p) {
 //     dE  = scale Aq^T dO + diag(e^(gamma_last - gamma)) K dH
 //     dH0 = e^gamma_last dH + scale Q^T diag(e^gamma) dO - W^T dE
 // dE and the bf16 dH of every chunk go to the workspace for the local pass.
-struct BwdStage {
-  __nv_bfloat16 K[kC * kS128];
-  __nv_bfloat16 Q[kC * kS128];
-  __nv_bfloat16 W[kC * kS128];
-  __nv_bfloat16 Aq[kC * kS64];
-  __nv_bfloat16 dO[kC * kS32];
-  float gam[kD];  // as StateStage::gam
-};
+// The same pipeline as the forward state pass, over the chunks in reverse.
 struct BwdStateSmem {
-  BwdStage st[kStateStages];
+  StatePipe pp;                  // W, K, Q, Aq, dO, gates
   __nv_bfloat16 H[kD * kS32];    // dH (bf16)
   __nv_bfloat16 E[kC * kS32];    // dE (bf16)
   __nv_bfloat16 G[kC * kS32];    // scale e^gamma dO (bf16)
 };
-static_assert(sizeof(BwdStateSmem) <= 227 * 1024, "the backward state CTA's shared memory fits one SM");
-
-template <bool kChan>
-__device__ __forceinline__ void load_bwd_stage(BwdStage& s, const GdnParams& p, int chunk, int h, int vb, int tid) {
-  constexpr int nt = kStateThreads;
-  const int4 ch = p.chunks[chunk];
-  const int len = chunk_len(ch, p.total), t0 = len > 0 ? ch.x : 0;
-  load_rows128(smem_u32(s.K), kChan ? p.KC : p.k, t0, len, h, p.nh, tid, nt);
-  load_rows128(smem_u32(s.Q), kChan ? p.QB : p.q, t0, len, h, p.nh, tid, nt);
-  load_rows128(smem_u32(s.W), p.W, t0, len, h, p.nh, tid, nt);
-  for (int e = tid; e < kC * 4; e += nt) {  // dO columns [32 vb, 32 vb + 32)
-    const int r = e >> 2, cc = (e & 3) * 8;
-    const bool ok = r < len;
-    cp_async16(smem_u32(&s.dO[r * kS32 + cc]), p.dO + ((size_t)(t0 + (ok ? r : 0)) * p.nh + h) * kD + kDvb * vb + cc,
-               ok);
-  }
-  const __nv_bfloat16* aq = p.Aqk + ((size_t)chunk * p.nh + h) * (kC * kC);
-  for (int e = tid; e < kC * 8; e += nt) {
-    const int r = e >> 3, cc = (e & 7) * 8;
-    cp_async16(smem_u32(&s.Aq[r * kS64 + cc]), aq + r * kC + cc, true);
-  }
-  if (kChan) {
-    if (tid < kD / 4) cp_async16(smem_u32(&s.gam[4 * tid]), p.Bc + ((size_t)chunk * p.nh + h) * kD + 4 * tid, true);
-  } else if (tid < kC) {
-    const bool ok = tid < len;
-    cp_async4(smem_u32(&s.gam[tid]), p.gam + (size_t)h * p.total + t0 + (ok ? tid : 0), ok);
-  }
-}
+static_assert(sizeof(BwdStateSmem) + 1024 <= 227 * 1024, "the backward state CTA's shared memory fits one SM");
 
 // kChan (Kimi Delta): KC and QB replace K and Q (no per-token factors), and
 // the gradient decays by e^gamma_last per channel (row).
 template <bool kChan>
-__global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams p) {
+__global__ void __launch_bounds__(kStateBlock) gdn_bwd_state_kernel(const __grid_constant__ StateMaps maps,
+                                                                    GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  BwdStateSmem& sm = *reinterpret_cast<BwdStateSmem*>(smem_raw);
+  BwdStateSmem& sm = *reinterpret_cast<BwdStateSmem*>(align1024(smem_raw));
   grid_dependency_wait();
   const int per_seg = p.nh * (kD / kDvb);
   const int r = blockIdx.x / per_seg, rem = blockIdx.x - r * per_seg;
@@ -1005,6 +1140,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
   const int first = sg.x, nch = min(sg.y, p.hdr[0] - sg.x);
   if (first < 0 || nch <= 0) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (!state_pipe_start<kChan, true>(sm.pp, maps, p, sg, nch, h, vb, tid)) return;
   const int r0 = 16 * (warp & 3);   // token rows of dE
   const int n0 = 16 * (warp >> 2);  // its value columns
   const int m0 = 16 * warp;         // dH rows (d_k)
@@ -1014,15 +1150,18 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
 #pragma unroll
     for (int e = 0; e < 4; ++e) dh[n][e] = 0.f;
   const uint32_t sH = smem_u32(sm.H), sE = smem_u32(sm.E), sG = smem_u32(sm.G);
-  // chunk ci (0 = the segment's last) is chunk first + nch - 1 - ci, in stage ci % 3
-  load_bwd_stage<kChan>(sm.st[0], p, first + nch - 1, h, vb, tid);
-  cp_async_commit();
-  if (nch > 1) load_bwd_stage<kChan>(sm.st[1], p, first + nch - 2, h, vb, tid);
-  cp_async_commit();
+  // step ci (0 = the segment's last chunk) is chunk first + nch - 1 - ci, in stage ci % 3
   for (int ci = 0; ci < nch; ++ci) {
-    if (ci + 2 < nch) load_bwd_stage<kChan>(sm.st[(ci + 2) % kStateStages], p, first + nch - 3 - ci, h, vb, tid);
-    cp_async_commit();
-    cp_async_wait<2>();
+    const int st = ci % kStateStages;
+    const int chunk = first + nch - 1 - ci;
+    StateStage& s = sm.pp.st[st];
+    const int4 ch = seg_chunk(sg, nch - 1 - ci);
+    const int t0 = ch.x, len = chunk_len(ch, p.total);
+    const bool landed =
+        mbar_wait(smem_u32(&sm.pp.full[st]), (uint32_t)(ci / kStateStages) & 1u, &sm.pp.abort, p.status);
+    if (landed && len > 0 && len < kC) zero_tail_rows(s, len, tid);
+    // dH (bf16); its last readers (the previous step's dE products and dH1
+    // store) finished before that step's second barrier
 #pragma unroll
     for (int n = 0; n < 4; ++n)
 #pragma unroll
@@ -1031,11 +1170,7 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
         const int j = 8 * n + 2 * (lane & 3);
         *reinterpret_cast<uint32_t*>(&sm.H[i * kS32 + j]) = pack2(dh[n][2 * hr], dh[n][2 * hr + 1]);
       }
-    __syncthreads();
-    const int chunk = first + nch - 1 - ci;
-    BwdStage& s = sm.st[ci % kStateStages];
-    const int4 ch = p.chunks[chunk];
-    const int t0 = ch.x, len = chunk_len(ch, p.total);
+    if (compute_sync_or(!landed)) return;  // the producer drains the copies in flight
     {
       __nv_bfloat16* dst = p.dH1 + ((size_t)chunk * p.nh + h) * (kD * kD) + kDvb * vb;
       for (int e = tid; e < kD * 4; e += kStateThreads) {
@@ -1044,11 +1179,12 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
       }
     }
     if (len <= 0) {  // only with a boundary list that breaks its rules
-      __syncthreads();
+      compute_sync();  // the dH reads above before the next step's dH write
+      release_stage(sm.pp, st, lane);
       continue;
     }
     const uint32_t sK = smem_u32(s.K), sQ = smem_u32(s.Q), sW = smem_u32(s.W), sAq = smem_u32(s.Aq),
-                   sdO = smem_u32(s.dO);
+                   sdO = smem_u32(s.cols);
     const float g_last = kChan ? 0.f : s.gam[len - 1];
     // ---- dE = scale Aq^T dO + diag(e^(gamma_last - gamma)) K dH
     float ca[2][4], ck[2][4];
@@ -1059,19 +1195,21 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
       uint32_t a[4], b[4];
-      ldsm_x4_t(a, frag_bt(sAq, kS64, 16 * kk, r0, lane));  // Aq^T: Aq stored [i][j]
-      ldsm_x4_t(b, frag_b(sdO, kS32, 16 * kk, n0, lane));
+      ldsm_x4_t(a, frag_bt_sw(sAq, 16 * kk, r0, lane));  // Aq^T: Aq stored [i][j]
+      ldsm_x4_t(b, frag_b_cols(sdO, 16 * kk, n0, lane));
       mma_bf16(ca[0], a, b[0], b[1]);
       mma_bf16(ca[1], a, b[2], b[3]);
     }
 #pragma unroll
     for (int kk = 0; kk < kD / 16; ++kk) {
       uint32_t a[4], b[4];
-      ldsm_x4(a, frag_a(sK, kS128, r0, 16 * kk, lane));
+      ldsm_x4(a, frag_a_sw(sK, r0, 16 * kk, lane));
       ldsm_x4_t(b, frag_b(sH, kS32, 16 * kk, n0, lane));
       mma_bf16(ck[0], a, b[0], b[1]);
       mma_bf16(ck[1], a, b[2], b[3]);
     }
+    // dE and G overwrite the previous step's, whose readers finished before
+    // this step's first barrier
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int i = r0 + (lane >> 2) + 8 * hr;
@@ -1088,10 +1226,10 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
     for (int e = tid; e < kC * 16; e += kStateThreads) {
       const int i = e >> 4, j = (e & 15) * 2;
       const float m = i < len ? p.scale * (kChan ? 1.f : __expf(s.gam[i])) : 0.f;
-      const float2 d = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&s.dO[i * kS32 + j]));
+      const float2 d = cols_pair(s, i, j);
       *reinterpret_cast<uint32_t*>(&sm.G[i * kS32 + j]) = pack2(m * d.x, m * d.y);
     }
-    __syncthreads();
+    compute_sync();
     for (int e = tid; e < kC * 4; e += kStateThreads) {
       const int rr = e >> 2, cc = (e & 3) * 8;
       if (rr < len)
@@ -1114,8 +1252,8 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
       uint32_t aq[4], aw[4], g0[4], g1[4], e0[4], e1[4];
-      ldsm_x4_t(aq, frag_bt(sQ, kS128, 16 * kk, m0, lane));
-      ldsm_x4_t(aw, frag_bt(sW, kS128, 16 * kk, m0, lane));
+      ldsm_x4_t(aq, frag_bt_sw(sQ, 16 * kk, m0, lane));
+      ldsm_x4_t(aw, frag_bt_sw(sW, 16 * kk, m0, lane));
       ldsm_x4_t(g0, frag_b(sG, kS32, 16 * kk, 0, lane));
       ldsm_x4_t(g1, frag_b(sG, kS32, 16 * kk, 16, lane));
       ldsm_x4_t(e0, frag_b(sE, kS32, 16 * kk, 0, lane));
@@ -1133,9 +1271,8 @@ __global__ void __launch_bounds__(kStateThreads) gdn_bwd_state_kernel(GdnParams 
     for (int n = 0; n < 4; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) dh[n][e] -= cw[n][e];
-    __syncthreads();
+    release_stage(sm.pp, st, lane);
   }
-  cp_async_wait<0>();
 }
 
 // ============================================================== backward: local, with the states
@@ -2545,6 +2682,72 @@ cudaError_t launch_kda_prep(const GdnParams& p, cudaStream_t s) {
   return e;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && f)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// An N-D bf16 map: sizes (innermost first), byte strides of the outer
+// dimensions, box, swizzle.  Out-of-range rows read as zero.
+template <int N>
+bool encode_bf16_map(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[N],
+                     const cuuint64_t (&strides)[N - 1], const cuuint32_t (&box)[N],
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint32_t es[N];
+  for (int i = 0; i < N; ++i) es[i] = 1;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The state passes' maps (StateMaps) over the inputs and the workspace.
+int make_state_maps(StateMaps& m, const GdnParams& p) {
+  // (64 columns, token, column half, head): the box's order in shared memory
+  // is [half][token][64 columns], the two swizzled halves of the tile
+  const cuuint64_t rows[4] = {64, (cuuint64_t)p.total, 2, (cuuint64_t)p.nh};
+  const cuuint64_t row_str[3] = {(cuuint64_t)p.nh * kD * 2, 64 * 2, (cuuint64_t)kD * 2};
+  const cuuint32_t row_box[4] = {64, (cuuint32_t)kC, 2, 1};
+  const cuuint64_t blocks[3] = {(cuuint64_t)kC, (cuuint64_t)kC, (cuuint64_t)p.max_chunks * p.nh};
+  const cuuint64_t blk_str[2] = {(cuuint64_t)kC * 2, (cuuint64_t)kC * kC * 2};
+  const cuuint32_t blk_box[3] = {(cuuint32_t)kC, (cuuint32_t)kC, 1};
+  // value columns: (128 columns, head, token), box 32 columns x 1 x 64 tokens
+  const cuuint64_t cols[3] = {(cuuint64_t)kD, (cuuint64_t)p.nh, (cuuint64_t)p.total};
+  const cuuint64_t col_str[2] = {(cuuint64_t)kD * 2, (cuuint64_t)p.nh * kD * 2};
+  const cuuint32_t col_box[3] = {(cuuint32_t)kDvb, 1, (cuuint32_t)kC};
+  const bool chan = p.KC != nullptr;  // Kimi Delta
+  m = StateMaps{};
+  bool ok = encode_bf16_map(&m.w, p.W, rows, row_str, row_box) &&
+            encode_bf16_map(&m.k, chan ? p.KC : p.k, rows, row_str, row_box) &&
+            encode_bf16_map(&m.q, chan ? p.QB : p.q, rows, row_str, row_box) &&
+            encode_bf16_map(&m.aq, p.Aqk, blocks, blk_str, blk_box) &&
+            encode_bf16_map(&m.u, p.U, cols, col_str, col_box, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (ok && p.dO) ok = encode_bf16_map(&m.d_o, p.dO, cols, col_str, col_box, CU_TENSOR_MAP_SWIZZLE_64B);
+  return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// A state pass: the maps, the parameters, and 1024 bytes of shared-memory
+// slack for the stage alignment.
+template <typename Smem, typename... KArgs>
+cudaError_t launch_state(void (*kernel)(KArgs...), dim3 grid, cudaStream_t s, const StateMaps& m,
+                         const GdnParams& p) {
+  const int bytes = (int)sizeof(Smem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) e = launch_pdl(kernel, grid, dim3(kStateBlock), (size_t)bytes, s, m, p);
+  return e;
+}
+
 template <typename Smem, typename... KArgs>
 cudaError_t launch_big(void (*kernel)(KArgs...), dim3 grid, cudaStream_t s, const GdnParams& p,
                        int threads = kStateThreads) {
@@ -2584,10 +2787,13 @@ int gdn_varlen_fwd(const void* q, const void* k, const void* v, const float* g, 
   if ((rc = device_for_call(&status, &sms))) return rc;
   if (total == 0) return ATTN_OK;
   p.o = static_cast<__nv_bfloat16*>(o);
+  p.status = status;
+  StateMaps maps;
+  if ((rc = make_state_maps(maps, p))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_gdn_prep(p, s);
   const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
-  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<false, false>, seg_grid, s, p);
+  if (e == cudaSuccess) e = launch_state<StateSmem>(gdn_state_kernel<false, false>, seg_grid, s, maps, p);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -2615,12 +2821,15 @@ int gdn_varlen_bwd(const void* q, const void* k, const void* v, const float* g, 
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.dg = dg;
   p.dbeta = dbeta;
+  p.status = status;
+  StateMaps maps;
+  if ((rc = make_state_maps(maps, p))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
   const dim3 chunk_grid((unsigned)p.max_chunks, (unsigned)num_heads);
   cudaError_t e = launch_gdn_prep(p, s);
-  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<true, false>, seg_grid, s, p);
-  if (e == cudaSuccess) e = launch_big<BwdStateSmem>(gdn_bwd_state_kernel<false>, seg_grid, s, p);
+  if (e == cudaSuccess) e = launch_state<StateSmem>(gdn_state_kernel<true, false>, seg_grid, s, maps, p);
+  if (e == cudaSuccess) e = launch_state<BwdStateSmem>(gdn_bwd_state_kernel<false>, seg_grid, s, maps, p);
   if (e == cudaSuccess) e = launch_big<LocalHSmem>(gdn_bwd_local_h_kernel, chunk_grid, s, p, kLocalThreads);
   if (e == cudaSuccess) e = launch_big<LocalWySmem>(gdn_bwd_local_wy_kernel, chunk_grid, s, p, kLocalThreads);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -2648,10 +2857,12 @@ int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* g, 
   if (total == 0) return ATTN_OK;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.status = status;
+  StateMaps maps;
+  if ((rc = make_state_maps(maps, p))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_kda_prep(p, s);
   const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
-  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<false, true>, seg_grid, s, p);
+  if (e == cudaSuccess) e = launch_state<StateSmem>(gdn_state_kernel<false, true>, seg_grid, s, maps, p);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -2686,12 +2897,14 @@ int kda_varlen_bwd(const void* q, const void* k, const void* v, const float* g, 
   p.dg = dg;
   p.dbeta = dbeta;
   p.status = status;
+  StateMaps maps;
+  if ((rc = make_state_maps(maps, p))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
   const dim3 chunk_grid((unsigned)p.max_chunks, (unsigned)num_heads);
   cudaError_t e = launch_kda_prep(p, s);
-  if (e == cudaSuccess) e = launch_big<StateSmem>(gdn_state_kernel<true, true>, seg_grid, s, p);
-  if (e == cudaSuccess) e = launch_big<BwdStateSmem>(gdn_bwd_state_kernel<true>, seg_grid, s, p);
+  if (e == cudaSuccess) e = launch_state<StateSmem>(gdn_state_kernel<true, true>, seg_grid, s, maps, p);
+  if (e == cudaSuccess) e = launch_state<BwdStateSmem>(gdn_bwd_state_kernel<true>, seg_grid, s, maps, p);
   if (e == cudaSuccess) e = launch_big<KdaLocalHSmem>(kda_bwd_local_h_kernel, chunk_grid, s, p, kLocalThreads);
   if (e == cudaSuccess) e = launch_big<KdaLocalWySmem>(kda_bwd_local_wy_kernel, chunk_grid, s, p, kLocalThreads);
   if (e == cudaSuccess) e = launch_big<KdaExpSmem>(kda_bwd_exp_kernel, chunk_grid, s, p, kLocalThreads);
