@@ -763,24 +763,41 @@ def main():
         ws = torch.empty(f_ws(gw.total, gw.nh, nseg), dtype=torch.uint8, device=dev)
         fwd = lambda: f_fwd(q, k, v, g_, be, cu, gw.scale, o, ws)  # noqa: E731
         bwd = lambda: f_bwd(q, k, v, g_, be, do, cu, gw.scale, dq, dk, dv, dg, db, ws)  # noqa: E731
-        for _ in range(warmup):
-            fwd()
-            bwd()
-            flush.fill_(1.0)
-        torch.cuda.synchronize()
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-        for i in range(steps):
-            flush.fill_(float(i))
-            evs[i][0].record(stream)
-            fwd()
-            evs[i][1].record(stream)
-            flush.fill_(float(i) + 0.5)
-            evs[i][2].record(stream)
-            bwd()
-            evs[i][3].record(stream)
-        torch.cuda.synchronize()
-        f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-        b_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+
+        def timed(fwd, bwd):
+            for _ in range(warmup):
+                fwd()
+                bwd()
+                flush.fill_(1.0)
+            torch.cuda.synchronize()
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+            for i in range(steps):
+                flush.fill_(float(i))
+                evs[i][0].record(stream)
+                fwd()
+                evs[i][1].record(stream)
+                flush.fill_(float(i) + 0.5)
+                evs[i][2].record(stream)
+                bwd()
+                evs[i][3].record(stream)
+            torch.cuda.synchronize()
+            return (statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+                    statistics.mean(e[2].elapsed_time(e[3]) for e in evs))
+
+        f_ms, b_ms = timed(fwd, bwd)
+        # The training pair that keeps the forward's factors, states and E for
+        # the backward (the *_fwd_save / *_bwd_saved calls), on the same
+        # workspace: its times, and its outputs against the pair above, bit for bit.
+        ref_plain = [x.clone() for x in (o, dq, dk, dv, dg, db)]
+        f_save, f_saved = ((binding.kda_varlen_fwd_save, binding.kda_varlen_bwd_saved) if gw.per_channel else
+                           (binding.gdn_varlen_fwd_save, binding.gdn_varlen_bwd_saved))
+        fs_ms, bs_ms = timed(lambda: f_save(q, k, v, g_, be, cu, gw.scale, o, ws),
+                             lambda: f_saved(q, k, v, g_, be, do, cu, gw.scale, dq, dk, dv, dg, db, ws))
+        saved_res = {"fwd_ms": fs_ms, "bwd_ms": bs_ms, "step_ms": fs_ms + bs_ms,
+                     "page_ratio": ((fs_ms + bs_ms) / (PAGE_KDA_MS if gw.per_channel else PAGE_GDN_MS)
+                                    if gw.context == 4096 else None),
+                     "bit_exact_vs_recomputing": all(torch.equal(a, b)
+                                                     for a, b in zip(ref_plain, (o, dq, dk, dv, dg, db)))}
         # The same step captured in a CUDA graph over the boundary list padded
         # with empty segments to 42 (the page replays these layers too, section
         # 06): replay time, and its outputs against the eager step's bits.
@@ -838,6 +855,7 @@ def main():
                                           "own unnamed GPU (research.dws.rip/llm/kernels, Fig. 5)"}
                                  if gw.context == 4096 else None),
                 "graph": graph_res,
+                "saved": saved_res,
                 "status": status}
 
     gdn = {}

@@ -89,6 +89,29 @@ int gdn_varlen_bwd(const void* q, const void* k, const void* v, const float* g, 
                    void* workspace, size_t workspace_bytes, int64_t total, int32_t num_heads, int32_t head_dim,
                    int32_t num_segments, void* stream);
 
+/* A training step's pair: the forward above that also keeps, in a workspace
+ * sized for the backward, everything the backward would recompute (the
+ * chunk tables, the WY factors, the state at every chunk start and every
+ * chunk's E), and the backward that reads them instead.  Same results, bit
+ * for bit, as gdn_varlen_fwd and gdn_varlen_bwd; the backward saves the plan,
+ * the prep pass and the recomputing state pass.
+ *
+ * gdn_varlen_fwd_save: the arguments of gdn_varlen_fwd, with workspace of at
+ * least gdn_varlen_bwd_workspace_bytes(T, H, num_segments) bytes.
+ * gdn_varlen_bwd_saved: the arguments of gdn_varlen_bwd.  It trusts the
+ * workspace: it must be the one the last gdn_varlen_fwd_save on this stream
+ * wrote, with the same q, k, v, g, beta, cu_seqlens, scale and sizes, and no
+ * other call may have used it in between.  Otherwise the gradients are
+ * meaningless, though every access stays inside the caller's buffers.
+ * Error codes as the calls they pair. */
+int gdn_varlen_fwd_save(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                        const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes,
+                        int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream);
+int gdn_varlen_bwd_saved(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const void* d_o, const int32_t* cu_seqlens, float scale, void* dq, void* dk, void* dv,
+                         float* dg, float* dbeta, void* workspace, size_t workspace_bytes, int64_t total,
+                         int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

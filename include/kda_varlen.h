@@ -71,6 +71,20 @@ int kda_varlen_bwd(const void* q, const void* k, const void* v, const float* g, 
                    void* workspace, size_t workspace_bytes, int64_t total, int32_t num_heads, int32_t head_dim,
                    int32_t num_segments, void* stream);
 
+/* The training step's pair, as gdn_varlen_fwd_save / gdn_varlen_bwd_saved:
+ * kda_varlen_fwd_save takes the arguments of kda_varlen_fwd with a workspace
+ * of at least kda_varlen_bwd_workspace_bytes(T, H, num_segments) bytes and
+ * also keeps X, the unscaled A, the states and E there; kda_varlen_bwd_saved
+ * takes the arguments of kda_varlen_bwd and trusts that workspace the same
+ * way.  Same results, bit for bit, as kda_varlen_fwd and kda_varlen_bwd. */
+int kda_varlen_fwd_save(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                        const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes,
+                        int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream);
+int kda_varlen_bwd_saved(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const void* d_o, const int32_t* cu_seqlens, float scale, void* dq, void* dk, void* dv,
+                         float* dg, float* dbeta, void* workspace, size_t workspace_bytes, int64_t total,
+                         int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -210,3 +210,31 @@ def test_gdn_backward_argument_validation(clib):
     assert bwd(ws_bytes=4096) == -14
     f, fb = clib.gdn_varlen_workspace_bytes, clib.gdn_varlen_bwd_workspace_bytes
     assert fb(16384, 8, 25) > f(16384, 8, 25) > 0
+
+
+def test_saving_forward_and_saved_backward_check_their_arguments(clib):
+    # The saving forward keeps the backward's data: it needs the backward's
+    # workspace size.  The saved backward checks what the backward checks.
+    vp = ctypes.c_void_p
+    for pre in ("gdn", "kda"):
+        fwd_save = getattr(clib, f"{pre}_varlen_fwd_save")
+        bwd_saved = getattr(clib, f"{pre}_varlen_bwd_saved")
+        nf = getattr(clib, f"{pre}_varlen_workspace_bytes")(64, 8, 1)
+        nb = getattr(clib, f"{pre}_varlen_bwd_workspace_bytes")(64, 8, 1)
+        assert nb > nf > 0
+
+        def fwd(ws_bytes, o=16, d=128):
+            return fwd_save(vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), 0.088, vp(o), vp(256), ws_bytes, 64, 8, d,
+                            1, vp(None))
+
+        assert fwd(nf) == -14
+        assert fwd(nb, o=None) == -1
+        assert fwd(nb, d=64) == -3
+
+        def bwd(ws_bytes, dq=16):
+            return bwd_saved(vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), 0.088, vp(dq), vp(16), vp(16),
+                             vp(16), vp(16), vp(256), ws_bytes, 64, 8, 128, 1, vp(None))
+
+        assert bwd(nf) == -14
+        assert bwd(nb, dq=None) == -1
+        assert bwd(nb, dq=40) == -4

@@ -211,6 +211,55 @@ def test_cuda_graph_replay_with_padded_boundaries_is_bit_exact():
     _graph_replay_is_bit_exact(synth.gdn_workloads(), "gdn_ctx4096", False)
 
 
+def check_saved_pair(wls, name, per_channel):
+    """The saving forward and the backward on its workspace
+    (include/gdn_varlen.h, include/kda_varlen.h) give the bits of the
+    recomputing pair: o, dq, dk, dv, dg, dbeta all equal, also when the
+    saved pair runs twice on one workspace."""
+    import torch
+    from varlen_sliding_window_gb300 import binding as b
+    w = wls[name]
+    inp = w.inputs()
+    pre = "kda" if per_channel else "gdn"
+    fwd, bwd = getattr(b, f"{pre}_varlen_fwd"), getattr(b, f"{pre}_varlen_bwd")
+    fwd_save, bwd_saved = getattr(b, f"{pre}_varlen_fwd_save"), getattr(b, f"{pre}_varlen_bwd_saved")
+    ws_f, ws_b = getattr(b, f"{pre}_varlen_workspace_bytes"), getattr(b, f"{pre}_varlen_bwd_workspace_bytes")
+    q, k, v, do = (_to_dev(x) for x in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
+    g = torch.from_numpy(inp.g).cuda()
+    beta = torch.from_numpy(inp.beta).cuda()
+    cu = torch.from_numpy(inp.cu_seqlens).cuda()
+    T, nh, _ = q.shape
+    nseg = len(inp.cu_seqlens) - 1
+
+    def outs():
+        o = torch.full_like(q, float("nan"))
+        grads = [torch.full_like(q, float("nan")) for _ in range(3)] + [torch.full_like(g, float("nan")),
+                                                                         torch.full_like(beta, float("nan"))]
+        return o, grads
+
+    o1, g1 = outs()
+    wf = torch.empty(ws_f(T, nh, nseg), dtype=torch.uint8, device="cuda")
+    wb = torch.empty(ws_b(T, nh, nseg), dtype=torch.uint8, device="cuda")
+    fwd(q, k, v, g, beta, cu, w.scale, o1, wf)
+    bwd(q, k, v, g, beta, do, cu, w.scale, *g1, wb)
+    ws = torch.empty(ws_b(T, nh, nseg), dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        o2, g2 = outs()
+        fwd_save(q, k, v, g, beta, cu, w.scale, o2, ws)
+        bwd_saved(q, k, v, g, beta, do, cu, w.scale, *g2, ws)
+        torch.cuda.synchronize()
+        assert b.attn_varlen_get_status() == 0
+        assert torch.equal(o1, o2)
+        for nm, a, c in zip(("dq", "dk", "dv", "dg", "dbeta"), g1, g2):
+            assert torch.equal(a, c), nm
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["gdn_ragged", "gdn_ctx4096"])
+def test_saving_forward_and_saved_backward_match_the_recomputing_pair(name):
+    check_saved_pair(WL, name, per_channel=False)
+
+
 # Ragged boundaries for the head-count cases: a 1-token segment, segments
 # ending one before, at and one after a 64-token chunk edge, an empty one.
 HEAD_CASE_CU = np.array([0, 1, 64, 65, 129, 129, 200, 330], dtype=np.int32)

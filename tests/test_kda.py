@@ -181,3 +181,10 @@ def test_gate_at_or_below_the_bound_sets_the_status_word():
 def test_head_counts(nh):
     from tests.test_gdn import check_head_counts
     check_head_counts(nh, per_channel=True)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["kda_ragged", "kda_ctx4096"])
+def test_saving_forward_and_saved_backward_match_the_recomputing_pair(name):
+    from tests.test_gdn import check_saved_pair
+    check_saved_pair(WL, name, per_channel=True)

@@ -83,6 +83,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.kda_varlen_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.kda_varlen_bwd.argtypes = lib.gdn_varlen_bwd.argtypes
     lib.kda_varlen_bwd.restype = ctypes.c_int
+    for name in ("gdn_varlen_fwd_save", "kda_varlen_fwd_save"):
+        getattr(lib, name).argtypes = lib.gdn_varlen_fwd.argtypes
+        getattr(lib, name).restype = ctypes.c_int
+    for name in ("gdn_varlen_bwd_saved", "kda_varlen_bwd_saved"):
+        getattr(lib, name).argtypes = lib.gdn_varlen_bwd.argtypes
+        getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -388,3 +394,59 @@ def kda_varlen_bwd(q, k, v, g, beta, d_o, cu_seqlens, scale: float, dq, dk, dv, 
                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(workspace),
                             int(workspace.numel()), total, nh, d, nseg, _stream_handle(stream))
     _check(rc, "kda_varlen_bwd")
+
+
+def _linear_fwd(name, q, k, v, g, beta, cu_seqlens, scale, o, workspace, stream):
+    _require_dense(name, q, k, v, o)
+    if not (g.is_contiguous() and beta.is_contiguous()):
+        raise ValueError("g and beta must be dense float32 tensors")
+    lib = load_library()
+    total, nh, d = (int(x) for x in q.shape)
+    nseg = int(cu_seqlens.numel()) - 1
+    rc = getattr(lib, name)(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), float(scale), _ptr(o),
+                            _ptr(workspace), int(workspace.numel()), total, nh, d, nseg, _stream_handle(stream))
+    _check(rc, name)
+
+
+def _linear_bwd(name, q, k, v, g, beta, d_o, cu_seqlens, scale, dq, dk, dv, dg, dbeta, workspace, stream):
+    _require_dense(name, q, k, v, d_o, dq, dk, dv)
+    for t in (g, beta, dg, dbeta):
+        if not t.is_contiguous():
+            raise ValueError("g, beta, dg and dbeta must be dense float32 tensors")
+    lib = load_library()
+    total, nh, d = (int(x) for x in q.shape)
+    nseg = int(cu_seqlens.numel()) - 1
+    rc = getattr(lib, name)(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(d_o), _ptr(cu_seqlens),
+                            float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(workspace),
+                            int(workspace.numel()), total, nh, d, nseg, _stream_handle(stream))
+    _check(rc, name)
+
+
+def gdn_varlen_fwd_save(q, k, v, g, beta, cu_seqlens, scale: float, o, workspace, stream=None) -> None:
+    """gdn_varlen_fwd that also keeps what the backward recomputes in
+    `workspace` (at least gdn_varlen_bwd_workspace_bytes(T, H, num_segments)
+    bytes), for gdn_varlen_bwd_saved (include/gdn_varlen.h)."""
+    _linear_fwd("gdn_varlen_fwd_save", q, k, v, g, beta, cu_seqlens, scale, o, workspace, stream)
+
+
+def gdn_varlen_bwd_saved(q, k, v, g, beta, d_o, cu_seqlens, scale: float, dq, dk, dv, dg, dbeta, workspace,
+                         stream=None) -> None:
+    """gdn_varlen_bwd on the workspace of the preceding gdn_varlen_fwd_save
+    with the same inputs: skips the recomputation, same bits."""
+    _linear_bwd("gdn_varlen_bwd_saved", q, k, v, g, beta, d_o, cu_seqlens, scale, dq, dk, dv, dg, dbeta, workspace,
+                stream)
+
+
+def kda_varlen_fwd_save(q, k, v, g, beta, cu_seqlens, scale: float, o, workspace, stream=None) -> None:
+    """kda_varlen_fwd that also keeps what the backward recomputes in
+    `workspace` (at least kda_varlen_bwd_workspace_bytes(T, H, num_segments)
+    bytes), for kda_varlen_bwd_saved (include/kda_varlen.h)."""
+    _linear_fwd("kda_varlen_fwd_save", q, k, v, g, beta, cu_seqlens, scale, o, workspace, stream)
+
+
+def kda_varlen_bwd_saved(q, k, v, g, beta, d_o, cu_seqlens, scale: float, dq, dk, dv, dg, dbeta, workspace,
+                         stream=None) -> None:
+    """kda_varlen_bwd on the workspace of the preceding kda_varlen_fwd_save
+    with the same inputs: skips the recomputation, same bits."""
+    _linear_bwd("kda_varlen_bwd_saved", q, k, v, g, beta, d_o, cu_seqlens, scale, dq, dk, dv, dg, dbeta, workspace,
+                stream)

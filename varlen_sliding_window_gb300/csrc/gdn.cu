@@ -948,11 +948,12 @@ __device__ __forceinline__ void release_stage(StatePipe& pp, int st, int lane) {
 // Eight compute warps.  Warp w computes, of the chunk's 64 x 32 products (E,
 // Q H, O), rows [16 (w % 4), +16) x columns [16 (w / 4), +16), and holds rows
 // [16 w, +16) of the 128 x 32 state.
-// kStore (the backward's recomputation): no O; the bf16 state at every chunk
-// start and every chunk's E go to the workspace instead.
+// kOut: O goes to p.o.  kStore (for the backward): the bf16 state at every
+// chunk start and every chunk's E go to the workspace.  The backward's own
+// recomputation stores without O; a saving forward does both.
 // kChan (Kimi Delta): K and Q arrive pre-scaled (KC, QB), so E and O take no
 // per-token factor, and the state decays by e^gamma_last per channel (row).
-template <bool kStore, bool kChan>
+template <bool kOut, bool kStore, bool kChan>
 __global__ void __launch_bounds__(kStateBlock) gdn_state_kernel(const __grid_constant__ StateMaps maps,
                                                                 GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -963,7 +964,9 @@ __global__ void __launch_bounds__(kStateBlock) gdn_state_kernel(const __grid_con
   const int h = rem / (kD / kDvb), vb = rem - h * (kD / kDvb);
   if (r >= p.hdr[1]) return;
   const int4 sg = p.segs[r];
-  const int first = sg.x, nch = min(sg.y, p.hdr[0] - sg.x);
+  // (the chunk count clamped to the table: the saved backward reads a
+  // workspace that only its caller vouches for)
+  const int first = sg.x, nch = min(sg.y, min(p.hdr[0], p.max_chunks) - sg.x);
   if (first < 0 || nch <= 0) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (!state_pipe_start<kChan, false>(sm.pp, maps, p, sg, nch, h, vb, tid)) return;
@@ -1024,7 +1027,7 @@ __global__ void __launch_bounds__(kStateBlock) gdn_state_kernel(const __grid_con
       ldsm_x4_t(b, frag_b(sH, kS32, 16 * kk, n0, lane));
       mma_bf16(ce[0], aw, b[0], b[1]);
       mma_bf16(ce[1], aw, b[2], b[3]);
-      if (!kStore) {
+      if (kOut) {
         mma_bf16(cq[0], aq, b[0], b[1]);
         mma_bf16(cq[1], aq, b[2], b[3]);
       }
@@ -1051,7 +1054,8 @@ __global__ void __launch_bounds__(kStateBlock) gdn_state_kernel(const __grid_con
           *reinterpret_cast<uint4*>(p.E + ((size_t)(t0 + rr) * p.nh + h) * kD + kDvb * vb + cc) =
               *reinterpret_cast<const uint4*>(&sm.E[rr * kS32 + cc]);
       }
-    } else {
+    }
+    if (kOut) {
       // ---- O = scale (e^gamma Q H + Aq E)
       float co[2][4];
 #pragma unroll
@@ -1137,7 +1141,9 @@ __global__ void __launch_bounds__(kStateBlock) gdn_bwd_state_kernel(const __grid
   const int h = rem / (kD / kDvb), vb = rem - h * (kD / kDvb);
   if (r >= p.hdr[1]) return;
   const int4 sg = p.segs[r];
-  const int first = sg.x, nch = min(sg.y, p.hdr[0] - sg.x);
+  // (the chunk count clamped to the table: the saved backward reads a
+  // workspace that only its caller vouches for)
+  const int first = sg.x, nch = min(sg.y, min(p.hdr[0], p.max_chunks) - sg.x);
   if (first < 0 || nch <= 0) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (!state_pipe_start<kChan, true>(sm.pp, maps, p, sg, nch, h, vb, tid)) return;
@@ -2756,6 +2762,116 @@ cudaError_t launch_big(void (*kernel)(KArgs...), dim3 grid, cudaStream_t s, cons
   return e;
 }
 
+// The forward's checks and set-up.  `save`: the workspace is the backward's
+// (the saving forward keeps what the backward would recompute there).
+int fwd_entry(GdnParams& p, StateMaps& maps, const void* q, const void* k, const void* v, const float* g,
+              const float* beta, const int32_t* cu_seqlens, float scale, void* o, void* workspace,
+              size_t workspace_bytes, int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments,
+              bool kda, bool save) {
+  int rc = gdn_setup(p, q, k, v, g, beta, cu_seqlens, scale, workspace, workspace_bytes, total, num_heads, head_dim,
+                     num_segments, save, kda);
+  if (rc) return rc;
+  if (!o) return ATTN_ERR_NULL_POINTER;
+  if (reinterpret_cast<uintptr_t>(o) & 15u) return ATTN_ERR_ALIGNMENT;
+  int* status = nullptr;
+  int sms = 0;
+  if ((rc = device_for_call(&status, &sms))) return rc;
+  if (total == 0) return ATTN_OK;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.status = status;
+  return make_state_maps(maps, p);
+}
+
+// The backward's checks and set-up.
+int bwd_entry(GdnParams& p, StateMaps& maps, const void* q, const void* k, const void* v, const float* g,
+              const float* beta, const void* d_o, const int32_t* cu_seqlens, float scale, void* dq, void* dk,
+              void* dv, float* dg, float* dbeta, void* workspace, size_t workspace_bytes, int64_t total,
+              int32_t num_heads, int32_t head_dim, int32_t num_segments, bool kda) {
+  int rc = gdn_setup(p, q, k, v, g, beta, cu_seqlens, scale, workspace, workspace_bytes, total, num_heads, head_dim,
+                     num_segments, true, kda);
+  if (rc) return rc;
+  const void* outs[] = {d_o, dq, dk, dv, dg, dbeta};
+  for (const void* x : outs)
+    if (!x) return ATTN_ERR_NULL_POINTER;
+  for (const void* x : outs)
+    if (reinterpret_cast<uintptr_t>(x) & 15u) return ATTN_ERR_ALIGNMENT;
+  int* status = nullptr;
+  int sms = 0;
+  if ((rc = device_for_call(&status, &sms))) return rc;
+  if (total == 0) return ATTN_OK;
+  p.dO = static_cast<const __nv_bfloat16*>(d_o);
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dg = dg;
+  p.dbeta = dbeta;
+  p.status = status;
+  return make_state_maps(maps, p);
+}
+
+dim3 seg_grid_of(const GdnParams& p) { return dim3((unsigned)((long long)p.nseg * p.nh * (kD / kDvb))); }
+dim3 chunk_grid_of(const GdnParams& p) { return dim3((unsigned)p.max_chunks, (unsigned)p.nh); }
+
+// The forward.  save: O and, for the backward, the chunk-start states and E.
+cudaError_t launch_layer_fwd(const GdnParams& p, const StateMaps& maps, cudaStream_t s, bool kda, bool save) {
+  cudaError_t e = kda ? launch_kda_prep(p, s) : launch_gdn_prep(p, s);
+  if (e != cudaSuccess) return e;
+  if (kda)
+    return save ? launch_state<StateSmem>(gdn_state_kernel<true, true, true>, seg_grid_of(p), s, maps, p)
+                : launch_state<StateSmem>(gdn_state_kernel<true, false, true>, seg_grid_of(p), s, maps, p);
+  return save ? launch_state<StateSmem>(gdn_state_kernel<true, true, false>, seg_grid_of(p), s, maps, p)
+              : launch_state<StateSmem>(gdn_state_kernel<true, false, false>, seg_grid_of(p), s, maps, p);
+}
+
+// The backward.  saved: the workspace already holds the saving forward's
+// factors, states and E, so the plan, the prep and the recomputation are skipped.
+cudaError_t launch_layer_bwd(const GdnParams& p, const StateMaps& maps, cudaStream_t s, bool kda, bool saved) {
+  const dim3 seg_grid = seg_grid_of(p), chunk_grid = chunk_grid_of(p);
+  cudaError_t e = cudaSuccess;
+  if (!saved) {
+    e = kda ? launch_kda_prep(p, s) : launch_gdn_prep(p, s);
+    if (e == cudaSuccess)
+      e = kda ? launch_state<StateSmem>(gdn_state_kernel<false, true, true>, seg_grid, s, maps, p)
+              : launch_state<StateSmem>(gdn_state_kernel<false, true, false>, seg_grid, s, maps, p);
+  }
+  if (kda) {
+    if (e == cudaSuccess) e = launch_state<BwdStateSmem>(gdn_bwd_state_kernel<true>, seg_grid, s, maps, p);
+    if (e == cudaSuccess) e = launch_big<KdaLocalHSmem>(kda_bwd_local_h_kernel, chunk_grid, s, p, kLocalThreads);
+    if (e == cudaSuccess) e = launch_big<KdaLocalWySmem>(kda_bwd_local_wy_kernel, chunk_grid, s, p, kLocalThreads);
+    if (e == cudaSuccess) e = launch_big<KdaExpSmem>(kda_bwd_exp_kernel, chunk_grid, s, p, kLocalThreads);
+  } else {
+    if (e == cudaSuccess) e = launch_state<BwdStateSmem>(gdn_bwd_state_kernel<false>, seg_grid, s, maps, p);
+    if (e == cudaSuccess) e = launch_big<LocalHSmem>(gdn_bwd_local_h_kernel, chunk_grid, s, p, kLocalThreads);
+    if (e == cudaSuccess) e = launch_big<LocalWySmem>(gdn_bwd_local_wy_kernel, chunk_grid, s, p, kLocalThreads);
+  }
+  return e;
+}
+
+int run_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+            const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes, int64_t total,
+            int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream, bool kda, bool save) {
+  GdnParams p;
+  StateMaps maps;
+  const int rc = fwd_entry(p, maps, q, k, v, g, beta, cu_seqlens, scale, o, workspace, workspace_bytes, total,
+                           num_heads, head_dim, num_segments, kda, save);
+  if (rc || total == 0) return rc;
+  const cudaError_t e = launch_layer_fwd(p, maps, static_cast<cudaStream_t>(stream), kda, save);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int run_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, const void* d_o,
+            const int32_t* cu_seqlens, float scale, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+            void* workspace, size_t workspace_bytes, int64_t total, int32_t num_heads, int32_t head_dim,
+            int32_t num_segments, void* stream, bool kda, bool saved) {
+  GdnParams p;
+  StateMaps maps;
+  const int rc = bwd_entry(p, maps, q, k, v, g, beta, d_o, cu_seqlens, scale, dq, dk, dv, dg, dbeta, workspace,
+                           workspace_bytes, total, num_heads, head_dim, num_segments, kda);
+  if (rc || total == 0) return rc;
+  const cudaError_t e = launch_layer_bwd(p, maps, static_cast<cudaStream_t>(stream), kda, saved);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace vsw
 
 extern "C" {
@@ -2775,64 +2891,31 @@ size_t gdn_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads, int32_t 
 int gdn_varlen_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                    const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes,
                    int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream) {
-  using namespace vsw;
-  GdnParams p;
-  int rc = gdn_setup(p, q, k, v, g, beta, cu_seqlens, scale, workspace, workspace_bytes, total, num_heads, head_dim,
-                     num_segments, false);
-  if (rc) return rc;
-  if (!o) return ATTN_ERR_NULL_POINTER;
-  if (reinterpret_cast<uintptr_t>(o) & 15u) return ATTN_ERR_ALIGNMENT;
-  int* status = nullptr;
-  int sms = 0;
-  if ((rc = device_for_call(&status, &sms))) return rc;
-  if (total == 0) return ATTN_OK;
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.status = status;
-  StateMaps maps;
-  if ((rc = make_state_maps(maps, p))) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_gdn_prep(p, s);
-  const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
-  if (e == cudaSuccess) e = launch_state<StateSmem>(gdn_state_kernel<false, false>, seg_grid, s, maps, p);
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return vsw::run_fwd(q, k, v, g, beta, cu_seqlens, scale, o, workspace, workspace_bytes, total, num_heads, head_dim,
+                      num_segments, stream, false, false);
+}
+
+int gdn_varlen_fwd_save(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                        const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes,
+                        int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream) {
+  return vsw::run_fwd(q, k, v, g, beta, cu_seqlens, scale, o, workspace, workspace_bytes, total, num_heads, head_dim,
+                      num_segments, stream, false, true);
 }
 
 int gdn_varlen_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, const void* d_o,
                    const int32_t* cu_seqlens, float scale, void* dq, void* dk, void* dv, float* dg, float* dbeta,
                    void* workspace, size_t workspace_bytes, int64_t total, int32_t num_heads, int32_t head_dim,
                    int32_t num_segments, void* stream) {
-  using namespace vsw;
-  GdnParams p;
-  int rc = gdn_setup(p, q, k, v, g, beta, cu_seqlens, scale, workspace, workspace_bytes, total, num_heads, head_dim,
-                     num_segments, true);
-  if (rc) return rc;
-  const void* outs[] = {d_o, dq, dk, dv, dg, dbeta};
-  for (const void* x : outs)
-    if (!x) return ATTN_ERR_NULL_POINTER;
-  for (const void* x : outs)
-    if (reinterpret_cast<uintptr_t>(x) & 15u) return ATTN_ERR_ALIGNMENT;
-  int* status = nullptr;
-  int sms = 0;
-  if ((rc = device_for_call(&status, &sms))) return rc;
-  if (total == 0) return ATTN_OK;
-  p.dO = static_cast<const __nv_bfloat16*>(d_o);
-  p.dq = static_cast<__nv_bfloat16*>(dq);
-  p.dk = static_cast<__nv_bfloat16*>(dk);
-  p.dv = static_cast<__nv_bfloat16*>(dv);
-  p.dg = dg;
-  p.dbeta = dbeta;
-  p.status = status;
-  StateMaps maps;
-  if ((rc = make_state_maps(maps, p))) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
-  const dim3 chunk_grid((unsigned)p.max_chunks, (unsigned)num_heads);
-  cudaError_t e = launch_gdn_prep(p, s);
-  if (e == cudaSuccess) e = launch_state<StateSmem>(gdn_state_kernel<true, false>, seg_grid, s, maps, p);
-  if (e == cudaSuccess) e = launch_state<BwdStateSmem>(gdn_bwd_state_kernel<false>, seg_grid, s, maps, p);
-  if (e == cudaSuccess) e = launch_big<LocalHSmem>(gdn_bwd_local_h_kernel, chunk_grid, s, p, kLocalThreads);
-  if (e == cudaSuccess) e = launch_big<LocalWySmem>(gdn_bwd_local_wy_kernel, chunk_grid, s, p, kLocalThreads);
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return vsw::run_bwd(q, k, v, g, beta, d_o, cu_seqlens, scale, dq, dk, dv, dg, dbeta, workspace, workspace_bytes,
+                      total, num_heads, head_dim, num_segments, stream, false, false);
+}
+
+int gdn_varlen_bwd_saved(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const void* d_o, const int32_t* cu_seqlens, float scale, void* dq, void* dk, void* dv,
+                         float* dg, float* dbeta, void* workspace, size_t workspace_bytes, int64_t total,
+                         int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream) {
+  return vsw::run_bwd(q, k, v, g, beta, d_o, cu_seqlens, scale, dq, dk, dv, dg, dbeta, workspace, workspace_bytes,
+                      total, num_heads, head_dim, num_segments, stream, false, true);
 }
 
 size_t kda_varlen_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments) {
@@ -2841,74 +2924,40 @@ size_t kda_varlen_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_
   return vsw::gdn_workspace_layout(total, num_heads, num_segments, off, false, true);
 }
 
-int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                   const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes,
-                   int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream) {
-  using namespace vsw;
-  GdnParams p;
-  int rc = gdn_setup(p, q, k, v, g, beta, cu_seqlens, scale, workspace, workspace_bytes, total, num_heads, head_dim,
-                     num_segments, false, true);
-  if (rc) return rc;
-  if (!o) return ATTN_ERR_NULL_POINTER;
-  if (reinterpret_cast<uintptr_t>(o) & 15u) return ATTN_ERR_ALIGNMENT;
-  int* status = nullptr;
-  int sms = 0;
-  if ((rc = device_for_call(&status, &sms))) return rc;
-  if (total == 0) return ATTN_OK;
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.status = status;
-  StateMaps maps;
-  if ((rc = make_state_maps(maps, p))) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_kda_prep(p, s);
-  const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
-  if (e == cudaSuccess) e = launch_state<StateSmem>(gdn_state_kernel<false, true>, seg_grid, s, maps, p);
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-}
-
 size_t kda_varlen_bwd_workspace_bytes(int64_t total, int32_t num_heads, int32_t num_segments) {
   if (total < 0 || num_heads <= 0 || num_segments < 0 || total > (1LL << 30) || num_heads > 1024) return 0;
   size_t off[23];
   return vsw::gdn_workspace_layout(total, num_heads, num_segments, off, true, true);
 }
 
+int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                   const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes,
+                   int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream) {
+  return vsw::run_fwd(q, k, v, g, beta, cu_seqlens, scale, o, workspace, workspace_bytes, total, num_heads, head_dim,
+                      num_segments, stream, true, false);
+}
+
+int kda_varlen_fwd_save(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                        const int32_t* cu_seqlens, float scale, void* o, void* workspace, size_t workspace_bytes,
+                        int64_t total, int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream) {
+  return vsw::run_fwd(q, k, v, g, beta, cu_seqlens, scale, o, workspace, workspace_bytes, total, num_heads, head_dim,
+                      num_segments, stream, true, true);
+}
+
 int kda_varlen_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, const void* d_o,
                    const int32_t* cu_seqlens, float scale, void* dq, void* dk, void* dv, float* dg, float* dbeta,
                    void* workspace, size_t workspace_bytes, int64_t total, int32_t num_heads, int32_t head_dim,
                    int32_t num_segments, void* stream) {
-  using namespace vsw;
-  GdnParams p;
-  int rc = gdn_setup(p, q, k, v, g, beta, cu_seqlens, scale, workspace, workspace_bytes, total, num_heads, head_dim,
-                     num_segments, true, true);
-  if (rc) return rc;
-  const void* outs[] = {d_o, dq, dk, dv, dg, dbeta};
-  for (const void* x : outs)
-    if (!x) return ATTN_ERR_NULL_POINTER;
-  for (const void* x : outs)
-    if (reinterpret_cast<uintptr_t>(x) & 15u) return ATTN_ERR_ALIGNMENT;
-  int* status = nullptr;
-  int sms = 0;
-  if ((rc = device_for_call(&status, &sms))) return rc;
-  if (total == 0) return ATTN_OK;
-  p.dO = static_cast<const __nv_bfloat16*>(d_o);
-  p.dq = static_cast<__nv_bfloat16*>(dq);
-  p.dk = static_cast<__nv_bfloat16*>(dk);
-  p.dv = static_cast<__nv_bfloat16*>(dv);
-  p.dg = dg;
-  p.dbeta = dbeta;
-  p.status = status;
-  StateMaps maps;
-  if ((rc = make_state_maps(maps, p))) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const dim3 seg_grid((unsigned)((long long)num_segments * num_heads * (kD / kDvb)));
-  const dim3 chunk_grid((unsigned)p.max_chunks, (unsigned)num_heads);
-  cudaError_t e = launch_kda_prep(p, s);
-  if (e == cudaSuccess) e = launch_state<StateSmem>(gdn_state_kernel<true, true>, seg_grid, s, maps, p);
-  if (e == cudaSuccess) e = launch_state<BwdStateSmem>(gdn_bwd_state_kernel<true>, seg_grid, s, maps, p);
-  if (e == cudaSuccess) e = launch_big<KdaLocalHSmem>(kda_bwd_local_h_kernel, chunk_grid, s, p, kLocalThreads);
-  if (e == cudaSuccess) e = launch_big<KdaLocalWySmem>(kda_bwd_local_wy_kernel, chunk_grid, s, p, kLocalThreads);
-  if (e == cudaSuccess) e = launch_big<KdaExpSmem>(kda_bwd_exp_kernel, chunk_grid, s, p, kLocalThreads);
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return vsw::run_bwd(q, k, v, g, beta, d_o, cu_seqlens, scale, dq, dk, dv, dg, dbeta, workspace, workspace_bytes,
+                      total, num_heads, head_dim, num_segments, stream, true, false);
+}
+
+int kda_varlen_bwd_saved(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const void* d_o, const int32_t* cu_seqlens, float scale, void* dq, void* dk, void* dv,
+                         float* dg, float* dbeta, void* workspace, size_t workspace_bytes, int64_t total,
+                         int32_t num_heads, int32_t head_dim, int32_t num_segments, void* stream) {
+  return vsw::run_bwd(q, k, v, g, beta, d_o, cu_seqlens, scale, dq, dk, dv, dg, dbeta, workspace, workspace_bytes,
+                      total, num_heads, head_dim, num_segments, stream, true, true);
 }
 
 }  // extern "C"
