@@ -323,6 +323,19 @@ __global__ void __launch_bounds__(256) gdn_plan_kernel(GdnParams p) {
 // X = (I + A)^-1 for the strictly lower triangular 64 x 64 A (fp32, row
 // stride kSF; X with row stride LDX), in 16 x 16 blocks, by all NT threads of the CTA; R
 // holds 3 x 256 floats of scratch.  Ends with a CTA barrier.
+// Four consecutive floats from shared memory: one 16-byte load where the
+// address allows it (rows of a stride that is a multiple of 4), else four.
+template <int LDX>
+__device__ __forceinline__ void load4_impl(float (&x)[4], const float* src) {
+  if constexpr (LDX % 4 == 0) {
+    const float4 v = *reinterpret_cast<const float4*>(src);
+    x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) x[q] = src[q];
+  }
+}
+
 template <int LDX = kSF, int NT = kGdnThreads>
 __device__ __forceinline__ void wy_inverse(const float* A, float* X, float* R, int tid) {
   // ---- X = (I + A)^-1 (unit lower triangular) in 16 x 16 blocks.
@@ -353,22 +366,45 @@ __device__ __forceinline__ void wy_inverse(const float* A, float* X, float* R, i
   __syncthreads();
   // Blocks below the diagonal, nearest first (d = i - j = 1, 2, 3):
   //     X_ij = -X_ii R_ij,   R_ij = sum_{j <= k < i} A_ik X_kj
-  // (the rows of block i of (I + A) X = I), R_ij kept in R.
+  // (the rows of block i of (I + A) X = I), R_ij kept in R.  Each thread
+  // computes four adjacent columns of one row: per k one broadcast element of
+  // the left factor and four of the right one, which bounds these products by
+  // shared-memory reads less than one element per product did.  Two partial
+  // sums per output (k even, odd), added in a fixed order.
   for (int d = 1; d < 4; ++d) {
     const int nb = 4 - d;  // blocks (j + d, j), j = 0 .. nb - 1
-    for (int e = tid; e < nb * 256; e += NT) {
-      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
-      float acc = 0.f;
-      for (int k = 16 * j; k < 16 * i; ++k) acc = fmaf(A[(16 * i + r) * kSF + k], X[k * LDX + 16 * j + c], acc);
-      R[e] = acc;
+    for (int e = tid; e < nb * 64; e += NT) {
+      const int j = e >> 6, r = (e >> 2) & 15, c = (e & 3) * 4, i = j + d;
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      for (int kb = 16 * j; kb < 16 * i; kb += 16) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float a = A[(16 * i + r) * kSF + kb + t];
+          float x[4];
+          load4_impl<LDX>(x, &X[(kb + t) * LDX + 16 * j + c]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[t & 1][q] = fmaf(a, x[q], acc[t & 1][q]);
+        }
+      }
+      *reinterpret_cast<float4*>(&R[(j << 8) + (r << 4) + c]) =
+          make_float4(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]);
     }
     __syncthreads();
-    for (int e = tid; e < nb * 256; e += NT) {
-      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
-      float acc = 0.f;
+    for (int e = tid; e < nb * 64; e += NT) {
+      const int j = e >> 6, r = (e >> 2) & 15, c = (e & 3) * 4, i = j + d;
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int k = 0; k < 16; ++k) acc = fmaf(X[(16 * i + r) * LDX + 16 * i + k], R[(j << 8) + (k << 4) + c], acc);
-      X[(16 * i + r) * LDX + 16 * j + c] = -acc;
+      for (int k = 0; k < 16; ++k) {
+        const float xa = X[(16 * i + r) * LDX + 16 * i + k];
+        const float4 rr = *reinterpret_cast<const float4*>(&R[(j << 8) + (k << 4) + c]);
+        acc[k & 1][0] = fmaf(xa, rr.x, acc[k & 1][0]);
+        acc[k & 1][1] = fmaf(xa, rr.y, acc[k & 1][1]);
+        acc[k & 1][2] = fmaf(xa, rr.z, acc[k & 1][2]);
+        acc[k & 1][3] = fmaf(xa, rr.w, acc[k & 1][3]);
+      }
+      float* xo = &X[(16 * i + r) * LDX + 16 * j + c];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xo[q] = -(acc[0][q] + acc[1][q]);
     }
     __syncthreads();
   }
@@ -382,7 +418,7 @@ struct PrepSmem {
   __nv_bfloat16 V[kC * kS128];
   float A[kC * kSF];    // A, fp32
   float X[kC * kSF];    // (I + A)^-1, fp32
-  float R[3 * 256];     // off-diagonal block products
+  alignas(16) float R[3 * 256];  // off-diagonal block products
   __nv_bfloat16 T1[kC * kS64];  // X diag(beta e^gamma)
   __nv_bfloat16 T2[kC * kS64];  // X diag(beta)
   float gam[kC];
@@ -551,7 +587,7 @@ struct KdaPrepSmem {
   __nv_bfloat16 KI[160 * kS128];    // per row block I: K_j o e^(gamma_rI - gamma_j), j < 16 (I + 1)
   float A[kC * kSF];
   float X[kC * kSF];
-  float R[3 * 256];
+  alignas(16) float R[3 * 256];
   __nv_bfloat16 T2[kC * kS64];      // X diag(beta)
   float bet[kC];
 };
@@ -1809,6 +1845,61 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_h_kernel(GdnParam
   }
 }
 
+// dA = strictly-lower(-X^T dX X^T) for the unit lower-triangular X of a
+// chunk, in fp32, by the 16 warps of a local CTA:
+//     Y = dX X^T  (into Y),   dA = -X^T Y  (into dA, zero on and above the diagonal).
+// dXT = dX transposed and XT = X transposed, [m][i] with row stride kS4; X
+// [m][i], Y [m][j] with kS4; dA with kSF.  Warp w owns four columns j0 .. j0
+// + 3 and lane l the rows 2l, 2l + 1.  X[j][m] = 0 for m > j, so Y's sums
+// stop at m = j0 + 3; X[m][i] = 0 for m < i and only i > j is kept, so dA's
+// sums start at m = j0 + 1.  The terms left out multiply exact zeros, so the
+// sums are the full ones, term for term in the same order.  The column
+// blocks are dealt so that the four warps of each scheduler have equal loop
+// lengths.
+__device__ __forceinline__ void wy_grad_a(const float* dXT, const float* XT, const float* X, float* Y, float* dA,
+                                          int warp, int lane) {
+  const int k = warp >> 2, sch = warp & 3;
+  const int cb = k == 0 ? sch : (k == 1 ? 7 - sch : (k == 2 ? 8 + sch : 15 - sch));
+  const int j0 = 4 * cb, i0 = 2 * lane;
+  float y[2][4];
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
+#pragma unroll 4
+  for (int m = 0; m < j0 + 4; ++m) {
+    const float2 xa = *reinterpret_cast<const float2*>(&dXT[m * kS4 + i0]);  // dX[i0 + a][m]
+    const float4 xb = *reinterpret_cast<const float4*>(&XT[m * kS4 + j0]);   // X[j0 + b][m], one broadcast
+    const float av[2] = {xa.x, xa.y}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
+  }
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+    *reinterpret_cast<float4*>(&Y[(i0 + a) * kS4 + j0]) = make_float4(y[a][0], y[a][1], y[a][2], y[a][3]);
+  __syncthreads();
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
+#pragma unroll 4
+  for (int m = j0 + 1; m < kC; ++m) {
+    const float2 xa = *reinterpret_cast<const float2*>(&X[m * kS4 + i0]);  // X[m][i0 + a]
+    const float4 xb = *reinterpret_cast<const float4*>(&Y[m * kS4 + j0]);  // Y[m][j0 + b], one broadcast
+    const float av[2] = {xa.x, xa.y}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
+  }
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) dA[(i0 + a) * kSF + j0 + b] = j0 + b < i0 + a ? -y[a][b] : 0.f;
+}
+
 // ============================================================== backward: local, the WY factors
 // Per (chunk, head), from K, V, dE, dW (A and X = (I + A)^-1 recomputed):
 //     dX  = (dE V^T) diag(beta) + (dW K^T) diag(beta e^gamma)
@@ -1830,7 +1921,7 @@ struct LocalWySmem {
   float XT[kC * kS4];   // its transpose
   float dXT[kC * kS4];  // dX, transposed
   float Y[kC * kS4];    // dX X^T
-  float R[3 * 256];
+  alignas(16) float R[3 * 256];
   __nv_bfloat16 Xb[kC * kS64];
   __nv_bfloat16 M[kC * kS64];
   float gam[kC];
@@ -1953,49 +2044,8 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_wy_kernel(GdnPara
         }
   }
   __syncthreads();
-  // ---- Y = dX X^T, then dA = -X^T Y, strictly lower; fp32, each thread a
-  // 2 x 4 block of outputs (8 independent sums, a float2 and a float4 load
-  // per step; the zeros of the triangular X make the full sums over m exact).
-  {
-    const int i0 = 2 * (tid >> 4), j0 = 4 * (tid & 15);
-    float y[2][4];
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
-#pragma unroll 4
-    for (int m = 0; m < kC; ++m) {
-      const float2 xa = *reinterpret_cast<const float2*>(&sm.dXT[m * kS4 + i0]);  // dX[i0 + a][m]
-      const float4 xb = *reinterpret_cast<const float4*>(&sm.XT[m * kS4 + j0]);   // X[j0 + b][m]
-      const float av[2] = {xa.x, xa.y}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
-    }
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-      *reinterpret_cast<float4*>(&sm.Y[(i0 + a) * kS4 + j0]) = make_float4(y[a][0], y[a][1], y[a][2], y[a][3]);
-    __syncthreads();
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
-#pragma unroll 4
-    for (int m = 0; m < kC; ++m) {
-      const float2 xa = *reinterpret_cast<const float2*>(&sm.X[m * kS4 + i0]);  // X[m][i0 + a]
-      const float4 xb = *reinterpret_cast<const float4*>(&sm.Y[m * kS4 + j0]);  // Y[m][j0 + b]
-      const float av[2] = {xa.x, xa.y}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
-    }
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) sm.A[(i0 + a) * kSF + j0 + b] = j0 + b < i0 + a ? -y[a][b] : 0.f;
-  }
+  // ---- Y = dX X^T, then dA = -X^T Y, strictly lower (fp32)
+  wy_grad_a(sm.dXT, sm.XT, sm.X, sm.Y, sm.A, warp, lane);
   __syncthreads();
   // ---- M = diag(beta) (dA o Gamma) (bf16); in place, A becomes dA o Gamma o KK
   // (its row sums go to dbeta) and KK becomes M o KK (row minus column sums
@@ -2032,6 +2082,17 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_wy_kernel(GdnPara
   __syncthreads();
   // ---- 64 x 128 products, rows [r0, +16) x columns [d0, +32)
   const int d0 = 32 * (warp >> 2);
+  // this thread's part of dKa, loaded now for the dk store at the end
+  float2 dka[2][4];
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int i = r0 + (lane >> 2) + 8 * hr;
+    const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + d0;
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+      dka[hr][n] = i < len ? *reinterpret_cast<const float2*>(p.dKa + off + 8 * n + 2 * (lane & 3))
+                           : make_float2(0.f, 0.f);
+  }
   float cv[4][4], ck[4][4];
 #pragma unroll
   for (int n = 0; n < 4; ++n)
@@ -2108,8 +2169,8 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_wy_kernel(GdnPara
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
         const int j = 8 * n + 2 * (lane & 3);
-        const float2 a = *reinterpret_cast<const float2*>(p.dKa + off + j);
-        *reinterpret_cast<uint32_t*>(p.dk + off + j) = pack2(ck[n][2 * hr] + a.x, ck[n][2 * hr + 1] + a.y);
+        *reinterpret_cast<uint32_t*>(p.dk + off + j) =
+            pack2(ck[n][2 * hr] + dka[hr][n].x, ck[n][2 * hr + 1] + dka[hr][n].y);
       }
     }
   }
@@ -2260,47 +2321,8 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_wy_kernel(GdnPara
         }
   }
   __syncthreads();
-  // ---- Y = dX X^T, then dA = -X^T Y, strictly lower (fp32, 2 x 4 blocks per thread)
-  {
-    const int i0 = 2 * (tid >> 4), j0 = 4 * (tid & 15);
-    float y[2][4];
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
-#pragma unroll 4
-    for (int m = 0; m < kC; ++m) {
-      const float2 xa = *reinterpret_cast<const float2*>(&sm.dXT[m * kS4 + i0]);
-      const float4 xb = *reinterpret_cast<const float4*>(&sm.XT[m * kS4 + j0]);
-      const float av[2] = {xa.x, xa.y}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
-    }
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-      *reinterpret_cast<float4*>(&sm.Y[(i0 + a) * kS4 + j0]) = make_float4(y[a][0], y[a][1], y[a][2], y[a][3]);
-    __syncthreads();
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) y[a][b] = 0.f;
-#pragma unroll 4
-    for (int m = 0; m < kC; ++m) {
-      const float2 xa = *reinterpret_cast<const float2*>(&sm.X[m * kS4 + i0]);
-      const float4 xb = *reinterpret_cast<const float4*>(&sm.Y[m * kS4 + j0]);
-      const float av[2] = {xa.x, xa.y}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) y[a][b] = fmaf(av[a], bv[b], y[a][b]);
-    }
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) sm.A[(i0 + a) * kSF + j0 + b] = j0 + b < i0 + a ? -y[a][b] : 0.f;
-  }
+  // ---- Y = dX X^T, then dA = -X^T Y, strictly lower (fp32)
+  wy_grad_a(sm.dXT, sm.XT, sm.X, sm.Y, sm.A, warp, lane);
   __syncthreads();
   // ---- M = diag(beta) dA to the workspace; sum_j dA_ij Araw_ij into dbeta
   {
