@@ -200,6 +200,32 @@ __device__ __forceinline__ int4 seg_chunk(const int4& sg, int ci) {
   return make_int4(sg.z + ci * kC, min(kC, sg.w - ci * kC), 0, ci);
 }
 
+// gamma per channel: the running sum of g down each of the 128 channels of a
+// 64 x 128 fp32 tile (row stride kG), in place, by the 512 threads of a local
+// CTA.  Each thread sums one 16-row segment of one channel; then every
+// segment adds the totals of the segments above it, in order.  The same
+// order in every kernel gives every kernel the same bits.  `tot`: 4 x 128
+// floats of scratch.  Begins and ends at a barrier of all threads.
+__device__ __forceinline__ void chan_running_sum(float* G, float* tot, int tid) {
+  const int c = tid & (kD - 1), sg = tid >> 7;
+  const int i0 = 16 * sg;
+  float acc = 0.f;
+#pragma unroll 4
+  for (int i = i0; i < i0 + 16; ++i) {
+    acc += G[i * kG + c];
+    G[i * kG + c] = acc;
+  }
+  tot[sg * kD + c] = acc;
+  __syncthreads();
+  if (sg > 0) {
+    float off = tot[c];
+    for (int s2 = 1; s2 < sg; ++s2) off += tot[s2 * kD + c];
+#pragma unroll 4
+    for (int i = i0; i < i0 + 16; ++i) G[i * kG + c] += off;
+  }
+  __syncthreads();
+}
+
 // ============================================================== plan
 __global__ void __launch_bounds__(256) gdn_plan_kernel(GdnParams p) {
   __shared__ int s_first[1024 + 1];
@@ -590,6 +616,7 @@ struct KdaPrepSmem {
   alignas(16) float R[3 * 256];
   __nv_bfloat16 T2[kC * kS64];      // X diag(beta)
   float bet[kC];
+  float tot[4 * kD];               // scratch of the channel running sums
 };
 static_assert(sizeof(KdaPrepSmem) <= 227 * 1024, "fits one SM");
 
@@ -635,14 +662,7 @@ __global__ void __launch_bounds__(kLocalThreads) kda_prep_kernel(GdnParams p) {
     if (__syncthreads_or(bad) && tid == 0 && p.status) atomicExch(p.status, kStatusGateRange);
   }
   // gamma per channel (rows past the chunk add zeros)
-  if (tid < kD) {
-    float acc = 0.f;
-    for (int i = 0; i < kC; ++i) {
-      acc += sm.G[i * kG + tid];
-      sm.G[i * kG + tid] = acc;
-    }
-  }
-  __syncthreads();
+  chan_running_sum(sm.G, sm.tot, tid);
   // scaled operands: KB, QB (reference = the row's block start) and the KI copies
   for (int e = tid; e < kC * kD / 2; e += nt) {
     const int i = e >> 6, cc = (e & 63) * 2;
@@ -1649,6 +1669,7 @@ struct KdaLocalHSmem {
   float G[kC * kG];  // gamma per channel
   float last[kD];    // the gamma_last terms per channel
   float lc[4][kD];   // their column partials from the four row groups, added in a fixed order
+  float tot[4 * kD];               // scratch of the channel running sums
 };
 static_assert(sizeof(KdaLocalHSmem) <= 227 * 1024, "fits one SM");
 
@@ -1689,12 +1710,8 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_h_kernel(GdnParam
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
-  if (tid < kD) {  // gamma per channel, and e^gamma_last rowsum(dH1 o H0) of the channel (row tid of H)
-    float acc = 0.f;
-    for (int i = 0; i < kC; ++i) {
-      acc += sm.G[i * kG + tid];
-      sm.G[i * kG + tid] = acc;
-    }
+  chan_running_sum(sm.G, sm.tot, tid);  // gamma per channel
+  if (tid < kD) {  // e^gamma_last rowsum(dH1 o H0) of the channel (row tid of H)
     float d = 0.f;
     for (int v = 0; v < kD; v += 2) {
       const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.H0[tid * kS128 + v]));
@@ -2220,6 +2237,7 @@ struct KdaLocalWySmem {
   float bet[kC];
   float dbs[kC];
   float pb[4][kC];  // row partials of dbeta from the four column groups, added in a fixed order
+  float tot[4 * kD];               // scratch of the channel running sums
 };
 static_assert(sizeof(KdaLocalWySmem) <= 227 * 1024, "fits one SM");
 
@@ -2265,14 +2283,7 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_wy_kernel(GdnPara
   }
   cp_async_wait<0>();
   __syncthreads();
-  if (tid < kD) {  // gamma per channel
-    float acc = 0.f;
-    for (int i = 0; i < kC; ++i) {
-      acc += sm.G[i * kG + tid];
-      sm.G[i * kG + tid] = acc;
-    }
-  }
-  __syncthreads();
+  chan_running_sum(sm.G, sm.tot, tid);  // gamma per channel
   // KB = K o e^gamma in place; Xb, XT
   for (int e = tid; e < kC * kD / 2; e += nt) {
     const int i = e >> 6, cc = (e & 63) * 2;
@@ -2423,6 +2434,7 @@ struct KdaExpSmem {
   __nv_bfloat16 QBr[kC * kS128];   // Q o e^(gamma - gamma_r)
   __nv_bfloat16 KI[160 * kS128];   // per row block I: K_j o e^(gamma_rI - gamma_j), j < 16 (I + 1)
   float G[kC * kG];                // gamma per channel, then dgam
+  float tot[4 * kD];               // scratch of the channel running sums
 };
 static_assert(sizeof(KdaExpSmem) <= 227 * 1024, "fits one SM");
 
@@ -2461,14 +2473,7 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_exp_kernel(GdnParams p)
   }
   cp_async_wait<0>();
   __syncthreads();
-  if (tid < kD) {
-    float acc = 0.f;
-    for (int i = 0; i < kC; ++i) {
-      acc += sm.G[i * kG + tid];
-      sm.G[i * kG + tid] = acc;
-    }
-  }
-  __syncthreads();
+  chan_running_sum(sm.G, sm.tot, tid);  // gamma per channel
   for (int e = tid; e < kC * kD / 2; e += nt) {
     const int i = e >> 6, cc = (e & 63) * 2;
     const int r = i & ~15;
@@ -2542,25 +2547,38 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_exp_kernel(GdnParams p)
         pn[n][e] = fmaf(f, tn[n][e], pn[n][e]);
       }
   }
-  // epilogue: this thread's (row, channel) elements
+  // epilogue: this thread's (row, channel) elements, two adjacent channels at a time
   float dgv[4][4];
 #pragma unroll
   for (int n = 0; n < 4; ++n)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = r0 + (lane >> 2) + 8 * (e >> 1);
-      const int cc = c0 + 8 * n + 2 * (lane & 3) + (e & 1);
-      const float f = __expf(sm.G[i * kG + cc] - sm.G[r0 * kG + cc]);
-      const float a = f * pa[n][e], m = f * pm[n][e], b = pb[n][e], nn = pn[n][e];
-      const float kv = __bfloat162float(sm.K[i * kS128 + cc]), qv = __bfloat162float(sm.Q[i * kS128 + cc]);
-      float dgi = 0.f;
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const int cc = c0 + 8 * n + 2 * (lane & 3);
+      float a[2], m[2], b[2], nn[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float f = __expf(sm.G[i * kG + cc + u] - sm.G[r0 * kG + cc + u]);
+        a[u] = f * pa[n][2 * hr + u];
+        m[u] = f * pm[n][2 * hr + u];
+        b[u] = pb[n][2 * hr + u];
+        nn[u] = pn[n][2 * hr + u];
+      }
+      const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[i * kS128 + cc]));
+      const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.Q[i * kS128 + cc]));
+      float dg0 = 0.f, dg1 = 0.f;
       if (i < len) {
         const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + cc;
-        p.dq[off] = __float2bfloat16_rn(p.dQa[off] + a);
-        p.dk[off] = __float2bfloat16_rn(p.dKa[off] + b + m + nn);
-        dgi = p.dgam[off] + qv * a + kv * (m - b - nn);
+        const float2 qa = *reinterpret_cast<const float2*>(p.dQa + off);
+        const float2 ka = *reinterpret_cast<const float2*>(p.dKa + off);
+        const float2 ga = *reinterpret_cast<const float2*>(p.dgam + off);
+        *reinterpret_cast<uint32_t*>(p.dq + off) = pack2(qa.x + a[0], qa.y + a[1]);
+        *reinterpret_cast<uint32_t*>(p.dk + off) = pack2(ka.x + b[0] + m[0] + nn[0], ka.y + b[1] + m[1] + nn[1]);
+        dg0 = ga.x + qv.x * a[0] + kv.x * (m[0] - b[0] - nn[0]);
+        dg1 = ga.y + qv.y * a[1] + kv.y * (m[1] - b[1] - nn[1]);
       }
-      dgv[n][e] = dgi;
+      dgv[n][2 * hr] = dg0;
+      dgv[n][2 * hr + 1] = dg1;
     }
   __syncthreads();  // gamma no longer read: dgam goes in its place
 #pragma unroll
@@ -2569,11 +2587,20 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_exp_kernel(GdnParams p)
     for (int e = 0; e < 4; ++e)
       sm.G[(r0 + (lane >> 2) + 8 * (e >> 1)) * kG + c0 + 8 * n + 2 * (lane & 3) + (e & 1)] = dgv[n][e];
   __syncthreads();
-  if (tid < kD) {
+  // dg = reverse running sum of dgam down each channel: four 16-row
+  // segments at once, each adding the totals of the segments below it
+  {
+    const int c = tid & (kD - 1), sg = tid >> 7, i0 = 16 * sg;
     float acc = 0.f;
-    for (int i = kC - 1; i >= 0; --i) {
-      acc += sm.G[i * kG + tid];
-      if (i < len) p.dg[((size_t)(t0 + i) * p.nh + h) * kD + tid] = acc;
+    for (int i = i0 + 15; i >= i0; --i) acc += sm.G[i * kG + c];
+    sm.tot[sg * kD + c] = acc;
+    __syncthreads();
+    float off = 0.f;
+    for (int s2 = 3; s2 > sg; --s2) off += sm.tot[s2 * kD + c];
+    acc = off;
+    for (int i = i0 + 15; i >= i0; --i) {
+      acc += sm.G[i * kG + c];
+      if (i < len) p.dg[((size_t)(t0 + i) * p.nh + h) * kD + c] = acc;
     }
   }
 }
