@@ -2351,6 +2351,20 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_wy_kernel(GdnPara
   __syncthreads();  // dbs gets atomic adds below
   // ---- dVb = X^T dE, XdW = X^T dW: rows [r0, +16) x columns [d0, +32)
   const int d0 = 32 * (warp >> 2);
+  // this thread's dKa and dgam elements, read now so that the reads overlap
+  // the products (the epilogue updates them in place)
+  float2 kav[2][4], gav[2][4];
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int i = r0 + (lane >> 2) + 8 * hr;
+    const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + d0;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const int j = 8 * n + 2 * (lane & 3);
+      kav[hr][n] = i < len ? *reinterpret_cast<const float2*>(p.dKa + off + j) : make_float2(0.f, 0.f);
+      gav[hr][n] = i < len ? *reinterpret_cast<const float2*>(p.dgam + off + j) : make_float2(0.f, 0.f);
+    }
+  }
   float cv[4][4], ck[4][4];
 #pragma unroll
   for (int n = 0; n < 4; ++n)
@@ -2388,11 +2402,11 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_wy_kernel(GdnPara
         if (i < len) {
           *reinterpret_cast<uint32_t*>(p.dv + off + j) = pack2(bi * cv[n][2 * hr], bi * cv[n][2 * hr + 1]);
           const float e0 = __expf(sm.G[i * kG + d0 + j]), e1 = __expf(sm.G[i * kG + d0 + j + 1]);
-          float2 ka = *reinterpret_cast<const float2*>(p.dKa + off + j);
+          float2 ka = kav[hr][n];
           ka.x += bi * ck[n][2 * hr] * e0;
           ka.y += bi * ck[n][2 * hr + 1] * e1;
           *reinterpret_cast<float2*>(p.dKa + off + j) = ka;
-          float2 ga = *reinterpret_cast<const float2*>(p.dgam + off + j);
+          float2 ga = gav[hr][n];
           ga.x += bi * ck[n][2 * hr] * kb.x;
           ga.y += bi * ck[n][2 * hr + 1] * kb.y;
           *reinterpret_cast<float2*>(p.dgam + off + j) = ga;
@@ -2547,10 +2561,22 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_exp_kernel(GdnParams p)
         pn[n][e] = fmaf(f, tn[n][e], pn[n][e]);
       }
   }
-  // epilogue: this thread's (row, channel) elements, two adjacent channels at a time
+  // epilogue: this thread's (row, channel) elements, two adjacent channels at
+  // a time; per group of channels the fp32 partial gradients of both rows
+  // are read before its stores
   float dgv[4][4];
 #pragma unroll
-  for (int n = 0; n < 4; ++n)
+  for (int n = 0; n < 4; ++n) {
+    float2 qav[2], kav[2], gav[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + c0 + 8 * n + 2 * (lane & 3);
+      const bool ok = i < len;
+      qav[hr] = ok ? *reinterpret_cast<const float2*>(p.dQa + off) : make_float2(0.f, 0.f);
+      kav[hr] = ok ? *reinterpret_cast<const float2*>(p.dKa + off) : make_float2(0.f, 0.f);
+      gav[hr] = ok ? *reinterpret_cast<const float2*>(p.dgam + off) : make_float2(0.f, 0.f);
+    }
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int i = r0 + (lane >> 2) + 8 * hr;
@@ -2569,9 +2595,7 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_exp_kernel(GdnParams p)
       float dg0 = 0.f, dg1 = 0.f;
       if (i < len) {
         const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + cc;
-        const float2 qa = *reinterpret_cast<const float2*>(p.dQa + off);
-        const float2 ka = *reinterpret_cast<const float2*>(p.dKa + off);
-        const float2 ga = *reinterpret_cast<const float2*>(p.dgam + off);
+        const float2 qa = qav[hr], ka = kav[hr], ga = gav[hr];
         *reinterpret_cast<uint32_t*>(p.dq + off) = pack2(qa.x + a[0], qa.y + a[1]);
         *reinterpret_cast<uint32_t*>(p.dk + off) = pack2(ka.x + b[0] + m[0] + nn[0], ka.y + b[1] + m[1] + nn[1]);
         dg0 = ga.x + qv.x * a[0] + kv.x * (m[0] - b[0] - nn[0]);
@@ -2580,6 +2604,7 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_exp_kernel(GdnParams p)
       dgv[n][2 * hr] = dg0;
       dgv[n][2 * hr + 1] = dg1;
     }
+  }
   __syncthreads();  // gamma no longer read: dgam goes in its place
 #pragma unroll
   for (int n = 0; n < 4; ++n)
