@@ -1394,19 +1394,24 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParam
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t sdO = smem_u32(sm.dO), sdE = smem_u32(sm.dE), sE = smem_u32(sm.E), sQ = smem_u32(sm.Q),
                  sK = smem_u32(sm.K), sH0 = smem_u32(sm.H0), sdH1 = smem_u32(sm.dH1), sDG = smem_u32(sm.DG);
+  // Three copy groups, waited for in the order the products need them:
+  // dO, E, Q, K (the masked block DG); H0, dE (dq, dW); dH1 (dKa, dgam).
   load_rows128(sdO, p.dO, t0, len, h, p.nh, tid, nt);
-  load_rows128(sdE, p.dE, t0, len, h, p.nh, tid, nt);
   load_rows128(sE, p.E, t0, len, h, p.nh, tid, nt);
   load_rows128(sQ, p.q, t0, len, h, p.nh, tid, nt);
   load_rows128(sK, p.k, t0, len, h, p.nh, tid, nt);
-  {
-    const __nv_bfloat16* h0 = p.H0 + ((size_t)c * p.nh + h) * (kD * kD);
-    const __nv_bfloat16* d1 = p.dH1 + ((size_t)c * p.nh + h) * (kD * kD);
-    for (int e = tid; e < kD * 16; e += nt) {
-      const int r = e >> 4, cc = (e & 15) * 8;
-      cp_async16(sH0 + 2u * (uint32_t)(r * kS128 + cc), h0 + r * kD + cc, true);
-      cp_async16(sdH1 + 2u * (uint32_t)(r * kS128 + cc), d1 + r * kD + cc, true);
-    }
+  cp_async_commit();
+  const __nv_bfloat16* h0 = p.H0 + ((size_t)c * p.nh + h) * (kD * kD);
+  const __nv_bfloat16* d1 = p.dH1 + ((size_t)c * p.nh + h) * (kD * kD);
+  for (int e = tid; e < kD * 16; e += nt) {
+    const int r = e >> 4, cc = (e & 15) * 8;
+    cp_async16(sH0 + 2u * (uint32_t)(r * kS128 + cc), h0 + r * kD + cc, true);
+  }
+  load_rows128(sdE, p.dE, t0, len, h, p.nh, tid, nt);
+  cp_async_commit();
+  for (int e = tid; e < kD * 16; e += nt) {
+    const int r = e >> 4, cc = (e & 15) * 8;
+    cp_async16(sdH1 + 2u * (uint32_t)(r * kS128 + cc), d1 + r * kD + cc, true);
   }
   cp_async_commit();
   if (tid < kC) {
@@ -1414,7 +1419,7 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParam
     sm.dgs[tid] = 0.f;
   }
   for (int e = tid; e < 16 * kC; e += nt) (&sm.part[0][0])[e] = 0.f;  // part and lw
-  cp_async_wait<0>();
+  cp_async_wait<2>();
   __syncthreads();
   const float g_last = sm.gam[len - 1];
   const int r0 = 16 * (warp & 3);
@@ -1478,6 +1483,7 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParam
         if (lane < 4) sm.part[4 + (warp & 3)][c0 + 8 * n + 2 * lane + e] = -x;
       }
   }
+  cp_async_wait<1>();  // H0, dE
   __syncthreads();
   // ---- 64 x 128 products: rows [r0, +16), columns [d0, +32)
   const int d0 = 32 * (warp >> 2);
@@ -1564,6 +1570,8 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParam
     }
   }
   // dKa = w E dH1^T + DG^T Q
+  cp_async_wait<0>();  // dH1
+  __syncthreads();
   zero(acc);
   zero(acc2);
   mm_abt(acc, sE, sdH1);
@@ -1688,39 +1696,34 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_h_kernel(GdnParam
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t sdO = smem_u32(sm.dO), sdE = smem_u32(sm.dE), sE = smem_u32(sm.E), sH0 = smem_u32(sm.H0),
                  sdH1 = smem_u32(sm.dH1);
+  // Three copy groups, waited for in the order the products need them:
+  // dO, E and the gates (gamma, N); H0, dE, QB (dQB, dW); dH1, KC (dKC).
   load_rows128(sdO, p.dO, t0, len, h, p.nh, tid, nt);
-  load_rows128(sdE, p.dE, t0, len, h, p.nh, tid, nt);
   load_rows128(sE, p.E, t0, len, h, p.nh, tid, nt);
-  load_rows128(smem_u32(sm.QB), p.QB, t0, len, h, p.nh, tid, nt);
-  load_rows128(smem_u32(sm.KC), p.KC, t0, len, h, p.nh, tid, nt);
-  {
-    const __nv_bfloat16* h0 = p.H0 + ((size_t)c * p.nh + h) * (kD * kD);
-    const __nv_bfloat16* d1 = p.dH1 + ((size_t)c * p.nh + h) * (kD * kD);
-    for (int e = tid; e < kD * 16; e += nt) {
-      const int r = e >> 4, cc = (e & 15) * 8;
-      cp_async16(sH0 + 2u * (uint32_t)(r * kS128 + cc), h0 + r * kD + cc, true);
-      cp_async16(sdH1 + 2u * (uint32_t)(r * kS128 + cc), d1 + r * kD + cc, true);
-    }
-  }
   for (int e = tid; e < kC * 32; e += nt) {
     const int r = e >> 5, cc = (e & 31) * 4;
     const bool ok = r < len;
     cp_async16(smem_u32(&sm.G[r * kG + cc]), p.g + ((size_t)(t0 + (ok ? r : 0)) * p.nh + h) * kD + cc, ok);
   }
   cp_async_commit();
-  cp_async_wait<0>();
+  const __nv_bfloat16* h0 = p.H0 + ((size_t)c * p.nh + h) * (kD * kD);
+  const __nv_bfloat16* d1 = p.dH1 + ((size_t)c * p.nh + h) * (kD * kD);
+  for (int e = tid; e < kD * 16; e += nt) {
+    const int r = e >> 4, cc = (e & 15) * 8;
+    cp_async16(sH0 + 2u * (uint32_t)(r * kS128 + cc), h0 + r * kD + cc, true);
+  }
+  load_rows128(sdE, p.dE, t0, len, h, p.nh, tid, nt);
+  load_rows128(smem_u32(sm.QB), p.QB, t0, len, h, p.nh, tid, nt);
+  cp_async_commit();
+  for (int e = tid; e < kD * 16; e += nt) {
+    const int r = e >> 4, cc = (e & 15) * 8;
+    cp_async16(sdH1 + 2u * (uint32_t)(r * kS128 + cc), d1 + r * kD + cc, true);
+  }
+  load_rows128(smem_u32(sm.KC), p.KC, t0, len, h, p.nh, tid, nt);
+  cp_async_commit();
+  cp_async_wait<2>();
   __syncthreads();
   chan_running_sum(sm.G, sm.tot, tid);  // gamma per channel
-  if (tid < kD) {  // e^gamma_last rowsum(dH1 o H0) of the channel (row tid of H)
-    float d = 0.f;
-    for (int v = 0; v < kD; v += 2) {
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.H0[tid * kS128 + v]));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.dH1[tid * kS128 + v]));
-      d += a.x * b.x + a.y * b.y;
-    }
-    sm.last[tid] = d * __expf(sm.G[(len - 1) * kG + tid]);
-  }
-  __syncthreads();
   const int r0 = 16 * (warp & 3);
   // ---- N = lower(scale dO E^T): rows [r0, +16) x columns [c0, +16)
   {
@@ -1749,6 +1752,8 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_h_kernel(GdnParam
             make_float2(j <= i ? p.scale * s1[n][2 * hr] : 0.f, j + 1 <= i ? p.scale * s1[n][2 * hr + 1] : 0.f);
       }
   }
+  cp_async_wait<1>();  // H0, dE, QB
+  __syncthreads();
   // ---- 64 x 128 products: rows [r0, +16), columns [d0, +32)
   const int d0 = 32 * (warp >> 2);
   float acc[4][4], dg[2][4][2];
@@ -1805,6 +1810,17 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_h_kernel(GdnParam
         *reinterpret_cast<uint32_t*>(row + j) = pack2(-acc[n][2 * hr], -acc[n][2 * hr + 1]);
       }
     }
+  }
+  cp_async_wait<0>();  // dH1, KC
+  __syncthreads();
+  if (tid < kD) {  // e^gamma_last rowsum(dH1 o H0) of the channel (row tid of H)
+    float d = 0.f;
+    for (int v = 0; v < kD; v += 2) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.H0[tid * kS128 + v]));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.dH1[tid * kS128 + v]));
+      d += a.x * b.x + a.y * b.y;
+    }
+    sm.last[tid] = d * __expf(sm.G[(len - 1) * kG + tid]);  // this thread adds the rest later
   }
   // dKC = E dH1^T
   zero(acc);
