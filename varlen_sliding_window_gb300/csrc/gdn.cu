@@ -205,18 +205,25 @@ __device__ __forceinline__ int4 seg_chunk(const int4& sg, int ci) {
 // CTA.  Each thread sums one 16-row segment of one channel; then every
 // segment adds the totals of the segments above it, in order.  The same
 // order in every kernel gives every kernel the same bits.  `tot`: 4 x 128
-// floats of scratch.  Begins and ends at a barrier of all threads.
-__device__ __forceinline__ void chan_running_sum(float* G, float* tot, int tid) {
+// floats of scratch.  Begins and ends at a barrier of all threads.  kCheck:
+// also returns, to every thread, whether any g of the tile is at or below
+// kKdaMinLogDecay or NaN (rows past the chunk hold zeros).
+template <bool kCheck = false>
+__device__ __forceinline__ bool chan_running_sum(float* G, float* tot, int tid) {
   const int c = tid & (kD - 1), sg = tid >> 7;
   const int i0 = 16 * sg;
   float acc = 0.f;
+  bool bad = false;
 #pragma unroll 4
   for (int i = i0; i < i0 + 16; ++i) {
-    acc += G[i * kG + c];
+    const float g = G[i * kG + c];
+    if (kCheck) bad |= !(g > kKdaMinLogDecay);
+    acc += g;
     G[i * kG + c] = acc;
   }
   tot[sg * kD + c] = acc;
-  __syncthreads();
+  if (kCheck) bad = __syncthreads_or(bad);
+  else __syncthreads();
   if (sg > 0) {
     float off = tot[c];
     for (int s2 = 1; s2 < sg; ++s2) off += tot[s2 * kD + c];
@@ -224,6 +231,7 @@ __device__ __forceinline__ void chan_running_sum(float* G, float* tot, int tid) 
     for (int i = i0; i < i0 + 16; ++i) G[i * kG + c] += off;
   }
   __syncthreads();
+  return bad;
 }
 
 // ============================================================== plan
@@ -620,6 +628,25 @@ struct KdaPrepSmem {
 };
 static_assert(sizeof(KdaPrepSmem) <= 227 * 1024, "fits one SM");
 
+// f[u] = e^(a[u] - b[u]) for eight consecutive channels (16-byte aligned rows).
+__device__ __forceinline__ void scaled_factors(float (&f)[8], const float* a, const float* b) {
+  const float4 a0 = *reinterpret_cast<const float4*>(a), a1 = *reinterpret_cast<const float4*>(a + 4);
+  const float4 b0 = *reinterpret_cast<const float4*>(b), b1 = *reinterpret_cast<const float4*>(b + 4);
+  f[0] = __expf(a0.x - b0.x), f[1] = __expf(a0.y - b0.y), f[2] = __expf(a0.z - b0.z), f[3] = __expf(a0.w - b0.w);
+  f[4] = __expf(a1.x - b1.x), f[5] = __expf(a1.y - b1.y), f[6] = __expf(a1.z - b1.z), f[7] = __expf(a1.w - b1.w);
+}
+// Eight bf16 values times f, rounded back to bf16.
+__device__ __forceinline__ uint4 scale8(const uint4 x, const float (&f)[8]) {
+  const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&x);
+  uint32_t o[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float2 t = __bfloat1622float2(v[u]);
+    o[u] = pack2(t.x * f[2 * u], t.y * f[2 * u + 1]);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Row offset of block I's scaled K copy inside KI (blocks of 16, 32, 48, 64 rows).
 __device__ __forceinline__ int ki_row0(int I) { return 8 * I * (I + 1); }
 
@@ -640,48 +667,45 @@ __global__ void __launch_bounds__(kLocalThreads) kda_prep_kernel(GdnParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t sK = smem_u32(sm.K), sQ = smem_u32(sm.Q), sV = smem_u32(sm.V), sKB = smem_u32(sm.KB),
                  sQB = smem_u32(sm.QB), sKI = smem_u32(sm.KI);
+  // two copy groups: K, Q and the gates first; V (needed only for U) second
   load_rows128(sK, p.k, t0, len, h, p.nh, tid, nt);
   load_rows128(sQ, p.q, t0, len, h, p.nh, tid, nt);
-  load_rows128(sV, p.v, t0, len, h, p.nh, tid, nt);
   for (int e = tid; e < kC * 32; e += nt) {  // g rows, 32 pieces of 16 bytes each
     const int r = e >> 5, cc = (e & 31) * 4;
     const bool ok = r < len;
     cp_async16(smem_u32(&sm.G[r * kG + cc]), p.g + ((size_t)(t0 + (ok ? r : 0)) * p.nh + h) * kD + cc, ok);
   }
   cp_async_commit();
+  load_rows128(sV, p.v, t0, len, h, p.nh, tid, nt);
+  cp_async_commit();
   if (tid < kC) sm.bet[tid] = tid < len ? p.beta[(size_t)(t0 + tid) * p.nh + h] : 0.f;
-  cp_async_wait<0>();
+  cp_async_wait<1>();
   __syncthreads();
-  {
-    // Every log decay must be above kKdaMinLogDecay (the block-referenced
-    // products need the decay of 15 tokens within float range); anything
-    // else, NaN included, is reported in the status word.  Rows past the
-    // chunk were zero-filled.
-    bool bad = false;
-    for (int e = tid; e < kC * kD; e += nt) bad |= !(sm.G[(e >> 7) * kG + (e & 127)] > kKdaMinLogDecay);
-    if (__syncthreads_or(bad) && tid == 0 && p.status) atomicExch(p.status, kStatusGateRange);
-  }
-  // gamma per channel (rows past the chunk add zeros)
-  chan_running_sum(sm.G, sm.tot, tid);
-  // scaled operands: KB, QB (reference = the row's block start) and the KI copies
-  for (int e = tid; e < kC * kD / 2; e += nt) {
-    const int i = e >> 6, cc = (e & 63) * 2;
+  // gamma per channel (rows past the chunk add zeros).  Every log decay must
+  // be above kKdaMinLogDecay (the block-referenced products need the decay of
+  // 15 tokens within float range); anything else, NaN included, is reported
+  // in the status word.
+  if (chan_running_sum<true>(sm.G, sm.tot, tid) && tid == 0 && p.status) atomicExch(p.status, kStatusGateRange);
+  // scaled operands: KB, QB (reference = the row's block start) and the KI
+  // copies, eight channels per thread (16-byte loads and stores)
+  for (int e = tid; e < kC * kD / 8; e += nt) {
+    const int i = e >> 4, cc = (e & 15) * 8;
     const int r = i & ~15;
-    const float f0 = __expf(sm.G[i * kG + cc] - sm.G[r * kG + cc]);
-    const float f1 = __expf(sm.G[i * kG + cc + 1] - sm.G[r * kG + cc + 1]);
-    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[i * kS128 + cc]));
-    const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.Q[i * kS128 + cc]));
-    *reinterpret_cast<uint32_t*>(&sm.KB[i * kS128 + cc]) = pack2(kv.x * f0, kv.y * f1);
-    *reinterpret_cast<uint32_t*>(&sm.QB[i * kS128 + cc]) = pack2(qv.x * f0, qv.y * f1);
+    float f[8];
+    scaled_factors(f, &sm.G[i * kG + cc], &sm.G[r * kG + cc]);
+    *reinterpret_cast<uint4*>(&sm.KB[i * kS128 + cc]) =
+        scale8(*reinterpret_cast<const uint4*>(&sm.K[i * kS128 + cc]), f);
+    *reinterpret_cast<uint4*>(&sm.QB[i * kS128 + cc]) =
+        scale8(*reinterpret_cast<const uint4*>(&sm.Q[i * kS128 + cc]), f);
   }
-  for (int e = tid; e < 160 * kD / 2; e += nt) {
-    const int row = e >> 6, cc = (e & 63) * 2;
+  for (int e = tid; e < 160 * kD / 8; e += nt) {
+    const int row = e >> 4, cc = (e & 15) * 8;
     const int I = row < 16 ? 0 : (row < 48 ? 1 : (row < 96 ? 2 : 3));
     const int j = row - ki_row0(I), r = 16 * I;
-    const float f0 = __expf(sm.G[r * kG + cc] - sm.G[j * kG + cc]);
-    const float f1 = __expf(sm.G[r * kG + cc + 1] - sm.G[j * kG + cc + 1]);
-    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[j * kS128 + cc]));
-    *reinterpret_cast<uint32_t*>(&sm.KI[row * kS128 + cc]) = pack2(kv.x * f0, kv.y * f1);
+    float f[8];
+    scaled_factors(f, &sm.G[r * kG + cc], &sm.G[j * kG + cc]);
+    *reinterpret_cast<uint4*>(&sm.KI[row * kS128 + cc]) =
+        scale8(*reinterpret_cast<const uint4*>(&sm.K[j * kS128 + cc]), f);
   }
   __syncthreads();
   // ---- the 10 blocks (I, J <= I) of 16 x 16: A and Aqk; warp w < 10 takes block w
@@ -767,6 +791,7 @@ __global__ void __launch_bounds__(kLocalThreads) kda_prep_kernel(GdnParams p) {
     }
   }
   if (tid < kD) p.Bc[((size_t)c * p.nh + h) * kD + tid] = __expf(sm.G[last * kG + tid]);
+  cp_async_wait<0>();  // V
   __syncthreads();
   // ---- W = T2 (K o e^gamma), U = T2 V: warp w rows [16 (w % 4), +16) x columns [32 (w / 4), +32)
   const int r0 = 16 * (warp & 3), d0 = 32 * (warp >> 2);
