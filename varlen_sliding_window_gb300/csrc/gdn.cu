@@ -771,23 +771,18 @@ __global__ void __launch_bounds__(kLocalThreads) kda_prep_kernel(GdnParams p) {
   const int last = len - 1;
   for (int e = tid; e < kC * kD / 8; e += nt) {
     const int i = e >> 4, cc = (e & 15) * 8;
-    uint32_t kb[4], qb[4], kc[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int c2 = cc + 2 * u;
-      const float g0 = sm.G[i * kG + c2], g1 = sm.G[i * kG + c2 + 1];
-      const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[i * kS128 + c2]));
-      const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.Q[i * kS128 + c2]));
-      const float e0 = __expf(g0), e1 = __expf(g1);
-      kb[u] = pack2(kv.x * e0, kv.y * e1);
-      qb[u] = pack2(qv.x * e0, qv.y * e1);
-      kc[u] = pack2(kv.x * __expf(sm.G[last * kG + c2] - g0), kv.y * __expf(sm.G[last * kG + c2 + 1] - g1));
-    }
-    *reinterpret_cast<uint4*>(&sm.KB[i * kS128 + cc]) = make_uint4(kb[0], kb[1], kb[2], kb[3]);
+    float eg[8], ec[8];
+    const float4 g0 = *reinterpret_cast<const float4*>(&sm.G[i * kG + cc]);
+    const float4 g1 = *reinterpret_cast<const float4*>(&sm.G[i * kG + cc + 4]);
+    eg[0] = __expf(g0.x), eg[1] = __expf(g0.y), eg[2] = __expf(g0.z), eg[3] = __expf(g0.w);
+    eg[4] = __expf(g1.x), eg[5] = __expf(g1.y), eg[6] = __expf(g1.z), eg[7] = __expf(g1.w);
+    scaled_factors(ec, &sm.G[last * kG + cc], &sm.G[i * kG + cc]);
+    const uint4 kv = *reinterpret_cast<const uint4*>(&sm.K[i * kS128 + cc]);
+    *reinterpret_cast<uint4*>(&sm.KB[i * kS128 + cc]) = scale8(kv, eg);
     if (i < len) {
       const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + cc;
-      *reinterpret_cast<uint4*>(p.QB + off) = make_uint4(qb[0], qb[1], qb[2], qb[3]);
-      *reinterpret_cast<uint4*>(p.KC + off) = make_uint4(kc[0], kc[1], kc[2], kc[3]);
+      *reinterpret_cast<uint4*>(p.QB + off) = scale8(*reinterpret_cast<const uint4*>(&sm.Q[i * kS128 + cc]), eg);
+      *reinterpret_cast<uint4*>(p.KC + off) = scale8(kv, ec);
     }
   }
   if (tid < kD) p.Bc[((size_t)c * p.nh + h) * kD + tid] = __expf(sm.G[last * kG + tid]);
@@ -2529,24 +2524,24 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_exp_kernel(GdnParams p)
   cp_async_wait<0>();
   __syncthreads();
   chan_running_sum(sm.G, sm.tot, tid);  // gamma per channel
-  for (int e = tid; e < kC * kD / 2; e += nt) {
-    const int i = e >> 6, cc = (e & 63) * 2;
+  for (int e = tid; e < kC * kD / 8; e += nt) {  // eight channels per thread
+    const int i = e >> 4, cc = (e & 15) * 8;
     const int r = i & ~15;
-    const float f0 = __expf(sm.G[i * kG + cc] - sm.G[r * kG + cc]);
-    const float f1 = __expf(sm.G[i * kG + cc + 1] - sm.G[r * kG + cc + 1]);
-    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[i * kS128 + cc]));
-    const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.Q[i * kS128 + cc]));
-    *reinterpret_cast<uint32_t*>(&sm.KBr[i * kS128 + cc]) = pack2(kv.x * f0, kv.y * f1);
-    *reinterpret_cast<uint32_t*>(&sm.QBr[i * kS128 + cc]) = pack2(qv.x * f0, qv.y * f1);
+    float f[8];
+    scaled_factors(f, &sm.G[i * kG + cc], &sm.G[r * kG + cc]);
+    *reinterpret_cast<uint4*>(&sm.KBr[i * kS128 + cc]) =
+        scale8(*reinterpret_cast<const uint4*>(&sm.K[i * kS128 + cc]), f);
+    *reinterpret_cast<uint4*>(&sm.QBr[i * kS128 + cc]) =
+        scale8(*reinterpret_cast<const uint4*>(&sm.Q[i * kS128 + cc]), f);
   }
-  for (int e = tid; e < 160 * kD / 2; e += nt) {
-    const int row = e >> 6, cc = (e & 63) * 2;
+  for (int e = tid; e < 160 * kD / 8; e += nt) {
+    const int row = e >> 4, cc = (e & 15) * 8;
     const int I = row < 16 ? 0 : (row < 48 ? 1 : (row < 96 ? 2 : 3));
     const int j = row - ki_row0(I), r = 16 * I;
-    const float f0 = __expf(sm.G[r * kG + cc] - sm.G[j * kG + cc]);
-    const float f1 = __expf(sm.G[r * kG + cc + 1] - sm.G[j * kG + cc + 1]);
-    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sm.K[j * kS128 + cc]));
-    *reinterpret_cast<uint32_t*>(&sm.KI[row * kS128 + cc]) = pack2(kv.x * f0, kv.y * f1);
+    float f[8];
+    scaled_factors(f, &sm.G[r * kG + cc], &sm.G[j * kG + cc]);
+    *reinterpret_cast<uint4*>(&sm.KI[row * kS128 + cc]) =
+        scale8(*reinterpret_cast<const uint4*>(&sm.K[j * kS128 + cc]), f);
   }
   __syncthreads();
   const int R = warp & 3, r0 = 16 * R, c0 = 32 * (warp >> 2);
