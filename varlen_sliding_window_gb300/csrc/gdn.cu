@@ -2135,16 +2135,17 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_wy_kernel(GdnPara
   __syncthreads();
   // ---- 64 x 128 products, rows [r0, +16) x columns [d0, +32)
   const int d0 = 32 * (warp >> 2);
-  // this thread's part of dKa, loaded now for the dk store at the end
+  // this thread's part of dKa, loaded now for the dk store at the end.  A
+  // row past the chunk reads row 0 instead (never used): no select on the
+  // loaded value, so the warp does not wait for it here.
   float2 dka[2][4];
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
     const int i = r0 + (lane >> 2) + 8 * hr;
-    const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + d0;
+    const size_t off = ((size_t)(t0 + (i < len ? i : 0)) * p.nh + h) * kD + d0;
 #pragma unroll
     for (int n = 0; n < 4; ++n)
-      dka[hr][n] = i < len ? *reinterpret_cast<const float2*>(p.dKa + off + 8 * n + 2 * (lane & 3))
-                           : make_float2(0.f, 0.f);
+      dka[hr][n] = *reinterpret_cast<const float2*>(p.dKa + off + 8 * n + 2 * (lane & 3));
   }
   float cv[4][4], ck[4][4];
 #pragma unroll
@@ -2315,7 +2316,15 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_wy_kernel(GdnPara
   }
   {
     const float* ar = p.Araw + ((size_t)c * p.nh + h) * (kC * kC);
-    for (int e = tid; e < kC * kC; e += nt) sm.Ar[(e >> 6) * kSF + (e & 63)] = ar[e];
+    static_assert(kC * kC % nt == 0, "whole rounds");
+    float v[kC * kC / nt];  // all loads in flight before the first store
+#pragma unroll
+    for (int k = 0; k < kC * kC / nt; ++k) v[k] = ar[tid + k * nt];
+#pragma unroll
+    for (int k = 0; k < kC * kC / nt; ++k) {
+      const int e = tid + k * nt;
+      sm.Ar[(e >> 6) * kSF + (e & 63)] = v[k];
+    }
   }
   cp_async_wait<0>();
   __syncthreads();
@@ -2392,13 +2401,15 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_wy_kernel(GdnPara
   float2 kav[2][4], gav[2][4];
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
+    // (a row past the chunk reads row 0 instead, never used: no select on the
+    // loaded values, so the warp does not wait for them here)
     const int i = r0 + (lane >> 2) + 8 * hr;
-    const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + d0;
+    const size_t off = ((size_t)(t0 + (i < len ? i : 0)) * p.nh + h) * kD + d0;
 #pragma unroll
     for (int n = 0; n < 4; ++n) {
       const int j = 8 * n + 2 * (lane & 3);
-      kav[hr][n] = i < len ? *reinterpret_cast<const float2*>(p.dKa + off + j) : make_float2(0.f, 0.f);
-      gav[hr][n] = i < len ? *reinterpret_cast<const float2*>(p.dgam + off + j) : make_float2(0.f, 0.f);
+      kav[hr][n] = *reinterpret_cast<const float2*>(p.dKa + off + j);
+      gav[hr][n] = *reinterpret_cast<const float2*>(p.dgam + off + j);
     }
   }
   float cv[4][4], ck[4][4];
@@ -2513,12 +2524,20 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_exp_kernel(GdnParams p)
   cp_async_commit();
   {
     const size_t base = ((size_t)ci * p.nh + h) * (kC * kC);
-    for (int e = tid; e < kC * kC / 2; e += nt) {
-      const int i = e >> 5, j = (e & 31) * 2;
-      const float2 nv = *reinterpret_cast<const float2*>(p.Nw + base + i * kC + j);
-      const float2 mv = *reinterpret_cast<const float2*>(p.Mw + base + i * kC + j);
-      *reinterpret_cast<uint32_t*>(&sm.N[i * kS64 + j]) = pack2(nv.x, nv.y);
-      *reinterpret_cast<uint32_t*>(&sm.M[i * kS64 + j]) = pack2(mv.x, mv.y);
+    constexpr int kRounds = kC * kC / 2 / nt;
+    static_assert(kC * kC / 2 % nt == 0, "whole rounds");
+    float2 nv[kRounds], mv[kRounds];  // all loads in flight before the first store
+#pragma unroll
+    for (int k = 0; k < kRounds; ++k) {
+      const int e = tid + k * nt;
+      nv[k] = *reinterpret_cast<const float2*>(p.Nw + base + 2 * e);
+      mv[k] = *reinterpret_cast<const float2*>(p.Mw + base + 2 * e);
+    }
+#pragma unroll
+    for (int k = 0; k < kRounds; ++k) {
+      const int e = tid + k * nt, i = e >> 5, j = (e & 31) * 2;
+      *reinterpret_cast<uint32_t*>(&sm.N[i * kS64 + j]) = pack2(nv[k].x, nv[k].y);
+      *reinterpret_cast<uint32_t*>(&sm.M[i * kS64 + j]) = pack2(mv[k].x, mv[k].y);
     }
   }
   cp_async_wait<0>();
