@@ -1662,12 +1662,18 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_h_kernel(GdnParam
     if (lane == 0) sm.tw[warp] = x;
   }
   __syncthreads();
-  if (tid == 0) {
-    float last = 0.f, t = 0.f;
-    for (int i = 0; i < kC; ++i)
-      for (int sl = 0; sl < 4; ++sl) last += sm.lw[sl][i];
-    for (int w = 0; w < kLocalThreads / 32; ++w) t += sm.tw[w];
-    sm.last = last + __expf(g_last) * t;
+  if (warp == 0) {
+    // the gamma_last terms: lane l adds rows l and l + 32 of the four slots
+    // and warp l's <dH1, H0> share, then a fixed butterfly over the lanes
+    float last = 0.f, t = lane < kLocalThreads / 32 ? sm.tw[lane] : 0.f;
+#pragma unroll
+    for (int sl = 0; sl < 4; ++sl) last += sm.lw[sl][lane] + sm.lw[sl][lane + 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      last += __shfl_xor_sync(0xffffffffu, last, o);
+      t += __shfl_xor_sync(0xffffffffu, t, o);
+    }
+    if (lane == 0) sm.last = last + __expf(g_last) * t;
   }
   if (tid < kC) {
     float d = 0.f;
