@@ -2623,21 +2623,28 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_exp_kernel(GdnParams p)
       }
   }
   // epilogue: this thread's (row, channel) elements, two adjacent channels at
-  // a time; per group of channels the fp32 partial gradients of both rows
-  // are read before its stores
+  // a time.  The fp32 partial gradients of channel group n + 1 are read
+  // before group n's stores, so each group's reads overlap the previous
+  // group's work (rows past the chunk read row 0 instead, never used).
   float dgv[4][4];
+  float2 nxt[3][2];
+  auto read_group = [&](float2 (&v)[3][2], int n) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = r0 + (lane >> 2) + 8 * hr;
+      const size_t off = ((size_t)(t0 + (i < len ? i : 0)) * p.nh + h) * kD + c0 + 8 * n + 2 * (lane & 3);
+      v[0][hr] = *reinterpret_cast<const float2*>(p.dQa + off);
+      v[1][hr] = *reinterpret_cast<const float2*>(p.dKa + off);
+      v[2][hr] = *reinterpret_cast<const float2*>(p.dgam + off);
+    }
+  };
+  read_group(nxt, 0);
 #pragma unroll
   for (int n = 0; n < 4; ++n) {
     float2 qav[2], kav[2], gav[2];
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int i = r0 + (lane >> 2) + 8 * hr;
-      const size_t off = ((size_t)(t0 + i) * p.nh + h) * kD + c0 + 8 * n + 2 * (lane & 3);
-      const bool ok = i < len;
-      qav[hr] = ok ? *reinterpret_cast<const float2*>(p.dQa + off) : make_float2(0.f, 0.f);
-      kav[hr] = ok ? *reinterpret_cast<const float2*>(p.dKa + off) : make_float2(0.f, 0.f);
-      gav[hr] = ok ? *reinterpret_cast<const float2*>(p.dgam + off) : make_float2(0.f, 0.f);
-    }
+    for (int hr = 0; hr < 2; ++hr) qav[hr] = nxt[0][hr], kav[hr] = nxt[1][hr], gav[hr] = nxt[2][hr];
+    if (n + 1 < 4) read_group(nxt, n + 1);
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int i = r0 + (lane >> 2) + 8 * hr;
