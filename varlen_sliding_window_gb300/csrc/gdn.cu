@@ -628,6 +628,25 @@ struct KdaPrepSmem {
 };
 static_assert(sizeof(KdaPrepSmem) <= 227 * 1024, "fits one SM");
 
+// dst[c] = src[c] e^(a[c] - b[c]) (rounded to bf16) for the eight channels
+// c of {4q, .., 4q + 3} and {64 + 4q, .., 64 + 4q + 3} of one 128-channel row:
+// sixteen lanes with q = 0 .. 15 read and write contiguous runs, which keeps
+// the shared-memory accesses free of bank conflicts.
+__device__ __forceinline__ void scale_row8(__nv_bfloat16* dst, const __nv_bfloat16* src, const float* a,
+                                          const float* b, int q) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int c = 64 * half + 4 * q;
+    const float4 av = *reinterpret_cast<const float4*>(a + c), bv = *reinterpret_cast<const float4*>(b + c);
+    const uint2 x = *reinterpret_cast<const uint2*>(src + c);
+    const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
+    const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
+    *reinterpret_cast<uint2*>(dst + c) =
+        make_uint2(pack2(x0.x * __expf(av.x - bv.x), x0.y * __expf(av.y - bv.y)),
+                   pack2(x1.x * __expf(av.z - bv.z), x1.y * __expf(av.w - bv.w)));
+  }
+}
+
 // f[u] = e^(a[u] - b[u]) for eight consecutive channels (16-byte aligned rows).
 __device__ __forceinline__ void scaled_factors(float (&f)[8], const float* a, const float* b) {
   const float4 a0 = *reinterpret_cast<const float4*>(a), a1 = *reinterpret_cast<const float4*>(a + 4);
@@ -689,23 +708,16 @@ __global__ void __launch_bounds__(kLocalThreads) kda_prep_kernel(GdnParams p) {
   // scaled operands: KB, QB (reference = the row's block start) and the KI
   // copies, eight channels per thread (16-byte loads and stores)
   for (int e = tid; e < kC * kD / 8; e += nt) {
-    const int i = e >> 4, cc = (e & 15) * 8;
+    const int i = e >> 4, q = e & 15;
     const int r = i & ~15;
-    float f[8];
-    scaled_factors(f, &sm.G[i * kG + cc], &sm.G[r * kG + cc]);
-    *reinterpret_cast<uint4*>(&sm.KB[i * kS128 + cc]) =
-        scale8(*reinterpret_cast<const uint4*>(&sm.K[i * kS128 + cc]), f);
-    *reinterpret_cast<uint4*>(&sm.QB[i * kS128 + cc]) =
-        scale8(*reinterpret_cast<const uint4*>(&sm.Q[i * kS128 + cc]), f);
+    scale_row8(&sm.KB[i * kS128], &sm.K[i * kS128], &sm.G[i * kG], &sm.G[r * kG], q);
+    scale_row8(&sm.QB[i * kS128], &sm.Q[i * kS128], &sm.G[i * kG], &sm.G[r * kG], q);
   }
   for (int e = tid; e < 160 * kD / 8; e += nt) {
-    const int row = e >> 4, cc = (e & 15) * 8;
+    const int row = e >> 4, q = e & 15;
     const int I = row < 16 ? 0 : (row < 48 ? 1 : (row < 96 ? 2 : 3));
     const int j = row - ki_row0(I), r = 16 * I;
-    float f[8];
-    scaled_factors(f, &sm.G[r * kG + cc], &sm.G[j * kG + cc]);
-    *reinterpret_cast<uint4*>(&sm.KI[row * kS128 + cc]) =
-        scale8(*reinterpret_cast<const uint4*>(&sm.K[j * kS128 + cc]), f);
+    scale_row8(&sm.KI[row * kS128], &sm.K[j * kS128], &sm.G[r * kG], &sm.G[j * kG], q);
   }
   __syncthreads();
   // ---- the 10 blocks (I, J <= I) of 16 x 16: A and Aqk; warp w < 10 takes block w
@@ -2550,23 +2562,16 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_exp_kernel(GdnParams p)
   __syncthreads();
   chan_running_sum(sm.G, sm.tot, tid);  // gamma per channel
   for (int e = tid; e < kC * kD / 8; e += nt) {  // eight channels per thread
-    const int i = e >> 4, cc = (e & 15) * 8;
+    const int i = e >> 4, q = e & 15;
     const int r = i & ~15;
-    float f[8];
-    scaled_factors(f, &sm.G[i * kG + cc], &sm.G[r * kG + cc]);
-    *reinterpret_cast<uint4*>(&sm.KBr[i * kS128 + cc]) =
-        scale8(*reinterpret_cast<const uint4*>(&sm.K[i * kS128 + cc]), f);
-    *reinterpret_cast<uint4*>(&sm.QBr[i * kS128 + cc]) =
-        scale8(*reinterpret_cast<const uint4*>(&sm.Q[i * kS128 + cc]), f);
+    scale_row8(&sm.KBr[i * kS128], &sm.K[i * kS128], &sm.G[i * kG], &sm.G[r * kG], q);
+    scale_row8(&sm.QBr[i * kS128], &sm.Q[i * kS128], &sm.G[i * kG], &sm.G[r * kG], q);
   }
   for (int e = tid; e < 160 * kD / 8; e += nt) {
-    const int row = e >> 4, cc = (e & 15) * 8;
+    const int row = e >> 4, q = e & 15;
     const int I = row < 16 ? 0 : (row < 48 ? 1 : (row < 96 ? 2 : 3));
     const int j = row - ki_row0(I), r = 16 * I;
-    float f[8];
-    scaled_factors(f, &sm.G[r * kG + cc], &sm.G[j * kG + cc]);
-    *reinterpret_cast<uint4*>(&sm.KI[row * kS128 + cc]) =
-        scale8(*reinterpret_cast<const uint4*>(&sm.K[j * kS128 + cc]), f);
+    scale_row8(&sm.KI[row * kS128], &sm.K[j * kS128], &sm.G[r * kG], &sm.G[j * kG], q);
   }
   __syncthreads();
   const int R = warp & 3, r0 = 16 * R, c0 = 32 * (warp >> 2);
