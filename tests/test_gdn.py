@@ -268,7 +268,8 @@ HEAD_CASE_CU = np.array([0, 1, 64, 65, 129, 129, 200, 330], dtype=np.int32)
 def check_head_counts(nh, per_channel):
     """Forward and backward against the oracle with nh heads: the kernels
     index the [T, H, 128] rows, the per-head chunk tables and every
-    workspace array by H, and the other tests use 8."""
+    workspace array by H, and the other tests use 8.  The saving pair on the
+    same inputs must give the same bits."""
     from oracle import gated_delta, kimi_delta
     oracle_mod = kimi_delta if per_channel else gated_delta
     inp = synth.make_gdn_inputs(HEAD_CASE_CU, nh, 128, tensor_seed=11, per_channel=per_channel)
@@ -290,6 +291,26 @@ def check_head_counts(nh, per_channel):
         assert np.isfinite(a).all(), nm
         assert rel_l2(a, b) <= tol_g[nm], (nm, rel_l2(a, b))
         assert_per_segment(a, b, inp.cu_seqlens, tol_g[nm], nm)
+    # the saving pair on the same inputs: the same bits as the calls above
+    import torch
+    from varlen_sliding_window_gb300 import binding as b
+    pre = "kda" if per_channel else "gdn"
+    q, k, v, do = (_to_dev(x) for x in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
+    g = torch.from_numpy(inp.g).cuda()
+    beta = torch.from_numpy(inp.beta).cuda()
+    cu = torch.from_numpy(inp.cu_seqlens).cuda()
+    T = q.shape[0]
+    ws = torch.empty(getattr(b, f"{pre}_varlen_bwd_workspace_bytes")(T, nh, len(inp.cu_seqlens) - 1),
+                     dtype=torch.uint8, device="cuda")
+    o2 = torch.empty_like(q)
+    g2 = [torch.empty_like(q) for _ in range(3)] + [torch.empty_like(g), torch.empty_like(beta)]
+    getattr(b, f"{pre}_varlen_fwd_save")(q, k, v, g, beta, cu, scale, o2, ws)
+    getattr(b, f"{pre}_varlen_bwd_saved")(q, k, v, g, beta, do, cu, scale, *g2, ws)
+    torch.cuda.synchronize()
+    assert b.attn_varlen_get_status() == 0
+    assert np.array_equal(o2.double().cpu().numpy(), got)
+    for nm, a, c in zip(("dq", "dk", "dv", "dg", "dbeta"), grads, g2):
+        assert np.array_equal(c.double().cpu().numpy(), a), nm
 
 
 @pytest.mark.gpu
