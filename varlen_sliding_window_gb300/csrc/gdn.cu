@@ -451,7 +451,7 @@ struct PrepSmem {
   __nv_bfloat16 Q[kC * kS128];
   __nv_bfloat16 V[kC * kS128];
   float A[kC * kSF];    // A, fp32
-  float X[kC * kSF];    // (I + A)^-1, fp32
+  float X[kC * kS4];    // (I + A)^-1, fp32 (rows of 16-byte multiples for the inverse's wide reads)
   alignas(16) float R[3 * 256];  // off-diagonal block products
   __nv_bfloat16 T1[kC * kS64];  // X diag(beta e^gamma)
   __nv_bfloat16 T2[kC * kS64];  // X diag(beta)
@@ -540,11 +540,11 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_prep_kernel(GdnParams p) {
     }
   }
   __syncthreads();
-  wy_inverse(sm.A, sm.X, sm.R, tid);
+  wy_inverse<kS4, kGdnThreads>(sm.A, sm.X, sm.R, tid);
   // ---- T1 = X diag(beta e^gamma), T2 = X diag(beta) (bf16)
   for (int e = tid; e < kC * kC / 2; e += kGdnThreads) {
     const int i = e >> 5, j = (e & 31) * 2;
-    const float x0 = sm.X[i * kSF + j], x1 = sm.X[i * kSF + j + 1];
+    const float x0 = sm.X[i * kS4 + j], x1 = sm.X[i * kS4 + j + 1];
     const float b0 = sm.bet[j], b1 = sm.bet[j + 1];
     *reinterpret_cast<uint32_t*>(&sm.T1[i * kS64 + j]) =
         pack2(x0 * b0 * __expf(sm.gam[j]), x1 * b1 * __expf(sm.gam[j + 1]));
@@ -620,7 +620,7 @@ struct KdaPrepSmem {
   __nv_bfloat16 QB[kC * kS128];     // Q o e^(gamma - gamma_r)
   __nv_bfloat16 KI[160 * kS128];    // per row block I: K_j o e^(gamma_rI - gamma_j), j < 16 (I + 1)
   float A[kC * kSF];
-  float X[kC * kSF];
+  float X[kC * kS4];
   alignas(16) float R[3 * 256];
   __nv_bfloat16 T2[kC * kS64];      // X diag(beta)
   float bet[kC];
@@ -769,16 +769,16 @@ __global__ void __launch_bounds__(kLocalThreads) kda_prep_kernel(GdnParams p) {
     if (kBwd) p.Araw[((size_t)c * p.nh + h) * (kC * kC) + i * kC + j] = 0.f;
   }
   __syncthreads();
-  wy_inverse<kSF, kLocalThreads>(sm.A, sm.X, sm.R, tid);
+  wy_inverse<kS4, kLocalThreads>(sm.A, sm.X, sm.R, tid);
   if (kBwd) {
     float* xw = p.Xw + ((size_t)c * p.nh + h) * (kC * kC);
-    for (int e = tid; e < kC * kC; e += nt) xw[e] = sm.X[(e >> 6) * kSF + (e & 63)];
+    for (int e = tid; e < kC * kC; e += nt) xw[e] = sm.X[(e >> 6) * kS4 + (e & 63)];
   }
   // ---- T2 = X diag(beta); KB <- K o e^gamma; QB, KC, e^gamma_last to the workspace
   for (int e = tid; e < kC * kC / 2; e += nt) {
     const int i = e >> 5, j = (e & 31) * 2;
     *reinterpret_cast<uint32_t*>(&sm.T2[i * kS64 + j]) =
-        pack2(sm.X[i * kSF + j] * sm.bet[j], sm.X[i * kSF + j + 1] * sm.bet[j + 1]);
+        pack2(sm.X[i * kS4 + j] * sm.bet[j], sm.X[i * kS4 + j + 1] * sm.bet[j + 1]);
   }
   const int last = len - 1;
   for (int e = tid; e < kC * kD / 8; e += nt) {
