@@ -114,6 +114,11 @@ def algorithmic_bytes(w) -> int:
 # ex2 results per clock per SM, measured on a GB300 with a microbenchmark of
 # back-to-back independent ex2.approx.f32 instructions.
 MUFU_EX2_PER_CLK_SM = 31.0
+# bf16 mma.sync m16n8k16 (the warp-level instruction the linear-attention
+# kernels use): one per 2 cycles per SM, 1,024 FMA per clock per SM, measured
+# on a GB300 with a microbenchmark (20 cycles latency; 4 warps with 4
+# independent accumulators reach it).
+MMA_SYNC_FMA_PER_CLK_SM = 1024.0
 NUM_SMS = 152
 
 
@@ -842,6 +847,8 @@ def main():
         dom = "bwd" if b_ms >= f_ms else "fwd"
         layer, page_ms = ("Kimi Delta", PAGE_KDA_MS) if gw.per_channel else ("Gated DeltaNet", PAGE_GDN_MS)
         ach = tf_b if dom == "bwd" else tf_f
+        mhz_g = sm_mhz or 2032.0
+        mma_sync_peak = 2 * MMA_SYNC_FMA_PER_CLK_SM * NUM_SMS * mhz_g * 1e6 / 1e12
         del ws
         return {"fwd_ms": f_ms, "bwd_ms": b_ms, "step_ms": f_ms + b_ms, "segments": nseg, "tokens": gw.total,
                 "heads": gw.nh, "gflop_fwd": ff / 1e9, "gflop_bwd": fb / 1e9, "tflops_fwd": tf_f, "tflops_bwd": tf_b,
@@ -849,7 +856,10 @@ def main():
                 "roofline": {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_t, "unit": "TFLOP/s",
                              "frac": ach / peak_t, "traffic": None,
                              "peak_source": f"bf16 dense burst, {'of measured' if peak_src == 'measured' else 'of fallback'}",
-                             "note": "warp-level mma.sync bf16 products; the peak is the tcgen05/cuBLAS one"},
+                             "note": "warp-level mma.sync bf16 products; the peak is the tcgen05/cuBLAS one",
+                             "mma_sync": {"peak": mma_sync_peak, "frac": ach / mma_sync_peak,
+                                          "peak_basis": f"{MMA_SYNC_FMA_PER_CLK_SM:g} FMA/clk/SM x 2 x {NUM_SMS} "
+                                                        f"SMs x {mhz_g:g} MHz (measured instruction rate)"}},
                 "page_context": ({"page_ms": page_ms, "ratio": (f_ms + b_ms) / page_ms,
                                   "what": f"the page's {layer} layer fwd+bwd per step at context 4,096 on its "
                                           "own unnamed GPU (research.dws.rip/llm/kernels, Fig. 5)"}
