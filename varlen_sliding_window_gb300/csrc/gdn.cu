@@ -1916,6 +1916,21 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_h_kernel(GdnParam
   }
 }
 
+// Xb = X in bf16 and XT = X transposed (fp32, row stride kS4), by the 512
+// threads of a local CTA.  A warp takes an 8 x 4 block per round (row = lane
+// % 8, column = lane / 8): its reads of X fall in 32 different banks, and
+// its writes of XT at most two to a bank.
+__device__ __forceinline__ void wy_copy_x(const float* X, __nv_bfloat16* Xb, float* XT, int tid) {
+#pragma unroll 4
+  for (int e = tid; e < kC * kC; e += kLocalThreads) {
+    const int blk = e >> 5, l = e & 31;
+    const int i = 8 * (blk >> 4) + (l & 7), j = 4 * (blk & 15) + (l >> 3);
+    const float x = X[i * kS4 + j];
+    Xb[i * kS64 + j] = __float2bfloat16_rn(x);
+    XT[j * kS4 + i] = x;
+  }
+}
+
 // dA = strictly-lower(-X^T dX X^T) for the unit lower-triangular X of a
 // chunk, in fp32, by the 16 warps of a local CTA:
 //     Y = dX X^T  (into Y),   dA = -X^T Y  (into dA, zero on and above the diagonal).
@@ -2072,13 +2087,7 @@ __global__ void __launch_bounds__(kLocalThreads) gdn_bwd_local_wy_kernel(GdnPara
   __syncthreads();
   wy_inverse<kS4, kLocalThreads>(sm.A, sm.X, sm.R, tid);
   // ---- Xb = bf16 X, XT; dX = (dE V^T) diag(beta) + (dW K^T) diag(beta e^gamma)
-  for (int e = tid; e < kC * kC / 2; e += nt) {
-    const int i = e >> 5, j = (e & 31) * 2;
-    const float x0 = sm.X[i * kS4 + j], x1 = sm.X[i * kS4 + j + 1];
-    *reinterpret_cast<uint32_t*>(&sm.Xb[i * kS64 + j]) = pack2(x0, x1);
-    sm.XT[j * kS4 + i] = x0;
-    sm.XT[(j + 1) * kS4 + i] = x1;
-  }
+  wy_copy_x(sm.X, sm.Xb, sm.XT, tid);
   {
     const int c0 = 16 * (warp >> 2);
     float pv[2][4], pk[2][4];
@@ -2354,13 +2363,7 @@ __global__ void __launch_bounds__(kLocalThreads) kda_bwd_local_wy_kernel(GdnPara
     *reinterpret_cast<uint32_t*>(&sm.KB[i * kS128 + cc]) =
         pack2(kv.x * __expf(sm.G[i * kG + cc]), kv.y * __expf(sm.G[i * kG + cc + 1]));
   }
-  for (int e = tid; e < kC * kC / 2; e += nt) {
-    const int i = e >> 5, j = (e & 31) * 2;
-    const float x0 = sm.X[i * kS4 + j], x1 = sm.X[i * kS4 + j + 1];
-    *reinterpret_cast<uint32_t*>(&sm.Xb[i * kS64 + j]) = pack2(x0, x1);
-    sm.XT[j * kS4 + i] = x0;
-    sm.XT[(j + 1) * kS4 + i] = x1;
-  }
+  wy_copy_x(sm.X, sm.Xb, sm.XT, tid);
   __syncthreads();
   const int r0 = 16 * (warp & 3);
   // ---- dX = (dE V^T + dW KB^T) diag(beta): rows [r0, +16) x columns [c0, +16), stored transposed
