@@ -1,9 +1,11 @@
-// Gated DeltaNet forward over packed documents (gdn_varlen.h).
+// Gated DeltaNet and Kimi Delta attention over packed documents
+// (gdn_varlen.h, kda_varlen.h): forward and backward.
 //
 // The recurrence (per head, state H of d_k x d_v = 128 x 128, reset at every
 // segment start):
 //     e_t = beta_t (v_t - alpha_t H_{t-1}^T k_t),  H_t = alpha_t H_{t-1} + k_t e_t^T,
-//     o_t = scale H_t^T q_t,  alpha_t = exp(g_t).
+//     o_t = scale H_t^T q_t,  alpha_t = exp(g_t)
+// (Kimi Delta: alpha_t a decay per key channel, applied as Diag(alpha_t)).
 // Chunked form, chunks of 64 tokens aligned to each segment's start, gamma_i
 // the running sum of g over the chunk and Gamma_ij = exp(gamma_i - gamma_j):
 //     A    = strictly-lower( diag(beta) (K K^T) o Gamma ),   Tm = (I + A)^-1
@@ -14,17 +16,22 @@
 // (unrolling the recurrence over the chunk: e_t depends on the earlier e_j
 // of the chunk through A, which the triangular inverse resolves at once).
 //
-// Three kernels:
+// Forward kernels:
 //   gdn_plan_kernel    one CTA: the chunk table (start, length of every
 //                      chunk) and the non-empty segments ordered longest first
 //   gdn_prep_kernel    one CTA per (chunk, head), all in parallel: A, Tm,
-//                      W, U and the masked Q K^T o Gamma, written to the
+//   (kda_prep_kernel)  W, U and the masked Q K^T o Gamma, written to the
 //                      workspace (bf16), and gamma (fp32)
 //   gdn_state_kernel   one CTA per (segment, head, 32 value columns):
 //                      eight warps carry H (fp32, in registers) across the
 //                      segment's chunks and write O; a producer warp loads
 //                      the tiles of chunks c+1 and c+2 by TMA while chunk c
 //                      computes
+// Backward: the same plan, prep and state pass (the state pass storing the
+// chunk-start states and E; the saving forward stores them and O at once),
+// then gdn_bwd_state_kernel carries the state's gradient back across each
+// segment, and per-chunk local passes form the gradients (gdn_bwd_local_h /
+// _wy, kda_bwd_local_h / _wy / _exp).
 // The products are small (64-row) and run in bf16 on the warp-level tensor
 // core instruction (mma.sync m16n8k16, fp32 accumulation): the state pass is
 // a dependent chain of 64-row steps whose state lives in registers, where the
