@@ -452,23 +452,36 @@ __device__ __forceinline__ void wy_inverse(const float* A, float* X, float* R, i
 }
 
 // ============================================================== prep
-// Shared memory of the prep CTA.
+// Shared memory of the prep CTA.  Arrays whose lifetimes do not overlap
+// share space, so that three CTAs fit on an SM: X takes Q's place (Q is last
+// read by Q K^T, X first written by the inverse, a barrier between them; the
+// two have the same size), T1 and T2 take the place of A and R (both last
+// read by the inverse, which ends on a barrier).
 struct PrepSmem {
   __nv_bfloat16 K[kC * kS128];
-  __nv_bfloat16 Q[kC * kS128];
+  union {
+    __nv_bfloat16 Q[kC * kS128];
+    float X[kC * kS4];  // (I + A)^-1, fp32 (rows of 16-byte multiples for the inverse's wide reads)
+  };
   __nv_bfloat16 V[kC * kS128];
-  float A[kC * kSF];    // A, fp32
-  float X[kC * kS4];    // (I + A)^-1, fp32 (rows of 16-byte multiples for the inverse's wide reads)
-  alignas(16) float R[3 * 256];  // off-diagonal block products
-  __nv_bfloat16 T1[kC * kS64];  // X diag(beta e^gamma)
-  __nv_bfloat16 T2[kC * kS64];  // X diag(beta)
+  union {
+    struct {
+      float A[kC * kSF];              // A, fp32
+      alignas(16) float R[3 * 256];  // off-diagonal block products
+    } ar;
+    struct {
+      __nv_bfloat16 T1[kC * kS64];  // X diag(beta e^gamma)
+      __nv_bfloat16 T2[kC * kS64];  // X diag(beta)
+    } t;
+  };
   float gam[kC];
   float bet[kC];
 };
 
-static_assert(sizeof(PrepSmem) <= 113 * 1024, "two prep CTAs per SM");
+static_assert(sizeof(PrepSmem::Q) == sizeof(PrepSmem::X), "X fills Q's place exactly");
+static_assert(sizeof(PrepSmem) <= 75 * 1024, "three prep CTAs per SM");
 
-__global__ void __launch_bounds__(kGdnThreads, 2) gdn_prep_kernel(GdnParams p) {
+__global__ void __launch_bounds__(kGdnThreads, 3) gdn_prep_kernel(GdnParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
   grid_dependency_wait();
@@ -541,21 +554,21 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_prep_kernel(GdnParams p) {
       const float gi = sm.gam[i], bi = sm.bet[i];
       const float G0 = j <= i ? __expf(gi - sm.gam[j]) : 0.f;
       const float G1 = j + 1 <= i ? __expf(gi - sm.gam[j + 1]) : 0.f;
-      sm.A[i * kSF + j] = j < i ? bi * G0 * skk[n][2 * hr] : 0.f;
-      sm.A[i * kSF + j + 1] = j + 1 < i ? bi * G1 * skk[n][2 * hr + 1] : 0.f;
+      sm.ar.A[i * kSF + j] = j < i ? bi * G0 * skk[n][2 * hr] : 0.f;
+      sm.ar.A[i * kSF + j + 1] = j + 1 < i ? bi * G1 * skk[n][2 * hr + 1] : 0.f;
       *reinterpret_cast<uint32_t*>(aqk + i * kC + j) = pack2(G0 * sqk[n][2 * hr], G1 * sqk[n][2 * hr + 1]);
     }
   }
   __syncthreads();
-  wy_inverse<kS4, kGdnThreads>(sm.A, sm.X, sm.R, tid);
+  wy_inverse<kS4, kGdnThreads>(sm.ar.A, sm.X, sm.ar.R, tid);
   // ---- T1 = X diag(beta e^gamma), T2 = X diag(beta) (bf16)
   for (int e = tid; e < kC * kC / 2; e += kGdnThreads) {
     const int i = e >> 5, j = (e & 31) * 2;
     const float x0 = sm.X[i * kS4 + j], x1 = sm.X[i * kS4 + j + 1];
     const float b0 = sm.bet[j], b1 = sm.bet[j + 1];
-    *reinterpret_cast<uint32_t*>(&sm.T1[i * kS64 + j]) =
+    *reinterpret_cast<uint32_t*>(&sm.t.T1[i * kS64 + j]) =
         pack2(x0 * b0 * __expf(sm.gam[j]), x1 * b1 * __expf(sm.gam[j + 1]));
-    *reinterpret_cast<uint32_t*>(&sm.T2[i * kS64 + j]) = pack2(x0 * b0, x1 * b1);
+    *reinterpret_cast<uint32_t*>(&sm.t.T2[i * kS64 + j]) = pack2(x0 * b0, x1 * b1);
   }
   __syncthreads();
   // ---- W = T1 K, U = T2 V: warp w rows [16 (w % 4), +16) x columns [64 (w / 4), +64).
@@ -565,7 +578,7 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_prep_kernel(GdnParams p) {
   for (int n = 0; n < 8; ++n)
 #pragma unroll
     for (int e = 0; e < 4; ++e) cw[n][e] = cu[n][e] = 0.f;
-  const uint32_t sT1 = smem_u32(sm.T1), sT2 = smem_u32(sm.T2);
+  const uint32_t sT1 = smem_u32(sm.t.T1), sT2 = smem_u32(sm.t.T2);
 #pragma unroll
   for (int kk = 0; kk < kC / 16; ++kk) {
     uint32_t a1[4], a2[4];
